@@ -1,0 +1,198 @@
+"""ctypes wrapper around the fp64 CPU oracle (oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it to check and time the CUDA path.
+The library package never imports it, and it shares no code with it.
+
+The oracle follows the simplified ``selective_scan`` loop of "Mamba:
+Selective State Space Models" (youngju.dev, section 3.3) in double
+precision; see the header of oracle.c for the exact statement.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
+           "-pthread", "-D_POSIX_C_SOURCE=200809L"]
+
+
+def _compile(src: str, out: str) -> None:
+    subprocess.run(["gcc", *_CFLAGS, "-o", out + ".tmp", src, "-lm"], check=True)
+    os.replace(out + ".tmp", out)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (plain gcc, no fast-math,
+    no FMA contraction, so every operation rounds as written)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SRC):
+        _compile(SRC, _LIB)
+    return _LIB
+
+
+def _f32(a, shape, name):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    if tuple(a.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _f64(a, shape, name):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if tuple(a.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+class Oracle:
+    """One loaded copy of the oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        INT = ctypes.c_int
+        lib.oracle_softplus.restype = ctypes.c_double
+        lib.oracle_softplus.argtypes = [ctypes.c_double]
+        lib.oracle_selscan_fwd.restype = INT
+        lib.oracle_selscan_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT]
+        lib.oracle_selscan_fwd_chains.restype = INT
+        lib.oracle_selscan_fwd_chains.argtypes = [P, P, P, P, P, P, P, I64, P, P,
+                                                  I64, I64, I64, I64, INT, INT]
+        lib.oracle_selscan_step.restype = INT
+        lib.oracle_selscan_step.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64]
+        self._lib = lib
+        self.path = path
+
+    def softplus(self, u: float) -> float:
+        """log(1 + e^u) in double."""
+        return self._lib.oracle_softplus(float(u))
+
+    def selscan_fwd(self, x, delta, A, B, C, delta_softplus=False, h0=None, nthreads=0):
+        """Sequential selective scan in fp64.
+
+        x, delta: (Bsz, L, D); A: (D, N); B, C: (Bsz, L, N); h0: (Bsz, D, N)
+        or None. Inputs are taken as float32 (the exact values the GPU reads);
+        h0 as float64 (fp32 states widen exactly).
+        Returns (y (Bsz, L, D) float64, hT (Bsz, D, N) float64).
+        """
+        x = np.asarray(x)
+        Bsz, L, D = x.shape
+        N = np.asarray(A).shape[1]
+        x = _f32(x, (Bsz, L, D), "x")
+        delta = _f32(delta, (Bsz, L, D), "delta")
+        A = _f32(A, (D, N), "A")
+        B = _f32(B, (Bsz, L, N), "B")
+        C = _f32(C, (Bsz, L, N), "C")
+        h0 = None if h0 is None else _f64(h0, (Bsz, D, N), "h0")
+        y = np.zeros((Bsz, L, D), np.float64)
+        hT = np.zeros((Bsz, D, N), np.float64)
+        rc = self._lib.oracle_selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),
+                                          _ptr(y), _ptr(hT), Bsz, L, D, N,
+                                          int(bool(delta_softplus)), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_selscan_fwd failed")
+        return y, hT
+
+    def selscan_fwd_chains(self, x, delta, A, B, C, chains, delta_softplus=False, h0=None,
+                           nthreads=0):
+        """The same scan for selected chains c = b * D + d only.
+        Returns (y (nchains, L), hT (nchains, N)) in float64."""
+        x = np.asarray(x)
+        Bsz, L, D = x.shape
+        N = np.asarray(A).shape[1]
+        x = _f32(x, (Bsz, L, D), "x")
+        delta = _f32(delta, (Bsz, L, D), "delta")
+        A = _f32(A, (D, N), "A")
+        B = _f32(B, (Bsz, L, N), "B")
+        C = _f32(C, (Bsz, L, N), "C")
+        h0 = None if h0 is None else _f64(h0, (Bsz, D, N), "h0")
+        chains = np.ascontiguousarray(chains, dtype=np.int64)
+        nc = chains.shape[0]
+        y = np.zeros((nc, L), np.float64)
+        hT = np.zeros((nc, N), np.float64)
+        rc = self._lib.oracle_selscan_fwd_chains(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                                 _ptr(h0), _ptr(chains), nc, _ptr(y), _ptr(hT),
+                                                 Bsz, L, D, N, int(bool(delta_softplus)),
+                                                 int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_selscan_fwd_chains failed")
+        return y, hT
+
+    def selscan_step(self, state, x, delta, A, B, C, chains=None):
+        """One decode step in place on a float64 state.
+
+        state: (Bsz, D, N) float64, or (nchains, N) when ``chains`` is given;
+        x, delta: (Bsz, D); A: (D, N); B, C: (Bsz, N). delta is used as given.
+        Returns y: (Bsz, D) float64, or (nchains,) when ``chains`` is given.
+        """
+        if not (isinstance(state, np.ndarray) and state.dtype == np.float64
+                and state.flags.c_contiguous):
+            raise ValueError("state must be a C-contiguous float64 array (updated in place)")
+        x = np.asarray(x)
+        Bsz, D = x.shape
+        N = np.asarray(A).shape[1]
+        x = _f32(x, (Bsz, D), "x")
+        delta = _f32(delta, (Bsz, D), "delta")
+        A = _f32(A, (D, N), "A")
+        B = _f32(B, (Bsz, N), "B")
+        C = _f32(C, (Bsz, N), "C")
+        if chains is None:
+            if state.shape != (Bsz, D, N):
+                raise ValueError("state shape")
+            y = np.zeros((Bsz, D), np.float64)
+            ch, nc = None, 0
+        else:
+            ch = np.ascontiguousarray(chains, dtype=np.int64)
+            nc = ch.shape[0]
+            if state.shape != (nc, N):
+                raise ValueError("state shape")
+            y = np.zeros((nc,), np.float64)
+        rc = self._lib.oracle_selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
+                                           _ptr(C), _ptr(y), _ptr(ch), nc, Bsz, D, N)
+        if rc != 0:
+            raise RuntimeError("oracle_selscan_step failed")
+        return y
+
+
+def compile_variant(src: str, out: str) -> Oracle:
+    """Build and load a copy of the oracle from another C source file
+    (the mutation tests plant mistakes this way, on the CPU)."""
+    _compile(src, out)
+    return Oracle(out)
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def softplus(u):
+    return default().softplus(u)
+
+
+def selscan_fwd(*args, **kwargs):
+    return default().selscan_fwd(*args, **kwargs)
+
+
+def selscan_fwd_chains(*args, **kwargs):
+    return default().selscan_fwd_chains(*args, **kwargs)
+
+
+def selscan_step(*args, **kwargs):
+    return default().selscan_step(*args, **kwargs)

@@ -1,0 +1,260 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle for Mamba's selective scan.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file exists so that the tests, the smoke
+ * check and the CPU-baseline leg of the benchmark can compare the CUDA path
+ * against an obviously correct restatement of the method. Nothing on the
+ * product path may link, load or call it, and it shares no code, header,
+ * table or helper with the CUDA library.
+ *
+ * What it computes (source: "Mamba: Selective State Space Models",
+ * youngju.dev, section 3.3 "Hardware-Aware algorithm", the simplified
+ * selective_scan listing; the discrete recurrence of section 2.2; shapes as
+ * in booiljung.github.io "3.1 LTI ... Input-Dependent parameters",
+ * section 0.4.2):
+ *
+ *   x, delta : (Bsz, L, D)      A : (D, N)      B, C : (Bsz, L, N)
+ *   for every batch b and channel d, with h[0..N) = h0[b,d,:] (zeros if absent):
+ *     for t = 0 .. L-1:
+ *       dl = delta[b,t,d]              (softplus(dl) = log(1 + e^dl) when asked)
+ *       for n: h[n] = exp(dl * A[d,n]) * h[n] + (dl * B[b,t,n]) * x[b,t,d]
+ *       y[b,t,d] = sum_n h[n] * C[b,t,n]          (read-out after the update)
+ *     hT[b,d,:] = h
+ *
+ * deltaB is the simplified dl * B of the listing, not the zero-order-hold
+ * form (dA)^-1 (exp(dA) - I) dB of section 2.2.
+ *
+ * The decode step (the O(1)-state recurrent mode of section 6 on the same
+ * page) is one iteration of the t-loop with L = 1, applied in place to a
+ * caller-held state, with delta taken as given (no softplus).
+ *
+ * Inputs are float (exactly the values the GPU sees: fp32 values or
+ * bf16 values widened to fp32) except the optional initial state h0, which
+ * is double so that a state handed over from an earlier call loses nothing;
+ * every operation is done in double.
+ * Chains (b, d) are independent, so a pool of POSIX threads splits them;
+ * each chain runs the loop above unchanged, so the thread count does not
+ * change any result bit.
+ *
+ * Pins (tests/test_oracle_pins.py): brute-force unrolled sum, A = 0 running
+ * sum, N = 1 scalar recurrence, L = 1 closed form, LTI convolution kernel,
+ * geometric closed form, delta -> 0 persistence, delta -> inf reset,
+ * chunked associative composition, step == forward, linearity.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* softplus(u) = log(1 + e^u)   (booiljung.github.io, section 0.4.2).
+ * Written as max(u, 0) + log1p(e^-|u|), which is the same function without
+ * overflow for large |u|. */
+double oracle_softplus(double u)
+{
+    double a = fabs(u);
+    return (u > 0.0 ? u : 0.0) + log1p(exp(-a));
+}
+
+/* One (b, d) chain of the forward scan.
+ * y_out[t * y_stride] receives y[b,t,d]; h_out[n] receives the final state. */
+static void scan_chain(const float *x, const float *delta, const float *A,
+                       const float *B, const float *C, const double *h0,
+                       int64_t b, int64_t d, int64_t L, int64_t D, int64_t N,
+                       int delta_softplus, double *y_out, int64_t y_stride,
+                       double *h_out, double *h)
+{
+    for (int64_t n = 0; n < N; ++n)
+        h[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        int64_t bt = b * L + t;
+        double dl = (double)delta[bt * D + d];
+        if (delta_softplus)
+            dl = oracle_softplus(dl);
+        double xv = (double)x[bt * D + d];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
+            double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            h[n] = dA * h[n] + dB * xv;
+        }
+        for (int64_t n = 0; n < N; ++n)
+            acc += h[n] * (double)C[bt * N + n];
+        if (y_out)
+            y_out[t * y_stride] = acc;
+    }
+    if (h_out)
+        for (int64_t n = 0; n < N; ++n)
+            h_out[n] = h[n];
+}
+
+/* ---- a small thread pool over chain indices -------------------------- */
+
+typedef struct {
+    const float *x, *delta, *A, *B, *C;
+    const double *h0;
+    int64_t Bsz, L, D, N;
+    int delta_softplus;
+    const int64_t *chains; /* NULL: all chains, index c = b * D + d */
+    int64_t nchains;
+    double *y, *hT;        /* full layout when chains == NULL, else packed */
+    int64_t next;          /* next chain to take (under lock) */
+    pthread_mutex_t lock;
+    int failed;
+} fwd_job;
+
+static void *fwd_worker(void *arg)
+{
+    fwd_job *j = (fwd_job *)arg;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+    if (!h) {
+        pthread_mutex_lock(&j->lock);
+        j->failed = 1;
+        pthread_mutex_unlock(&j->lock);
+        return NULL;
+    }
+    for (;;) {
+        int64_t i;
+        pthread_mutex_lock(&j->lock);
+        i = j->next++;
+        pthread_mutex_unlock(&j->lock);
+        if (i >= j->nchains)
+            break;
+        int64_t c = j->chains ? j->chains[i] : i;
+        int64_t b = c / j->D, d = c % j->D;
+        double *y_out, *h_out;
+        int64_t y_stride;
+        if (j->chains) { /* packed: y (nchains, L), hT (nchains, N) */
+            y_out = j->y ? j->y + i * j->L : NULL;
+            y_stride = 1;
+            h_out = j->hT ? j->hT + i * j->N : NULL;
+        } else {         /* full: y (Bsz, L, D), hT (Bsz, D, N) */
+            y_out = j->y ? j->y + b * j->L * j->D + d : NULL;
+            y_stride = j->D;
+            h_out = j->hT ? j->hT + c * j->N : NULL;
+        }
+        scan_chain(j->x, j->delta, j->A, j->B, j->C, j->h0, b, d, j->L, j->D,
+                   j->N, j->delta_softplus, y_out, y_stride, h_out, h);
+    }
+    free(h);
+    return NULL;
+}
+
+static int pick_threads(int nthreads, int64_t work)
+{
+    if (nthreads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = n > 0 ? (int)n : 1;
+    }
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((int64_t)nthreads > work)
+        nthreads = work > 0 ? (int)work : 1;
+    return nthreads;
+}
+
+static int run_fwd(fwd_job *j, int nthreads)
+{
+    pthread_t tid[256];
+    int started = 0;
+    nthreads = pick_threads(nthreads, j->nchains);
+    pthread_mutex_init(&j->lock, NULL);
+    j->next = 0;
+    j->failed = 0;
+    for (int i = 1; i < nthreads; ++i)
+        if (pthread_create(&tid[started], NULL, fwd_worker, j) == 0)
+            ++started;
+    fwd_worker(j); /* the calling thread works too */
+    for (int i = 0; i < started; ++i)
+        pthread_join(tid[i], NULL);
+    pthread_mutex_destroy(&j->lock);
+    return j->failed ? -1 : 0;
+}
+
+/* Full forward scan over every chain.
+ * y: (Bsz, L, D) double, may be NULL; hT: (Bsz, D, N) double, may be NULL;
+ * h0: (Bsz, D, N) double or NULL for zeros. nthreads <= 0 uses every online
+ * CPU. Returns 0, or -1 on bad arguments / allocation failure. */
+int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
+                       const float *B, const float *C, const double *h0,
+                       double *y, double *hT, int64_t Bsz, int64_t L,
+                       int64_t D, int64_t N, int delta_softplus, int nthreads)
+{
+    if (Bsz < 0 || L < 0 || D < 0 || N < 0)
+        return -1;
+    if (L > 0 && (!x || !delta || !B || !C))
+        return -1;
+    if (N > 0 && !A)
+        return -1;
+    fwd_job j;
+    memset(&j, 0, sizeof j);
+    j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
+    j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
+    j.delta_softplus = delta_softplus;
+    j.chains = NULL;
+    j.nchains = Bsz * D;
+    j.y = y; j.hT = hT;
+    return run_fwd(&j, nthreads);
+}
+
+/* Forward scan for a chosen set of chains only (chain c = b * D + d), for
+ * sampled checks of sizes the full oracle would take too long on.
+ * y_out: (nchains, L), hT_out: (nchains, N); either may be NULL. */
+int oracle_selscan_fwd_chains(const float *x, const float *delta,
+                              const float *A, const float *B, const float *C,
+                              const double *h0, const int64_t *chains,
+                              int64_t nchains, double *y_out, double *hT_out,
+                              int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                              int delta_softplus, int nthreads)
+{
+    if (Bsz < 0 || L < 0 || D < 0 || N < 0 || nchains < 0 || (nchains && !chains))
+        return -1;
+    for (int64_t i = 0; i < nchains; ++i)
+        if (chains[i] < 0 || chains[i] >= Bsz * D)
+            return -1;
+    fwd_job j;
+    memset(&j, 0, sizeof j);
+    j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
+    j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
+    j.delta_softplus = delta_softplus;
+    j.chains = chains;
+    j.nchains = nchains;
+    j.y = y_out; j.hT = hT_out;
+    return run_fwd(&j, nthreads);
+}
+
+/* Decode step: one iteration of the loop above, state updated in place.
+ *   state : (Bsz, D, N) double, in/out        x, delta : (Bsz, D) float
+ *   A : (D, N)        B, C : (Bsz, N)          y : (Bsz, D) double
+ * delta is used as given. When chains != NULL only those chains are
+ * updated, with state packed as (nchains, N) and y as (nchains). */
+int oracle_selscan_step(double *state, const float *x, const float *delta,
+                        const float *A, const float *B, const float *C,
+                        double *y, const int64_t *chains, int64_t nchains,
+                        int64_t Bsz, int64_t D, int64_t N)
+{
+    if (!state || !x || !delta || !A || !B || !C || Bsz < 0 || D < 0 || N < 0)
+        return -1;
+    int64_t count = chains ? nchains : Bsz * D;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t c = chains ? chains[i] : i;
+        if (c < 0 || c >= Bsz * D)
+            return -1;
+        int64_t b = c / D, d = c % D;
+        double *h = state + (chains ? i : c) * N;
+        double dl = (double)delta[b * D + d];
+        double xv = (double)x[b * D + d];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double dA = exp(dl * (double)A[d * N + n]);
+            double dB = dl * (double)B[b * N + n];
+            h[n] = dA * h[n] + dB * xv;
+        }
+        for (int64_t n = 0; n < N; ++n)
+            acc += h[n] * (double)C[b * N + n];
+        if (y)
+            y[i] = acc;
+    }
+    return 0;
+}

@@ -1,0 +1,100 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case below plants one mistake in a copy of oracle.c (compiled on the CPU
+into a temporary directory) and runs every pin of test_oracle_pins.py against
+that copy; at least one pin has to fail. The real oracle is never modified.
+"""
+import inspect
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTATIONS = {
+    "readout_before_update": (
+        """        for (int64_t n = 0; n < N; ++n) {
+            double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
+            double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            h[n] = dA * h[n] + dB * xv;
+        }
+        for (int64_t n = 0; n < N; ++n)
+            acc += h[n] * (double)C[bt * N + n];
+""",
+        """        for (int64_t n = 0; n < N; ++n)
+            acc += h[n] * (double)C[bt * N + n];
+        for (int64_t n = 0; n < N; ++n) {
+            double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
+            double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            h[n] = dA * h[n] + dB * xv;
+        }
+"""),
+    "exp_sign": ("double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */",
+                 "double dA = exp(-dl * (double)A[d * N + n]);   /* deltaA */"),
+    "A_transposed": ("double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */",
+                     "double dA = exp(dl * (double)A[n * D + d]);   /* deltaA */"),
+    "dropped_input_term": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for",
+                           "            h[n] = dA * h[n];\n        }\n        for"),
+    "deltaB_without_delta": ("double dB = dl * (double)B[bt * N + n];        /* deltaB */",
+                             "double dB = (double)B[bt * N + n];        /* deltaB */"),
+    "B_ignores_time": ("double dB = dl * (double)B[bt * N + n];        /* deltaB */",
+                       "double dB = dl * (double)B[b * L * N + n];        /* deltaB */"),
+    "C_previous_step": ("            acc += h[n] * (double)C[bt * N + n];\n        if (y_out)",
+                        "            acc += h[n] * (double)C[(t > 0 ? bt - 1 : bt) * N + n];\n        if (y_out)"),
+    "x_wrong_channel": ("double xv = (double)x[bt * D + d];",
+                        "double xv = (double)x[bt * D + (D - 1 - d)];"),
+    "h0_ignored": ("h[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;", "h[n] = 0.0;"),
+    "hT_not_written": ("            h_out[n] = h[n];", "            h_out[n] = 0.0;"),
+    "softplus_missing_max_term": ("return (u > 0.0 ? u : 0.0) + log1p(exp(-a));",
+                                  "return log1p(exp(-a));"),
+    "softplus_flag_ignored": ("        if (delta_softplus)\n            dl = oracle_softplus(dl);\n", ""),
+    "step_wrong_decay": ("            double dA = exp(dl * (double)A[d * N + n]);\n            double dB = dl * (double)B[b * N + n];",
+                         "            double dA = exp(dl * (double)A[n]);\n            double dB = dl * (double)B[b * N + n];"),
+    "step_dropped_input": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];",
+                           "            h[n] = dA * h[n];\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];"),
+}
+
+
+def _pin_calls():
+    """(name, callable(orc)) for every pin, expanding parametrized ones."""
+    out = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+        if not marks:
+            out.append((name, lambda o, fn=fn: fn(o)))
+            continue
+        (argnames, values), = [m.args for m in marks]
+        argnames = [a.strip() for a in argnames.split(",")] if isinstance(argnames, str) else list(argnames)
+        for v in values:
+            v = v if isinstance(v, tuple) and len(argnames) > 1 else (v,)
+            kw = dict(zip(argnames, v))
+            out.append((f"{name}{v}", lambda o, fn=fn, kw=kw: fn(o, **kw)))
+    return out
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    src = open(oracle.SRC).read()
+    p = tmp_path / "same.c"
+    p.write_text(src)
+    o = oracle.compile_variant(str(p), str(tmp_path / "same.so"))
+    for name, call in _pin_calls():
+        call(o)
+
+
+@pytest.mark.parametrize("mutation", sorted(MUTATIONS))
+def test_mutation_is_caught(tmp_path, mutation):
+    old, new = MUTATIONS[mutation]
+    src = open(oracle.SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {mutation} not found"
+    p = tmp_path / f"{mutation}.c"
+    p.write_text(src.replace(old, new, 1))
+    o = oracle.compile_variant(str(p), str(tmp_path / f"{mutation}.so"))
+    failed = []
+    for name, call in _pin_calls():
+        try:
+            call(o)
+        except (AssertionError, RuntimeError):
+            failed.append(name)
+    assert failed, f"no pin caught the planted mistake '{mutation}'"

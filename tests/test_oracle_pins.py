@@ -1,0 +1,366 @@
+"""Pins on the fp64 oracle: each checks it against something other than itself.
+
+The oracle restates the selective_scan loop of "Mamba: Selective State Space
+Models" (youngju.dev, section 3.3). The pins below fix its result through
+independent routes (brute-force unrolling, closed forms, special cases that
+reduce to textbook formulas, invariants), so that a dropped term, a wrong sign
+or index, or a transposed operand fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from selective_state_space_157_b300 import workloads as W
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def rand_inputs(Bsz, L, D, N, seed, softplus=True, h0=False, a_scale=1.0):
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((Bsz, L, D)).astype(np.float32)
+    u = (g.standard_normal((Bsz, L, D)) - 1.0).astype(np.float32)
+    if not softplus:
+        u = np.abs(u) * np.float32(0.3)
+    # distinct, asymmetric A entries so a transposed A[n, d] would differ
+    A = (-a_scale * (0.2 + g.random((D, N)))).astype(np.float32)
+    B = g.standard_normal((Bsz, L, N)).astype(np.float32)
+    C = g.standard_normal((Bsz, L, N)).astype(np.float32)
+    hh = g.standard_normal((Bsz, D, N)) if h0 else None
+    return x, u, A, B, C, hh
+
+
+def sp(u):
+    u = np.asarray(u, np.float64)
+    return np.maximum(u, 0) + np.log1p(np.exp(-np.abs(u)))
+
+
+def brute_force(x, delta, A, B, C, h0):
+    """Unrolled form: y_t = sum_{s<=t} sum_n C_t[n] prod_{s<r<=t} exp(d_r A[n]) d_s B_s[n] x_s
+    + sum_n C_t[n] prod_{r<=t} exp(d_r A[n]) h0[n]. Products taken literally."""
+    x = x.astype(np.float64); delta = delta.astype(np.float64)
+    A = A.astype(np.float64); B = B.astype(np.float64); C = C.astype(np.float64)
+    Bsz, L, D = x.shape
+    N = A.shape[1]
+    y = np.zeros((Bsz, L, D))
+    hT = np.zeros((Bsz, D, N))
+    for b in range(Bsz):
+        for d in range(D):
+            E = np.exp(delta[b, :, d, None] * A[d][None, :])     # (L, N) per-step decay
+            for t in range(L):
+                tot = 0.0
+                for s in range(t + 1):
+                    decay = np.prod(E[s + 1:t + 1], axis=0)       # empty product = 1
+                    tot += np.sum(C[b, t] * decay * delta[b, s, d] * B[b, s] * x[b, s, d])
+                if h0 is not None:
+                    tot += np.sum(C[b, t] * np.prod(E[:t + 1], axis=0) * h0[b, d])
+                y[b, t, d] = tot
+            st = np.zeros(N)
+            for s in range(L):
+                st += np.prod(E[s + 1:], axis=0) * delta[b, s, d] * B[b, s] * x[b, s, d]
+            if h0 is not None:
+                st += np.prod(E, axis=0) * h0[b, d]
+            hT[b, d] = st
+    return y, hT
+
+
+def close(a, b, rtol, atol=0.0):
+    np.testing.assert_allclose(a, b, rtol=rtol, atol=atol)
+
+
+# ---------------------------------------------------------------- softplus
+
+def test_softplus_values(orc):
+    assert orc.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    for u in (-30.0, -5.0, -0.7, 0.3, 2.0, 19.0, 45.0):
+        assert orc.softplus(u) - orc.softplus(-u) == pytest.approx(u, rel=1e-13, abs=1e-15)
+        assert orc.softplus(u) == pytest.approx(math.log1p(math.exp(u)), rel=1e-14)
+    assert orc.softplus(800.0) == 800.0                      # no overflow
+    assert orc.softplus(-60.0) == pytest.approx(math.exp(-60.0), rel=1e-14)
+
+
+# ---------------------------------------------------------------- golden
+
+def test_hand_worked_cases(orc):
+    g = json.load(open(os.path.join(HERE, "golden", "hand_worked.json")))
+    for c in g["cases"]:
+        arr = lambda k: np.array(c[k], np.float64)
+        h0 = arr("h0") if "h0" in c else None
+        y, hT = orc.selscan_fwd(arr("x"), arr("delta"), arr("A"), arr("B"), arr("C"),
+                                delta_softplus=c["delta_softplus"], h0=h0)
+        close(y, arr("y"), c["rtol"], c.get("atol", 0.0))
+        close(hT, arr("hT"), c["rtol"], c.get("atol", 0.0))
+
+
+# ---------------------------------------------------------------- P1 brute force
+
+@pytest.mark.parametrize("Bsz,L,D,N,softplus,h0", [
+    (1, 1, 1, 1, True, False),
+    (2, 9, 3, 4, True, True),
+    (1, 17, 2, 5, False, True),
+    (2, 24, 3, 7, True, False),
+])
+def test_brute_force(orc, Bsz, L, D, N, softplus, h0):
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=L * 7 + N, softplus=softplus, h0=h0)
+    dl = sp(u) if softplus else u.astype(np.float64)
+    yb, hb = brute_force(x, dl, A, B, C, hh)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=softplus, h0=hh)
+    scale = 1.0 + np.abs(yb)
+    assert np.max(np.abs(y - yb) / scale) < 1e-12
+    assert np.max(np.abs(hT - hb) / (1.0 + np.abs(hb))) < 1e-12
+
+
+# ---------------------------------------------------------------- P2 A = 0
+
+def test_A_zero_running_sum(orc):
+    Bsz, L, D, N = 2, 40, 3, 6
+    x, u, _, B, C, hh = rand_inputs(Bsz, L, D, N, seed=2, h0=True)
+    A = np.zeros((D, N), np.float32)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=True, h0=hh)
+    dl = sp(u)
+    # h_t = h0 + sum_{s<=t} delta_s B_s x_s
+    contrib = dl[..., None] * B.astype(np.float64)[:, :, None, :] * x.astype(np.float64)[..., None]  # (Bsz,L,D,N)
+    h = hh[:, None, :, :] + np.cumsum(contrib, axis=1)
+    yr = np.einsum("bldn,bln->bld", h, C.astype(np.float64))
+    close(y, yr, 1e-12, 1e-12)
+    close(hT, h[:, -1], 1e-12, 1e-12)
+
+
+# ---------------------------------------------------------------- P3 N = 1
+
+def test_N1_scalar_recurrence(orc):
+    """One state is the scalar recurrence h = a*h + b*x with a = exp(delta*A), b = delta*B."""
+    Bsz, L, D = 2, 50, 4
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, 1, seed=3, h0=True)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=True, h0=hh)
+    for b in range(Bsz):
+        for d in range(D):
+            h = float(hh[b, d, 0])
+            for t in range(L):
+                dl = math.log1p(math.exp(float(u[b, t, d])))
+                a = math.exp(dl * float(A[d, 0]))
+                bb = dl * float(B[b, t, 0])
+                h = a * h + bb * float(x[b, t, d])
+                assert y[b, t, d] == pytest.approx(h * float(C[b, t, 0]), rel=1e-13, abs=1e-15)
+            assert hT[b, d, 0] == pytest.approx(h, rel=1e-13, abs=1e-15)
+
+
+# ---------------------------------------------------------------- P4 L = 1
+
+def test_L1_closed_form(orc):
+    Bsz, D, N = 3, 5, 8
+    x, u, A, B, C, _ = rand_inputs(Bsz, 1, D, N, seed=4)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=True)
+    dl = sp(u)[:, 0, :]                                       # (Bsz, D)
+    h = dl[..., None] * B[:, 0, None, :].astype(np.float64) * x[:, 0, :, None].astype(np.float64)
+    close(hT, h, 1e-14)
+    close(y[:, 0, :], np.einsum("bdn,bn->bd", h, C[:, 0].astype(np.float64)), 1e-13, 1e-15)
+
+
+# ---------------------------------------------------------------- P5 LTI convolution
+
+def test_lti_convolution_kernel(orc):
+    """Delta, B, C constant over t: y = x * K with K_k = sum_n C[n] abar[n]^k delta B[n]
+    (booiljung.github.io section 0.2.2, the convolution kernel of an LTI SSM)."""
+    L, D, N = 64, 3, 5
+    g = np.random.default_rng(5)
+    x = g.standard_normal((1, L, D)).astype(np.float32)
+    dl_d = (0.05 + g.random(D)).astype(np.float32)
+    delta = np.broadcast_to(dl_d, (1, L, D)).copy()
+    A = (-0.1 - g.random((D, N))).astype(np.float32)
+    Bv = g.standard_normal(N).astype(np.float32)
+    Cv = g.standard_normal(N).astype(np.float32)
+    B = np.broadcast_to(Bv, (1, L, N)).copy()
+    C = np.broadcast_to(Cv, (1, L, N)).copy()
+    y, _ = orc.selscan_fwd(x, delta, A, B, C, delta_softplus=False)
+    k = np.arange(L)
+    for d in range(D):
+        abar = np.exp(float(dl_d[d]) * A[d].astype(np.float64))          # (N,)
+        K = np.sum(Cv.astype(np.float64)[None, :] * abar[None, :] ** k[:, None]
+                   * float(dl_d[d]) * Bv.astype(np.float64)[None, :], axis=1)
+        yc = np.convolve(x[0, :, d].astype(np.float64), K)[:L]
+        close(y[0, :, d], yc, 1e-11, 1e-12)
+
+
+# ---------------------------------------------------------------- P6 geometric
+
+def test_geometric_closed_form(orc):
+    L = 300
+    xv, dv, Av, Bv = 0.7, 0.2, -0.3, 1.3
+    x = np.full((1, L, 1), xv, np.float32)
+    delta = np.full((1, L, 1), dv, np.float32)
+    A = np.full((1, 1), Av, np.float32)
+    B = np.full((1, L, 1), Bv, np.float32)
+    C = np.ones((1, L, 1), np.float32)
+    y, _ = orc.selscan_fwd(x, delta, A, B, C)
+    a = math.exp(float(np.float32(dv)) * float(np.float32(Av)))
+    b = float(np.float32(dv)) * float(np.float32(Bv)) * float(np.float32(xv))
+    t = np.arange(L)
+    close(y[0, :, 0], b * (1 - a ** (t + 1)) / (1 - a), 1e-12)
+
+
+# ---------------------------------------------------------------- P7 delta -> 0
+
+def test_delta_zero_persists_state(orc):
+    Bsz, L, D, N = 2, 30, 3, 4
+    x, _, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=7, h0=True)
+    delta = np.zeros((Bsz, L, D), np.float32)
+    y, hT = orc.selscan_fwd(x, delta, A, B, C, delta_softplus=False, h0=hh)
+    assert np.array_equal(hT, hh)                                      # bit-exact
+    yr = np.einsum("bdn,bln->bld", hh, C.astype(np.float64))
+    close(y, yr, 1e-14, 1e-15)
+    tiny = np.full((Bsz, L, D), 1e-12, np.float32)
+    _, hT2 = orc.selscan_fwd(x, tiny, A, B, C, delta_softplus=False, h0=hh)
+    assert np.max(np.abs(hT2 - hh)) < 1e-9
+
+
+# ---------------------------------------------------------------- P8 delta -> inf
+
+def test_large_delta_resets_state(orc):
+    """A < 0 and a huge step: exp(delta*A) underflows to 0, so h_t = delta_t B_t x_t."""
+    Bsz, L, D, N = 1, 12, 2, 3
+    x, _, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=8, h0=True)
+    delta = np.full((Bsz, L, D), 1e4, np.float32)
+    y, hT = orc.selscan_fwd(x, delta, A, B, C, delta_softplus=False, h0=hh)
+    h = 1e4 * B.astype(np.float64)[:, :, None, :] * x.astype(np.float64)[..., None]
+    close(hT, h[:, -1], 1e-15)
+    close(y, np.einsum("bldn,bln->bld", h, C.astype(np.float64)), 1e-14)
+
+
+# ---------------------------------------------------------------- P9 chunked == sequential
+
+@pytest.mark.parametrize("cuts", [(1,), (17,), (5, 40, 41), (10, 20, 30, 50, 63)])
+def test_split_resume(orc, cuts):
+    """Running [0, L1) then [L1, L) with the handed-over state equals one pass."""
+    Bsz, L, D, N = 2, 64, 3, 5
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=9, h0=True)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=True, h0=hh)
+    bounds = [0, *cuts, L]
+    h = hh
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        yi, h = orc.selscan_fwd(x[:, a:b], u[:, a:b], A, B[:, a:b], C[:, a:b], delta_softplus=True, h0=h)
+        close(yi, y[:, a:b], 1e-13, 1e-14)
+    close(h, hT, 1e-13, 1e-14)
+
+
+def test_associative_chunk_composition(orc):
+    """Parallel-scan form (booiljung.github.io section 3.1.5.2): each chunk reduced from a
+    zero state to (prod abar, h_end) and composed with (a1,b1) o (a2,b2) = (a2 a1, a2 b1 + b2)
+    gives the sequential state; the in-chunk outputs follow from a correction by the carry."""
+    Bsz, L, D, N = 1, 96, 2, 4
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=10, h0=True)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, delta_softplus=True, h0=hh)
+    dl = sp(u)
+    chunks = [(0, 30), (30, 31), (31, 80), (80, 96)]
+    aggs = []
+    for a, b in chunks:
+        ylocal, hend = orc.selscan_fwd(x[:, a:b], u[:, a:b], A, B[:, a:b], C[:, a:b], delta_softplus=True)
+        P = np.exp(A.astype(np.float64)[None] * dl[:, a:b].sum(axis=1)[..., None])  # (Bsz,D,N)
+        aggs.append((P, hend, ylocal))
+    carry = hh.copy()
+    for (a, b), (P, hend, ylocal) in zip(chunks, aggs):
+        # outputs: local outputs plus C_t . (prod_{s<=t} abar_s) carry
+        cum = np.exp(A.astype(np.float64)[None, None] * np.cumsum(dl[:, a:b], axis=1)[..., None])
+        corr = np.einsum("bldn,bdn,bln->bld", cum, carry, C[:, a:b].astype(np.float64))
+        close(ylocal + corr, y[:, a:b], 1e-12, 1e-13)
+        carry = P * carry + hend                                     # (a2 a1, a2 b1 + b2)
+    close(carry, hT, 1e-12, 1e-13)
+
+
+# ---------------------------------------------------------------- P10 step == fwd
+
+def test_step_closed_form(orc):
+    Bsz, D, N = 3, 4, 6
+    g = np.random.default_rng(11)
+    st = g.standard_normal((Bsz, D, N))
+    x = g.standard_normal((Bsz, D)).astype(np.float32)
+    dl = (0.05 + g.random((Bsz, D))).astype(np.float32)
+    A = (-0.2 - g.random((D, N))).astype(np.float32)
+    B = g.standard_normal((Bsz, N)).astype(np.float32)
+    C = g.standard_normal((Bsz, N)).astype(np.float32)
+    s = st.copy()
+    y = orc.selscan_step(s, x, dl, A, B, C)
+    ref = np.exp(dl.astype(np.float64)[..., None] * A.astype(np.float64)[None]) * st \
+        + dl.astype(np.float64)[..., None] * B.astype(np.float64)[:, None, :] * x.astype(np.float64)[..., None]
+    close(s, ref, 1e-14)
+    close(y, np.einsum("bdn,bn->bd", ref, C.astype(np.float64)), 1e-13, 1e-15)
+
+
+def test_steps_equal_forward(orc):
+    Bsz, L, D, N = 2, 25, 3, 4
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=12, h0=True)
+    dl = sp(u).astype(np.float32)
+    y, hT = orc.selscan_fwd(x, dl, A, B, C, delta_softplus=False, h0=hh)
+    s = hh.copy()
+    for t in range(L):
+        yt = orc.selscan_step(s, x[:, t], dl[:, t], A, B[:, t], C[:, t])
+        assert np.array_equal(yt, y[:, t])
+    assert np.array_equal(s, hT)
+    # chains subset of the step
+    s2 = hh.reshape(Bsz * D, N)[[1, 4]].copy()
+    for t in range(L):
+        yt = orc.selscan_step(s2, x[:, t], dl[:, t], A, B[:, t], C[:, t], chains=[1, 4])
+        assert np.array_equal(yt, y[:, t].reshape(-1)[[1, 4]])
+
+
+# ---------------------------------------------------------------- P11 structure
+
+def test_linearity_and_independence(orc):
+    Bsz, L, D, N = 2, 20, 4, 3
+    x1, u, A, B, C, h1 = rand_inputs(Bsz, L, D, N, seed=13, h0=True)
+    x2, _, _, _, _, h2 = rand_inputs(Bsz, L, D, N, seed=14, h0=True)
+    al, be = 0.75, -1.25
+    y1, t1 = orc.selscan_fwd(x1, u, A, B, C, True, h1)
+    y2, t2 = orc.selscan_fwd(x2, u, A, B, C, True, h2)
+    x12 = (al * x1.astype(np.float64) + be * x2.astype(np.float64))
+    # keep x exact in fp32: use multiples that are exact for these factors
+    y12, t12 = orc.selscan_fwd(x12.astype(np.float32), u, A, B, C, True, al * h1 + be * h2)
+    assert np.abs(x12.astype(np.float32) - x12).max() < 1e-6
+    lin = al * y1 + be * y2
+    # the fp32 rounding of x12 is the only perturbation; bound it loosely
+    close(y12, lin, 1e-5, 1e-5)
+    # scaling B or C by a power of two scales y exactly (no h0)
+    y0, _ = orc.selscan_fwd(x1, u, A, B, C, True)
+    yb, _ = orc.selscan_fwd(x1, u, A, B * 4, C, True)
+    yc, _ = orc.selscan_fwd(x1, u, A, B, C * 0.5, True)
+    assert np.array_equal(yb, 4 * y0) and np.array_equal(yc, 0.5 * y0)
+    # permuting channels permutes outputs (A permuted with them)
+    perm = np.array([2, 0, 3, 1])
+    yp, tp = orc.selscan_fwd(x1[:, :, perm], u[:, :, perm], A[perm], B, C, True, h1[:, perm])
+    y0h, t0h = orc.selscan_fwd(x1, u, A, B, C, True, h1)
+    assert np.array_equal(yp, y0h[:, :, perm]) and np.array_equal(tp, t0h[:, perm])
+    # chains are independent: changing channel 3 of batch 1 leaves every other chain alone
+    x3 = x1.copy(); x3[1, :, 3] += 1.0
+    y3, _ = orc.selscan_fwd(x3, u, A, B, C, True, h1)
+    mask = np.ones_like(y3, bool); mask[1, :, 3] = False
+    assert np.array_equal(y3[mask], y0h[mask]) and not np.array_equal(y3[1, :, 3], y0h[1, :, 3])
+
+
+def test_threads_and_chain_subset_bit_identical(orc):
+    Bsz, L, D, N = 3, 33, 5, 4
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=15, h0=True)
+    y1, h1 = orc.selscan_fwd(x, u, A, B, C, True, hh, nthreads=1)
+    y4, h4 = orc.selscan_fwd(x, u, A, B, C, True, hh, nthreads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(h1, h4)
+    chains = np.array([0, 7, 14, 3])
+    yc, hc = orc.selscan_fwd_chains(x, u, A, B, C, chains, True, hh, nthreads=2)
+    for i, c in enumerate(chains):
+        b, d = divmod(int(c), D)
+        assert np.array_equal(yc[i], y1[b, :, d]) and np.array_equal(hc[i], h1[b, d])
+
+
+def test_empty_sequence(orc):
+    hh = np.arange(2 * 3 * 4, dtype=np.float64).reshape(2, 3, 4)
+    z = np.zeros((2, 0, 3), np.float32)
+    y, hT = orc.selscan_fwd(z, z, np.zeros((3, 4), np.float32), np.zeros((2, 0, 4), np.float32),
+                            np.zeros((2, 0, 4), np.float32), True, hh)
+    assert y.shape == (2, 0, 3) and np.array_equal(hT, hh)
+
+
+def test_workload_inputs_feed_oracle(orc):
+    """The tiny workload runs end to end and its bf16 encoding round-trips."""
+    i = W.workload_inputs(1)
+    y, hT = orc.selscan_fwd(i.f32("x"), i.f32("delta"), i.A, i.f32("B"), i.f32("C"), True)
+    assert y.shape == (1, 64, 16) and np.all(np.isfinite(y))
