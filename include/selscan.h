@@ -1,0 +1,144 @@
+/*
+ * selscan.h -- C ABI of libselscan, Mamba's selective scan on one NVIDIA
+ * B300 (sm_103a).
+ *
+ * The operation (youngju.dev, "Mamba: Selective State Space Models",
+ * section 3.3, the simplified selective_scan listing; the recurrence of
+ * section 2.2; the (B, L, D) / (B, L, N) shapes of booiljung.github.io
+ * "3.1 LTI systems and input-dependent parameters", section 0.4.2):
+ *
+ *   for every batch b and channel d, starting from h[n] = h0[b,d,n] (or 0):
+ *     for t = 0 .. L-1:
+ *       dl = delta[b,t,d], or softplus(dl) = log(1 + e^dl) when delta_softplus
+ *       h[n] = exp(dl * A[d,n]) * h[n] + (dl * B[b,t,n]) * x[b,t,d]   (n < N)
+ *       y[b,t,d] = sum_n h[n] * C[b,t,n]
+ *     hT[b,d,n] = h[n]
+ *
+ * deltaB is the simplified dl * B of that listing (not the zero-order-hold
+ * form of section 2.2). The hidden state h never goes to device memory:
+ * it lives in registers; long sequences are cut into chunks whose carries
+ * are composed as associative (decay, offset) pairs (booiljung.github.io
+ * section 3.1.5.2, the parallel scan).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a DEVICE pointer (memory the current CUDA
+ *    device can read), row-major and contiguous, last axis fastest. The
+ *    caller owns all of them; the library keeps no pointer after a call
+ *    returns.
+ *  - dtype selects the element type of x, delta, B, C and y:
+ *    SELSCAN_F32 (IEEE fp32) or SELSCAN_BF16 (bfloat16). A, h0, hT and the
+ *    decode state are always fp32; all arithmetic is fp32. bf16 outputs are
+ *    rounded to nearest even.
+ *  - stream is a cudaStream_t (NULL = the legacy default stream). Work is
+ *    enqueued on it and the call returns without waiting: results are ready
+ *    once the stream reaches that point. Faults inside kernels surface, as
+ *    with any CUDA library, at the caller's next synchronisation (see
+ *    selscan_check_device_error).
+ *  - Return value: SELSCAN_OK (0) or a selscan_status code. Argument checks
+ *    run before any CUDA call: on SELSCAN_ERR_INVALID_ARG or
+ *    SELSCAN_ERR_UNSUPPORTED nothing was launched and no output was
+ *    touched. selscan_last_error() then describes the failure.
+ *  - Thread safety: calls may be made concurrently from several host
+ *    threads on different streams.
+ */
+#ifndef SELSCAN_H
+#define SELSCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SELSCAN_F32 = 0,
+    SELSCAN_BF16 = 1
+} selscan_dtype;
+
+typedef enum {
+    SELSCAN_OK = 0,
+    SELSCAN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad dtype, overlapping buffers */
+    SELSCAN_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (N > 64) */
+    SELSCAN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    SELSCAN_ERR_NO_MEMORY = 4     /* the chunk-carry workspace could not be allocated */
+} selscan_status;
+
+/* Largest state size N the kernels implement. */
+#define SELSCAN_MAX_N 64
+
+/*
+ * selscan_fwd -- the forward selective scan over a whole sequence.
+ * (youngju.dev "Mamba: Selective State Space Models", section 3.3;
+ *  softplus from booiljung.github.io section 0.4.2.)
+ *
+ *   x, delta : (Bsz, L, D), dtype        delta is the step size, or its raw
+ *                                        pre-activation when delta_softplus != 0
+ *   A        : (D, N) fp32               the diagonal state matrix per channel
+ *   B, C     : (Bsz, L, N), dtype        input / output matrices per token
+ *   y        : (Bsz, L, D), dtype        written
+ *   h0       : (Bsz, D, N) fp32 or NULL  initial state (NULL = zeros)
+ *   hT       : (Bsz, D, N) fp32 or NULL  final state, written when non-NULL
+ *
+ * Sizes: Bsz >= 0, L >= 0, D >= 0, 1 <= N <= SELSCAN_MAX_N. Bsz == 0 or
+ * D == 0 is an empty problem (OK, nothing written). L == 0 writes only hT
+ * (= h0, or zeros). x, delta, B, C and y must be non-NULL when L > 0 and
+ * Bsz * D > 0; A must be non-NULL when Bsz * D > 0.
+ *
+ * Aliasing: y may equal x or delta exactly (in-place output); h0 may equal
+ * hT exactly (resume in place). Any other overlap between y or hT and
+ * another argument is SELSCAN_ERR_INVALID_ARG.
+ *
+ * Memory: long sequences use a small library-owned workspace for the chunk
+ * carries (2 * ceil(L / chunk) * Bsz * D * N fp32 at most), taken from a
+ * private stream-ordered pool on `stream` and returned to it before the
+ * call's work completes; selscan_release_workspace() gives the pool's
+ * memory back to the device. SELSCAN_ERR_NO_MEMORY if it cannot be had.
+ */
+int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
+                const void *C, void *y, int64_t Bsz, int64_t L, int64_t D,
+                int64_t N, int dtype, int delta_softplus, const float *h0,
+                float *hT, void *stream);
+
+/*
+ * selscan_step -- one decode step of the recurrent mode, O(1) state per
+ * token (youngju.dev section 6: inference O(1) per token with a fixed
+ * state; the same update as selscan_fwd with L = 1).
+ *
+ *   state : (Bsz, D, N) fp32, read and updated in place
+ *   x     : (Bsz, D) fp32      delta : (Bsz, D) fp32, used as given (already
+ *                                      positive; no softplus is applied)
+ *   A     : (D, N) fp32        B, C  : (Bsz, N) fp32
+ *   y     : (Bsz, D) fp32, written:  y[b,d] = sum_n state'[b,d,n] * C[b,n]
+ *   where state'[b,d,n] = exp(delta[b,d] * A[d,n]) * state[b,d,n]
+ *                         + delta[b,d] * B[b,n] * x[b,d]
+ *
+ * Sizes as for selscan_fwd (Bsz, D >= 0; 1 <= N <= SELSCAN_MAX_N). y must
+ * not overlap state or any input; state must not overlap an input.
+ */
+int selscan_step(float *state, const float *x, const float *delta, const float *A,
+                 const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
+                 int64_t N, void *stream);
+
+/* Message describing the last non-OK status returned on this host thread
+ * (empty string if none). The pointer stays valid until the next call on
+ * the same thread. */
+const char *selscan_last_error(void);
+
+/* Waits for `stream` and reports whether work enqueued on it failed:
+ * SELSCAN_OK, or SELSCAN_ERR_CUDA with the CUDA error in
+ * selscan_last_error(). */
+int selscan_check_device_error(void *stream);
+
+/* Returns the memory held by the chunk-carry workspace pools of every
+ * device this process used to the device. Safe to call at any time; work
+ * already enqueued keeps its memory until it completes. */
+void selscan_release_workspace(void);
+
+/* Library version string, e.g. "libselscan 0.1.0 (sm_103a)". */
+const char *selscan_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELSCAN_H */

@@ -1,0 +1,223 @@
+"""libselscan: Mamba's selective scan on one NVIDIA B300 (sm_103a).
+
+A thin binding over the C ABI declared in ``include/selscan.h``; it only
+checks and marshals arguments. Every step of the scan runs in the library's
+CUDA kernels; PyTorch provides device memory and streams. There is no CPU
+path: if ``libselscan.so`` is missing the first call raises.
+
+    y = selscan_fwd(x, delta, A, B, C, delta_softplus=True)
+    y, hT = selscan_fwd(x, delta, A, B, C, h0=h0, return_final_state=True)
+    y = selscan_step(state, x, delta, A, B, C)     # state updated in place
+
+Tensors may live on the current CUDA device (the call is asynchronous on the
+current stream) or in host memory (preferably pinned): host inputs are copied
+to the device, the kernels run, and the outputs are copied back before the
+call returns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["selscan_fwd", "selscan_step", "last_error", "check_device_error",
+           "release_workspace", "version", "library_path", "SelscanError",
+           "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "MAX_N"]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY = 0, 1, 2, 3, 4
+F32, BF16 = 0, 1
+MAX_N = 64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libselscan.so")
+_lib = None
+
+
+class SelscanError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libselscan error {code}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with `python -m selective_state_space_157_b300.build`"
+                " (there is no fallback path)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I64, INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.selscan_fwd.restype = INT
+        L.selscan_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_step.restype = INT
+        L.selscan_step.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P]
+        L.selscan_last_error.restype = ctypes.c_char_p
+        L.selscan_last_error.argtypes = []
+        L.selscan_check_device_error.restype = INT
+        L.selscan_check_device_error.argtypes = [P]
+        L.selscan_release_workspace.restype = None
+        L.selscan_release_workspace.argtypes = []
+        L.selscan_version.restype = ctypes.c_char_p
+        L.selscan_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().selscan_last_error().decode()
+
+
+def version() -> str:
+    return lib().selscan_version().decode()
+
+
+def release_workspace() -> None:
+    lib().selscan_release_workspace()
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        raise SelscanError(rc, last_error())
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def check_device_error(stream=None) -> None:
+    """Wait for the stream and raise if work on it failed."""
+    _check(lib().selscan_check_device_error(_stream_ptr(stream)))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"x, delta, B, C must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, name, shape, dtype, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
+                return_final_state: bool = False, y=None, hT=None, stream=None):
+    """Forward selective scan (see ``include/selscan.h``).
+
+    x, delta: (Bsz, L, D) float32 or bfloat16; A: (D, N) float32;
+    B, C: (Bsz, L, N) same dtype as x; h0: (Bsz, D, N) float32 or None.
+    Returns y (Bsz, L, D), or (y, hT) with hT (Bsz, D, N) float32 when
+    ``return_final_state``. ``y`` / ``hT`` may be passed preallocated.
+    """
+    import torch
+    if x.device.type == "cpu":
+        return _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT)
+    dev = x.device
+    Bsz, L, D = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    code = _dtype_code(x)
+    _need(delta, "delta", (Bsz, L, D), x.dtype, dev)
+    _need(A, "A", (D, N), torch.float32, dev)
+    _need(B, "B", (Bsz, L, N), x.dtype, dev)
+    _need(C, "C", (Bsz, L, N), x.dtype, dev)
+    _need(x, "x", (Bsz, L, D), x.dtype, dev)
+    if h0 is not None:
+        _need(h0, "h0", (Bsz, D, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bsz, L, D), dtype=x.dtype, device=dev)
+    else:
+        _need(y, "y", (Bsz, L, D), x.dtype, dev)
+    if return_final_state and hT is None:
+        hT = torch.empty((Bsz, D, N), dtype=torch.float32, device=dev)
+    if hT is not None:
+        _need(hT, "hT", (Bsz, D, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
+                               Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
+                               _stream_ptr(stream))
+    _check(rc)
+    return (y, hT) if (return_final_state or hT is not None) else y
+
+
+def selscan_step(state, x, delta, A, B, C, y=None, stream=None):
+    """One decode step (see ``include/selscan.h``): ``state`` (Bsz, D, N)
+    float32 is updated in place; returns y (Bsz, D) float32. delta is used
+    as given (no softplus)."""
+    import torch
+    if state.device.type == "cpu":
+        return _step_host(state, x, delta, A, B, C, y)
+    dev = state.device
+    Bsz, D, N = state.shape
+    f = torch.float32
+    _need(state, "state", (Bsz, D, N), f, dev)
+    _need(x, "x", (Bsz, D), f, dev)
+    _need(delta, "delta", (Bsz, D), f, dev)
+    _need(A, "A", (D, N), f, dev)
+    _need(B, "B", (Bsz, N), f, dev)
+    _need(C, "C", (Bsz, N), f, dev)
+    if y is None:
+        y = torch.empty((Bsz, D), dtype=f, device=dev)
+    else:
+        _need(y, "y", (Bsz, D), f, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                _ptr(y), Bsz, D, N, _stream_ptr(stream))
+    _check(rc)
+    return y
+
+
+# ---- host tensors: copy in, run on the current device, copy out ------------
+
+def _to_dev(t, dev):
+    return None if t is None else t.to(dev, non_blocking=True)
+
+
+def _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT):
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    xd, dd, Ad, Bd, Cd, h0d = (_to_dev(t, dev) for t in (x, delta, A, B, C, h0))
+    want_state = return_final_state or hT is not None
+    out = selscan_fwd(xd, dd, Ad, Bd, Cd, delta_softplus, h0d, return_final_state=want_state)
+    yd, hTd = out if want_state else (out, None)
+    if y is None:
+        y = torch.empty(yd.shape, dtype=yd.dtype, pin_memory=True)
+    y.copy_(yd, non_blocking=True)
+    if want_state:
+        if hT is None:
+            hT = torch.empty(hTd.shape, dtype=hTd.dtype, pin_memory=True)
+        hT.copy_(hTd, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return (y, hT) if want_state else y
+
+
+def _step_host(state, x, delta, A, B, C, y):
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sd, xd, dd, Ad, Bd, Cd = (_to_dev(t, dev) for t in (state, x, delta, A, B, C))
+    yd = selscan_step(sd, xd, dd, Ad, Bd, Cd)
+    if y is None:
+        y = torch.empty(yd.shape, dtype=yd.dtype, pin_memory=True)
+    y.copy_(yd, non_blocking=True)
+    state.copy_(sd, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return y

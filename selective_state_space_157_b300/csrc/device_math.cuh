@@ -1,0 +1,107 @@
+// device_math.cuh -- small device helpers shared by the libselscan kernels:
+// element loads/stores for fp32 and bf16, the base-2 exponential on the
+// MUFU unit, and softplus.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace selscan {
+
+// log2(e): exp(v) = 2^(v * log2 e), so A is pre-scaled once per thread and
+// every per-step exponential is one MUFU ex2.
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^v on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// of a few ulp; results below the normal range flush to zero).
+__device__ __forceinline__ float ex2(float v)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// softplus(u) = log(1 + e^u) (booiljung.github.io, "3.1 LTI systems and
+// input-dependent parameters", section 0.4.2), evaluated as
+// max(u, 0) + log1p(e^-|u|) so that neither term overflows.
+__device__ __forceinline__ float softplus(float u)
+{
+    float e = ex2(-fabsf(u) * kLog2e);
+    return fmaxf(u, 0.0f) + log1pf(e);
+}
+
+template <typename T> struct Io;
+
+template <> struct Io<float> {
+    __device__ __forceinline__ static float load(const float *p) { return __ldg(p); }
+    __device__ __forceinline__ static void store(float *p, float v) { *p = v; }
+};
+
+template <> struct Io<__nv_bfloat16> {
+    __device__ __forceinline__ static float load(const __nv_bfloat16 *p)
+    {
+        return __bfloat162float(__ldg(p));
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *p, float v)
+    {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+// Loads NS consecutive state-indexed values p[0..NS) as fp32.
+// VEC: the caller guarantees p is 16-byte aligned (8-byte for 4 bf16) and
+// all NS values exist. Otherwise only the first `valid` are read and the
+// rest are zero.
+template <typename T, int NS, bool VEC> struct StateLoad;
+
+template <int NS> struct StateLoad<float, NS, true> {
+    __device__ __forceinline__ static void run(const float *p, int, float (&v)[NS])
+    {
+        static_assert(NS % 4 == 0, "fp32 vector loads take 4 states");
+#pragma unroll
+        for (int j = 0; j < NS; j += 4) {
+            float4 w = __ldg(reinterpret_cast<const float4 *>(p + j));
+            v[j] = w.x; v[j + 1] = w.y; v[j + 2] = w.z; v[j + 3] = w.w;
+        }
+    }
+};
+
+template <int NS> struct StateLoad<__nv_bfloat16, NS, true> {
+    __device__ __forceinline__ static void run(const __nv_bfloat16 *p, int, float (&v)[NS])
+    {
+        static_assert(NS % 4 == 0, "bf16 vector loads take 4 states");
+        if constexpr (NS % 8 == 0) {
+#pragma unroll
+            for (int j = 0; j < NS; j += 8) {
+                uint4 w = __ldg(reinterpret_cast<const uint4 *>(p + j));
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[j + 2 * i] = __uint_as_float(u[i] << 16);
+                    v[j + 2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < NS; j += 4) {
+                uint2 w = __ldg(reinterpret_cast<const uint2 *>(p + j));
+                v[j] = __uint_as_float(w.x << 16);
+                v[j + 1] = __uint_as_float(w.x & 0xffff0000u);
+                v[j + 2] = __uint_as_float(w.y << 16);
+                v[j + 3] = __uint_as_float(w.y & 0xffff0000u);
+            }
+        }
+    }
+};
+
+template <typename T, int NS> struct StateLoad<T, NS, false> {
+    __device__ __forceinline__ static void run(const T *p, int valid, float (&v)[NS])
+    {
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+            v[j] = (j < valid) ? Io<T>::load(p + j) : 0.0f;
+    }
+};
+
+} // namespace selscan

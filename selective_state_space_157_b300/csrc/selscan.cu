@@ -1,0 +1,398 @@
+// selscan.cu -- host side of libselscan: argument checks, launch planning,
+// the chunk-carry workspace, and the exported C entry points declared in
+// include/selscan.h.
+#include "selscan.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "scan_fwd.cuh"
+#include "scan_step.cuh"
+
+namespace selscan {
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(SELSCAN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---- argument checks ------------------------------------------------------
+
+constexpr int64_t kMaxElems = int64_t(1) << 60;
+
+bool mul_ok(int64_t a, int64_t b, int64_t c, int64_t *out)
+{
+    if (a == 0 || b == 0 || c == 0) { *out = 0; return true; }
+    if (a > kMaxElems / b) return false;
+    int64_t ab = a * b;
+    if (ab > kMaxElems / c) return false;
+    *out = ab * c;
+    return true;
+}
+
+struct Range {
+    uintptr_t lo, hi;   // [lo, hi)
+    const char *name;
+};
+
+Range range(const void *p, int64_t bytes, const char *name)
+{
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, p ? lo + (uintptr_t)bytes : lo, name};
+}
+
+bool overlaps(const Range &a, const Range &b)
+{
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+long env_long(const char *name, long dflt)
+{
+    const char *s = getenv(name);
+    if (!s || !*s) return dflt;
+    char *end = nullptr;
+    long v = strtol(s, &end, 10);
+    return (end && *end == '\0') ? v : dflt;
+}
+
+// ---- per-device state -----------------------------------------------------
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+cudaMemPool_t g_pool[kMaxDevices];
+int g_sms[kMaxDevices];
+
+int device_info(int *dev, int *sms)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= kMaxDevices) return fail(SELSCAN_ERR_UNSUPPORTED, "device ordinal %d", *dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[*dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_sms[*dev] = n;
+    }
+    *sms = g_sms[*dev];
+    return SELSCAN_OK;
+}
+
+int workspace_pool(int dev, cudaMemPool_t *pool)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p;
+        cudaError_t e = cudaMemPoolCreate(&p, &props);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;   // keep freed blocks for reuse until released
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pool[dev] = p;
+    }
+    *pool = g_pool[dev];
+    return SELSCAN_OK;
+}
+
+// ---- forward dispatch -----------------------------------------------------
+
+using ScanKernel = void (*)(ScanArgs);
+
+struct ScanKernels {
+    ScanKernel readout, aggregate;
+};
+
+template <typename T, int NS, int NSPLIT>
+ScanKernels pick_vec(bool vec)
+{
+    if (vec)
+        return {scan_chunk_kernel<T, NS, NSPLIT, true, true>, scan_chunk_kernel<T, NS, NSPLIT, false, true>};
+    return {scan_chunk_kernel<T, NS, NSPLIT, true, false>, scan_chunk_kernel<T, NS, NSPLIT, false, false>};
+}
+
+template <typename T>
+bool pick_shape(int ns, int nsplit, bool vec, ScanKernels *out)
+{
+    switch (ns * 100 + nsplit) {
+    case 401: *out = pick_vec<T, 4, 1>(vec); return true;
+    case 801: *out = pick_vec<T, 8, 1>(vec); return true;
+    case 1601: *out = pick_vec<T, 16, 1>(vec); return true;
+    case 402: *out = pick_vec<T, 4, 2>(vec); return true;
+    case 802: *out = pick_vec<T, 8, 2>(vec); return true;
+    case 1602: *out = pick_vec<T, 16, 2>(vec); return true;
+    case 404: *out = pick_vec<T, 4, 4>(vec); return true;
+    case 804: *out = pick_vec<T, 8, 4>(vec); return true;
+    case 1604: *out = pick_vec<T, 16, 4>(vec); return true;
+    default: return false;
+    }
+}
+
+struct FwdPlan {
+    int ns, nsplit;
+    bool vec;
+    int64_t chunk;
+    int K;
+    int dtiles;
+};
+
+// States per thread and threads per chain: the smallest NS in {4, 8, 16}
+// covering N / NSPLIT. NSPLIT is 1 up to N = 16 (2 and 4 beyond), unless
+// SELSCAN_NSPLIT asks for more threads per chain.
+void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const void *B,
+              const void *C, int sms, FwdPlan *p)
+{
+    int nsplit = N <= 16 ? 1 : (N <= 32 ? 2 : 4);
+    long want = env_long("SELSCAN_NSPLIT", 0);
+    if ((want == 2 || want == 4) && want > nsplit && N >= 4 * want)
+        nsplit = (int)want;
+    int64_t per = (N + nsplit - 1) / nsplit;
+    int ns = per <= 4 ? 4 : (per <= 8 ? 8 : 16);
+    p->ns = ns;
+    p->nsplit = nsplit;
+    p->vec = (N == (int64_t)ns * nsplit) && ((N * (int64_t)es) % 16 == 0) && aligned(B, 16) &&
+             aligned(C, 16);
+    const int chan_per_cta = kScanThreads / nsplit;
+    p->dtiles = (int)((D + chan_per_cta - 1) / chan_per_cta);
+
+    // Chunking: enough chains in flight to keep every SM busy; each chunk
+    // beyond the first costs one extra reduction pass over its timesteps.
+    const int64_t warps1 = Bsz * (int64_t)p->dtiles * (kScanThreads / 32);
+    const long target = env_long("SELSCAN_TARGET_WARPS", 8) * (long)sms;
+    int64_t K = warps1 >= target ? 1 : (target + warps1 - 1) / warps1;
+    const int64_t min_chunk = 64;
+    int64_t maxK = (L + min_chunk - 1) / min_chunk;
+    if (K > maxK) K = maxK;
+    if (K < 1) K = 1;
+    int64_t chunk = L > 0 ? (L + K - 1) / K : 1;
+    long force = env_long("SELSCAN_CHUNK", -1);
+    if (force == 0) chunk = L > 0 ? L : 1;
+    else if (force > 0) chunk = force;
+    if (chunk < 1) chunk = 1;
+    const int64_t min_for_grid = (L + 65534) / 65535;   // gridDim.y limit
+    if (chunk < min_for_grid) chunk = min_for_grid;
+    p->chunk = chunk;
+    p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
+}
+
+int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cudaStream_t st)
+{
+    ScanKernels ks;
+    bool ok = dtype == SELSCAN_F32 ? pick_shape<float>(plan.ns, plan.nsplit, plan.vec, &ks)
+                                   : pick_shape<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, &ks);
+    if (!ok) return fail(SELSCAN_ERR_UNSUPPORTED, "no kernel for NS=%d NSPLIT=%d", plan.ns, plan.nsplit);
+
+    ScanArgs a = base;
+    a.chunk = plan.chunk;
+    a.K = plan.K;
+    a.dtiles = plan.dtiles;
+    const int64_t gx = a.Bsz * plan.dtiles;
+    if (gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+
+    void *ws = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if (plan.K > 1) {
+        const int64_t bd = a.Bsz * a.D;
+        const size_t bytes = (size_t)(plan.K - 1) * (size_t)bd * (size_t)(a.N + 1) * sizeof(float);
+        int rc = workspace_pool(dev, &pool);
+        if (rc != SELSCAN_OK) return rc;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SELSCAN_ERR_NO_MEMORY, "chunk workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+        }
+        a.agg_h = static_cast<float *>(ws);
+        a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
+
+        ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
+        CarryArgs c{a.A, a.h0, a.agg_h, a.agg_s, a.Bsz, a.D, a.N, plan.K};
+        const int64_t total = a.Bsz * a.D * a.N;
+        scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(c);
+    }
+    ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (ws) cudaFreeAsync(ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return SELSCAN_OK;
+}
+
+} // namespace
+} // namespace selscan
+
+using namespace selscan;
+
+extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
+                           const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                           int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
+{
+    g_err[0] = '\0';
+    if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
+        return fail(SELSCAN_ERR_INVALID_ARG, "dtype %d is neither SELSCAN_F32 nor SELSCAN_BF16", dtype);
+    if (Bsz < 0 || L < 0 || D < 0)
+        return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld L=%lld D=%lld)",
+                    (long long)Bsz, (long long)L, (long long)D);
+    if (N < 1)
+        return fail(SELSCAN_ERR_INVALID_ARG, "N=%lld must be >= 1", (long long)N);
+    if (N > SELSCAN_MAX_N)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "N=%lld exceeds SELSCAN_MAX_N=%d", (long long)N, SELSCAN_MAX_N);
+    int64_t nld, nln, ndn;
+    if (!mul_ok(Bsz, L, D, &nld) || !mul_ok(Bsz, L, N, &nln) || !mul_ok(Bsz, D, N, &ndn))
+        return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow (Bsz=%lld L=%lld D=%lld N=%lld)",
+                    (long long)Bsz, (long long)L, (long long)D, (long long)N);
+    if (Bsz == 0 || D == 0)
+        return SELSCAN_OK;
+    if (!A)
+        return fail(SELSCAN_ERR_INVALID_ARG, "A is NULL");
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    if (L > 0) {
+        if (!x || !delta || !B || !C || !y)
+            return fail(SELSCAN_ERR_INVALID_ARG, "x, delta, B, C and y must be non-NULL when L > 0");
+        if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) || !aligned(y, es))
+            return fail(SELSCAN_ERR_INVALID_ARG, "x, delta, B, C, y must be aligned to their element size");
+    }
+    if (!aligned(A, 4) || !aligned(h0, 4) || !aligned(hT, 4))
+        return fail(SELSCAN_ERR_INVALID_ARG, "A, h0, hT must be 4-byte aligned");
+
+    const Range ry = range(L > 0 ? y : nullptr, nld * es, "y"), rhT = range(hT, ndn * 4, "hT");
+    struct Input {
+        Range r;
+        bool y_may_equal;    // y may be this buffer exactly (in-place output)
+        bool hT_may_equal;   // hT may be this buffer exactly (resume in place)
+    };
+    const Input ins[] = {
+        {range(x, nld * es, "x"), true, false},      {range(delta, nld * es, "delta"), true, false},
+        {range(B, nln * es, "B"), false, false},     {range(C, nln * es, "C"), false, false},
+        {range(A, D * N * 4, "A"), false, false},    {range(h0, ndn * 4, "h0"), false, true},
+    };
+    for (const Input &in : ins) {
+        if (overlaps(ry, in.r) && !(in.y_may_equal && in.r.lo == ry.lo))
+            return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps %s", in.r.name);
+        if (overlaps(rhT, in.r) && !(in.hT_may_equal && in.r.lo == rhT.lo))
+            return fail(SELSCAN_ERR_INVALID_ARG, "hT overlaps %s", in.r.name);
+    }
+    if (overlaps(ry, rhT))
+        return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps hT");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (L == 0) {
+        if (!hT || hT == h0) return SELSCAN_OK;
+        cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, (size_t)ndn * 4, cudaMemcpyDeviceToDevice, st)
+                           : cudaMemsetAsync(hT, 0, (size_t)ndn * 4, st);
+        return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state copy");
+    }
+
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    FwdPlan plan;
+    plan_fwd(Bsz, L, D, N, es, B, C, sms, &plan);
+    ScanArgs a;
+    memset(&a, 0, sizeof a);
+    a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
+    a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
+    a.softplus = delta_softplus ? 1 : 0;
+    return launch_fwd(a, plan, dtype, dev, st);
+}
+
+extern "C" int selscan_step(float *state, const float *x, const float *delta, const float *A,
+                            const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
+                            int64_t N, void *stream)
+{
+    g_err[0] = '\0';
+    if (Bsz < 0 || D < 0)
+        return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld D=%lld)", (long long)Bsz, (long long)D);
+    if (N < 1)
+        return fail(SELSCAN_ERR_INVALID_ARG, "N=%lld must be >= 1", (long long)N);
+    if (N > SELSCAN_MAX_N)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "N=%lld exceeds SELSCAN_MAX_N=%d", (long long)N, SELSCAN_MAX_N);
+    int64_t ndn, nd1;
+    if (!mul_ok(Bsz, D, N, &ndn) || !mul_ok(Bsz, D, 1, &nd1))
+        return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
+    if (Bsz == 0 || D == 0)
+        return SELSCAN_OK;
+    if (!state || !x || !delta || !A || !B || !C || !y)
+        return fail(SELSCAN_ERR_INVALID_ARG, "state, x, delta, A, B, C and y must be non-NULL");
+    const void *ptrs[] = {state, x, delta, A, B, C, y};
+    for (const void *p : ptrs)
+        if (!aligned(p, 4))
+            return fail(SELSCAN_ERR_INVALID_ARG, "every pointer must be 4-byte aligned");
+    const Range rs = range(state, ndn * 4, "state"), ry = range(y, nd1 * 4, "y");
+    const Range ins[] = {range(x, nd1 * 4, "x"), range(delta, nd1 * 4, "delta"), range(A, D * N * 4, "A"),
+                         range(B, Bsz * N * 4, "B"), range(C, Bsz * N * 4, "C")};
+    for (const Range &r : ins) {
+        if (overlaps(rs, r)) return fail(SELSCAN_ERR_INVALID_ARG, "state overlaps %s", r.name);
+        if (overlaps(ry, r)) return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps %s", r.name);
+    }
+    if (overlaps(rs, ry))
+        return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps state");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    StepArgs a{state, x, delta, A, B, C, y, Bsz, D, N};
+    const int64_t chains = Bsz * D;
+    const int G = (int)(N / 4);
+    // 4 states per lane, G lanes per chain; G must divide the warp so that a
+    // chain's lanes never straddle two warps.
+    const bool vec = (N % 4 == 0) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&
+                     aligned(state, 16) && aligned(A, 16) && aligned(B, 16) && aligned(C, 16);
+    if (vec) {
+        const int64_t blocks = (chains * G + kStepThreads - 1) / kStepThreads;
+        if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+        switch (G) {
+        case 1: step_vec_kernel<1><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
+        case 2: step_vec_kernel<2><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
+        case 4: step_vec_kernel<4><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
+        case 8: step_vec_kernel<8><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
+        default: step_vec_kernel<16><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
+        }
+    } else {
+        const int64_t blocks = (chains + kStepThreads - 1) / kStepThreads;
+        if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+        step_scalar_kernel<<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+}
+
+extern "C" const char *selscan_last_error(void) { return g_err; }
+
+extern "C" int selscan_check_device_error(void *stream)
+{
+    g_err[0] = '\0';
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "device work");
+}
+
+extern "C" void selscan_release_workspace(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < kMaxDevices; ++i)
+        if (g_pool[i]) cudaMemPoolTrimTo(g_pool[i], 0);
+}
+
+extern "C" const char *selscan_version(void) { return "libselscan 0.1.0 (sm_103a)"; }
