@@ -60,7 +60,9 @@ typedef enum {
     SELSCAN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad dtype, overlapping buffers */
     SELSCAN_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (N > 64) */
     SELSCAN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-    SELSCAN_ERR_NO_MEMORY = 4     /* the chunk-carry workspace could not be allocated */
+    SELSCAN_ERR_NO_MEMORY = 4,    /* the chunk-carry workspace could not be allocated */
+    SELSCAN_ERR_TIMEOUT = 5       /* a kernel gave up waiting for its input tiles (reported by
+                                     selscan_check_device_error; the kernel's outputs are invalid) */
 } selscan_status;
 
 /* Largest state size N the kernels implement. */
@@ -119,14 +121,31 @@ int selscan_step(float *state, const float *x, const float *delta, const float *
                  const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
                  int64_t N, void *stream);
 
+/*
+ * selscan_fwd_plan -- how selscan_fwd would run a problem of this size on
+ * the current device, without running it (for tests and benchmarks).
+ *   chunks    : number of chunks the sequence is cut into (1 = one pass)
+ *   chunk_len : timesteps per chunk
+ *   launches  : kernels one selscan_fwd call enqueues (1, or 3 when chunked)
+ * Any output pointer may be NULL. Same size checks as selscan_fwd; needs a
+ * CUDA device (it reads the SM count). The plan depends only on the sizes,
+ * dtype and device, plus the tuning variables SELSCAN_CHUNK and
+ * SELSCAN_TARGET_WARPS when set.
+ */
+int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype,
+                     int *chunks, int64_t *chunk_len, int *launches);
+
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on
  * the same thread. */
 const char *selscan_last_error(void);
 
 /* Waits for `stream` and reports whether work enqueued on it failed:
- * SELSCAN_OK, or SELSCAN_ERR_CUDA with the CUDA error in
- * selscan_last_error(). */
+ * SELSCAN_OK; SELSCAN_ERR_CUDA with the CUDA error in selscan_last_error();
+ * or SELSCAN_ERR_TIMEOUT when a kernel stopped waiting for input tiles that
+ * never arrived (every wait inside the kernels is bounded, so a broken
+ * pipeline ends with this status instead of a hang). The fault word is
+ * per device and is cleared by this call. */
 int selscan_check_device_error(void *stream);
 
 /* Returns the memory held by the chunk-carry workspace pools of every

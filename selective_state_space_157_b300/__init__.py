@@ -19,11 +19,12 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["selscan_fwd", "selscan_step", "last_error", "check_device_error",
+__all__ = ["selscan_fwd", "selscan_step", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
-           "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "MAX_N"]
+           "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
+           "MAX_N"]
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 F32, BF16 = 0, 1
 MAX_N = 64
 
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_release_workspace.argtypes = []
         L.selscan_version.restype = ctypes.c_char_p
         L.selscan_version.argtypes = []
+        L.selscan_fwd_plan.restype = INT
+        L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P]
         _lib = L
     return _lib
 
@@ -74,6 +77,17 @@ def last_error() -> str:
 
 def version() -> str:
     return lib().selscan_version().decode()
+
+
+def fwd_plan(Bsz: int, L: int, D: int, N: int, bf16: bool = False) -> dict:
+    """How selscan_fwd would split this problem on the current device:
+    {"chunks", "chunk_len", "launches"}."""
+    k = ctypes.c_int(0)
+    t = ctypes.c_int64(0)
+    n = ctypes.c_int(0)
+    _check(lib().selscan_fwd_plan(Bsz, L, D, N, BF16 if bf16 else F32, ctypes.byref(k),
+                                  ctypes.byref(t), ctypes.byref(n)))
+    return {"chunks": k.value, "chunk_len": t.value, "launches": n.value}
 
 
 def release_workspace() -> None:

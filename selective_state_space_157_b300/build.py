@@ -26,6 +26,19 @@ def sources():
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
+def source_digest() -> str:
+    """sha256 over the kernel sources and the public header (identifies the
+    build a profile was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in sources():
+        if p.endswith(".py"):
+            continue
+        h.update(os.path.basename(p).encode())
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False

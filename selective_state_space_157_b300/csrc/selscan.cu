@@ -3,6 +3,8 @@
 // include/selscan.h.
 #include "selscan.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -15,6 +17,7 @@
 
 #include "scan_fwd.cuh"
 #include "scan_step.cuh"
+#include "scan_tma.cuh"
 
 namespace selscan {
 namespace {
@@ -153,9 +156,109 @@ bool pick_shape(int ns, int nsplit, bool vec, ScanKernels *out)
     }
 }
 
+// ---- TMA path -----------------------------------------------------------
+
+constexpr int kTT = 16;       // timesteps per pipeline stage (default)
+constexpr int kStages = 4;    // buffers in flight (default)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// 3-D map over a row-major (d2, d1, d0) tensor, box (box0, box1, 1).
+bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, size_t es, const void *base, uint64_t d0, uint64_t d1,
+               uint64_t d2, uint32_t box0, uint32_t box1)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+using TmaKernel = void (*)(TmaScanArgs);
+
+struct TmaKernels {
+    TmaKernel readout, aggregate;
+    size_t smem_readout, smem_aggregate;
+    int tt, stages;
+};
+
+template <typename T, int NS, int NSPLIT, bool VEC, int TT>
+bool prepare_tma_tt(int64_t N, int stages, TmaKernels *out)
+{
+    constexpr int DPB = kScanThreads / NSPLIT;
+    auto kr = scan_tma_kernel<T, NS, NSPLIT, true, VEC, TT>;
+    auto ka = scan_tma_kernel<T, NS, NSPLIT, false, VEC, TT>;
+    const size_t sr = tma_smem_bytes(sizeof(T), TT, DPB, N, true, stages);
+    const size_t sa = tma_smem_bytes(sizeof(T), TT, DPB, N, false, stages);
+    // The shared-memory ceiling is per kernel; raise it to what this N needs.
+    if (cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr) != cudaSuccess ||
+        cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    *out = TmaKernels{kr, ka, sr, sa, TT, stages};
+    return true;
+}
+
+// Timesteps per stage and buffers in flight: 16 x 4 unless SELSCAN_TMA_TT /
+// SELSCAN_TMA_STAGES ask otherwise (tuning knobs; TT is 8 or 16).
+template <typename T, int NS, int NSPLIT, bool VEC>
+bool prepare_tma(int64_t N, TmaKernels *out)
+{
+    long stages = env_long("SELSCAN_TMA_STAGES", kStages);
+    if (stages < 2) stages = 2;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (env_long("SELSCAN_TMA_TT", kTT) == 8)
+        return prepare_tma_tt<T, NS, NSPLIT, VEC, 8>(N, (int)stages, out);
+    return prepare_tma_tt<T, NS, NSPLIT, VEC, kTT>(N, (int)stages, out);
+}
+
+template <typename T, int NS, int NSPLIT>
+bool prepare_tma_vec(bool vec, int64_t N, TmaKernels *out)
+{
+    return vec ? prepare_tma<T, NS, NSPLIT, true>(N, out) : prepare_tma<T, NS, NSPLIT, false>(N, out);
+}
+
+template <typename T>
+bool pick_tma(int ns, int nsplit, bool vec, int64_t N, TmaKernels *out)
+{
+    switch (ns * 100 + nsplit) {
+    case 401: return prepare_tma_vec<T, 4, 1>(vec, N, out);
+    case 801: return prepare_tma_vec<T, 8, 1>(vec, N, out);
+    case 1601: return prepare_tma_vec<T, 16, 1>(vec, N, out);
+    case 1602: return prepare_tma_vec<T, 16, 2>(vec, N, out);
+    case 1604: return prepare_tma_vec<T, 16, 4>(vec, N, out);
+    case 802: return prepare_tma_vec<T, 8, 2>(vec, N, out);
+    case 404: return prepare_tma_vec<T, 4, 4>(vec, N, out);
+    default: return false;
+    }
+}
+
 struct FwdPlan {
     int ns, nsplit;
     bool vec;
+    bool tma;
     int64_t chunk;
     int K;
     int dtiles;
@@ -164,8 +267,8 @@ struct FwdPlan {
 // States per thread and threads per chain: the smallest NS in {4, 8, 16}
 // covering N / NSPLIT. NSPLIT is 1 up to N = 16 (2 and 4 beyond), unless
 // SELSCAN_NSPLIT asks for more threads per chain.
-void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const void *B,
-              const void *C, int sms, FwdPlan *p)
+void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const void *x, const void *delta,
+              const void *B, const void *C, int sms, FwdPlan *p)
 {
     int nsplit = N <= 16 ? 1 : (N <= 32 ? 2 : 4);
     long want = env_long("SELSCAN_NSPLIT", 0);
@@ -177,14 +280,18 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->nsplit = nsplit;
     p->vec = (N == (int64_t)ns * nsplit) && ((N * (int64_t)es) % 16 == 0) && aligned(B, 16) &&
              aligned(C, 16);
+    const bool bases16 = aligned(x, 16) && aligned(delta, 16) && aligned(B, 16) && aligned(C, 16);
     const int chan_per_cta = kScanThreads / nsplit;
     p->dtiles = (int)((D + chan_per_cta - 1) / chan_per_cta);
+    // TMA needs 16-byte aligned bases and row strides, and 32-bit coordinates.
+    p->tma = bases16 && env_long("SELSCAN_NO_TMA", 0) == 0 && (D * (int64_t)es) % 16 == 0 && (N * (int64_t)es) % 16 == 0 &&
+             L <= 0x7fffffffLL && D <= 0x7fffffffLL && Bsz <= 0x7fffffffLL;
 
     // Chunking: enough chains in flight to keep every SM busy; each chunk
     // beyond the first costs one extra reduction pass over its timesteps.
     const int64_t warps1 = Bsz * (int64_t)p->dtiles * (kScanThreads / 32);
     const long target = env_long("SELSCAN_TARGET_WARPS", 8) * (long)sms;
-    int64_t K = warps1 >= target ? 1 : (target + warps1 - 1) / warps1;
+    int64_t K = (warps1 <= 0 || warps1 >= target) ? 1 : (target + warps1 - 1) / warps1;
     const int64_t min_chunk = 64;
     int64_t maxK = (L + min_chunk - 1) / min_chunk;
     if (K > maxK) K = maxK;
@@ -202,7 +309,12 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
 
 int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cudaStream_t st)
 {
-    ScanKernels ks;
+    ScanKernels ks{};
+    TmaKernels tk{};
+    bool use_tma = plan.tma;
+    if (use_tma)
+        use_tma = dtype == SELSCAN_F32 ? pick_tma<float>(plan.ns, plan.nsplit, plan.vec, base.N, &tk)
+                                       : pick_tma<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, base.N, &tk);
     bool ok = dtype == SELSCAN_F32 ? pick_shape<float>(plan.ns, plan.nsplit, plan.vec, &ks)
                                    : pick_shape<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, &ks);
     if (!ok) return fail(SELSCAN_ERR_UNSUPPORTED, "no kernel for NS=%d NSPLIT=%d", plan.ns, plan.nsplit);
@@ -213,6 +325,21 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cu
     a.dtiles = plan.dtiles;
     const int64_t gx = a.Bsz * plan.dtiles;
     if (gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+
+    TmaScanArgs ta;
+    if (use_tma) {
+        memset(&ta, 0, sizeof ta);
+        const CUtensorMapDataType dt =
+            dtype == SELSCAN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+        const uint32_t dpb = (uint32_t)(kScanThreads / plan.nsplit);
+        const uint32_t tt = (uint32_t)tk.tt;
+        ta.stages = tk.stages;
+        use_tma = encode_3d(&ta.mx, dt, es, a.x, a.D, a.L, a.Bsz, dpb, tt) &&
+                  encode_3d(&ta.md, dt, es, a.delta, a.D, a.L, a.Bsz, dpb, tt) &&
+                  encode_3d(&ta.mB, dt, es, a.B, a.N, a.L, a.Bsz, (uint32_t)a.N, tt) &&
+                  encode_3d(&ta.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt);
+    }
 
     void *ws = nullptr;
     cudaMemPool_t pool = nullptr;
@@ -228,13 +355,22 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cu
         }
         a.agg_h = static_cast<float *>(ws);
         a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
-
-        ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
+        if (use_tma) {
+            ta.s = a;
+            tk.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, tk.smem_aggregate, st>>>(ta);
+        } else {
+            ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
+        }
         CarryArgs c{a.A, a.h0, a.agg_h, a.agg_s, a.Bsz, a.D, a.N, plan.K};
         const int64_t total = a.Bsz * a.D * a.N;
         scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(c);
     }
-    ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
+    if (use_tma) {
+        ta.s = a;
+        tk.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, tk.smem_readout, st>>>(ta);
+    } else {
+        ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (ws) cudaFreeAsync(ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -310,7 +446,7 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     int rc = device_info(&dev, &sms);
     if (rc != SELSCAN_OK) return rc;
     FwdPlan plan;
-    plan_fwd(Bsz, L, D, N, es, B, C, sms, &plan);
+    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, sms, &plan);
     ScanArgs a;
     memset(&a, 0, sizeof a);
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
@@ -378,6 +514,31 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
+extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, int *chunks,
+                                int64_t *chunk_len, int *launches)
+{
+    g_err[0] = '\0';
+    if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
+        return fail(SELSCAN_ERR_INVALID_ARG, "dtype %d is neither SELSCAN_F32 nor SELSCAN_BF16", dtype);
+    if (Bsz < 0 || L < 0 || D < 0 || N < 1)
+        return fail(SELSCAN_ERR_INVALID_ARG, "bad sizes");
+    if (N > SELSCAN_MAX_N)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "N=%lld exceeds SELSCAN_MAX_N=%d", (long long)N, SELSCAN_MAX_N);
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    FwdPlan plan;
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    // Alignment does not change the chunking; pass 16-byte aligned stand-ins.
+    const void *al = reinterpret_cast<const void *>(uintptr_t(256));
+    plan_fwd(Bsz, L, D, N, es, al, al, al, al, sms, &plan);
+    const bool empty = Bsz == 0 || D == 0 || L == 0;
+    if (chunks) *chunks = empty ? 0 : plan.K;
+    if (chunk_len) *chunk_len = empty ? 0 : plan.chunk;
+    if (launches) *launches = empty ? 0 : (plan.K > 1 ? 3 : 1);
+    return SELSCAN_OK;
+}
+
 extern "C" const char *selscan_last_error(void) { return g_err; }
 
 extern "C" int selscan_check_device_error(void *stream)
@@ -385,7 +546,15 @@ extern "C" int selscan_check_device_error(void *stream)
     g_err[0] = '\0';
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = cudaGetLastError();
-    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "device work");
+    if (e != cudaSuccess) return cuda_fail(e, "device work");
+    unsigned fault = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&fault, g_selscan_fault, sizeof fault);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device fault word");
+    if (fault != 0) {
+        cudaMemcpyToSymbol(g_selscan_fault, &zero, sizeof zero);
+        return fail(SELSCAN_ERR_TIMEOUT, "a kernel gave up waiting for its input tiles (fault code %u)", fault);
+    }
+    return SELSCAN_OK;
 }
 
 extern "C" void selscan_release_workspace(void)

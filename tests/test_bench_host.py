@@ -1,0 +1,102 @@
+"""Host-side logic of bench.py on the CPU: algorithmic work counts, roofline
+arithmetic, the JSON line, the reference (oracle) arm, and the max-over-ranks
+reduction with two gloo ranks."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_work_counts_mamba130m():
+    w = bench.work_counts(2, 2048, 1536, 16, 4)
+    assert w["elems"] == 6_291_456
+    assert w["bytes"] == 76_120_064          # x, delta, y + B, C + A
+    assert w["mufu"] == 6_291_456 * 16 + 2 * 6_291_456
+    assert w["fp32"] == 4 * 6_291_456 * 16
+
+
+def test_work_counts_bf16_and_state():
+    w = bench.work_counts(8, 2048, 2048, 16, 2)
+    assert w["bytes"] == 202_506_240
+    w4 = bench.work_counts(1, 131072, 1536, 16, 4, hT=True)
+    assert w4["bytes"] == 2_432_892_928          # includes the final state hT
+
+
+def test_roofline_arithmetic():
+    pk = bench.peaks(148, 2032.0, 6484.3)
+    assert pk["mufu_per_s"] == pytest.approx(148 * 32 * 2.032e9)
+    w = bench.work_counts(2, 2048, 1536, 16, 4)
+    t_mufu = w["mufu"] / pk["mufu_per_s"]
+    r = bench.roofline(w, pk, seconds=2 * t_mufu)
+    assert r["bound"] == "alu"
+    assert r["frac"] == pytest.approx(0.5)
+    assert r["achieved"] == pytest.approx(w["updates"] / (2 * t_mufu) / 1e12)
+    assert r["frac_summed_bound"] > r["frac"]
+    assert r["peak"] * r["frac"] == pytest.approx(r["achieved"])
+
+
+def test_result_line_has_contract_keys():
+    line = bench.result_line(value=1.0, n_gpus=1, steps=3, warmup=3, ms_per_step=1.0,
+                             config={"workload": "w"}, roof={}, cpu={}, e2e={}, launches=3,
+                             clocks={}, dtype="f32")
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert k in line
+    json.dumps(line)
+
+
+def test_reference_arm_runs_on_cpu():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "1", "--steps", "3", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        v = bench.max_over_ranks(float(rank + 1) * 1.5, world)
+        bench.barrier(world)
+        q.put((rank, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 3.0), (1, 3.0)]
+
+
+def test_single_process_is_identity():
+    assert bench.max_over_ranks(2.5, 1) == 2.5

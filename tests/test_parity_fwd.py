@@ -236,3 +236,31 @@ def test_invalid_arguments_raise():
         ss.selscan_fwd(x, x.clone(), A, B, B.clone(), y=B.view(1, 8, 4))   # y overlaps B
     assert e.value.code == ss.ERR_INVALID_ARG
     ss.check_device_error()
+
+
+@pytest.mark.parametrize("shape", [(2, 300, 256, 16), (1, 129, 96, 8), (3, 70, 64, 32), (1, 50, 128, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_plain_load_path(orc, env, shape, dtype):
+    """The kernels that read global memory directly (used when TMA's
+    alignment rules do not hold) give the same results as the TMA path."""
+    env(SELSCAN_NO_TMA=1, SELSCAN_CHUNK=64)
+    Bsz, L, D, N = shape
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=L + D, dtype=dtype, with_h0=True)
+    check(orc, inp)
+
+
+def test_device_fault_word_clear_after_normal_runs():
+    inp = W.fwd_inputs(1, 256, 128, 16, seed=1)
+    x, dl, A, B, C, _ = fwd_dev(inp)
+    ss.selscan_fwd(x, dl, A, B, C, True)
+    ss.check_device_error()
+
+
+def test_plan_query_matches_launches():
+    p1 = ss.fwd_plan(1, 64, 16, 4)
+    assert p1 == {"chunks": 1, "chunk_len": 64, "launches": 1}
+    p2 = ss.fwd_plan(2, 2048, 1536, 16)
+    assert p2["chunks"] > 1 and p2["launches"] == 3
+    assert p2["chunks"] * p2["chunk_len"] >= 2048 > (p2["chunks"] - 1) * p2["chunk_len"]
+    assert ss.fwd_plan(0, 10, 5, 4)["launches"] == 0
