@@ -307,7 +307,14 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
 }
 
-int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cudaStream_t st)
+size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
+{
+    return plan.K > 1 ? (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float) : 0;
+}
+
+// Enqueues the kernels of one forward call. `ws` holds the chunk-carry
+// workspace (fwd_workspace_bytes of it; unused when the plan has one chunk).
+int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, float *ws, cudaStream_t st)
 {
     ScanKernels ks{};
     TmaKernels tk{};
@@ -341,19 +348,9 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cu
                   encode_3d(&ta.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt);
     }
 
-    void *ws = nullptr;
-    cudaMemPool_t pool = nullptr;
     if (plan.K > 1) {
         const int64_t bd = a.Bsz * a.D;
-        const size_t bytes = (size_t)(plan.K - 1) * (size_t)bd * (size_t)(a.N + 1) * sizeof(float);
-        int rc = workspace_pool(dev, &pool);
-        if (rc != SELSCAN_OK) return rc;
-        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return fail(SELSCAN_ERR_NO_MEMORY, "chunk workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
-        }
-        a.agg_h = static_cast<float *>(ws);
+        a.agg_h = ws;
         a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
         if (use_tma) {
             ta.s = a;
@@ -372,21 +369,37 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cu
         ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
     }
     cudaError_t e = cudaGetLastError();
-    if (ws) cudaFreeAsync(ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return SELSCAN_OK;
 }
 
-} // namespace
-} // namespace selscan
-
-using namespace selscan;
-
-extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
-                           const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
-                           int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
+// One forward call with its workspace from the library's stream-ordered pool.
+int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cudaStream_t st)
 {
-    g_err[0] = '\0';
+    const size_t bytes = fwd_workspace_bytes(plan, base.Bsz, base.D, base.N);
+    void *ws = nullptr;
+    if (bytes > 0) {
+        cudaMemPool_t pool = nullptr;
+        int rc = workspace_pool(dev, &pool);
+        if (rc != SELSCAN_OK) return rc;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SELSCAN_ERR_NO_MEMORY, "chunk workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+        }
+    }
+    int rc = launch_fwd_into(base, plan, dtype, static_cast<float *>(ws), st);
+    if (ws) cudaFreeAsync(ws, st);
+    return rc;
+}
+
+// Argument checks shared by the forward entry points (no CUDA call).
+// *empty is set when there is nothing to compute (Bsz == 0 or D == 0).
+int check_fwd_args(const void *x, const void *delta, const float *A, const void *B, const void *C,
+                   const void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, const float *h0,
+                   const float *hT, bool *empty)
+{
+    *empty = false;
     if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
         return fail(SELSCAN_ERR_INVALID_ARG, "dtype %d is neither SELSCAN_F32 nor SELSCAN_BF16", dtype);
     if (Bsz < 0 || L < 0 || D < 0)
@@ -400,8 +413,10 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     if (!mul_ok(Bsz, L, D, &nld) || !mul_ok(Bsz, L, N, &nln) || !mul_ok(Bsz, D, N, &ndn))
         return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow (Bsz=%lld L=%lld D=%lld N=%lld)",
                     (long long)Bsz, (long long)L, (long long)D, (long long)N);
-    if (Bsz == 0 || D == 0)
+    if (Bsz == 0 || D == 0) {
+        *empty = true;
         return SELSCAN_OK;
+    }
     if (!A)
         return fail(SELSCAN_ERR_INVALID_ARG, "A is NULL");
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
@@ -433,18 +448,38 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     }
     if (overlaps(ry, rhT))
         return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps hT");
+    return SELSCAN_OK;
+}
 
+// L == 0: the final state is the initial state (or zeros); nothing else is written.
+int empty_sequence_state(const float *h0, float *hT, int64_t Bsz, int64_t D, int64_t N, cudaStream_t st)
+{
+    if (!hT || hT == h0) return SELSCAN_OK;
+    const size_t bytes = (size_t)(Bsz * D * N) * 4;
+    cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(hT, 0, bytes, st);
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state copy");
+}
+
+} // namespace
+} // namespace selscan
+
+using namespace selscan;
+
+extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
+                           const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                           int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
+{
+    g_err[0] = '\0';
+    bool empty = false;
+    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty);
+    if (rc != SELSCAN_OK || empty) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (L == 0) {
-        if (!hT || hT == h0) return SELSCAN_OK;
-        cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, (size_t)ndn * 4, cudaMemcpyDeviceToDevice, st)
-                           : cudaMemsetAsync(hT, 0, (size_t)ndn * 4, st);
-        return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state copy");
-    }
+    if (L == 0) return empty_sequence_state(h0, hT, Bsz, D, N, st);
 
     int dev = 0, sms = 0;
-    int rc = device_info(&dev, &sms);
+    rc = device_info(&dev, &sms);
     if (rc != SELSCAN_OK) return rc;
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     FwdPlan plan;
     plan_fwd(Bsz, L, D, N, es, x, delta, B, C, sms, &plan);
     ScanArgs a;
