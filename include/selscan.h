@@ -122,6 +122,44 @@ int selscan_step(float *state, const float *x, const float *delta, const float *
                  int64_t N, void *stream);
 
 /*
+ * selscan_fwd_noalloc -- selscan_fwd for callers that cannot allocate device
+ * memory. The pages describe no counterpart: this is a deployment variant of
+ * selscan_fwd, not part of the method.
+ *
+ * Who needs it: code that runs where another allocator owns every byte of
+ * device memory (a framework's caching allocator, or a server that reserves
+ * the whole GPU at start-up, so cudaMalloc would fail or fragment its pool);
+ * code on a latency budget that cannot afford cudaMalloc/cudaFree, which can
+ * synchronise the device and take milliseconds; and plugins whose host
+ * program forbids them to allocate. selscan_fwd takes a small workspace from
+ * a pool for long sequences; this entry point takes it from a fixed array
+ * compiled into the library instead, and makes no allocation of any kind.
+ *
+ * Arguments, results, alias rules and error codes are those of selscan_fwd,
+ * and it splits the work the same way. The scratch array holds
+ * SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB); every GPU that loads the library
+ * holds it until the process exits. A call whose plan needs more scratch,
+ * (chunks - 1) * Bsz * D * (N + 1) * 4 bytes with chunks from
+ * selscan_fwd_plan, returns SELSCAN_ERR_UNSUPPORTED before anything is
+ * launched; run such a problem through selscan_fwd, or in pieces along L,
+ * handing hT of one piece to h0 of the next.
+ *
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture. Every call on a device shares
+ * the one array, and it keeps whatever the last call left in it: calls that
+ * can overlap on the GPU (on streams not ordered with each other) race on it
+ * and produce wrong results, so order them on one stream or synchronise
+ * between them. Nothing in the array has to start at zero: each call writes
+ * every scratch element before it reads it.
+ */
+#define SELSCAN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+int selscan_fwd_noalloc(const void *x, const void *delta, const float *A, const void *B,
+                        const void *C, void *y, int64_t Bsz, int64_t L, int64_t D,
+                        int64_t N, int dtype, int delta_softplus, const float *h0,
+                        float *hT, void *stream);
+
+/*
  * selscan_fwd_plan -- how selscan_fwd would run a problem of this size on
  * the current device, without running it (for tests and benchmarks).
  *   chunks    : number of chunks the sequence is cut into (1 = one pass)

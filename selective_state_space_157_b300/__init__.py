@@ -19,7 +19,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["selscan_fwd", "selscan_step", "fwd_plan", "last_error", "check_device_error",
+__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
            "MAX_N"]
@@ -27,6 +27,7 @@ __all__ = ["selscan_fwd", "selscan_step", "fwd_plan", "last_error", "check_devic
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 F32, BF16 = 0, 1
 MAX_N = 64
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libselscan.so")
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_release_workspace.argtypes = []
         L.selscan_version.restype = ctypes.c_char_p
         L.selscan_version.argtypes = []
+        L.selscan_fwd_noalloc.restype = INT
+        L.selscan_fwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P]
         _lib = L
@@ -171,6 +174,33 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
                                _stream_ptr(stream))
     _check(rc)
     return (y, hT) if (return_final_state or hT is not None) else y
+
+
+def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=None, hT=None,
+                        stream=None):
+    """selscan_fwd without any allocation, for callers that cannot allocate
+    device memory (another allocator owns it, or allocation latency is not
+    allowed); see ``include/selscan.h``. Device tensors only, with the outputs
+    ``y`` (and ``hT`` if wanted) supplied by the caller. Calls that may overlap
+    on the GPU share one scratch array and must be ordered."""
+    import torch
+    dev = x.device
+    Bsz, L, D = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    code = _dtype_code(x)
+    for t, name, shape, dt in ((x, "x", (Bsz, L, D), x.dtype), (delta, "delta", (Bsz, L, D), x.dtype),
+                               (A, "A", (D, N), torch.float32), (B, "B", (Bsz, L, N), x.dtype),
+                               (C, "C", (Bsz, L, N), x.dtype), (y, "y", (Bsz, L, D), x.dtype)):
+        _need(t, name, shape, dt, dev)
+    for t, name in ((h0, "h0"), (hT, "hT")):
+        if t is not None:
+            _need(t, name, (Bsz, D, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_fwd_noalloc(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
+                                       Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
+                                       _stream_ptr(stream))
+    _check(rc)
+    return y
 
 
 def selscan_step(state, x, delta, A, B, C, y=None, stream=None):

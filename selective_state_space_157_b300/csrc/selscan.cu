@@ -490,6 +490,69 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     return launch_fwd(a, plan, dtype, dev, st);
 }
 
+// ---- allocation-free forward ----------------------------------------------
+// Chunk-carry scratch for callers that cannot allocate: a fixed array in the
+// library's device image. Host code must not use the name as an address (on
+// the host it is only a stand-in); its device address is looked up once per
+// device with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SELSCAN_NOALLOC_SCRATCH_BYTES];
+
+namespace selscan {
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+int noalloc_scratch(int dev, float **out)
+{
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the scratch array");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = static_cast<float *>(g_noalloc_ptr[dev]);
+    return SELSCAN_OK;
+}
+} // namespace
+} // namespace selscan
+
+extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float *A, const void *B,
+                                   const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                                   int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
+{
+    g_err[0] = '\0';
+    bool empty = false;
+    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty);
+    if (rc != SELSCAN_OK || empty) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (L == 0) return empty_sequence_state(h0, hT, Bsz, D, N, st);
+
+    int dev = 0, sms = 0;
+    rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    FwdPlan plan;
+    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, sms, &plan);
+    const size_t need = fwd_workspace_bytes(plan, Bsz, D, N);
+    if (need > SELSCAN_NOALLOC_SCRATCH_BYTES)
+        return fail(SELSCAN_ERR_UNSUPPORTED,
+                    "this problem needs %zu bytes of chunk scratch (%d chunks) but the allocation-free entry "
+                    "point has %u; use selscan_fwd or split the sequence",
+                    need, plan.K, (unsigned)SELSCAN_NOALLOC_SCRATCH_BYTES);
+    float *ws = nullptr;
+    if (need > 0) {
+        rc = noalloc_scratch(dev, &ws);
+        if (rc != SELSCAN_OK) return rc;
+    }
+    ScanArgs a;
+    memset(&a, 0, sizeof a);
+    a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
+    a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
+    a.softplus = delta_softplus ? 1 : 0;
+    return launch_fwd_into(a, plan, dtype, ws, st);
+}
+
 extern "C" int selscan_step(float *state, const float *x, const float *delta, const float *A,
                             const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
                             int64_t N, void *stream)
