@@ -138,11 +138,11 @@ int selscan_step(float *state, const float *x, const float *delta, const float *
  * Arguments, results, alias rules and error codes are those of selscan_fwd,
  * and it splits the work the same way. The scratch array holds
  * SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB); every GPU that loads the library
- * holds it until the process exits. A call whose plan needs more scratch,
- * (chunks - 1) * Bsz * D * (N + 1) * 4 bytes with chunks from
- * selscan_fwd_plan, returns SELSCAN_ERR_UNSUPPORTED before anything is
- * launched; run such a problem through selscan_fwd, or in pieces along L,
- * handing hT of one piece to h0 of the next.
+ * holds it until the process exits. A call whose plan needs more scratch
+ * (the workspace_bytes that selscan_fwd_plan reports; about
+ * 8 * (chunks - 1) * Bsz * D * N bytes) returns SELSCAN_ERR_UNSUPPORTED
+ * before anything is launched; run such a problem through selscan_fwd, or in
+ * pieces along L, handing hT of one piece to h0 of the next.
  *
  * The first call on each device looks up the array's device address; make
  * that first call before any stream capture. Every call on a device shares
@@ -162,16 +162,19 @@ int selscan_fwd_noalloc(const void *x, const void *delta, const float *A, const 
 /*
  * selscan_fwd_plan -- how selscan_fwd would run a problem of this size on
  * the current device, without running it (for tests and benchmarks).
- *   chunks    : number of chunks the sequence is cut into (1 = one pass)
- *   chunk_len : timesteps per chunk
- *   launches  : kernels one selscan_fwd call enqueues (1, or 3 when chunked)
- * Any output pointer may be NULL. Same size checks as selscan_fwd; needs a
+ *   chunks          : number of chunks the sequence is cut into (1 = one pass)
+ *   chunk_len       : timesteps per chunk
+ *   launches        : kernels one selscan_fwd call enqueues
+ *   workspace_bytes : chunk-carry workspace the call uses (0 for one chunk)
+ * Any output pointer may be NULL. The figures assume 16-byte aligned
+ * tensors (alignment decides between the TMA-staged and the plain kernels). Same size checks as selscan_fwd; needs a
  * CUDA device (it reads the SM count). The plan depends only on the sizes,
  * dtype and device, plus the tuning variables SELSCAN_CHUNK and
  * SELSCAN_TARGET_WARPS when set.
  */
 int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype,
-                     int *chunks, int64_t *chunk_len, int *launches);
+                     int *chunks, int64_t *chunk_len, int *launches,
+                     int64_t *workspace_bytes);
 
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on

@@ -69,7 +69,7 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_noalloc.restype = INT
         L.selscan_fwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
-        L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P]
+        L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
         _lib = L
     return _lib
 
@@ -84,13 +84,14 @@ def version() -> str:
 
 def fwd_plan(Bsz: int, L: int, D: int, N: int, bf16: bool = False) -> dict:
     """How selscan_fwd would split this problem on the current device:
-    {"chunks", "chunk_len", "launches"}."""
+    {"chunks", "chunk_len", "launches", "workspace_bytes"} (16-byte aligned tensors)."""
     k = ctypes.c_int(0)
     t = ctypes.c_int64(0)
     n = ctypes.c_int(0)
+    w = ctypes.c_int64(0)
     _check(lib().selscan_fwd_plan(Bsz, L, D, N, BF16 if bf16 else F32, ctypes.byref(k),
-                                  ctypes.byref(t), ctypes.byref(n)))
-    return {"chunks": k.value, "chunk_len": t.value, "launches": n.value}
+                                  ctypes.byref(t), ctypes.byref(n), ctypes.byref(w)))
+    return {"chunks": k.value, "chunk_len": t.value, "launches": n.value, "workspace_bytes": w.value}
 
 
 def release_workspace() -> None:

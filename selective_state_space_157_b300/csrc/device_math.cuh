@@ -28,18 +28,18 @@ __device__ __forceinline__ float ex2(float v)
 // log1p(e) = e * P(e) with P a degree-8 fit of log1p(e)/e on [0, 1]
 // (derived by csrc/fit_log1p_poly.py; relative error <= 2e-7 in fp32). It
 // runs on the FMA pipe: one MUFU op (the exponential) per softplus.
+// Coefficients c0..c8 of P, lowest degree first.
+__device__ constexpr float kLog1pPoly[9] = {9.999999404e-01f, -4.999949336e-01f, 3.331909776e-01f,
+                                            -2.484298497e-01f, 1.910601407e-01f, -1.366325915e-01f,
+                                            7.822608948e-02f, -2.950531431e-02f, 5.232710857e-03f};
+
 __device__ __forceinline__ float softplus(float u)
 {
     const float e = ex2(-fabsf(u) * kLog2e);
-    float p = 5.232710857e-03f;
-    p = fmaf(p, e, -2.950531431e-02f);
-    p = fmaf(p, e, 7.822608948e-02f);
-    p = fmaf(p, e, -1.366325915e-01f);
-    p = fmaf(p, e, 1.910601407e-01f);
-    p = fmaf(p, e, -2.484298497e-01f);
-    p = fmaf(p, e, 3.331909776e-01f);
-    p = fmaf(p, e, -4.999949336e-01f);
-    p = fmaf(p, e, 9.999999404e-01f);
+    float p = kLog1pPoly[8];
+#pragma unroll
+    for (int c = 7; c >= 0; --c)
+        p = fmaf(p, e, kLog1pPoly[c]);
     return fmaf(p, e, fmaxf(u, 0.0f));
 }
 

@@ -17,6 +17,7 @@
 
 #include "scan_fwd.cuh"
 #include "scan_step.cuh"
+#include "scan_fused.cuh"
 #include "scan_tma.cuh"
 
 namespace selscan {
@@ -195,62 +196,74 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, size_t es, const void *ba
     return r == CUDA_SUCCESS;
 }
 
-using TmaKernel = void (*)(TmaScanArgs);
+using FusedKernel = void (*)(FusedArgs);
 
-struct TmaKernels {
-    TmaKernel readout, aggregate;
-    size_t smem_readout, smem_aggregate;
+struct FusedLaunch {
+    FusedKernel kernel;
+    size_t smem;
+    int ctas_per_sm;
     int tt, stages;
 };
 
-template <typename T, int NS, int NSPLIT, bool VEC, int TT>
-bool prepare_tma_tt(int64_t N, int stages, TmaKernels *out)
+// Resident CTAs per SM for a kernel at a shared-memory size (cached).
+int occupancy(const void *fn, size_t smem)
 {
-    constexpr int DPB = kScanThreads / NSPLIT;
-    auto kr = scan_tma_kernel<T, NS, NSPLIT, true, VEC, TT>;
-    auto ka = scan_tma_kernel<T, NS, NSPLIT, false, VEC, TT>;
-    const size_t sr = tma_smem_bytes(sizeof(T), TT, DPB, N, true, stages);
-    const size_t sa = tma_smem_bytes(sizeof(T), TT, DPB, N, false, stages);
-    // The shared-memory ceiling is per kernel; raise it to what this N needs.
-    if (cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sr) != cudaSuccess ||
-        cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa) != cudaSuccess) {
+    struct Entry { const void *fn; size_t smem; int n; };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].smem == smem) return cache[i].n;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kScanThreads, smem) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        n = 1;
     }
-    *out = TmaKernels{kr, ka, sr, sa, TT, stages};
-    return true;
+    if (n < 1) n = 1;
+    if (used < 64) cache[used++] = Entry{fn, smem, n};
+    return n;
 }
 
-// Timesteps per stage and buffers in flight: 16 x 4 unless SELSCAN_TMA_TT /
-// SELSCAN_TMA_STAGES ask otherwise (tuning knobs; TT is 8 or 16).
-template <typename T, int NS, int NSPLIT, bool VEC>
-bool prepare_tma(int64_t N, TmaKernels *out)
+template <typename T, int NS, int NSPLIT, bool VEC, bool SP>
+bool prepare_fused_sp(int64_t N, FusedLaunch *out)
 {
+    constexpr int DPB = kScanThreads / NSPLIT;
     long stages = env_long("SELSCAN_TMA_STAGES", kStages);
     if (stages < 2) stages = 2;
     if (stages > kMaxStages) stages = kMaxStages;
-    if (env_long("SELSCAN_TMA_TT", kTT) == 8)
-        return prepare_tma_tt<T, NS, NSPLIT, VEC, 8>(N, (int)stages, out);
-    return prepare_tma_tt<T, NS, NSPLIT, VEC, kTT>(N, (int)stages, out);
+    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP>;
+    const int64_t nrow = VEC ? NS * NSPLIT : N;
+    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, (int)stages);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    *out = FusedLaunch{k, smem, occupancy(reinterpret_cast<const void *>(k), smem), kTT, (int)stages};
+    return true;
 }
 
 template <typename T, int NS, int NSPLIT>
-bool prepare_tma_vec(bool vec, int64_t N, TmaKernels *out)
+bool prepare_fused(bool vec, bool softplus, int64_t N, FusedLaunch *out)
 {
-    return vec ? prepare_tma<T, NS, NSPLIT, true>(N, out) : prepare_tma<T, NS, NSPLIT, false>(N, out);
+    if (vec)
+        return softplus ? prepare_fused_sp<T, NS, NSPLIT, true, true>(N, out)
+                        : prepare_fused_sp<T, NS, NSPLIT, true, false>(N, out);
+    return softplus ? prepare_fused_sp<T, NS, NSPLIT, false, true>(N, out)
+                    : prepare_fused_sp<T, NS, NSPLIT, false, false>(N, out);
 }
 
 template <typename T>
-bool pick_tma(int ns, int nsplit, bool vec, int64_t N, TmaKernels *out)
+bool pick_fused(int ns, int nsplit, bool vec, bool softplus, int64_t N, FusedLaunch *out)
 {
     switch (ns * 100 + nsplit) {
-    case 401: return prepare_tma_vec<T, 4, 1>(vec, N, out);
-    case 801: return prepare_tma_vec<T, 8, 1>(vec, N, out);
-    case 1601: return prepare_tma_vec<T, 16, 1>(vec, N, out);
-    case 1602: return prepare_tma_vec<T, 16, 2>(vec, N, out);
-    case 1604: return prepare_tma_vec<T, 16, 4>(vec, N, out);
-    case 802: return prepare_tma_vec<T, 8, 2>(vec, N, out);
-    case 404: return prepare_tma_vec<T, 4, 4>(vec, N, out);
+    case 401: return prepare_fused<T, 4, 1>(vec, softplus, N, out);
+    case 801: return prepare_fused<T, 8, 1>(vec, softplus, N, out);
+    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, N, out);
+    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, N, out);
+    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, N, out);
+    case 802: return prepare_fused<T, 8, 2>(vec, softplus, N, out);
+    case 404: return prepare_fused<T, 4, 4>(vec, softplus, N, out);
     default: return false;
     }
 }
@@ -287,11 +300,16 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->tma = bases16 && env_long("SELSCAN_NO_TMA", 0) == 0 && (D * (int64_t)es) % 16 == 0 && (N * (int64_t)es) % 16 == 0 &&
              L <= 0x7fffffffLL && D <= 0x7fffffffLL && Bsz <= 0x7fffffffLL;
 
-    // Chunking: enough chains in flight to keep every SM busy; each chunk
-    // beyond the first costs one extra reduction pass over its timesteps.
+    // Chunking. Each chunk beyond the first costs an extra reduction pass over
+    // its timesteps, and a readout must wait for the reductions of the chunks
+    // before it, so chunking pays only when the chains alone leave the GPU
+    // mostly idle. Measured on B300: with >= 3 warps of chains per SM one pass
+    // is fastest (Bsz=8, D=2048); below that, about 12 warps per SM in
+    // flight is best (Bsz=2, D=1536: ~18 chunks; Bsz=1, L=131072: ~40).
     const int64_t warps1 = Bsz * (int64_t)p->dtiles * (kScanThreads / 32);
-    const long target = env_long("SELSCAN_TARGET_WARPS", 8) * (long)sms;
-    int64_t K = (warps1 <= 0 || warps1 >= target) ? 1 : (target + warps1 - 1) / warps1;
+    const long target = env_long("SELSCAN_TARGET_WARPS", 12) * (long)sms;
+    const bool enough = warps1 >= 3 * (int64_t)sms && env_long("SELSCAN_TARGET_WARPS", 0) == 0;
+    int64_t K = (warps1 <= 0 || enough || warps1 >= target) ? 1 : (target + warps1 - 1) / warps1;
     const int64_t min_chunk = 64;
     int64_t maxK = (L + min_chunk - 1) / min_chunk;
     if (K > maxK) K = maxK;
@@ -307,74 +325,104 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
 }
 
+// Chunk-carry workspace of a plan: per chunk boundary and chain the pair
+// (decay, end state) of N floats each, then the ticket counter and one done
+// flag per aggregate item. The plain-load path uses a smaller part of it.
 size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
 {
-    return plan.K > 1 ? (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float) : 0;
+    if (plan.K <= 1) return 0;
+    const size_t pairs = 2 * (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)N * sizeof(float);
+    const size_t flags = (1 + (size_t)(plan.K - 1) * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
+    return pairs + flags;
 }
 
-// Enqueues the kernels of one forward call. `ws` holds the chunk-carry
-// workspace (fwd_workspace_bytes of it; unused when the plan has one chunk).
-int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, float *ws, cudaStream_t st)
+int launch_plain(const ScanArgs &base, const FwdPlan &plan, int dtype, float *ws, cudaStream_t st)
 {
     ScanKernels ks{};
-    TmaKernels tk{};
-    bool use_tma = plan.tma;
-    if (use_tma)
-        use_tma = dtype == SELSCAN_F32 ? pick_tma<float>(plan.ns, plan.nsplit, plan.vec, base.N, &tk)
-                                       : pick_tma<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, base.N, &tk);
     bool ok = dtype == SELSCAN_F32 ? pick_shape<float>(plan.ns, plan.nsplit, plan.vec, &ks)
                                    : pick_shape<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, &ks);
     if (!ok) return fail(SELSCAN_ERR_UNSUPPORTED, "no kernel for NS=%d NSPLIT=%d", plan.ns, plan.nsplit);
-
     ScanArgs a = base;
-    a.chunk = plan.chunk;
-    a.K = plan.K;
-    a.dtiles = plan.dtiles;
     const int64_t gx = a.Bsz * plan.dtiles;
-    if (gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-
-    TmaScanArgs ta;
-    if (use_tma) {
-        memset(&ta, 0, sizeof ta);
-        const CUtensorMapDataType dt =
-            dtype == SELSCAN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
-        const uint32_t dpb = (uint32_t)(kScanThreads / plan.nsplit);
-        const uint32_t tt = (uint32_t)tk.tt;
-        ta.stages = tk.stages;
-        use_tma = encode_3d(&ta.mx, dt, es, a.x, a.D, a.L, a.Bsz, dpb, tt) &&
-                  encode_3d(&ta.md, dt, es, a.delta, a.D, a.L, a.Bsz, dpb, tt) &&
-                  encode_3d(&ta.mB, dt, es, a.B, a.N, a.L, a.Bsz, (uint32_t)a.N, tt) &&
-                  encode_3d(&ta.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt);
-    }
-
     if (plan.K > 1) {
         const int64_t bd = a.Bsz * a.D;
         a.agg_h = ws;
         a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
-        if (use_tma) {
-            ta.s = a;
-            tk.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, tk.smem_aggregate, st>>>(ta);
-        } else {
-            ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
-        }
+        ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
         CarryArgs c{a.A, a.h0, a.agg_h, a.agg_s, a.Bsz, a.D, a.N, plan.K};
         const int64_t total = a.Bsz * a.D * a.N;
         scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(c);
     }
-    if (use_tma) {
-        ta.s = a;
-        tk.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, tk.smem_readout, st>>>(ta);
-    } else {
-        ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
-    }
+    ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-    return SELSCAN_OK;
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+}
+
+// TMA path: one persistent kernel (aggregates, carries and readout together).
+// Returns SELSCAN_ERR_UNSUPPORTED when TMA cannot be set up (the caller then
+// takes the plain path); nothing has been enqueued in that case.
+int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, float *ws, cudaStream_t st)
+{
+    FusedLaunch fl;
+    const bool sp = a.softplus != 0;
+    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, a.N, &fl)
+                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, a.N, &fl);
+    if (!ok) return SELSCAN_ERR_UNSUPPORTED;
+    FusedArgs fa;
+    memset(&fa, 0, sizeof fa);
+    const CUtensorMapDataType dt = dtype == SELSCAN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    const uint32_t dpb = (uint32_t)(kScanThreads / plan.nsplit);
+    const uint32_t tt = (uint32_t)fl.tt;
+    if (!(encode_3d(&fa.mx, dt, es, a.x, a.D, a.L, a.Bsz, dpb, tt) &&
+          encode_3d(&fa.md, dt, es, a.delta, a.D, a.L, a.Bsz, dpb, tt) &&
+          encode_3d(&fa.mB, dt, es, a.B, a.N, a.L, a.Bsz, (uint32_t)a.N, tt) &&
+          encode_3d(&fa.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt)))
+        return SELSCAN_ERR_UNSUPPORTED;
+    fa.s = a;
+    fa.stages = fl.stages;
+    const int64_t groups = a.Bsz * plan.dtiles;
+    const int64_t items_agg = (int64_t)(plan.K - 1) * groups;
+    const int64_t items_total = items_agg + (int64_t)plan.K * groups;
+    if (items_total > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "too many work items");
+    fa.groups = (int)groups;
+    fa.items_agg = (int)items_agg;
+    fa.items_total = (int)items_total;
+    int64_t grid = items_total;
+    if (plan.K > 1) {
+        const size_t bdn = (size_t)(a.Bsz * a.D * a.N);
+        fa.aggP = ws;
+        fa.aggH = ws + (size_t)(plan.K - 1) * bdn;
+        fa.ctrl = reinterpret_cast<unsigned *>(ws + 2 * (size_t)(plan.K - 1) * bdn);
+        cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, (size_t)(1 + items_agg) * sizeof(unsigned), st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk flags");
+        const int64_t resident = (int64_t)sms * fl.ctas_per_sm;
+        if (grid > resident) grid = resident;
+    }
+    fl.kernel<<<(unsigned)grid, kScanThreads, fl.smem, st>>>(fa);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+}
+
+// Enqueues the kernels of one forward call. `ws` holds the chunk-carry
+// workspace (fwd_workspace_bytes of it; unused when the plan has one chunk).
+int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int sms, float *ws, cudaStream_t st)
+{
+    ScanArgs a = base;
+    a.chunk = plan.chunk;
+    a.K = plan.K;
+    a.dtiles = plan.dtiles;
+    if (a.Bsz * plan.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+    if (plan.tma) {
+        int rc = launch_fused(a, plan, dtype, sms, ws, st);
+        if (rc != SELSCAN_ERR_UNSUPPORTED) return rc;
+        g_err[0] = '\0';
+    }
+    return launch_plain(a, plan, dtype, ws, st);
 }
 
 // One forward call with its workspace from the library's stream-ordered pool.
-int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cudaStream_t st)
+int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, int sms, cudaStream_t st)
 {
     const size_t bytes = fwd_workspace_bytes(plan, base.Bsz, base.D, base.N);
     void *ws = nullptr;
@@ -388,7 +436,7 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, cu
             return fail(SELSCAN_ERR_NO_MEMORY, "chunk workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
         }
     }
-    int rc = launch_fwd_into(base, plan, dtype, static_cast<float *>(ws), st);
+    int rc = launch_fwd_into(base, plan, dtype, sms, static_cast<float *>(ws), st);
     if (ws) cudaFreeAsync(ws, st);
     return rc;
 }
@@ -487,7 +535,7 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.softplus = delta_softplus ? 1 : 0;
-    return launch_fwd(a, plan, dtype, dev, st);
+    return launch_fwd(a, plan, dtype, dev, sms, st);
 }
 
 // ---- allocation-free forward ----------------------------------------------
@@ -550,7 +598,7 @@ extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.softplus = delta_softplus ? 1 : 0;
-    return launch_fwd_into(a, plan, dtype, ws, st);
+    return launch_fwd_into(a, plan, dtype, sms, ws, st);
 }
 
 extern "C" int selscan_step(float *state, const float *x, const float *delta, const float *A,
@@ -613,7 +661,7 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
 }
 
 extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, int *chunks,
-                                int64_t *chunk_len, int *launches)
+                                int64_t *chunk_len, int *launches, int64_t *workspace_bytes)
 {
     g_err[0] = '\0';
     if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
@@ -633,7 +681,10 @@ extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, in
     const bool empty = Bsz == 0 || D == 0 || L == 0;
     if (chunks) *chunks = empty ? 0 : plan.K;
     if (chunk_len) *chunk_len = empty ? 0 : plan.chunk;
-    if (launches) *launches = empty ? 0 : (plan.K > 1 ? 3 : 1);
+    // The TMA path runs as one kernel (plus a flag reset when chunked); the
+    // plain path as aggregate + carry + readout kernels.
+    if (launches) *launches = empty ? 0 : (plan.tma ? 1 : (plan.K > 1 ? 3 : 1));
+    if (workspace_bytes) *workspace_bytes = empty ? 0 : (int64_t)fwd_workspace_bytes(plan, Bsz, D, N);
     return SELSCAN_OK;
 }
 

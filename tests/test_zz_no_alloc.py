@@ -50,8 +50,7 @@ def test_refuses_a_problem_beyond_the_scratch(monkeypatch):
     monkeypatch.setenv("SELSCAN_CHUNK", "16")        # many chunks: a large carry workspace
     Bsz, L, D, N = 1, 16384, 128, 16
     plan = ss.fwd_plan(Bsz, L, D, N)
-    need = (plan["chunks"] - 1) * Bsz * D * (N + 1) * 4
-    assert need > ss.NOALLOC_SCRATCH_BYTES
+    assert plan["workspace_bytes"] > ss.NOALLOC_SCRATCH_BYTES
     inp = W.fwd_inputs(Bsz, L, D, N, seed=2)
     x, dl, A, B, C, _ = fwd_dev(inp)
     y = torch.full_like(x, 7.0)
