@@ -64,6 +64,15 @@ def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False):
             "mufu": E * N + (2 * E if softplus else 0), "fp32": 4 * E * N}
 
 
+def step_work_counts(Bsz, D, N):
+    """Algorithmic work of one decode step: the state is read and written once
+    (2 * B*D*N fp32), x, delta and y move once (3 * B*D), B and C once per batch
+    row (2 * B*N), A once (D*N)."""
+    E = Bsz * D
+    nbytes = 2 * E * N * 4 + 3 * E * 4 + 2 * Bsz * N * 4 + D * N * 4
+    return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": E * N, "fp32": 4 * E * N}
+
+
 def peaks(sms: int, sm_mhz: float, hbm_gbs: float):
     return {"mufu_per_s": sms * MUFU_EX2_PER_CLK_SM * sm_mhz * 1e6,
             "fp32_per_s": sms * FP32_PER_CLK_SM * sm_mhz * 1e6,
@@ -133,8 +142,50 @@ def result_line(*, value, n_gpus, steps, warmup, ms_per_step, config, roof, cpu,
 
 # --------------------------------------------------------------- clocks
 
+class _Nvml:
+    """Minimal ctypes binding to the driver's NVML library (libnvidia-ml.so.1)."""
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def handle(self, cuda_index: int):
+        """NVML numbers GPUs on its own: find the CUDA device by PCI address."""
+        c = self.c
+        h = c.c_void_p()
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(c.c_char_p(bus), c.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(cuda_index), c.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def clock(self, h, maximum=False):
+        v = self.c.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        return v.value if fn(h, self.CLOCK_SM, self.c.byref(v)) == 0 else None
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong()
+        for name in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            fn = getattr(self.lib, name, None)
+            if fn is not None and fn(h, self.c.byref(v)) == 0:
+                return v.value
+        return 0
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons through NVML
+    every millisecond while running."""
 
     REASONS = {
         0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
@@ -142,43 +193,29 @@ class ClockSampler:
     }
 
     def __init__(self, index: int, period_s: float = 0.001):
-        self.index, self.period = index, period_s
+        self.period = period_s
         self.samples, self.reasons = [], set()
         self._stop = threading.Event()
         self._thread = None
         self.max_mhz = None
+        self.error = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = self._handle(pynvml, index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self._reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
-        except Exception:
+            self.nv = _Nvml()
+            self.h = self.nv.handle(index)
+            self.max_mhz = self.nv.clock(self.h, maximum=True)
+        except Exception as e:   # no NVML: the line says so
             self.nv = None
-
-    @staticmethod
-    def _handle(pynvml, index):
-        """NVML numbers GPUs on its own; find the CUDA device by PCI address."""
-        try:
-            import torch
-            p = torch.cuda.get_device_properties(index)
-            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
-            return pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-        except Exception:
-            return pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.error = str(e)
 
     def _run(self):
         while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self._reasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
-            except Exception:
-                pass
+            mhz = self.nv.clock(self.h)
+            if mhz is not None:
+                self.samples.append(mhz)
+            r = self.nv.reasons(self.h)
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    self.reasons.add(name)
             time.sleep(self.period)
 
     def __enter__(self):
@@ -195,9 +232,10 @@ class ClockSampler:
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                    "source": "unavailable"}
+                    "source": "unavailable" + (f" ({self.error})" if self.error else "")}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "NVML, 1 ms"}
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "NVML every 1 ms during the timed region"}
 
 
 # --------------------------------------------------------------- distributed
@@ -269,7 +307,7 @@ def run_gpu(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     w = W.WORKLOADS[args.workload]
     if w.steps:
-        raise SystemExit("bench.py times the forward workloads 1-4; the decode workload is a parity case")
+        return run_decode(args, world, rank, local, dev, w)
     inp = W.workload_inputs(args.workload)
     bf16 = w.dtype == W.BF16
     es = 2 if bf16 else 4
@@ -374,6 +412,96 @@ def run_gpu(args, world, rank, local):
                        dtype="bf16 io, f32 math" if bf16 else "f32")
 
 
+def run_decode(args, world, rank, local, dev, w):
+    """The decode workload: one step = one selscan_step over (Bsz, D, N).
+    Four independent decode streams (state and per-step inputs each) are
+    rotated so that every step reads its 42 MB state from HBM rather than L2,
+    as a server interleaving several sequences would."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+
+    streams = 4
+    A = torch.from_numpy(W.decode_A(w)).to(dev)
+    states = [torch.from_numpy(W.decode_state(w)).to(dev) for _ in range(streams)]
+    inputs = [[torch.from_numpy(a).to(dev) for a in W.decode_step_inputs(w, k)] for k in range(streams)]
+    ys = [torch.empty(w.Bsz, w.D, device=dev) for _ in range(streams)]
+
+    def step(i):
+        x, dl, B, C = inputs[i % streams]
+        ss.selscan_step(states[i % streams], x, dl, A, B, C, y=ys[i % streams])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ss.check_device_error()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, dev)
+    ss.check_device_error()
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    per_step = sec / args.steps
+    elems = w.Bsz * w.D
+    value = world * elems * args.steps / sec
+
+    # end to end: host inputs of the step in, y out, state kept on the device
+    hx = [torch.from_numpy(a).pin_memory() for a in W.decode_step_inputs(w, 0)]
+    hy = torch.empty(w.Bsz, w.D, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 50))
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x, dl, B, C = (t.to(dev, non_blocking=True) for t in hx)
+        ss.selscan_step(states[0], x, dl, A, B, C, y=ys[0])
+        hy.copy_(ys[0], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx),
+           "d2h_bytes_per_step": hy.numel() * hy.element_size()}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    hbm_gbs, max_mhz, src = read_measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pk = peaks(sms, max_mhz, hbm_gbs)
+    pk["source"] = f"HBM {src}"
+    roof = roofline(step_work_counts(w.Bsz, w.D, w.N), pk, per_step, traffic=profiled_traffic(args.workload),
+                    kernel="selscan_step (1 launch)")
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        chains = sample_chains(w.Bsz, w.D, 4096)
+        st = W.decode_state(w).reshape(-1, w.N)[chains].astype(np.float64)
+        Ah = W.decode_A(w)
+        steps_h = 32
+        hin = [W.decode_step_inputs(w, k) for k in range(steps_h)]
+        t0 = time.perf_counter()
+        for k in range(steps_h):
+            oracle.selscan_step(st, *hin[k][:2], Ah, *hin[k][2:], chains=chains)
+        secs = time.perf_counter() - t0
+        cpu = {"value": len(chains) * steps_h / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{len(chains)} of {w.Bsz * w.D} chains x {steps_h} steps ({secs:.2f} s, fp64, one thread)"}
+    config = {"workload": f"{w.name}: Bsz={w.Bsz} D={w.D} N={w.N} f32 decode step, state updated in place",
+              "global_batch": w.Bsz * world, "seq_len": 1, "parallelism": f"replicas x{world}",
+              "l2": f"{streams} rotating decode streams ({streams * w.Bsz * w.D * w.N * 4 / 1e6:.0f} MB of state) > L2"}
+    return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                       ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
+                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step is one oracle run over a
     bounded sample of the workload's chains, on the host cores."""
@@ -381,6 +509,8 @@ def run_reference(args, world, rank):
         return None
     from selective_state_space_157_b300 import workloads as W
     w = W.WORKLOADS[args.workload]
+    if w.steps:
+        return run_reference_decode(args, world, w)
     inp = W.workload_inputs(args.workload)
     Bsz, L, D = inp.x.shape
     chains = sample_chains(Bsz, D, args.ref_chains)
@@ -405,12 +535,44 @@ def run_reference(args, world, rank):
     }
 
 
+def run_reference_decode(args, world, w):
+    """Reference arm for the decode workload: each step is one oracle decode
+    step over a sample of the chains, on the host."""
+    import numpy as np
+    import oracle
+    from selective_state_space_157_b300 import workloads as W
+    chains = sample_chains(w.Bsz, w.D, args.ref_chains * 64)
+    st = W.decode_state(w).reshape(-1, w.N)[chains].astype(np.float64)
+    A = W.decode_A(w)
+    ins = [W.decode_step_inputs(w, k) for k in range(max(1, min(args.steps, 8)))]
+    for i in range(args.warmup):
+        x, dl, B, C = ins[i % len(ins)]
+        oracle.selscan_step(st, x, dl, A, B, C, chains=chains)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        x, dl, B, C = ins[i % len(ins)]
+        oracle.selscan_step(st, x, dl, A, B, C, chains=chains)
+    tot = time.perf_counter() - t0
+    value = len(chains) * args.steps / tot
+    sample = f"{len(chains)} of {w.Bsz * w.D} chains per step (fp64, one thread)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: Bsz={w.Bsz} D={w.D} N={w.N} f32 decode step", "seq_len": 1,
+                   "parallelism": "host"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")

@@ -129,9 +129,13 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     const int xbytes = TT * DPB * (int)sizeof(T);
     const int nbytes = TT * (int)Nrow * (int)sizeof(T);
     const int sbytes = 2 * xbytes + 2 * nbytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * sbytes);
+    constexpr bool kBf16 = sizeof(T) == 2;
+    const int cfloats = kBf16 ? 2 * TT * (int)Nrow : 0;   // fp32 copy of a stage's B and C rows
+    float *conv_buf = reinterpret_cast<float *>(smem + STAGES * sbytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * (sbytes + cfloats * 4));
     uint64_t *empty = full + STAGES;
-    unsigned *issued = reinterpret_cast<unsigned *>(empty + STAGES);
+    uint64_t *conv = empty + STAGES;   // bf16: every warp converted its share of the stage
+    unsigned *issued = reinterpret_cast<unsigned *>(conv + STAGES);
     volatile int *s_item = reinterpret_cast<volatile int *>(issued + STAGES);
     volatile int *s_abort = s_item + 1;
 
@@ -150,6 +154,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
+            mbar_init(&conv[s], kWarps);
             issued[s] = 0;
         }
         *s_abort = 0;
@@ -221,17 +226,26 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 h[j] = make_float2(0.0f, 0.0f);
         }
         if (readout && k > 0) {
-            if (threadIdx.x == 0) {
+            // Warp 0 checks the done flags of chunks 0..k-1, 32 per round trip.
+            if (threadIdx.x < 32) {
                 const uint64_t tstart = global_ns();
-                for (int j = 0; j < k && !*s_abort; ++j) {
-                    const unsigned *f = fa.ctrl + 1 + j * fa.groups + g;
-                    while (ld_acquire_u32(f) == 0u) {
+                for (int j0 = 0; j0 < k; j0 += 32) {
+                    const int j = j0 + lane;
+                    const unsigned *f = fa.ctrl + 1 + (int64_t)j * fa.groups + g;
+                    bool done = j >= k || ld_acquire_u32(f) != 0u;
+                    while (!__all_sync(0xffffffffu, done)) {
+                        if (!done)
+                            done = ld_acquire_u32(f) != 0u;
                         if (global_ns() - tstart > kWaitLimitNs) {
-                            record_fault(kFaultFlagTimeout);
-                            *s_abort = 1;
+                            if (lane == 0) {
+                                record_fault(kFaultFlagTimeout);
+                                *s_abort = 1;
+                            }
                             break;
                         }
                     }
+                    if (*s_abort)
+                        break;
                 }
             }
             __syncthreads();
@@ -275,8 +289,32 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 const unsigned char *p = buf(r);
                 const T *xs = reinterpret_cast<const T *>(p) + grp;
                 const T *ds = reinterpret_cast<const T *>(p + xbytes) + grp;
-                const T *Bs = reinterpret_cast<const T *>(p + 2 * xbytes) + n0;
-                const T *Cs = reinterpret_cast<const T *>(p + 2 * xbytes + nbytes) + n0;
+                // B and C rows in fp32: straight from the tile, or (bf16
+                // input) from this stage's fp32 copy, which the four warps
+                // convert together -- every thread needs every row, so
+                // converting once per CTA instead of once per thread saves
+                // most of the unpacking work.
+                const float *Bs;
+                const float *Cs;
+                if constexpr (kBf16) {
+                    float *cb = conv_buf + s * cfloats;
+                    const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p + 2 * xbytes);
+                    const int total = (RO ? 2 : 1) * TT * (int)Nrow;
+                    for (int e = threadIdx.x; e < total; e += kScanThreads)
+                        cb[e] = __bfloat162float(src[e]);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&conv[s]);
+                    if (!__all_sync(0xffffffffu, mbar_wait(&conv[s], (r / STAGES) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    Bs = cb + n0;
+                    Cs = cb + TT * Nrow + n0;
+                } else {
+                    Bs = reinterpret_cast<const float *>(p + 2 * xbytes) + n0;
+                    Cs = reinterpret_cast<const float *>(p + 2 * xbytes + nbytes) + n0;
+                }
                 const int64_t rem = nsteps - (int64_t)i * TT;
                 const int tc = rem < TT ? (int)rem : TT;
 
@@ -335,12 +373,12 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 
                 auto step = [&](int tt) {
                     float Bv[NS];
-                    SmemStateLoad<T, NS, VEC>::run(Bs + tt * Nrow, valid, Bv);
+                    SmemStateLoad<float, NS, VEC>::run(Bs + tt * Nrow, valid, Bv);
                     const float2 dl2 = make_float2(dlv[tt], dlv[tt]);
                     const float2 u2 = make_float2(uv[tt], uv[tt]);
                     if constexpr (RO) {
                         float Cv[NS];
-                        SmemStateLoad<T, NS, VEC>::run(Cs + tt * Nrow, valid, Cv);
+                        SmemStateLoad<float, NS, VEC>::run(Cs + tt * Nrow, valid, Cv);
                         float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                                          make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
@@ -375,10 +413,40 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     for (int tt = 0; tt < TT; ++tt)
                         step(tt);
                 } else {
+                    // The chunk's last, partial stage (at most one per item):
+                    // a compact loop, so that the unrolled body above is the
+                    // only large copy of the step code in the instruction cache.
+#pragma unroll 1
+                    for (int tt = 0; tt < tc; ++tt) {
+                        float dl = smem_val(ds + tt * DPB);
+                        if (SOFTPLUS)
+                            dl = softplus(dl);
+                        const float2 dl2 = make_float2(dl, dl);
+                        const float u = dl * smem_val(xs + tt * DPB);
+                        const float2 u2 = make_float2(u, u);
+                        float Bv[NS], Cv[NS];
+                        SmemStateLoad<float, NS, VEC>::run(Bs + tt * Nrow, valid, Bv);
+                        if constexpr (RO)
+                            SmemStateLoad<float, NS, VEC>::run(Cs + tt * Nrow, valid, Cv);
+                        float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                    for (int tt = 0; tt < TT; ++tt)
-                        if (tt < tc)
-                            step(tt);
+                        for (int j = 0; j < NP; ++j) {
+                            const float2 e = __fmul2_rn(dl2, A2[j]);
+                            const float2 decay = make_float2(ex2(e.x), ex2(e.y));
+                            const float2 inp = __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                            h[j] = __ffma2_rn(decay, h[j], inp);
+                            if constexpr (RO)
+                                acc = __ffma2_rn(h[j], make_float2(Cv[2 * j], Cv[2 * j + 1]), acc);
+                        }
+                        if constexpr (RO) {
+                            float yv = acc.x + acc.y;
+#pragma unroll
+                            for (int o = NSPLIT / 2; o > 0; o >>= 1)
+                                yv += __shfl_xor_sync(0xffffffffu, yv, o);
+                            if (active && q == 0)
+                                Io<T>::store(yp + tt * D, yv);
+                        }
+                    }
                 }
                 yp += (int64_t)TT * D;
                 // This warp is done with the buffer.
@@ -449,7 +517,8 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 inline size_t fused_smem_bytes(size_t es, int TT, int DPB, int64_t Nrow, int stages)
 {
     const size_t stage = (2 * (size_t)TT * DPB + 2 * (size_t)TT * (size_t)Nrow) * es;
-    return (size_t)stages * stage + (size_t)stages * (8 + 8 + 4) + 16;
+    const size_t conv = es == 2 ? 2 * (size_t)TT * (size_t)Nrow * 4 : 0;
+    return (size_t)stages * (stage + conv) + (size_t)stages * (8 + 8 + 8 + 4) + 16;
 }
 
 } // namespace selscan

@@ -29,6 +29,21 @@ def test_work_counts_bf16_and_state():
     assert w4["bytes"] == 2_432_892_928          # includes the final state hT
 
 
+def test_decode_step_work_counts():
+    w = bench.step_work_counts(256, 2560, 16)
+    assert w["bytes"] == 91_947_008          # state read + write dominates (83.9 MB)
+    assert w["elems"] == 655_360
+
+
+def test_reference_arm_decode_workload():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "5", "--steps", "2", "--warmup", "1", "--ref-chains", "4"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+
+
 def test_roofline_arithmetic():
     pk = bench.peaks(148, 2032.0, 6484.3)
     assert pk["mufu_per_s"] == pytest.approx(148 * 32 * 2.032e9)
