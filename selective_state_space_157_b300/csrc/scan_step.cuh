@@ -5,10 +5,10 @@
 //   y[b,d]        = sum_n state'[b,d,n] * C[b,n]
 //
 // The step reads and writes the whole state once: it is bound by HBM
-// bandwidth. G = N/4 consecutive lanes share a chain, each holding 4 states
-// moved as one 16-byte load and store, so a warp streams 32 contiguous
-// 16-byte pieces of the state; the outputs of the G lanes are summed with
-// warp shuffles.
+// bandwidth. G consecutive lanes share a chain, each holding 4V states moved
+// as V 16-byte loads and stores issued together, so a warp streams contiguous
+// state and every lane keeps several requests in flight; the outputs of the G
+// lanes are summed with warp shuffles.
 #pragma once
 
 #include "device_math.cuh"
@@ -24,7 +24,8 @@ struct StepArgs {
     int64_t Bsz, D, N;
 };
 
-template <int G>
+// V 16-byte groups (4V states) per lane, G lanes per chain (N = 4 V G).
+template <int G, int V>
 __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a)
 {
     const int64_t chains = a.Bsz * a.D;
@@ -35,25 +36,36 @@ __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a
     const int64_t chain = active ? chain_raw : chains - 1;
     const int64_t b = chain / a.D, d = chain - b * a.D;
 
-    float4 *sp = reinterpret_cast<float4 *>(a.state) + chain * G + q;
-    float4 s = *sp;
-    const float4 A4 = __ldg(reinterpret_cast<const float4 *>(a.A) + d * G + q);
-    const float4 B4 = __ldg(reinterpret_cast<const float4 *>(a.B) + b * G + q);
-    const float4 C4 = __ldg(reinterpret_cast<const float4 *>(a.C) + b * G + q);
+    // All loads first, so that each lane has V + 3V + 2 requests in flight.
+    float4 *sp = reinterpret_cast<float4 *>(a.state) + (chain * G + q) * V;
+    float4 s[V], A4[V], B4[V], C4[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        s[v] = __ldcs(sp + v);   // read once: streaming
+        A4[v] = __ldg(reinterpret_cast<const float4 *>(a.A) + (d * G + q) * V + v);
+        B4[v] = __ldg(reinterpret_cast<const float4 *>(a.B) + (b * G + q) * V + v);
+        C4[v] = __ldg(reinterpret_cast<const float4 *>(a.C) + (b * G + q) * V + v);
+    }
     const float dl = __ldg(a.delta + chain);
     const float u = dl * __ldg(a.x + chain);
     const float dk = dl * kLog2e;
 
-    s.x = fmaf(ex2(dk * A4.x), s.x, u * B4.x);
-    s.y = fmaf(ex2(dk * A4.y), s.y, u * B4.y);
-    s.z = fmaf(ex2(dk * A4.z), s.z, u * B4.z);
-    s.w = fmaf(ex2(dk * A4.w), s.w, u * B4.w);
-    float yv = fmaf(s.x, C4.x, s.y * C4.y) + fmaf(s.z, C4.z, s.w * C4.w);
+    float yv = 0.0f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        s[v].x = fmaf(ex2(dk * A4[v].x), s[v].x, u * B4[v].x);
+        s[v].y = fmaf(ex2(dk * A4[v].y), s[v].y, u * B4[v].y);
+        s[v].z = fmaf(ex2(dk * A4[v].z), s[v].z, u * B4[v].z);
+        s[v].w = fmaf(ex2(dk * A4[v].w), s[v].w, u * B4[v].w);
+        yv += fmaf(s[v].x, C4[v].x, s[v].y * C4[v].y) + fmaf(s[v].z, C4[v].z, s[v].w * C4[v].w);
+    }
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1)
         yv += __shfl_xor_sync(0xffffffffu, yv, o);
     if (active) {
-        *sp = s;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            __stcs(sp + v, s[v]);   // written once: streaming
         if (q == 0)
             a.y[chain] = yv;
     }

@@ -636,21 +636,27 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     StepArgs a{state, x, delta, A, B, C, y, Bsz, D, N};
     const int64_t chains = Bsz * D;
-    const int G = (int)(N / 4);
-    // 4 states per lane, G lanes per chain; G must divide the warp so that a
-    // chain's lanes never straddle two warps.
+    // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
+    // must divide the warp so that a chain's lanes never straddle two warps.
+    // V = 2 (8 states per lane) unless N is too small or SELSCAN_STEP_V says.
+    long V = env_long("SELSCAN_STEP_V", 2);
+    if (V != 1 && V != 2 && V != 4) V = 2;
+    while (V > 1 && N % (4 * V) != 0) V /= 2;
+    const int G = (int)(N / (4 * V));
     const bool vec = (N % 4 == 0) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&
                      aligned(state, 16) && aligned(A, 16) && aligned(B, 16) && aligned(C, 16);
     if (vec) {
         const int64_t blocks = (chains * G + kStepThreads - 1) / kStepThreads;
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-        switch (G) {
-        case 1: step_vec_kernel<1><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
-        case 2: step_vec_kernel<2><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
-        case 4: step_vec_kernel<4><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
-        case 8: step_vec_kernel<8><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
-        default: step_vec_kernel<16><<<(unsigned)blocks, kStepThreads, 0, st>>>(a); break;
-        }
+        const unsigned nb = (unsigned)blocks;
+#define SELSCAN_STEP_CASE(g, v) \
+        if (G == g && V == v) { step_vec_kernel<g, v><<<nb, kStepThreads, 0, st>>>(a); }
+        SELSCAN_STEP_CASE(1, 1) else SELSCAN_STEP_CASE(2, 1) else SELSCAN_STEP_CASE(4, 1)
+        else SELSCAN_STEP_CASE(8, 1) else SELSCAN_STEP_CASE(16, 1)
+        else SELSCAN_STEP_CASE(1, 2) else SELSCAN_STEP_CASE(2, 2) else SELSCAN_STEP_CASE(4, 2)
+        else SELSCAN_STEP_CASE(8, 2) else SELSCAN_STEP_CASE(1, 4) else SELSCAN_STEP_CASE(2, 4)
+        else SELSCAN_STEP_CASE(4, 4)
+#undef SELSCAN_STEP_CASE
     } else {
         const int64_t blocks = (chains + kStepThreads - 1) / kStepThreads;
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");

@@ -87,3 +87,36 @@ def test_step_rejects_overlap():
     with pytest.raises(ss.SelscanError) as e:
         ss.selscan_step(s, x, x, A, B, B, y=x)
     assert e.value.code == ss.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("V", [1, 2, 4])
+@pytest.mark.parametrize("N", [4, 8, 16, 32, 64])
+def test_step_lane_widths(orc, monkeypatch, V, N):
+    """Every states-per-lane choice of the vectorised step (4, 8 or 16 states
+    per lane, narrowed where N is too small) gives the oracle's result."""
+    monkeypatch.setenv("SELSCAN_STEP_V", str(V))
+    Bsz, D = 5, 29
+    st, x, dl, A, B, C = rand_step(Bsz, D, N, seed=100 + N + V)
+    s_dev = to_dev(st)
+    y = ss.selscan_step(s_dev, to_dev(x), to_dev(dl), to_dev(A), to_dev(B), to_dev(C))
+    torch.cuda.synchronize()
+    s_ref = st.astype(np.float64)
+    y_ref = orc.selscan_step(s_ref, x, dl, A, B, C)
+    assert scaled_err(to_np(y), y_ref) <= TOL[W.F32]
+    assert scaled_err(to_np(s_dev), s_ref) <= TOL[W.F32]
+
+
+def test_step_unaligned_state(orc):
+    """A state that starts 4 bytes past a 16-byte boundary takes the one-thread-
+    per-chain kernel and gives the same result."""
+    Bsz, D, N = 2, 33, 16
+    st, x, dl, A, B, C = rand_step(Bsz, D, N, seed=7)
+    buf = torch.empty(Bsz * D * N + 1, device="cuda")
+    s_dev = buf[1:].view(Bsz, D, N)
+    s_dev.copy_(torch.from_numpy(st))
+    y = ss.selscan_step(s_dev, to_dev(x), to_dev(dl), to_dev(A), to_dev(B), to_dev(C))
+    torch.cuda.synchronize()
+    s_ref = st.astype(np.float64)
+    y_ref = orc.selscan_step(s_ref, x, dl, A, B, C)
+    assert scaled_err(to_np(y), y_ref) <= TOL[W.F32]
+    assert scaled_err(to_np(s_dev), s_ref) <= TOL[W.F32]
