@@ -414,14 +414,17 @@ def run_gpu(args, world, rank, local):
 
 def run_decode(args, world, rank, local, dev, w):
     """The decode workload: one step = one selscan_step over (Bsz, D, N).
-    Four independent decode streams (state and per-step inputs each) are
+    Eight independent decode streams (state and per-step inputs each) are
     rotated so that every step reads its 42 MB state from HBM rather than L2,
-    as a server interleaving several sequences would."""
+    as a server interleaving several sequences would. The steps are captured
+    in CUDA graphs and the timed steps replay them, as a decode loop launches
+    a fixed step sequence; the same steps launched one Python call at a time
+    are timed too and reported beside it."""
     import torch
     import selective_state_space_157_b300 as ss
     from selective_state_space_157_b300 import workloads as W
 
-    streams = 4
+    streams = 8
     A = torch.from_numpy(W.decode_A(w)).to(dev)
     states = [torch.from_numpy(W.decode_state(w)).to(dev) for _ in range(streams)]
     inputs = [[torch.from_numpy(a).to(dev) for a in W.decode_step_inputs(w, k)] for k in range(streams)]
@@ -436,18 +439,50 @@ def run_decode(args, world, rank, local, dev, w):
     torch.cuda.synchronize()
     ss.check_device_error()
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, dev)
+    # One graph holds `per_graph` consecutive steps (the streams in turn); K
+    # steps replay it K // per_graph times, then a graph of the K % per_graph
+    # steps that remain.
+    per_graph = 4 * streams
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(i)
+        return g
+
+    full = capture(per_graph)
+    rest = capture(args.steps % per_graph) if args.steps % per_graph else None
+    stream.wait_stream(side)
+    for _ in range(max(1, args.warmup // per_graph)):
+        full.replay()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
+
+    def replay_all(_):
+        for _ in range(args.steps // per_graph):
+            full.replay()
+        if rest is not None:
+            rest.replay()
+
+    def timed(run, calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world, dev)
         torch.cuda.synchronize()
-    barrier(world, dev)
-    ss.check_device_error()
-    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        with ClockSampler(local) as clk:
+            e0.record(stream)
+            for i in range(calls):
+                run(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        barrier(world, dev)
+        ss.check_device_error()
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev), clk
+
+    sec_eager, _ = timed(step, args.steps)
+    sec, clk = timed(replay_all, 1)
     per_step = sec / args.steps
     elems = w.Bsz * w.D
     value = world * elems * args.steps / sec
@@ -496,7 +531,9 @@ def run_decode(args, world, rank, local, dev, w):
                "sample": f"{len(chains)} of {w.Bsz * w.D} chains x {steps_h} steps ({secs:.2f} s, fp64, one thread)"}
     config = {"workload": f"{w.name}: Bsz={w.Bsz} D={w.D} N={w.N} f32 decode step, state updated in place",
               "global_batch": w.Bsz * world, "seq_len": 1, "parallelism": f"replicas x{world}",
-              "l2": f"{streams} rotating decode streams ({streams * w.Bsz * w.D * w.N * 4 / 1e6:.0f} MB of state) > L2"}
+              "l2": f"{streams} rotating decode streams ({streams * w.Bsz * w.D * w.N * 4 / 1e6:.0f} MB of state) > 2x L2",
+              "launch": f"CUDA graph replay of {per_graph} captured selscan_step calls (the {streams} decode streams in turn); "
+                        f"one Python call per step: {sec_eager / args.steps * 1e6:.1f} us per step"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
                        launches=args.steps, clocks=clk.summary(), dtype="f32")

@@ -160,7 +160,9 @@ bool pick_shape(int ns, int nsplit, bool vec, ScanKernels *out)
 // ---- TMA path -----------------------------------------------------------
 
 constexpr int kTT = 16;       // timesteps per pipeline stage (default)
-constexpr int kStages = 4;    // buffers in flight (default)
+// Buffers in flight per CTA (default). Two measured fastest on B300 (Bsz=2,
+// L=2048, D=1536: 72 us against 79 us with four); no workload measured slower.
+constexpr int kStages = 2;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -304,12 +306,25 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     // its timesteps, and a readout must wait for the reductions of the chunks
     // before it, so chunking pays only when the chains alone leave the GPU
     // mostly idle. Measured on B300: with >= 3 warps of chains per SM one pass
-    // is fastest (Bsz=8, D=2048); below that, about 12 warps per SM in
-    // flight is best (Bsz=2, D=1536: ~18 chunks; Bsz=1, L=131072: ~40).
+    // is fastest (Bsz=8, D=2048). Below that, about 12 warps per SM in flight
+    // is best while chunks stay short (Bsz=2, L=2048, D=1536: 19 chunks of
+    // 108 steps, where per-item costs weigh); once that leaves chunks of 512
+    // steps or more, 24 warps per SM is faster (Bsz=1, L=131072: 74 chunks,
+    // 5% faster than 37; Bsz=4, L=16384: 9% faster).
     const int64_t warps1 = Bsz * (int64_t)p->dtiles * (kScanThreads / 32);
-    const long target = env_long("SELSCAN_TARGET_WARPS", 12) * (long)sms;
-    const bool enough = warps1 >= 3 * (int64_t)sms && env_long("SELSCAN_TARGET_WARPS", 0) == 0;
-    int64_t K = (warps1 <= 0 || enough || warps1 >= target) ? 1 : (target + warps1 - 1) / warps1;
+    const long want_warps = env_long("SELSCAN_TARGET_WARPS", 0);
+    auto chunks_for = [&](long warps_per_sm) -> int64_t {
+        const int64_t target = (int64_t)warps_per_sm * sms;
+        return warps1 >= target ? 1 : (target + warps1 - 1) / warps1;
+    };
+    int64_t K = 1;
+    if (warps1 > 0 && want_warps > 0) {
+        K = chunks_for(want_warps);
+    } else if (warps1 > 0 && warps1 < 3 * (int64_t)sms) {
+        K = chunks_for(12);
+        if (K > 1 && L / K >= 512)
+            K = chunks_for(24);
+    }
     const int64_t min_chunk = 64;
     int64_t maxK = (L + min_chunk - 1) / min_chunk;
     if (K > maxK) K = maxK;
@@ -638,9 +653,11 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
     const int64_t chains = Bsz * D;
     // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
     // must divide the warp so that a chain's lanes never straddle two warps.
-    // V = 2 (8 states per lane) unless N is too small or SELSCAN_STEP_V says.
-    long V = env_long("SELSCAN_STEP_V", 2);
-    if (V != 1 && V != 2 && V != 4) V = 2;
+    // V = 1 measured fastest on B300 (Bsz=256, D=2560, N=16, state from HBM:
+    // 17.3 us per step against 18.7 with V = 2 and 24.4 with V = 4);
+    // SELSCAN_STEP_V selects another.
+    long V = env_long("SELSCAN_STEP_V", 1);
+    if (V != 1 && V != 2 && V != 4) V = 1;
     while (V > 1 && N % (4 * V) != 0) V /= 2;
     const int G = (int)(N / (4 * V));
     const bool vec = (N % 4 == 0) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&

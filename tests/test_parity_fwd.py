@@ -118,6 +118,17 @@ def test_threads_per_chain(orc, env, nsplit, dtype):
     check(orc, inp)
 
 
+@pytest.mark.parametrize("stages", [2, 3, 4, 8])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_ring_depths(orc, env, stages, dtype):
+    """Any number of shared-memory buffers in flight per CTA (the ring the
+    tiles arrive in) gives the same result, with chunk lengths that are and
+    are not multiples of the 16-step tile, and a ragged last chunk."""
+    env(SELSCAN_TMA_STAGES=stages, SELSCAN_CHUNK=16 * stages + 5)
+    inp = W.fwd_inputs(2, 401, 136, 16, seed=stages, dtype=dtype, with_h0=True)
+    check(orc, inp)
+
+
 def test_chunked_matches_sequential_closely(env):
     inp = W.fwd_inputs(1, 4096, 256, 16, seed=77, with_h0=True)
     outs = []
