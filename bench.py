@@ -88,11 +88,15 @@ def roofline(work: dict, pk: dict, seconds: float, traffic=None, kernel="selscan
     t_roof = max(t_hbm, t_mufu, t_fp32)
     t_sum = max(t_hbm, t_mufu + t_fp32)
     bound = "hbm" if t_hbm >= max(t_mufu, t_fp32) else "alu"
+    if bound == "hbm":   # bytes moved per second against the measured copy bandwidth
+        achieved, peak, unit = work["bytes"] / seconds / 1e9, pk["hbm_bytes_per_s"] / 1e9, "GB/s"
+    else:                # state updates per second against the MUFU / FP32 bound
+        achieved, peak, unit = work["updates"] / seconds / 1e12, work["updates"] / t_roof / 1e12, "Tupdate/s"
     return {
         "bound": bound,
-        "achieved": work["updates"] / seconds / 1e12,
-        "peak": work["updates"] / t_roof / 1e12,
-        "unit": "Tupdate/s",
+        "achieved": achieved,
+        "peak": peak,
+        "unit": unit,
         "frac": t_roof / seconds,
         "frac_summed_bound": t_sum / seconds,
         "hbm_gbs": work["bytes"] / seconds / 1e9,

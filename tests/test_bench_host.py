@@ -57,6 +57,20 @@ def test_roofline_arithmetic():
     assert r["peak"] * r["frac"] == pytest.approx(r["achieved"])
 
 
+def test_roofline_hbm_bound_in_bytes():
+    """An HBM-bound call (the decode step) reports bytes per second against the
+    measured copy bandwidth; frac is the same ratio either way."""
+    pk = bench.peaks(148, 2032.0, 6484.3)
+    w = bench.step_work_counts(256, 2560, 16)
+    assert w["bytes"] == 2 * 256 * 2560 * 16 * 4 + 3 * 256 * 2560 * 4 + 2 * 256 * 16 * 4 + 2560 * 16 * 4
+    t = 2 * w["bytes"] / pk["hbm_bytes_per_s"]
+    r = bench.roofline(w, pk, seconds=t)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["peak"] == pytest.approx(6484.3)
+    assert r["frac"] == pytest.approx(0.5)
+    assert r["achieved"] == pytest.approx(0.5 * 6484.3)
+
+
 def test_result_line_has_contract_keys():
     line = bench.result_line(value=1.0, n_gpus=1, steps=3, warmup=3, ms_per_step=1.0,
                              config={"workload": "w"}, roof={}, cpu={}, e2e={}, launches=3,
