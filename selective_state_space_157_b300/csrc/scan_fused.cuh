@@ -6,7 +6,7 @@
 //     (K-1)*G .. (2K-1)*G - 1   readout items  (chunk k,       group g), k-major
 // and CTAs take them in that order from an atomic ticket counter. An
 // aggregate item scans its chunk from a zero state and publishes the pair
-// (decay[n] = exp(A[d,n] * sum dl), end[n]) -- one operand of the
+// (decay[n] = exp(A[d,n] * sum dl), end[n]), as sum dl and end[n] -- one operand of the
 // associative composition (a1,b1) o (a2,b2) = (a2 a1, a2 b1 + b2) of the
 // parallel scan (booiljung.github.io "3.1 LTI systems ...", section 3.1.5.2)
 // -- then raises its done flag. A readout item folds the published pairs of
@@ -40,7 +40,7 @@ namespace selscan {
 struct FusedArgs {
     CUtensorMap mx, md, mB, mC;
     ScanArgs s;
-    float *aggP;          // (K-1, Bsz, D, N): chunk decay exp(A * sum dl)
+    float *aggS;          // (K-1, Bsz, D): sum of dl over the chunk
     float *aggH;          // (K-1, Bsz, D, N): chunk end state from zero
     unsigned *ctrl;       // [0]: ticket counter; [1 + k*G + g]: aggregate done flags (zeroed per call)
     int stages;
@@ -50,6 +50,7 @@ struct FusedArgs {
 };
 
 constexpr unsigned kFaultFlagTimeout = 2;   // a chunk aggregate never appeared
+constexpr int kFoldBatch = 4;               // chunk pairs in flight per fold round
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
 {
@@ -253,15 +254,34 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             __syncthreads();
             if (*s_abort)
                 break;
-            const int64_t slot = (int64_t)a.Bsz * D * N;
+            // Fold the pairs of chunks 0..k-1, kFoldBatch at a time: all loads
+            // of a batch are issued before the first is used. A chunk's decay
+            // exp(A * sum dl) is rebuilt here from its sum of dl, exactly as the
+            // aggregate item would have computed it.
+            const int64_t bd_all = (int64_t)a.Bsz * D;
+            const int64_t slot = bd_all * N;
             const int64_t off = (b * D + d) * N + n0;
-            for (int j = 0; j < k; ++j) {
-                float2 P[NP], E[NP];
-                load_state_cg<NS, VEC>(fa.aggP + j * slot + off, valid, P);
-                load_state_cg<NS, VEC>(fa.aggH + j * slot + off, valid, E);
+            const float *Sp = fa.aggS + b * D + d;
+            for (int j0 = 0; j0 < k; j0 += kFoldBatch) {
+                float S[kFoldBatch];
+                float2 E[kFoldBatch][NP];
 #pragma unroll
-                for (int i = 0; i < NP; ++i)
-                    h[i] = __ffma2_rn(P[i], h[i], E[i]);
+                for (int jj = 0; jj < kFoldBatch; ++jj) {
+                    const int64_t j = j0 + jj < k ? j0 + jj : k - 1;   // past the end: a repeat, unused
+                    S[jj] = __ldcg(Sp + j * bd_all);
+                    load_state_cg<NS, VEC>(fa.aggH + j * slot + off, valid, E[jj]);
+                }
+#pragma unroll
+                for (int jj = 0; jj < kFoldBatch; ++jj) {
+                    if (j0 + jj < k) {
+                        const float2 s2 = make_float2(S[jj], S[jj]);
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) {
+                            const float2 e = __fmul2_rn(s2, A2[i]);
+                            h[i] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h[i], E[jj][i]);
+                        }
+                    }
+                }
             }
         }
 
@@ -485,16 +505,11 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 const int64_t off = ((int64_t)k * a.Bsz * D + b * D + d) * N + n0;
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
-                    const float2 e = __fmul2_rn(make_float2(s_sum, s_sum), A2[j]);
-                    if (2 * j < valid) {
-                        fa.aggP[off + 2 * j] = ex2(e.x);
-                        fa.aggH[off + 2 * j] = h[j].x;
-                    }
-                    if (2 * j + 1 < valid) {
-                        fa.aggP[off + 2 * j + 1] = ex2(e.y);
-                        fa.aggH[off + 2 * j + 1] = h[j].y;
-                    }
+                    if (2 * j < valid) fa.aggH[off + 2 * j] = h[j].x;
+                    if (2 * j + 1 < valid) fa.aggH[off + 2 * j + 1] = h[j].y;
                 }
+                if (q == 0)
+                    fa.aggS[(int64_t)k * a.Bsz * D + b * D + d] = s_sum;
             }
         }
         if (!readout) {

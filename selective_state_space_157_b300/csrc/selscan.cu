@@ -340,13 +340,13 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
 }
 
-// Chunk-carry workspace of a plan: per chunk boundary and chain the pair
-// (decay, end state) of N floats each, then the ticket counter and one done
-// flag per aggregate item. The plain-load path uses a smaller part of it.
+// Chunk-carry workspace of a plan: per chunk boundary and chain the end
+// state (N floats) and the sum of dl (1 float), then the ticket counter and
+// one done flag per aggregate item (the plain-load path uses no flags).
 size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
 {
     if (plan.K <= 1) return 0;
-    const size_t pairs = 2 * (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)N * sizeof(float);
+    const size_t pairs = (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float);
     const size_t flags = (1 + (size_t)(plan.K - 1) * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
     return pairs + flags;
 }
@@ -405,10 +405,10 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
     fa.items_total = (int)items_total;
     int64_t grid = items_total;
     if (plan.K > 1) {
-        const size_t bdn = (size_t)(a.Bsz * a.D * a.N);
-        fa.aggP = ws;
-        fa.aggH = ws + (size_t)(plan.K - 1) * bdn;
-        fa.ctrl = reinterpret_cast<unsigned *>(ws + 2 * (size_t)(plan.K - 1) * bdn);
+        const size_t bdn = (size_t)(a.Bsz * a.D * a.N), bd = (size_t)(a.Bsz * a.D);
+        fa.aggH = ws;
+        fa.aggS = ws + (size_t)(plan.K - 1) * bdn;
+        fa.ctrl = reinterpret_cast<unsigned *>(fa.aggS + (size_t)(plan.K - 1) * bd);
         cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, (size_t)(1 + items_agg) * sizeof(unsigned), st);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk flags");
         const int64_t resident = (int64_t)sms * fl.ctas_per_sm;
