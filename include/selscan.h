@@ -61,8 +61,9 @@ typedef enum {
     SELSCAN_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (N > 64) */
     SELSCAN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     SELSCAN_ERR_NO_MEMORY = 4,    /* the chunk-carry workspace could not be allocated */
-    SELSCAN_ERR_TIMEOUT = 5       /* a kernel gave up waiting for its input tiles (reported by
-                                     selscan_check_device_error; the kernel's outputs are invalid) */
+    SELSCAN_ERR_TIMEOUT = 5       /* a kernel gave up waiting for an input tile or a chunk carry
+                                     (reported by selscan_check_device_error; the kernel's outputs
+                                     are invalid) */
 } selscan_status;
 
 /* Largest state size N the kernels implement. */
@@ -183,10 +184,20 @@ const char *selscan_last_error(void);
 
 /* Waits for `stream` and reports whether work enqueued on it failed:
  * SELSCAN_OK; SELSCAN_ERR_CUDA with the CUDA error in selscan_last_error();
- * or SELSCAN_ERR_TIMEOUT when a kernel stopped waiting for input tiles that
- * never arrived (every wait inside the kernels is bounded, so a broken
- * pipeline ends with this status instead of a hang). The fault word is
- * per device and is cleared by this call. */
+ * or SELSCAN_ERR_TIMEOUT when a kernel stopped waiting for an input tile
+ * (fault code 1) or for the carry of an earlier chunk (fault code 2) that
+ * never came. Every wait inside the kernels is bounded (2 s), so a broken
+ * pipeline ends with this status instead of a hang, and the context stays
+ * usable. The fault word is per device and is cleared by this call.
+ *
+ * Testing the timeout path. Two environment variables, read at each
+ * selscan_fwd call, exist only so that tests can make a wait run out
+ * without any fault: SELSCAN_TEST_WITHHOLD_CARRIES=1 makes the chunked
+ * path's reduction items withhold their completion flags, so every readout
+ * of a later chunk waits for a flag that nothing sets; and
+ * SELSCAN_TEST_WAIT_LIMIT_MS (1..2000) shortens the wait. The call then
+ * ends early with invalid outputs, and selscan_check_device_error returns
+ * SELSCAN_ERR_TIMEOUT (fault code 2). */
 int selscan_check_device_error(void *stream);
 
 /* Returns the memory held by the chunk-carry workspace pools of every

@@ -43,6 +43,8 @@ struct FusedArgs {
     float *aggS;          // (K-1, Bsz, D): sum of dl over the chunk
     float *aggH;          // (K-1, Bsz, D, N): chunk end state from zero
     unsigned *ctrl;       // [0]: ticket counter; [1 + k*G + g]: aggregate done flags (zeroed per call)
+    uint64_t wait_ns;     // limit of a readout's wait for the done flags
+    int publish;          // 0 only for the timeout test: aggregates raise no flags
     int stages;
     int groups;           // G
     int items_agg;        // (K-1) * G
@@ -239,7 +241,8 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     while (!__all_sync(0xffffffffu, done)) {
                         if (!done)
                             done = ld_acquire_u32(f) != 0u;
-                        if (global_ns() - tstart > kWaitLimitNs) {
+                        // Warp-uniform decision: every lane leaves together.
+                        if (__any_sync(0xffffffffu, global_ns() - tstart > fa.wait_ns)) {
                             if (lane == 0) {
                                 record_fault(kFaultFlagTimeout);
                                 *s_abort = 1;
@@ -247,6 +250,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                             break;
                         }
                     }
+                    __syncwarp();
                     if (*s_abort)
                         break;
                 }
@@ -516,7 +520,8 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             __syncthreads();   // every thread's pair is written
             if (threadIdx.x == 0) {
                 __threadfence();
-                st_release_u32(fa.ctrl + 1 + idx, 1u);
+                if (fa.publish)
+                    st_release_u32(fa.ctrl + 1 + idx, 1u);
             }
         }
     }

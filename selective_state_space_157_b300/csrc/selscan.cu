@@ -396,6 +396,13 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         return SELSCAN_ERR_UNSUPPORTED;
     fa.s = a;
     fa.stages = fl.stages;
+    // Timeout test (documented in selscan.h): aggregates withhold their done
+    // flags and readouts give up after SELSCAN_TEST_WAIT_LIMIT_MS.
+    fa.publish = env_long("SELSCAN_TEST_WITHHOLD_CARRIES", 0) == 0;
+    long limit_ms = env_long("SELSCAN_TEST_WAIT_LIMIT_MS", (long)(kWaitLimitNs / 1000000ull));
+    if (limit_ms < 1) limit_ms = 1;
+    if ((uint64_t)limit_ms > kWaitLimitNs / 1000000ull) limit_ms = (long)(kWaitLimitNs / 1000000ull);
+    fa.wait_ns = (uint64_t)limit_ms * 1000000ull;
     const int64_t groups = a.Bsz * plan.dtiles;
     const int64_t items_agg = (int64_t)(plan.K - 1) * groups;
     const int64_t items_total = items_agg + (int64_t)plan.K * groups;
@@ -724,7 +731,10 @@ extern "C" int selscan_check_device_error(void *stream)
     if (e != cudaSuccess) return cuda_fail(e, "reading the device fault word");
     if (fault != 0) {
         cudaMemcpyToSymbol(g_selscan_fault, &zero, sizeof zero);
-        return fail(SELSCAN_ERR_TIMEOUT, "a kernel gave up waiting for its input tiles (fault code %u)", fault);
+        const char *what = fault == kFaultTmaTimeout    ? "an input tile never arrived"
+                           : fault == kFaultFlagTimeout ? "a chunk carry never appeared"
+                                                        : "unknown";
+        return fail(SELSCAN_ERR_TIMEOUT, "a kernel gave up waiting (fault code %u: %s)", fault, what);
     }
     return SELSCAN_OK;
 }
