@@ -92,7 +92,8 @@ typedef enum {
  * another argument is SELSCAN_ERR_INVALID_ARG.
  *
  * Memory: long sequences use a small library-owned workspace for the chunk
- * carries (2 * ceil(L / chunk) * Bsz * D * N fp32 at most), taken from a
+ * carries ((ceil(L / chunk) - 1) * Bsz * D * (N + 1) fp32 plus one flag per
+ * chunk and channel tile), taken from a
  * private stream-ordered pool on `stream` and returned to it before the
  * call's work completes; selscan_release_workspace() gives the pool's
  * memory back to the device. SELSCAN_ERR_NO_MEMORY if it cannot be had.
@@ -176,6 +177,32 @@ int selscan_fwd_noalloc(const void *x, const void *delta, const float *A, const 
 int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype,
                      int *chunks, int64_t *chunk_len, int *launches,
                      int64_t *workspace_bytes);
+
+/*
+ * selscan_fwd_host -- selscan_fwd with every tensor in HOST memory.
+ * (No counterpart on the pages: this is the library's host-to-device path.)
+ *
+ * Same arguments, shapes, sizes, aliasing rules and results as selscan_fwd,
+ * except that x, delta, A, B, C, y, h0 and hT are host pointers. They need
+ * not be page-locked, but only page-locked (pinned) buffers let the copies
+ * run asynchronously and overlap the scan.
+ *
+ * The sequence is cut into pieces along L (about 32 MB of input each, and at
+ * least two when L >= 128). Inputs go in on two copy streams. While
+ * piece p is scanned on the current device, piece p+1's inputs are copied
+ * in and piece p-1's output is copied out, on library-owned streams;
+ * each piece starts from the device-resident final state of the one before,
+ * so the pieces compose exactly like the chunks of one call. Device staging
+ * (two pieces' inputs and outputs, A and the state) comes from the same
+ * stream-ordered pool as the chunk workspace.
+ *
+ * Blocking: returns once y (and hT) are in host memory. Work already
+ * enqueued on `stream` is waited for first. Calls on one device are
+ * serialised by the library; calls on different devices may run together.
+ */
+int selscan_fwd_host(const void *x, const void *delta, const float *A, const void *B,
+                     const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                     int dtype, int delta_softplus, const float *h0, float *hT, void *stream);
 
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_version.argtypes = []
         L.selscan_fwd_noalloc.restype = INT
         L.selscan_fwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_fwd_host.restype = INT
+        L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
         _lib = L
@@ -238,20 +240,34 @@ def _to_dev(t, dev):
 
 
 def _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT):
+    """Host tensors: one selscan_fwd_host call (the library pipelines the
+    copies in, the scan and the copies out on the current device). Returns
+    once the outputs are in host memory. Page-locked tensors let the copies
+    overlap the scan."""
     import torch
-    dev = torch.device("cuda", torch.cuda.current_device())
-    xd, dd, Ad, Bd, Cd, h0d = (_to_dev(t, dev) for t in (x, delta, A, B, C, h0))
+    Bsz, L, D = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    code = _dtype_code(x)
+    cpu = torch.device("cpu")
+    for t, name, shape, dt in ((x, "x", (Bsz, L, D), x.dtype), (delta, "delta", (Bsz, L, D), x.dtype),
+                               (A, "A", (D, N), torch.float32), (B, "B", (Bsz, L, N), x.dtype),
+                               (C, "C", (Bsz, L, N), x.dtype)):
+        _need(t, name, shape, dt, cpu)
+    if h0 is not None:
+        _need(h0, "h0", (Bsz, D, N), torch.float32, cpu)
     want_state = return_final_state or hT is not None
-    out = selscan_fwd(xd, dd, Ad, Bd, Cd, delta_softplus, h0d, return_final_state=want_state)
-    yd, hTd = out if want_state else (out, None)
     if y is None:
-        y = torch.empty(yd.shape, dtype=yd.dtype, pin_memory=True)
-    y.copy_(yd, non_blocking=True)
-    if want_state:
-        if hT is None:
-            hT = torch.empty(hTd.shape, dtype=hTd.dtype, pin_memory=True)
-        hT.copy_(hTd, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+        y = torch.empty((Bsz, L, D), dtype=x.dtype, pin_memory=True)
+    else:
+        _need(y, "y", (Bsz, L, D), x.dtype, cpu)
+    if want_state and hT is None:
+        hT = torch.empty((Bsz, D, N), dtype=torch.float32, pin_memory=True)
+    if hT is not None:
+        _need(hT, "hT", (Bsz, D, N), torch.float32, cpu)
+    rc = lib().selscan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
+                                Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
+                                _stream_ptr(None))
+    _check(rc)
     return (y, hT) if want_state else y
 
 

@@ -623,6 +623,205 @@ extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float
     return launch_fwd_into(a, plan, dtype, sms, ws, st);
 }
 
+// ---- forward from host buffers --------------------------------------------
+// The sequence is cut into pieces along L. Piece p's inputs are copied in on
+// one stream while piece p-1 is scanned on a second and piece p-2's output is
+// copied out on a third; the scan of each piece starts from the final state
+// of the one before (h0/hT chaining on the device), so pieces compose exactly
+// like chunks. Device staging is double-buffered per piece.
+
+namespace selscan {
+namespace {
+
+struct HostPipe {
+    cudaStream_t in = nullptr, in2 = nullptr, comp = nullptr, out = nullptr;
+    cudaEvent_t ev[10] = {};  // start, alloc, in[2], comp[2], out[2], in2[2]
+    std::mutex mu;            // one host-buffer call at a time per device
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_init;
+
+int host_pipe(int dev, HostPipe **out)
+{
+    std::lock_guard<std::mutex> lk(g_pipe_init);
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.in) {
+        cudaStream_t s[4];
+        for (int i = 0; i < 4; ++i) {
+            cudaError_t e = cudaStreamCreateWithFlags(&s[i], cudaStreamNonBlocking);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+        }
+        for (cudaEvent_t &ev : hp.ev) {
+            cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
+        hp.in = s[0];
+        hp.comp = s[1];
+        hp.out = s[2];
+        hp.in2 = s[3];
+    }
+    *out = &hp;
+    return SELSCAN_OK;
+}
+
+// Rows of `width` bytes, `rows` of them, between pitched buffers.
+cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t rows,
+                      cudaMemcpyKind kind, cudaStream_t st)
+{
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, st);
+}
+
+} // namespace
+} // namespace selscan
+
+extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A, const void *B,
+                                const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                                int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
+{
+    g_err[0] = '\0';
+    bool empty = false;
+    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty);
+    if (rc != SELSCAN_OK || empty) return rc;
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    const size_t state_bytes = (size_t)(Bsz * D * N) * 4;
+    if (L == 0) {   // the final state is the initial state (or zeros)
+        if (hT && hT != h0) {
+            if (h0) memcpy(hT, h0, state_bytes);
+            else memset(hT, 0, state_bytes);
+        }
+        return SELSCAN_OK;
+    }
+
+    int dev = 0, sms = 0;
+    rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    HostPipe *hp = nullptr;
+    rc = host_pipe(dev, &hp);
+    if (rc != SELSCAN_OK) return rc;
+    std::lock_guard<std::mutex> lk(hp->mu);
+
+    // Piece length: about 32 MB of input per piece, at least 64 steps, and
+    // at least two pieces when L >= 128 so that copies overlap. Measured on
+    // B300 (pinned buffers): Bsz=2 L=2048 D=1536 takes 1.40 ms per call in
+    // two pieces against 1.54 ms in seven; Bsz=1 L=131072 37 ms in 32 pieces
+    // against 43 ms in 194 (fewer, larger copies and launches per call).
+    // SELSCAN_HOST_PIECE overrides it, for tests.
+    const size_t step_in = (size_t)Bsz * (size_t)(2 * D + 2 * N) * es;
+    int64_t lp = (int64_t)((32u << 20) / (step_in ? step_in : 1));
+    if (lp < 64) lp = 64;
+    if (lp >= L && L >= 128) lp = (L + 1) / 2;
+    const long force = env_long("SELSCAN_HOST_PIECE", 0);
+    if (force > 0) lp = force;
+    if (lp > L) lp = L;
+    const int64_t pieces = (L + lp - 1) / lp;
+    const bool chain = pieces > 1 || h0 || hT;
+
+    // Device staging: per slot x, delta, y (Bsz, lp, D) and B, C (Bsz, lp, N);
+    // then A and the state. Every part starts on a 256-byte boundary.
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t bx = up((size_t)(Bsz * lp * D) * es), bn = up((size_t)(Bsz * lp * N) * es);
+    const size_t slot_bytes = 3 * bx + 2 * bn;
+    const size_t total = 2 * slot_bytes + up((size_t)(D * N) * 4) + (chain ? up(state_bytes) : 0);
+    cudaMemPool_t pool = nullptr;
+    rc = workspace_pool(dev, &pool);
+    if (rc != SELSCAN_OK) return rc;
+
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    cudaEvent_t ev_start = hp->ev[0], ev_alloc = hp->ev[1];
+    cudaEvent_t *ev_in = hp->ev + 2, *ev_comp = hp->ev + 4, *ev_out = hp->ev + 6, *ev_in2 = hp->ev + 8;
+    // Inputs over two copy streams (x and B on one, delta and C on the other)
+    // unless SELSCAN_HOST_COPY_STREAMS=1.
+    const bool two_in = env_long("SELSCAN_HOST_COPY_STREAMS", 2) != 1;
+    cudaStream_t in2 = two_in ? hp->in2 : hp->in;
+    cudaError_t e = cudaEventRecord(ev_start, caller);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    cudaStreamWaitEvent(hp->comp, ev_start, 0);
+    unsigned char *ws = nullptr;
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), total, pool, hp->comp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SELSCAN_ERR_NO_MEMORY, "host staging of %zu bytes: %s", total, cudaGetErrorString(e));
+    }
+    cudaEventRecord(ev_alloc, hp->comp);
+    cudaStreamWaitEvent(hp->in, ev_alloc, 0);
+    cudaStreamWaitEvent(hp->in2, ev_alloc, 0);
+    cudaStreamWaitEvent(hp->out, ev_alloc, 0);
+    float *A_d = reinterpret_cast<float *>(ws + 2 * slot_bytes);
+    float *state_d = chain ? reinterpret_cast<float *>(ws + 2 * slot_bytes + up((size_t)(D * N) * 4)) : nullptr;
+
+    e = cudaMemcpyAsync(A_d, A, (size_t)(D * N) * 4, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess && h0)
+        e = cudaMemcpyAsync(state_d, h0, state_bytes, cudaMemcpyHostToDevice, hp->in);
+
+    const size_t rows = (size_t)Bsz;
+    const size_t xpitch = (size_t)(L * D) * es, npitch = (size_t)(L * N) * es;
+    for (int64_t p = 0; p < pieces && e == cudaSuccess && rc == SELSCAN_OK; ++p) {
+        const int slot = (int)(p & 1);
+        unsigned char *base = ws + slot * slot_bytes;
+        void *x_d = base, *dl_d = base + bx, *y_d = base + 2 * bx, *B_d = base + 3 * bx, *C_d = base + 3 * bx + bn;
+        const int64_t l0 = p * lp;
+        const int64_t n = L - l0 < lp ? L - l0 : lp;
+        const size_t wx = (size_t)(n * D) * es, wn = (size_t)(n * N) * es;
+        const size_t ox = (size_t)(l0 * D) * es, on = (size_t)(l0 * N) * es;
+
+        // In: the slot's inputs are free once the scan of piece p-2 is done.
+        if (p >= 2) {
+            cudaStreamWaitEvent(hp->in, ev_comp[slot], 0);
+            if (two_in) cudaStreamWaitEvent(in2, ev_comp[slot], 0);
+        }
+        e = copy_rows(x_d, wx, static_cast<const unsigned char *>(x) + ox, xpitch, wx, rows, cudaMemcpyHostToDevice, hp->in);
+        if (e == cudaSuccess)
+            e = copy_rows(dl_d, wx, static_cast<const unsigned char *>(delta) + ox, xpitch, wx, rows, cudaMemcpyHostToDevice, in2);
+        if (e == cudaSuccess)
+            e = copy_rows(B_d, wn, static_cast<const unsigned char *>(B) + on, npitch, wn, rows, cudaMemcpyHostToDevice, hp->in);
+        if (e == cudaSuccess)
+            e = copy_rows(C_d, wn, static_cast<const unsigned char *>(C) + on, npitch, wn, rows, cudaMemcpyHostToDevice, in2);
+        if (e != cudaSuccess) break;
+        cudaEventRecord(ev_in[slot], hp->in);
+        if (two_in) cudaEventRecord(ev_in2[slot], in2);
+
+        // Scan: after the inputs landed and piece p-2's output left the slot.
+        cudaStreamWaitEvent(hp->comp, ev_in[slot], 0);
+        if (two_in) cudaStreamWaitEvent(hp->comp, ev_in2[slot], 0);
+        if (p >= 2) cudaStreamWaitEvent(hp->comp, ev_out[slot], 0);
+        FwdPlan plan;
+        plan_fwd(Bsz, n, D, N, es, x_d, dl_d, B_d, C_d, sms, &plan);
+        ScanArgs a;
+        memset(&a, 0, sizeof a);
+        a.x = x_d; a.delta = dl_d; a.B = B_d; a.C = C_d; a.A = A_d; a.y = y_d;
+        a.h0 = (p == 0 && !h0) ? nullptr : state_d;
+        a.hT = chain ? state_d : nullptr;
+        a.Bsz = Bsz; a.L = n; a.D = D; a.N = N;
+        a.softplus = delta_softplus ? 1 : 0;
+        rc = launch_fwd(a, plan, dtype, dev, sms, hp->comp);
+        if (rc != SELSCAN_OK) break;
+        cudaEventRecord(ev_comp[slot], hp->comp);
+
+        // Out.
+        cudaStreamWaitEvent(hp->out, ev_comp[slot], 0);
+        e = copy_rows(static_cast<unsigned char *>(y) + ox, xpitch, y_d, wx, wx, rows, cudaMemcpyDeviceToHost, hp->out);
+        if (e != cudaSuccess) break;
+        cudaEventRecord(ev_out[slot], hp->out);
+    }
+    if (e == cudaSuccess && rc == SELSCAN_OK && hT)
+        e = cudaMemcpyAsync(hT, state_d, state_bytes, cudaMemcpyDeviceToHost, hp->out);
+
+    // Drain every stream, then give the staging back and let the caller's
+    // stream continue after this call.
+    cudaError_t e2 = cudaStreamSynchronize(hp->in);
+    cudaError_t e5 = cudaStreamSynchronize(hp->in2);
+    cudaError_t e3 = cudaStreamSynchronize(hp->out);
+    cudaFreeAsync(ws, hp->comp);
+    cudaError_t e4 = cudaStreamSynchronize(hp->comp);
+    if (rc != SELSCAN_OK) return rc;
+    if (e == cudaSuccess) e = e2;
+    if (e == cudaSuccess) e = e5;
+    if (e == cudaSuccess) e = e3;
+    if (e == cudaSuccess) e = e4;
+    if (e != cudaSuccess) return cuda_fail(e, "host-buffer pipeline");
+    return SELSCAN_OK;
+}
+
 extern "C" int selscan_step(float *state, const float *x, const float *delta, const float *A,
                             const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
                             int64_t N, void *stream)
