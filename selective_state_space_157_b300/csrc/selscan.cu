@@ -703,8 +703,9 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     // Piece length: about 32 MB of input per piece, at least 64 steps, and
     // at least two pieces when L >= 128 so that copies overlap. Measured on
     // B300 (pinned buffers): Bsz=2 L=2048 D=1536 takes 1.40 ms per call in
-    // two pieces against 1.54 ms in seven; Bsz=1 L=131072 37 ms in 32 pieces
-    // against 43 ms in 194 (fewer, larger copies and launches per call).
+    // two pieces against 1.54 ms in seven; Bsz=1 L=131072 37 ms in pieces of
+    // 2700 or 4096 steps against 43 ms in pieces of 676 (fewer, larger
+    // copies and launches per call).
     // SELSCAN_HOST_PIECE overrides it, for tests.
     const size_t step_in = (size_t)Bsz * (size_t)(2 * D + 2 * N) * es;
     int64_t lp = (int64_t)((32u << 20) / (step_in ? step_in : 1));
