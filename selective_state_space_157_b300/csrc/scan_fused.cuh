@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kScanThreads, 3)
 scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 {
     static_assert(NS % 4 == 0, "states are processed in pairs of pairs");
+    static_assert(TT % 2 == 0, "timesteps are processed in pairs");
     constexpr int DPB = kScanThreads / NSPLIT;
     constexpr int NP = NS / 2;
     constexpr int kWarps = kScanThreads / 32;
@@ -350,26 +351,35 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 #pragma unroll
                 for (int tt = 0; tt < TT; ++tt)
                     dlv[tt] = smem_val(ds + tt * DPB);
+                // Pairs of timesteps share one packed fp32x2 instruction; each
+                // lane rounds exactly as the scalar operation would.
                 if constexpr (SOFTPLUS) {
-                    float ev[TT], pv[TT];
+                    float2 ev[TT / 2], pv[TT / 2];
 #pragma unroll
-                    for (int tt = 0; tt < TT; ++tt) {
-                        ev[tt] = ex2(-fabsf(dlv[tt]) * kLog2e);
-                        pv[tt] = kLog1pPoly[8];
+                    for (int j = 0; j < TT / 2; ++j) {
+                        ev[j] = make_float2(ex2(-fabsf(dlv[2 * j]) * kLog2e), ex2(-fabsf(dlv[2 * j + 1]) * kLog2e));
+                        pv[j] = make_float2(kLog1pPoly[8], kLog1pPoly[8]);
                     }
 #pragma unroll
                     for (int c = 7; c >= 0; --c) {
 #pragma unroll
-                        for (int tt = 0; tt < TT; ++tt)
-                            pv[tt] = fmaf(pv[tt], ev[tt], kLog1pPoly[c]);
+                        for (int j = 0; j < TT / 2; ++j)
+                            pv[j] = __ffma2_rn(pv[j], ev[j], make_float2(kLog1pPoly[c], kLog1pPoly[c]));
                     }
 #pragma unroll
-                    for (int tt = 0; tt < TT; ++tt)
-                        dlv[tt] = fmaf(pv[tt], ev[tt], fmaxf(dlv[tt], 0.0f));
+                    for (int j = 0; j < TT / 2; ++j) {
+                        const float2 r = __ffma2_rn(pv[j], ev[j], make_float2(fmaxf(dlv[2 * j], 0.0f), fmaxf(dlv[2 * j + 1], 0.0f)));
+                        dlv[2 * j] = r.x;
+                        dlv[2 * j + 1] = r.y;
+                    }
                 }
 #pragma unroll
-                for (int tt = 0; tt < TT; ++tt)
-                    uv[tt] = dlv[tt] * smem_val(xs + tt * DPB);
+                for (int j = 0; j < TT / 2; ++j) {
+                    const float2 u = __fmul2_rn(make_float2(dlv[2 * j], dlv[2 * j + 1]),
+                                                make_float2(smem_val(xs + 2 * j * DPB), smem_val(xs + (2 * j + 1) * DPB)));
+                    uv[2 * j] = u.x;
+                    uv[2 * j + 1] = u.y;
+                }
                 if constexpr (!RO) {
                     // Stage sum of dl by pairwise halving (rows past the chunk
                     // end do not count), then one compensated add.
@@ -405,20 +415,17 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     if constexpr (RO) {
                         float Cv[NS];
                         SmemStateLoad<float, NS, VEC>::run(Cs + tt * Nrow, valid, Cv);
-                        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                                         make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+                        float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
                         for (int j = 0; j < NP; ++j) {
                             const float2 e = __fmul2_rn(dl2, A2[j]);
                             const float2 decay = make_float2(ex2(e.x), ex2(e.y));
                             const float2 inp = __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
                             h[j] = __ffma2_rn(decay, h[j], inp);
-                            acc[j & 3] = __ffma2_rn(h[j], make_float2(Cv[2 * j], Cv[2 * j + 1]), acc[j & 3]);
+                            acc[j & 1] = __ffma2_rn(h[j], make_float2(Cv[2 * j], Cv[2 * j + 1]), acc[j & 1]);
                         }
-                        const float2 s01 = __fadd2_rn(acc[0], acc[1]);
-                        const float2 s23 = __fadd2_rn(acc[2], acc[3]);
-                        const float2 s4 = __fadd2_rn(s01, s23);
-                        float yv = s4.x + s4.y;
+                        const float2 s2 = __fadd2_rn(acc[0], acc[1]);
+                        float yv = s2.x + s2.y;
 #pragma unroll
                         for (int o = NSPLIT / 2; o > 0; o >>= 1)
                             yv += __shfl_xor_sync(0xffffffffu, yv, o);
