@@ -71,6 +71,13 @@ class Oracle:
                                                   I64, I64, I64, I64, INT, INT]
         lib.oracle_selscan_step.restype = INT
         lib.oracle_selscan_step.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64]
+        lib.oracle_selscan_fwd_gated.restype = INT
+        lib.oracle_selscan_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT]
+        lib.oracle_selscan_fwd_chains_gated.restype = INT
+        lib.oracle_selscan_fwd_chains_gated.argtypes = [P, P, P, P, P, P, P, P, P, I64, P, P,
+                                                        I64, I64, I64, I64, INT, INT]
+        lib.oracle_selscan_step_gated.restype = INT
+        lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64]
         self._lib = lib
         self.path = path
 
@@ -78,12 +85,14 @@ class Oracle:
         """log(1 + e^u) in double."""
         return self._lib.oracle_softplus(float(u))
 
-    def selscan_fwd(self, x, delta, A, B, C, delta_softplus=False, h0=None, nthreads=0):
+    def selscan_fwd(self, x, delta, A, B, C, delta_softplus=False, h0=None, nthreads=0,
+                    Dskip=None, z=None):
         """Sequential selective scan in fp64.
 
         x, delta: (Bsz, L, D); A: (D, N); B, C: (Bsz, L, N); h0: (Bsz, D, N)
         or None. Inputs are taken as float32 (the exact values the GPU reads);
-        h0 as float64 (fp32 states widen exactly).
+        h0 as float64 (fp32 states widen exactly). Dskip (D,) and z
+        (Bsz, L, D) add the block's skip and gate: y = (y + Dskip x) silu(z).
         Returns (y (Bsz, L, D) float64, hT (Bsz, D, N) float64).
         """
         x = np.asarray(x)
@@ -95,17 +104,20 @@ class Oracle:
         B = _f32(B, (Bsz, L, N), "B")
         C = _f32(C, (Bsz, L, N), "C")
         h0 = None if h0 is None else _f64(h0, (Bsz, D, N), "h0")
+        Dskip = None if Dskip is None else _f32(Dskip, (D,), "Dskip")
+        z = None if z is None else _f32(z, (Bsz, L, D), "z")
         y = np.zeros((Bsz, L, D), np.float64)
         hT = np.zeros((Bsz, D, N), np.float64)
-        rc = self._lib.oracle_selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),
-                                          _ptr(y), _ptr(hT), Bsz, L, D, N,
-                                          int(bool(delta_softplus)), int(nthreads))
+        rc = self._lib.oracle_selscan_fwd_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                                _ptr(Dskip), _ptr(z), _ptr(h0),
+                                                _ptr(y), _ptr(hT), Bsz, L, D, N,
+                                                int(bool(delta_softplus)), int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_selscan_fwd failed")
         return y, hT
 
     def selscan_fwd_chains(self, x, delta, A, B, C, chains, delta_softplus=False, h0=None,
-                           nthreads=0):
+                           nthreads=0, Dskip=None, z=None):
         """The same scan for selected chains c = b * D + d only.
         Returns (y (nchains, L), hT (nchains, N)) in float64."""
         x = np.asarray(x)
@@ -121,19 +133,22 @@ class Oracle:
         nc = chains.shape[0]
         y = np.zeros((nc, L), np.float64)
         hT = np.zeros((nc, N), np.float64)
-        rc = self._lib.oracle_selscan_fwd_chains(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                                                 _ptr(h0), _ptr(chains), nc, _ptr(y), _ptr(hT),
-                                                 Bsz, L, D, N, int(bool(delta_softplus)),
-                                                 int(nthreads))
+        Dskip = None if Dskip is None else _f32(Dskip, (D,), "Dskip")
+        z = None if z is None else _f32(z, (Bsz, L, D), "z")
+        rc = self._lib.oracle_selscan_fwd_chains_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                                       _ptr(Dskip), _ptr(z), _ptr(h0), _ptr(chains), nc,
+                                                       _ptr(y), _ptr(hT), Bsz, L, D, N,
+                                                       int(bool(delta_softplus)), int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_selscan_fwd_chains failed")
         return y, hT
 
-    def selscan_step(self, state, x, delta, A, B, C, chains=None):
+    def selscan_step(self, state, x, delta, A, B, C, chains=None, Dskip=None, z=None):
         """One decode step in place on a float64 state.
 
         state: (Bsz, D, N) float64, or (nchains, N) when ``chains`` is given;
         x, delta: (Bsz, D); A: (D, N); B, C: (Bsz, N). delta is used as given.
+        Dskip (D,) and z (Bsz, D) add the block's skip and gate.
         Returns y: (Bsz, D) float64, or (nchains,) when ``chains`` is given.
         """
         if not (isinstance(state, np.ndarray) and state.dtype == np.float64
@@ -158,8 +173,11 @@ class Oracle:
             if state.shape != (nc, N):
                 raise ValueError("state shape")
             y = np.zeros((nc,), np.float64)
-        rc = self._lib.oracle_selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
-                                           _ptr(C), _ptr(y), _ptr(ch), nc, Bsz, D, N)
+        Dskip = None if Dskip is None else _f32(Dskip, (D,), "Dskip")
+        z = None if z is None else _f32(z, (Bsz, D), "z")
+        rc = self._lib.oracle_selscan_step_gated(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
+                                                 _ptr(C), _ptr(Dskip), _ptr(z), _ptr(y), _ptr(ch), nc,
+                                                 Bsz, D, N)
         if rc != 0:
             raise RuntimeError("oracle_selscan_step failed")
         return y

@@ -24,6 +24,13 @@
  * deltaB is the simplified dl * B of the listing, not the zero-order-hold
  * form (dA)^-1 (exp(dA) - I) dB of section 2.2.
  *
+ * Optionally (the *_gated entry points) the output of the block around the
+ * scan, as the MambaBlock listing of section 3.4 on the same page has it:
+ *   y[b,t,d] = (sum_n h[n] * C[b,t,n] + Dskip[d] * x[b,t,d]) * silu(z[b,t,d])
+ * with silu(z) = z / (1 + e^-z). The listing shows the gate and defines the
+ * per-channel parameter D (Dskip here) but elides where D enters; the skip is
+ * taken before the gate. Either term may be absent.
+ *
  * The decode step (the O(1)-state recurrent mode of section 6 on the same
  * page) is one iteration of the t-loop with L = 1, applied in place to a
  * caller-held state, with delta taken as given (no softplus).
@@ -57,10 +64,26 @@ double oracle_softplus(double u)
     return (u > 0.0 ? u : 0.0) + log1p(exp(-a));
 }
 
+/* The block's output around the scan's read-out y for element (b, t, d) at
+ * flat index btd: the skip term Dskip[d] * x, then the gate silu(z)
+ * = z / (1 + e^-z) (section 3.4). Dskip NULL: no skip; z NULL: no gate. */
+static double gate(double y, const float *Dskip, const float *z, int64_t d,
+                   int64_t btd, double xv)
+{
+    if (Dskip)
+        y += (double)Dskip[d] * xv;
+    if (z) {
+        double zv = (double)z[btd];
+        y *= zv / (1.0 + exp(-zv));
+    }
+    return y;
+}
+
 /* One (b, d) chain of the forward scan.
  * y_out[t * y_stride] receives y[b,t,d]; h_out[n] receives the final state. */
 static void scan_chain(const float *x, const float *delta, const float *A,
                        const float *B, const float *C, const double *h0,
+                       const float *Dskip, const float *z,
                        int64_t b, int64_t d, int64_t L, int64_t D, int64_t N,
                        int delta_softplus, double *y_out, int64_t y_stride,
                        double *h_out, double *h)
@@ -82,7 +105,7 @@ static void scan_chain(const float *x, const float *delta, const float *A,
         for (int64_t n = 0; n < N; ++n)
             acc += h[n] * (double)C[bt * N + n];
         if (y_out)
-            y_out[t * y_stride] = acc;
+            y_out[t * y_stride] = gate(acc, Dskip, z, d, bt * D + d, xv);
     }
     if (h_out)
         for (int64_t n = 0; n < N; ++n)
@@ -93,6 +116,7 @@ static void scan_chain(const float *x, const float *delta, const float *A,
 
 typedef struct {
     const float *x, *delta, *A, *B, *C;
+    const float *Dskip, *z;   /* optional block output (NULL: absent) */
     const double *h0;
     int64_t Bsz, L, D, N;
     int delta_softplus;
@@ -134,8 +158,8 @@ static void *fwd_worker(void *arg)
             y_stride = j->D;
             h_out = j->hT ? j->hT + c * j->N : NULL;
         }
-        scan_chain(j->x, j->delta, j->A, j->B, j->C, j->h0, b, d, j->L, j->D,
-                   j->N, j->delta_softplus, y_out, y_stride, h_out, h);
+        scan_chain(j->x, j->delta, j->A, j->B, j->C, j->h0, j->Dskip, j->z, b, d,
+                   j->L, j->D, j->N, j->delta_softplus, y_out, y_stride, h_out, h);
     }
     free(h);
     return NULL;
@@ -176,10 +200,28 @@ static int run_fwd(fwd_job *j, int nthreads)
  * y: (Bsz, L, D) double, may be NULL; hT: (Bsz, D, N) double, may be NULL;
  * h0: (Bsz, D, N) double or NULL for zeros. nthreads <= 0 uses every online
  * CPU. Returns 0, or -1 on bad arguments / allocation failure. */
+int oracle_selscan_fwd_gated(const float *x, const float *delta, const float *A,
+                             const float *B, const float *C, const float *Dskip,
+                             const float *z, const double *h0, double *y, double *hT,
+                             int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                             int delta_softplus, int nthreads);
+
 int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
                        const float *B, const float *C, const double *h0,
                        double *y, double *hT, int64_t Bsz, int64_t L,
                        int64_t D, int64_t N, int delta_softplus, int nthreads)
+{
+    return oracle_selscan_fwd_gated(x, delta, A, B, C, NULL, NULL, h0, y, hT,
+                                    Bsz, L, D, N, delta_softplus, nthreads);
+}
+
+/* The forward scan with the block's skip and gate (either may be NULL):
+ * Dskip (D), z (Bsz, L, D). */
+int oracle_selscan_fwd_gated(const float *x, const float *delta, const float *A,
+                             const float *B, const float *C, const float *Dskip,
+                             const float *z, const double *h0, double *y, double *hT,
+                             int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                             int delta_softplus, int nthreads)
 {
     if (Bsz < 0 || L < 0 || D < 0 || N < 0)
         return -1;
@@ -190,6 +232,7 @@ int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
     fwd_job j;
     memset(&j, 0, sizeof j);
     j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
+    j.Dskip = Dskip; j.z = z;
     j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
     j.delta_softplus = delta_softplus;
     j.chains = NULL;
@@ -201,12 +244,34 @@ int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
 /* Forward scan for a chosen set of chains only (chain c = b * D + d), for
  * sampled checks of sizes the full oracle would take too long on.
  * y_out: (nchains, L), hT_out: (nchains, N); either may be NULL. */
+int oracle_selscan_fwd_chains_gated(const float *x, const float *delta,
+                                    const float *A, const float *B, const float *C,
+                                    const float *Dskip, const float *z,
+                                    const double *h0, const int64_t *chains,
+                                    int64_t nchains, double *y_out, double *hT_out,
+                                    int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                                    int delta_softplus, int nthreads);
+
 int oracle_selscan_fwd_chains(const float *x, const float *delta,
                               const float *A, const float *B, const float *C,
                               const double *h0, const int64_t *chains,
                               int64_t nchains, double *y_out, double *hT_out,
                               int64_t Bsz, int64_t L, int64_t D, int64_t N,
                               int delta_softplus, int nthreads)
+{
+    return oracle_selscan_fwd_chains_gated(x, delta, A, B, C, NULL, NULL, h0, chains,
+                                           nchains, y_out, hT_out, Bsz, L, D, N,
+                                           delta_softplus, nthreads);
+}
+
+/* oracle_selscan_fwd_chains with the block's skip and gate. */
+int oracle_selscan_fwd_chains_gated(const float *x, const float *delta,
+                                    const float *A, const float *B, const float *C,
+                                    const float *Dskip, const float *z,
+                                    const double *h0, const int64_t *chains,
+                                    int64_t nchains, double *y_out, double *hT_out,
+                                    int64_t Bsz, int64_t L, int64_t D, int64_t N,
+                                    int delta_softplus, int nthreads)
 {
     if (Bsz < 0 || L < 0 || D < 0 || N < 0 || nchains < 0 || (nchains && !chains))
         return -1;
@@ -216,6 +281,7 @@ int oracle_selscan_fwd_chains(const float *x, const float *delta,
     fwd_job j;
     memset(&j, 0, sizeof j);
     j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
+    j.Dskip = Dskip; j.z = z;
     j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
     j.delta_softplus = delta_softplus;
     j.chains = chains;
@@ -229,10 +295,27 @@ int oracle_selscan_fwd_chains(const float *x, const float *delta,
  *   A : (D, N)        B, C : (Bsz, N)          y : (Bsz, D) double
  * delta is used as given. When chains != NULL only those chains are
  * updated, with state packed as (nchains, N) and y as (nchains). */
+int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
+                              const float *A, const float *B, const float *C,
+                              const float *Dskip, const float *z, double *y,
+                              const int64_t *chains, int64_t nchains,
+                              int64_t Bsz, int64_t D, int64_t N);
+
 int oracle_selscan_step(double *state, const float *x, const float *delta,
                         const float *A, const float *B, const float *C,
                         double *y, const int64_t *chains, int64_t nchains,
                         int64_t Bsz, int64_t D, int64_t N)
+{
+    return oracle_selscan_step_gated(state, x, delta, A, B, C, NULL, NULL, y,
+                                     chains, nchains, Bsz, D, N);
+}
+
+/* oracle_selscan_step with the block's skip and gate: Dskip (D), z (Bsz, D). */
+int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
+                              const float *A, const float *B, const float *C,
+                              const float *Dskip, const float *z, double *y,
+                              const int64_t *chains, int64_t nchains,
+                              int64_t Bsz, int64_t D, int64_t N)
 {
     if (!state || !x || !delta || !A || !B || !C || Bsz < 0 || D < 0 || N < 0)
         return -1;
@@ -254,7 +337,7 @@ int oracle_selscan_step(double *state, const float *x, const float *delta,
         for (int64_t n = 0; n < N; ++n)
             acc += h[n] * (double)C[b * N + n];
         if (y)
-            y[i] = acc;
+            y[i] = gate(acc, Dskip, z, d, b * D + d, xv);
     }
     return 0;
 }

@@ -50,6 +50,21 @@ MUTATIONS = {
     "softplus_flag_ignored": ("        if (delta_softplus)\n            dl = oracle_softplus(dl);\n", ""),
     "step_wrong_decay": ("            double dA = exp(dl * (double)A[d * N + n]);\n            double dB = dl * (double)B[b * N + n];",
                          "            double dA = exp(dl * (double)A[n]);\n            double dB = dl * (double)B[b * N + n];"),
+    "gate_sign": ("y *= zv / (1.0 + exp(-zv));", "y *= zv / (1.0 + exp(zv));"),
+    "gate_without_z": ("y *= zv / (1.0 + exp(-zv));", "y *= 1.0 / (1.0 + exp(-zv));"),
+    "skip_dropped": ("        y += (double)Dskip[d] * xv;\n", ""),
+    "skip_wrong_channel": ("y += (double)Dskip[d] * xv;", "y += (double)Dskip[0] * xv;"),
+    "skip_after_gate": ("""    if (Dskip)
+        y += (double)Dskip[d] * xv;
+    if (z) {
+        double zv = (double)z[btd];
+        y *= zv / (1.0 + exp(-zv));
+    }""", """    if (z) {
+        double zv = (double)z[btd];
+        y *= zv / (1.0 + exp(-zv));
+    }
+    if (Dskip)
+        y += (double)Dskip[d] * xv;"""),
     "step_dropped_input": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];",
                            "            h[n] = dA * h[n];\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];"),
 }

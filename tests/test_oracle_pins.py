@@ -364,3 +364,67 @@ def test_workload_inputs_feed_oracle(orc):
     i = W.workload_inputs(1)
     y, hT = orc.selscan_fwd(i.f32("x"), i.f32("delta"), i.A, i.f32("B"), i.f32("C"), True)
     assert y.shape == (1, 64, 16) and np.all(np.isfinite(y))
+
+
+# ---- the block's skip and gate around the scan (section 3.4, MambaBlock) ----
+
+def gate_inputs(Bsz, L, D, seed):
+    g = np.random.default_rng(seed)
+    Dskip = (0.5 + g.random(D)).astype(np.float32)
+    z = (2.0 * g.standard_normal((Bsz, L, D))).astype(np.float32)
+    return Dskip, z
+
+
+def test_gate_with_zero_readout_is_skip_times_silu(orc):
+    """C = 0 silences the scan: the block's output is Dskip[d] x silu(z), with
+    silu(z) = z * sigmoid(z) from scipy's logistic function."""
+    from scipy.special import expit
+    x, u, A, B, C, _ = rand_inputs(2, 20, 5, 4, seed=31)
+    Dskip, z = gate_inputs(2, 20, 5, seed=32)
+    y, _ = orc.selscan_fwd(x, u, A, B, np.zeros_like(C), True, Dskip=Dskip, z=z)
+    zz = z.astype(np.float64)
+    ref = Dskip.astype(np.float64)[None, None, :] * x.astype(np.float64) * zz * expit(zz)
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_skip_without_gate_adds_Dx_to_the_scan(orc):
+    x, u, A, B, C, hh = rand_inputs(2, 30, 6, 4, seed=33, h0=True)
+    Dskip, _ = gate_inputs(2, 30, 6, seed=34)
+    y0, h0 = orc.selscan_fwd(x, u, A, B, C, True, hh)
+    y1, h1 = orc.selscan_fwd(x, u, A, B, C, True, hh, Dskip=Dskip)
+    assert np.array_equal(h0, h1)                      # the state does not see the skip
+    assert np.allclose(y1, y0 + Dskip[None, None, :].astype(np.float64) * x, rtol=1e-14, atol=1e-14)
+
+
+def test_gate_odd_part_is_identity(orc):
+    """silu(z) - silu(-z) = z for every z, so gating with z and with -z differ
+    by exactly (scan + skip) * z."""
+    x, u, A, B, C, hh = rand_inputs(2, 25, 5, 3, seed=35, h0=True)
+    Dskip, z = gate_inputs(2, 25, 5, seed=36)
+    yp, _ = orc.selscan_fwd(x, u, A, B, C, True, hh, Dskip=Dskip, z=z)
+    yn, _ = orc.selscan_fwd(x, u, A, B, C, True, hh, Dskip=Dskip, z=-z)
+    ys, _ = orc.selscan_fwd(x, u, A, B, C, True, hh, Dskip=Dskip)
+    assert np.allclose(yp - yn, ys * z.astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
+def test_gate_limits(orc):
+    """silu(0) = 0 silences the block; silu(z) -> z for large z."""
+    x, u, A, B, C, _ = rand_inputs(1, 12, 4, 4, seed=37)
+    Dskip, _ = gate_inputs(1, 12, 4, seed=38)
+    y0, _ = orc.selscan_fwd(x, u, A, B, C, True, Dskip=Dskip, z=np.zeros_like(x))
+    assert np.array_equal(y0, np.zeros_like(y0))
+    ys, _ = orc.selscan_fwd(x, u, A, B, C, True, Dskip=Dskip)
+    y40, _ = orc.selscan_fwd(x, u, A, B, C, True, Dskip=Dskip, z=np.full_like(x, 40.0))
+    assert np.allclose(y40, 40.0 * ys, rtol=1e-15, atol=0)
+
+
+def test_gated_steps_equal_gated_forward(orc):
+    Bsz, L, D, N = 2, 9, 4, 5
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=39, softplus=False, h0=True)
+    Dskip, z = gate_inputs(Bsz, L, D, seed=40)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, False, hh, Dskip=Dskip, z=z)
+    st = hh.copy()
+    for t in range(L):
+        yt = orc.selscan_step(st, x[:, t], u[:, t], A, B[:, t], C[:, t], Dskip=Dskip, z=z[:, t])
+        assert np.allclose(yt, y[:, t], rtol=1e-13, atol=1e-13)
+    assert np.allclose(st, hT, rtol=1e-13, atol=1e-13)
