@@ -104,6 +104,32 @@ int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
                 float *hT, void *stream);
 
 /*
+ * selscan_fwd_gated -- selscan_fwd with the block's output around the scan
+ * fused into the read-out (youngju.dev "Mamba: Selective State Space
+ * Models", section 3.4, the MambaBlock listing):
+ *
+ *   y[b,t,d] = (sum_n h[n] * C[b,t,n] + Dskip[d] * x[b,t,d]) * silu(z[b,t,d])
+ *   silu(z)  = z / (1 + e^-z)
+ *
+ *   Dskip : (D) fp32 or NULL    the per-channel skip parameter (D in the
+ *                               listing); NULL = no skip term
+ *   z     : (Bsz, L, D), dtype  the gate input; NULL = no gate
+ *
+ * The listing shows the gate and defines the skip parameter but elides where
+ * it is applied; the skip is added before the gate. The final state hT does
+ * not see either term. Everything else (shapes, sizes, aliasing, memory,
+ * errors) is as for selscan_fwd; y may also equal z exactly, and neither
+ * may partially overlap y or hT. With both NULL this is selscan_fwd.
+ * The fused kernel applies them in its read-out when the rows are 16-byte
+ * aligned and delta_softplus is set; other cases take the plain-load
+ * kernels, with the same results.
+ */
+int selscan_fwd_gated(const void *x, const void *delta, const float *A, const void *B,
+                      const void *C, const float *Dskip, const void *z, void *y,
+                      int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype,
+                      int delta_softplus, const float *h0, float *hT, void *stream);
+
+/*
  * selscan_step -- one decode step of the recurrent mode, O(1) state per
  * token (youngju.dev section 6: inference O(1) per token with a fixed
  * state; the same update as selscan_fwd with L = 1).
@@ -122,6 +148,14 @@ int selscan_fwd(const void *x, const void *delta, const float *A, const void *B,
 int selscan_step(float *state, const float *x, const float *delta, const float *A,
                  const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
                  int64_t N, void *stream);
+
+/* selscan_step with the block's skip and gate on the step's output, as in
+ * selscan_fwd_gated: y = (sum_n state'[n] * C[n] + Dskip[d] * x) * silu(z).
+ * Dskip (D) and z (Bsz, D) are fp32 device pointers or NULL; the state does
+ * not see either term. Neither may overlap y or state. */
+int selscan_step_gated(float *state, const float *x, const float *delta, const float *A,
+                       const float *B, const float *C, const float *Dskip, const float *z,
+                       float *y, int64_t Bsz, int64_t D, int64_t N, void *stream);
 
 /*
  * selscan_fwd_noalloc -- selscan_fwd for callers that cannot allocate device

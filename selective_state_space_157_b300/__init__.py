@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
         L.selscan_version.argtypes = []
         L.selscan_fwd_noalloc.restype = INT
         L.selscan_fwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_fwd_gated.restype = INT
+        L.selscan_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_step_gated.restype = INT
+        L.selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, P]
         L.selscan_fwd_host.restype = INT
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
@@ -141,16 +145,23 @@ def _need(t, name, shape, dtype, device):
 
 
 def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
-                return_final_state: bool = False, y=None, hT=None, stream=None):
+                return_final_state: bool = False, y=None, hT=None, stream=None,
+                D_skip=None, z=None):
     """Forward selective scan (see ``include/selscan.h``).
 
     x, delta: (Bsz, L, D) float32 or bfloat16; A: (D, N) float32;
     B, C: (Bsz, L, N) same dtype as x; h0: (Bsz, D, N) float32 or None.
     Returns y (Bsz, L, D), or (y, hT) with hT (Bsz, D, N) float32 when
     ``return_final_state``. ``y`` / ``hT`` may be passed preallocated.
+    ``D_skip`` (D,) float32 and ``z`` (like x) add the block's skip and gate
+    (selscan_fwd_gated): y = (scan + D_skip * x) * silu(z). Device tensors
+    only for those.
     """
     import torch
+    gated = D_skip is not None or z is not None
     if x.device.type == "cpu":
+        if gated:
+            raise ValueError("D_skip / z are supported for device tensors only")
         return _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT)
     dev = x.device
     Bsz, L, D = x.shape
@@ -171,10 +182,19 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
         hT = torch.empty((Bsz, D, N), dtype=torch.float32, device=dev)
     if hT is not None:
         _need(hT, "hT", (Bsz, D, N), torch.float32, dev)
+    if D_skip is not None:
+        _need(D_skip, "D_skip", (D,), torch.float32, dev)
+    if z is not None:
+        _need(z, "z", (Bsz, L, D), x.dtype, dev)
     with torch.cuda.device(dev):
-        rc = lib().selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
-                               Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
-                               _stream_ptr(stream))
+        if gated:
+            rc = lib().selscan_fwd_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D_skip),
+                                         _ptr(z), _ptr(y), Bsz, L, D, N, code, int(bool(delta_softplus)),
+                                         _ptr(h0), _ptr(hT), _stream_ptr(stream))
+        else:
+            rc = lib().selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
+                                   Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
+                                   _stream_ptr(stream))
     _check(rc)
     return (y, hT) if (return_final_state or hT is not None) else y
 
@@ -206,12 +226,16 @@ def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=N
     return y
 
 
-def selscan_step(state, x, delta, A, B, C, y=None, stream=None):
+def selscan_step(state, x, delta, A, B, C, y=None, stream=None, D_skip=None, z=None):
     """One decode step (see ``include/selscan.h``): ``state`` (Bsz, D, N)
     float32 is updated in place; returns y (Bsz, D) float32. delta is used
-    as given (no softplus)."""
+    as given (no softplus). ``D_skip`` (D,) and ``z`` (Bsz, D) add the
+    block's skip and gate (selscan_step_gated; device tensors only)."""
     import torch
+    gated = D_skip is not None or z is not None
     if state.device.type == "cpu":
+        if gated:
+            raise ValueError("D_skip / z are supported for device tensors only")
         return _step_host(state, x, delta, A, B, C, y)
     dev = state.device
     Bsz, D, N = state.shape
@@ -226,9 +250,17 @@ def selscan_step(state, x, delta, A, B, C, y=None, stream=None):
         y = torch.empty((Bsz, D), dtype=f, device=dev)
     else:
         _need(y, "y", (Bsz, D), f, dev)
+    if D_skip is not None:
+        _need(D_skip, "D_skip", (D,), f, dev)
+    if z is not None:
+        _need(z, "z", (Bsz, D), f, dev)
     with torch.cuda.device(dev):
-        rc = lib().selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                                _ptr(y), Bsz, D, N, _stream_ptr(stream))
+        if gated:
+            rc = lib().selscan_step_gated(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                          _ptr(D_skip), _ptr(z), _ptr(y), Bsz, D, N, _stream_ptr(stream))
+        else:
+            rc = lib().selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                    _ptr(y), Bsz, D, N, _stream_ptr(stream))
     _check(rc)
     return y
 

@@ -43,6 +43,21 @@ __device__ __forceinline__ float softplus(float u)
     return fmaf(p, e, fmaxf(u, 0.0f));
 }
 
+// The block's output around the scan's read-out (youngju.dev "Mamba:
+// Selective State Space Models", section 3.4, the MambaBlock listing): the
+// per-channel skip term dsk * x, then the gate silu(z) = z / (1 + e^-z).
+// ex2 of a large positive argument gives +inf and the quotient 0, the limit.
+__device__ __forceinline__ float silu(float z)
+{
+    return __fdividef(z, 1.0f + ex2(-z * kLog2e));
+}
+
+__device__ __forceinline__ float block_out(float y, float dsk, float x, bool gated, float z)
+{
+    y = fmaf(dsk, x, y);
+    return gated ? y * silu(z) : y;
+}
+
 template <typename T> struct Io;
 
 template <> struct Io<float> {

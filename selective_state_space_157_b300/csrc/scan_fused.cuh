@@ -39,6 +39,7 @@ namespace selscan {
 
 struct FusedArgs {
     CUtensorMap mx, md, mB, mC;
+    CUtensorMap mz;       // the gate's z, like x (GATE kernels with z only)
     ScanArgs s;
     float *aggS;          // (K-1, Bsz, D): sum of dl over the chunk
     float *aggH;          // (K-1, Bsz, D, N): chunk end state from zero
@@ -114,7 +115,9 @@ __device__ __forceinline__ void load_state_cg(const float *p, int valid, float2 
     }
 }
 
-template <typename T, int NS, int NSPLIT, bool VEC, int TT, bool SOFTPLUS>
+// GATE: the readout also applies the block's skip and gate (block_out),
+// with z staged beside x in the ring.
+template <typename T, int NS, int NSPLIT, bool VEC, int TT, bool SOFTPLUS, bool GATE>
 // Three CTAs per SM fit the shared-memory ring; the register cap this implies
 // (168) is above what the kernel needs, and measured faster than 128.
 __global__ void __launch_bounds__(kScanThreads, 3)
@@ -134,7 +137,11 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     const int64_t N = a.N, D = a.D, L = a.L;
     const int xbytes = TT * DPB * (int)sizeof(T);
     const int nbytes = TT * (int)Nrow * (int)sizeof(T);
-    const int sbytes = 2 * xbytes + 2 * nbytes;
+    const int sbytes = 2 * xbytes + 2 * nbytes + (GATE ? xbytes : 0);
+    const bool has_z = GATE && a.z != nullptr;
+    // Bytes a stage brings: x, delta and B, plus C (and z) for a readout.
+    const int agg_bytes = 2 * xbytes + nbytes;
+    const int ro_bytes = 2 * xbytes + 2 * nbytes + (has_z ? xbytes : 0);
     constexpr bool kBf16 = sizeof(T) == 2;
     const int cfloats = kBf16 ? 2 * TT * (int)Nrow : 0;   // fp32 copy of a stage's B and C rows
     float *conv_buf = reinterpret_cast<float *>(smem + STAGES * sbytes);
@@ -198,12 +205,14 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             unsigned char *p = buf(r);
             const int t = (int)(t0 + (int64_t)i * TT);
             issued[s] += 1;
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(readout ? sbytes : sbytes - nbytes));
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(readout ? ro_bytes : agg_bytes));
             tma_load_3d(p, &fa.mx, &full[s], d0, t, (int)b);
             tma_load_3d(p + xbytes, &fa.md, &full[s], d0, t, (int)b);
             tma_load_3d(p + 2 * xbytes, &fa.mB, &full[s], 0, t, (int)b);
             if (readout)
                 tma_load_3d(p + 2 * xbytes + nbytes, &fa.mC, &full[s], 0, t, (int)b);
+            if (readout && has_z)
+                tma_load_3d(p + 2 * xbytes + 2 * nbytes, &fa.mz, &full[s], d0, t, (int)b);
         };
 
         // Every warp finished the previous item: its buffers may be refilled.
@@ -213,6 +222,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 issue(ring + f, f);
         }
 
+        const float dsk = (GATE && readout && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
         float2 A2[NP];
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
@@ -316,6 +326,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 const unsigned char *p = buf(r);
                 const T *xs = reinterpret_cast<const T *>(p) + grp;
                 const T *ds = reinterpret_cast<const T *>(p + xbytes) + grp;
+                const T *zs = reinterpret_cast<const T *>(p + 2 * xbytes + 2 * nbytes) + grp;
                 // B and C rows in fp32: straight from the tile, or (bf16
                 // input) from this stage's fp32 copy, which the four warps
                 // convert together -- every thread needs every row, so
@@ -429,6 +440,9 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 #pragma unroll
                         for (int o = NSPLIT / 2; o > 0; o >>= 1)
                             yv += __shfl_xor_sync(0xffffffffu, yv, o);
+                        if constexpr (GATE)
+                            yv = block_out(yv, dsk, smem_val(xs + tt * DPB), has_z,
+                                           has_z ? smem_val(zs + tt * DPB) : 0.0f);
                         if (active && q == 0)
                             Io<T>::store(yp + tt * D, yv);
                     } else {
@@ -476,6 +490,9 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 #pragma unroll
                             for (int o = NSPLIT / 2; o > 0; o >>= 1)
                                 yv += __shfl_xor_sync(0xffffffffu, yv, o);
+                            if constexpr (GATE)
+                                yv = block_out(yv, dsk, smem_val(xs + tt * DPB), has_z,
+                                               has_z ? smem_val(zs + tt * DPB) : 0.0f);
                             if (active && q == 0)
                                 Io<T>::store(yp + tt * D, yv);
                         }
@@ -543,9 +560,9 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     }
 }
 
-inline size_t fused_smem_bytes(size_t es, int TT, int DPB, int64_t Nrow, int stages)
+inline size_t fused_smem_bytes(size_t es, int TT, int DPB, int64_t Nrow, int stages, bool gate)
 {
-    const size_t stage = (2 * (size_t)TT * DPB + 2 * (size_t)TT * (size_t)Nrow) * es;
+    const size_t stage = ((gate ? 3 : 2) * (size_t)TT * DPB + 2 * (size_t)TT * (size_t)Nrow) * es;
     const size_t conv = es == 2 ? 2 * (size_t)TT * (size_t)Nrow * 4 : 0;
     return (size_t)stages * (stage + conv) + (size_t)stages * (8 + 8 + 8 + 4) + 16;
 }

@@ -37,6 +37,8 @@ struct ScanArgs {
     const void *x, *delta, *B, *C;
     const float *A;
     void *y;
+    const float *Dskip;   // (D) or null: the block's skip term Dskip[d] * x
+    const void *z;        // (Bsz, L, D) like x, or null: the block's gate silu(z)
     const float *h0;   // (Bsz, D, N) or null
     float *hT;         // (Bsz, D, N) or null
     float *agg_h;      // (K-1, Bsz, D, N): chunk end states from zero; overwritten by carries
@@ -102,6 +104,9 @@ scan_chunk_kernel(const ScanArgs a)
     const T *Bp = static_cast<const T *>(a.B) + (b * L + t0) * N + n0;
     const T *Cp = static_cast<const T *>(a.C) + (b * L + t0) * N + n0;
     T *yp = static_cast<T *>(a.y) + (b * L + t0) * D + d;
+    const T *zp = a.z ? static_cast<const T *>(a.z) + (b * L + t0) * D + d : nullptr;
+    const bool block = READOUT && (a.Dskip || a.z);
+    const float dsk = (READOUT && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
 
     float s = 0.0f, s_err = 0.0f;   // compensated sum of dl (aggregate pass)
 
@@ -136,6 +141,10 @@ scan_chunk_kernel(const ScanArgs a)
 #pragma unroll
             for (int o = NSPLIT / 2; o > 0; o >>= 1)
                 yv += __shfl_xor_sync(0xffffffffu, yv, o);
+            if (block) {
+                yv = block_out(yv, dsk, xv, zp != nullptr, zp ? Io<T>::load(zp) : 0.0f);
+                if (zp) zp += D;
+            }
             if (active && q == 0)
                 Io<T>::store(yp, yv);
             Cp += N;

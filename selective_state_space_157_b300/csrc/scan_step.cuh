@@ -21,8 +21,18 @@ struct StepArgs {
     float *state;
     const float *x, *delta, *A, *B, *C;
     float *y;
+    const float *Dskip;   // (D) or null: the block's skip term
+    const float *z;       // (Bsz, D) or null: the block's gate
     int64_t Bsz, D, N;
 };
+
+// The block's skip and gate on a chain's read-out (block_out), if asked for.
+__device__ __forceinline__ float step_block(const StepArgs &a, float yv, float xv, int64_t chain, int64_t d)
+{
+    if (!a.Dskip && !a.z)
+        return yv;
+    return block_out(yv, a.Dskip ? __ldg(a.Dskip + d) : 0.0f, xv, a.z != nullptr, a.z ? __ldg(a.z + chain) : 0.0f);
+}
 
 // V 16-byte groups (4V states) per lane, G lanes per chain (N = 4 V G).
 template <int G, int V>
@@ -47,7 +57,8 @@ __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a
         C4[v] = __ldg(reinterpret_cast<const float4 *>(a.C) + (b * G + q) * V + v);
     }
     const float dl = __ldg(a.delta + chain);
-    const float u = dl * __ldg(a.x + chain);
+    const float xv = __ldg(a.x + chain);
+    const float u = dl * xv;
     const float dk = dl * kLog2e;
 
     float yv = 0.0f;
@@ -67,7 +78,7 @@ __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a
         for (int v = 0; v < V; ++v)
             __stcs(sp + v, s[v]);   // written once: streaming
         if (q == 0)
-            a.y[chain] = yv;
+            a.y[chain] = step_block(a, yv, xv, chain, d);
     }
 }
 
@@ -79,7 +90,8 @@ __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const StepArg
         return;
     const int64_t b = chain / a.D, d = chain - b * a.D;
     const float dl = a.delta[chain];
-    const float u = dl * a.x[chain];
+    const float xv = a.x[chain];
+    const float u = dl * xv;
     const float dk = dl * kLog2e;
     float *sp = a.state + chain * a.N;
     const float *Ap = a.A + d * a.N;
@@ -91,7 +103,7 @@ __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const StepArg
         sp[n] = s;
         yv = fmaf(s, Cp[n], yv);
     }
-    a.y[chain] = yv;
+    a.y[chain] = step_block(a, yv, xv, chain, d);
 }
 
 } // namespace selscan

@@ -227,16 +227,16 @@ int occupancy(const void *fn, size_t smem)
     return n;
 }
 
-template <typename T, int NS, int NSPLIT, bool VEC, bool SP>
+template <typename T, int NS, int NSPLIT, bool VEC, bool SP, bool GATE = false>
 bool prepare_fused_sp(int64_t N, FusedLaunch *out)
 {
     constexpr int DPB = kScanThreads / NSPLIT;
     long stages = env_long("SELSCAN_TMA_STAGES", kStages);
     if (stages < 2) stages = 2;
     if (stages > kMaxStages) stages = kMaxStages;
-    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP>;
+    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP, GATE>;
     const int64_t nrow = VEC ? NS * NSPLIT : N;
-    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, (int)stages);
+    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, (int)stages, GATE);
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return false;
@@ -245,9 +245,13 @@ bool prepare_fused_sp(int64_t N, FusedLaunch *out)
     return true;
 }
 
+// The block's skip and gate run fused on the vectorised, softplus form (the
+// block's own use); other gated forms take the plain-load path.
 template <typename T, int NS, int NSPLIT>
-bool prepare_fused(bool vec, bool softplus, int64_t N, FusedLaunch *out)
+bool prepare_fused(bool vec, bool softplus, bool gate, int64_t N, FusedLaunch *out)
 {
+    if (gate)
+        return vec && softplus && prepare_fused_sp<T, NS, NSPLIT, true, true, true>(N, out);
     if (vec)
         return softplus ? prepare_fused_sp<T, NS, NSPLIT, true, true>(N, out)
                         : prepare_fused_sp<T, NS, NSPLIT, true, false>(N, out);
@@ -256,16 +260,16 @@ bool prepare_fused(bool vec, bool softplus, int64_t N, FusedLaunch *out)
 }
 
 template <typename T>
-bool pick_fused(int ns, int nsplit, bool vec, bool softplus, int64_t N, FusedLaunch *out)
+bool pick_fused(int ns, int nsplit, bool vec, bool softplus, bool gate, int64_t N, FusedLaunch *out)
 {
     switch (ns * 100 + nsplit) {
-    case 401: return prepare_fused<T, 4, 1>(vec, softplus, N, out);
-    case 801: return prepare_fused<T, 8, 1>(vec, softplus, N, out);
-    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, N, out);
-    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, N, out);
-    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, N, out);
-    case 802: return prepare_fused<T, 8, 2>(vec, softplus, N, out);
-    case 404: return prepare_fused<T, 4, 4>(vec, softplus, N, out);
+    case 401: return prepare_fused<T, 4, 1>(vec, softplus, gate, N, out);
+    case 801: return prepare_fused<T, 8, 1>(vec, softplus, gate, N, out);
+    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, gate, N, out);
+    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, gate, N, out);
+    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, gate, N, out);
+    case 802: return prepare_fused<T, 8, 2>(vec, softplus, gate, N, out);
+    case 404: return prepare_fused<T, 4, 4>(vec, softplus, gate, N, out);
     default: return false;
     }
 }
@@ -380,8 +384,10 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
 {
     FusedLaunch fl;
     const bool sp = a.softplus != 0;
-    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, a.N, &fl)
-                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, a.N, &fl);
+    const bool gate = a.Dskip != nullptr || a.z != nullptr;
+    if (a.z && !aligned(a.z, 16)) return SELSCAN_ERR_UNSUPPORTED;
+    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, gate, a.N, &fl)
+                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, gate, a.N, &fl);
     if (!ok) return SELSCAN_ERR_UNSUPPORTED;
     FusedArgs fa;
     memset(&fa, 0, sizeof fa);
@@ -392,7 +398,8 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
     if (!(encode_3d(&fa.mx, dt, es, a.x, a.D, a.L, a.Bsz, dpb, tt) &&
           encode_3d(&fa.md, dt, es, a.delta, a.D, a.L, a.Bsz, dpb, tt) &&
           encode_3d(&fa.mB, dt, es, a.B, a.N, a.L, a.Bsz, (uint32_t)a.N, tt) &&
-          encode_3d(&fa.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt)))
+          encode_3d(&fa.mC, dt, es, a.C, a.N, a.L, a.Bsz, (uint32_t)a.N, tt) &&
+          (!a.z || encode_3d(&fa.mz, dt, es, a.z, a.D, a.L, a.Bsz, dpb, tt))))
         return SELSCAN_ERR_UNSUPPORTED;
     fa.s = a;
     fa.stages = fl.stages;
@@ -467,7 +474,7 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, in
 // *empty is set when there is nothing to compute (Bsz == 0 or D == 0).
 int check_fwd_args(const void *x, const void *delta, const float *A, const void *B, const void *C,
                    const void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, const float *h0,
-                   const float *hT, bool *empty)
+                   const float *hT, bool *empty, const float *Dskip = nullptr, const void *z = nullptr)
 {
     *empty = false;
     if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
@@ -493,11 +500,12 @@ int check_fwd_args(const void *x, const void *delta, const float *A, const void 
     if (L > 0) {
         if (!x || !delta || !B || !C || !y)
             return fail(SELSCAN_ERR_INVALID_ARG, "x, delta, B, C and y must be non-NULL when L > 0");
-        if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) || !aligned(y, es))
-            return fail(SELSCAN_ERR_INVALID_ARG, "x, delta, B, C, y must be aligned to their element size");
+        if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) || !aligned(y, es) ||
+            !aligned(z, es))
+            return fail(SELSCAN_ERR_INVALID_ARG, "x, delta, B, C, y, z must be aligned to their element size");
     }
-    if (!aligned(A, 4) || !aligned(h0, 4) || !aligned(hT, 4))
-        return fail(SELSCAN_ERR_INVALID_ARG, "A, h0, hT must be 4-byte aligned");
+    if (!aligned(A, 4) || !aligned(h0, 4) || !aligned(hT, 4) || !aligned(Dskip, 4))
+        return fail(SELSCAN_ERR_INVALID_ARG, "A, h0, hT, Dskip must be 4-byte aligned");
 
     const Range ry = range(L > 0 ? y : nullptr, nld * es, "y"), rhT = range(hT, ndn * 4, "hT");
     struct Input {
@@ -509,6 +517,7 @@ int check_fwd_args(const void *x, const void *delta, const float *A, const void 
         {range(x, nld * es, "x"), true, false},      {range(delta, nld * es, "delta"), true, false},
         {range(B, nln * es, "B"), false, false},     {range(C, nln * es, "C"), false, false},
         {range(A, D * N * 4, "A"), false, false},    {range(h0, ndn * 4, "h0"), false, true},
+        {range(L > 0 ? z : nullptr, nld * es, "z"), true, false}, {range(Dskip, D * 4, "Dskip"), false, false},
     };
     for (const Input &in : ins) {
         if (overlaps(ry, in.r) && !(in.y_may_equal && in.r.lo == ry.lo))
@@ -539,9 +548,18 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
                            const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
                            int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
 {
+    return selscan_fwd_gated(x, delta, A, B, C, nullptr, nullptr, y, Bsz, L, D, N, dtype, delta_softplus,
+                             h0, hT, stream);
+}
+
+extern "C" int selscan_fwd_gated(const void *x, const void *delta, const float *A, const void *B,
+                                 const void *C, const float *Dskip, const void *z, void *y, int64_t Bsz,
+                                 int64_t L, int64_t D, int64_t N, int dtype, int delta_softplus,
+                                 const float *h0, float *hT, void *stream)
+{
     g_err[0] = '\0';
     bool empty = false;
-    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty);
+    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty, Dskip, z);
     if (rc != SELSCAN_OK || empty) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (L == 0) return empty_sequence_state(h0, hT, Bsz, D, N, st);
@@ -556,6 +574,7 @@ extern "C" int selscan_fwd(const void *x, const void *delta, const float *A, con
     memset(&a, 0, sizeof a);
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
+    a.Dskip = Dskip; a.z = z;
     a.softplus = delta_softplus ? 1 : 0;
     return launch_fwd(a, plan, dtype, dev, sms, st);
 }
@@ -827,6 +846,13 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
                             const float *B, const float *C, float *y, int64_t Bsz, int64_t D,
                             int64_t N, void *stream)
 {
+    return selscan_step_gated(state, x, delta, A, B, C, nullptr, nullptr, y, Bsz, D, N, stream);
+}
+
+extern "C" int selscan_step_gated(float *state, const float *x, const float *delta, const float *A,
+                                  const float *B, const float *C, const float *Dskip, const float *z,
+                                  float *y, int64_t Bsz, int64_t D, int64_t N, void *stream)
+{
     g_err[0] = '\0';
     if (Bsz < 0 || D < 0)
         return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld D=%lld)", (long long)Bsz, (long long)D);
@@ -841,13 +867,14 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
         return SELSCAN_OK;
     if (!state || !x || !delta || !A || !B || !C || !y)
         return fail(SELSCAN_ERR_INVALID_ARG, "state, x, delta, A, B, C and y must be non-NULL");
-    const void *ptrs[] = {state, x, delta, A, B, C, y};
+    const void *ptrs[] = {state, x, delta, A, B, C, y, Dskip, z};
     for (const void *p : ptrs)
         if (!aligned(p, 4))
             return fail(SELSCAN_ERR_INVALID_ARG, "every pointer must be 4-byte aligned");
     const Range rs = range(state, ndn * 4, "state"), ry = range(y, nd1 * 4, "y");
     const Range ins[] = {range(x, nd1 * 4, "x"), range(delta, nd1 * 4, "delta"), range(A, D * N * 4, "A"),
-                         range(B, Bsz * N * 4, "B"), range(C, Bsz * N * 4, "C")};
+                         range(B, Bsz * N * 4, "B"), range(C, Bsz * N * 4, "C"),
+                         range(Dskip, D * 4, "Dskip"), range(z, nd1 * 4, "z")};
     for (const Range &r : ins) {
         if (overlaps(rs, r)) return fail(SELSCAN_ERR_INVALID_ARG, "state overlaps %s", r.name);
         if (overlaps(ry, r)) return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps %s", r.name);
@@ -856,7 +883,7 @@ extern "C" int selscan_step(float *state, const float *x, const float *delta, co
         return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps state");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    StepArgs a{state, x, delta, A, B, C, y, Bsz, D, N};
+    StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N};
     const int64_t chains = Bsz * D;
     // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
     // must divide the warp so that a chain's lanes never straddle two warps.

@@ -29,7 +29,7 @@ F32 = "f32"
 BF16 = "bf16"
 
 # tensor ids of the per-tensor random streams
-_TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6}
+_TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6, "Dskip": 7, "z": 8}
 
 
 @dataclass(frozen=True)
@@ -172,3 +172,15 @@ def decode_step_inputs(w: Workload, k: int):
     B = normal(rng(w.seed, _TID["B"], k), (w.Bsz, w.N))
     C = normal(rng(w.seed, _TID["C"], k), (w.Bsz, w.N))
     return x, delta, B, C
+
+
+def gate_inputs(Bsz: int, L: int, D: int, *, seed: int, dtype: str = F32, steps: bool = False):
+    """Inputs of the block's skip and gate around the scan: Dskip (D,) fp32
+    drawn around the listing's initial value of ones, U(0.5, 1.5); z ~ N(0, 1)
+    shaped like x, (Bsz, L, D) (or (Bsz, D) for a decode step when L is
+    ignored and ``steps`` is set), as bf16 bit patterns for bf16 I/O."""
+    Dskip = rng(seed, _TID["Dskip"]).uniform(0.5, 1.5, size=(D,)).astype(np.float32)
+    z = normal(rng(seed, _TID["z"]), (Bsz, D) if steps else (Bsz, L, D))
+    if dtype == BF16:
+        z = to_bf16_bits(z)
+    return Dskip, z
