@@ -47,21 +47,29 @@ FALLBACK_HBM_GBS = 6400.0   # used only if the measured peak file is absent
 
 # --------------------------------------------------------------- roofline
 
-def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False):
+def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gated=False):
     """Algorithmic work of one forward call.
 
     bytes: x, delta, y streams (3 * B*L*D elements) + B, C (2 * B*L*N) + A (D*N fp32)
-    (+ h0 / hT, B*D*N fp32 each when used); the (B, L, D, N) intermediates
-    are never formed, so they do not count.
-    mufu: one exponential per (t, d, n), plus exp and log per (t, d) for softplus.
-    fp32: four per (t, d, n): dl*A, (dl*x)*B, the state FMA and the read-out FMA.
+    (+ h0 / hT, B*D*N fp32 each when used; + the gate's z stream and Dskip
+    (D fp32) for the gated form); the (B, L, D, N) intermediates are never
+    formed, so they do not count.
+    mufu: one exponential per (t, d, n), plus exp and log per (t, d) for
+    softplus, plus exp and reciprocal per (t, d) for silu(z).
+    fp32: four per (t, d, n): dl*A, (dl*x)*B, the state FMA and the read-out
+    FMA; the gated form adds the skip FMA, 1 + e^-z and the product per (t, d).
     """
     E = Bsz * L * D
     S = Bsz * L * N
     nbytes = 3 * E * elem_bytes + 2 * S * elem_bytes + D * N * 4
     nbytes += Bsz * D * N * 4 * (int(bool(h0)) + int(bool(hT)))
-    return {"elems": E, "updates": E * N, "bytes": nbytes,
-            "mufu": E * N + (2 * E if softplus else 0), "fp32": 4 * E * N}
+    mufu = E * N + (2 * E if softplus else 0)
+    fp32 = 4 * E * N
+    if gated:
+        nbytes += E * elem_bytes + D * 4
+        mufu += 2 * E
+        fp32 += 3 * E
+    return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": mufu, "fp32": fp32}
 
 
 def step_work_counts(Bsz, D, N):
@@ -273,8 +281,9 @@ def barrier(world: int, device=None):
 
 # --------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_run(inp, chains=None, nthreads=0):
-    """Times the fp64 oracle on the given chains (all when None). Returns
+def cpu_oracle_run(inp, chains=None, nthreads=0, gate=None):
+    """Times the fp64 oracle on the given chains (all when None), with the
+    block's skip and gate when ``gate`` = (Dskip, z fp32). Returns
     (seconds, elements processed, threads used)."""
     import numpy as np
     import oracle
@@ -282,12 +291,14 @@ def cpu_oracle_run(inp, chains=None, nthreads=0):
     nthreads = nthreads or len(os.sched_getaffinity(0))
     o = oracle.default()
     x, dl, A, B, C = inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C")
+    Dskip, z = gate if gate is not None else (None, None)
     t0 = time.perf_counter()
     if chains is None:
-        o.selscan_fwd(x, dl, A, B, C, inp.delta_softplus, nthreads=nthreads)
+        o.selscan_fwd(x, dl, A, B, C, inp.delta_softplus, nthreads=nthreads, Dskip=Dskip, z=z)
         n = Bsz * D
     else:
-        o.selscan_fwd_chains(x, dl, A, B, C, np.asarray(chains), inp.delta_softplus, nthreads=nthreads)
+        o.selscan_fwd_chains(x, dl, A, B, C, np.asarray(chains), inp.delta_softplus, nthreads=nthreads,
+                             Dskip=Dskip, z=z)
         n = len(chains)
     return time.perf_counter() - t0, n * L, nthreads
 
@@ -324,18 +335,26 @@ def run_gpu(args, world, rank, local):
     Bsz, L, D = inp.x.shape
     N = inp.A.shape[1]
     want_hT = w.return_state
-    foot = (3 * Bsz * L * D + 2 * Bsz * L * N) * es
+    gate = W.workload_gate_inputs(args.workload) if w.gated else None
+    foot = ((4 if w.gated else 3) * Bsz * L * D + 2 * Bsz * L * N) * es
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(1, -(-(2 * l2) // foot))          # rotate until > 2x L2 is touched between reuses
     base = [dev_t(inp.x, "io"), dev_t(inp.delta, "io"), dev_t(inp.A, "f"),
             dev_t(inp.B, "io"), dev_t(inp.C, "io")]
+    if w.gated:
+        base += [dev_t(gate[1], "io")]
+        Dskip_dev = dev_t(gate[0], "f")
     sets = [base] + [[t.clone() for t in base] for _ in range(copies - 1)]
     ys = [torch.empty_like(base[0]) for _ in range(copies)]
     hT = torch.empty(Bsz, D, N, device=dev) if want_hT else None
 
     def step(i):
-        x, dl, A, B, C = sets[i % copies]
-        ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT)
+        x, dl, A, B, C = sets[i % copies][:5]
+        if w.gated:
+            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT,
+                           D_skip=Dskip_dev, z=sets[i % copies][5])
+        else:
+            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT)
 
     for i in range(args.warmup):
         step(i)
@@ -369,14 +388,29 @@ def run_gpu(args, world, rank, local):
                 torch.from_numpy(inp.A),
                 torch.from_numpy(inp.B.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.B),
                 torch.from_numpy(inp.C.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.C)]
-        host = [t.pin_memory() for t in host]
         y_host = torch.empty(ys[0].shape, dtype=ys[0].dtype, pin_memory=True)
         e2e_steps = max(1, min(args.steps, 20))
-        ss.selscan_fwd(*host, True, y=y_host)            # warm the copy path
+        if w.gated:
+            # The gated form takes device tensors: copy the step's inputs in,
+            # run it, copy y out, synchronise.
+            host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
+            host = [t.pin_memory() for t in host]
+
+            def e2e_call():
+                d = [t.to(dev, non_blocking=True) for t in host]
+                yd = ss.selscan_fwd(*d[:5], True, D_skip=d[6], z=d[5])
+                y_host.copy_(yd, non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+        else:
+            host = [t.pin_memory() for t in host]
+
+            def e2e_call():
+                ss.selscan_fwd(*host, True, y=y_host)  # H2D, kernels, D2H, synchronise
+        e2e_call()                                       # warm the copy path
         barrier(world, dev)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            ss.selscan_fwd(*host, True, y=y_host)      # H2D, kernels, D2H, synchronise
+            e2e_call()
         t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in host)
         e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
@@ -392,20 +426,21 @@ def run_gpu(args, world, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pk = peaks(sms, max_mhz, hbm_gbs)
     pk["source"] = f"HBM {src}; MUFU/FP32 derived: {sms} SMs x (32 ex2, 128 fp32)/clk x {max_mhz:.0f} MHz"
-    work = work_counts(Bsz, L, D, N, es, softplus=True, hT=want_hT)
+    work = work_counts(Bsz, L, D, N, es, softplus=True, hT=want_hT, gated=w.gated)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel=f"selscan_fwd call ({plan['launches']} launches, {plan['chunks']} chunks)")
 
     cpu = None
     if not args.no_cpu_baseline:
         chains = None if Bsz * D * L <= 8_000_000 else sample_chains(Bsz, D, 256)
-        secs, n_el, thr = cpu_oracle_run(inp, chains)
+        secs, n_el, thr = cpu_oracle_run(inp, chains, gate=gate)
         cpu = {"value": n_el / secs, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": ("the whole workload" if chains is None else f"{len(chains)} of {Bsz * D} chains over all L")
                + f" ({n_el} elements, {secs:.2f} s, fp64)"}
 
     config = {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={N} {w.dtype}, softplus on"
-                          + (", returns hT" if want_hT else ""),
+                          + (", returns hT" if want_hT else "")
+                          + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else ""),
               "global_batch": Bsz * world, "seq_len": L, "parallelism": f"replicas x{world}",
               "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2 ({l2 / 1e6:.0f} MB)"
                     if copies > 1 else f"inputs {foot / 1e6:.0f} MB > 2x L2",
@@ -553,13 +588,14 @@ def run_reference(args, world, rank):
     if w.steps:
         return run_reference_decode(args, world, w)
     inp = W.workload_inputs(args.workload)
+    gate = W.workload_gate_inputs(args.workload) if w.gated else None
     Bsz, L, D = inp.x.shape
     chains = sample_chains(Bsz, D, args.ref_chains)
     for _ in range(args.warmup):
-        cpu_oracle_run(inp, chains)
+        cpu_oracle_run(inp, chains, gate=gate)
     tot, n_total, thr = 0.0, 0, 0
     for _ in range(args.steps):
-        s, n, thr = cpu_oracle_run(inp, chains)
+        s, n, thr = cpu_oracle_run(inp, chains, gate=gate)
         tot += s
         n_total += n
     value = n_total / tot
@@ -569,7 +605,8 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={inp.A.shape[1]} {w.dtype}, softplus on",
+        "config": {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={inp.A.shape[1]} {w.dtype}, softplus on"
+                               + (", skip and SiLU gate" if w.gated else ""),
                    "seq_len": L, "parallelism": "host threads"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -613,7 +650,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")

@@ -46,6 +46,7 @@ class Workload:
     seed: int
     steps: int = 0    # decode steps (decode workload only)
     return_state: bool = False
+    gated: bool = False   # with the block's skip and gate (gate_inputs)
 
     @property
     def elems(self) -> int:
@@ -59,6 +60,7 @@ WORKLOADS = {
     3: Workload(3, "mamba370m", 8, 2048, 2048, 16, BF16, -3.0, "loguniform", 103),
     4: Workload(4, "long", 1, 131072, 1536, 16, F32, -4.0, "arange", 104, return_state=True),
     5: Workload(5, "decode", 256, 1, 2560, 16, F32, -3.0, "arange", 105, steps=1024),
+    6: Workload(6, "mamba130m-gated", 2, 2048, 1536, 16, F32, -3.0, "arange", 106, gated=True),
 }
 
 
@@ -139,7 +141,8 @@ def fwd_inputs(Bsz: int, L: int, D: int, N: int, *, seed: int, dtype: str = F32,
 
 
 def workload_inputs(wid: int) -> FwdInputs:
-    """Inputs of forward workload 1-4."""
+    """Inputs of a forward workload (all but the decode one); the gated
+    workload's skip and gate inputs come from workload_gate_inputs."""
     w = WORKLOADS[wid]
     if w.steps:
         raise ValueError("workload %d is the decode workload; use decode_state/decode_step_inputs" % wid)
@@ -184,3 +187,9 @@ def gate_inputs(Bsz: int, L: int, D: int, *, seed: int, dtype: str = F32, steps:
     if dtype == BF16:
         z = to_bf16_bits(z)
     return Dskip, z
+
+
+def workload_gate_inputs(wid: int):
+    """(Dskip, z) of a gated forward workload."""
+    w = WORKLOADS[wid]
+    return gate_inputs(w.Bsz, w.L, w.D, seed=w.seed, dtype=w.dtype)

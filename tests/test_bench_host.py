@@ -129,3 +129,21 @@ def test_max_over_two_gloo_ranks():
 
 def test_single_process_is_identity():
     assert bench.max_over_ranks(2.5, 1) == 2.5
+
+
+def test_gated_work_counts_add_z_and_silu():
+    w0 = bench.work_counts(2, 2048, 1536, 16, 4)
+    w1 = bench.work_counts(2, 2048, 1536, 16, 4, gated=True)
+    E = 2 * 2048 * 1536
+    assert w1["bytes"] - w0["bytes"] == E * 4 + 1536 * 4
+    assert w1["mufu"] - w0["mufu"] == 2 * E and w1["fp32"] - w0["fp32"] == 3 * E
+    assert w1["updates"] == w0["updates"]
+
+
+def test_reference_arm_runs_gated_workload():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "6", "--steps", "1", "--warmup", "0", "--ref-chains", "4"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and "gate" in line["config"]["workload"]
