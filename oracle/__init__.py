@@ -72,12 +72,12 @@ class Oracle:
         lib.oracle_selscan_step.restype = INT
         lib.oracle_selscan_step.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64]
         lib.oracle_selscan_fwd_gated.restype = INT
-        lib.oracle_selscan_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT]
+        lib.oracle_selscan_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, INT]
         lib.oracle_selscan_fwd_chains_gated.restype = INT
         lib.oracle_selscan_fwd_chains_gated.argtypes = [P, P, P, P, P, P, P, P, P, I64, P, P,
-                                                        I64, I64, I64, I64, INT, INT]
+                                                        I64, I64, I64, I64, INT, INT, INT]
         lib.oracle_selscan_step_gated.restype = INT
-        lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64]
+        lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         self._lib = lib
         self.path = path
 
@@ -86,13 +86,14 @@ class Oracle:
         return self._lib.oracle_softplus(float(u))
 
     def selscan_fwd(self, x, delta, A, B, C, delta_softplus=False, h0=None, nthreads=0,
-                    Dskip=None, z=None):
+                    Dskip=None, z=None, zoh=False):
         """Sequential selective scan in fp64.
 
         x, delta: (Bsz, L, D); A: (D, N); B, C: (Bsz, L, N); h0: (Bsz, D, N)
         or None. Inputs are taken as float32 (the exact values the GPU reads);
         h0 as float64 (fp32 states widen exactly). Dskip (D,) and z
         (Bsz, L, D) add the block's skip and gate: y = (y + Dskip x) silu(z).
+        zoh: the zero-order-hold Bbar of section 2.2 instead of dl * B.
         Returns (y (Bsz, L, D) float64, hT (Bsz, D, N) float64).
         """
         x = np.asarray(x)
@@ -111,13 +112,13 @@ class Oracle:
         rc = self._lib.oracle_selscan_fwd_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                                 _ptr(Dskip), _ptr(z), _ptr(h0),
                                                 _ptr(y), _ptr(hT), Bsz, L, D, N,
-                                                int(bool(delta_softplus)), int(nthreads))
+                                                int(bool(delta_softplus)), int(bool(zoh)), int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_selscan_fwd failed")
         return y, hT
 
     def selscan_fwd_chains(self, x, delta, A, B, C, chains, delta_softplus=False, h0=None,
-                           nthreads=0, Dskip=None, z=None):
+                           nthreads=0, Dskip=None, z=None, zoh=False):
         """The same scan for selected chains c = b * D + d only.
         Returns (y (nchains, L), hT (nchains, N)) in float64."""
         x = np.asarray(x)
@@ -138,12 +139,13 @@ class Oracle:
         rc = self._lib.oracle_selscan_fwd_chains_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                                        _ptr(Dskip), _ptr(z), _ptr(h0), _ptr(chains), nc,
                                                        _ptr(y), _ptr(hT), Bsz, L, D, N,
-                                                       int(bool(delta_softplus)), int(nthreads))
+                                                       int(bool(delta_softplus)), int(bool(zoh)),
+                                                       int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_selscan_fwd_chains failed")
         return y, hT
 
-    def selscan_step(self, state, x, delta, A, B, C, chains=None, Dskip=None, z=None):
+    def selscan_step(self, state, x, delta, A, B, C, chains=None, Dskip=None, z=None, zoh=False):
         """One decode step in place on a float64 state.
 
         state: (Bsz, D, N) float64, or (nchains, N) when ``chains`` is given;
@@ -177,7 +179,7 @@ class Oracle:
         z = None if z is None else _f32(z, (Bsz, D), "z")
         rc = self._lib.oracle_selscan_step_gated(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
                                                  _ptr(C), _ptr(Dskip), _ptr(z), _ptr(y), _ptr(ch), nc,
-                                                 Bsz, D, N)
+                                                 Bsz, D, N, int(bool(zoh)))
         if rc != 0:
             raise RuntimeError("oracle_selscan_step failed")
         return y

@@ -21,8 +21,10 @@
  *       y[b,t,d] = sum_n h[n] * C[b,t,n]          (read-out after the update)
  *     hT[b,d,:] = h
  *
- * deltaB is the simplified dl * B of the listing, not the zero-order-hold
- * form (dA)^-1 (exp(dA) - I) dB of section 2.2.
+ * deltaB is the simplified dl * B of the listing. The *_gated entry points
+ * take a zoh flag for the zero-order-hold form of section 2.2 instead,
+ * Bbar = (dA)^-1 (exp(dA) - I) dB, which for a diagonal A is, per state,
+ *   Bbar[n] = dl * B[n] * phi(dl * A[d,n]),   phi(w) = (e^w - 1) / w, phi(0) = 1.
  *
  * Optionally (the *_gated entry points) the output of the block around the
  * scan, as the MambaBlock listing of section 3.4 on the same page has it:
@@ -79,11 +81,18 @@ static double gate(double y, const float *Dskip, const float *z, int64_t d,
     return y;
 }
 
+/* phi(w) = (e^w - 1) / w, the zero-order-hold factor of section 2.2 for a
+ * diagonal A (its limit 1 at w = 0, where dA is not invertible). */
+static double zoh_factor(double w)
+{
+    return w == 0.0 ? 1.0 : expm1(w) / w;
+}
+
 /* One (b, d) chain of the forward scan.
  * y_out[t * y_stride] receives y[b,t,d]; h_out[n] receives the final state. */
 static void scan_chain(const float *x, const float *delta, const float *A,
                        const float *B, const float *C, const double *h0,
-                       const float *Dskip, const float *z,
+                       const float *Dskip, const float *z, int zoh,
                        int64_t b, int64_t d, int64_t L, int64_t D, int64_t N,
                        int delta_softplus, double *y_out, int64_t y_stride,
                        double *h_out, double *h)
@@ -100,6 +109,8 @@ static void scan_chain(const float *x, const float *delta, const float *A,
         for (int64_t n = 0; n < N; ++n) {
             double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
             double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            if (zoh)
+                dB *= zoh_factor(dl * (double)A[d * N + n]);
             h[n] = dA * h[n] + dB * xv;
         }
         for (int64_t n = 0; n < N; ++n)
@@ -117,6 +128,7 @@ static void scan_chain(const float *x, const float *delta, const float *A,
 typedef struct {
     const float *x, *delta, *A, *B, *C;
     const float *Dskip, *z;   /* optional block output (NULL: absent) */
+    int zoh;                  /* zero-order-hold Bbar instead of dl * B */
     const double *h0;
     int64_t Bsz, L, D, N;
     int delta_softplus;
@@ -158,7 +170,7 @@ static void *fwd_worker(void *arg)
             y_stride = j->D;
             h_out = j->hT ? j->hT + c * j->N : NULL;
         }
-        scan_chain(j->x, j->delta, j->A, j->B, j->C, j->h0, j->Dskip, j->z, b, d,
+        scan_chain(j->x, j->delta, j->A, j->B, j->C, j->h0, j->Dskip, j->z, j->zoh, b, d,
                    j->L, j->D, j->N, j->delta_softplus, y_out, y_stride, h_out, h);
     }
     free(h);
@@ -204,7 +216,7 @@ int oracle_selscan_fwd_gated(const float *x, const float *delta, const float *A,
                              const float *B, const float *C, const float *Dskip,
                              const float *z, const double *h0, double *y, double *hT,
                              int64_t Bsz, int64_t L, int64_t D, int64_t N,
-                             int delta_softplus, int nthreads);
+                             int delta_softplus, int zoh, int nthreads);
 
 int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
                        const float *B, const float *C, const double *h0,
@@ -212,16 +224,16 @@ int oracle_selscan_fwd(const float *x, const float *delta, const float *A,
                        int64_t D, int64_t N, int delta_softplus, int nthreads)
 {
     return oracle_selscan_fwd_gated(x, delta, A, B, C, NULL, NULL, h0, y, hT,
-                                    Bsz, L, D, N, delta_softplus, nthreads);
+                                    Bsz, L, D, N, delta_softplus, 0, nthreads);
 }
 
 /* The forward scan with the block's skip and gate (either may be NULL):
- * Dskip (D), z (Bsz, L, D). */
+ * Dskip (D), z (Bsz, L, D); zoh selects the zero-order-hold Bbar. */
 int oracle_selscan_fwd_gated(const float *x, const float *delta, const float *A,
                              const float *B, const float *C, const float *Dskip,
                              const float *z, const double *h0, double *y, double *hT,
                              int64_t Bsz, int64_t L, int64_t D, int64_t N,
-                             int delta_softplus, int nthreads)
+                             int delta_softplus, int zoh, int nthreads)
 {
     if (Bsz < 0 || L < 0 || D < 0 || N < 0)
         return -1;
@@ -232,7 +244,7 @@ int oracle_selscan_fwd_gated(const float *x, const float *delta, const float *A,
     fwd_job j;
     memset(&j, 0, sizeof j);
     j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
-    j.Dskip = Dskip; j.z = z;
+    j.Dskip = Dskip; j.z = z; j.zoh = zoh;
     j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
     j.delta_softplus = delta_softplus;
     j.chains = NULL;
@@ -250,7 +262,7 @@ int oracle_selscan_fwd_chains_gated(const float *x, const float *delta,
                                     const double *h0, const int64_t *chains,
                                     int64_t nchains, double *y_out, double *hT_out,
                                     int64_t Bsz, int64_t L, int64_t D, int64_t N,
-                                    int delta_softplus, int nthreads);
+                                    int delta_softplus, int zoh, int nthreads);
 
 int oracle_selscan_fwd_chains(const float *x, const float *delta,
                               const float *A, const float *B, const float *C,
@@ -261,17 +273,17 @@ int oracle_selscan_fwd_chains(const float *x, const float *delta,
 {
     return oracle_selscan_fwd_chains_gated(x, delta, A, B, C, NULL, NULL, h0, chains,
                                            nchains, y_out, hT_out, Bsz, L, D, N,
-                                           delta_softplus, nthreads);
+                                           delta_softplus, 0, nthreads);
 }
 
-/* oracle_selscan_fwd_chains with the block's skip and gate. */
+/* oracle_selscan_fwd_chains with the block's skip and gate, and zoh. */
 int oracle_selscan_fwd_chains_gated(const float *x, const float *delta,
                                     const float *A, const float *B, const float *C,
                                     const float *Dskip, const float *z,
                                     const double *h0, const int64_t *chains,
                                     int64_t nchains, double *y_out, double *hT_out,
                                     int64_t Bsz, int64_t L, int64_t D, int64_t N,
-                                    int delta_softplus, int nthreads)
+                                    int delta_softplus, int zoh, int nthreads)
 {
     if (Bsz < 0 || L < 0 || D < 0 || N < 0 || nchains < 0 || (nchains && !chains))
         return -1;
@@ -281,7 +293,7 @@ int oracle_selscan_fwd_chains_gated(const float *x, const float *delta,
     fwd_job j;
     memset(&j, 0, sizeof j);
     j.x = x; j.delta = delta; j.A = A; j.B = B; j.C = C; j.h0 = h0;
-    j.Dskip = Dskip; j.z = z;
+    j.Dskip = Dskip; j.z = z; j.zoh = zoh;
     j.Bsz = Bsz; j.L = L; j.D = D; j.N = N;
     j.delta_softplus = delta_softplus;
     j.chains = chains;
@@ -299,7 +311,7 @@ int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
                               const float *A, const float *B, const float *C,
                               const float *Dskip, const float *z, double *y,
                               const int64_t *chains, int64_t nchains,
-                              int64_t Bsz, int64_t D, int64_t N);
+                              int64_t Bsz, int64_t D, int64_t N, int zoh);
 
 int oracle_selscan_step(double *state, const float *x, const float *delta,
                         const float *A, const float *B, const float *C,
@@ -307,15 +319,16 @@ int oracle_selscan_step(double *state, const float *x, const float *delta,
                         int64_t Bsz, int64_t D, int64_t N)
 {
     return oracle_selscan_step_gated(state, x, delta, A, B, C, NULL, NULL, y,
-                                     chains, nchains, Bsz, D, N);
+                                     chains, nchains, Bsz, D, N, 0);
 }
 
-/* oracle_selscan_step with the block's skip and gate: Dskip (D), z (Bsz, D). */
+/* oracle_selscan_step with the block's skip and gate: Dskip (D), z (Bsz, D);
+ * zoh selects the zero-order-hold Bbar. */
 int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
                               const float *A, const float *B, const float *C,
                               const float *Dskip, const float *z, double *y,
                               const int64_t *chains, int64_t nchains,
-                              int64_t Bsz, int64_t D, int64_t N)
+                              int64_t Bsz, int64_t D, int64_t N, int zoh)
 {
     if (!state || !x || !delta || !A || !B || !C || Bsz < 0 || D < 0 || N < 0)
         return -1;
@@ -332,6 +345,8 @@ int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
         for (int64_t n = 0; n < N; ++n) {
             double dA = exp(dl * (double)A[d * N + n]);
             double dB = dl * (double)B[b * N + n];
+            if (zoh)
+                dB *= zoh_factor(dl * (double)A[d * N + n]);
             h[n] = dA * h[n] + dB * xv;
         }
         for (int64_t n = 0; n < N; ++n)

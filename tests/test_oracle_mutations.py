@@ -16,6 +16,8 @@ MUTATIONS = {
         """        for (int64_t n = 0; n < N; ++n) {
             double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
             double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            if (zoh)
+                dB *= zoh_factor(dl * (double)A[d * N + n]);
             h[n] = dA * h[n] + dB * xv;
         }
         for (int64_t n = 0; n < N; ++n)
@@ -26,6 +28,8 @@ MUTATIONS = {
         for (int64_t n = 0; n < N; ++n) {
             double dA = exp(dl * (double)A[d * N + n]);   /* deltaA */
             double dB = dl * (double)B[bt * N + n];        /* deltaB */
+            if (zoh)
+                dB *= zoh_factor(dl * (double)A[d * N + n]);
             h[n] = dA * h[n] + dB * xv;
         }
 """),
@@ -65,6 +69,9 @@ MUTATIONS = {
     }
     if (Dskip)
         y += (double)Dskip[d] * xv;"""),
+    "zoh_without_division": ("return w == 0.0 ? 1.0 : expm1(w) / w;", "return w == 0.0 ? 1.0 : expm1(w);"),
+    "zoh_uses_exp": ("return w == 0.0 ? 1.0 : expm1(w) / w;", "return w == 0.0 ? 1.0 : exp(w) / w;"),
+    "zoh_flag_ignored": ("            if (zoh)\n                dB *= zoh_factor(dl * (double)A[d * N + n]);\n", ""),
     "step_dropped_input": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];",
                            "            h[n] = dA * h[n];\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];"),
 }

@@ -428,3 +428,64 @@ def test_gated_steps_equal_gated_forward(orc):
         yt = orc.selscan_step(st, x[:, t], u[:, t], A, B[:, t], C[:, t], Dskip=Dskip, z=z[:, t])
         assert np.allclose(yt, y[:, t], rtol=1e-13, atol=1e-13)
     assert np.allclose(st, hT, rtol=1e-13, atol=1e-13)
+
+
+# ---- zero-order-hold discretisation (section 2.2) ----------------------------
+
+def test_zoh_is_the_exact_solution_for_held_inputs(orc):
+    """With x, delta and B held over each step, the continuous system
+    h' = A h + B x (diagonal A) moves from h to exp(dA) h + (exp(dA) - 1)/A B x.
+    Each state is checked against scipy's matrix exponential of the augmented
+    2x2 system [[A dl, B x dl], [0, 0]] applied to (h, 1)."""
+    from scipy.linalg import expm
+    Bsz, L, D, N = 1, 6, 3, 4
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=41, softplus=False, h0=True)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, False, hh, zoh=True)
+    h = hh.copy()
+    for t in range(L):
+        for d in range(D):
+            dl = float(u[0, t, d])
+            for n in range(N):
+                M = np.array([[float(A[d, n]) * dl, float(B[0, t, n]) * float(x[0, t, d]) * dl], [0.0, 0.0]])
+                h[0, d, n] = (expm(M) @ np.array([h[0, d, n], 1.0]))[0]
+        assert np.allclose(y[0, t], (h[0] * C[0, t].astype(np.float64)[None, :]).sum(-1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(hT, h, rtol=1e-12, atol=1e-12)
+
+
+def test_zoh_fixed_point_does_not_depend_on_delta(orc):
+    """Held x and B: every step maps h to exp(dA) h + (exp(dA) - 1)/A B x, whose
+    fixed point -B x / A is the continuous system's, for any step size."""
+    D, N, L = 2, 3, 3000
+    A = np.array([[-0.5, -1.0, -2.0], [-0.75, -1.5, -3.0]], np.float32)
+    Bv = np.array([0.3, -0.7, 1.1], np.float32)
+    for dl in (0.05, 0.5):
+        x = np.full((1, L, D), 0.8, np.float32)
+        u = np.full((1, L, D), dl, np.float32)
+        B = np.tile(Bv, (1, L, 1)).astype(np.float32)
+        _, hT = orc.selscan_fwd(x, u, A, B, np.zeros_like(B), False, zoh=True)
+        star = -(Bv[None, :].astype(np.float64) * float(np.float32(0.8))) / A.astype(np.float64)
+        assert np.allclose(hT[0], star, rtol=1e-9, atol=1e-12)
+
+
+def test_zoh_limits(orc):
+    """dl * A -> 0: the zero-order-hold Bbar tends to dl * B (the simplified
+    form), exactly at A = 0; it stays below dl * B for A < 0."""
+    x, u, A, B, C, hh = rand_inputs(2, 10, 3, 4, seed=43, softplus=False, h0=True)
+    y0, h0_ = orc.selscan_fwd(x, u, np.zeros_like(A), B, C, False, hh)
+    y1, h1 = orc.selscan_fwd(x, u, np.zeros_like(A), B, C, False, hh, zoh=True)
+    assert np.array_equal(y0, y1) and np.array_equal(h0_, h1)
+    tiny = (u * np.float32(1e-7)).astype(np.float32)
+    ye, _ = orc.selscan_fwd(x, tiny, A, B, C, False, hh)
+    yz, _ = orc.selscan_fwd(x, tiny, A, B, C, False, hh, zoh=True)
+    assert np.allclose(yz, ye, rtol=1e-5, atol=1e-12)
+
+
+def test_zoh_steps_equal_zoh_forward(orc):
+    Bsz, L, D, N = 2, 8, 3, 5
+    x, u, A, B, C, hh = rand_inputs(Bsz, L, D, N, seed=44, softplus=False, h0=True)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, False, hh, zoh=True)
+    st = hh.copy()
+    for t in range(L):
+        yt = orc.selscan_step(st, x[:, t], u[:, t], A, B[:, t], C[:, t], zoh=True)
+        assert np.allclose(yt, y[:, t], rtol=1e-13, atol=1e-13)
+    assert np.allclose(st, hT, rtol=1e-13, atol=1e-13)
