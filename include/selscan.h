@@ -69,6 +69,10 @@ typedef enum {
 /* Largest state size N the kernels implement. */
 #define SELSCAN_MAX_N 64
 
+/* Flags of selscan_fwd_ex and selscan_step_ex. */
+#define SELSCAN_FLAG_SOFTPLUS 1   /* delta is the pre-activation: dl = softplus(delta) */
+#define SELSCAN_FLAG_ZOH 2        /* zero-order-hold Bbar instead of dl * B (see selscan_fwd_ex) */
+
 /*
  * selscan_fwd -- the forward selective scan over a whole sequence.
  * (youngju.dev "Mamba: Selective State Space Models", section 3.3;
@@ -130,6 +134,26 @@ int selscan_fwd_gated(const void *x, const void *delta, const float *A, const vo
                       int delta_softplus, const float *h0, float *hT, void *stream);
 
 /*
+ * selscan_fwd_ex -- selscan_fwd_gated with a flags word in place of
+ * delta_softplus: SELSCAN_FLAG_SOFTPLUS as delta_softplus != 0, and
+ * SELSCAN_FLAG_ZOH for the zero-order-hold discretisation of youngju.dev
+ * section 2.2, Bbar = (dl A)^-1 (exp(dl A) - I) dl B, which for the diagonal
+ * A is, per state,
+ *
+ *   Bbar[n] = dl * B[n] * phi(dl * A[d,n]),   phi(w) = (e^w - 1) / w,  phi(0) = 1
+ *
+ * in place of the simplified dl * B[n] (the decay exp(dl A) is the same).
+ * phi is evaluated from the decay, or from its series where |w| < 1/16, so
+ * A == 0 gives the limit dl * B. The zero-order-hold form runs on the
+ * plain-load kernels (not the fused TMA kernel). Unknown flag bits are
+ * SELSCAN_ERR_INVALID_ARG.
+ */
+int selscan_fwd_ex(const void *x, const void *delta, const float *A, const void *B,
+                   const void *C, const float *Dskip, const void *z, void *y,
+                   int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, int flags,
+                   const float *h0, float *hT, void *stream);
+
+/*
  * selscan_step -- one decode step of the recurrent mode, O(1) state per
  * token (youngju.dev section 6: inference O(1) per token with a fixed
  * state; the same update as selscan_fwd with L = 1).
@@ -156,6 +180,13 @@ int selscan_step(float *state, const float *x, const float *delta, const float *
 int selscan_step_gated(float *state, const float *x, const float *delta, const float *A,
                        const float *B, const float *C, const float *Dskip, const float *z,
                        float *y, int64_t Bsz, int64_t D, int64_t N, void *stream);
+
+/* selscan_step_gated with a flags word: SELSCAN_FLAG_ZOH selects the
+ * zero-order-hold Bbar as in selscan_fwd_ex (the step takes no softplus;
+ * any other bit is SELSCAN_ERR_INVALID_ARG). */
+int selscan_step_ex(float *state, const float *x, const float *delta, const float *A,
+                    const float *B, const float *C, const float *Dskip, const float *z,
+                    float *y, int64_t Bsz, int64_t D, int64_t N, int flags, void *stream);
 
 /*
  * selscan_fwd_noalloc -- selscan_fwd for callers that cannot allocate device

@@ -22,9 +22,10 @@ import os
 __all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
-           "MAX_N"]
+           "MAX_N", "FLAG_SOFTPLUS", "FLAG_ZOH"]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
+FLAG_SOFTPLUS, FLAG_ZOH = 1, 2
 F32, BF16 = 0, 1
 MAX_N = 64
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_step_gated.restype = INT
         L.selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, P]
+        L.selscan_fwd_ex.restype = INT
+        L.selscan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_step_ex.restype = INT
+        L.selscan_step_ex.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, P]
         L.selscan_fwd_host.restype = INT
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
@@ -146,7 +151,7 @@ def _need(t, name, shape, dtype, device):
 
 def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
                 return_final_state: bool = False, y=None, hT=None, stream=None,
-                D_skip=None, z=None):
+                D_skip=None, z=None, zoh: bool = False):
     """Forward selective scan (see ``include/selscan.h``).
 
     x, delta: (Bsz, L, D) float32 or bfloat16; A: (D, N) float32;
@@ -154,14 +159,15 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
     Returns y (Bsz, L, D), or (y, hT) with hT (Bsz, D, N) float32 when
     ``return_final_state``. ``y`` / ``hT`` may be passed preallocated.
     ``D_skip`` (D,) float32 and ``z`` (like x) add the block's skip and gate
-    (selscan_fwd_gated): y = (scan + D_skip * x) * silu(z). Device tensors
-    only for those.
+    (selscan_fwd_gated): y = (scan + D_skip * x) * silu(z). ``zoh`` selects
+    the zero-order-hold discretisation (selscan_fwd_ex). Device tensors only
+    for those.
     """
     import torch
     gated = D_skip is not None or z is not None
     if x.device.type == "cpu":
-        if gated:
-            raise ValueError("D_skip / z are supported for device tensors only")
+        if gated or zoh:
+            raise ValueError("D_skip / z / zoh are supported for device tensors only")
         return _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT)
     dev = x.device
     Bsz, L, D = x.shape
@@ -187,10 +193,11 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
     if z is not None:
         _need(z, "z", (Bsz, L, D), x.dtype, dev)
     with torch.cuda.device(dev):
-        if gated:
-            rc = lib().selscan_fwd_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D_skip),
-                                         _ptr(z), _ptr(y), Bsz, L, D, N, code, int(bool(delta_softplus)),
-                                         _ptr(h0), _ptr(hT), _stream_ptr(stream))
+        if gated or zoh:
+            flags = (FLAG_SOFTPLUS if delta_softplus else 0) | (FLAG_ZOH if zoh else 0)
+            rc = lib().selscan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D_skip),
+                                      _ptr(z), _ptr(y), Bsz, L, D, N, code, flags,
+                                      _ptr(h0), _ptr(hT), _stream_ptr(stream))
         else:
             rc = lib().selscan_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
                                    Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
@@ -226,16 +233,18 @@ def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=N
     return y
 
 
-def selscan_step(state, x, delta, A, B, C, y=None, stream=None, D_skip=None, z=None):
+def selscan_step(state, x, delta, A, B, C, y=None, stream=None, D_skip=None, z=None,
+                 zoh: bool = False):
     """One decode step (see ``include/selscan.h``): ``state`` (Bsz, D, N)
     float32 is updated in place; returns y (Bsz, D) float32. delta is used
     as given (no softplus). ``D_skip`` (D,) and ``z`` (Bsz, D) add the
-    block's skip and gate (selscan_step_gated; device tensors only)."""
+    block's skip and gate; ``zoh`` selects the zero-order-hold discretisation
+    (selscan_step_ex; device tensors only)."""
     import torch
     gated = D_skip is not None or z is not None
     if state.device.type == "cpu":
-        if gated:
-            raise ValueError("D_skip / z are supported for device tensors only")
+        if gated or zoh:
+            raise ValueError("D_skip / z / zoh are supported for device tensors only")
         return _step_host(state, x, delta, A, B, C, y)
     dev = state.device
     Bsz, D, N = state.shape
@@ -255,9 +264,10 @@ def selscan_step(state, x, delta, A, B, C, y=None, stream=None, D_skip=None, z=N
     if z is not None:
         _need(z, "z", (Bsz, D), f, dev)
     with torch.cuda.device(dev):
-        if gated:
-            rc = lib().selscan_step_gated(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                                          _ptr(D_skip), _ptr(z), _ptr(y), Bsz, D, N, _stream_ptr(stream))
+        if gated or zoh:
+            rc = lib().selscan_step_ex(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                       _ptr(D_skip), _ptr(z), _ptr(y), Bsz, D, N, FLAG_ZOH if zoh else 0,
+                                       _stream_ptr(stream))
         else:
             rc = lib().selscan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                     _ptr(y), Bsz, D, N, _stream_ptr(stream))

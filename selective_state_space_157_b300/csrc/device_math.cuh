@@ -58,6 +58,23 @@ __device__ __forceinline__ float block_out(float y, float dsk, float x, bool gat
     return gated ? y * silu(z) : y;
 }
 
+// Zero-order-hold input coefficient (youngju.dev "Mamba: Selective State
+// Space Models", section 2.2, for a diagonal A): Bbar / B = dl * phi(w) with
+// phi(w) = (e^w - 1) / w and w = dl * a, given the decay e^w already
+// computed. For |w| < 1/16 the difference e^w - 1 would lose digits, so phi
+// comes from its series 1 + w/2 + w^2/6 + w^3/24 (truncation below
+// w^4/120 < 1.3e-7, and exact at w = 0 where the limit is dl); elsewhere
+// (e^w - 1) / a, where a != 0.
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float zoh_coef(float dl, float a, float decay)
+{
+    const float w = dl * a;
+    if (fabsf(w) < 0.0625f)
+        return dl * fmaf(w, fmaf(w, fmaf(w, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+    return __fdividef(decay - 1.0f, a);
+}
+
 template <typename T> struct Io;
 
 template <> struct Io<float> {

@@ -48,7 +48,16 @@ struct ScanArgs {
     int K;             // number of chunks
     int dtiles;        // ceil(D / channels per CTA)
     int softplus;
+    int zoh;           // zero-order-hold Bbar (zoh_coef) instead of dl * B
 };
+
+// The zero-order-hold input term of a pair of states: Bbar x with
+// Bbar = zoh_coef * B, from the log2(e)-scaled A pair.
+__device__ __forceinline__ float2 zoh_input(float dl, float xv, float2 A2, float2 decay, float b0, float b1)
+{
+    return make_float2(zoh_coef(dl, A2.x * kLn2, decay.x) * xv * b0,
+                       zoh_coef(dl, A2.y * kLn2, decay.y) * xv * b1);
+}
 
 template <typename T, int NS, int NSPLIT, bool READOUT, bool VEC>
 __global__ void __launch_bounds__(kScanThreads)
@@ -129,7 +138,8 @@ scan_chunk_kernel(const ScanArgs a)
             for (int j = 0; j < NP; ++j) {
                 const float2 e = __fmul2_rn(dl2, A2[j]);
                 const float2 decay = make_float2(ex2(e.x), ex2(e.y));
-                const float2 inp = __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                const float2 inp = a.zoh ? zoh_input(dl, xv, A2[j], decay, Bv[2 * j], Bv[2 * j + 1])
+                                         : __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
                 h[j] = __ffma2_rn(decay, h[j], inp);
                 const float2 c = make_float2(Cv[2 * j], Cv[2 * j + 1]);
                 if (j & 1)
@@ -154,7 +164,8 @@ scan_chunk_kernel(const ScanArgs a)
             for (int j = 0; j < NP; ++j) {
                 const float2 e = __fmul2_rn(dl2, A2[j]);
                 const float2 decay = make_float2(ex2(e.x), ex2(e.y));
-                const float2 inp = __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                const float2 inp = a.zoh ? zoh_input(dl, xv, A2[j], decay, Bv[2 * j], Bv[2 * j + 1])
+                                         : __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
                 h[j] = __ffma2_rn(decay, h[j], inp);
             }
             // Kahan summation keeps sum(dl) to fp32 rounding over long chunks.

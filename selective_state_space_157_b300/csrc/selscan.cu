@@ -442,7 +442,7 @@ int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int sm
     a.K = plan.K;
     a.dtiles = plan.dtiles;
     if (a.Bsz * plan.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-    if (plan.tma) {
+    if (plan.tma && !a.zoh) {   // the fused kernel implements the simplified dl * B only
         int rc = launch_fused(a, plan, dtype, sms, ws, st);
         if (rc != SELSCAN_ERR_UNSUPPORTED) return rc;
         g_err[0] = '\0';
@@ -557,7 +557,19 @@ extern "C" int selscan_fwd_gated(const void *x, const void *delta, const float *
                                  int64_t L, int64_t D, int64_t N, int dtype, int delta_softplus,
                                  const float *h0, float *hT, void *stream)
 {
+    return selscan_fwd_ex(x, delta, A, B, C, Dskip, z, y, Bsz, L, D, N, dtype,
+                          delta_softplus ? SELSCAN_FLAG_SOFTPLUS : 0, h0, hT, stream);
+}
+
+extern "C" int selscan_fwd_ex(const void *x, const void *delta, const float *A, const void *B,
+                              const void *C, const float *Dskip, const void *z, void *y, int64_t Bsz,
+                              int64_t L, int64_t D, int64_t N, int dtype, int flags, const float *h0,
+                              float *hT, void *stream)
+{
     g_err[0] = '\0';
+    if (flags & ~(SELSCAN_FLAG_SOFTPLUS | SELSCAN_FLAG_ZOH))
+        return fail(SELSCAN_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)flags);
+    const int delta_softplus = (flags & SELSCAN_FLAG_SOFTPLUS) != 0;
     bool empty = false;
     int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty, Dskip, z);
     if (rc != SELSCAN_OK || empty) return rc;
@@ -576,6 +588,7 @@ extern "C" int selscan_fwd_gated(const void *x, const void *delta, const float *
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.Dskip = Dskip; a.z = z;
     a.softplus = delta_softplus ? 1 : 0;
+    a.zoh = (flags & SELSCAN_FLAG_ZOH) ? 1 : 0;
     return launch_fwd(a, plan, dtype, dev, sms, st);
 }
 
@@ -853,7 +866,17 @@ extern "C" int selscan_step_gated(float *state, const float *x, const float *del
                                   const float *B, const float *C, const float *Dskip, const float *z,
                                   float *y, int64_t Bsz, int64_t D, int64_t N, void *stream)
 {
+    return selscan_step_ex(state, x, delta, A, B, C, Dskip, z, y, Bsz, D, N, 0, stream);
+}
+
+extern "C" int selscan_step_ex(float *state, const float *x, const float *delta, const float *A,
+                               const float *B, const float *C, const float *Dskip, const float *z,
+                               float *y, int64_t Bsz, int64_t D, int64_t N, int flags, void *stream)
+{
     g_err[0] = '\0';
+    if (flags & ~SELSCAN_FLAG_ZOH)
+        return fail(SELSCAN_ERR_INVALID_ARG, "unknown flags 0x%x (the decode step takes SELSCAN_FLAG_ZOH only)",
+                    (unsigned)flags);
     if (Bsz < 0 || D < 0)
         return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld D=%lld)", (long long)Bsz, (long long)D);
     if (N < 1)
@@ -883,7 +906,7 @@ extern "C" int selscan_step_gated(float *state, const float *x, const float *del
         return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps state");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N};
+    StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N, (flags & SELSCAN_FLAG_ZOH) ? 1 : 0};
     const int64_t chains = Bsz * D;
     // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
     // must divide the warp so that a chain's lanes never straddle two warps.
