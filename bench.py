@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6400.0   # used only if the measured peak file is absent
 
 # --------------------------------------------------------------- roofline
 
-def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gated=False):
+def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gated=False, zoh=False):
     """Algorithmic work of one forward call.
 
     bytes: x, delta, y streams (3 * B*L*D elements) + B, C (2 * B*L*N) + A (D*N fp32)
@@ -58,6 +58,8 @@ def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gat
     softplus, plus exp and reciprocal per (t, d) for silu(z).
     fp32: four per (t, d, n): dl*A, (dl*x)*B, the state FMA and the read-out
     FMA; the gated form adds the skip FMA, 1 + e^-z and the product per (t, d).
+    The zero-order-hold form adds per (t, d, n) one division (a MUFU
+    reciprocal) and three FP32 operations for (e^w - 1) / A * x * B.
     """
     E = Bsz * L * D
     S = Bsz * L * N
@@ -69,6 +71,9 @@ def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gat
         nbytes += E * elem_bytes + D * 4
         mufu += 2 * E
         fp32 += 3 * E
+    if zoh:
+        mufu += E * N
+        fp32 += 3 * E * N
     return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": mufu, "fp32": fp32}
 
 
@@ -281,7 +286,7 @@ def barrier(world: int, device=None):
 
 # --------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_run(inp, chains=None, nthreads=0, gate=None):
+def cpu_oracle_run(inp, chains=None, nthreads=0, gate=None, zoh=False):
     """Times the fp64 oracle on the given chains (all when None), with the
     block's skip and gate when ``gate`` = (Dskip, z fp32). Returns
     (seconds, elements processed, threads used)."""
@@ -294,11 +299,11 @@ def cpu_oracle_run(inp, chains=None, nthreads=0, gate=None):
     Dskip, z = gate if gate is not None else (None, None)
     t0 = time.perf_counter()
     if chains is None:
-        o.selscan_fwd(x, dl, A, B, C, inp.delta_softplus, nthreads=nthreads, Dskip=Dskip, z=z)
+        o.selscan_fwd(x, dl, A, B, C, inp.delta_softplus, nthreads=nthreads, Dskip=Dskip, z=z, zoh=zoh)
         n = Bsz * D
     else:
         o.selscan_fwd_chains(x, dl, A, B, C, np.asarray(chains), inp.delta_softplus, nthreads=nthreads,
-                             Dskip=Dskip, z=z)
+                             Dskip=Dskip, z=z, zoh=zoh)
         n = len(chains)
     return time.perf_counter() - t0, n * L, nthreads
 
@@ -350,7 +355,9 @@ def run_gpu(args, world, rank, local):
 
     def step(i):
         x, dl, A, B, C = sets[i % copies][:5]
-        if w.gated:
+        if w.zoh:
+            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT, zoh=True)
+        elif w.gated:
             ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT,
                            D_skip=Dskip_dev, z=sets[i % copies][5])
         else:
@@ -390,7 +397,15 @@ def run_gpu(args, world, rank, local):
                 torch.from_numpy(inp.C.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.C)]
         y_host = torch.empty(ys[0].shape, dtype=ys[0].dtype, pin_memory=True)
         e2e_steps = max(1, min(args.steps, 20))
-        if w.gated:
+        if w.zoh:
+            host = [t.pin_memory() for t in host]
+
+            def e2e_call():
+                d = [t.to(dev, non_blocking=True) for t in host]
+                yd = ss.selscan_fwd(*d, True, zoh=True)
+                y_host.copy_(yd, non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+        elif w.gated:
             # The gated form takes device tensors: copy the step's inputs in,
             # run it, copy y out, synchronise.
             host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
@@ -426,21 +441,22 @@ def run_gpu(args, world, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pk = peaks(sms, max_mhz, hbm_gbs)
     pk["source"] = f"HBM {src}; MUFU/FP32 derived: {sms} SMs x (32 ex2, 128 fp32)/clk x {max_mhz:.0f} MHz"
-    work = work_counts(Bsz, L, D, N, es, softplus=True, hT=want_hT, gated=w.gated)
+    work = work_counts(Bsz, L, D, N, es, softplus=True, hT=want_hT, gated=w.gated, zoh=w.zoh)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel=f"selscan_fwd call ({plan['launches']} launches, {plan['chunks']} chunks)")
 
     cpu = None
     if not args.no_cpu_baseline:
         chains = None if Bsz * D * L <= 8_000_000 else sample_chains(Bsz, D, 256)
-        secs, n_el, thr = cpu_oracle_run(inp, chains, gate=gate)
+        secs, n_el, thr = cpu_oracle_run(inp, chains, gate=gate, zoh=w.zoh)
         cpu = {"value": n_el / secs, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": ("the whole workload" if chains is None else f"{len(chains)} of {Bsz * D} chains over all L")
                + f" ({n_el} elements, {secs:.2f} s, fp64)"}
 
     config = {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={N} {w.dtype}, softplus on"
                           + (", returns hT" if want_hT else "")
-                          + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else ""),
+                          + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else "")
+                          + (", zero-order-hold Bbar (plain-load kernels)" if w.zoh else ""),
               "global_batch": Bsz * world, "seq_len": L, "parallelism": f"replicas x{world}",
               "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2 ({l2 / 1e6:.0f} MB)"
                     if copies > 1 else f"inputs {foot / 1e6:.0f} MB > 2x L2",
@@ -592,10 +608,10 @@ def run_reference(args, world, rank):
     Bsz, L, D = inp.x.shape
     chains = sample_chains(Bsz, D, args.ref_chains)
     for _ in range(args.warmup):
-        cpu_oracle_run(inp, chains, gate=gate)
+        cpu_oracle_run(inp, chains, gate=gate, zoh=w.zoh)
     tot, n_total, thr = 0.0, 0, 0
     for _ in range(args.steps):
-        s, n, thr = cpu_oracle_run(inp, chains, gate=gate)
+        s, n, thr = cpu_oracle_run(inp, chains, gate=gate, zoh=w.zoh)
         tot += s
         n_total += n
     value = n_total / tot
@@ -606,7 +622,8 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={inp.A.shape[1]} {w.dtype}, softplus on"
-                               + (", skip and SiLU gate" if w.gated else ""),
+                               + (", skip and SiLU gate" if w.gated else "")
+                               + (", zero-order hold" if w.zoh else ""),
                    "seq_len": L, "parallelism": "host threads"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -650,7 +667,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")

@@ -47,6 +47,7 @@ class Workload:
     steps: int = 0    # decode steps (decode workload only)
     return_state: bool = False
     gated: bool = False   # with the block's skip and gate (gate_inputs)
+    zoh: bool = False     # zero-order-hold discretisation instead of dl * B
 
     @property
     def elems(self) -> int:
@@ -61,6 +62,7 @@ WORKLOADS = {
     4: Workload(4, "long", 1, 131072, 1536, 16, F32, -4.0, "arange", 104, return_state=True),
     5: Workload(5, "decode", 256, 1, 2560, 16, F32, -3.0, "arange", 105, steps=1024),
     6: Workload(6, "mamba130m-gated", 2, 2048, 1536, 16, F32, -3.0, "arange", 106, gated=True),
+    7: Workload(7, "mamba130m-zoh", 2, 2048, 1536, 16, F32, -3.0, "arange", 107, zoh=True),
 }
 
 
