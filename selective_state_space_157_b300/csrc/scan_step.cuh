@@ -24,16 +24,16 @@ struct StepArgs {
     const float *Dskip;   // (D) or null: the block's skip term
     const float *z;       // (Bsz, D) or null: the block's gate
     int64_t Bsz, D, N;
-    int zoh;              // zero-order-hold Bbar (zoh_coef) instead of dl * B
 };
 
 // One state: h' = e^(dl a) h + Bbar x, with Bbar = dl * b, or the
-// zero-order-hold form when asked.
-__device__ __forceinline__ float step_state(const StepArgs &sa, float h, float a, float b, float dl,
-                                            float dk, float u, float xv)
+// zero-order-hold form (compiled separately, so the simplified form keeps
+// its short instruction stream).
+template <bool ZOH>
+__device__ __forceinline__ float step_state(float h, float a, float b, float dl, float dk, float u, float xv)
 {
     const float decay = ex2(dk * a);
-    if (sa.zoh)
+    if constexpr (ZOH)
         return fmaf(decay, h, zoh_coef(dl, a, decay) * xv * b);
     return fmaf(decay, h, u * b);
 }
@@ -47,7 +47,7 @@ __device__ __forceinline__ float step_block(const StepArgs &a, float yv, float x
 }
 
 // V 16-byte groups (4V states) per lane, G lanes per chain (N = 4 V G).
-template <int G, int V>
+template <int G, int V, bool ZOH>
 __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a)
 {
     const int64_t chains = a.Bsz * a.D;
@@ -76,10 +76,10 @@ __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a
     float yv = 0.0f;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        s[v].x = step_state(a, s[v].x, A4[v].x, B4[v].x, dl, dk, u, xv);
-        s[v].y = step_state(a, s[v].y, A4[v].y, B4[v].y, dl, dk, u, xv);
-        s[v].z = step_state(a, s[v].z, A4[v].z, B4[v].z, dl, dk, u, xv);
-        s[v].w = step_state(a, s[v].w, A4[v].w, B4[v].w, dl, dk, u, xv);
+        s[v].x = step_state<ZOH>(s[v].x, A4[v].x, B4[v].x, dl, dk, u, xv);
+        s[v].y = step_state<ZOH>(s[v].y, A4[v].y, B4[v].y, dl, dk, u, xv);
+        s[v].z = step_state<ZOH>(s[v].z, A4[v].z, B4[v].z, dl, dk, u, xv);
+        s[v].w = step_state<ZOH>(s[v].w, A4[v].w, B4[v].w, dl, dk, u, xv);
         yv += fmaf(s[v].x, C4[v].x, s[v].y * C4[v].y) + fmaf(s[v].z, C4[v].z, s[v].w * C4[v].w);
     }
 #pragma unroll
@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a
 }
 
 // Any N <= 64 and any 4-byte alignment: one thread per chain.
+template <bool ZOH>
 __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const StepArgs a)
 {
     const int64_t chain = (int64_t)blockIdx.x * kStepThreads + threadIdx.x;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kStepThreads) step_scalar_kernel(const StepArg
     const float *Cp = a.C + b * a.N;
     float yv = 0.0f;
     for (int64_t n = 0; n < a.N; ++n) {
-        const float s = step_state(a, sp[n], Ap[n], Bp[n], dl, dk, u, xv);
+        const float s = step_state<ZOH>(sp[n], Ap[n], Bp[n], dl, dk, u, xv);
         sp[n] = s;
         yv = fmaf(s, Cp[n], yv);
     }

@@ -906,7 +906,8 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
         return fail(SELSCAN_ERR_INVALID_ARG, "y overlaps state");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N, (flags & SELSCAN_FLAG_ZOH) ? 1 : 0};
+    StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N};
+    const bool zoh = (flags & SELSCAN_FLAG_ZOH) != 0;
     const int64_t chains = Bsz * D;
     // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
     // must divide the warp so that a chain's lanes never straddle two warps.
@@ -924,7 +925,10 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
         const unsigned nb = (unsigned)blocks;
 #define SELSCAN_STEP_CASE(g, v) \
-        if (G == g && V == v) { step_vec_kernel<g, v><<<nb, kStepThreads, 0, st>>>(a); }
+        if (G == g && V == v) { \
+            if (zoh) step_vec_kernel<g, v, true><<<nb, kStepThreads, 0, st>>>(a); \
+            else step_vec_kernel<g, v, false><<<nb, kStepThreads, 0, st>>>(a); \
+        }
         SELSCAN_STEP_CASE(1, 1) else SELSCAN_STEP_CASE(2, 1) else SELSCAN_STEP_CASE(4, 1)
         else SELSCAN_STEP_CASE(8, 1) else SELSCAN_STEP_CASE(16, 1)
         else SELSCAN_STEP_CASE(1, 2) else SELSCAN_STEP_CASE(2, 2) else SELSCAN_STEP_CASE(4, 2)
@@ -934,7 +938,8 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
     } else {
         const int64_t blocks = (chains + kStepThreads - 1) / kStepThreads;
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-        step_scalar_kernel<<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
+        if (zoh) step_scalar_kernel<true><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
+        else step_scalar_kernel<false><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
