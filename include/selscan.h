@@ -14,15 +14,18 @@
  *       y[b,t,d] = sum_n h[n] * C[b,t,n]
  *     hT[b,d,n] = h[n]
  *
- * deltaB is the simplified dl * B of that listing (not the zero-order-hold
- * form of section 2.2). The hidden state h never goes to device memory:
+ * deltaB is the simplified dl * B of that listing; selscan_fwd_ex offers
+ * the zero-order-hold form of section 2.2 instead, and selscan_fwd_gated /
+ * selscan_fwd_ex the block's skip and gate around the scan (section 3.4).
+ * The hidden state h never goes to device memory:
  * it lives in registers; long sequences are cut into chunks whose carries
  * are composed as associative (decay, offset) pairs (booiljung.github.io
  * section 3.1.5.2, the parallel scan).
  *
  * Conventions shared by every entry point
  *  - Every tensor argument is a DEVICE pointer (memory the current CUDA
- *    device can read), row-major and contiguous, last axis fastest. The
+ *    device can read), except in selscan_fwd_host, whose tensors are all in
+ *    host memory; always row-major and contiguous, last axis fastest. The
  *    caller owns all of them; the library keeps no pointer after a call
  *    returns.
  *  - dtype selects the element type of x, delta, B, C and y:
@@ -207,7 +210,7 @@ int selscan_step_ex(float *state, const float *x, const float *delta, const floa
  * SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB); every GPU that loads the library
  * holds it until the process exits. A call whose plan needs more scratch
  * (the workspace_bytes that selscan_fwd_plan reports; about
- * 8 * (chunks - 1) * Bsz * D * N bytes) returns SELSCAN_ERR_UNSUPPORTED
+ * 4 * (chunks - 1) * Bsz * D * (N + 1) bytes) returns SELSCAN_ERR_UNSUPPORTED
  * before anything is launched; run such a problem through selscan_fwd, or in
  * pieces along L, handing hT of one piece to h0 of the next.
  *
@@ -234,8 +237,9 @@ int selscan_fwd_noalloc(const void *x, const void *delta, const float *A, const 
  *   launches        : kernels one selscan_fwd call enqueues
  *   workspace_bytes : chunk-carry workspace the call uses (0 for one chunk)
  * Any output pointer may be NULL. The figures assume 16-byte aligned
- * tensors (alignment decides between the TMA-staged and the plain kernels). Same size checks as selscan_fwd; needs a
- * CUDA device (it reads the SM count). The plan depends only on the sizes,
+ * tensors (alignment decides between the TMA-staged and the plain
+ * kernels). Same size checks as selscan_fwd; needs a CUDA device (it reads
+ * the SM count). The plan depends only on the sizes,
  * dtype and device, plus the tuning variables SELSCAN_CHUNK and
  * SELSCAN_TARGET_WARPS when set.
  */

@@ -27,12 +27,12 @@ def sources():
 
 
 def source_digest() -> str:
-    """sha256 over the kernel sources and the public header (identifies the
-    build a profile was taken on)."""
+    """sha256 over the CUDA sources (identifies the kernels a profile was
+    taken on; the public header's comments do not change them)."""
     import hashlib
     h = hashlib.sha256()
     for p in sources():
-        if p.endswith(".py"):
+        if p.endswith(".py") or p.endswith(".h"):
             continue
         h.update(os.path.basename(p).encode())
         h.update(open(p, "rb").read())
