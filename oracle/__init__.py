@@ -78,6 +78,8 @@ class Oracle:
                                                         I64, I64, I64, I64, INT, INT, INT]
         lib.oracle_selscan_step_gated.restype = INT
         lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
+        lib.oracle_conv1d.restype = INT
+        lib.oracle_conv1d.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT]
         self._lib = lib
         self.path = path
 
@@ -185,6 +187,27 @@ class Oracle:
         return y
 
 
+    def conv1d(self, x, w, bias=None, state_in=None, silu=True):
+        """Causal depthwise convolution over L with K taps per channel, then
+        SiLU (the MambaBlock's conv1d): x (Bsz, L, D), w (D, K), bias (D,) or
+        None, state_in (Bsz, D, K-1) or None (zeros). Returns (out (Bsz, L, D)
+        float64, state_out (Bsz, D, K-1) float32: the last K-1 inputs)."""
+        x = np.asarray(x)
+        Bsz, L, D = x.shape
+        K = np.asarray(w).shape[1]
+        x = _f32(x, (Bsz, L, D), "x")
+        w = _f32(w, (D, K), "w")
+        bias = None if bias is None else _f32(bias, (D,), "bias")
+        state_in = None if state_in is None else _f32(state_in, (Bsz, D, K - 1), "state_in")
+        out = np.zeros((Bsz, L, D), np.float64)
+        st = np.zeros((Bsz, D, K - 1), np.float32)
+        rc = self._lib.oracle_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(state_in), _ptr(out), _ptr(st),
+                                     Bsz, L, D, K, int(bool(silu)))
+        if rc != 0:
+            raise RuntimeError("oracle_conv1d failed")
+        return out, st
+
+
 def compile_variant(src: str, out: str) -> Oracle:
     """Build and load a copy of the oracle from another C source file
     (the mutation tests plant mistakes this way, on the CPU)."""
@@ -216,3 +239,7 @@ def selscan_fwd_chains(*args, **kwargs):
 
 def selscan_step(*args, **kwargs):
     return default().selscan_step(*args, **kwargs)
+
+
+def conv1d(*args, **kwargs):
+    return default().conv1d(*args, **kwargs)

@@ -356,3 +356,55 @@ int oracle_selscan_step_gated(double *state, const float *x, const float *delta,
     }
     return 0;
 }
+
+/* ---- the causal depthwise convolution before the scan ------------------
+ * youngju.dev "Mamba: Selective State Space Models", section 3.4, the
+ * MambaBlock listing: a Conv1d over the sequence with one filter of d_conv
+ * taps per channel (groups = channels), padded by d_conv - 1 in front and cut
+ * back to L outputs, then SiLU:
+ *   out[b,t,d] = silu(bias[d] + sum_{k<K} w[d,k] * x[b, t-K+1+k, d])
+ * Inputs before t = 0 come from state_in (Bsz, D, K-1), the previous K-1
+ * inputs of each channel, oldest first (zeros when NULL); state_out
+ * receives the last K-1 inputs in the same layout. bias may be NULL
+ * (zero); silu = 0 leaves the sum as it is. out: (Bsz, L, D) double.
+ * The decode step is the same with L = 1 and the state updated in place. */
+int oracle_conv1d(const float *x, const float *w, const float *bias,
+                  const float *state_in, double *out, float *state_out,
+                  int64_t Bsz, int64_t L, int64_t D, int64_t K, int silu)
+{
+    if (Bsz < 0 || L < 0 || D < 0 || K < 1 || (L > 0 && !x) || !w)
+        return -1;
+    for (int64_t b = 0; b < Bsz; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            /* the value of x at time tau (tau < 0: from the carried state) */
+            for (int64_t t = 0; t < L; ++t) {
+                double acc = bias ? (double)bias[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    int64_t tau = t - (K - 1) + k;
+                    double v;
+                    if (tau >= 0)
+                        v = (double)x[(b * L + tau) * D + d];
+                    else
+                        v = state_in ? (double)state_in[(b * D + d) * (K - 1) + (K - 1 + tau)] : 0.0;
+                    acc += (double)w[d * K + k] * v;
+                }
+                if (silu)
+                    acc = acc / (1.0 + exp(-acc));
+                if (out)
+                    out[(b * L + t) * D + d] = acc;
+            }
+            if (state_out) {
+                for (int64_t j = 0; j < K - 1; ++j) {
+                    int64_t tau = L - (K - 1) + j;   /* the last K-1 inputs, oldest first */
+                    float v;
+                    if (tau >= 0)
+                        v = x[(b * L + tau) * D + d];
+                    else
+                        v = state_in ? state_in[(b * D + d) * (K - 1) + (K - 1 + tau)] : 0.0f;
+                    state_out[(b * D + d) * (K - 1) + j] = v;
+                }
+            }
+        }
+    }
+    return 0;
+}

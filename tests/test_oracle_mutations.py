@@ -72,6 +72,11 @@ MUTATIONS = {
     "zoh_without_division": ("return w == 0.0 ? 1.0 : expm1(w) / w;", "return w == 0.0 ? 1.0 : expm1(w);"),
     "zoh_uses_exp": ("return w == 0.0 ? 1.0 : expm1(w) / w;", "return w == 0.0 ? 1.0 : exp(w) / w;"),
     "zoh_flag_ignored": ("            if (zoh)\n                dB *= zoh_factor(dl * (double)A[d * N + n]);\n", ""),
+    "conv_taps_reversed": ("acc += (double)w[d * K + k] * v;", "acc += (double)w[d * K + (K - 1 - k)] * v;"),
+    "conv_bias_dropped": ("double acc = bias ? (double)bias[d] : 0.0;", "double acc = 0.0;"),
+    "conv_shift_off_by_one": ("int64_t tau = t - (K - 1) + k;", "int64_t tau = t - K + k;"),
+    "conv_state_newest_first": ("v = state_in ? (double)state_in[(b * D + d) * (K - 1) + (K - 1 + tau)] : 0.0;",
+                                "v = state_in ? (double)state_in[(b * D + d) * (K - 1) + (-1 - tau)] : 0.0;"),
     "step_dropped_input": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];",
                            "            h[n] = dA * h[n];\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];"),
 }

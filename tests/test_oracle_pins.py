@@ -489,3 +489,60 @@ def test_zoh_steps_equal_zoh_forward(orc):
         yt = orc.selscan_step(st, x[:, t], u[:, t], A, B[:, t], C[:, t], zoh=True)
         assert np.allclose(yt, y[:, t], rtol=1e-13, atol=1e-13)
     assert np.allclose(st, hT, rtol=1e-13, atol=1e-13)
+
+
+# ---- the causal depthwise convolution before the scan (section 3.4) ---------
+
+def conv_inputs(Bsz, L, D, K, seed):
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((Bsz, L, D)).astype(np.float32)
+    w = g.standard_normal((D, K)).astype(np.float32)
+    bias = g.standard_normal(D).astype(np.float32)
+    return x, w, bias
+
+
+def test_conv_is_a_fir_filter(orc):
+    """Without SiLU each channel is numpy's full convolution with the taps in
+    reverse order, cut to the first L outputs, plus the bias."""
+    x, w, bias = conv_inputs(2, 37, 5, 4, seed=51)
+    out, _ = orc.conv1d(x, w, bias, silu=False)
+    for b in range(2):
+        for d in range(5):
+            ref = np.convolve(x[b, :, d].astype(np.float64), w[d, ::-1].astype(np.float64))[:37] + bias[d]
+            assert np.allclose(out[b, :, d], ref, rtol=1e-14, atol=1e-14)
+
+
+def test_conv_silu(orc):
+    from scipy.special import expit
+    x, w, bias = conv_inputs(1, 20, 3, 4, seed=52)
+    lin, _ = orc.conv1d(x, w, bias, silu=False)
+    out, _ = orc.conv1d(x, w, bias, silu=True)
+    assert np.allclose(out, lin * expit(lin), rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 7])
+def test_conv_streams_through_its_state(orc, K):
+    """Cutting the sequence anywhere and handing the last K-1 inputs over as
+    the state gives the same outputs and the same final state; decode steps
+    of one token each do too."""
+    x, w, bias = conv_inputs(2, 30, 4, K, seed=53 + K)
+    full, st_full = orc.conv1d(x, w, bias)
+    a, st_a = orc.conv1d(x[:, :11], w, bias)
+    b_, st_b = orc.conv1d(x[:, 11:], w, bias, state_in=st_a)
+    assert np.array_equal(np.concatenate([a, b_], axis=1), full)
+    assert np.array_equal(st_b, st_full)
+    st = None
+    for t in range(30):
+        o, st = orc.conv1d(x[:, t:t + 1], w, bias, state_in=st)
+        assert np.array_equal(o[:, 0], full[:, t])
+    assert np.array_equal(st, st_full)
+    if K > 1:
+        assert np.array_equal(st_full, np.transpose(x[:, -(K - 1):], (0, 2, 1)))
+
+
+def test_conv_single_tap_is_pointwise(orc):
+    from scipy.special import expit
+    x, w, bias = conv_inputs(1, 9, 3, 1, seed=58)
+    out, st = orc.conv1d(x, w, bias)
+    lin = x.astype(np.float64) * w[:, 0].astype(np.float64) + bias.astype(np.float64)
+    assert np.allclose(out, lin * expit(lin), rtol=1e-14, atol=1e-15) and st.shape == (1, 3, 0)
