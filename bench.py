@@ -328,6 +328,8 @@ def run_gpu(args, world, rank, local):
     w = W.WORKLOADS[args.workload]
     if w.steps:
         return run_decode(args, world, rank, local, dev, w)
+    if w.conv_K:
+        return run_conv(args, world, rank, local, dev, w)
     inp = W.workload_inputs(args.workload)
     bf16 = w.dtype == W.BF16
     es = 2 if bf16 else 4
@@ -467,6 +469,90 @@ def run_gpu(args, world, rank, local):
                        dtype="bf16 io, f32 math" if bf16 else "f32")
 
 
+def run_conv(args, world, rank, local, dev, w):
+    """The conv1d workload: one step = one selscan_conv1d (K taps, SiLU) over
+    (Bsz, L, D), a carried state handed in and out. Input sets rotate past
+    2x L2. HBM-bound: x read and out written once."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+
+    K = w.conv_K
+    x, wt, bias, state = W.conv_inputs(w.Bsz, w.L, w.D, K, seed=w.seed, with_state=True)
+    es = 4
+    foot = 2 * w.Bsz * w.L * w.D * es
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(1, -(-(2 * l2) // foot))
+    xs = [torch.from_numpy(x).to(dev) for _ in range(copies)]
+    outs = [torch.empty_like(xs[0]) for _ in range(copies)]
+    wd, bd, sd = (torch.from_numpy(a).to(dev) for a in (wt, bias, state))
+    so = torch.empty_like(sd)
+
+    def step(i):
+        ss.conv1d(xs[i % copies], wd, bd, state_in=sd, out=outs[i % copies], state_out=so)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, dev)
+    ss.check_device_error()
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    per_step = sec / args.steps
+    elems = w.Bsz * w.L * w.D
+    value = world * elems * args.steps / sec
+
+    hx = torch.from_numpy(x).pin_memory()
+    hy = torch.empty(hx.shape, dtype=hx.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 20))
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        yd, _ = ss.conv1d(hx.to(dev, non_blocking=True), wd, bd, state_in=sd, state_out=so)
+        hy.copy_(yd, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": hx.numel() * 4, "d2h_bytes_per_step": hy.numel() * 4}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    hbm_gbs, max_mhz, src = read_measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pk = peaks(sms, max_mhz, hbm_gbs)
+    pk["source"] = f"HBM {src}"
+    nbytes = 2 * elems * es + w.D * (K + 1) * 4 + 2 * w.Bsz * w.D * (K - 1) * 4
+    work = {"elems": elems, "updates": elems * K, "bytes": nbytes, "mufu": 2 * elems, "fp32": (K + 2) * elems}
+    roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload), kernel="selscan_conv1d (1 launch)")
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        thr = 1
+        t0 = time.perf_counter()
+        oracle.default().conv1d(x, wt, bias, state_in=state)
+        secs = time.perf_counter() - t0
+        cpu = {"value": elems / secs, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"the whole workload ({elems} elements, {secs:.2f} s, fp64, one thread)"}
+    config = {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} K={K} f32, causal depthwise conv1d + SiLU",
+              "global_batch": w.Bsz * world, "seq_len": w.L, "parallelism": f"replicas x{world}",
+              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
+    return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                       ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
+                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+
+
 def run_decode(args, world, rank, local, dev, w):
     """The decode workload: one step = one selscan_step over (Bsz, D, N).
     Eight independent decode streams (state and per-step inputs each) are
@@ -603,6 +689,8 @@ def run_reference(args, world, rank):
     w = W.WORKLOADS[args.workload]
     if w.steps:
         return run_reference_decode(args, world, w)
+    if w.conv_K:
+        return run_reference_conv(args, world, w)
     inp = W.workload_inputs(args.workload)
     gate = W.workload_gate_inputs(args.workload) if w.gated else None
     Bsz, L, D = inp.x.shape
@@ -626,6 +714,33 @@ def run_reference(args, world, rank):
                                + (", zero-order hold" if w.zoh else ""),
                    "seq_len": L, "parallelism": "host threads"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_conv(args, world, w):
+    """Reference arm for the conv1d workload: each step is one oracle
+    convolution over the whole workload, on the host."""
+    import oracle
+    from selective_state_space_157_b300 import workloads as W
+    x, wt, bias, state = W.conv_inputs(w.Bsz, w.L, w.D, w.conv_K, seed=w.seed, with_state=True)
+    o = oracle.default()
+    for _ in range(args.warmup):
+        o.conv1d(x, wt, bias, state_in=state)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.conv1d(x, wt, bias, state_in=state)
+    tot = time.perf_counter() - t0
+    elems = w.Bsz * w.L * w.D
+    value = elems * args.steps / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} K={w.conv_K} f32, causal depthwise conv1d + SiLU",
+                   "seq_len": w.L, "parallelism": "host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the whole workload per step ({elems} elements, fp64)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -667,7 +782,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")

@@ -273,6 +273,38 @@ int selscan_fwd_host(const void *x, const void *delta, const float *A, const voi
                      const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
                      int dtype, int delta_softplus, const float *h0, float *hT, void *stream);
 
+/*
+ * selscan_conv1d -- the causal depthwise convolution and SiLU in front of
+ * the scan (youngju.dev "Mamba: Selective State Space Models", section 3.4,
+ * the MambaBlock listing: Conv1d with one filter of K taps per channel,
+ * padded by K - 1 in front and cut back to L outputs, then SiLU):
+ *
+ *   out[b,t,d] = silu(bias[d] + sum_{k<K} w[d,k] * x[b, t-K+1+k, d])
+ *
+ *   x, out    : (Bsz, L, D), dtype     w : (D, K) fp32    bias : (D) fp32 or NULL
+ *   state_in  : (Bsz, D, K-1) fp32 or NULL   the K-1 inputs before t = 0 of
+ *               every channel, oldest first (NULL = zeros: a fresh sequence)
+ *   state_out : (Bsz, D, K-1) fp32 or NULL   receives the last K-1 inputs, for
+ *               the next piece of the sequence or for selscan_conv1d_step
+ *   silu      : 0 leaves the sum without the SiLU
+ *
+ * Sizes: Bsz, L, D >= 0 (Bsz <= 65535, L <= 65535 * 64); 1 <= K <= 8
+ * (K = 1 carries no state). out must not overlap any input; state_out must
+ * not overlap out or any input (state_in included: pass another buffer).
+ * L == 0 copies state_in (or zeros) to state_out. Errors as for selscan_fwd.
+ * Bound by HBM bandwidth: x is read once and out written once.
+ */
+int selscan_conv1d(const void *x, const float *w, const float *bias, void *out, int64_t Bsz,
+                   int64_t L, int64_t D, int64_t K, int dtype, int silu, const float *state_in,
+                   float *state_out, void *stream);
+
+/* One decode step of selscan_conv1d, fp32: out (Bsz, D) from the carried
+ * conv_state (Bsz, D, K-1, oldest first) and this token's x (Bsz, D); the
+ * state then shifts by one and takes x, in place. conv_state may be NULL
+ * when K == 1. out must not overlap conv_state or an input. */
+int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const float *bias,
+                        float *out, int64_t Bsz, int64_t D, int64_t K, int silu, void *stream);
+
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on
  * the same thread. */

@@ -19,7 +19,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "fwd_plan", "last_error", "check_device_error",
+__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
            "MAX_N", "FLAG_SOFTPLUS", "FLAG_ZOH"]
@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_step_ex.restype = INT
         L.selscan_step_ex.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, INT, P]
+        L.selscan_conv1d.restype = INT
+        L.selscan_conv1d.argtypes = [P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_conv1d_step.restype = INT
+        L.selscan_conv1d_step.argtypes = [P, P, P, P, P, I64, I64, I64, INT, P]
         L.selscan_fwd_host.restype = INT
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
@@ -273,6 +277,63 @@ def selscan_step(state, x, delta, A, B, C, y=None, stream=None, D_skip=None, z=N
                                     _ptr(y), Bsz, D, N, _stream_ptr(stream))
     _check(rc)
     return y
+
+
+def conv1d(x, w, bias=None, silu: bool = True, state_in=None, return_state: bool = False, out=None,
+           state_out=None, stream=None):
+    """Causal depthwise convolution and SiLU in front of the scan (see
+    ``include/selscan.h``, selscan_conv1d): x (Bsz, L, D) float32 or
+    bfloat16, w (D, K) float32, bias (D,) or None, state_in (Bsz, D, K-1)
+    float32 or None. Returns out (like x), or (out, state_out) with the last
+    K-1 inputs when ``return_state``. Device tensors only."""
+    import torch
+    dev = x.device
+    Bsz, L, D = x.shape
+    K = w.shape[1] if w.dim() == 2 else -1
+    code = _dtype_code(x)
+    _need(x, "x", (Bsz, L, D), x.dtype, dev)
+    _need(w, "w", (D, K), torch.float32, dev)
+    if bias is not None:
+        _need(bias, "bias", (D,), torch.float32, dev)
+    if state_in is not None:
+        _need(state_in, "state_in", (Bsz, D, K - 1), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _need(out, "out", (Bsz, L, D), x.dtype, dev)
+    if return_state and state_out is None:
+        state_out = torch.empty((Bsz, D, K - 1), dtype=torch.float32, device=dev)
+    if state_out is not None:
+        _need(state_out, "state_out", (Bsz, D, K - 1), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), Bsz, L, D, K, code,
+                                  int(bool(silu)), _ptr(state_in), _ptr(state_out), _stream_ptr(stream))
+    _check(rc)
+    return (out, state_out) if (return_state or state_out is not None) else out
+
+
+def conv1d_step(conv_state, x, w, bias=None, silu: bool = True, out=None, stream=None):
+    """One decode step of conv1d (selscan_conv1d_step): conv_state
+    (Bsz, D, K-1) float32 is updated in place; returns out (Bsz, D)."""
+    import torch
+    dev = x.device
+    Bsz, D = x.shape
+    K = w.shape[1] if w.dim() == 2 else -1
+    f = torch.float32
+    _need(x, "x", (Bsz, D), f, dev)
+    _need(w, "w", (D, K), f, dev)
+    _need(conv_state, "conv_state", (Bsz, D, K - 1), f, dev)
+    if bias is not None:
+        _need(bias, "bias", (D,), f, dev)
+    if out is None:
+        out = torch.empty((Bsz, D), dtype=f, device=dev)
+    else:
+        _need(out, "out", (Bsz, D), f, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_conv1d_step(_ptr(conv_state) if K > 1 else None, _ptr(x), _ptr(w), _ptr(bias),
+                                       _ptr(out), Bsz, D, K, int(bool(silu)), _stream_ptr(stream))
+    _check(rc)
+    return out
 
 
 # ---- host tensors: copy in, run on the current device, copy out ------------

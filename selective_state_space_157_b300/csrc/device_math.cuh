@@ -52,6 +52,12 @@ __device__ __forceinline__ float silu(float z)
     return __fdividef(z, 1.0f + ex2(-z * kLog2e));
 }
 
+// sigmoid(z) = 1 / (1 + e^-z), so that silu(z) = z * silu_gate(z).
+__device__ __forceinline__ float silu_gate(float z)
+{
+    return __fdividef(1.0f, 1.0f + ex2(-z * kLog2e));
+}
+
 __device__ __forceinline__ float block_out(float y, float dsk, float x, bool gated, float z)
 {
     y = fmaf(dsk, x, y);

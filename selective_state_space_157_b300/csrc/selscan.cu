@@ -15,6 +15,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "conv1d.cuh"
 #include "scan_fwd.cuh"
 #include "scan_step.cuh"
 #include "scan_fused.cuh"
@@ -940,6 +941,126 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
         if (zoh) step_scalar_kernel<true><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
         else step_scalar_kernel<false><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+}
+
+// ---- causal depthwise convolution before the scan ------------------------
+
+namespace selscan {
+namespace {
+
+template <typename T>
+int launch_conv1d(const ConvArgs &a, int64_t K, cudaStream_t st)
+{
+    const dim3 grid((unsigned)((a.D + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
+                    (unsigned)((a.L + kConvT - 1) / kConvT));
+    switch (K) {
+    case 1: conv1d_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 2: conv1d_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 3: conv1d_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 4: conv1d_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 5: conv1d_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 6: conv1d_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 7: conv1d_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a); break;
+    default: conv1d_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+}
+
+} // namespace
+} // namespace selscan
+
+extern "C" int selscan_conv1d(const void *x, const float *w, const float *bias, void *out, int64_t Bsz,
+                              int64_t L, int64_t D, int64_t K, int dtype, int silu, const float *state_in,
+                              float *state_out, void *stream)
+{
+    g_err[0] = '\0';
+    if (dtype != SELSCAN_F32 && dtype != SELSCAN_BF16)
+        return fail(SELSCAN_ERR_INVALID_ARG, "dtype %d is neither SELSCAN_F32 nor SELSCAN_BF16", dtype);
+    if (Bsz < 0 || L < 0 || D < 0)
+        return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld L=%lld D=%lld)", (long long)Bsz,
+                    (long long)L, (long long)D);
+    if (K < 1 || K > kConvMaxK)
+        return fail(K < 1 ? SELSCAN_ERR_INVALID_ARG : SELSCAN_ERR_UNSUPPORTED, "K=%lld must be in 1..%d",
+                    (long long)K, kConvMaxK);
+    int64_t nld, nds;
+    if (!mul_ok(Bsz, L, D, &nld) || !mul_ok(Bsz, D, K - 1, &nds))
+        return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
+    if (Bsz == 0 || D == 0)
+        return SELSCAN_OK;
+    if (Bsz > 65535 || (L + kConvT - 1) / kConvT > 65535 || (D + kConvThreads - 1) / kConvThreads > 0x7fffffffLL)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large (Bsz <= 65535, L <= %lld)", 65535LL * kConvT);
+    const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
+    if (!w || (L > 0 && (!x || !out)))
+        return fail(SELSCAN_ERR_INVALID_ARG, "w, and x and out when L > 0, must be non-NULL");
+    if (!aligned(x, es) || !aligned(out, es) || !aligned(w, 4) || !aligned(bias, 4) || !aligned(state_in, 4) ||
+        !aligned(state_out, 4))
+        return fail(SELSCAN_ERR_INVALID_ARG, "x and out must be aligned to their element size, the rest to 4 bytes");
+    const Range ro = range(L > 0 ? out : nullptr, nld * (int64_t)es, "out"), rs = range(state_out, nds * 4, "state_out");
+    const Range ins[] = {range(L > 0 ? x : nullptr, nld * (int64_t)es, "x"), range(w, D * K * 4, "w"),
+                         range(bias, D * 4, "bias"), range(state_in, nds * 4, "state_in")};
+    for (const Range &r : ins) {
+        if (overlaps(ro, r)) return fail(SELSCAN_ERR_INVALID_ARG, "out overlaps %s", r.name);
+        if (overlaps(rs, r)) return fail(SELSCAN_ERR_INVALID_ARG, "state_out overlaps %s", r.name);
+    }
+    if (overlaps(ro, rs))
+        return fail(SELSCAN_ERR_INVALID_ARG, "out overlaps state_out");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (L == 0) {   // the carried state passes through unchanged
+        if (!state_out || nds == 0) return SELSCAN_OK;
+        cudaError_t e = state_in ? cudaMemcpyAsync(state_out, state_in, (size_t)nds * 4, cudaMemcpyDeviceToDevice, st)
+                                 : cudaMemsetAsync(state_out, 0, (size_t)nds * 4, st);
+        return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state copy");
+    }
+    ConvArgs a{x, w, bias, out, state_in, state_out, Bsz, L, D, silu ? 1 : 0};
+    return dtype == SELSCAN_F32 ? launch_conv1d<float>(a, K, st) : launch_conv1d<__nv_bfloat16>(a, K, st);
+}
+
+extern "C" int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const float *bias,
+                                   float *out, int64_t Bsz, int64_t D, int64_t K, int silu, void *stream)
+{
+    g_err[0] = '\0';
+    if (Bsz < 0 || D < 0)
+        return fail(SELSCAN_ERR_INVALID_ARG, "negative size (Bsz=%lld D=%lld)", (long long)Bsz, (long long)D);
+    if (K < 1 || K > kConvMaxK)
+        return fail(K < 1 ? SELSCAN_ERR_INVALID_ARG : SELSCAN_ERR_UNSUPPORTED, "K=%lld must be in 1..%d",
+                    (long long)K, kConvMaxK);
+    int64_t nd, nds;
+    if (!mul_ok(Bsz, D, 1, &nd) || !mul_ok(Bsz, D, K - 1, &nds))
+        return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
+    if (Bsz == 0 || D == 0)
+        return SELSCAN_OK;
+    if (!x || !w || !out || (K > 1 && !conv_state))
+        return fail(SELSCAN_ERR_INVALID_ARG, "x, w, out (and conv_state when K > 1) must be non-NULL");
+    const void *ptrs[] = {conv_state, x, w, bias, out};
+    for (const void *p : ptrs)
+        if (!aligned(p, 4))
+            return fail(SELSCAN_ERR_INVALID_ARG, "every pointer must be 4-byte aligned");
+    const Range rs = range(K > 1 ? conv_state : nullptr, nds * 4, "conv_state"), ro = range(out, nd * 4, "out");
+    const Range ins[] = {range(x, nd * 4, "x"), range(w, D * K * 4, "w"), range(bias, D * 4, "bias")};
+    for (const Range &r : ins) {
+        if (overlaps(rs, r)) return fail(SELSCAN_ERR_INVALID_ARG, "conv_state overlaps %s", r.name);
+        if (overlaps(ro, r)) return fail(SELSCAN_ERR_INVALID_ARG, "out overlaps %s", r.name);
+    }
+    if (overlaps(rs, ro))
+        return fail(SELSCAN_ERR_INVALID_ARG, "out overlaps conv_state");
+    const int64_t blocks = (nd + kConvThreads - 1) / kConvThreads;
+    if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+    ConvStepArgs a{conv_state, x, w, bias, out, Bsz, D, silu ? 1 : 0};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const unsigned nb = (unsigned)blocks;
+    switch (K) {
+    case 1: conv1d_step_kernel<1><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 2: conv1d_step_kernel<2><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 3: conv1d_step_kernel<3><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 4: conv1d_step_kernel<4><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 5: conv1d_step_kernel<5><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 6: conv1d_step_kernel<6><<<nb, kConvThreads, 0, st>>>(a); break;
+    case 7: conv1d_step_kernel<7><<<nb, kConvThreads, 0, st>>>(a); break;
+    default: conv1d_step_kernel<8><<<nb, kConvThreads, 0, st>>>(a); break;
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");

@@ -29,7 +29,8 @@ F32 = "f32"
 BF16 = "bf16"
 
 # tensor ids of the per-tensor random streams
-_TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6, "Dskip": 7, "z": 8}
+_TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6, "Dskip": 7, "z": 8, "conv_w": 9, "conv_b": 10,
+        "conv_state": 11}
 
 
 @dataclass(frozen=True)
@@ -48,6 +49,7 @@ class Workload:
     return_state: bool = False
     gated: bool = False   # with the block's skip and gate (gate_inputs)
     zoh: bool = False     # zero-order-hold discretisation instead of dl * B
+    conv_K: int = 0       # > 0: the causal conv1d + SiLU before the scan, with K taps
 
     @property
     def elems(self) -> int:
@@ -63,6 +65,7 @@ WORKLOADS = {
     5: Workload(5, "decode", 256, 1, 2560, 16, F32, -3.0, "arange", 105, steps=1024),
     6: Workload(6, "mamba130m-gated", 2, 2048, 1536, 16, F32, -3.0, "arange", 106, gated=True),
     7: Workload(7, "mamba130m-zoh", 2, 2048, 1536, 16, F32, -3.0, "arange", 107, zoh=True),
+    8: Workload(8, "mamba130m-conv1d", 2, 2048, 1536, 16, F32, -3.0, "arange", 108, conv_K=4),
 }
 
 
@@ -195,3 +198,19 @@ def workload_gate_inputs(wid: int):
     """(Dskip, z) of a gated forward workload."""
     w = WORKLOADS[wid]
     return gate_inputs(w.Bsz, w.L, w.D, seed=w.seed, dtype=w.dtype)
+
+
+def conv_inputs(Bsz: int, L: int, D: int, K: int, *, seed: int, dtype: str = F32, with_state: bool = False):
+    """Inputs of the causal depthwise convolution before the scan: x like the
+    scan's input (Bsz, L, D) ~ N(0, 1) (bf16 bit patterns for bf16 I/O),
+    taps w (D, K) and bias (D,) ~ U(-1/sqrt(K), 1/sqrt(K)) (the usual
+    initialisation of a Conv1d with K inputs per output), and optionally a
+    carried state (Bsz, D, K-1) ~ N(0, 1)."""
+    x = normal(rng(seed, _TID["x"]), (Bsz, L, D))
+    if dtype == BF16:
+        x = to_bf16_bits(x)
+    r = 1.0 / np.sqrt(K)
+    w = rng(seed, _TID["conv_w"]).uniform(-r, r, size=(D, K)).astype(np.float32)
+    bias = rng(seed, _TID["conv_b"]).uniform(-r, r, size=(D,)).astype(np.float32)
+    state = normal(rng(seed, _TID["conv_state"]), (Bsz, D, K - 1)) if with_state else None
+    return x, w, bias, state
