@@ -495,13 +495,34 @@ def run_conv(args, world, rank, local, dev, w):
         step(i)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    # The steps are replayed from CUDA graphs (as in the decode workload):
+    # the Python call per step takes longer than the kernel.
+    per_graph = 4 * copies
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(i)
+        return g
+
+    full = capture(per_graph)
+    rest = capture(args.steps % per_graph) if args.steps % per_graph else None
+    stream.wait_stream(side)
+    full.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         e0.record(stream)
-        for i in range(args.steps):
-            step(i)
+        for _ in range(args.steps // per_graph):
+            full.replay()
+        if rest is not None:
+            rest.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(world, dev)
@@ -547,7 +568,8 @@ def run_conv(args, world, rank, local, dev, w):
                "sample": f"the whole workload ({elems} elements, {secs:.2f} s, fp64, one thread)"}
     config = {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} K={K} f32, causal depthwise conv1d + SiLU",
               "global_batch": w.Bsz * world, "seq_len": w.L, "parallelism": f"replicas x{world}",
-              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
+              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2",
+              "launch": f"CUDA graph replay of {per_graph} captured selscan_conv1d calls"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
                        launches=args.steps, clocks=clk.summary(), dtype="f32")

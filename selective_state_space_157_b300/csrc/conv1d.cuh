@@ -23,6 +23,7 @@ namespace selscan {
 constexpr int kConvThreads = 128;
 constexpr int kConvT = 64;        // timesteps per thread
 constexpr int kConvMaxK = 8;
+constexpr int kConvBatch = 8;     // inputs loaded ahead of the stores that use them
 
 struct ConvArgs {
     const void *x;
@@ -68,20 +69,29 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a)
 
     T *op = static_cast<T *>(a.out) + b * L * D + d;
     const int64_t n = L - t0 < kConvT ? L - t0 : kConvT;
-#pragma unroll 8
-    for (int64_t t = t0; t < t0 + n; ++t) {
-        const float xv = Io<T>::load(xp + t * D);
-        float acc = bias;
+    // kConvBatch inputs are loaded before any output of the batch is stored:
+    // out never overlaps x (checked on the host), but the compiler cannot
+    // know that, and would otherwise wait for each load in turn.
+    for (int64_t tb = t0; tb < t0 + n; tb += kConvBatch) {
+        float xv[kConvBatch];
 #pragma unroll
-        for (int k = 0; k < K - 1; ++k)
-            acc = fmaf(w[k], win[k], acc);
-        acc = fmaf(w[K - 1], xv, acc);
+        for (int i = 0; i < kConvBatch; ++i)
+            xv[i] = tb + i < t0 + n ? Io<T>::load(xp + (tb + i) * D) : 0.0f;
 #pragma unroll
-        for (int k = 0; k + 1 < K - 1; ++k)
-            win[k] = win[k + 1];
-        if (K > 1)
-            win[K > 1 ? K - 2 : 0] = xv;
-        Io<T>::store(op + t * D, a.silu ? acc * silu_gate(acc) : acc);
+        for (int i = 0; i < kConvBatch; ++i) {
+            float acc = bias;
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k)
+                acc = fmaf(w[k], win[k], acc);
+            acc = fmaf(w[K - 1], xv[i], acc);
+#pragma unroll
+            for (int k = 0; k + 1 < K - 1; ++k)
+                win[k] = win[k + 1];
+            if (K > 1)
+                win[K > 1 ? K - 2 : 0] = xv[i];
+            if (tb + i < t0 + n)
+                Io<T>::store(op + (tb + i) * D, a.silu ? acc * silu_gate(acc) : acc);
+        }
     }
 
     // The run that ends the sequence hands the last K - 1 inputs over.
@@ -91,6 +101,114 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a)
             const int64_t tau = L - (K - 1) + j;
             a.state_out[(b * D + d) * (K - 1) + j] =
                 tau >= 0 ? Io<T>::load(xp + tau * D) : conv_state_value<K>(a, b, d, tau);
+        }
+    }
+}
+
+// Four consecutive channels per thread (16-byte fp32 or 8-byte bf16 loads
+// and stores), kConvVecT timesteps per run; taken when D is a multiple of 4
+// and x and out are aligned for it. Lanes cover 4 * 32 channels of a row.
+constexpr int kConvVecT = 32;
+
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+    using S = float4;
+    __device__ __forceinline__ static float4 load(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    __device__ __forceinline__ static void store(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    __device__ __forceinline__ static float4 load(const __nv_bfloat16 *p)
+    {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *p, float4 v)
+    {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
+};
+
+__device__ __forceinline__ float conv_out(float acc, int silu)
+{
+    return silu ? acc * silu_gate(acc) : acc;
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv1d_vec_kernel(const ConvArgs a)
+{
+    const int64_t d0 = ((int64_t)blockIdx.x * kConvThreads + threadIdx.x) * 4;
+    const int64_t b = blockIdx.y;
+    const int64_t t0 = (int64_t)blockIdx.z * kConvVecT;
+    if (d0 >= a.D)
+        return;
+    const int64_t D = a.D, L = a.L;
+    float4 w[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+        w[k] = make_float4(__ldg(a.w + d0 * K + k), __ldg(a.w + (d0 + 1) * K + k),
+                           __ldg(a.w + (d0 + 2) * K + k), __ldg(a.w + (d0 + 3) * K + k));
+    const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    const T *xp = static_cast<const T *>(a.x) + b * L * D + d0;
+    float4 win[K > 1 ? K - 1 : 1];
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+        const int64_t tau = t0 - (K - 1) + j;
+        win[j] = tau >= 0 ? Vec4<T>::load(xp + tau * D)
+                          : make_float4(conv_state_value<K>(a, b, d0, tau), conv_state_value<K>(a, b, d0 + 1, tau),
+                                        conv_state_value<K>(a, b, d0 + 2, tau), conv_state_value<K>(a, b, d0 + 3, tau));
+    }
+
+    T *op = static_cast<T *>(a.out) + b * L * D + d0;
+    const int64_t n = L - t0 < kConvVecT ? L - t0 : kConvVecT;
+    for (int64_t tb = t0; tb < t0 + n; tb += kConvBatch) {
+        float4 xb[kConvBatch];
+#pragma unroll
+        for (int i = 0; i < kConvBatch; ++i)
+            xb[i] = tb + i < t0 + n ? Vec4<T>::load(xp + (tb + i) * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kConvBatch; ++i) {
+            const int64_t t = tb + i;
+            const float4 xv = xb[i];
+            float4 acc = bias;
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k) {
+                acc.x = fmaf(w[k].x, win[k].x, acc.x);
+                acc.y = fmaf(w[k].y, win[k].y, acc.y);
+                acc.z = fmaf(w[k].z, win[k].z, acc.z);
+                acc.w = fmaf(w[k].w, win[k].w, acc.w);
+            }
+            acc.x = fmaf(w[K - 1].x, xv.x, acc.x);
+            acc.y = fmaf(w[K - 1].y, xv.y, acc.y);
+            acc.z = fmaf(w[K - 1].z, xv.z, acc.z);
+            acc.w = fmaf(w[K - 1].w, xv.w, acc.w);
+#pragma unroll
+            for (int k = 0; k + 1 < K - 1; ++k)
+                win[k] = win[k + 1];
+            if (K > 1)
+                win[K > 1 ? K - 2 : 0] = xv;
+            if (t < t0 + n)
+                Vec4<T>::store(op + t * D, make_float4(conv_out(acc.x, a.silu), conv_out(acc.y, a.silu),
+                                                        conv_out(acc.z, a.silu), conv_out(acc.w, a.silu)));
+        }
+    }
+
+    if (a.state_out && t0 + n == L) {
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int64_t tau = L - (K - 1) + j;
+            float4 v = tau >= 0 ? Vec4<T>::load(xp + tau * D)
+                                : make_float4(conv_state_value<K>(a, b, d0, tau), conv_state_value<K>(a, b, d0 + 1, tau),
+                                              conv_state_value<K>(a, b, d0 + 2, tau), conv_state_value<K>(a, b, d0 + 3, tau));
+            a.state_out[(b * D + d0) * (K - 1) + j] = v.x;
+            a.state_out[(b * D + d0 + 1) * (K - 1) + j] = v.y;
+            a.state_out[(b * D + d0 + 2) * (K - 1) + j] = v.z;
+            a.state_out[(b * D + d0 + 3) * (K - 1) + j] = v.w;
         }
     }
 }

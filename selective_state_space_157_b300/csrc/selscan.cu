@@ -954,6 +954,27 @@ namespace {
 template <typename T>
 int launch_conv1d(const ConvArgs &a, int64_t K, cudaStream_t st)
 {
+    // Four channels per thread when rows allow vector access (D % 4 == 0,
+    // x and out aligned to 4 elements, bias to 16 bytes).
+    const size_t es = sizeof(T);
+    const bool vec = a.D % 4 == 0 && aligned(a.x, 4 * es) && aligned(a.out, 4 * es) && aligned(a.bias, 16) &&
+                     env_long("SELSCAN_CONV_VEC", 1) != 0;
+    if (vec) {
+        const dim3 grid((unsigned)((a.D / 4 + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
+                        (unsigned)((a.L + kConvVecT - 1) / kConvVecT));
+        switch (K) {
+        case 1: conv1d_vec_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 2: conv1d_vec_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 3: conv1d_vec_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 4: conv1d_vec_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 5: conv1d_vec_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 6: conv1d_vec_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a); break;
+        case 7: conv1d_vec_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a); break;
+        default: conv1d_vec_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a); break;
+        }
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+    }
     const dim3 grid((unsigned)((a.D + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
                     (unsigned)((a.L + kConvT - 1) / kConvT));
     switch (K) {
@@ -991,8 +1012,8 @@ extern "C" int selscan_conv1d(const void *x, const float *w, const float *bias, 
         return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
     if (Bsz == 0 || D == 0)
         return SELSCAN_OK;
-    if (Bsz > 65535 || (L + kConvT - 1) / kConvT > 65535 || (D + kConvThreads - 1) / kConvThreads > 0x7fffffffLL)
-        return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large (Bsz <= 65535, L <= %lld)", 65535LL * kConvT);
+    if (Bsz > 65535 || (L + kConvVecT - 1) / kConvVecT > 65535 || (D + kConvThreads - 1) / kConvThreads > 0x7fffffffLL)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large (Bsz <= 65535, L <= %lld)", 65535LL * kConvVecT);
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     if (!w || (L > 0 && (!x || !out)))
         return fail(SELSCAN_ERR_INVALID_ARG, "w, and x and out when L > 0, must be non-NULL");
