@@ -458,7 +458,7 @@ def run_gpu(args, world, rank, local):
     config = {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={N} {w.dtype}, softplus on"
                           + (", returns hT" if want_hT else "")
                           + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else "")
-                          + (", zero-order-hold Bbar (plain-load kernels)" if w.zoh else ""),
+                          + (", zero-order-hold Bbar" if w.zoh else ""),
               "global_batch": Bsz * world, "seq_len": L, "parallelism": f"replicas x{world}",
               "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2 ({l2 / 1e6:.0f} MB)"
                     if copies > 1 else f"inputs {foot / 1e6:.0f} MB > 2x L2",

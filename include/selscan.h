@@ -147,8 +147,9 @@ int selscan_fwd_gated(const void *x, const void *delta, const float *A, const vo
  *
  * in place of the simplified dl * B[n] (the decay exp(dl A) is the same).
  * phi is evaluated from the decay, or from its series where |w| < 1/16, so
- * A == 0 gives the limit dl * B. The zero-order-hold form runs on the
- * plain-load kernels (not the fused TMA kernel). Unknown flag bits are
+ * A == 0 gives the limit dl * B. The zero-order-hold form runs in the
+ * fused TMA kernel for N <= 16 with 16-byte rows and SELSCAN_FLAG_SOFTPLUS
+ * set, and on the plain-load kernels otherwise. Unknown flag bits are
  * SELSCAN_ERR_INVALID_ARG.
  */
 int selscan_fwd_ex(const void *x, const void *delta, const float *A, const void *B,

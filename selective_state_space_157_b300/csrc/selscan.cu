@@ -228,14 +228,14 @@ int occupancy(const void *fn, size_t smem)
     return n;
 }
 
-template <typename T, int NS, int NSPLIT, bool VEC, bool SP, bool GATE = false>
+template <typename T, int NS, int NSPLIT, bool VEC, bool SP, bool GATE = false, bool ZOH = false>
 bool prepare_fused_sp(int64_t N, FusedLaunch *out)
 {
     constexpr int DPB = kScanThreads / NSPLIT;
     long stages = env_long("SELSCAN_TMA_STAGES", kStages);
     if (stages < 2) stages = 2;
     if (stages > kMaxStages) stages = kMaxStages;
-    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP, GATE>;
+    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP, GATE, ZOH>;
     const int64_t nrow = VEC ? NS * NSPLIT : N;
     const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, (int)stages, GATE);
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
@@ -247,10 +247,19 @@ bool prepare_fused_sp(int64_t N, FusedLaunch *out)
 }
 
 // The block's skip and gate run fused on the vectorised, softplus form (the
-// block's own use); other gated forms take the plain-load path.
+// block's own use); other gated forms take the plain-load path. So does the
+// zero-order hold, for one thread per chain (N <= 16).
 template <typename T, int NS, int NSPLIT>
-bool prepare_fused(bool vec, bool softplus, bool gate, int64_t N, FusedLaunch *out)
+bool prepare_fused(bool vec, bool softplus, bool gate, bool zoh, int64_t N, FusedLaunch *out)
 {
+    if (zoh) {
+        if constexpr (NSPLIT == 1) {
+            if (!(vec && softplus)) return false;
+            return gate ? prepare_fused_sp<T, NS, NSPLIT, true, true, true, true>(N, out)
+                        : prepare_fused_sp<T, NS, NSPLIT, true, true, false, true>(N, out);
+        }
+        return false;
+    }
     if (gate)
         return vec && softplus && prepare_fused_sp<T, NS, NSPLIT, true, true, true>(N, out);
     if (vec)
@@ -261,16 +270,16 @@ bool prepare_fused(bool vec, bool softplus, bool gate, int64_t N, FusedLaunch *o
 }
 
 template <typename T>
-bool pick_fused(int ns, int nsplit, bool vec, bool softplus, bool gate, int64_t N, FusedLaunch *out)
+bool pick_fused(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, FusedLaunch *out)
 {
     switch (ns * 100 + nsplit) {
-    case 401: return prepare_fused<T, 4, 1>(vec, softplus, gate, N, out);
-    case 801: return prepare_fused<T, 8, 1>(vec, softplus, gate, N, out);
-    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, gate, N, out);
-    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, gate, N, out);
-    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, gate, N, out);
-    case 802: return prepare_fused<T, 8, 2>(vec, softplus, gate, N, out);
-    case 404: return prepare_fused<T, 4, 4>(vec, softplus, gate, N, out);
+    case 401: return prepare_fused<T, 4, 1>(vec, softplus, gate, zoh, N, out);
+    case 801: return prepare_fused<T, 8, 1>(vec, softplus, gate, zoh, N, out);
+    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, gate, zoh, N, out);
+    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, gate, zoh, N, out);
+    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, gate, zoh, N, out);
+    case 802: return prepare_fused<T, 8, 2>(vec, softplus, gate, zoh, N, out);
+    case 404: return prepare_fused<T, 4, 4>(vec, softplus, gate, zoh, N, out);
     default: return false;
     }
 }
@@ -387,8 +396,9 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
     const bool sp = a.softplus != 0;
     const bool gate = a.Dskip != nullptr || a.z != nullptr;
     if (a.z && !aligned(a.z, 16)) return SELSCAN_ERR_UNSUPPORTED;
-    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, gate, a.N, &fl)
-                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, gate, a.N, &fl);
+    const bool zoh = a.zoh != 0;
+    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, &fl)
+                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, &fl);
     if (!ok) return SELSCAN_ERR_UNSUPPORTED;
     FusedArgs fa;
     memset(&fa, 0, sizeof fa);
@@ -443,7 +453,7 @@ int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int sm
     a.K = plan.K;
     a.dtiles = plan.dtiles;
     if (a.Bsz * plan.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-    if (plan.tma && !a.zoh) {   // the fused kernel implements the simplified dl * B only
+    if (plan.tma) {
         int rc = launch_fused(a, plan, dtype, sms, ws, st);
         if (rc != SELSCAN_ERR_UNSUPPORTED) return rc;
         g_err[0] = '\0';
