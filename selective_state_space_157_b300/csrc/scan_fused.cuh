@@ -117,7 +117,23 @@ __device__ __forceinline__ void load_state_cg(const float *p, int valid, float2 
 
 // GATE: the readout also applies the block's skip and gate (block_out),
 // with z staged beside x in the ring.
-// ZOH: the zero-order-hold input term (zoh_input) in place of dl * B * x.
+// The zero-order-hold input term of a pair of states, packed and without a
+// branch or a divide: the coefficient dl * phi(w) (see zoh_coef) is the
+// series where |w| < 1/16 and (decay - 1) / A elsewhere, with 1/A held per
+// item (0 where A is 0, where the series is taken). e = dl * A * log2(e).
+__device__ __forceinline__ float2 zoh_pair(float2 dl2, float2 e, float2 decay, float2 ainv, float2 xb)
+{
+    const float2 w = __fmul2_rn(e, make_float2(kLn2, kLn2));
+    float2 p = __ffma2_rn(w, make_float2(1.0f / 24.0f, 1.0f / 24.0f), make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+    p = __ffma2_rn(w, p, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(w, p, make_float2(1.0f, 1.0f));
+    p = __fmul2_rn(p, dl2);
+    const float2 q = __fmul2_rn(__fadd2_rn(decay, make_float2(-1.0f, -1.0f)), ainv);
+    const float2 c = make_float2(fabsf(w.x) < 0.0625f ? p.x : q.x, fabsf(w.y) < 0.0625f ? p.y : q.y);
+    return __fmul2_rn(c, xb);
+}
+
+// ZOH: the zero-order-hold input term (zoh_pair) in place of dl * B * x.
 template <typename T, int NS, int NSPLIT, bool VEC, int TT, bool SOFTPLUS, bool GATE, bool ZOH = false>
 // Three CTAs per SM fit the shared-memory ring; the register cap this implies
 // (168) is above what the kernel needs, and measured faster than 128.
@@ -225,11 +241,14 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 
         const float dsk = (GATE && readout && a.Dskip) ? __ldg(a.Dskip + d) : 0.0f;
         float2 A2[NP];
+        float2 Ainv[ZOH ? NP : 1];   // 1/A for the zero-order hold (0 where A is 0)
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
             const float lo = (2 * j < valid) ? __ldg(a.A + d * N + n0 + 2 * j) : 0.0f;
             const float hi = (2 * j + 1 < valid) ? __ldg(a.A + d * N + n0 + 2 * j + 1) : 0.0f;
             A2[j] = make_float2(lo * kLog2e, hi * kLog2e);
+            if constexpr (ZOH)
+                Ainv[j] = make_float2(lo != 0.0f ? __frcp_rn(lo) : 0.0f, hi != 0.0f ? __frcp_rn(hi) : 0.0f);
         }
 
         // Incoming state: h0 (or zeros), and for a readout of chunk k >= 1
@@ -425,9 +444,12 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     const float2 dl2 = make_float2(dlv[tt], dlv[tt]);
                     const float2 u2 = make_float2(uv[tt], uv[tt]);
                     const float xt = ZOH ? smem_val(xs + tt * DPB) : 0.0f;
-                    auto in_term = [&](int j, float2 decay) {
-                        return ZOH ? zoh_input(dlv[tt], xt, A2[j], decay, Bv[2 * j], Bv[2 * j + 1])
-                                   : __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                    auto in_term = [&](int j, float2 e, float2 decay) {
+                        if constexpr (ZOH)
+                            return zoh_pair(dl2, e, decay, Ainv[j],
+                                            __fmul2_rn(make_float2(xt, xt), make_float2(Bv[2 * j], Bv[2 * j + 1])));
+                        else
+                            return __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
                     };
                     if constexpr (RO) {
                         float Cv[NS];
@@ -437,7 +459,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                         for (int j = 0; j < NP; ++j) {
                             const float2 e = __fmul2_rn(dl2, A2[j]);
                             const float2 decay = make_float2(ex2(e.x), ex2(e.y));
-                            h[j] = __ffma2_rn(decay, h[j], in_term(j, decay));
+                            h[j] = __ffma2_rn(decay, h[j], in_term(j, e, decay));
                             acc[j & 1] = __ffma2_rn(h[j], make_float2(Cv[2 * j], Cv[2 * j + 1]), acc[j & 1]);
                         }
                         const float2 s2 = __fadd2_rn(acc[0], acc[1]);
@@ -455,7 +477,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                         for (int j = 0; j < NP; ++j) {
                             const float2 e = __fmul2_rn(dl2, A2[j]);
                             const float2 decay = make_float2(ex2(e.x), ex2(e.y));
-                            h[j] = __ffma2_rn(decay, h[j], in_term(j, decay));
+                            h[j] = __ffma2_rn(decay, h[j], in_term(j, e, decay));
                         }
                     }
                 };
@@ -485,8 +507,12 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                         for (int j = 0; j < NP; ++j) {
                             const float2 e = __fmul2_rn(dl2, A2[j]);
                             const float2 decay = make_float2(ex2(e.x), ex2(e.y));
-                            const float2 inp = ZOH ? zoh_input(dl, xt, A2[j], decay, Bv[2 * j], Bv[2 * j + 1])
-                                                   : __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                            float2 inp;
+                            if constexpr (ZOH)
+                                inp = zoh_pair(dl2, e, decay, Ainv[j],
+                                               __fmul2_rn(make_float2(xt, xt), make_float2(Bv[2 * j], Bv[2 * j + 1])));
+                            else
+                                inp = __fmul2_rn(u2, make_float2(Bv[2 * j], Bv[2 * j + 1]));
                             h[j] = __ffma2_rn(decay, h[j], inp);
                             if constexpr (RO)
                                 acc = __ffma2_rn(h[j], make_float2(Cv[2 * j], Cv[2 * j + 1]), acc);
