@@ -104,3 +104,101 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ss, "_lib", None)
     with pytest.raises(ImportError):
         ss.lib()
+
+
+# ---- the extended, gated, conv1d and host-buffer entry points ---------------
+
+def fwd_ex(lib, flags=1, Dskip=None, z=None, **kw):
+    a = dict(x=0x10000, delta=0x20000, A=0x30000, B=0x40000, C=0x50000, y=0x60000,
+             Bsz=1, L=8, D=4, N=4, dtype=F32, h0=None, hT=None)
+    a.update(kw)
+    return lib.selscan_fwd_ex(a["x"], a["delta"], a["A"], a["B"], a["C"], Dskip, z, a["y"], a["Bsz"], a["L"],
+                              a["D"], a["N"], a["dtype"], flags, a["h0"], a["hT"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(flags=4), ss.ERR_INVALID_ARG),                       # unknown flag bit
+    (dict(z=0x60000 + 4), ss.ERR_INVALID_ARG),                 # z overlaps y partially
+    (dict(z=0x70000, hT=0x70000 + 8), ss.ERR_INVALID_ARG),     # hT overlaps z
+    (dict(Dskip=0x60000), ss.ERR_INVALID_ARG),                 # y overlaps Dskip
+    (dict(Dskip=0x70002), ss.ERR_INVALID_ARG),                 # misaligned Dskip
+    (dict(z=0x70002), ss.ERR_INVALID_ARG),                     # misaligned z
+    (dict(N=65), ss.ERR_UNSUPPORTED),
+])
+def test_fwd_ex_argument_errors(lib, kw, code):
+    assert fwd_ex(lib, **kw) == code
+    assert ss.last_error() != ""
+
+
+def test_fwd_ex_empty_problem_is_ok_without_cuda(lib):
+    assert fwd_ex(lib, flags=ss.FLAG_SOFTPLUS | ss.FLAG_ZOH, Bsz=0) == ss.OK
+
+
+def test_gated_forward_shares_the_checks(lib):
+    rc = lib.selscan_fwd_gated(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, None, 0x60000 + 4, 0x60000,
+                               1, 8, 4, 4, F32, 1, None, None, None)
+    assert rc == ss.ERR_INVALID_ARG
+
+
+def test_step_ex_takes_zoh_only(lib):
+    rc = lib.selscan_step_ex(0x10000, 0x20000, 0x28000, 0x30000, 0x40000, 0x50000, None, None, 0x60000,
+                             2, 4, 16, ss.FLAG_SOFTPLUS, None)
+    assert rc == ss.ERR_INVALID_ARG and "ZOH" in ss.last_error()
+    rc = lib.selscan_step_ex(0x10000, 0x20000, 0x28000, 0x30000, 0x40000, 0x50000, None, 0x60000, 0x60000,
+                             2, 4, 16, ss.FLAG_ZOH, None)
+    assert rc == ss.ERR_INVALID_ARG                            # y overlaps z
+
+
+def conv(lib, **kw):
+    a = dict(x=0x10000, w=0x20000, bias=None, out=0x30000, Bsz=1, L=8, D=4, K=4, dtype=F32, silu=1,
+             state_in=None, state_out=None)
+    a.update(kw)
+    return lib.selscan_conv1d(a["x"], a["w"], a["bias"], a["out"], a["Bsz"], a["L"], a["D"], a["K"],
+                              a["dtype"], a["silu"], a["state_in"], a["state_out"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), ss.ERR_INVALID_ARG),
+    (dict(K=9), ss.ERR_UNSUPPORTED),
+    (dict(dtype=3), ss.ERR_INVALID_ARG),
+    (dict(L=-1), ss.ERR_INVALID_ARG),
+    (dict(w=None), ss.ERR_INVALID_ARG),
+    (dict(out=0x10000 + 8), ss.ERR_INVALID_ARG),               # out overlaps x (no in-place)
+    (dict(state_in=0x40000, state_out=0x40000), ss.ERR_INVALID_ARG),  # state_out is state_in
+    (dict(state_out=0x20000), ss.ERR_INVALID_ARG),             # state_out overlaps w
+    (dict(x=0x10002), ss.ERR_INVALID_ARG),                     # misaligned
+    (dict(Bsz=70000), ss.ERR_UNSUPPORTED),                     # grid limit
+])
+def test_conv1d_argument_errors(lib, kw, code):
+    assert conv(lib, **kw) == code
+    assert ss.last_error() != ""
+
+
+def test_conv1d_empty_problem_is_ok_without_cuda(lib):
+    assert conv(lib, Bsz=0) == ss.OK
+    assert conv(lib, D=0) == ss.OK
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), ss.ERR_INVALID_ARG),
+    (dict(K=9), ss.ERR_UNSUPPORTED),
+    (dict(state=None), ss.ERR_INVALID_ARG),                    # K > 1 needs the state
+    (dict(out=0x10000), ss.ERR_INVALID_ARG),                   # out overlaps the state
+    (dict(x=0x20001), ss.ERR_INVALID_ARG),
+])
+def test_conv1d_step_argument_errors(lib, kw, code):
+    a = dict(state=0x10000, x=0x20000, w=0x30000, bias=None, out=0x40000, Bsz=2, D=4, K=4, silu=1)
+    a.update(kw)
+    rc = lib.selscan_conv1d_step(a["state"], a["x"], a["w"], a["bias"], a["out"], a["Bsz"], a["D"], a["K"],
+                                 a["silu"], None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("entry", ["selscan_fwd_host", "selscan_fwd_noalloc"])
+def test_host_and_noalloc_forward_share_the_checks(lib, entry):
+    f = getattr(lib, entry)
+    assert f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 1, 8, 4, 4, 9, 1, None, None, None) \
+        == ss.ERR_INVALID_ARG                                  # bad dtype
+    assert f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x10000 + 4, 1, 8, 4, 4, F32, 1, None, None, None) \
+        == ss.ERR_INVALID_ARG                                  # y overlaps x partially
+    assert f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0, 8, 4, 4, F32, 1, None, None, None) == ss.OK
