@@ -80,6 +80,8 @@ class Oracle:
         lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         lib.oracle_conv1d.restype = INT
         lib.oracle_conv1d.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT]
+        lib.oracle_selscan_bwd.restype = INT
+        lib.oracle_selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         self._lib = lib
         self.path = path
 
@@ -208,6 +210,36 @@ class Oracle:
         return out, st
 
 
+    def selscan_bwd(self, x, delta, A, B, C, gy, delta_softplus=False, h0=None, ghT=None):
+        """Gradients of a loss through the scan (dl * B form, no gate), by the
+        plain reverse sweep over each chain's stored states.
+
+        Shapes as selscan_fwd; gy (Bsz, L, D) = dLoss/dy, ghT (Bsz, D, N) =
+        dLoss/dhT or None. Returns a dict of float64 arrays dx, ddelta
+        (Bsz, L, D), dA (D, N), dB, dC (Bsz, L, N) and dh0 (Bsz, D, N).
+        """
+        x = np.asarray(x)
+        Bsz, L, D = x.shape
+        N = np.asarray(A).shape[1]
+        x = _f32(x, (Bsz, L, D), "x")
+        delta = _f32(delta, (Bsz, L, D), "delta")
+        A = _f32(A, (D, N), "A")
+        B = _f32(B, (Bsz, L, N), "B")
+        C = _f32(C, (Bsz, L, N), "C")
+        h0 = None if h0 is None else _f64(h0, (Bsz, D, N), "h0")
+        gy = _f64(gy, (Bsz, L, D), "gy")
+        ghT = None if ghT is None else _f64(ghT, (Bsz, D, N), "ghT")
+        g = dict(dx=np.zeros((Bsz, L, D)), ddelta=np.zeros((Bsz, L, D)), dA=np.zeros((D, N)),
+                 dB=np.zeros((Bsz, L, N)), dC=np.zeros((Bsz, L, N)), dh0=np.zeros((Bsz, D, N)))
+        rc = self._lib.oracle_selscan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),
+                                          _ptr(gy), _ptr(ghT), _ptr(g["dx"]), _ptr(g["ddelta"]),
+                                          _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dh0"]),
+                                          Bsz, L, D, N, int(bool(delta_softplus)))
+        if rc != 0:
+            raise RuntimeError("oracle_selscan_bwd failed")
+        return g
+
+
 def compile_variant(src: str, out: str) -> Oracle:
     """Build and load a copy of the oracle from another C source file
     (the mutation tests plant mistakes this way, on the CPU)."""
@@ -243,3 +275,7 @@ def selscan_step(*args, **kwargs):
 
 def conv1d(*args, **kwargs):
     return default().conv1d(*args, **kwargs)
+
+
+def selscan_bwd(*args, **kwargs):
+    return default().selscan_bwd(*args, **kwargs)

@@ -408,3 +408,100 @@ int oracle_conv1d(const float *x, const float *w, const float *bias,
     }
     return 0;
 }
+
+/* ---- backward pass of the scan --------------------------------------------
+ * Gradients of a scalar loss through the forward scan above (dl * B form,
+ * optional softplus), given the loss's gradients gy (Bsz, L, D) with respect
+ * to y and, optionally, ghT (Bsz, D, N) with respect to hT. The pages give
+ * the backward pass only as part of the hardware-aware design, whose states
+ * are recomputed rather than stored (booiljung.github.io "3.1 LTI ...
+ * Input-Dependent parameters", section 3.1.5.3); they print no gradient
+ * formulas, so these are the chain rule applied to the recurrence. This is
+ * the plain reverse sweep, keeping each chain's states:
+ *   forward   h_t = a_t h_{t-1} + b_t,  a_t = exp(dl_t A),  b_t = dl_t B_t x_t,
+ *             y_t = sum_n h_t C_t
+ *   backward  g_t = gy_t C_t + a_{t+1} g_{t+1}   (g_{L-1} also takes ghT)
+ *             dC_t += gy_t h_t,  da_t = g_t h_{t-1},  db_t = g_t
+ *             d dl_t = sum_n (da_t a_t A + db_t B_t x_t),  dA += da_t a_t dl_t,
+ *             dB_t += db_t dl_t x_t,  dx_t = sum_n db_t dl_t B_t,
+ *             d delta_t = d dl_t * sigmoid(delta_t) when softplus is applied,
+ *             dh0 = a_0 g_0.
+ * Outputs (all double, zeroed here): dx, ddelta (Bsz, L, D); dA (D, N);
+ * dB, dC (Bsz, L, N); dh0 (Bsz, D, N) or NULL. Single-threaded. */
+int oracle_selscan_bwd(const float *x, const float *delta, const float *A,
+                       const float *B, const float *C, const double *h0,
+                       const double *gy, const double *ghT,
+                       double *dx, double *ddelta, double *dA, double *dB,
+                       double *dC, double *dh0, int64_t Bsz, int64_t L,
+                       int64_t D, int64_t N, int delta_softplus)
+{
+    if (Bsz < 0 || L < 0 || D < 0 || N < 1 || !A || !gy || !dx || !ddelta || !dA || !dB || !dC)
+        return -1;
+    if (L > 0 && (!x || !delta || !B || !C))
+        return -1;
+    memset(dx, 0, sizeof(double) * (size_t)(Bsz * L * D));
+    memset(ddelta, 0, sizeof(double) * (size_t)(Bsz * L * D));
+    memset(dA, 0, sizeof(double) * (size_t)(D * N));
+    memset(dB, 0, sizeof(double) * (size_t)(Bsz * L * N));
+    memset(dC, 0, sizeof(double) * (size_t)(Bsz * L * N));
+    if (dh0)
+        memset(dh0, 0, sizeof(double) * (size_t)(Bsz * D * N));
+    /* hs[(t + 1) * N + n] = h after step t; hs[n] = the initial state */
+    double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N));
+    double *g = (double *)malloc(sizeof(double) * (size_t)N);
+    double *dls = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    if (!hs || !g || !dls) {
+        free(hs); free(g); free(dls);
+        return -1;
+    }
+    for (int64_t b = 0; b < Bsz; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            for (int64_t n = 0; n < N; ++n)
+                hs[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {   /* forward, keeping the states */
+                int64_t bt = b * L + t;
+                double dl = (double)delta[bt * D + d];
+                if (delta_softplus)
+                    dl = oracle_softplus(dl);
+                dls[t] = dl;
+                double xv = (double)x[bt * D + d];
+                for (int64_t n = 0; n < N; ++n)
+                    hs[(t + 1) * N + n] = exp(dl * (double)A[d * N + n]) * hs[t * N + n]
+                                          + dl * (double)B[bt * N + n] * xv;
+            }
+            for (int64_t n = 0; n < N; ++n)
+                g[n] = ghT ? ghT[(b * D + d) * N + n] : 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {   /* reverse sweep */
+                int64_t bt = b * L + t;
+                double dl = dls[t];
+                double xv = (double)x[bt * D + d];
+                double gyv = gy[bt * D + d];
+                double gdl = 0.0, gx = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double an = (double)A[d * N + n];
+                    double a = exp(dl * an);
+                    double Bn = (double)B[bt * N + n];
+                    g[n] += gyv * (double)C[bt * N + n];           /* y_t reads h_t */
+                    dC[bt * N + n] += gyv * hs[(t + 1) * N + n];
+                    double da = g[n] * hs[t * N + n];
+                    gdl += da * a * an + g[n] * Bn * xv;
+                    dA[d * N + n] += da * a * dl;
+                    dB[bt * N + n] += g[n] * dl * xv;
+                    gx += g[n] * dl * Bn;
+                    g[n] *= a;                                      /* into h_{t-1} */
+                }
+                dx[bt * D + d] = gx;
+                if (delta_softplus) {
+                    double u = (double)delta[bt * D + d];
+                    gdl *= 1.0 / (1.0 + exp(-u));                   /* softplus' = sigmoid */
+                }
+                ddelta[bt * D + d] = gdl;
+            }
+            if (dh0)
+                for (int64_t n = 0; n < N; ++n)
+                    dh0[(b * D + d) * N + n] = g[n];
+        }
+    }
+    free(hs); free(g); free(dls);
+    return 0;
+}

@@ -79,6 +79,16 @@ MUTATIONS = {
                                 "v = state_in ? (double)state_in[(b * D + d) * (K - 1) + (-1 - tau)] : 0.0;"),
     "step_dropped_input": ("            h[n] = dA * h[n] + dB * xv;\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];",
                            "            h[n] = dA * h[n];\n        }\n        for (int64_t n = 0; n < N; ++n)\n            acc += h[n] * (double)C[b * N + n];"),
+    "bwd_sigmoid_dropped": ("                    gdl *= 1.0 / (1.0 + exp(-u));", ""),
+    "bwd_dC_previous_state": ("dC[bt * N + n] += gyv * hs[(t + 1) * N + n];",
+                              "dC[bt * N + n] += gyv * hs[t * N + n];"),
+    "bwd_no_decay_carry": ("                    g[n] *= a;                                      /* into h_{t-1} */\n", ""),
+    "bwd_dA_without_dl": ("dA[d * N + n] += da * a * dl;", "dA[d * N + n] += da * a;"),
+    "bwd_dx_without_dl": ("gx += g[n] * dl * Bn;", "gx += g[n] * Bn;"),
+    "bwd_ddelta_drops_decay_term": ("gdl += da * a * an + g[n] * Bn * xv;", "gdl += g[n] * Bn * xv;"),
+    "bwd_dh0_before_last_decay": ("        for (int64_t n = 0; n < N; ++n)\n                    dh0[(b * D + d) * N + n] = g[n];",
+                                  "        for (int64_t n = 0; n < N; ++n)\n                    dh0[(b * D + d) * N + n] = g[n] / exp(dls[0] * (double)A[d * N + n]);"),
+    "bwd_ghT_ignored": ("g[n] = ghT ? ghT[(b * D + d) * N + n] : 0.0;", "g[n] = 0.0;"),
 }
 
 

@@ -546,3 +546,118 @@ def test_conv_single_tap_is_pointwise(orc):
     out, st = orc.conv1d(x, w, bias)
     lin = x.astype(np.float64) * w[:, 0].astype(np.float64) + bias.astype(np.float64)
     assert np.allclose(out, lin * expit(lin), rtol=1e-14, atol=1e-15) and st.shape == (1, 3, 0)
+
+
+# ---- the backward pass -------------------------------------------------------
+# The pages give no gradient formulas (the hardware-aware design of
+# booiljung.github.io "3.1 LTI ... Input-Dependent parameters", section
+# 3.1.5.3, only says the backward pass recomputes the states). The oracle's
+# reverse sweep is the chain rule on the recurrence; these pins fix it by
+# numerical differentiation of the forward oracle, by automatic
+# differentiation of an unrolled forward, and by homogeneity identities.
+
+def _loss(orc, x, u, A, B, C, h0, gy, ghT, softplus):
+    y, hT = orc.selscan_fwd(x, u, A, B, C, softplus, h0=h0)
+    tot = float(np.sum(gy * y))
+    if ghT is not None:
+        tot += float(np.sum(ghT * hT))
+    return tot
+
+
+def _central(f, v, h):
+    return (f(v + h) - f(v - h)) / (2 * h)
+
+
+@pytest.mark.parametrize("softplus,h0", [(True, False), (True, True), (False, True)])
+def test_bwd_matches_central_differences(orc, softplus, h0):
+    """Every gradient entry against a Richardson-extrapolated central
+    difference of the forward oracle's loss. The fp32 inputs are rounded to
+    multiples of 2^-12, so every perturbed value v +- 2^-9, v +- 2^-10 is
+    exact in fp32 and the differences are symmetric."""
+    x, u, A, B, C, hh = rand_inputs(2, 5, 2, 3, seed=70 + 2 * softplus + h0, softplus=softplus, h0=h0)
+    x, u, A, B, C = (np.round(v * 4096.0).astype(np.float32) / np.float32(4096.0) for v in (x, u, A, B, C))
+    g = np.random.default_rng(71)
+    gy = g.standard_normal(x.shape)
+    ghT = g.standard_normal((2, 2, 3))
+    grads = orc.selscan_bwd(x, u, A, B, C, gy, softplus, h0=hh, ghT=ghT)
+    args = dict(x=x, u=u, A=A, B=B, C=C, h0=hh)
+    names = dict(x="dx", u="ddelta", A="dA", B="dB", C="dC", h0="dh0")
+    for key, gname in names.items():
+        base = args[key]
+        if base is None:
+            continue
+        num = np.zeros(base.shape)
+        for idx in np.ndindex(base.shape):
+            def f(v, key=key, idx=idx):
+                a = {k: (None if w is None else w.copy()) for k, w in args.items()}
+                a[key][idx] = v
+                return _loss(orc, a["x"], a["u"], a["A"], a["B"], a["C"], a["h0"], gy, ghT, softplus)
+            v0 = float(base[idx])
+            d1, d2 = _central(f, v0, 2.0 ** -9), _central(f, v0, 2.0 ** -10)
+            num[idx] = (4 * d2 - d1) / 3
+        close(grads[gname], num, rtol=1e-9, atol=1e-10)
+
+
+def _torch_grads(x, u, A, B, C, h0, gy, ghT, softplus):
+    """Gradients by torch autograd (fp64, CPU) of the recurrence unrolled
+    step by step with tensor ops."""
+    import torch
+    t = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    tx, tu, tA, tB, tC = t(x), t(u), t(A), t(B), t(C)
+    th0 = t(h0) if h0 is not None else None
+    Bsz, L, D = x.shape
+    dl = torch.nn.functional.softplus(tu) if softplus else tu
+    h = th0 if th0 is not None else torch.zeros(Bsz, D, A.shape[1], dtype=torch.float64)
+    ys = []
+    for s in range(L):
+        d = dl[:, s, :, None]                                   # (Bsz, D, 1)
+        h = torch.exp(d * tA[None]) * h + d * tB[:, s, None, :] * tx[:, s, :, None]
+        ys.append((h * tC[:, s, None, :]).sum(-1))
+    y = torch.stack(ys, 1)
+    loss = (y * torch.from_numpy(gy)).sum() + (h * torch.from_numpy(ghT)).sum()
+    loss.backward()
+    out = dict(dx=tx.grad, ddelta=tu.grad, dA=tA.grad, dB=tB.grad, dC=tC.grad)
+    if th0 is not None:
+        out["dh0"] = th0.grad
+    return {k: v.numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("softplus", [True, False])
+def test_bwd_matches_autograd(orc, softplus):
+    x, u, A, B, C, hh = rand_inputs(2, 33, 3, 4, seed=72 + softplus, softplus=softplus, h0=True)
+    g = np.random.default_rng(73)
+    gy = g.standard_normal(x.shape)
+    ghT = g.standard_normal(hh.shape)
+    got = orc.selscan_bwd(x, u, A, B, C, gy, softplus, h0=hh, ghT=ghT)
+    ref = _torch_grads(x, u, A, B, C, hh, gy, ghT, softplus)
+    for k, v in ref.items():
+        close(got[k], v, rtol=1e-11, atol=1e-12)
+
+
+def test_bwd_homogeneity_identities(orc):
+    """y and hT are linear in (x, h0) jointly, so by Euler's identity the loss
+    equals sum dx*x + sum dh0*h0; y is linear in C, so sum gy*y = sum dC*C;
+    with h0 = 0 everything is linear in B, so the loss equals sum dB*B."""
+    x, u, A, B, C, hh = rand_inputs(2, 200, 8, 16, seed=74, h0=True)
+    g = np.random.default_rng(75)
+    gy = g.standard_normal(x.shape)
+    ghT = g.standard_normal(hh.shape)
+    y, hT = orc.selscan_fwd(x, u, A, B, C, True, h0=hh)
+    gr = orc.selscan_bwd(x, u, A, B, C, gy, True, h0=hh, ghT=ghT)
+    loss = np.sum(gy * y) + np.sum(ghT * hT)
+    scale = np.sum(np.abs(gy * y)) + np.sum(np.abs(ghT * hT))
+    assert abs(np.sum(gr["dx"] * x) + np.sum(gr["dh0"] * hh) - loss) <= 1e-12 * scale
+    gr0 = orc.selscan_bwd(x, u, A, B, C, gy, True, h0=hh)   # no hT gradient
+    assert abs(np.sum(gr0["dC"] * C) - np.sum(gy * y)) <= 1e-12 * np.sum(np.abs(gy * y))
+    y0, hT0 = orc.selscan_fwd(x, u, A, B, C, True)          # h0 = 0
+    gr1 = orc.selscan_bwd(x, u, A, B, C, gy, True, ghT=ghT)
+    loss0 = np.sum(gy * y0) + np.sum(ghT * hT0)
+    scale0 = np.sum(np.abs(gy * y0)) + np.sum(np.abs(ghT * hT0))
+    assert abs(np.sum(gr1["dB"] * B) - loss0) <= 1e-12 * scale0
+
+
+def test_bwd_empty_sequence_passes_the_state_gradient_through(orc):
+    x, u, A, B, C, hh = rand_inputs(2, 0, 3, 4, seed=76, h0=True)
+    ghT = np.random.default_rng(77).standard_normal(hh.shape)
+    gr = orc.selscan_bwd(x, u, A, B, C, np.zeros(x.shape), True, h0=hh, ghT=ghT)
+    assert np.array_equal(gr["dh0"], ghT) and not gr["dA"].any()
