@@ -77,6 +77,25 @@ def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gat
     return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": mufu, "fp32": fp32}
 
 
+def bwd_work_counts(Bsz, L, D, N):
+    """Algorithmic work of one backward call (fp32, softplus on, no h0/dhT).
+
+    bytes: x, delta, dy read and dx, ddelta written (5 * B*L*D fp32), B, C read
+    and dB, dC written (4 * B*L*N), A read and dA written (2 * D*N).
+    mufu: the decay exp(dl*A) once per (t, d, n), which the recomputed
+    forward and the adjoint share; per (t, d) exp and log for softplus and
+    exp and reciprocal for its derivative.
+    fp32: 21 per (t, d, n): 4 for the recomputed state update (as in the
+    forward), 13 for the adjoint step (g += gy*C, gy*h, g*h*a, (.)*A + g*B*x,
+    dA += (.)*dl, g*dl*x, g*dl*B, g *= a), and one addition for each of the
+    four sums (dx and ddelta over n, dB and dC over d).
+    """
+    E = Bsz * L * D
+    S = Bsz * L * N
+    nbytes = 5 * E * 4 + 4 * S * 4 + 2 * D * N * 4
+    return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": E * N + 4 * E, "fp32": 21 * E * N}
+
+
 def step_work_counts(Bsz, D, N):
     """Algorithmic work of one decode step: the state is read and written once
     (2 * B*D*N fp32), x, delta and y move once (3 * B*D), B and C once per batch
@@ -137,9 +156,10 @@ def profiled_traffic(workload_id: int):
         return None
     try:
         d = json.load(open(p))
+        from selective_state_space_157_b300 import workloads as W
         from selective_state_space_157_b300.build import source_digest
         entry = d.get(str(workload_id))
-        if entry and entry.get("sources") == source_digest():
+        if entry and entry.get("sources") == source_digest(backward=W.WORKLOADS[workload_id].backward):
             return entry["dram_bytes_per_call"]
     except Exception:
         return None
@@ -330,6 +350,8 @@ def run_gpu(args, world, rank, local):
         return run_decode(args, world, rank, local, dev, w)
     if w.conv_K:
         return run_conv(args, world, rank, local, dev, w)
+    if w.backward:
+        return run_bwd(args, world, rank, local, dev, w)
     inp = W.workload_inputs(args.workload)
     bf16 = w.dtype == W.BF16
     es = 2 if bf16 else 4
@@ -575,6 +597,95 @@ def run_conv(args, world, rank, local, dev, w):
                        launches=args.steps, clocks=clk.summary(), dtype="f32")
 
 
+def run_bwd(args, world, rank, local, dev, w):
+    """The backward workload: one step = one selscan_bwd over (Bsz, L, D, N)
+    with softplus on and upstream gradient dy (no dhT). Input sets rotate past
+    2x L2."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+
+    inp = W.workload_inputs(args.workload)
+    dy, _ = W.bwd_grads(w.Bsz, w.L, w.D, w.N, seed=w.seed, with_dhT=False)
+    host = {k: inp.f32(k) for k in ("x", "delta", "B", "C")}
+    host["dy"] = dy
+    foot = sum(a.nbytes for a in host.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(1, -(-(2 * l2) // foot))
+    sets = [{k: torch.from_numpy(a).to(dev) for k, a in host.items()} for _ in range(copies)]
+    A = torch.from_numpy(inp.A).to(dev)
+
+    def step(i):
+        s = sets[i % copies]
+        return ss.selscan_bwd(s["x"], s["delta"], A, s["B"], s["C"], s["dy"], True, want_dh0=False)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, dev)
+    ss.check_device_error()
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    per_step = sec / args.steps
+    elems = w.Bsz * w.L * w.D
+    value = world * elems * args.steps / sec
+
+    hin = {k: torch.from_numpy(a).pin_memory() for k, a in host.items()}
+    outs = {"dx": (w.Bsz, w.L, w.D), "ddelta": (w.Bsz, w.L, w.D), "dA": (w.D, w.N), "dB": (w.Bsz, w.L, w.N),
+            "dC": (w.Bsz, w.L, w.N)}
+    hout = {k: torch.empty(shape, dtype=torch.float32, pin_memory=True) for k, shape in outs.items()}
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        d = {k: t.to(dev, non_blocking=True) for k, t in hin.items()}
+        g = ss.selscan_bwd(d["x"], d["delta"], A, d["B"], d["C"], d["dy"], True, want_dh0=False)
+        for k in outs:
+            hout[k].copy_(g[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": sum(t.numel() * 4 for t in hin.values()),
+           "d2h_bytes_per_step": sum(t.numel() * 4 for t in hout.values())}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    hbm_gbs, max_mhz, src = read_measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pk = peaks(sms, max_mhz, hbm_gbs)
+    pk["source"] = f"HBM {src}; MUFU {MUFU_EX2_PER_CLK_SM}/clk/SM and FP32 {FP32_PER_CLK_SM}/clk/SM at {max_mhz:.0f} MHz"
+    work = bwd_work_counts(w.Bsz, w.L, w.D, w.N)
+    roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
+                    kernel="scan_bwd_kernel (1 launch + 3 memsets)")
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.default().selscan_bwd(host["x"], host["delta"], inp.A, host["B"], host["C"], dy, True)
+        secs = time.perf_counter() - t0
+        cpu = {"value": elems / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the whole workload ({elems} elements, {secs:.2f} s, fp64 reverse sweep, one thread)"}
+    config = {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} N={w.N} f32, softplus on, backward "
+                          "(dx, ddelta, dA, dB, dC from dy)",
+              "global_batch": w.Bsz * world, "seq_len": w.L, "parallelism": f"replicas x{world}",
+              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
+    return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                       ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
+                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+
+
 def run_decode(args, world, rank, local, dev, w):
     """The decode workload: one step = one selscan_step over (Bsz, D, N).
     Eight independent decode streams (state and per-step inputs each) are
@@ -713,6 +824,8 @@ def run_reference(args, world, rank):
         return run_reference_decode(args, world, w)
     if w.conv_K:
         return run_reference_conv(args, world, w)
+    if w.backward:
+        return run_reference_bwd(args, world, w)
     inp = W.workload_inputs(args.workload)
     gate = W.workload_gate_inputs(args.workload) if w.gated else None
     Bsz, L, D = inp.x.shape
@@ -767,6 +880,35 @@ def run_reference_conv(args, world, w):
     }
 
 
+def run_reference_bwd(args, world, w):
+    """Reference arm for the backward workload: each step is one oracle
+    reverse sweep over the whole workload, on the host."""
+    import oracle
+    from selective_state_space_157_b300 import workloads as W
+    inp = W.workload_inputs(args.workload)
+    dy, _ = W.bwd_grads(w.Bsz, w.L, w.D, w.N, seed=w.seed, with_dhT=False)
+    a = (inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), dy, True)
+    o = oracle.default()
+    for _ in range(args.warmup):
+        o.selscan_bwd(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.selscan_bwd(*a)
+    tot = time.perf_counter() - t0
+    elems = w.Bsz * w.L * w.D
+    value = elems * args.steps / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} N={w.N} f32, softplus on, backward",
+                   "seq_len": w.L, "parallelism": "host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the whole workload per step ({elems} elements, fp64)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference_decode(args, world, w):
     """Reference arm for the decode workload: each step is one oracle decode
     step over a sample of the chains, on the host."""
@@ -804,7 +946,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")

@@ -306,6 +306,42 @@ int selscan_conv1d(const void *x, const float *w, const float *bias, void *out, 
 int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const float *bias,
                         float *out, int64_t Bsz, int64_t D, int64_t K, int silu, void *stream);
 
+/*
+ * selscan_bwd -- the backward pass of selscan_fwd (fp32, dl * B form, no
+ * skip or gate): the gradients of a scalar loss with respect to every input,
+ * given its gradients with respect to y and hT. The hardware-aware design of
+ * booiljung.github.io "3.1 LTI systems and input-dependent parameters",
+ * section 3.1.5.3, recomputes the states in the backward pass instead of
+ * storing them; so does this call. With g_t = dLoss/dh_t, carried backwards
+ * as g_t = gy_t C_t + exp(dl_{t+1} A) g_{t+1} from g_{L-1} = gy C + dhT:
+ *
+ *   dC[b,t,n]  = sum_d gy[b,t,d] h_t[n]     dB[b,t,n] = sum_d g_t[n] dl x[b,t,d]
+ *   dx[b,t,d]  = sum_n g_t[n] dl B[b,t,n]   dA[d,n]   = sum_{b,t} g_t h_{t-1} a_t dl
+ *   ddelta[b,t,d] = sum_n (g_t h_{t-1} a_t A[d,n] + g_t B x), times
+ *                   sigmoid(delta) when delta_softplus (d softplus / du)
+ *   dh0[b,d,n] = exp(dl_0 A) g_0
+ *
+ *   x, delta, dy, dx, ddelta : (Bsz, L, D) fp32   A, dA : (D, N) fp32
+ *   B, C, dB, dC             : (Bsz, L, N) fp32
+ *   h0, dhT, dh0             : (Bsz, D, N) fp32 or NULL (h0 NULL = zeros,
+ *                              dhT NULL = no loss on hT, dh0 NULL = not wanted)
+ *
+ * Sizes: Bsz, L, D >= 0 with Bsz <= 65535; 1 <= N <= 32. Every output is
+ * overwritten; no output may overlap an input or another output. Pointers
+ * 4-byte aligned. L == 0 gives dA = 0 and dh0 = dhT (or zeros).
+ * Workspace: the state at the start of every 16-step chunk, Bsz * D * 16
+ * * ceil(L / 16) floats for N <= 16 (the state rows padded to a power of
+ * two), from the same stream-ordered pool as selscan_fwd's.
+ * dA, dB and dC are sums formed with atomic additions, so their last bits
+ * may differ from run to run; dx, ddelta and dh0 are reproducible.
+ * Errors as for selscan_fwd.
+ */
+int selscan_bwd(const float *x, const float *delta, const float *A, const float *B,
+                const float *C, const float *h0, const float *dy, const float *dhT,
+                float *dx, float *ddelta, float *dA, float *dB, float *dC, float *dh0,
+                int64_t Bsz, int64_t L, int64_t D, int64_t N, int delta_softplus,
+                void *stream);
+
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on
  * the same thread. */

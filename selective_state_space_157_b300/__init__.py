@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
+        L.selscan_bwd.restype = INT
+        L.selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, P]
         _lib = L
     return _lib
 
@@ -208,6 +210,42 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
                                    _stream_ptr(stream))
     _check(rc)
     return (y, hT) if (return_final_state or hT is not None) else y
+
+
+def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dhT=None,
+                want_dh0: bool = True, stream=None):
+    """Backward pass of the forward scan (fp32, no skip or gate; see
+    ``include/selscan.h``): gradients of a loss with respect to x, delta, A,
+    B, C and h0, given dy (Bsz, L, D) = dLoss/dy and dhT (Bsz, D, N) =
+    dLoss/dhT or None. Device float32 tensors only. Returns a dict with
+    dx, ddelta (Bsz, L, D), dA (D, N), dB, dC (Bsz, L, N) and, when
+    ``want_dh0``, dh0 (Bsz, D, N).
+    """
+    import torch
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("selscan_bwd takes device tensors")
+    Bsz, L, D = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    f = torch.float32
+    for t, name, shape in ((x, "x", (Bsz, L, D)), (delta, "delta", (Bsz, L, D)), (A, "A", (D, N)),
+                           (B, "B", (Bsz, L, N)), (C, "C", (Bsz, L, N)), (dy, "dy", (Bsz, L, D))):
+        _need(t, name, shape, f, dev)
+    if h0 is not None:
+        _need(h0, "h0", (Bsz, D, N), f, dev)
+    if dhT is not None:
+        _need(dhT, "dhT", (Bsz, D, N), f, dev)
+    g = dict(dx=torch.empty((Bsz, L, D), dtype=f, device=dev), ddelta=torch.empty((Bsz, L, D), dtype=f, device=dev),
+             dA=torch.empty((D, N), dtype=f, device=dev), dB=torch.empty((Bsz, L, N), dtype=f, device=dev),
+             dC=torch.empty((Bsz, L, N), dtype=f, device=dev))
+    if want_dh0:
+        g["dh0"] = torch.empty((Bsz, D, N), dtype=f, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(dy), _ptr(dhT),
+                               _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                               _ptr(g.get("dh0")), Bsz, L, D, N, int(bool(delta_softplus)), _stream_ptr(stream))
+    _check(rc)
+    return g
 
 
 def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=None, hT=None,

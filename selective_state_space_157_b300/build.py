@@ -26,13 +26,22 @@ def sources():
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources (identifies the kernels a profile was
-    taken on; the public header's comments do not change them)."""
+# Device code of the backward pass only; the forward, decode and conv1d
+# kernels do not include it.
+BACKWARD_ONLY = ("scan_bwd.cuh",)
+
+
+def source_digest(backward: bool = False) -> str:
+    """sha256 over the CUDA sources a kernel is built from (identifies the
+    kernels a profile was taken on; the public header's comments do not change
+    them). The forward, decode and conv1d kernels leave out the backward's
+    own header; the backward kernel takes every source."""
     import hashlib
     h = hashlib.sha256()
     for p in sources():
         if p.endswith(".py") or p.endswith(".h"):
+            continue
+        if not backward and os.path.basename(p) in BACKWARD_ONLY:
             continue
         h.update(os.path.basename(p).encode())
         h.update(open(p, "rb").read())

@@ -30,7 +30,7 @@ BF16 = "bf16"
 
 # tensor ids of the per-tensor random streams
 _TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6, "Dskip": 7, "z": 8, "conv_w": 9, "conv_b": 10,
-        "conv_state": 11}
+        "conv_state": 11, "dy": 12, "dhT": 13}
 
 
 @dataclass(frozen=True)
@@ -50,6 +50,7 @@ class Workload:
     gated: bool = False   # with the block's skip and gate (gate_inputs)
     zoh: bool = False     # zero-order-hold discretisation instead of dl * B
     conv_K: int = 0       # > 0: the causal conv1d + SiLU before the scan, with K taps
+    backward: bool = False  # the backward pass (dy from bwd_grads, no dhT)
 
     @property
     def elems(self) -> int:
@@ -66,6 +67,7 @@ WORKLOADS = {
     6: Workload(6, "mamba130m-gated", 2, 2048, 1536, 16, F32, -3.0, "arange", 106, gated=True),
     7: Workload(7, "mamba130m-zoh", 2, 2048, 1536, 16, F32, -3.0, "arange", 107, zoh=True),
     8: Workload(8, "mamba130m-conv1d", 2, 2048, 1536, 16, F32, -3.0, "arange", 108, conv_K=4),
+    9: Workload(9, "mamba130m-bwd", 2, 2048, 1536, 16, F32, -3.0, "arange", 109, backward=True),
 }
 
 
@@ -214,3 +216,11 @@ def conv_inputs(Bsz: int, L: int, D: int, K: int, *, seed: int, dtype: str = F32
     bias = rng(seed, _TID["conv_b"]).uniform(-r, r, size=(D,)).astype(np.float32)
     state = normal(rng(seed, _TID["conv_state"]), (Bsz, D, K - 1)) if with_state else None
     return x, w, bias, state
+
+
+def bwd_grads(Bsz: int, L: int, D: int, N: int, *, seed: int, with_dhT: bool = True):
+    """Upstream gradients of a backward call: dy ~ N(0, 1) of shape (Bsz, L, D)
+    and dhT ~ N(0, 1) of shape (Bsz, D, N) (None unless ``with_dhT``)."""
+    dy = normal(rng(seed, _TID["dy"]), (Bsz, L, D))
+    dhT = normal(rng(seed, _TID["dhT"]), (Bsz, D, N)) if with_dhT else None
+    return dy, dhT

@@ -202,3 +202,36 @@ def test_host_and_noalloc_forward_share_the_checks(lib, entry):
     assert f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x10000 + 4, 1, 8, 4, 4, F32, 1, None, None, None) \
         == ss.ERR_INVALID_ARG                                  # y overlaps x partially
     assert f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0, 8, 4, 4, F32, 1, None, None, None) == ss.OK
+
+
+def bwd(lib, **kw):
+    a = dict(x=0x10000, delta=0x20000, A=0x30000, B=0x40000, C=0x50000, h0=None, dy=0x60000, dhT=None,
+             dx=0x70000, ddelta=0x80000, dA=0x90000, dB=0xA0000, dC=0xB0000, dh0=None,
+             Bsz=1, L=8, D=4, N=16, sp=1)
+    a.update(kw)
+    return lib.selscan_bwd(a["x"], a["delta"], a["A"], a["B"], a["C"], a["h0"], a["dy"], a["dhT"], a["dx"],
+                           a["ddelta"], a["dA"], a["dB"], a["dC"], a["dh0"], a["Bsz"], a["L"], a["D"], a["N"],
+                           a["sp"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=0), ss.ERR_INVALID_ARG),
+    (dict(N=33), ss.ERR_UNSUPPORTED),                          # lane groups end at one warp
+    (dict(Bsz=70000), ss.ERR_UNSUPPORTED),                     # grid limit
+    (dict(L=-1), ss.ERR_INVALID_ARG),
+    (dict(dA=None), ss.ERR_INVALID_ARG),
+    (dict(dy=None), ss.ERR_INVALID_ARG),
+    (dict(x=0x10002), ss.ERR_INVALID_ARG),                     # misaligned
+    (dict(dx=0x10000 + 4), ss.ERR_INVALID_ARG),                # dx overlaps x
+    (dict(dB=0x70000 + 8), ss.ERR_INVALID_ARG),                # dB overlaps dx
+    (dict(dh0=0xC0000, h0=0xC0000), ss.ERR_INVALID_ARG),       # dh0 overlaps h0
+    (dict(dA=0x60000), ss.ERR_INVALID_ARG),                    # dA overlaps dy
+    (dict(L=1 << 40, D=1 << 30), ss.ERR_INVALID_ARG),          # size overflow
+])
+def test_bwd_argument_errors(lib, kw, code):
+    assert bwd(lib, **kw) == code
+    assert ss.last_error() != ""
+
+
+def test_bwd_empty_channel_count_is_ok_without_cuda(lib):
+    assert bwd(lib, D=0, A=None, dA=None) == ss.OK

@@ -1,0 +1,84 @@
+"""selscan_bwd: the backward pass of the scan against the fp64 oracle's
+reverse sweep, on the same fp32 inputs and upstream gradients. Covers one
+and many 16-step chunks with ragged tails, channel counts that leave the
+last block partly empty, every lane-group width (N = 1, 5, 16, 32), with and
+without softplus, h0 and dhT, the empty sequence, and the 130M-like layer
+at full size."""
+import numpy as np
+import pytest
+import torch
+
+import selective_state_space_157_b300 as ss
+from selective_state_space_157_b300 import workloads as W
+from tests.helpers import TOL, scaled_err, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("dx", "ddelta", "dA", "dB", "dC", "dh0")
+
+
+def run(orc, Bsz, L, D, N, seed, softplus=True, with_h0=True, with_dhT=True, a_init="loguniform"):
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=seed, a_init=a_init, with_h0=with_h0, delta_softplus=softplus,
+                       u_mean=-3.0 if softplus else 0.0)
+    dy, dhT = W.bwd_grads(Bsz, L, D, N, seed=seed + 1, with_dhT=with_dhT)
+    x, u = inp.f32("x"), inp.f32("delta")
+    if not softplus:
+        u = np.abs(u) * np.float32(0.3)       # a positive step size taken as given
+    h0 = inp.h0
+    got = ss.selscan_bwd(to_dev(x), to_dev(u), to_dev(inp.A), to_dev(inp.f32("B")), to_dev(inp.f32("C")),
+                         to_dev(dy), softplus, h0=to_dev(h0), dhT=to_dev(dhT))
+    torch.cuda.synchronize()
+    ss.check_device_error()
+    ref = orc.selscan_bwd(x, u, inp.A, inp.f32("B"), inp.f32("C"), dy, softplus,
+                          h0=None if h0 is None else h0.astype(np.float64),
+                          ghT=None if dhT is None else dhT.astype(np.float64))
+    errs = {k: scaled_err(to_np(got[k]), ref[k]) for k in NAMES}
+    assert max(errs.values()) <= TOL[W.F32], errs
+    return got
+
+
+@pytest.mark.parametrize("shape", [(1, 64, 16, 4), (2, 300, 96, 16), (2, 37, 20, 16), (1, 16, 5, 3)])
+@pytest.mark.parametrize("softplus", [True, False])
+def test_shapes(orc, shape, softplus):
+    run(orc, *shape, seed=sum(shape) + softplus, softplus=softplus)
+
+
+@pytest.mark.parametrize("shape", [(2, 50, 300, 1), (1, 70, 9, 32), (1, 41, 33, 5), (3, 1, 40, 16)])
+def test_lane_group_widths_and_one_step(orc, shape):
+    """P = 1 (256 chains a block), 32 (one warp a chain), 8 with padding
+    lanes, and L = 1."""
+    run(orc, *shape, seed=sum(shape))
+
+
+def test_without_initial_state_or_final_gradient(orc):
+    run(orc, 2, 100, 48, 16, seed=11, with_h0=False, with_dhT=False, a_init="arange")
+
+
+def test_empty_sequence(orc):
+    Bsz, D, N = 2, 24, 16
+    dhT = torch.randn(Bsz, D, N, device="cuda")
+    e = torch.empty(Bsz, 0, D, device="cuda")
+    g = ss.selscan_bwd(e, e, -torch.rand(D, N, device="cuda"), torch.empty(Bsz, 0, N, device="cuda"),
+                       torch.empty(Bsz, 0, N, device="cuda"), e, True, dhT=dhT)
+    torch.cuda.synchronize()
+    assert torch.equal(g["dh0"], dhT) and not g["dA"].any()
+
+
+def test_state_gradients_are_reproducible(orc):
+    """dx, ddelta and dh0 come from one lane each, in a fixed order."""
+    inp = W.fwd_inputs(2, 200, 64, 16, seed=13, a_init="loguniform")
+    dy, dhT = W.bwd_grads(2, 200, 64, 16, seed=14)
+    args = [to_dev(inp.f32(k)) for k in ("x", "delta")] + [to_dev(inp.A)] + \
+           [to_dev(inp.f32(k)) for k in ("B", "C")] + [to_dev(dy)]
+    g1 = ss.selscan_bwd(*args, True, dhT=to_dev(dhT))
+    g2 = ss.selscan_bwd(*args, True, dhT=to_dev(dhT))
+    torch.cuda.synchronize()
+    for k in ("dx", "ddelta", "dh0"):
+        assert torch.equal(g1[k], g2[k])
+
+
+def test_mamba130m_layer_full_size(orc):
+    """The 130M-like layer (Bsz 2, L 2048, D 1536, N 16, softplus on), every
+    output compared."""
+    w = W.WORKLOADS[2]
+    run(orc, w.Bsz, w.L, w.D, w.N, seed=w.seed, with_h0=False, a_init="arange")
