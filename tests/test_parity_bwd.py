@@ -43,10 +43,11 @@ def test_shapes(orc, shape, softplus):
     run(orc, *shape, seed=sum(shape) + softplus, softplus=softplus)
 
 
-@pytest.mark.parametrize("shape", [(2, 50, 300, 1), (1, 70, 9, 32), (1, 41, 33, 5), (3, 1, 40, 16)])
+@pytest.mark.parametrize("shape", [(2, 50, 300, 1), (1, 45, 130, 2), (1, 70, 9, 32), (1, 41, 33, 5),
+                                   (3, 1, 40, 16)])
 def test_lane_group_widths_and_one_step(orc, shape):
-    """P = 1 (256 chains a block), 32 (one warp a chain), 8 with padding
-    lanes, and L = 1."""
+    """P = 1 (256 chains a block), 2, 32 (one warp a chain, two lanes a
+    step in the reduce-scatter), 8 with padding lanes, and L = 1."""
     run(orc, *shape, seed=sum(shape))
 
 
