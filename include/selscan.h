@@ -329,9 +329,9 @@ int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const
  * Sizes: Bsz, L, D >= 0 with Bsz <= 65535; 1 <= N <= 32. Every output is
  * overwritten; no output may overlap an input or another output. Pointers
  * 4-byte aligned. L == 0 gives dA = 0 and dh0 = dhT (or zeros).
- * Workspace: the state at the start of every 16-step chunk, Bsz * D * 16
- * * ceil(L / 16) floats for N <= 16 (the state rows padded to a power of
- * two), from the same stream-ordered pool as selscan_fwd's.
+ * Workspace: the state at the start of every 32-step chunk, Bsz * D * P
+ * * ceil(L / 32) floats with P the power of two >= N, from the same
+ * stream-ordered pool as selscan_fwd's.
  * dA, dB and dC are sums formed with atomic additions, so their last bits
  * may differ from run to run; dx, ddelta and dh0 are reproducible.
  * Errors as for selscan_fwd.
