@@ -8,6 +8,7 @@ path: if ``libselscan.so`` is missing the first call raises.
     y = selscan_fwd(x, delta, A, B, C, delta_softplus=True)
     y, hT = selscan_fwd(x, delta, A, B, C, h0=h0, return_final_state=True)
     y = selscan_step(state, x, delta, A, B, C)     # state updated in place
+    y, hT = selective_scan(x, delta, A, B, C, True)  # differentiable (fp32)
 
 Tensors may live on the current CUDA device (the call is asynchronous on the
 current stream) or in host memory (preferably pinned): host inputs are copied
@@ -19,7 +20,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step", "fwd_plan", "last_error", "check_device_error",
+__all__ = ["selscan_fwd", "selscan_bwd", "selective_scan", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
            "MAX_N", "FLAG_SOFTPLUS", "FLAG_ZOH"]
@@ -246,6 +247,43 @@ def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dh
                                _ptr(g.get("dh0")), Bsz, L, D, N, int(bool(delta_softplus)), _stream_ptr(stream))
     _check(rc)
     return g
+
+
+_autograd_fn = None
+
+
+def _selective_scan_fn():
+    """The autograd Function behind ``selective_scan`` (built on first use, so
+    importing the binding does not import torch)."""
+    global _autograd_fn
+    if _autograd_fn is None:
+        import torch
+
+        class SelectiveScan(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, x, delta, A, B, C, h0, delta_softplus):
+                y, hT = selscan_fwd(x, delta, A, B, C, delta_softplus, h0=h0, return_final_state=True)
+                ctx.save_for_backward(x, delta, A, B, C, h0)
+                ctx.delta_softplus = delta_softplus
+                return y, hT
+
+            @staticmethod
+            def backward(ctx, dy, dhT):
+                x, delta, A, B, C, h0 = ctx.saved_tensors
+                want_dh0 = h0 is not None and ctx.needs_input_grad[5]
+                g = selscan_bwd(x, delta, A, B, C, dy.contiguous(), ctx.delta_softplus, h0=h0,
+                                dhT=None if dhT is None else dhT.contiguous(), want_dh0=want_dh0)
+                return g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dh0"), None
+
+        _autograd_fn = SelectiveScan
+    return _autograd_fn
+
+
+def selective_scan(x, delta, A, B, C, delta_softplus: bool = False, h0=None):
+    """The forward scan as a differentiable torch operation: returns (y, hT),
+    and ``backward`` runs ``selscan_bwd`` (the states are recomputed, not
+    stored). Device float32 tensors; h0 (Bsz, D, N) or None."""
+    return _selective_scan_fn().apply(x, delta, A, B, C, h0, bool(delta_softplus))
 
 
 def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=None, hT=None,

@@ -83,3 +83,21 @@ def test_mamba130m_layer_full_size(orc):
     output compared."""
     w = W.WORKLOADS[2]
     run(orc, w.Bsz, w.L, w.D, w.N, seed=w.seed, with_h0=False, a_init="arange")
+
+
+def test_selective_scan_autograd(orc):
+    """loss.backward() through the differentiable wrapper reaches the CUDA
+    backward: its gradients equal the oracle's for the same upstream ones."""
+    Bsz, L, D, N = 2, 100, 48, 16
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=31, a_init="loguniform", with_h0=True)
+    wy, wh = W.bwd_grads(Bsz, L, D, N, seed=32)
+    leaves = [to_dev(a).requires_grad_() for a in (inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"),
+                                                   inp.f32("C"), inp.h0)]
+    x, dl, A, B, C, h0 = leaves
+    y, hT = ss.selective_scan(x, dl, A, B, C, True, h0=h0)
+    ((y * to_dev(wy)).sum() + (hT * to_dev(wh)).sum()).backward()
+    torch.cuda.synchronize()
+    ref = orc.selscan_bwd(inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), wy, True,
+                          h0=inp.h0.astype(np.float64), ghT=wh.astype(np.float64))
+    for t, k in zip(leaves, NAMES):
+        assert scaled_err(to_np(t.grad), ref[k]) <= TOL[W.F32], k
