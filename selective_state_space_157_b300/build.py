@@ -26,16 +26,17 @@ def sources():
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-# Device code of the backward pass only; the forward, decode and conv1d
-# kernels do not include it.
-BACKWARD_ONLY = ("scan_bwd.cuh",)
+# The backward pass's own sources, and the file that puts the library's one
+# translation unit together; the forward, decode and conv1d kernels and their
+# host code do not depend on them.
+BACKWARD_ONLY = ("scan_bwd.cuh", "selscan_bwd.cu", "libselscan.cu")
 
 
 def source_digest(backward: bool = False) -> str:
     """sha256 over the CUDA sources a kernel is built from (identifies the
     kernels a profile was taken on; the public header's comments do not change
     them). The forward, decode and conv1d kernels leave out the backward's
-    own header; the backward kernel takes every source."""
+    own files; the backward kernel takes every source."""
     import hashlib
     h = hashlib.sha256()
     for p in sources():
@@ -60,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     cmd = [NVCC, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-cudart", "shared", "-I", INCLUDE, "-I", CSRC,
-           "-o", LIB + ".tmp", os.path.join(CSRC, "selscan.cu")]
+           "-o", LIB + ".tmp", os.path.join(CSRC, "libselscan.cu")]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
