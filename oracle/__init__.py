@@ -80,6 +80,8 @@ class Oracle:
         lib.oracle_selscan_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         lib.oracle_conv1d.restype = INT
         lib.oracle_conv1d.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT]
+        lib.oracle_ssd_fwd.restype = INT
+        lib.oracle_ssd_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, INT]
         lib.oracle_selscan_bwd.restype = INT
         lib.oracle_selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         self._lib = lib
@@ -240,6 +242,28 @@ class Oracle:
         return g
 
 
+    def ssd_fwd(self, x, dt, A, B, C, dt_softplus=False, h0=None):
+        """Mamba-2 SSD forward in fp64 (see oracle.c): x (Bsz, L, H, P),
+        dt (Bsz, L, H), A (H,), B, C (Bsz, L, N), h0 (Bsz, H, N, P) or None.
+        Returns (y (Bsz, L, H, P), hT (Bsz, H, N, P)) in float64."""
+        x = np.asarray(x)
+        Bsz, L, H, P = x.shape
+        N = np.asarray(B).shape[2]
+        x = _f32(x, (Bsz, L, H, P), "x")
+        dt = _f32(dt, (Bsz, L, H), "dt")
+        A = _f32(A, (H,), "A")
+        B = _f32(B, (Bsz, L, N), "B")
+        C = _f32(C, (Bsz, L, N), "C")
+        h0 = None if h0 is None else _f64(h0, (Bsz, H, N, P), "h0")
+        y = np.zeros((Bsz, L, H, P))
+        hT = np.zeros((Bsz, H, N, P))
+        rc = self._lib.oracle_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(y), _ptr(hT),
+                                      Bsz, L, H, P, N, int(bool(dt_softplus)))
+        if rc != 0:
+            raise RuntimeError("oracle_ssd_fwd failed")
+        return y, hT
+
+
 def compile_variant(src: str, out: str) -> Oracle:
     """Build and load a copy of the oracle from another C source file
     (the mutation tests plant mistakes this way, on the CPU)."""
@@ -279,3 +303,7 @@ def conv1d(*args, **kwargs):
 
 def selscan_bwd(*args, **kwargs):
     return default().selscan_bwd(*args, **kwargs)
+
+
+def ssd_fwd(*args, **kwargs):
+    return default().ssd_fwd(*args, **kwargs)

@@ -505,3 +505,64 @@ int oracle_selscan_bwd(const float *x, const float *delta, const float *A,
     free(hs); free(g); free(dls);
     return 0;
 }
+
+/* ---- Mamba-2 SSD -------------------------------------------------------
+ * The state-space-dual model of youngju.dev "Mamba: Selective State Space
+ * Models", section 4.1 (recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t)
+ * with the multi-head layout of section 5.2 (heads of headdim P, state size
+ * N). A_t is a scalar per head, exp(dt * A[hd]) (the structured form whose
+ * dual matrix M is semiseparable), and the input term takes dt * B as in the
+ * simplified selective_scan listing of section 3.3. B and C are shared by
+ * all heads.
+ *
+ *   x : (Bsz, L, H, P)   dt : (Bsz, L, H)   A : (H)   B, C : (Bsz, L, N)
+ *   h0, hT : (Bsz, H, N, P) double (h0 NULL: zeros)   y : (Bsz, L, H, P) double
+ *   for every batch b and head hd, from h[n][p] = h0:
+ *     for t: dl = dt[b,t,hd] (softplus(dl) when asked), a = exp(dl * A[hd])
+ *            h[n][p] = a * h[n][p] + (dl * B[b,t,n]) * x[b,t,hd,p]
+ *            y[b,t,hd,p] = sum_n C[b,t,n] * h[n][p]
+ * Single-threaded. */
+int oracle_ssd_fwd(const float *x, const float *dt, const float *A, const float *B,
+                   const float *C, const double *h0, double *y, double *hT,
+                   int64_t Bsz, int64_t L, int64_t H, int64_t P, int64_t N,
+                   int dt_softplus)
+{
+    if (Bsz < 0 || L < 0 || H < 0 || P < 1 || N < 1 || !y || !hT || (H > 0 && !A))
+        return -1;
+    if (L > 0 && (!x || !dt || !B || !C))
+        return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(N * P));
+    if (!h)
+        return -1;
+    for (int64_t b = 0; b < Bsz; ++b) {
+        for (int64_t hd = 0; hd < H; ++hd) {
+            const int64_t s0 = (b * H + hd) * N * P;
+            for (int64_t i = 0; i < N * P; ++i)
+                h[i] = h0 ? h0[s0 + i] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t bt = b * L + t;
+                double dl = (double)dt[bt * H + hd];
+                if (dt_softplus)
+                    dl = oracle_softplus(dl);
+                const double a = exp(dl * (double)A[hd]);
+                const float *xv = x + (bt * H + hd) * P;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double db = dl * (double)B[bt * N + n];
+                    for (int64_t p = 0; p < P; ++p)
+                        h[n * P + p] = a * h[n * P + p] + db * (double)xv[p];
+                }
+                double *yv = y + (bt * H + hd) * P;
+                for (int64_t p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n)
+                        acc += (double)C[bt * N + n] * h[n * P + p];
+                    yv[p] = acc;
+                }
+            }
+            for (int64_t i = 0; i < N * P; ++i)
+                hT[s0 + i] = h[i];
+        }
+    }
+    free(h);
+    return 0;
+}

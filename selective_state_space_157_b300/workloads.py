@@ -30,7 +30,8 @@ BF16 = "bf16"
 
 # tensor ids of the per-tensor random streams
 _TID = {"x": 1, "delta": 2, "A": 3, "B": 4, "C": 5, "h0": 6, "Dskip": 7, "z": 8, "conv_w": 9, "conv_b": 10,
-        "conv_state": 11, "dy": 12, "dhT": 13}
+        "conv_state": 11, "dy": 12, "dhT": 13,
+        "ssd_x": 14, "ssd_dt": 15, "ssd_A": 16, "ssd_B": 17, "ssd_C": 18, "ssd_h0": 19}
 
 
 @dataclass(frozen=True)
@@ -224,3 +225,17 @@ def bwd_grads(Bsz: int, L: int, D: int, N: int, *, seed: int, with_dhT: bool = T
     dy = normal(rng(seed, _TID["dy"]), (Bsz, L, D))
     dhT = normal(rng(seed, _TID["dhT"]), (Bsz, D, N)) if with_dhT else None
     return dy, dhT
+
+
+def ssd_inputs(Bsz: int, L: int, H: int, P: int, N: int, *, seed: int, u_mean: float = -3.0,
+               with_h0: bool = False):
+    """Inputs of a Mamba-2 SSD call: x (Bsz, L, H, P), B, C (Bsz, L, N) ~ N(0, 1);
+    the step pre-activation dt (Bsz, L, H) ~ N(u_mean, 1); A (H,) = -exp(U(log 1,
+    log 16)), one scalar per head; h0 (Bsz, H, N, P) ~ N(0, 1) when asked (fp32)."""
+    x = normal(rng(seed, _TID["ssd_x"]), (Bsz, L, H, P))
+    dt = normal(rng(seed, _TID["ssd_dt"]), (Bsz, L, H), u_mean)
+    A = (-np.exp(rng(seed, _TID["ssd_A"]).uniform(0.0, np.log(16.0), size=(H,)))).astype(np.float32)
+    B = normal(rng(seed, _TID["ssd_B"]), (Bsz, L, N))
+    C = normal(rng(seed, _TID["ssd_C"]), (Bsz, L, N))
+    h0 = normal(rng(seed, _TID["ssd_h0"]), (Bsz, H, N, P)) if with_h0 else None
+    return x, dt, A, B, C, h0

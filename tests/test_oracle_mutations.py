@@ -89,6 +89,13 @@ MUTATIONS = {
     "bwd_dh0_before_last_decay": ("        for (int64_t n = 0; n < N; ++n)\n                    dh0[(b * D + d) * N + n] = g[n];",
                                   "        for (int64_t n = 0; n < N; ++n)\n                    dh0[(b * D + d) * N + n] = g[n] / exp(dls[0] * (double)A[d * N + n]);"),
     "bwd_ghT_ignored": ("g[n] = ghT ? ghT[(b * D + d) * N + n] : 0.0;", "g[n] = 0.0;"),
+    "ssd_decay_first_head": ("const double a = exp(dl * (double)A[hd]);", "const double a = exp(dl * (double)A[0]);"),
+    "ssd_input_without_dt": ("const double db = dl * (double)B[bt * N + n];", "const double db = (double)B[bt * N + n];"),
+    "ssd_readout_uses_B": ("acc += (double)C[bt * N + n] * h[n * P + p];", "acc += (double)B[bt * N + n] * h[n * P + p];"),
+    "ssd_h0_ignored": ("h[i] = h0 ? h0[s0 + i] : 0.0;", "h[i] = 0.0;"),
+    "ssd_x_first_column": ("h[n * P + p] = a * h[n * P + p] + db * (double)xv[p];",
+                           "h[n * P + p] = a * h[n * P + p] + db * (double)xv[0];"),
+    "ssd_softplus_ignored": ("                if (dt_softplus)\n                    dl = oracle_softplus(dl);\n                const double a", "                const double a"),
 }
 
 

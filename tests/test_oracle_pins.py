@@ -661,3 +661,108 @@ def test_bwd_empty_sequence_passes_the_state_gradient_through(orc):
     ghT = np.random.default_rng(77).standard_normal(hh.shape)
     gr = orc.selscan_bwd(x, u, A, B, C, np.zeros(x.shape), True, h0=hh, ghT=ghT)
     assert np.array_equal(gr["dh0"], ghT) and not gr["dA"].any()
+
+
+# ---- Mamba-2 SSD -------------------------------------------------------------
+# The state-space-dual model of "Mamba: Selective State Space Models"
+# (youngju.dev), section 4.1: a recurrence with a scalar decay per head, and
+# its dual Y = (T * M) X with T the causal mask and M semiseparable.
+
+def ssd_case(Bsz, L, H, P, N, seed, h0=True, softplus=True):
+    x, dt, A, B, C, hh = W.ssd_inputs(Bsz, L, H, P, N, seed=seed, with_h0=h0)
+    if not softplus:
+        dt = np.abs(dt) * np.float32(0.1)
+    return x, dt, A, B, C, hh
+
+
+def test_ssd_headdim_one_is_the_selective_scan(orc):
+    """With headdim 1 and one head per channel, the SSD recurrence is the
+    selective scan with A[d, n] = A_head for every state n."""
+    Bsz, L, H, N = 2, 40, 5, 6
+    x, dt, A, B, C, hh = ssd_case(Bsz, L, H, 1, N, seed=80)
+    y, hT = orc.ssd_fwd(x, dt, A, B, C, True, h0=hh)
+    A_dn = np.repeat(A[:, None], N, axis=1)
+    ys, hs = orc.selscan_fwd(x[..., 0], dt, A_dn, B, C, True, h0=hh[..., 0].astype(np.float64))
+    close(y[..., 0], ys, rtol=1e-14, atol=1e-15)
+    close(hT[..., 0], hs, rtol=1e-14, atol=1e-15)
+
+
+def ssd_dual(x, dt, A, B, C, h0, softplus):
+    """The attention view: for each (b, head), with cum_t = sum_{r<=t} dl_r A,
+    M[t, s] = (C_t . B_s) dl_s exp(cum_t - cum_s) under the causal mask, y = M x
+    (+ C_t exp(cum_t) h0); hT = sum_s exp(cum_{L-1} - cum_s) dl_s B_s x_s^T
+    (+ exp(cum_{L-1}) h0)."""
+    x = x.astype(np.float64); B = B.astype(np.float64); C = C.astype(np.float64)
+    dl = sp(dt) if softplus else dt.astype(np.float64)
+    Bsz, L, H, P = x.shape
+    N = B.shape[2]
+    y = np.zeros(x.shape); hT = np.zeros((Bsz, H, N, P))
+    T = np.tril(np.ones((L, L)))
+    for b in range(Bsz):
+        G = C[b] @ B[b].T                                   # (L, L): C_t . B_s
+        for hd in range(H):
+            cum = np.cumsum(dl[b, :, hd] * np.float64(A[hd]))
+            decay = np.exp(np.minimum(cum[:, None] - cum[None, :], 0.0))
+            M = T * G * dl[b, None, :, hd] * decay
+            y[b, :, hd] = M @ x[b, :, hd]
+            w = np.exp(cum[-1] - cum) * dl[b, :, hd]
+            hT[b, hd] = (B[b] * w[:, None]).T @ x[b, :, hd]
+            if h0 is not None:
+                y[b, :, hd] += (C[b] * np.exp(cum)[:, None]) @ h0[b, hd]
+                hT[b, hd] += np.exp(cum[-1]) * h0[b, hd]
+    return y, hT
+
+
+@pytest.mark.parametrize("softplus,h0", [(True, True), (False, False)])
+def test_ssd_dual_quadratic_form(orc, softplus, h0):
+    x, dt, A, B, C, hh = ssd_case(2, 33, 3, 4, 5, seed=81 + h0, h0=h0, softplus=softplus)
+    y, hT = orc.ssd_fwd(x, dt, A, B, C, softplus, h0=hh)
+    yd, hd = ssd_dual(x, dt, A, B, C, None if hh is None else hh.astype(np.float64), softplus)
+    close(y, yd, rtol=1e-11, atol=1e-12)
+    close(hT, hd, rtol=1e-11, atol=1e-12)
+
+
+def ssd_chunked(x, dt, A, B, C, h0, Q):
+    """The chunked form: inside a chunk of Q steps the dual form, across
+    chunks the state carried by its decay (the composition of section 4.1's
+    recurrence over a chunk)."""
+    x = x.astype(np.float64); B = B.astype(np.float64); C = C.astype(np.float64)
+    dl = sp(dt)
+    Bsz, L, H, P = x.shape
+    N = B.shape[2]
+    y = np.zeros(x.shape); hT = np.zeros((Bsz, H, N, P))
+    for b in range(Bsz):
+        for hd in range(H):
+            st = np.zeros((N, P)) if h0 is None else h0[b, hd].copy()
+            for c0 in range(0, L, Q):
+                sl = slice(c0, min(L, c0 + Q))
+                q = sl.stop - sl.start
+                cum = np.cumsum(dl[b, sl, hd] * np.float64(A[hd]))
+                decay = np.tril(np.exp(np.minimum(cum[:, None] - cum[None, :], 0.0)))
+                M = (C[b, sl] @ B[b, sl].T) * dl[b, None, sl, hd] * decay
+                y[b, sl, hd] = M @ x[b, sl, hd] + (C[b, sl] * np.exp(cum)[:, None]) @ st
+                w = np.exp(cum[-1] - cum) * dl[b, sl, hd]
+                st = np.exp(cum[-1]) * st + (B[b, sl] * w[:, None]).T @ x[b, sl, hd]
+                assert q >= 1
+            hT[b, hd] = st
+    return y, hT
+
+
+@pytest.mark.parametrize("Q", [1, 8, 16, 64])
+def test_ssd_chunked_algorithm_equals_recurrence(orc, Q):
+    x, dt, A, B, C, hh = ssd_case(1, 50, 2, 8, 16, seed=83)
+    y, hT = orc.ssd_fwd(x, dt, A, B, C, True, h0=hh)
+    yc, hc = ssd_chunked(x, dt, A, B, C, hh.astype(np.float64), Q)
+    close(y, yc, rtol=1e-11, atol=1e-12)
+    close(hT, hc, rtol=1e-11, atol=1e-12)
+
+
+def test_ssd_heads_are_independent_and_linear(orc):
+    x, dt, A, B, C, hh = ssd_case(1, 20, 4, 3, 5, seed=84)
+    y, hT = orc.ssd_fwd(x, dt, A, B, C, True, h0=hh)
+    perm = np.array([2, 0, 3, 1])
+    yp, hp = orc.ssd_fwd(x[:, :, perm], dt[:, :, perm], A[perm], B, C, True, h0=hh[:, perm])
+    assert np.array_equal(yp, y[:, :, perm]) and np.array_equal(hp, hT[:, perm])
+    y2, h2 = orc.ssd_fwd(2 * x, dt, A, B, C, True, h0=2 * hh.astype(np.float64))
+    close(y2, 2 * y, rtol=1e-14, atol=1e-15)
+    close(h2, 2 * hT, rtol=1e-14, atol=1e-15)
