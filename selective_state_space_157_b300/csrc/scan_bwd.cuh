@@ -22,12 +22,15 @@
 //   2. The chunks are then taken last to first: the chunk's states and decays
 //      are recomputed from its checkpoint into registers, and the adjoint runs
 //      backwards through them.
-// Per-timestep inputs of a chunk are staged in shared memory by the whole
-// block with coalesced loads (one row of cpb channels per step). dx and
-// d delta are written by lane 0 of each chain; dB and dC are summed over the
-// chains of a warp with shuffles, over the warps in shared memory, and added
-// to global memory with one atomic per block, timestep and state; dA is
-// summed over t in registers and added with one atomic per chain.
+// Per-timestep inputs of a chunk are loaded by the whole block with
+// coalesced loads (one row of cpb channels per step) into registers one
+// chunk ahead, then staged in shared memory. Each lane keeps its dx and
+// d delta terms for the chunk's steps; one reduce-scatter over the lane group
+// per chunk leaves every lane with whole steps to store. dB and dC are summed
+// over the chains of a warp with shuffles, over the warps in shared memory,
+// and added to global memory with one atomic per block, timestep and state;
+// dA is summed over t in registers and added with one atomic per chain.
+// Chunks that lie wholly inside L run without per-step bounds checks.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -357,6 +360,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(BwdArgs a)
 
 // ---- host side: the launch shape and the launch --------------------------
 
+// The checkpoint workspace of a call is Bsz * nch * D * P floats.
 struct BwdShape {
     int P;           // lanes per chain
     int cpb;         // chains per block
@@ -375,13 +379,6 @@ inline BwdShape bwd_shape(int64_t L, int64_t D, int64_t N)
     s.gx = (D + s.cpb - 1) / s.cpb;
     s.smem = (size_t)bwd_smem_floats(s.P, s.cpb) * 4;
     return s;
-}
-
-// Checkpoint workspace of a call, in floats: Bsz * nch * D * P (the caller
-// checks the product for overflow).
-inline int64_t bwd_ckpt_floats(const BwdShape &s, int64_t Bsz, int64_t D)
-{
-    return Bsz * s.nch * D * s.P;
 }
 
 // a.P, a.cpb and a.nch are filled in from s; grid (s.gx, Bsz).
