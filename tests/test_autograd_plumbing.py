@@ -75,3 +75,13 @@ def test_selective_scan_gradients(orc, monkeypatch, with_h0, use_hT, softplus):
     for got, ref in pairs:
         assert got.grad.dtype == torch.float32        # the stand-in's fp64 gradients, cast by autograd
         assert torch.allclose(got.grad.double(), ref.grad, rtol=1e-6, atol=1e-7)
+
+
+def test_smoke_backward_block_runs_on_stand_ins(orc, monkeypatch):
+    """The backward block of the smoke check, with selscan_bwd routed to the
+    oracle-backed stand-in (so its own code runs here, on the CPU)."""
+    import numpy as np
+    import __graft_entry__ as ge
+    monkeypatch.setattr(ss, "selscan_bwd", fake_bwd(orc))
+    err = lambda got, ref: float(np.max(np.abs(got - ref) / (1.0 + np.abs(ref))))
+    ge._smoke_backward(torch.device("cpu"), err)
