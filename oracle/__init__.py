@@ -82,6 +82,8 @@ class Oracle:
         lib.oracle_conv1d.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT]
         lib.oracle_ssd_fwd.restype = INT
         lib.oracle_ssd_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, INT]
+        lib.oracle_selscan_bwd_gated.restype = INT
+        lib.oracle_selscan_bwd_gated.argtypes = [P] * 18 + [I64, I64, I64, I64, INT]
         lib.oracle_selscan_bwd.restype = INT
         lib.oracle_selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT]
         self._lib = lib
@@ -212,14 +214,19 @@ class Oracle:
         return out, st
 
 
-    def selscan_bwd(self, x, delta, A, B, C, gy, delta_softplus=False, h0=None, ghT=None):
-        """Gradients of a loss through the scan (dl * B form, no gate), by the
-        plain reverse sweep over each chain's stored states.
+    def selscan_bwd(self, x, delta, A, B, C, gy, delta_softplus=False, h0=None, ghT=None, Dskip=None, z=None):
+        """Gradients of a loss through the scan (dl * B form), by the plain
+        reverse sweep over each chain's stored states.
 
         Shapes as selscan_fwd; gy (Bsz, L, D) = dLoss/dy, ghT (Bsz, D, N) =
         dLoss/dhT or None. Returns a dict of float64 arrays dx, ddelta
         (Bsz, L, D), dA (D, N), dB, dC (Bsz, L, N) and dh0 (Bsz, D, N).
+        With Dskip (D,) and/or z (Bsz, L, D), y is the block's output
+        (y + Dskip x) silu(z), gy its gradient, and the dict adds dDskip (D,)
+        and/or dz (Bsz, L, D).
         """
+        if Dskip is not None or z is not None:
+            return self._selscan_bwd_gated(x, delta, A, B, C, gy, delta_softplus, h0, ghT, Dskip, z)
         x = np.asarray(x)
         Bsz, L, D = x.shape
         N = np.asarray(A).shape[1]
@@ -241,6 +248,34 @@ class Oracle:
             raise RuntimeError("oracle_selscan_bwd failed")
         return g
 
+
+    def _selscan_bwd_gated(self, x, delta, A, B, C, gy, delta_softplus, h0, ghT, Dskip, z):
+        x = np.asarray(x)
+        Bsz, L, D = x.shape
+        N = np.asarray(A).shape[1]
+        x = _f32(x, (Bsz, L, D), "x")
+        delta = _f32(delta, (Bsz, L, D), "delta")
+        A = _f32(A, (D, N), "A")
+        B = _f32(B, (Bsz, L, N), "B")
+        C = _f32(C, (Bsz, L, N), "C")
+        h0 = None if h0 is None else _f64(h0, (Bsz, D, N), "h0")
+        gy = _f64(gy, (Bsz, L, D), "gy")
+        ghT = None if ghT is None else _f64(ghT, (Bsz, D, N), "ghT")
+        Dskip = None if Dskip is None else _f32(Dskip, (D,), "Dskip")
+        z = None if z is None else _f32(z, (Bsz, L, D), "z")
+        g = dict(dx=np.zeros((Bsz, L, D)), ddelta=np.zeros((Bsz, L, D)), dA=np.zeros((D, N)),
+                 dB=np.zeros((Bsz, L, N)), dC=np.zeros((Bsz, L, N)), dh0=np.zeros((Bsz, D, N)))
+        if Dskip is not None:
+            g["dDskip"] = np.zeros((D,))
+        if z is not None:
+            g["dz"] = np.zeros((Bsz, L, D))
+        rc = self._lib.oracle_selscan_bwd_gated(
+            _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip), _ptr(z), _ptr(h0), _ptr(gy), _ptr(ghT),
+            _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dh0"]),
+            _ptr(g.get("dDskip")), _ptr(g.get("dz")), Bsz, L, D, N, int(bool(delta_softplus)))
+        if rc != 0:
+            raise RuntimeError("oracle_selscan_bwd_gated failed")
+        return g
 
     def ssd_fwd(self, x, dt, A, B, C, dt_softplus=False, h0=None):
         """Mamba-2 SSD forward in fp64 (see oracle.c): x (Bsz, L, H, P),

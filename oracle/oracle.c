@@ -566,3 +566,67 @@ int oracle_ssd_fwd(const float *x, const float *dt, const float *A, const float 
     free(h);
     return 0;
 }
+
+/* Backward of the block's output around the scan (youngju.dev "Mamba:
+ * Selective State Space Models", section 3.4, the MambaBlock listing):
+ * out = (y + Dskip[d] x) * silu(z) with y the scan's read-out, given dout =
+ * dLoss/dout (Bsz, L, D) and dLoss/dhT. With s = sigmoid(z), silu(z) = z s
+ * and silu'(z) = s (1 + z (1 - s)):
+ *   the scan's backward (oracle_selscan_bwd) takes gy = dout * silu(z);
+ *   dz      = dout * (y + Dskip x) * silu'(z)            (Bsz, L, D)
+ *   dDskip  = sum_{b,t} dout * silu(z) * x               (D)
+ *   dx     += dout * silu(z) * Dskip.
+ * Either term may be absent (Dskip NULL: no skip, dDskip untouched; z NULL:
+ * no gate, dz untouched). Outputs as oracle_selscan_bwd, plus dDskip and dz
+ * (double, zeroed here when their term is present). */
+int oracle_selscan_bwd_gated(const float *x, const float *delta, const float *A,
+                             const float *B, const float *C, const float *Dskip,
+                             const float *z, const double *h0, const double *dout,
+                             const double *ghT, double *dx, double *ddelta, double *dA,
+                             double *dB, double *dC, double *dh0, double *dDskip, double *dz,
+                             int64_t Bsz, int64_t L, int64_t D, int64_t N, int delta_softplus)
+{
+    if (Bsz < 0 || L < 0 || D < 0 || N < 1 || !dout || (Dskip && !dDskip) || (z && !dz))
+        return -1;
+    const size_t E = (size_t)(Bsz * L * D);
+    double *y = (double *)malloc(sizeof(double) * (E > 0 ? E : 1));
+    double *gy = (double *)malloc(sizeof(double) * (E > 0 ? E : 1));
+    if (!y || !gy) {
+        free(y); free(gy);
+        return -1;
+    }
+    int rc = oracle_selscan_fwd_gated(x, delta, A, B, C, NULL, NULL, h0, y, NULL, Bsz, L, D, N,
+                                      delta_softplus, 0, 1);
+    if (rc == 0) {
+        for (size_t i = 0; i < E; ++i) {
+            double g = dout[i];
+            if (z) {
+                const double zv = (double)z[i];
+                g *= zv / (1.0 + exp(-zv));
+            }
+            gy[i] = g;
+        }
+        rc = oracle_selscan_bwd(x, delta, A, B, C, h0, gy, ghT, dx, ddelta, dA, dB, dC, dh0,
+                                Bsz, L, D, N, delta_softplus);
+    }
+    if (rc == 0) {
+        if (Dskip)
+            memset(dDskip, 0, sizeof(double) * (size_t)D);
+        for (size_t i = 0; i < E; ++i) {
+            const int64_t d = (int64_t)(i % (size_t)D);
+            const double xv = (double)x[i];
+            if (Dskip) {
+                dDskip[d] += gy[i] * xv;
+                dx[i] += gy[i] * (double)Dskip[d];
+            }
+            if (z) {
+                const double zv = (double)z[i];
+                const double s = 1.0 / (1.0 + exp(-zv));
+                const double pre = y[i] + (Dskip ? (double)Dskip[d] * xv : 0.0);
+                dz[i] = dout[i] * pre * s * (1.0 + zv * (1.0 - s));
+            }
+        }
+    }
+    free(y); free(gy);
+    return rc;
+}

@@ -96,6 +96,11 @@ MUTATIONS = {
     "ssd_x_first_column": ("h[n * P + p] = a * h[n * P + p] + db * (double)xv[p];",
                            "h[n * P + p] = a * h[n * P + p] + db * (double)xv[0];"),
     "ssd_softplus_ignored": ("                if (dt_softplus)\n                    dl = oracle_softplus(dl);\n                const double a", "                const double a"),
+    "bwd_gate_derivative_partial": ("dz[i] = dout[i] * pre * s * (1.0 + zv * (1.0 - s));", "dz[i] = dout[i] * pre * s;"),
+    "bwd_gate_scan_gradient_ungated": ("                g *= zv / (1.0 + exp(-zv));\n", ""),
+    "bwd_skip_missing_from_dx": ("                dx[i] += gy[i] * (double)Dskip[d];\n", ""),
+    "bwd_dDskip_ungated": ("dDskip[d] += gy[i] * xv;", "dDskip[d] += dout[i] * xv;"),
+    "bwd_dz_without_skip": ("const double pre = y[i] + (Dskip ? (double)Dskip[d] * xv : 0.0);", "const double pre = y[i];"),
 }
 
 

@@ -766,3 +766,75 @@ def test_ssd_heads_are_independent_and_linear(orc):
     y2, h2 = orc.ssd_fwd(2 * x, dt, A, B, C, True, h0=2 * hh.astype(np.float64))
     close(y2, 2 * y, rtol=1e-14, atol=1e-15)
     close(h2, 2 * hT, rtol=1e-14, atol=1e-15)
+
+
+# ---- the backward of the block's skip and gate ------------------------------
+
+def _gated_case(seed, terms):
+    x, u, A, B, C, hh = rand_inputs(2, 5, 2, 3, seed=seed, h0=True)
+    g = np.random.default_rng(seed + 1)
+    Dskip = (0.5 + g.random(2)).astype(np.float32) if terms != "gate" else None
+    z = g.standard_normal(x.shape).astype(np.float32) if terms != "skip" else None
+    q = lambda v: None if v is None else np.round(v * 4096.0).astype(np.float32) / np.float32(4096.0)
+    return tuple(q(v) for v in (x, u, A, B, C)) + (hh, q(Dskip), q(z))
+
+
+@pytest.mark.parametrize("terms", ["both", "skip", "gate"])
+def test_bwd_gated_matches_central_differences(orc, terms):
+    """Every gradient of a loss on the block's output (y + Dskip x) silu(z)
+    against Richardson central differences of the gated forward oracle (inputs
+    on a 2^-12 grid, so every perturbation is exact in fp32)."""
+    x, u, A, B, C, hh, Dskip, z = _gated_case(90 + len(terms), terms)
+    g = np.random.default_rng(91)
+    gy = g.standard_normal(x.shape)
+    ghT = g.standard_normal((2, 2, 3))
+    grads = orc.selscan_bwd(x, u, A, B, C, gy, True, h0=hh, ghT=ghT, Dskip=Dskip, z=z)
+    args = dict(x=x, u=u, A=A, B=B, C=C, h0=hh, Dskip=Dskip, z=z)
+    names = dict(x="dx", u="ddelta", A="dA", B="dB", C="dC", h0="dh0", Dskip="dDskip", z="dz")
+
+    def loss(a):
+        y, hT = orc.selscan_fwd(a["x"], a["u"], a["A"], a["B"], a["C"], True, h0=a["h0"], Dskip=a["Dskip"],
+                                z=a["z"])
+        return float(np.sum(gy * y) + np.sum(ghT * hT))
+
+    for key, gname in names.items():
+        base = args[key]
+        if base is None:
+            assert gname not in grads
+            continue
+        num = np.zeros(base.shape)
+        for idx in np.ndindex(base.shape):
+            def f(v, key=key, idx=idx):
+                a = {k: (None if w is None else w.copy()) for k, w in args.items()}
+                a[key][idx] = v
+                return loss(a)
+            v0 = float(base[idx])
+            d1, d2 = _central(f, v0, 2.0 ** -9), _central(f, v0, 2.0 ** -10)
+            num[idx] = (4 * d2 - d1) / 3
+        close(grads[gname], num, rtol=1e-9, atol=1e-10)
+
+
+def test_bwd_gated_matches_autograd(orc):
+    import torch
+    x, u, A, B, C, hh = rand_inputs(2, 40, 3, 4, seed=94, h0=True)
+    g = np.random.default_rng(95)
+    Dskip = (0.5 + g.random(3)).astype(np.float32)
+    z = g.standard_normal(x.shape).astype(np.float32)
+    gy = g.standard_normal(x.shape)
+    ghT = g.standard_normal(hh.shape)
+    got = orc.selscan_bwd(x, u, A, B, C, gy, True, h0=hh, ghT=ghT, Dskip=Dskip, z=z)
+    t = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    tx, tu, tA, tB, tC, th0, tD, tz = (t(v) for v in (x, u, A, B, C, hh, Dskip, z))
+    dl = torch.nn.functional.softplus(tu)
+    h = th0
+    ys = []
+    for s in range(x.shape[1]):
+        d = dl[:, s, :, None]
+        h = torch.exp(d * tA[None]) * h + d * tB[:, s, None, :] * tx[:, s, :, None]
+        ys.append((h * tC[:, s, None, :]).sum(-1))
+    y = (torch.stack(ys, 1) + tD * tx) * torch.nn.functional.silu(tz)
+    ((y * torch.from_numpy(gy)).sum() + (h * torch.from_numpy(ghT)).sum()).backward()
+    ref = dict(dx=tx.grad, ddelta=tu.grad, dA=tA.grad, dB=tB.grad, dC=tC.grad, dh0=th0.grad, dDskip=tD.grad,
+               dz=tz.grad)
+    for k, v in ref.items():
+        close(got[k], v.numpy(), rtol=1e-11, atol=1e-12)
