@@ -147,3 +147,21 @@ def test_reference_arm_runs_gated_workload():
     assert out.returncode == 0, out.stderr
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and "gate" in line["config"]["workload"]
+
+
+def test_backward_work_counts():
+    w = bench.bwd_work_counts(2, 2048, 1536, 16)
+    E, S = 2 * 2048 * 1536, 2 * 2048 * 16
+    assert w["bytes"] == 5 * E * 4 + 4 * S * 4 + 2 * 1536 * 16 * 4 == 127_074_304
+    assert w["mufu"] == E * 16 + 4 * E and w["fp32"] == 21 * E * 16
+    roof = bench.roofline(w, bench.peaks(148, 2032.0, 6484.3), 389e-6)
+    assert roof["bound"] == "alu"                     # the adjoint's FP32 work binds, not the bytes
+    assert roof["frac"] == pytest.approx(roof["t_roof_us"]["fp32"] / 389.0)
+
+
+def test_traffic_is_null_when_the_kernel_changed(monkeypatch):
+    """profiled_traffic returns the stored bytes only while the digest of the
+    kernel's sources matches the one stored with them."""
+    from selective_state_space_157_b300 import build as bld
+    monkeypatch.setattr(bld, "source_digest", lambda backward=False: "0000000000000000")
+    assert bench.profiled_traffic(2) is None and bench.profiled_traffic(9) is None
