@@ -45,10 +45,19 @@
  * each chain runs the loop above unchanged, so the thread count does not
  * change any result bit.
  *
+ * Also here, each with its own comment below: the backward pass of the scan
+ * (oracle_selscan_bwd, a plain reverse sweep over each chain's stored
+ * states) and of the block's skip and gate (oracle_selscan_bwd_gated), the
+ * causal conv1d before the scan (oracle_conv1d), and the Mamba-2 SSD
+ * forward (oracle_ssd_fwd).
+ *
  * Pins (tests/test_oracle_pins.py): brute-force unrolled sum, A = 0 running
  * sum, N = 1 scalar recurrence, L = 1 closed form, LTI convolution kernel,
  * geometric closed form, delta -> 0 persistence, delta -> inf reset,
- * chunked associative composition, step == forward, linearity.
+ * chunked associative composition, step == forward, linearity; for the
+ * backward, central differences of the forward, autograd of an unrolled
+ * forward and homogeneity identities; for SSD, its dual quadratic form, a
+ * chunked form and the selective scan at headdim 1.
  */
 #include <math.h>
 #include <pthread.h>
