@@ -1,9 +1,10 @@
 """selscan_bwd: the backward pass of the scan against the fp64 oracle's
 reverse sweep, on the same fp32 inputs and upstream gradients. Covers one
-and many 16-step chunks with ragged tails, channel counts that leave the
-last block partly empty, every lane-group width (N = 1, 5, 16, 32), with and
-without softplus, h0 and dhT, the empty sequence, and the 130M-like layer
-at full size."""
+and many 32-step chunks with ragged tails, channel counts that leave the
+last block partly empty, every lane-group width (N = 1, 2, 3 to 4, 5 to 8,
+16, 32), with and without softplus, h0 and dhT, the empty sequence, the
+130M-like layer at full size, and autograd through the differentiable
+wrapper."""
 import numpy as np
 import pytest
 import torch
