@@ -54,3 +54,18 @@ def test_decode_inputs():
     assert np.all(dl > 0)
     x2, _, _, _ = W.decode_step_inputs(w, 4)
     assert not np.array_equal(x, x2)
+
+
+def test_backward_gradients_and_ssd_inputs():
+    dy, dhT = W.bwd_grads(2, 50, 8, 4, seed=5)
+    dy2, _ = W.bwd_grads(2, 50, 8, 4, seed=5, with_dhT=False)
+    assert dy.shape == (2, 50, 8) and dhT.shape == (2, 8, 4) and np.array_equal(dy, dy2)
+    assert dy.dtype == np.float32 and not np.array_equal(dy[0, :4, :4], dhT[0])
+    w9 = W.WORKLOADS[9]
+    assert w9.backward and (w9.Bsz, w9.L, w9.D, w9.N) == (2, 2048, 1536, 16)
+    x, dt, A, B, C, h0 = W.ssd_inputs(1, 64, 8, 16, 32, seed=6, with_h0=True)
+    assert x.shape == (1, 64, 8, 16) and dt.shape == (1, 64, 8) and A.shape == (8,)
+    assert B.shape == C.shape == (1, 64, 32) and h0.shape == (1, 8, 32, 16)
+    assert np.all(A <= -1.0) and np.all(A >= -16.0) and not np.array_equal(B, C)
+    x2, *_ = W.ssd_inputs(1, 64, 8, 16, 32, seed=6)
+    assert np.array_equal(x, x2)
