@@ -165,3 +165,13 @@ def test_traffic_is_null_when_the_kernel_changed(monkeypatch):
     from selective_state_space_157_b300 import build as bld
     monkeypatch.setattr(bld, "source_digest", lambda backward=False: "0000000000000000")
     assert bench.profiled_traffic(2) is None and bench.profiled_traffic(9) is None
+
+
+def test_reference_arm_runs_backward_workload():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "9", "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and "backward" in line["config"]["workload"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
