@@ -4,12 +4,22 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl reference]
 
 One step is one selscan_fwd call over one batch of the workload (default:
-the Mamba-130M-like layer scan, Bsz=2 L=2048 D=1536 N=16 fp32, softplus on),
-with its inputs already in device memory. Several copies of the inputs are
-rotated so that every step reads from HBM, not from L2. W untimed warm-up
-steps, then exactly K steps between a barrier and a synchronisation, timed
-with CUDA events on the launching stream; the maximum over ranks is taken.
-Rank 0 prints one JSON line.
+the long-context scan, Bsz=1 L=131072 D=1536 N=16 fp32, softplus on, final
+state returned -- the largest configuration the benchmark statement names),
+with its inputs already in device memory. Inputs larger than L2 are read
+from HBM on every step; smaller ones are rotated over several copies so that
+they are. W untimed warm-up steps, then exactly K steps between a barrier and
+a synchronisation, timed with CUDA events on the launching stream; the
+maximum over ranks is taken. Rank 0 prints one JSON line. With the default
+workload the line also carries ``per_config``: the same measurement, shorter,
+of the 130M-like (2), 370M-like bf16 (3) and decode (5) workloads.
+
+The roofline is the benchmark statement's: the slower of the HBM time
+(algorithmic bytes over the measured copy bandwidth) and the MUFU time plus
+the FP32 time (exponentials over the measured ex2 rate, plus FP32 operations
+over the measured FMA rate; both rates from the committed probe
+csrc/probe/alu_peaks.cu, run at the start of every bench). ``frac`` is
+measured against that bound; ``frac_strict`` against max(HBM, MUFU, FP32).
 
 Several GPUs run independent replicas (the scan has no cross-GPU exchange):
 every rank processes the same workload on its own GPU and `value` counts
@@ -36,13 +46,14 @@ if ROOT not in sys.path:
 METRIC = "selective-scan B·L·D elems/s and HBM GB/s as % of roofline (1 B300)"
 UNIT = "elem/s"
 
-# Per-SM unit counts of the B300 (sm_103) used for the arithmetic roofline:
-# the special-function unit issues 32 base-2 exponentials per clock per SM
-# (measured: 29.7/clk at the nominal clock, 8.9 T/s on 148 SMs), the FP32
-# pipe 128 lanes per clock per SM.
+# Per-SM unit counts of the B300 (sm_103), used for the arithmetic roofline
+# only when the peak probe cannot run (the line then says "derived"): 32
+# base-2 exponentials and 128 FP32 lanes per clock per SM.
 MUFU_EX2_PER_CLK_SM = 32
 FP32_PER_CLK_SM = 128
 FALLBACK_HBM_GBS = 6400.0   # used only if the measured peak file is absent
+DEFAULT_WORKLOAD = 4
+PER_CONFIG = (2, 3, 5)
 
 
 # --------------------------------------------------------------- roofline
@@ -105,32 +116,38 @@ def step_work_counts(Bsz, D, N):
     return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": E * N, "fp32": 4 * E * N}
 
 
-def peaks(sms: int, sm_mhz: float, hbm_gbs: float):
-    return {"mufu_per_s": sms * MUFU_EX2_PER_CLK_SM * sm_mhz * 1e6,
-            "fp32_per_s": sms * FP32_PER_CLK_SM * sm_mhz * 1e6,
-            "hbm_bytes_per_s": hbm_gbs * 1e9}
+def peaks(sms: int, sm_mhz: float, hbm_gbs: float, alu=None):
+    """Roofline denominators: the measured HBM copy rate, and the ex2 and FP32
+    rates from the probe (``alu``, ops/s) or, failing that, derived from the
+    unit counts at the maximum SM clock."""
+    if alu:
+        mufu, fp32 = alu["ex2_per_s"], alu["fp32_per_s"]
+    else:
+        mufu, fp32 = sms * MUFU_EX2_PER_CLK_SM * sm_mhz * 1e6, sms * FP32_PER_CLK_SM * sm_mhz * 1e6
+    return {"mufu_per_s": mufu, "fp32_per_s": fp32, "hbm_bytes_per_s": hbm_gbs * 1e9}
 
 
 def roofline(work: dict, pk: dict, seconds: float, traffic=None, kernel="selscan_fwd"):
-    """Roofline of one call: strict bound max(t_HBM, t_MUFU, t_FP32), and the
-    summed form max(t_HBM, t_MUFU + t_FP32) as the benchmark statement words it."""
+    """Roofline of one call. The bound is the benchmark statement's: the
+    slower of t_HBM and t_MUFU + t_FP32 (``frac``); the stricter
+    max(t_HBM, t_MUFU, t_FP32) is reported as ``frac_strict``."""
     t_hbm = work["bytes"] / pk["hbm_bytes_per_s"]
     t_mufu = work["mufu"] / pk["mufu_per_s"]
     t_fp32 = work["fp32"] / pk["fp32_per_s"]
-    t_roof = max(t_hbm, t_mufu, t_fp32)
+    t_strict = max(t_hbm, t_mufu, t_fp32)
     t_sum = max(t_hbm, t_mufu + t_fp32)
-    bound = "hbm" if t_hbm >= max(t_mufu, t_fp32) else "alu"
+    bound = "hbm" if t_hbm >= t_mufu + t_fp32 else "alu"
     if bound == "hbm":   # bytes moved per second against the measured copy bandwidth
         achieved, peak, unit = work["bytes"] / seconds / 1e9, pk["hbm_bytes_per_s"] / 1e9, "GB/s"
-    else:                # state updates per second against the MUFU / FP32 bound
-        achieved, peak, unit = work["updates"] / seconds / 1e12, work["updates"] / t_roof / 1e12, "Tupdate/s"
+    else:                # state updates per second against the MUFU + FP32 bound
+        achieved, peak, unit = work["updates"] / seconds / 1e12, work["updates"] / t_sum / 1e12, "Tupdate/s"
     return {
         "bound": bound,
         "achieved": achieved,
         "peak": peak,
         "unit": unit,
-        "frac": t_roof / seconds,
-        "frac_summed_bound": t_sum / seconds,
+        "frac": t_sum / seconds,
+        "frac_strict": t_strict / seconds,
         "hbm_gbs": work["bytes"] / seconds / 1e9,
         "hbm_frac": t_hbm / seconds,
         "t_roof_us": {"hbm": t_hbm * 1e6, "mufu": t_mufu * 1e6, "fp32": t_fp32 * 1e6},
@@ -140,12 +157,51 @@ def roofline(work: dict, pk: dict, seconds: float, traffic=None, kernel="selscan
     }
 
 
+def measure_alu_peaks():
+    """Runs the committed probe (libselscan_probe.so): ex2 results per second
+    and FP32 lane-operations per second (the larger of the scalar and packed
+    FMA rates). None if the probe is missing or fails."""
+    import ctypes
+    path = os.path.join(ROOT, "selective_state_space_157_b300", "libselscan_probe.so")
+    if not os.path.exists(path):
+        return None
+    try:
+        lib = ctypes.CDLL(path)
+        e, f, f2 = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+        if lib.selscan_probe_alu_peaks(ctypes.byref(e), ctypes.byref(f), ctypes.byref(f2)) != 0:
+            return None
+        return {"ex2_per_s": e.value, "ffma_per_s": f.value, "ffma2_per_s": f2.value,
+                "fp32_per_s": max(f.value, f2.value)}
+    except OSError:
+        return None
+
+
+def peak_source(src_hbm: str, alu, sms: int, mhz: float) -> str:
+    if alu:
+        return (f"HBM {src_hbm}; MUFU {alu['ex2_per_s'] / 1e12:.2f} T ex2/s and FP32 "
+                f"{alu['fp32_per_s'] / 1e12:.2f} T op/s measured by csrc/probe/alu_peaks.cu "
+                f"(scalar FMA {alu['ffma_per_s'] / 1e12:.2f}, packed {alu['ffma2_per_s'] / 1e12:.2f} T op/s)")
+    return (f"HBM {src_hbm}; MUFU/FP32 derived (probe unavailable): {sms} SMs x "
+            f"({MUFU_EX2_PER_CLK_SM} ex2, {FP32_PER_CLK_SM} fp32)/clk x {mhz:.0f} MHz")
+
+
 def read_measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2032.0)), "measured (MEASURED_PEAKS.json)"
     return FALLBACK_HBM_GBS, 2032.0, "fallback"
+
+
+def kernel_family(w) -> str:
+    """The kernel family a workload times (the key of its sources' digest)."""
+    if w.backward:
+        return "bwd"
+    if w.steps:
+        return "step"
+    if w.conv_K:
+        return "conv1d"
+    return "fwd"
 
 
 def profiled_traffic(workload_id: int):
@@ -159,7 +215,7 @@ def profiled_traffic(workload_id: int):
         from selective_state_space_157_b300 import workloads as W
         from selective_state_space_157_b300.build import source_digest
         entry = d.get(str(workload_id))
-        if entry and entry.get("sources") == source_digest(backward=W.WORKLOADS[workload_id].backward):
+        if entry and entry.get("sources") == source_digest(kernel_family(W.WORKLOADS[workload_id])):
             return entry["dram_bytes_per_call"]
     except Exception:
         return None
@@ -335,6 +391,94 @@ def sample_chains(Bsz, D, count):
 
 # --------------------------------------------------------------- GPU runs
 
+class _FwdBench:
+    """Device inputs of a forward workload, rotated over enough copies that
+    more than 2x L2 is touched between reuses, and its step function."""
+
+    def __init__(self, wid, dev):
+        import torch
+        import selective_state_space_157_b300 as ss
+        from selective_state_space_157_b300 import workloads as W
+        self.w = w = W.WORKLOADS[wid]
+        self.inp = inp = W.workload_inputs(wid)
+        self.bf16 = bf16 = w.dtype == W.BF16
+        self.es = es = 2 if bf16 else 4
+        self.gate = W.workload_gate_inputs(wid) if w.gated else None
+
+        def dev_t(a, kind):
+            if bf16 and kind == "io":
+                return torch.from_numpy(a.view("int16")).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        self.Bsz, self.L, self.D = Bsz, L, D = inp.x.shape
+        self.N = N = inp.A.shape[1]
+        self.foot = ((4 if w.gated else 3) * Bsz * L * D + 2 * Bsz * L * N) * es
+        self.l2 = l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.copies = copies = max(1, -(-(2 * l2) // self.foot))
+        base = [dev_t(inp.x, "io"), dev_t(inp.delta, "io"), dev_t(inp.A, "f"), dev_t(inp.B, "io"),
+                dev_t(inp.C, "io")]
+        if w.gated:
+            base += [dev_t(self.gate[1], "io")]
+            self.Dskip_dev = dev_t(self.gate[0], "f")
+        self.sets = [base] + [[t.clone() for t in base] for _ in range(copies - 1)]
+        self.ys = [torch.empty_like(base[0]) for _ in range(copies)]
+        self.hT = torch.empty(Bsz, D, N, device=dev) if w.return_state else None
+        self.ss = ss
+
+    def step(self, i):
+        k = i % self.copies
+        x, dl, A, B, C = self.sets[k][:5]
+        if self.w.zoh:
+            self.ss.selscan_fwd(x, dl, A, B, C, True, None, y=self.ys[k], hT=self.hT, zoh=True)
+        elif self.w.gated:
+            self.ss.selscan_fwd(x, dl, A, B, C, True, None, y=self.ys[k], hT=self.hT,
+                                D_skip=self.Dskip_dev, z=self.sets[k][5])
+        else:
+            self.ss.selscan_fwd(x, dl, A, B, C, True, None, y=self.ys[k], hT=self.hT)
+
+    def l2_note(self):
+        if self.copies > 1:
+            return (f"{self.copies} rotating input sets ({self.copies * self.foot / 1e6:.0f} MB) "
+                    f"> 2x L2 ({self.l2 / 1e6:.0f} MB)")
+        return f"inputs {self.foot / 1e6:.0f} MB > 2x L2 ({self.l2 / 1e6:.0f} MB)"
+
+    def workload_name(self):
+        w = self.w
+        return (f"{w.name}: Bsz={self.Bsz} L={self.L} D={self.D} N={self.N} {w.dtype}, softplus on"
+                + (", returns hT" if w.return_state else "")
+                + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else "")
+                + (", zero-order-hold Bbar" if w.zoh else ""))
+
+    def work(self):
+        return work_counts(self.Bsz, self.L, self.D, self.N, self.es, softplus=True, hT=self.w.return_state,
+                           gated=self.w.gated, zoh=self.w.zoh)
+
+
+def timed_steps(step, steps, warmup, world, dev, local):
+    """W warm-up steps, then K steps between a barrier and a synchronisation,
+    timed with CUDA events on the launching stream, clocks sampled meanwhile.
+    Returns (seconds over all K steps, max over ranks; clock summary)."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ss.check_device_error()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, dev)
+    ss.check_device_error()
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev), clk.summary()
+
+
 def run_gpu(args, world, rank, local):
     import torch
     import selective_state_space_157_b300 as ss
@@ -345,115 +489,37 @@ def run_gpu(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    alu = measure_alu_peaks()
     w = W.WORKLOADS[args.workload]
     if w.steps:
-        return run_decode(args, world, rank, local, dev, w)
+        return run_decode(args, world, rank, local, dev, w, alu)
     if w.conv_K:
-        return run_conv(args, world, rank, local, dev, w)
+        return run_conv(args, world, rank, local, dev, w, alu)
     if w.backward:
-        return run_bwd(args, world, rank, local, dev, w)
-    inp = W.workload_inputs(args.workload)
-    bf16 = w.dtype == W.BF16
-    es = 2 if bf16 else 4
+        return run_bwd(args, world, rank, local, dev, w, alu)
 
-    def dev_t(a, kind):
-        if bf16 and kind == "io":
-            return torch.from_numpy(a.view("int16")).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(a).to(dev)
-
-    Bsz, L, D = inp.x.shape
-    N = inp.A.shape[1]
-    want_hT = w.return_state
-    gate = W.workload_gate_inputs(args.workload) if w.gated else None
-    foot = ((4 if w.gated else 3) * Bsz * L * D + 2 * Bsz * L * N) * es
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    copies = max(1, -(-(2 * l2) // foot))          # rotate until > 2x L2 is touched between reuses
-    base = [dev_t(inp.x, "io"), dev_t(inp.delta, "io"), dev_t(inp.A, "f"),
-            dev_t(inp.B, "io"), dev_t(inp.C, "io")]
-    if w.gated:
-        base += [dev_t(gate[1], "io")]
-        Dskip_dev = dev_t(gate[0], "f")
-    sets = [base] + [[t.clone() for t in base] for _ in range(copies - 1)]
-    ys = [torch.empty_like(base[0]) for _ in range(copies)]
-    hT = torch.empty(Bsz, D, N, device=dev) if want_hT else None
-
-    def step(i):
-        x, dl, A, B, C = sets[i % copies][:5]
-        if w.zoh:
-            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT, zoh=True)
-        elif w.gated:
-            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT,
-                           D_skip=Dskip_dev, z=sets[i % copies][5])
-        else:
-            ss.selscan_fwd(x, dl, A, B, C, True, None, y=ys[i % copies], hT=hT)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    ss.check_device_error()
-
-    plan = ss.fwd_plan(Bsz, L, D, N, bf16=bf16)
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, dev)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world, dev)
-    ss.check_device_error()
-    sec = e0.elapsed_time(e1) / 1e3
-    sec = max_over_ranks(sec, world, dev)
+    fb = _FwdBench(args.workload, dev)
+    Bsz, L, D, N, bf16 = fb.Bsz, fb.L, fb.D, fb.N, fb.bf16
+    sec, clocks = timed_steps(fb.step, args.steps, args.warmup, world, dev, local)
     per_step = sec / args.steps
     elems = Bsz * L * D
     value = world * elems * args.steps / sec
+    plan = ss.fwd_plan(Bsz, L, D, N, bf16=bf16)
+    config = {"workload": fb.workload_name(), "global_batch": Bsz * world, "seq_len": L,
+              "parallelism": f"replicas x{world}", "l2": fb.l2_note(), "plan": plan}
+    work = fb.work()
+    inp, gate = fb.inp, fb.gate
+    del fb
+    torch.cuda.empty_cache()
 
-    # end to end through the public API from pinned host buffers
-    e2e = None
-    if rank == 0 or world > 1:
-        host = [torch.from_numpy(inp.x.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.x),
-                torch.from_numpy(inp.delta.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.delta),
-                torch.from_numpy(inp.A),
-                torch.from_numpy(inp.B.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.B),
-                torch.from_numpy(inp.C.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.C)]
-        y_host = torch.empty(ys[0].shape, dtype=ys[0].dtype, pin_memory=True)
-        e2e_steps = max(1, min(args.steps, 20))
-        if w.zoh:
-            host = [t.pin_memory() for t in host]
+    e2e = fwd_e2e(args, world, dev, w, inp, gate, bf16, elems)
 
-            def e2e_call():
-                d = [t.to(dev, non_blocking=True) for t in host]
-                yd = ss.selscan_fwd(*d, True, zoh=True)
-                y_host.copy_(yd, non_blocking=True)
-                torch.cuda.current_stream().synchronize()
-        elif w.gated:
-            # The gated form takes device tensors: copy the step's inputs in,
-            # run it, copy y out, synchronise.
-            host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
-            host = [t.pin_memory() for t in host]
-
-            def e2e_call():
-                d = [t.to(dev, non_blocking=True) for t in host]
-                yd = ss.selscan_fwd(*d[:5], True, D_skip=d[6], z=d[5])
-                y_host.copy_(yd, non_blocking=True)
-                torch.cuda.current_stream().synchronize()
-        else:
-            host = [t.pin_memory() for t in host]
-
-            def e2e_call():
-                ss.selscan_fwd(*host, True, y=y_host)  # H2D, kernels, D2H, synchronise
-        e2e_call()                                       # warm the copy path
-        barrier(world, dev)
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_call()
-        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in host)
-        e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
+    per_config = None
+    if args.workload == DEFAULT_WORKLOAD and not args.no_per_config:
+        per_config = {}
+        for wid in PER_CONFIG:
+            per_config[str(wid)] = measure_config(wid, args, world, local, dev, alu)
+            torch.cuda.empty_cache()
 
     if world > 1:
         import torch.distributed as dist
@@ -463,9 +529,8 @@ def run_gpu(args, world, rank, local):
 
     hbm_gbs, max_mhz, src = read_measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pk = peaks(sms, max_mhz, hbm_gbs)
-    pk["source"] = f"HBM {src}; MUFU/FP32 derived: {sms} SMs x (32 ex2, 128 fp32)/clk x {max_mhz:.0f} MHz"
-    work = work_counts(Bsz, L, D, N, es, softplus=True, hT=want_hT, gated=w.gated, zoh=w.zoh)
+    pk = peaks(sms, max_mhz, hbm_gbs, alu)
+    pk["source"] = peak_source(src, alu, sms, max_mhz)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel=f"selscan_fwd call ({plan['launches']} launches, {plan['chunks']} chunks)")
 
@@ -476,22 +541,99 @@ def run_gpu(args, world, rank, local):
         cpu = {"value": n_el / secs, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": ("the whole workload" if chains is None else f"{len(chains)} of {Bsz * D} chains over all L")
                + f" ({n_el} elements, {secs:.2f} s, fp64)"}
-
-    config = {"workload": f"{w.name}: Bsz={Bsz} L={L} D={D} N={N} {w.dtype}, softplus on"
-                          + (", returns hT" if want_hT else "")
-                          + (", skip and SiLU gate fused (y = (scan + Dskip x) silu(z))" if w.gated else "")
-                          + (", zero-order-hold Bbar" if w.zoh else ""),
-              "global_batch": Bsz * world, "seq_len": L, "parallelism": f"replicas x{world}",
-              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2 ({l2 / 1e6:.0f} MB)"
-                    if copies > 1 else f"inputs {foot / 1e6:.0f} MB > 2x L2",
-              "plan": plan}
-    return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+    line = result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
-                       launches=plan["launches"] * args.steps, clocks=clk.summary(),
+                       launches=plan["launches"] * args.steps, clocks=clocks,
                        dtype="bf16 io, f32 math" if bf16 else "f32")
+    if per_config is not None:
+        line["per_config"] = per_config
+    return line
 
 
-def run_conv(args, world, rank, local, dev, w):
+def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
+    """End to end through the public API: the step's inputs copied in from
+    pinned host memory, the scan, y copied out, inside the timed region."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    host = [torch.from_numpy(inp.x.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.x),
+            torch.from_numpy(inp.delta.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.delta),
+            torch.from_numpy(inp.A),
+            torch.from_numpy(inp.B.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.B),
+            torch.from_numpy(inp.C.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.C)]
+    y_host = torch.empty(tuple(inp.x.shape), dtype=torch.bfloat16 if bf16 else torch.float32, pin_memory=True)
+    hT_host = torch.empty(inp.x.shape[0], inp.x.shape[2], inp.A.shape[1], pin_memory=True) \
+        if w.return_state else None
+    e2e_steps = max(1, min(args.steps, 20 if elems < 50_000_000 else 5))
+    if w.zoh:
+        host = [t.pin_memory() for t in host]
+
+        def e2e_call():
+            d = [t.to(dev, non_blocking=True) for t in host]
+            yd = ss.selscan_fwd(*d, True, zoh=True)
+            y_host.copy_(yd, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+    elif w.gated:
+        # The gated form takes device tensors: copy the step's inputs in,
+        # run it, copy y out, synchronise.
+        host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
+        host = [t.pin_memory() for t in host]
+
+        def e2e_call():
+            d = [t.to(dev, non_blocking=True) for t in host]
+            yd = ss.selscan_fwd(*d[:5], True, D_skip=d[6], z=d[5])
+            y_host.copy_(yd, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+    else:
+        host = [t.pin_memory() for t in host]
+
+        def e2e_call():
+            ss.selscan_fwd(*host, True, y=y_host, hT=hT_host)  # H2D, kernels, D2H, synchronise
+    e2e_call()                                       # warm the copy path
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_call()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = y_host.numel() * y_host.element_size() + (hT_host.numel() * 4 if hT_host is not None else 0)
+    return {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def measure_config(wid, args, world, local, dev, alu):
+    """A shorter measurement of another workload for ``per_config``: per-step
+    time, throughput and roofline fractions (no end-to-end or CPU legs)."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+    w = W.WORKLOADS[wid]
+    steps = max(1, min(args.steps, 50))
+    warmup = max(3, min(args.warmup, 10))
+    hbm_gbs, max_mhz, src = read_measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pk = peaks(sms, max_mhz, hbm_gbs, alu)
+    if w.steps:
+        per_step, clocks, note = decode_time(w, steps, warmup, world, dev, local)
+        work = step_work_counts(w.Bsz, w.D, w.N)
+        name = f"{w.name}: Bsz={w.Bsz} D={w.D} N={w.N} f32 decode step, state updated in place ({note})"
+        elems = w.Bsz * w.D
+    else:
+        fb = _FwdBench(wid, dev)
+        sec, clocks = timed_steps(fb.step, steps, warmup, world, dev, local)
+        per_step = sec / steps
+        work = fb.work()
+        plan = ss.fwd_plan(fb.Bsz, fb.L, fb.D, fb.N, bf16=fb.bf16)
+        name = fb.workload_name() + f" ({plan['chunks']} chunks; {fb.l2_note()})"
+        elems = fb.Bsz * fb.L * fb.D
+        del fb
+    roof = roofline(work, pk, per_step)
+    return {"workload": name, "ms_per_step": per_step * 1e3, "value": world * elems / per_step, "unit": UNIT,
+            "frac": roof["frac"], "frac_strict": roof["frac_strict"], "bound": roof["bound"],
+            "hbm_gbs": roof["hbm_gbs"], "t_roof_us": roof["t_roof_us"], "steps": steps, "warmup": warmup,
+            "clocks": clocks}
+
+
+def run_conv(args, world, rank, local, dev, w, alu=None):
     """The conv1d workload: one step = one selscan_conv1d (K taps, SiLU) over
     (Bsz, L, D), a carried state handed in and out. Input sets rotate past
     2x L2. HBM-bound: x read and out written once."""
@@ -574,8 +716,8 @@ def run_conv(args, world, rank, local, dev, w):
 
     hbm_gbs, max_mhz, src = read_measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pk = peaks(sms, max_mhz, hbm_gbs)
-    pk["source"] = f"HBM {src}"
+    pk = peaks(sms, max_mhz, hbm_gbs, alu)
+    pk["source"] = peak_source(src, alu, sms, max_mhz)
     nbytes = 2 * elems * es + w.D * (K + 1) * 4 + 2 * w.Bsz * w.D * (K - 1) * 4
     work = {"elems": elems, "updates": elems * K, "bytes": nbytes, "mufu": 2 * elems, "fp32": (K + 2) * elems}
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload), kernel="selscan_conv1d (1 launch)")
@@ -597,7 +739,7 @@ def run_conv(args, world, rank, local, dev, w):
                        launches=args.steps, clocks=clk.summary(), dtype="f32")
 
 
-def run_bwd(args, world, rank, local, dev, w):
+def run_bwd(args, world, rank, local, dev, w, alu=None):
     """The backward workload: one step = one selscan_bwd over (Bsz, L, D, N)
     with softplus on and upstream gradient dy (no dhT). Input sets rotate past
     2x L2."""
@@ -664,8 +806,8 @@ def run_bwd(args, world, rank, local, dev, w):
 
     hbm_gbs, max_mhz, src = read_measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pk = peaks(sms, max_mhz, hbm_gbs)
-    pk["source"] = f"HBM {src}; MUFU {MUFU_EX2_PER_CLK_SM}/clk/SM and FP32 {FP32_PER_CLK_SM}/clk/SM at {max_mhz:.0f} MHz"
+    pk = peaks(sms, max_mhz, hbm_gbs, alu)
+    pk["source"] = peak_source(src, alu, sms, max_mhz)
     work = bwd_work_counts(w.Bsz, w.L, w.D, w.N)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel="scan_bwd_kernel (1 launch + 3 memsets)")
@@ -686,14 +828,14 @@ def run_bwd(args, world, rank, local, dev, w):
                        launches=args.steps, clocks=clk.summary(), dtype="f32")
 
 
-def run_decode(args, world, rank, local, dev, w):
-    """The decode workload: one step = one selscan_step over (Bsz, D, N).
-    Eight independent decode streams (state and per-step inputs each) are
-    rotated so that every step reads its 42 MB state from HBM rather than L2,
-    as a server interleaving several sequences would. The steps are captured
-    in CUDA graphs and the timed steps replay them, as a decode loop launches
-    a fixed step sequence; the same steps launched one Python call at a time
-    are timed too and reported beside it."""
+def decode_time(w, steps, warmup, world, dev, local, eager=True):
+    """Times K decode steps. Eight independent decode streams (state and
+    per-step inputs each) are rotated so that every step reads its 42 MB
+    state from HBM rather than L2, as a server interleaving several sequences
+    would. The steps are captured in CUDA graphs and the timed steps replay
+    them, as a decode loop launches a fixed step sequence. Returns (seconds
+    per step, clock summary, a note with the launch form and, when ``eager``,
+    the time of the same steps launched one Python call at a time)."""
     import torch
     import selective_state_space_157_b300 as ss
     from selective_state_space_157_b300 import workloads as W
@@ -708,7 +850,7 @@ def run_decode(args, world, rank, local, dev, w):
         x, dl, B, C = inputs[i % streams]
         ss.selscan_step(states[i % streams], x, dl, A, B, C, y=ys[i % streams])
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     ss.check_device_error()
@@ -729,37 +871,38 @@ def run_decode(args, world, rank, local, dev, w):
         return g
 
     full = capture(per_graph)
-    rest = capture(args.steps % per_graph) if args.steps % per_graph else None
+    rest = capture(steps % per_graph) if steps % per_graph else None
     stream.wait_stream(side)
-    for _ in range(max(1, args.warmup // per_graph)):
+    for _ in range(max(1, warmup // per_graph)):
         full.replay()
     torch.cuda.synchronize()
 
     def replay_all(_):
-        for _ in range(args.steps // per_graph):
+        for _ in range(steps // per_graph):
             full.replay()
         if rest is not None:
             rest.replay()
 
-    def timed(run, calls):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world, dev)
-        torch.cuda.synchronize()
-        with ClockSampler(local) as clk:
-            e0.record(stream)
-            for i in range(calls):
-                run(i)
-            e1.record(stream)
-            torch.cuda.synchronize()
-        barrier(world, dev)
-        ss.check_device_error()
-        return max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev), clk
+    note = f"CUDA graph replay of {per_graph} captured selscan_step calls (the {streams} decode streams in turn)"
+    if eager:
+        sec_eager, _ = timed_steps(step, steps, 0, world, dev, local)
+        note += f"; one Python call per step: {sec_eager / steps * 1e6:.1f} us per step"
+    sec, clocks = timed_steps(replay_all, 1, 0, world, dev, local)
+    decode_time.state = (A, states, ys)
+    return sec / steps, clocks, note
 
-    sec_eager, _ = timed(step, args.steps)
-    sec, clk = timed(replay_all, 1)
-    per_step = sec / args.steps
+
+def run_decode(args, world, rank, local, dev, w, alu=None):
+    """The decode workload: one step = one selscan_step over (Bsz, D, N),
+    graph-replayed over eight rotating decode streams (decode_time)."""
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+
+    per_step, clocks, note = decode_time(w, args.steps, args.warmup, world, dev, local)
+    A, states, ys = decode_time.state
     elems = w.Bsz * w.D
-    value = world * elems * args.steps / sec
+    value = world * elems / per_step
 
     # end to end: host inputs of the step in, y out, state kept on the device
     hx = [torch.from_numpy(a).pin_memory() for a in W.decode_step_inputs(w, 0)]
@@ -784,8 +927,8 @@ def run_decode(args, world, rank, local, dev, w):
 
     hbm_gbs, max_mhz, src = read_measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pk = peaks(sms, max_mhz, hbm_gbs)
-    pk["source"] = f"HBM {src}"
+    pk = peaks(sms, max_mhz, hbm_gbs, alu)
+    pk["source"] = peak_source(src, alu, sms, max_mhz)
     roof = roofline(step_work_counts(w.Bsz, w.D, w.N), pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel="selscan_step (1 launch)")
     cpu = None
@@ -805,12 +948,11 @@ def run_decode(args, world, rank, local, dev, w):
                "sample": f"{len(chains)} of {w.Bsz * w.D} chains x {steps_h} steps ({secs:.2f} s, fp64, one thread)"}
     config = {"workload": f"{w.name}: Bsz={w.Bsz} D={w.D} N={w.N} f32 decode step, state updated in place",
               "global_batch": w.Bsz * world, "seq_len": 1, "parallelism": f"replicas x{world}",
-              "l2": f"{streams} rotating decode streams ({streams * w.Bsz * w.D * w.N * 4 / 1e6:.0f} MB of state) > 2x L2",
-              "launch": f"CUDA graph replay of {per_graph} captured selscan_step calls (the {streams} decode streams in turn); "
-                        f"one Python call per step: {sec_eager / args.steps * 1e6:.1f} us per step"}
+              "l2": f"8 rotating decode streams ({8 * w.Bsz * w.D * w.N * 4 / 1e6:.0f} MB of state) > 2x L2",
+              "launch": note}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
-                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+                       launches=args.steps, clocks=clocks, dtype="f32")
 
 
 def run_reference(args, world, rank):
@@ -946,9 +1088,10 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per_config measurements")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":

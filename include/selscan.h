@@ -42,7 +42,11 @@
  *    SELSCAN_ERR_UNSUPPORTED nothing was launched and no output was
  *    touched. selscan_last_error() then describes the failure.
  *  - Thread safety: calls may be made concurrently from several host
- *    threads on different streams.
+ *    threads on different streams. A kernel that gives up waiting records
+ *    the failure in a fault word of the stream it ran on, and only
+ *    selscan_check_device_error on that stream reports it (up to 64
+ *    streams per device have words of their own; beyond that, streams
+ *    share one).
  */
 #ifndef SELSCAN_H
 #define SELSCAN_H
@@ -96,11 +100,16 @@ typedef enum {
  *
  * Aliasing: y may equal x or delta exactly (in-place output); h0 may equal
  * hT exactly (resume in place). Any other overlap between y or hT and
- * another argument is SELSCAN_ERR_INVALID_ARG.
+ * another argument is SELSCAN_ERR_INVALID_ARG. When the sequence is cut
+ * into chunks, in-place output makes the readout of each chunk wait until
+ * that chunk's reduction has read its inputs, and in-place resume writes
+ * the final state to the workspace first and copies it to hT after the
+ * scan.
  *
  * Memory: long sequences use a small library-owned workspace for the chunk
  * carries ((ceil(L / chunk) - 1) * Bsz * D * (N + 1) fp32 plus one flag per
- * chunk and channel tile), taken from a
+ * chunk and channel tile, plus Bsz * D * N fp32 for in-place resume), taken
+ * from a
  * private stream-ordered pool on `stream` and returned to it before the
  * call's work completes; selscan_release_workspace() gives the pool's
  * memory back to the device. SELSCAN_ERR_NO_MEMORY if it cannot be had.
@@ -351,19 +360,24 @@ const char *selscan_last_error(void);
  * SELSCAN_OK; SELSCAN_ERR_CUDA with the CUDA error in selscan_last_error();
  * or SELSCAN_ERR_TIMEOUT when a kernel stopped waiting for an input tile
  * (fault code 1) or for the carry of an earlier chunk (fault code 2) that
- * never came. Every wait inside the kernels is bounded (2 s), so a broken
- * pipeline ends with this status instead of a hang, and the context stays
- * usable. The fault word is per device and is cleared by this call.
- *
- * Testing the timeout path. Two environment variables, read at each
- * selscan_fwd call, exist only so that tests can make a wait run out
- * without any fault: SELSCAN_TEST_WITHHOLD_CARRIES=1 makes the chunked
- * path's reduction items withhold their completion flags, so every readout
- * of a later chunk waits for a flag that nothing sets; and
- * SELSCAN_TEST_WAIT_LIMIT_MS (1..2000) shortens the wait. The call then
- * ends early with invalid outputs, and selscan_check_device_error returns
- * SELSCAN_ERR_TIMEOUT (fault code 2). */
+ * never came. Every wait inside the kernels is bounded (2 s of GPU time,
+ * which keeps counting while the context is time-sliced out on a shared
+ * GPU), so a broken pipeline ends with this status instead of a hang, and
+ * the context stays usable. A call that timed out left its outputs
+ * invalid. Each stream has its own fault word (see "Thread safety"); this
+ * call reads and clears the word of `stream` only. */
 int selscan_check_device_error(void *stream);
+
+/* Test hook for the timeout path: makes a wait run out without any fault.
+ * With withhold_carries = 1, the reduction items of later chunked forward
+ * calls in this process raise no completion flags, so every readout of a
+ * later chunk waits for a flag that nothing sets; wait_limit_ms (1..2000)
+ * shortens that wait (0 = the default 2 s). Such calls end early with
+ * invalid outputs, and selscan_check_device_error on their stream returns
+ * SELSCAN_ERR_TIMEOUT (fault code 2). selscan_test_fault_injection(0, 0)
+ * restores normal operation. Off by default; nothing in the environment can
+ * turn it on. SELSCAN_ERR_INVALID_ARG for arguments out of range. */
+int selscan_test_fault_injection(int withhold_carries, int wait_limit_ms);
 
 /* Returns the memory held by the chunk-carry workspace pools of every
  * device this process used to the device. Safe to call at any time; work

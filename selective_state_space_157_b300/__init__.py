@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
+        L.selscan_test_fault_injection.restype = INT
+        L.selscan_test_fault_injection.argtypes = [INT, INT]
         L.selscan_bwd.restype = INT
         L.selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, P]
         _lib = L

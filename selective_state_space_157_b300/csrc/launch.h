@@ -1,0 +1,48 @@
+// launch.h -- what the kernel translation units export to the host code in
+// selscan.cu: the forward kernels' launch descriptions and the launchers of
+// the plain-load forward, the decode step and the convolution. Each kernel
+// family is compiled in its own translation unit (fwd_fused_f32.cu,
+// fwd_fused_bf16.cu, fwd_plain.cu, step.cu, conv1d.cu) so the library builds
+// in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "conv1d.cuh"
+#include "scan_fused.cuh"
+#include "scan_step.cuh"
+
+namespace selscan {
+
+// The persistent forward kernel chosen for a problem: launched by the host
+// with cudaLaunchKernel(kernel, grid, kScanThreads, {&FusedArgs}, smem).
+struct FusedLaunch {
+    const void *kernel;
+    size_t smem;        // dynamic shared memory per CTA
+    int ctas_per_sm;    // resident CTAs per SM at that shared-memory size
+    int tt, stages;     // timesteps per pipeline stage, ring buffers
+};
+
+// False when no fused variant fits (the caller then takes the plain path).
+bool pick_fused_f32(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, int stages,
+                    FusedLaunch *out);
+bool pick_fused_bf16(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, int stages,
+                     FusedLaunch *out);
+
+// Plain-load forward: aggregate, carry and readout launches (K > 1), or one
+// readout launch. a.chunk, a.K, a.dtiles and, for K > 1, a.agg_h / a.agg_s
+// are set by the caller. Returns a selscan_status.
+int launch_plain_kernels(const ScanArgs &a, int ns, int nsplit, bool vec, int dtype, cudaStream_t st);
+
+// Decode step: G lanes per chain with V 16-byte groups each (vec), or one
+// thread per chain.
+int launch_step_kernel(const StepArgs &a, int G, int V, bool vec, bool zoh, cudaStream_t st);
+
+// Causal depthwise convolution (+ SiLU) over a sequence, and its decode step.
+int launch_conv1d_kernel(const ConvArgs &a, int64_t K, int dtype, bool vec, cudaStream_t st);
+int launch_conv1d_step_kernel(const ConvStepArgs &a, int64_t K, cudaStream_t st);
+
+} // namespace selscan

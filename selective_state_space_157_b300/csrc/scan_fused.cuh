@@ -44,8 +44,10 @@ struct FusedArgs {
     float *aggS;          // (K-1, Bsz, D): sum of dl over the chunk
     float *aggH;          // (K-1, Bsz, D, N): chunk end state from zero
     unsigned *ctrl;       // [0]: ticket counter; [1 + k*G + g]: aggregate done flags (zeroed per call)
+    unsigned *fault;      // fault word of the launching stream
     uint64_t wait_ns;     // limit of a readout's wait for the done flags
     int publish;          // 0 only for the timeout test: aggregates raise no flags
+    int alias_wait;       // y is x, delta or z: readout k also waits for aggregate k, which reads those rows
     int stages;
     int groups;           // G
     int items_agg;        // (K-1) * G
@@ -261,21 +263,25 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             for (int j = 0; j < NP; ++j)
                 h[j] = make_float2(0.0f, 0.0f);
         }
-        if (readout && k > 0) {
-            // Warp 0 checks the done flags of chunks 0..k-1, 32 per round trip.
+        // Flags a readout waits for: chunks 0..k-1 (their pairs are folded),
+        // and chunk k as well when y overwrites an input that chunk k's
+        // aggregate item reads (in-place output).
+        const int kwait = readout ? (fa.alias_wait ? min(k + 1, a.K - 1) : k) : 0;
+        if (kwait > 0) {
+            // Warp 0 checks the done flags, 32 per round trip.
             if (threadIdx.x < 32) {
                 const uint64_t tstart = global_ns();
-                for (int j0 = 0; j0 < k; j0 += 32) {
+                for (int j0 = 0; j0 < kwait; j0 += 32) {
                     const int j = j0 + lane;
                     const unsigned *f = fa.ctrl + 1 + (int64_t)j * fa.groups + g;
-                    bool done = j >= k || ld_acquire_u32(f) != 0u;
+                    bool done = j >= kwait || ld_acquire_u32(f) != 0u;
                     while (!__all_sync(0xffffffffu, done)) {
                         if (!done)
                             done = ld_acquire_u32(f) != 0u;
                         // Warp-uniform decision: every lane leaves together.
                         if (__any_sync(0xffffffffu, global_ns() - tstart > fa.wait_ns)) {
                             if (lane == 0) {
-                                record_fault(kFaultFlagTimeout);
+                                record_fault(fa.fault, kFaultFlagTimeout);
                                 *s_abort = 1;
                             }
                             break;
@@ -289,6 +295,8 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             __syncthreads();
             if (*s_abort)
                 break;
+        }
+        if (readout && k > 0) {
             // Fold the pairs of chunks 0..k-1, kFoldBatch at a time: all loads
             // of a batch are issued before the first is used. A chunk's decay
             // exp(A * sum dl) is rebuilt here from its sum of dl, exactly as the
@@ -585,7 +593,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     // A tile or an aggregate that never arrived: let this CTA's copies in
     // flight land (bounded) before its shared memory goes away.
     if (*s_abort && threadIdx.x == 0) {
-        record_fault(kFaultTmaTimeout);
+        record_fault(fa.fault, kFaultTmaTimeout);
         for (int s = 0; s < STAGES; ++s)
             if (issued[s] > 0)
                 mbar_wait(&full[s], (issued[s] - 1) & 1u);

@@ -199,35 +199,4 @@ scan_chunk_kernel(const ScanArgs a)
     }
 }
 
-// Step 2: compose chunk pairs in order. One thread per (b, d, n); the K-1
-// aggregates are replaced in place by the incoming states of chunks 1..K-1.
-struct CarryArgs {
-    const float *A;
-    const float *h0;   // (Bsz, D, N) or null
-    float *agg_h;      // (K-1, Bsz, D, N) in: end states from zero; out: incoming states
-    const float *agg_s;
-    int64_t Bsz, D, N;
-    int K;
-};
-
-__global__ void __launch_bounds__(256) scan_carry_kernel(const CarryArgs a)
-{
-    const int64_t total = a.Bsz * a.D * a.N;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= total)
-        return;
-    const int64_t bd = i / a.N;
-    const int64_t n = i - bd * a.N;
-    const int64_t d = bd % a.D;
-    const float A2 = __ldg(a.A + d * a.N + n) * kLog2e;
-    float c = a.h0 ? a.h0[i] : 0.0f;
-    const int64_t bdn = total, bdsz = a.Bsz * a.D;
-    for (int k = 0; k + 1 < a.K; ++k) {
-        const float decay = ex2(A2 * a.agg_s[(int64_t)k * bdsz + bd]);
-        float *slot = a.agg_h + (int64_t)k * bdn + i;
-        c = fmaf(decay, c, *slot);   // (decay, end) o carry
-        *slot = c;                   // incoming state of chunk k+1
-    }
-}
-
 } // namespace selscan

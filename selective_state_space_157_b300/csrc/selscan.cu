@@ -15,14 +15,10 @@
 #include <cstring>
 #include <mutex>
 
-#include "conv1d.cuh"
-#include "scan_fwd.cuh"
-#include "scan_step.cuh"
-#include "scan_fused.cuh"
-#include "scan_tma.cuh"
+#include "host_common.h"
+#include "launch.h"
 
 namespace selscan {
-namespace {
 
 thread_local char g_err[512];
 
@@ -40,39 +36,6 @@ int cuda_fail(cudaError_t e, const char *what)
     return fail(SELSCAN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-// ---- argument checks ------------------------------------------------------
-
-constexpr int64_t kMaxElems = int64_t(1) << 60;
-
-bool mul_ok(int64_t a, int64_t b, int64_t c, int64_t *out)
-{
-    if (a == 0 || b == 0 || c == 0) { *out = 0; return true; }
-    if (a > kMaxElems / b) return false;
-    int64_t ab = a * b;
-    if (ab > kMaxElems / c) return false;
-    *out = ab * c;
-    return true;
-}
-
-struct Range {
-    uintptr_t lo, hi;   // [lo, hi)
-    const char *name;
-};
-
-Range range(const void *p, int64_t bytes, const char *name)
-{
-    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-    return Range{lo, p ? lo + (uintptr_t)bytes : lo, name};
-}
-
-bool overlaps(const Range &a, const Range &b)
-{
-    if (a.lo == a.hi || b.lo == b.hi) return false;
-    return a.lo < b.hi && b.lo < a.hi;
-}
-
-bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
-
 long env_long(const char *name, long dflt)
 {
     const char *s = getenv(name);
@@ -84,10 +47,11 @@ long env_long(const char *name, long dflt)
 
 // ---- per-device state -----------------------------------------------------
 
-constexpr int kMaxDevices = 64;
+namespace {
 std::mutex g_mu;
 cudaMemPool_t g_pool[kMaxDevices];
 int g_sms[kMaxDevices];
+} // namespace
 
 int device_info(int *dev, int *sms)
 {
@@ -125,43 +89,57 @@ int workspace_pool(int dev, cudaMemPool_t *pool)
     return SELSCAN_OK;
 }
 
-// ---- forward dispatch -----------------------------------------------------
+// ---- fault words ----------------------------------------------------------
+// Kernels that wait (on a TMA tile or a chunk carry) give up after a time
+// limit and record a code in a fault word. Each stream gets its own word, so
+// selscan_check_device_error reports a timeout to checks on the stream the
+// kernel ran on, and to no other.
 
-using ScanKernel = void (*)(ScanArgs);
+constexpr int kFaultSlots = 64;
+static __device__ unsigned g_fault_slots[kFaultSlots];
 
-struct ScanKernels {
-    ScanKernel readout, aggregate;
+namespace {
+struct FaultTable {
+    unsigned *base = nullptr;   // device address of g_fault_slots on this device
+    cudaStream_t streams[kFaultSlots];
+    int used = 0;
 };
+FaultTable g_faults[kMaxDevices];
+std::mutex g_fault_mu;
+} // namespace
 
-template <typename T, int NS, int NSPLIT>
-ScanKernels pick_vec(bool vec)
+int fault_word(int dev, cudaStream_t st, unsigned **out)
 {
-    if (vec)
-        return {scan_chunk_kernel<T, NS, NSPLIT, true, true>, scan_chunk_kernel<T, NS, NSPLIT, false, true>};
-    return {scan_chunk_kernel<T, NS, NSPLIT, true, false>, scan_chunk_kernel<T, NS, NSPLIT, false, false>};
-}
-
-template <typename T>
-bool pick_shape(int ns, int nsplit, bool vec, ScanKernels *out)
-{
-    switch (ns * 100 + nsplit) {
-    case 401: *out = pick_vec<T, 4, 1>(vec); return true;
-    case 801: *out = pick_vec<T, 8, 1>(vec); return true;
-    case 1601: *out = pick_vec<T, 16, 1>(vec); return true;
-    case 402: *out = pick_vec<T, 4, 2>(vec); return true;
-    case 802: *out = pick_vec<T, 8, 2>(vec); return true;
-    case 1602: *out = pick_vec<T, 16, 2>(vec); return true;
-    case 404: *out = pick_vec<T, 4, 4>(vec); return true;
-    case 804: *out = pick_vec<T, 8, 4>(vec); return true;
-    case 1604: *out = pick_vec<T, 16, 4>(vec); return true;
-    default: return false;
+    std::lock_guard<std::mutex> lk(g_fault_mu);
+    FaultTable &t = g_faults[dev];
+    if (!t.base) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_fault_slots);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fault words");
+        t.base = static_cast<unsigned *>(p);
     }
+    int i = 0;
+    while (i < t.used && t.streams[i] != st) ++i;
+    if (i == t.used) {
+        if (t.used < kFaultSlots) t.streams[t.used++] = st;
+        else i = kFaultSlots - 1;   // beyond kFaultSlots streams, one shared word
+    }
+    *out = t.base + i;
+    return SELSCAN_OK;
 }
 
-// ---- TMA path -----------------------------------------------------------
+namespace {
 
-constexpr int kTT = 16;       // timesteps per pipeline stage (default)
-// Buffers in flight per CTA (default). Two measured fastest on B300 (Bsz=2,
+// ---- fault injection for the failure-detection test -------------------------
+// Off unless selscan_test_fault_injection turns it on; nothing in the
+// environment can enable it.
+std::mutex g_test_mu;
+int g_test_withhold = 0;      // aggregates raise no done flags
+long g_test_wait_ms = 0;      // readouts' wait limit (0: the default)
+
+// ---- forward planning ---------------------------------------------------
+
+// Default buffers in flight per CTA. Two measured fastest on B300 (Bsz=2,
 // L=2048, D=1536: 72 us against 79 us with four); no workload measured slower.
 constexpr int kStages = 2;
 
@@ -199,91 +177,6 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, size_t es, const void *ba
     return r == CUDA_SUCCESS;
 }
 
-using FusedKernel = void (*)(FusedArgs);
-
-struct FusedLaunch {
-    FusedKernel kernel;
-    size_t smem;
-    int ctas_per_sm;
-    int tt, stages;
-};
-
-// Resident CTAs per SM for a kernel at a shared-memory size (cached).
-int occupancy(const void *fn, size_t smem)
-{
-    struct Entry { const void *fn; size_t smem; int n; };
-    static std::mutex mu;
-    static Entry cache[64];
-    static int used = 0;
-    std::lock_guard<std::mutex> lk(mu);
-    for (int i = 0; i < used; ++i)
-        if (cache[i].fn == fn && cache[i].smem == smem) return cache[i].n;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kScanThreads, smem) != cudaSuccess) {
-        cudaGetLastError();
-        n = 1;
-    }
-    if (n < 1) n = 1;
-    if (used < 64) cache[used++] = Entry{fn, smem, n};
-    return n;
-}
-
-template <typename T, int NS, int NSPLIT, bool VEC, bool SP, bool GATE = false, bool ZOH = false>
-bool prepare_fused_sp(int64_t N, FusedLaunch *out)
-{
-    constexpr int DPB = kScanThreads / NSPLIT;
-    long stages = env_long("SELSCAN_TMA_STAGES", kStages);
-    if (stages < 2) stages = 2;
-    if (stages > kMaxStages) stages = kMaxStages;
-    auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP, GATE, ZOH>;
-    const int64_t nrow = VEC ? NS * NSPLIT : N;
-    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, (int)stages, GATE);
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    *out = FusedLaunch{k, smem, occupancy(reinterpret_cast<const void *>(k), smem), kTT, (int)stages};
-    return true;
-}
-
-// The block's skip and gate run fused on the vectorised, softplus form (the
-// block's own use); other gated forms take the plain-load path. So does the
-// zero-order hold, for one thread per chain (N <= 16).
-template <typename T, int NS, int NSPLIT>
-bool prepare_fused(bool vec, bool softplus, bool gate, bool zoh, int64_t N, FusedLaunch *out)
-{
-    if (zoh) {
-        if constexpr (NSPLIT == 1) {
-            if (!(vec && softplus)) return false;
-            return gate ? prepare_fused_sp<T, NS, NSPLIT, true, true, true, true>(N, out)
-                        : prepare_fused_sp<T, NS, NSPLIT, true, true, false, true>(N, out);
-        }
-        return false;
-    }
-    if (gate)
-        return vec && softplus && prepare_fused_sp<T, NS, NSPLIT, true, true, true>(N, out);
-    if (vec)
-        return softplus ? prepare_fused_sp<T, NS, NSPLIT, true, true>(N, out)
-                        : prepare_fused_sp<T, NS, NSPLIT, true, false>(N, out);
-    return softplus ? prepare_fused_sp<T, NS, NSPLIT, false, true>(N, out)
-                    : prepare_fused_sp<T, NS, NSPLIT, false, false>(N, out);
-}
-
-template <typename T>
-bool pick_fused(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, FusedLaunch *out)
-{
-    switch (ns * 100 + nsplit) {
-    case 401: return prepare_fused<T, 4, 1>(vec, softplus, gate, zoh, N, out);
-    case 801: return prepare_fused<T, 8, 1>(vec, softplus, gate, zoh, N, out);
-    case 1601: return prepare_fused<T, 16, 1>(vec, softplus, gate, zoh, N, out);
-    case 1602: return prepare_fused<T, 16, 2>(vec, softplus, gate, zoh, N, out);
-    case 1604: return prepare_fused<T, 16, 4>(vec, softplus, gate, zoh, N, out);
-    case 802: return prepare_fused<T, 8, 2>(vec, softplus, gate, zoh, N, out);
-    case 404: return prepare_fused<T, 4, 4>(vec, softplus, gate, zoh, N, out);
-    default: return false;
-    }
-}
-
 struct FwdPlan {
     int ns, nsplit;
     bool vec;
@@ -291,13 +184,14 @@ struct FwdPlan {
     int64_t chunk;
     int K;
     int dtiles;
+    bool stage_hT;   // hT is h0 and K > 1: the final state goes to the workspace, then to hT
 };
 
 // States per thread and threads per chain: the smallest NS in {4, 8, 16}
 // covering N / NSPLIT. NSPLIT is 1 up to N = 16 (2 and 4 beyond), unless
 // SELSCAN_NSPLIT asks for more threads per chain.
 void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const void *x, const void *delta,
-              const void *B, const void *C, int sms, FwdPlan *p)
+              const void *B, const void *C, const float *h0, const float *hT, int sms, FwdPlan *p)
 {
     int nsplit = N <= 16 ? 1 : (N <= 32 ? 2 : 4);
     long want = env_long("SELSCAN_NSPLIT", 0);
@@ -352,53 +246,50 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     if (chunk < min_for_grid) chunk = min_for_grid;
     p->chunk = chunk;
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
+    // Readouts of every chunk load h0 when they start, and the last chunk's
+    // readouts write hT when they end: in place, that would race.
+    p->stage_hT = hT != nullptr && hT == h0 && p->K > 1;
 }
 
-// Chunk-carry workspace of a plan: per chunk boundary and chain the end
-// state (N floats) and the sum of dl (1 float), then the ticket counter and
-// one done flag per aggregate item (the plain-load path uses no flags).
+// Workspace of a plan, in this order: per chunk boundary and chain the end
+// state (N floats) and the sum of dl (1 float); the ticket counter and one
+// done flag per aggregate item (the plain-load path uses no flags); then,
+// for in-place resume, the staged final state (Bsz * D * N floats).
+struct WsLayout {
+    size_t pairs, flags, stage, total;
+};
+
+WsLayout fwd_workspace_layout(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
+{
+    WsLayout w{0, 0, 0, 0};
+    if (plan.K > 1) {
+        w.pairs = (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float);
+        w.flags = (1 + (size_t)(plan.K - 1) * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
+    }
+    if (plan.stage_hT) w.stage = (size_t)(Bsz * D * N) * sizeof(float);
+    w.total = w.pairs + ((w.flags + 15) & ~(size_t)15) + w.stage;
+    return w;
+}
+
 size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
 {
-    if (plan.K <= 1) return 0;
-    const size_t pairs = (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float);
-    const size_t flags = (1 + (size_t)(plan.K - 1) * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
-    return pairs + flags;
-}
-
-int launch_plain(const ScanArgs &base, const FwdPlan &plan, int dtype, float *ws, cudaStream_t st)
-{
-    ScanKernels ks{};
-    bool ok = dtype == SELSCAN_F32 ? pick_shape<float>(plan.ns, plan.nsplit, plan.vec, &ks)
-                                   : pick_shape<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, &ks);
-    if (!ok) return fail(SELSCAN_ERR_UNSUPPORTED, "no kernel for NS=%d NSPLIT=%d", plan.ns, plan.nsplit);
-    ScanArgs a = base;
-    const int64_t gx = a.Bsz * plan.dtiles;
-    if (plan.K > 1) {
-        const int64_t bd = a.Bsz * a.D;
-        a.agg_h = ws;
-        a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
-        ks.aggregate<<<dim3((unsigned)gx, (unsigned)(plan.K - 1)), kScanThreads, 0, st>>>(a);
-        CarryArgs c{a.A, a.h0, a.agg_h, a.agg_s, a.Bsz, a.D, a.N, plan.K};
-        const int64_t total = a.Bsz * a.D * a.N;
-        scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(c);
-    }
-    ks.readout<<<dim3((unsigned)gx, (unsigned)plan.K), kScanThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+    return fwd_workspace_layout(plan, Bsz, D, N).total;
 }
 
 // TMA path: one persistent kernel (aggregates, carries and readout together).
 // Returns SELSCAN_ERR_UNSUPPORTED when TMA cannot be set up (the caller then
 // takes the plain path); nothing has been enqueued in that case.
-int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, float *ws, cudaStream_t st)
+int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, float *ws, unsigned *fault,
+                 cudaStream_t st)
 {
     FusedLaunch fl;
     const bool sp = a.softplus != 0;
     const bool gate = a.Dskip != nullptr || a.z != nullptr;
     if (a.z && !aligned(a.z, 16)) return SELSCAN_ERR_UNSUPPORTED;
     const bool zoh = a.zoh != 0;
-    bool ok = dtype == SELSCAN_F32 ? pick_fused<float>(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, &fl)
-                                   : pick_fused<__nv_bfloat16>(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, &fl);
+    const int stages = (int)env_long("SELSCAN_TMA_STAGES", kStages);
+    bool ok = dtype == SELSCAN_F32 ? pick_fused_f32(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, stages, &fl)
+                                   : pick_fused_bf16(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, stages, &fl);
     if (!ok) return SELSCAN_ERR_UNSUPPORTED;
     FusedArgs fa;
     memset(&fa, 0, sizeof fa);
@@ -414,13 +305,16 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         return SELSCAN_ERR_UNSUPPORTED;
     fa.s = a;
     fa.stages = fl.stages;
-    // Timeout test (documented in selscan.h): aggregates withhold their done
-    // flags and readouts give up after SELSCAN_TEST_WAIT_LIMIT_MS.
-    fa.publish = env_long("SELSCAN_TEST_WITHHOLD_CARRIES", 0) == 0;
-    long limit_ms = env_long("SELSCAN_TEST_WAIT_LIMIT_MS", (long)(kWaitLimitNs / 1000000ull));
-    if (limit_ms < 1) limit_ms = 1;
-    if ((uint64_t)limit_ms > kWaitLimitNs / 1000000ull) limit_ms = (long)(kWaitLimitNs / 1000000ull);
-    fa.wait_ns = (uint64_t)limit_ms * 1000000ull;
+    fa.fault = fault;
+    {
+        std::lock_guard<std::mutex> lk(g_test_mu);
+        fa.publish = g_test_withhold ? 0 : 1;
+        const uint64_t limit_ms = g_test_wait_ms > 0 ? (uint64_t)g_test_wait_ms : kWaitLimitNs / 1000000ull;
+        fa.wait_ns = limit_ms * 1000000ull;
+    }
+    // In-place output: aggregate k reads the rows of x, delta (and z) that
+    // readout k overwrites.
+    fa.alias_wait = (a.y == a.x || a.y == a.delta || (a.z && a.y == a.z)) ? 1 : 0;
     const int64_t groups = a.Bsz * plan.dtiles;
     const int64_t items_agg = (int64_t)(plan.K - 1) * groups;
     const int64_t items_total = items_agg + (int64_t)plan.K * groups;
@@ -430,35 +324,56 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
     fa.items_total = (int)items_total;
     int64_t grid = items_total;
     if (plan.K > 1) {
-        const size_t bdn = (size_t)(a.Bsz * a.D * a.N), bd = (size_t)(a.Bsz * a.D);
+        const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.D, a.N);
+        const size_t bdn = (size_t)(a.Bsz * a.D * a.N);
         fa.aggH = ws;
         fa.aggS = ws + (size_t)(plan.K - 1) * bdn;
-        fa.ctrl = reinterpret_cast<unsigned *>(fa.aggS + (size_t)(plan.K - 1) * bd);
+        fa.ctrl = reinterpret_cast<unsigned *>(reinterpret_cast<unsigned char *>(ws) + w.pairs);
         cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, (size_t)(1 + items_agg) * sizeof(unsigned), st);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk flags");
         const int64_t resident = (int64_t)sms * fl.ctas_per_sm;
         if (grid > resident) grid = resident;
     }
-    fl.kernel<<<(unsigned)grid, kScanThreads, fl.smem, st>>>(fa);
-    cudaError_t e = cudaGetLastError();
+    void *args[] = {&fa};
+    cudaError_t e = cudaLaunchKernel(fl.kernel, dim3((unsigned)grid), dim3(kScanThreads), args, fl.smem, st);
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
-// Enqueues the kernels of one forward call. `ws` holds the chunk-carry
-// workspace (fwd_workspace_bytes of it; unused when the plan has one chunk).
-int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int sms, float *ws, cudaStream_t st)
+// Enqueues the kernels of one forward call. `ws` holds fwd_workspace_bytes
+// of the plan (null when that is 0).
+int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, int sms, float *ws,
+                    cudaStream_t st)
 {
     ScanArgs a = base;
     a.chunk = plan.chunk;
     a.K = plan.K;
     a.dtiles = plan.dtiles;
     if (a.Bsz * plan.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+    const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.D, a.N);
+    float *hT_final = a.hT;
+    if (plan.stage_hT)
+        a.hT = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(ws) + w.total - w.stage);
+    unsigned *fault = nullptr;
+    int rc = fault_word(dev, st, &fault);
+    if (rc != SELSCAN_OK) return rc;
+    rc = SELSCAN_ERR_UNSUPPORTED;
     if (plan.tma) {
-        int rc = launch_fused(a, plan, dtype, sms, ws, st);
-        if (rc != SELSCAN_ERR_UNSUPPORTED) return rc;
-        g_err[0] = '\0';
+        rc = launch_fused(a, plan, dtype, sms, ws, fault, st);
+        if (rc == SELSCAN_ERR_UNSUPPORTED) g_err[0] = '\0';
     }
-    return launch_plain(a, plan, dtype, ws, st);
+    if (rc == SELSCAN_ERR_UNSUPPORTED) {
+        if (plan.K > 1) {
+            const int64_t bd = a.Bsz * a.D;
+            a.agg_h = ws;
+            a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
+        }
+        rc = launch_plain_kernels(a, plan.ns, plan.nsplit, plan.vec, dtype, st);
+    }
+    if (rc == SELSCAN_OK && plan.stage_hT) {
+        const cudaError_t e = cudaMemcpyAsync(hT_final, a.hT, w.stage, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "final state copy");
+    }
+    return rc;
 }
 
 // One forward call with its workspace from the library's stream-ordered pool.
@@ -476,7 +391,7 @@ int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, in
             return fail(SELSCAN_ERR_NO_MEMORY, "chunk workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
         }
     }
-    int rc = launch_fwd_into(base, plan, dtype, sms, static_cast<float *>(ws), st);
+    int rc = launch_fwd_into(base, plan, dtype, dev, sms, static_cast<float *>(ws), st);
     if (ws) cudaFreeAsync(ws, st);
     return rc;
 }
@@ -592,7 +507,7 @@ extern "C" int selscan_fwd_ex(const void *x, const void *delta, const float *A, 
     if (rc != SELSCAN_OK) return rc;
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     FwdPlan plan;
-    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, sms, &plan);
+    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, h0, hT, sms, &plan);
     ScanArgs a;
     memset(&a, 0, sizeof a);
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
@@ -646,7 +561,7 @@ extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float
     if (rc != SELSCAN_OK) return rc;
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     FwdPlan plan;
-    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, sms, &plan);
+    plan_fwd(Bsz, L, D, N, es, x, delta, B, C, h0, hT, sms, &plan);
     const size_t need = fwd_workspace_bytes(plan, Bsz, D, N);
     if (need > SELSCAN_NOALLOC_SCRATCH_BYTES)
         return fail(SELSCAN_ERR_UNSUPPORTED,
@@ -663,7 +578,7 @@ extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float
     a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.y = y; a.h0 = h0; a.hT = hT;
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.softplus = delta_softplus ? 1 : 0;
-    return launch_fwd_into(a, plan, dtype, sms, ws, st);
+    return launch_fwd_into(a, plan, dtype, dev, sms, ws, st);
 }
 
 // ---- forward from host buffers --------------------------------------------
@@ -761,11 +676,13 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     const bool chain = pieces > 1 || h0 || hT;
 
     // Device staging: per slot x, delta, y (Bsz, lp, D) and B, C (Bsz, lp, N);
-    // then A and the state. Every part starts on a 256-byte boundary.
+    // then A and two states (piece p reads one and writes the other, so no
+    // scan updates its state in place). Every part starts on a 256-byte
+    // boundary.
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
     const size_t bx = up((size_t)(Bsz * lp * D) * es), bn = up((size_t)(Bsz * lp * N) * es);
     const size_t slot_bytes = 3 * bx + 2 * bn;
-    const size_t total = 2 * slot_bytes + up((size_t)(D * N) * 4) + (chain ? up(state_bytes) : 0);
+    const size_t total = 2 * slot_bytes + up((size_t)(D * N) * 4) + (chain ? 2 * up(state_bytes) : 0);
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
@@ -791,11 +708,15 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     cudaStreamWaitEvent(hp->in2, ev_alloc, 0);
     cudaStreamWaitEvent(hp->out, ev_alloc, 0);
     float *A_d = reinterpret_cast<float *>(ws + 2 * slot_bytes);
-    float *state_d = chain ? reinterpret_cast<float *>(ws + 2 * slot_bytes + up((size_t)(D * N) * 4)) : nullptr;
+    float *state_d[2] = {nullptr, nullptr};
+    if (chain) {
+        state_d[0] = reinterpret_cast<float *>(ws + 2 * slot_bytes + up((size_t)(D * N) * 4));
+        state_d[1] = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(state_d[0]) + up(state_bytes));
+    }
 
     e = cudaMemcpyAsync(A_d, A, (size_t)(D * N) * 4, cudaMemcpyHostToDevice, hp->in);
     if (e == cudaSuccess && h0)
-        e = cudaMemcpyAsync(state_d, h0, state_bytes, cudaMemcpyHostToDevice, hp->in);
+        e = cudaMemcpyAsync(state_d[0], h0, state_bytes, cudaMemcpyHostToDevice, hp->in);
 
     const size_t rows = (size_t)Bsz;
     const size_t xpitch = (size_t)(L * D) * es, npitch = (size_t)(L * N) * es;
@@ -829,12 +750,14 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
         if (two_in) cudaStreamWaitEvent(hp->comp, ev_in2[slot], 0);
         if (p >= 2) cudaStreamWaitEvent(hp->comp, ev_out[slot], 0);
         FwdPlan plan;
-        plan_fwd(Bsz, n, D, N, es, x_d, dl_d, B_d, C_d, sms, &plan);
+        const float *h_in = (p == 0 && !h0) ? nullptr : state_d[p & 1];
+        float *h_out = state_d[(p + 1) & 1];
+        plan_fwd(Bsz, n, D, N, es, x_d, dl_d, B_d, C_d, h_in, h_out, sms, &plan);
         ScanArgs a;
         memset(&a, 0, sizeof a);
         a.x = x_d; a.delta = dl_d; a.B = B_d; a.C = C_d; a.A = A_d; a.y = y_d;
-        a.h0 = (p == 0 && !h0) ? nullptr : state_d;
-        a.hT = chain ? state_d : nullptr;
+        a.h0 = h_in;
+        a.hT = h_out;
         a.Bsz = Bsz; a.L = n; a.D = D; a.N = N;
         a.softplus = delta_softplus ? 1 : 0;
         rc = launch_fwd(a, plan, dtype, dev, sms, hp->comp);
@@ -848,7 +771,7 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
         cudaEventRecord(ev_out[slot], hp->out);
     }
     if (e == cudaSuccess && rc == SELSCAN_OK && hT)
-        e = cudaMemcpyAsync(hT, state_d, state_bytes, cudaMemcpyDeviceToHost, hp->out);
+        e = cudaMemcpyAsync(hT, state_d[pieces & 1], state_bytes, cudaMemcpyDeviceToHost, hp->out);
 
     // Drain every stream, then give the staging back and let the caller's
     // stream continue after this call.
@@ -919,7 +842,6 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     StepArgs a{state, x, delta, A, B, C, y, Dskip, z, Bsz, D, N};
     const bool zoh = (flags & SELSCAN_FLAG_ZOH) != 0;
-    const int64_t chains = Bsz * D;
     // 4V states per lane (V 16-byte groups), G = N / (4V) lanes per chain; G
     // must divide the warp so that a chain's lanes never straddle two warps.
     // V = 1 measured fastest on B300 (Bsz=256, D=2560, N=16, state from HBM:
@@ -931,78 +853,10 @@ extern "C" int selscan_step_ex(float *state, const float *x, const float *delta,
     const int G = (int)(N / (4 * V));
     const bool vec = (N % 4 == 0) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&
                      aligned(state, 16) && aligned(A, 16) && aligned(B, 16) && aligned(C, 16);
-    if (vec) {
-        const int64_t blocks = (chains * G + kStepThreads - 1) / kStepThreads;
-        if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-        const unsigned nb = (unsigned)blocks;
-#define SELSCAN_STEP_CASE(g, v) \
-        if (G == g && V == v) { \
-            if (zoh) step_vec_kernel<g, v, true><<<nb, kStepThreads, 0, st>>>(a); \
-            else step_vec_kernel<g, v, false><<<nb, kStepThreads, 0, st>>>(a); \
-        }
-        SELSCAN_STEP_CASE(1, 1) else SELSCAN_STEP_CASE(2, 1) else SELSCAN_STEP_CASE(4, 1)
-        else SELSCAN_STEP_CASE(8, 1) else SELSCAN_STEP_CASE(16, 1)
-        else SELSCAN_STEP_CASE(1, 2) else SELSCAN_STEP_CASE(2, 2) else SELSCAN_STEP_CASE(4, 2)
-        else SELSCAN_STEP_CASE(8, 2) else SELSCAN_STEP_CASE(1, 4) else SELSCAN_STEP_CASE(2, 4)
-        else SELSCAN_STEP_CASE(4, 4)
-#undef SELSCAN_STEP_CASE
-    } else {
-        const int64_t blocks = (chains + kStepThreads - 1) / kStepThreads;
-        if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-        if (zoh) step_scalar_kernel<true><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
-        else step_scalar_kernel<false><<<(unsigned)blocks, kStepThreads, 0, st>>>(a);
-    }
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+    return launch_step_kernel(a, G, (int)V, vec, zoh, st);
 }
 
 // ---- causal depthwise convolution before the scan ------------------------
-
-namespace selscan {
-namespace {
-
-template <typename T>
-int launch_conv1d(const ConvArgs &a, int64_t K, cudaStream_t st)
-{
-    // Four channels per thread when rows allow vector access (D % 4 == 0,
-    // x and out aligned to 4 elements, bias to 16 bytes).
-    const size_t es = sizeof(T);
-    const bool vec = a.D % 4 == 0 && aligned(a.x, 4 * es) && aligned(a.out, 4 * es) && aligned(a.bias, 16) &&
-                     env_long("SELSCAN_CONV_VEC", 1) != 0;
-    if (vec) {
-        const dim3 grid((unsigned)((a.D / 4 + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
-                        (unsigned)((a.L + kConvVecT - 1) / kConvVecT));
-        switch (K) {
-        case 1: conv1d_vec_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 2: conv1d_vec_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 3: conv1d_vec_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 4: conv1d_vec_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 5: conv1d_vec_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 6: conv1d_vec_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 7: conv1d_vec_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a); break;
-        default: conv1d_vec_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a); break;
-        }
-        cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
-    }
-    const dim3 grid((unsigned)((a.D + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
-                    (unsigned)((a.L + kConvT - 1) / kConvT));
-    switch (K) {
-    case 1: conv1d_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 2: conv1d_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 3: conv1d_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 4: conv1d_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 5: conv1d_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 6: conv1d_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 7: conv1d_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a); break;
-    default: conv1d_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a); break;
-    }
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
-}
-
-} // namespace
-} // namespace selscan
 
 extern "C" int selscan_conv1d(const void *x, const float *w, const float *bias, void *out, int64_t Bsz,
                               int64_t L, int64_t D, int64_t K, int dtype, int silu, const float *state_in,
@@ -1047,7 +901,11 @@ extern "C" int selscan_conv1d(const void *x, const float *w, const float *bias, 
         return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state copy");
     }
     ConvArgs a{x, w, bias, out, state_in, state_out, Bsz, L, D, silu ? 1 : 0};
-    return dtype == SELSCAN_F32 ? launch_conv1d<float>(a, K, st) : launch_conv1d<__nv_bfloat16>(a, K, st);
+    // Four channels per thread when rows allow vector access (D % 4 == 0,
+    // x and out aligned to 4 elements, bias to 16 bytes).
+    const bool vec = D % 4 == 0 && aligned(x, 4 * es) && aligned(out, 4 * es) && aligned(bias, 16) &&
+                     env_long("SELSCAN_CONV_VEC", 1) != 0;
+    return launch_conv1d_kernel(a, K, dtype, vec, st);
 }
 
 extern "C" int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const float *bias,
@@ -1078,23 +936,8 @@ extern "C" int selscan_conv1d_step(float *conv_state, const float *x, const floa
     }
     if (overlaps(rs, ro))
         return fail(SELSCAN_ERR_INVALID_ARG, "out overlaps conv_state");
-    const int64_t blocks = (nd + kConvThreads - 1) / kConvThreads;
-    if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
     ConvStepArgs a{conv_state, x, w, bias, out, Bsz, D, silu ? 1 : 0};
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned nb = (unsigned)blocks;
-    switch (K) {
-    case 1: conv1d_step_kernel<1><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 2: conv1d_step_kernel<2><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 3: conv1d_step_kernel<3><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 4: conv1d_step_kernel<4><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 5: conv1d_step_kernel<5><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 6: conv1d_step_kernel<6><<<nb, kConvThreads, 0, st>>>(a); break;
-    case 7: conv1d_step_kernel<7><<<nb, kConvThreads, 0, st>>>(a); break;
-    default: conv1d_step_kernel<8><<<nb, kConvThreads, 0, st>>>(a); break;
-    }
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
+    return launch_conv1d_step_kernel(a, K, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype, int *chunks,
@@ -1114,7 +957,7 @@ extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, in
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     // Alignment does not change the chunking; pass 16-byte aligned stand-ins.
     const void *al = reinterpret_cast<const void *>(uintptr_t(256));
-    plan_fwd(Bsz, L, D, N, es, al, al, al, al, sms, &plan);
+    plan_fwd(Bsz, L, D, N, es, al, al, al, al, nullptr, nullptr, sms, &plan);
     const bool empty = Bsz == 0 || D == 0 || L == 0;
     if (chunks) *chunks = empty ? 0 : plan.K;
     if (chunk_len) *chunk_len = empty ? 0 : plan.chunk;
@@ -1130,19 +973,41 @@ extern "C" const char *selscan_last_error(void) { return g_err; }
 extern "C" int selscan_check_device_error(void *stream)
 {
     g_err[0] = '\0';
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "device work");
-    unsigned fault = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&fault, g_selscan_fault, sizeof fault);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device fault word");
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    unsigned *word = nullptr;
+    rc = fault_word(dev, st, &word);
+    if (rc != SELSCAN_OK) return rc;
+    unsigned fault = 0;
+    e = cudaMemcpyAsync(&fault, word, sizeof fault, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the stream's fault word");
     if (fault != 0) {
-        cudaMemcpyToSymbol(g_selscan_fault, &zero, sizeof zero);
+        e = cudaMemsetAsync(word, 0, sizeof fault, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the stream's fault word");
         const char *what = fault == kFaultTmaTimeout    ? "an input tile never arrived"
                            : fault == kFaultFlagTimeout ? "a chunk carry never appeared"
                                                         : "unknown";
         return fail(SELSCAN_ERR_TIMEOUT, "a kernel gave up waiting (fault code %u: %s)", fault, what);
     }
+    return SELSCAN_OK;
+}
+
+extern "C" int selscan_test_fault_injection(int withhold_carries, int wait_limit_ms)
+{
+    g_err[0] = '\0';
+    if (withhold_carries < 0 || wait_limit_ms < 0 || (uint64_t)wait_limit_ms > kWaitLimitNs / 1000000ull)
+        return fail(SELSCAN_ERR_INVALID_ARG, "withhold_carries must be 0 or 1 and wait_limit_ms in 0..%llu",
+                    (unsigned long long)(kWaitLimitNs / 1000000ull));
+    std::lock_guard<std::mutex> lk(g_test_mu);
+    g_test_withhold = withhold_carries ? 1 : 0;
+    g_test_wait_ms = wait_limit_ms;
     return SELSCAN_OK;
 }
 

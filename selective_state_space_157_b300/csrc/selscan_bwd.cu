@@ -1,7 +1,8 @@
-// selscan_bwd.cu -- host side of the backward pass: argument checks, the
-// checkpoint workspace and the launch of scan_bwd_kernel. Compiled in the
-// library's one translation unit after selscan.cu (see libselscan.cu), whose
-// argument-check, error and workspace helpers it uses.
+// selscan_bwd.cu -- the backward pass: scan_bwd_kernel (scan_bwd.cuh), its
+// argument checks, checkpoint workspace and launch.
+#include <cstring>
+
+#include "host_common.h"
 #include "scan_bwd.cuh"
 
 using namespace selscan;

@@ -3,18 +3,16 @@
 // fault word. Inline PTX for sm_100-family GPUs (here sm_103a).
 //
 // Every wait is bounded: a wait that has not completed after kWaitLimitNs of
-// GPU time records a fault code in g_selscan_fault and reports failure, so a
-// broken pipeline ends the kernel with an error the host can read
-// (selscan_check_device_error) instead of hanging the GPU.
+// GPU time reports failure, and the kernel records a fault code in the fault
+// word of the stream it was launched on, so a broken pipeline ends the
+// kernel with an error the host can read (selscan_check_device_error)
+// instead of hanging the GPU.
 #pragma once
 
 #include <cuda.h>   // CUtensorMap (type only; the driver entry point is fetched at run time)
 #include <stdint.h>
 
 namespace selscan {
-
-// Device fault word: 0 = none; otherwise a kFault* code of the first fault.
-__device__ unsigned int g_selscan_fault = 0;
 
 constexpr unsigned kFaultTmaTimeout = 1;   // a TMA tile never arrived
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
@@ -31,9 +29,10 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-__device__ __forceinline__ void record_fault(unsigned code)
+// Fault word: 0 = none; otherwise the kFault* code of the first fault.
+__device__ __forceinline__ void record_fault(unsigned *word, unsigned code)
 {
-    atomicCAS(&g_selscan_fault, 0u, code);
+    atomicCAS(word, 0u, code);
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

@@ -40,6 +40,11 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), f"{name} declared in include/selscan.h but not exported"
 
 
+@pytest.mark.parametrize("withhold, wait_ms", [(-1, 0), (0, -1), (1, 2001)])
+def test_fault_injection_hook_checks_its_arguments(lib, withhold, wait_ms):
+    assert lib.selscan_test_fault_injection(withhold, wait_ms) == ss.ERR_INVALID_ARG
+
+
 def test_version(lib):
     assert "sm_103a" in ss.version()
 

@@ -45,16 +45,29 @@ def test_reference_arm_decode_workload():
 
 
 def test_roofline_arithmetic():
+    """frac is against the benchmark statement's bound, max(t_HBM, t_MUFU + t_FP32);
+    frac_strict against max(t_HBM, t_MUFU, t_FP32)."""
     pk = bench.peaks(148, 2032.0, 6484.3)
     assert pk["mufu_per_s"] == pytest.approx(148 * 32 * 2.032e9)
     w = bench.work_counts(2, 2048, 1536, 16, 4)
     t_mufu = w["mufu"] / pk["mufu_per_s"]
-    r = bench.roofline(w, pk, seconds=2 * t_mufu)
+    t_fp32 = w["fp32"] / pk["fp32_per_s"]
+    t = 2 * (t_mufu + t_fp32)
+    r = bench.roofline(w, pk, seconds=t)
     assert r["bound"] == "alu"
     assert r["frac"] == pytest.approx(0.5)
-    assert r["achieved"] == pytest.approx(w["updates"] / (2 * t_mufu) / 1e12)
-    assert r["frac_summed_bound"] > r["frac"]
+    assert r["frac_strict"] == pytest.approx(max(t_mufu, t_fp32) / t)
+    assert r["frac_strict"] < r["frac"]
+    assert r["achieved"] == pytest.approx(w["updates"] / t / 1e12)
     assert r["peak"] * r["frac"] == pytest.approx(r["achieved"])
+
+
+def test_measured_alu_peaks_replace_the_derived_ones():
+    alu = {"ex2_per_s": 8.0e12, "fp32_per_s": 30.0e12, "ffma_per_s": 30.0e12, "ffma2_per_s": 29.0e12}
+    pk = bench.peaks(148, 2032.0, 6484.3, alu)
+    assert pk["mufu_per_s"] == 8.0e12 and pk["fp32_per_s"] == 30.0e12
+    assert "measured" in bench.peak_source("measured", alu, 148, 2032.0)
+    assert "derived" in bench.peak_source("measured", None, 148, 2032.0)
 
 
 def test_roofline_hbm_bound_in_bytes():
@@ -156,14 +169,15 @@ def test_backward_work_counts():
     assert w["mufu"] == E * 16 + 4 * E and w["fp32"] == 21 * E * 16
     roof = bench.roofline(w, bench.peaks(148, 2032.0, 6484.3), 389e-6)
     assert roof["bound"] == "alu"                     # the adjoint's FP32 work binds, not the bytes
-    assert roof["frac"] == pytest.approx(roof["t_roof_us"]["fp32"] / 389.0)
+    assert roof["frac_strict"] == pytest.approx(roof["t_roof_us"]["fp32"] / 389.0)
+    assert roof["frac"] == pytest.approx((roof["t_roof_us"]["fp32"] + roof["t_roof_us"]["mufu"]) / 389.0)
 
 
 def test_traffic_is_null_when_the_kernel_changed(monkeypatch):
     """profiled_traffic returns the stored bytes only while the digest of the
     kernel's sources matches the one stored with them."""
     from selective_state_space_157_b300 import build as bld
-    monkeypatch.setattr(bld, "source_digest", lambda backward=False: "0000000000000000")
+    monkeypatch.setattr(bld, "source_digest", lambda kernel="fwd": "0000000000000000")
     assert bench.profiled_traffic(2) is None and bench.profiled_traffic(9) is None
 
 
