@@ -35,7 +35,8 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
 # code that plans its launches): the digest of their sources identifies the
 # kernels a profile was taken on.
 KERNEL_UNITS = {
-    "fwd": ("selscan.cu", "fwd_fused_f32.cu", "fwd_fused_bf16.cu", "fwd_plain.cu"),
+    "fwd": ("selscan.cu", "fwd_fused_f32_onepass.cu", "fwd_fused_f32_chunked.cu", "fwd_fused_bf16_onepass.cu",
+            "fwd_fused_bf16_chunked.cu", "fwd_plain.cu"),
     "step": ("selscan.cu", "step.cu"),
     "conv1d": ("selscan.cu", "conv1d.cu"),
     "bwd": ("selscan_bwd.cu",),

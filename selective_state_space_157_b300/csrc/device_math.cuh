@@ -83,8 +83,11 @@ __device__ __forceinline__ float zoh_coef(float dl, float a, float decay)
 
 template <typename T> struct Io;
 
+// load: read-only data (may be cached anywhere); load_cg: data written
+// earlier in the same launch by another CTA (read from L2, not L1).
 template <> struct Io<float> {
     __device__ __forceinline__ static float load(const float *p) { return __ldg(p); }
+    __device__ __forceinline__ static float load_cg(const float *p) { return __ldcg(p); }
     __device__ __forceinline__ static void store(float *p, float v) { *p = v; }
 };
 
@@ -92,6 +95,10 @@ template <> struct Io<__nv_bfloat16> {
     __device__ __forceinline__ static float load(const __nv_bfloat16 *p)
     {
         return __bfloat162float(__ldg(p));
+    }
+    __device__ __forceinline__ static float load_cg(const __nv_bfloat16 *p)
+    {
+        return __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short *>(p)) << 16);
     }
     __device__ __forceinline__ static void store(__nv_bfloat16 *p, float v)
     {

@@ -17,20 +17,34 @@
 
 namespace selscan {
 
+// CTA size of the persistent forward kernel: one pass runs CTAs of 128
+// threads (128 / NSPLIT channels each, up to three per SM); the chunked form
+// runs one CTA of 384 threads per SM (its launch bounds), so that no item
+// waits behind an older CTA on its SM. The planner sizes the chunking by it.
+constexpr int kFusedChunkedThreads = 384;
+constexpr int kFusedChunkedCtasPerSm = 1;
+
 // The persistent forward kernel chosen for a problem: launched by the host
-// with cudaLaunchKernel(kernel, grid, kScanThreads, {&FusedArgs}, smem).
+// with cudaLaunchKernel(kernel, grid, threads, {&FusedArgs}, smem).
 struct FusedLaunch {
     const void *kernel;
     size_t smem;        // dynamic shared memory per CTA
     int ctas_per_sm;    // resident CTAs per SM at that shared-memory size
     int tt, stages;     // timesteps per pipeline stage, ring buffers
+    int threads;        // CTA size
+    int box_w;          // channels per TMA box of x, delta and z (at most 256)
 };
 
 // False when no fused variant fits (the caller then takes the plain path).
-bool pick_fused_f32(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, int stages,
-                    FusedLaunch *out);
-bool pick_fused_bf16(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N, int stages,
-                     FusedLaunch *out);
+// The one-pass form serves plans with one chunk, the chunked form the rest.
+bool pick_fused_f32_onepass(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N,
+                            int stages, FusedLaunch *out);
+bool pick_fused_f32_chunked(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N,
+                            int stages, FusedLaunch *out);
+bool pick_fused_bf16_onepass(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N,
+                             int stages, FusedLaunch *out);
+bool pick_fused_bf16_chunked(int ns, int nsplit, bool vec, bool softplus, bool gate, bool zoh, int64_t N,
+                             int stages, FusedLaunch *out);
 
 // Plain-load forward: aggregate, carry and readout launches (K > 1), or one
 // readout launch. a.chunk, a.K, a.dtiles and, for K > 1, a.agg_h / a.agg_s

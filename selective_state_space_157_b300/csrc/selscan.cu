@@ -183,7 +183,8 @@ struct FwdPlan {
     bool tma;
     int64_t chunk;
     int K;
-    int dtiles;
+    int threads;     // CTA size of the fused kernel
+    int dtiles;      // channel tiles of threads / nsplit channels
     bool stage_hT;   // hT is h0 and K > 1: the final state goes to the workspace, then to hT
 };
 
@@ -204,22 +205,23 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     p->vec = (N == (int64_t)ns * nsplit) && ((N * (int64_t)es) % 16 == 0) && aligned(B, 16) &&
              aligned(C, 16);
     const bool bases16 = aligned(x, 16) && aligned(delta, 16) && aligned(B, 16) && aligned(C, 16);
-    const int chan_per_cta = kScanThreads / nsplit;
-    p->dtiles = (int)((D + chan_per_cta - 1) / chan_per_cta);
     // TMA needs 16-byte aligned bases and row strides, and 32-bit coordinates.
     p->tma = bases16 && env_long("SELSCAN_NO_TMA", 0) == 0 && (D * (int64_t)es) % 16 == 0 && (N * (int64_t)es) % 16 == 0 &&
              L <= 0x7fffffffLL && D <= 0x7fffffffLL && Bsz <= 0x7fffffffLL;
 
-    // Chunking. Each chunk beyond the first costs an extra reduction pass over
-    // its timesteps, and a readout must wait for the reductions of the chunks
-    // before it, so chunking pays only when the chains alone leave the GPU
-    // mostly idle. Measured on B300: with >= 3 warps of chains per SM one pass
-    // is fastest (Bsz=8, D=2048). Below that, about 12 warps per SM in flight
-    // is best while chunks stay short (Bsz=2, L=2048, D=1536: 19 chunks of
-    // 108 steps, where per-item costs weigh); once that leaves chunks of 512
-    // steps or more, 24 warps per SM is faster (Bsz=1, L=131072: 74 chunks,
-    // 5% faster than 37; Bsz=4, L=16384: 9% faster).
-    const int64_t warps1 = Bsz * (int64_t)p->dtiles * (kScanThreads / 32);
+    // Chunking. One pass whenever the chains alone give three or more warps
+    // per SM: on B300 that is the fastest form (Bsz=8, D=2048).
+    // Below that, on the TMA path (one persistent kernel), every chunk is
+    // scanned once from a zero state by a local item, and chunks 1..K-1 get a
+    // correction pass that ends once the carried state has faded. So the
+    // sequence is cut into as many chunks as fill the GPU with local items in
+    // one wave: K = floor(resident CTAs / channel groups), with one CTA of
+    // kFusedChunkedThreads per SM.
+    // The plain-load path (aggregate, carry and readout kernels; every chunk
+    // but the last is scanned twice) measured best with about 12 warps per
+    // SM in flight while chunks stay short, 24 once chunks reach 512 steps.
+    auto tiles = [&](int threads) { const int64_t c = threads / nsplit; return (D + c - 1) / c; };
+    const int64_t warps1 = Bsz * tiles(kScanThreads) * (kScanThreads / 32);
     const long want_warps = env_long("SELSCAN_TARGET_WARPS", 0);
     auto chunks_for = [&](long warps_per_sm) -> int64_t {
         const int64_t target = (int64_t)warps_per_sm * sms;
@@ -228,6 +230,12 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     int64_t K = 1;
     if (warps1 > 0 && want_warps > 0) {
         K = chunks_for(want_warps);
+    } else if (warps1 > 0 && p->tma) {
+        if (warps1 < 3 * (int64_t)sms) {
+            const int64_t groups = Bsz * tiles(kFusedChunkedThreads);
+            const int64_t resident = (int64_t)sms * kFusedChunkedCtasPerSm;
+            K = groups >= resident ? 1 : resident / groups;
+        }
     } else if (warps1 > 0 && warps1 < 3 * (int64_t)sms) {
         K = chunks_for(12);
         if (K > 1 && L / K >= 512)
@@ -246,34 +254,42 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     if (chunk < min_for_grid) chunk = min_for_grid;
     p->chunk = chunk;
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
+    // The chunked TMA kernel runs CTAs of kFusedChunkedThreads; everything
+    // else CTAs of kScanThreads.
+    p->threads = (p->tma && p->K > 1) ? kFusedChunkedThreads : kScanThreads;
+    p->dtiles = (int)tiles(p->threads);
     // Readouts of every chunk load h0 when they start, and the last chunk's
     // readouts write hT when they end: in place, that would race.
     p->stage_hT = hT != nullptr && hT == h0 && p->K > 1;
 }
 
-// Workspace of a plan, in this order: per chunk boundary and chain the end
-// state (N floats) and the sum of dl (1 float); the ticket counter and one
-// done flag per aggregate item (the plain-load path uses no flags); then,
-// for in-place resume, the staged final state (Bsz * D * N floats).
+// Workspace of a plan, in this order: per chunk and chain the end state
+// (N floats, K slots), then the sum of dl (1 float, K slots); the ticket
+// counter and two words per channel group (local items done, carries
+// ready; the plain-load path uses none of them); then, for in-place resume,
+// the staged final state (Bsz * D * N floats).
+// With bf16 output on the TMA path, chunks >= 1 also keep the bf16 rounding
+// residual of their local y (Bsz * L * D bf16, chunk 0's part unused).
 struct WsLayout {
-    size_t pairs, flags, stage, total;
+    size_t pairs, flags, res, stage, total;
 };
 
-WsLayout fwd_workspace_layout(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
+WsLayout fwd_workspace_layout(const FwdPlan &plan, int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype)
 {
-    WsLayout w{0, 0, 0, 0};
+    WsLayout w{0, 0, 0, 0, 0};
     if (plan.K > 1) {
-        w.pairs = (size_t)(plan.K - 1) * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float);
-        w.flags = (1 + (size_t)(plan.K - 1) * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
+        w.pairs = (size_t)plan.K * (size_t)(Bsz * D) * (size_t)(N + 1) * sizeof(float);
+        w.flags = (1 + 2 * (size_t)(Bsz * plan.dtiles)) * sizeof(unsigned);
+        if (plan.tma && dtype == SELSCAN_BF16) w.res = (size_t)(Bsz * L * D) * 2;
     }
     if (plan.stage_hT) w.stage = (size_t)(Bsz * D * N) * sizeof(float);
-    w.total = w.pairs + ((w.flags + 15) & ~(size_t)15) + w.stage;
+    w.total = w.pairs + ((w.flags + 255) & ~(size_t)255) + ((w.res + 15) & ~(size_t)15) + w.stage;
     return w;
 }
 
-size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t D, int64_t N)
+size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype)
 {
-    return fwd_workspace_layout(plan, Bsz, D, N).total;
+    return fwd_workspace_layout(plan, Bsz, L, D, N, dtype).total;
 }
 
 // TMA path: one persistent kernel (aggregates, carries and readout together).
@@ -288,14 +304,17 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
     if (a.z && !aligned(a.z, 16)) return SELSCAN_ERR_UNSUPPORTED;
     const bool zoh = a.zoh != 0;
     const int stages = (int)env_long("SELSCAN_TMA_STAGES", kStages);
-    bool ok = dtype == SELSCAN_F32 ? pick_fused_f32(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, stages, &fl)
-                                   : pick_fused_bf16(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, stages, &fl);
+    const bool chunked = plan.K > 1;
+    auto pick = dtype == SELSCAN_F32 ? (chunked ? pick_fused_f32_chunked : pick_fused_f32_onepass)
+                                     : (chunked ? pick_fused_bf16_chunked : pick_fused_bf16_onepass);
+    const bool ok = pick(plan.ns, plan.nsplit, plan.vec, sp, gate, zoh, a.N, stages, &fl);
     if (!ok) return SELSCAN_ERR_UNSUPPORTED;
     FusedArgs fa;
     memset(&fa, 0, sizeof fa);
     const CUtensorMapDataType dt = dtype == SELSCAN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
-    const uint32_t dpb = (uint32_t)(kScanThreads / plan.nsplit);
+    if (fl.threads != plan.threads) return SELSCAN_ERR_UNSUPPORTED;
+    const uint32_t dpb = (uint32_t)fl.box_w;
     const uint32_t tt = (uint32_t)fl.tt;
     if (!(encode_3d(&fa.mx, dt, es, a.x, a.D, a.L, a.Bsz, dpb, tt) &&
           encode_3d(&fa.md, dt, es, a.delta, a.D, a.L, a.Bsz, dpb, tt) &&
@@ -312,30 +331,42 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         const uint64_t limit_ms = g_test_wait_ms > 0 ? (uint64_t)g_test_wait_ms : kWaitLimitNs / 1000000ull;
         fa.wait_ns = limit_ms * 1000000ull;
     }
-    // In-place output: aggregate k reads the rows of x, delta (and z) that
-    // readout k overwrites.
-    fa.alias_wait = (a.y == a.x || a.y == a.delta || (a.z && a.y == a.z)) ? 1 : 0;
+    // Only with a softplus step is every dl >= 0, so that a state with
+    // A <= 0 can only shrink and may be dropped once negligible.
+    fa.trunc_tau = a.softplus ? kTruncTau : 0.0f;
     const int64_t groups = a.Bsz * plan.dtiles;
-    const int64_t items_agg = (int64_t)(plan.K - 1) * groups;
-    const int64_t items_total = items_agg + (int64_t)plan.K * groups;
+    const int64_t items_local = (int64_t)plan.K * groups;
+    const int64_t items_total = items_local + (int64_t)(plan.K - 1) * groups;
     if (items_total > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "too many work items");
     fa.groups = (int)groups;
-    fa.items_agg = (int)items_agg;
+    fa.items_local = (int)items_local;
     fa.items_total = (int)items_total;
     int64_t grid = items_total;
     if (plan.K > 1) {
-        const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.D, a.N);
+        // A correction item reads delta (and z) of its chunk after the local
+        // item of that chunk wrote y: in place over those, take the plain path.
+        if (a.y == a.delta || (a.z && a.y == a.z)) return SELSCAN_ERR_UNSUPPORTED;
+        const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.L, a.D, a.N, dtype);
         const size_t bdn = (size_t)(a.Bsz * a.D * a.N);
         fa.aggH = ws;
-        fa.aggS = ws + (size_t)(plan.K - 1) * bdn;
+        fa.aggS = ws + (size_t)plan.K * bdn;
         fa.ctrl = reinterpret_cast<unsigned *>(reinterpret_cast<unsigned char *>(ws) + w.pairs);
-        cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, (size_t)(1 + items_agg) * sizeof(unsigned), st);
+        if (w.res)
+            fa.yres = reinterpret_cast<unsigned char *>(ws) + w.pairs + ((w.flags + 255) & ~(size_t)255);
+        cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, w.flags, st);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk flags");
         const int64_t resident = (int64_t)sms * fl.ctas_per_sm;
         if (grid > resident) grid = resident;
+        // When every local item is resident at once, the group's local items
+        // compose its carries in slices (each waits for the group's pairs,
+        // which all running items publish); otherwise the group's last local
+        // item composes them alone.
+        fa.spread = items_local <= grid ? 1 : 0;
+        const int64_t dpb = fl.threads / plan.nsplit;
+        fa.nslices = (int)((dpb * a.N + fl.threads - 1) / fl.threads);
     }
     void *args[] = {&fa};
-    cudaError_t e = cudaLaunchKernel(fl.kernel, dim3((unsigned)grid), dim3(kScanThreads), args, fl.smem, st);
+    cudaError_t e = cudaLaunchKernel(fl.kernel, dim3((unsigned)grid), dim3(fl.threads), args, fl.smem, st);
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
@@ -349,7 +380,7 @@ int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int de
     a.K = plan.K;
     a.dtiles = plan.dtiles;
     if (a.Bsz * plan.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-    const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.D, a.N);
+    const WsLayout w = fwd_workspace_layout(plan, a.Bsz, a.L, a.D, a.N, dtype);
     float *hT_final = a.hT;
     if (plan.stage_hT)
         a.hT = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(ws) + w.total - w.stage);
@@ -362,10 +393,14 @@ int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int de
         if (rc == SELSCAN_ERR_UNSUPPORTED) g_err[0] = '\0';
     }
     if (rc == SELSCAN_ERR_UNSUPPORTED) {
+        // The plain-load kernels run CTAs of kScanThreads.
+        const int64_t cpc = kScanThreads / plan.nsplit;
+        a.dtiles = (int)((a.D + cpc - 1) / cpc);
+        if (a.Bsz * a.dtiles > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
         if (plan.K > 1) {
             const int64_t bd = a.Bsz * a.D;
             a.agg_h = ws;
-            a.agg_s = a.agg_h + (size_t)(plan.K - 1) * (size_t)bd * (size_t)a.N;
+            a.agg_s = a.agg_h + (size_t)plan.K * (size_t)bd * (size_t)a.N;
         }
         rc = launch_plain_kernels(a, plan.ns, plan.nsplit, plan.vec, dtype, st);
     }
@@ -379,7 +414,7 @@ int launch_fwd_into(const ScanArgs &base, const FwdPlan &plan, int dtype, int de
 // One forward call with its workspace from the library's stream-ordered pool.
 int launch_fwd(const ScanArgs &base, const FwdPlan &plan, int dtype, int dev, int sms, cudaStream_t st)
 {
-    const size_t bytes = fwd_workspace_bytes(plan, base.Bsz, base.D, base.N);
+    const size_t bytes = fwd_workspace_bytes(plan, base.Bsz, base.L, base.D, base.N, dtype);
     void *ws = nullptr;
     if (bytes > 0) {
         cudaMemPool_t pool = nullptr;
@@ -562,7 +597,7 @@ extern "C" int selscan_fwd_noalloc(const void *x, const void *delta, const float
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     FwdPlan plan;
     plan_fwd(Bsz, L, D, N, es, x, delta, B, C, h0, hT, sms, &plan);
-    const size_t need = fwd_workspace_bytes(plan, Bsz, D, N);
+    const size_t need = fwd_workspace_bytes(plan, Bsz, L, D, N, dtype);
     if (need > SELSCAN_NOALLOC_SCRATCH_BYTES)
         return fail(SELSCAN_ERR_UNSUPPORTED,
                     "this problem needs %zu bytes of chunk scratch (%d chunks) but the allocation-free entry "
@@ -964,7 +999,7 @@ extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, in
     // The TMA path runs as one kernel (plus a flag reset when chunked); the
     // plain path as aggregate + carry + readout kernels.
     if (launches) *launches = empty ? 0 : (plan.tma ? 1 : (plan.K > 1 ? 3 : 1));
-    if (workspace_bytes) *workspace_bytes = empty ? 0 : (int64_t)fwd_workspace_bytes(plan, Bsz, D, N);
+    if (workspace_bytes) *workspace_bytes = empty ? 0 : (int64_t)fwd_workspace_bytes(plan, Bsz, L, D, N, dtype);
     return SELSCAN_OK;
 }
 

@@ -11,9 +11,20 @@ fp64.
 
 Every case runs the forward scan on the TMA path and the plain-load path,
 in one pass and chunked, for fp32 and bf16 I/O, and the decode step; every
-output is compared element by element with the oracle at the usual
-tolerances (1e-4 fp32, 2e-2 bf16). With delta = 0 exactly the final state
-must equal h0 bit for bit.
+output is compared element by element with the oracle. With delta = 0
+exactly the final state must equal h0 bit for bit.
+
+The bound. Steps of 1e4 make every state a sum of terms around 1e4 that
+cancel to a much smaller result (and A = 0 turns a state into a running sum
+of such terms), so no fp32 evaluation can hold |got - ref| / (1 + |ref|):
+its rounding error scales with the terms, not with their sum. The error is
+therefore measured against the magnitude of what was summed,
+|got - ref| / (1 + M), with M the same scan run by the oracle on |x|, |B|,
+|C| and |h0| (every decay is positive, so that scan adds the magnitudes of
+the signed scan's terms) -- the forward-error bound of a floating-point sum.
+The tolerances are the usual ones (1e-4 fp32, 2e-2 bf16). Where nothing
+cancels (delta = 0, A = 0 with ordinary steps, softplus tails) the plain
+metric must hold as well.
 """
 import numpy as np
 import pytest
@@ -68,6 +79,21 @@ def _case(name, dtype, seed=7):
 
 
 CASES = ["delta_zero", "delta_1e4", "A_zero", "softplus_tails", "mixed"]
+CANCELLING = {"delta_1e4", "mixed"}
+
+
+def bounded_err(got, ref, mag) -> float:
+    """max |got - ref| / (1 + M): the error against the magnitude of the terms."""
+    got, ref, mag = (np.asarray(a, np.float64) for a in (got, ref, mag))
+    return float(np.max(np.abs(got - ref) / (1.0 + np.abs(mag))))
+
+
+def magnitudes(orc, inp):
+    """The oracle's scan on |x|, |B|, |C|, |h0| (same steps and A): the sums
+    of the magnitudes of the terms the signed scan adds, for y and hT."""
+    h0 = None if inp.h0 is None else np.abs(inp.h0).astype(np.float64)
+    return orc.selscan_fwd(np.abs(inp.f32("x")), inp.f32("delta"), inp.A, np.abs(inp.f32("B")),
+                           np.abs(inp.f32("C")), inp.delta_softplus, h0)
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -83,9 +109,14 @@ def test_forward_limits(orc, monkeypatch, case, dtype, path):
     ss.check_device_error()
     yr, hr = oracle_fwd(orc, inp)
     assert torch.isfinite(y.float()).all() and torch.isfinite(hT).all()
-    ey, eh = scaled_err(to_np(y), yr), scaled_err(to_np(hT), hr)
-    assert ey <= TOL[dtype], f"y error {ey:.3e}"
-    assert eh <= TOL[W.F32], f"hT error {eh:.3e}"
+    ym, hm = magnitudes(orc, inp)
+    ey, eh = bounded_err(to_np(y), yr, ym), bounded_err(to_np(hT), hr, hm)
+    assert ey <= TOL[dtype], f"y error {ey:.3e} against the terms' magnitude"
+    assert eh <= TOL[W.F32], f"hT error {eh:.3e} against the terms' magnitude"
+    if case not in CANCELLING:
+        ey, eh = scaled_err(to_np(y), yr), scaled_err(to_np(hT), hr)
+        assert ey <= TOL[dtype], f"y error {ey:.3e}"
+        assert eh <= TOL[W.F32], f"hT error {eh:.3e}"
     if case == "delta_zero":
         assert torch.equal(hT, h0), "delta = 0 must leave the state exactly as it was"
 
@@ -131,8 +162,13 @@ def test_decode_step_limits(orc, case):
     torch.cuda.synchronize()
     st_ref = np.ascontiguousarray(state, dtype=np.float64)
     y_ref = orc.selscan_step(st_ref, x, delta, A, B, C)
-    assert scaled_err(to_np(y), y_ref) <= TOL[W.F32]
-    assert scaled_err(to_np(sd), st_ref) <= TOL[W.F32]
+    st_mag = np.abs(state).astype(np.float64)
+    y_mag = orc.selscan_step(st_mag, np.abs(x), delta, A, np.abs(B), np.abs(C))
+    assert bounded_err(to_np(y), y_ref, y_mag) <= TOL[W.F32]
+    assert bounded_err(to_np(sd), st_ref, st_mag) <= TOL[W.F32]
+    if case not in CANCELLING:
+        assert scaled_err(to_np(y), y_ref) <= TOL[W.F32]
+        assert scaled_err(to_np(sd), st_ref) <= TOL[W.F32]
     if case == "delta_zero":
         assert torch.equal(sd, to_dev(state)), "delta = 0 must leave the state exactly as it was"
 
