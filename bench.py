@@ -195,6 +195,8 @@ def read_measured_peaks():
 
 def kernel_family(w) -> str:
     """The kernel family a workload times (the key of its sources' digest)."""
+    if w.ssd_heads:
+        return "ssd"
     if w.backward:
         return "bwd"
     if w.steps:
@@ -491,6 +493,8 @@ def run_gpu(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     alu = measure_alu_peaks()
     w = W.WORKLOADS[args.workload]
+    if w.ssd_heads:
+        return run_ssd(args, world, rank, local, dev, w)
     if w.steps:
         return run_decode(args, world, rank, local, dev, w, alu)
     if w.conv_K:
@@ -955,6 +959,117 @@ def run_decode(args, world, rank, local, dev, w, alu=None):
                        launches=args.steps, clocks=clocks, dtype="f32")
 
 
+def ssd_work_counts(Bsz, L, H, P, N, elem_bytes):
+    """Algorithmic work of one SSD call (chunks of Q = 64 steps).
+
+    bytes: x read and y written (2 * B*L*H*P elements), B and C read
+    (2 * B*L*N), dt (B*L*H fp32) and A (H fp32).
+    tensor flops: per batch row and chunk, C B^T once (2 Q Q N, shared by the
+    heads); per head and chunk the masked dual product with X (2 Q Q P), the
+    incoming state's contribution C H (2 Q N P) and the chunk's state
+    (B o w)^T X (2 N Q P). (The kernel recomputes C B^T for every head; that
+    repeat is not counted.)"""
+    Q = 64
+    nch = -(-L // Q)
+    nbytes = 2 * Bsz * L * H * P * elem_bytes + 2 * Bsz * L * N * elem_bytes + Bsz * L * H * 4 + H * 4
+    flops = Bsz * nch * (2 * Q * Q * N + H * (2 * Q * Q * P + 4 * Q * N * P))
+    return {"elems": Bsz * L * H * P, "bytes": nbytes, "flops": flops}
+
+
+def run_ssd(args, world, rank, local, dev, w):
+    """The Mamba-2 SSD workload: one step = one selscan_ssd_fwd over the
+    pages' layer (bf16 I/O). Input sets rotate past 2x L2."""
+    import numpy as np
+    import torch
+    import selective_state_space_157_b300 as ss
+    from selective_state_space_157_b300 import workloads as W
+
+    (x, dt, A, B, C), (Bsz, L, H, P, N) = W.ssd_workload_inputs(args.workload)
+    bf16 = w.dtype == W.BF16
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    es = 2 if bf16 else 4
+    t = lambda a, d=torch.float32: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev).to(d)
+    foot = 2 * Bsz * L * H * P * es + 2 * Bsz * L * N * es + Bsz * L * H * 4
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(1, -(-(2 * l2) // foot))
+    sets = [[t(x, tdt), t(dt), t(A), t(B, tdt), t(C, tdt)] for _ in range(copies)]
+    ys = [torch.empty_like(s_[0]) for s_ in sets]
+
+    def step(i):
+        xs, dts, As, Bs, Cs = sets[i % copies]
+        ss.ssd_fwd(xs, dts, As, Bs, Cs, True, y=ys[i % copies])
+
+    sec, clocks = timed_steps(step, args.steps, args.warmup, world, dev, local)
+    per_step = sec / args.steps
+    elems = Bsz * L * H * P
+    value = world * elems * args.steps / sec
+
+    host = [torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(d).pin_memory()
+            for a, d in ((x, tdt), (dt, torch.float32), (A, torch.float32), (B, tdt), (C, tdt))]
+    hy = torch.empty(tuple(x.shape), dtype=tdt, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 20))
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        d = [h_.to(dev, non_blocking=True) for h_ in host]
+        yd = ss.ssd_fwd(*d, True)
+        hy.copy_(yd, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": sum(h_.numel() * h_.element_size() for h_ in host),
+           "d2h_bytes_per_step": hy.numel() * hy.element_size()}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    hbm_gbs, max_mhz, src = read_measured_peaks()
+    work = ssd_work_counts(Bsz, L, H, P, N, es)
+    tf = read_measured_tensor_peak()
+    t_hbm = work["bytes"] / (hbm_gbs * 1e9)
+    t_tc = work["flops"] / (tf["tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = work["bytes"] / per_step / 1e9, hbm_gbs, "GB/s"
+    else:
+        achieved, peak, unit = work["flops"] / per_step / 1e12, tf["tflops"], "TFLOP/s"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": max(t_hbm, t_tc) / per_step,
+            "hbm_gbs": work["bytes"] / per_step / 1e9, "tensor_tflops": work["flops"] / per_step / 1e12,
+            "t_roof_us": {"hbm": t_hbm * 1e6, "tensor": t_tc * 1e6},
+            "traffic": profiled_traffic(args.workload),
+            "kernel": "selscan_ssd_fwd call (3 launches: chunk states, carries, outputs)",
+            "peak_source": f"HBM {src}; tensor {tf['source']}"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        hs = 4   # a sample of heads: the oracle's time is linear in the heads
+        t0 = time.perf_counter()
+        oracle.default().ssd_fwd(x[:, :, :hs], dt[:, :, :hs], A[:hs], B, C, True)
+        secs = time.perf_counter() - t0
+        cpu = {"value": Bsz * L * hs * P / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{hs} of {H} heads over all L ({Bsz * L * hs * P} elements, {secs:.2f} s, fp64, one thread)"}
+    config = {"workload": f"{w.name}: Bsz={Bsz} L={L} H={H} P={P} N={N} {w.dtype} I/O, softplus on "
+                          "(Mamba-2 SSD, fp16 tensor-core operands)",
+              "global_batch": Bsz * world, "seq_len": L, "parallelism": f"replicas x{world}",
+              "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
+    return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                       ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
+                       launches=3 * args.steps, clocks=clocks, dtype="bf16 io, f16 tensor operands, f32 accumulate"
+                       if bf16 else "f32 io, f16 tensor operands, f32 accumulate")
+
+
+def read_measured_tensor_peak():
+    """Dense fp16 tensor throughput: MEASURED_PEAKS.json's cuBLAS bf16 burst
+    figure (fp16 and bf16 share one rate on this part: nominal ratio 1)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"tflops": float(d["bf16_tflops"]), "source": "measured bf16 burst (MEASURED_PEAKS.json) x 1 for fp16"}
+    return {"tflops": 1800.0, "source": "fallback 1.8 PFLOP/s bf16 burst x 1 for fp16"}
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step is one oracle run over a
     bounded sample of the workload's chains, on the host cores."""
@@ -962,6 +1077,8 @@ def run_reference(args, world, rank):
         return None
     from selective_state_space_157_b300 import workloads as W
     w = W.WORKLOADS[args.workload]
+    if w.ssd_heads:
+        return run_reference_ssd(args, world, w)
     if w.steps:
         return run_reference_decode(args, world, w)
     if w.conv_K:
@@ -991,6 +1108,35 @@ def run_reference(args, world, rank):
                                + (", zero-order hold" if w.zoh else ""),
                    "seq_len": L, "parallelism": "host threads"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_ssd(args, world, w):
+    """Reference arm for the SSD workload: each step is one oracle run over a
+    sample of the heads, on the host."""
+    import oracle
+    from selective_state_space_157_b300 import workloads as W
+    (x, dt, A, B, C), (Bsz, L, H, P, N) = W.ssd_workload_inputs(args.workload)
+    hs = 4
+    o = oracle.default()
+    a = (x[:, :, :hs], dt[:, :, :hs], A[:hs], B, C, True)
+    for _ in range(args.warmup):
+        o.ssd_fwd(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.ssd_fwd(*a)
+    tot = time.perf_counter() - t0
+    elems = Bsz * L * hs * P
+    value = elems * args.steps / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: Bsz={Bsz} L={L} H={H} P={P} N={N}, Mamba-2 SSD", "seq_len": L,
+                   "parallelism": "host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{hs} of {H} heads per step ({elems} elements, fp64)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -1088,7 +1234,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=list(range(1, 11)))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per_config measurements")

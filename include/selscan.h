@@ -351,6 +351,37 @@ int selscan_bwd(const float *x, const float *delta, const float *A, const float 
                 int64_t Bsz, int64_t L, int64_t D, int64_t N, int delta_softplus,
                 void *stream);
 
+/*
+ * selscan_ssd_fwd -- the Mamba-2 state space duality (SSD) forward
+ * (youngju.dev "Mamba: Selective State Space Models", section 4.1: the
+ * recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t and its dual form
+ * Y = (T o M) X; section 5.2: heads of headdim P with a state of size N).
+ * Per batch row b and head hd, with dl = dt[b,t,hd] (softplus(dt) when
+ * dt_softplus), a scalar decay per step and B, C shared by all heads:
+ *
+ *   h[n][p] = exp(dl * A[hd]) * h[n][p] + (dl * B[b,t,n]) * x[b,t,hd,p]
+ *   y[b,t,hd,p] = sum_n C[b,t,n] * h[n][p]
+ *
+ *   x, y  : (Bsz, L, H, P), dtype    dt : (Bsz, L, H) fp32    A : (H) fp32
+ *   B, C  : (Bsz, L, N), dtype
+ *   h0    : (Bsz, H, N, P) fp32 or NULL (zeros)
+ *   hT    : (Bsz, H, N, P) fp32 or NULL (not written)
+ *
+ * Sizes: N = 64 or 128, P = 32, 64 or 128, Bsz and H at most 65535, any
+ * L >= 0 (L == 0 writes only hT). The products run on the tensor cores
+ * (tcgen05) with fp16 operands and fp32 accumulators, in chunks of 64 steps
+ * (the dual form inside a chunk, the states carried across chunks), so
+ * results agree with an exact evaluation to about 1e-3 relative for either
+ * dtype. Pointers: x, B, C, y, h0 and hT 16-byte aligned, dt and A
+ * 4-byte aligned. y and hT must not overlap any input or each other.
+ * Workspace: Bsz * H * ceil(L / 64) * (N * P + 1) fp32 from the same
+ * stream-ordered pool as selscan_fwd's. Errors as for selscan_fwd.
+ */
+int selscan_ssd_fwd(const void *x, const float *dt, const float *A, const void *B,
+                    const void *C, void *y, const float *h0, float *hT, int64_t Bsz,
+                    int64_t L, int64_t H, int64_t P, int64_t N, int dtype, int dt_softplus,
+                    void *stream);
+
 /* Message describing the last non-OK status returned on this host thread
  * (empty string if none). The pointer stays valid until the next call on
  * the same thread. */
@@ -359,8 +390,8 @@ const char *selscan_last_error(void);
 /* Waits for `stream` and reports whether work enqueued on it failed:
  * SELSCAN_OK; SELSCAN_ERR_CUDA with the CUDA error in selscan_last_error();
  * or SELSCAN_ERR_TIMEOUT when a kernel stopped waiting for an input tile
- * (fault code 1) or for the carry of an earlier chunk (fault code 2) that
- * never came. Every wait inside the kernels is bounded (2 s of GPU time,
+ * (fault code 1), for the carry of an earlier chunk (fault code 2) or for a
+ * tensor-core product (fault code 3) that never came. Every wait inside the kernels is bounded (2 s of GPU time,
  * which keeps counting while the context is time-sliced out on a shared
  * GPU), so a broken pipeline ends with this status instead of a hang, and
  * the context stays usable. A call that timed out left its outputs

@@ -20,7 +20,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["selscan_fwd", "selscan_bwd", "selective_scan", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step", "fwd_plan", "last_error", "check_device_error",
+__all__ = ["selscan_fwd", "selscan_bwd", "selective_scan", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step",
+           "ssd_fwd", "fwd_plan", "last_error", "check_device_error",
            "release_workspace", "version", "library_path", "SelscanError",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
            "MAX_N", "FLAG_SOFTPLUS", "FLAG_ZOH"]
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
+        L.selscan_ssd_fwd.restype = INT
+        L.selscan_ssd_fwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, INT, INT, P]
         L.selscan_test_fault_injection.restype = INT
         L.selscan_test_fault_injection.argtypes = [INT, INT]
         L.selscan_bwd.restype = INT
@@ -412,6 +415,40 @@ def conv1d_step(conv_state, x, w, bias=None, silu: bool = True, out=None, stream
                                        _ptr(out), Bsz, D, K, int(bool(silu)), _stream_ptr(stream))
     _check(rc)
     return out
+
+
+def ssd_fwd(x, dt, A, B, C, dt_softplus: bool = True, h0=None, return_final_state: bool = False, y=None,
+            hT=None, stream=None):
+    """Mamba-2 SSD forward (selscan_ssd_fwd): x (Bsz, L, H, P) float32 or
+    bfloat16, dt (Bsz, L, H) float32, A (H,) float32, B, C (Bsz, L, N) like
+    x, h0 (Bsz, H, N, P) float32 or None. Returns y (like x), or (y, hT)
+    when ``return_final_state``. Device tensors only."""
+    import torch
+    dev = x.device
+    Bsz, L, H, P = x.shape
+    N = B.shape[2] if B.dim() == 3 else -1
+    code = _dtype_code(x)
+    f = torch.float32
+    _need(x, "x", (Bsz, L, H, P), x.dtype, dev)
+    _need(dt, "dt", (Bsz, L, H), f, dev)
+    _need(A, "A", (H,), f, dev)
+    _need(B, "B", (Bsz, L, N), x.dtype, dev)
+    _need(C, "C", (Bsz, L, N), x.dtype, dev)
+    if h0 is not None:
+        _need(h0, "h0", (Bsz, H, N, P), f, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", (Bsz, L, H, P), x.dtype, dev)
+    if return_final_state and hT is None:
+        hT = torch.empty((Bsz, H, N, P), dtype=f, device=dev)
+    if hT is not None:
+        _need(hT, "hT", (Bsz, H, N, P), f, dev)
+    with torch.cuda.device(dev):
+        rc = lib().selscan_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(y), _ptr(h0), _ptr(hT),
+                                   Bsz, L, H, P, N, code, int(bool(dt_softplus)), _stream_ptr(stream))
+    _check(rc)
+    return (y, hT) if (return_final_state or hT is not None) else y
 
 
 # ---- host tensors: copy in, run on the current device, copy out ------------

@@ -36,11 +36,11 @@ int occupancy(const void *fn, int threads, size_t smem)
 template <typename T, bool CH, int NS, int NSPLIT, bool VEC, bool SP, bool GATE = false, bool ZOH = false>
 bool prepare_fused_sp(int64_t N, int stages, FusedLaunch *out)
 {
-    constexpr int THREADS = CH ? kFusedChunkedThreads : kScanThreads;
+    constexpr int THREADS = fused_threads(CH, NSPLIT);
     constexpr int DPB = THREADS / NSPLIT;
     auto k = scan_fused_kernel<T, NS, NSPLIT, VEC, kTT, SP, GATE, ZOH, CH, THREADS>;
     const int64_t nrow = VEC ? NS * NSPLIT : N;
-    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, stages, GATE);
+    const size_t smem = fused_smem_bytes(sizeof(T), kTT, DPB, nrow, stages, GATE, NSPLIT);
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return false;

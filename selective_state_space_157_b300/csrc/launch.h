@@ -24,6 +24,14 @@ namespace selscan {
 constexpr int kFusedChunkedThreads = 384;
 constexpr int kFusedChunkedCtasPerSm = 1;
 
+// CTA size of the fused kernel: chunked plans kFusedChunkedThreads; one pass
+// 256 threads (one CTA per SM, 128 channels) with two threads per chain,
+// else kScanThreads.
+constexpr int fused_threads(bool chunked, int nsplit)
+{
+    return chunked ? kFusedChunkedThreads : (nsplit == 2 ? 2 * kScanThreads : kScanThreads);
+}
+
 // The persistent forward kernel chosen for a problem: launched by the host
 // with cudaLaunchKernel(kernel, grid, threads, {&FusedArgs}, smem).
 struct FusedLaunch {

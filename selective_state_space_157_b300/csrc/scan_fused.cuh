@@ -218,11 +218,12 @@ __device__ __forceinline__ void store_state(float *p, int valid, const float2 (&
 // with z staged beside x in the ring.
 // CHUNKED: the sequence is cut into chunks (local and correction items, a
 // ticket counter); otherwise one pass, CTA x scanning channel group x.
-// THREADS: 128 (three CTAs per SM), or 384 (one CTA per SM). SMs give their
-// oldest CTA priority, so three CTAs with equal items end far apart (on a
-// B300 the youngest took 1.6x as long as the oldest); the chunked form
-// therefore runs one CTA of twelve warps per SM, whose ring keeps every warp
-// within a few stages of the others.
+// THREADS: 128 (up to three CTAs per SM), 256 or 384 (one CTA per SM). SMs
+// give their oldest CTA priority, so several CTAs with equal items end far
+// apart (on a B300 the youngest of three took 1.6x as long as the oldest);
+// the chunked form therefore runs one CTA of twelve warps per SM, and a
+// one-pass plan with two threads per chain one CTA of eight warps, whose ring
+// keeps every warp within a few stages of the others.
 template <typename T, int NS, int NSPLIT, bool VEC, int TT, bool SOFTPLUS, bool GATE, bool ZOH, bool CHUNKED,
           int THREADS = kScanThreads>
 // Three CTAs per SM fit the shared-memory ring; the register cap this implies
@@ -259,7 +260,11 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     constexpr bool kBf16 = sizeof(T) == 2;
     const int cfloats = kBf16 ? 2 * TT * (int)Nrow : 0;   // fp32 copy of a stage's B and C rows
     float *conv_buf = reinterpret_cast<float *>(smem + STAGES * sbytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * (sbytes + cfloats * 4));
+    // With NSPLIT threads per chain, each stage's (dl, dl * x) per channel is
+    // computed once, cooperatively, into this buffer (one per ring slot).
+    constexpr int kDluFloats = NSPLIT > 1 ? 2 * TT * DPB : 0;
+    float2 *dlu = reinterpret_cast<float2 *>(smem + STAGES * (sbytes + cfloats * 4));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * (sbytes + cfloats * 4 + kDluFloats * 4));
     uint64_t *empty = full + STAGES;
     uint64_t *conv = empty + STAGES;   // bf16: every warp converted its share of the stage
     unsigned *issued = reinterpret_cast<unsigned *>(conv + STAGES);
@@ -366,19 +371,47 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
         // convert together -- every thread needs every row, so converting
         // once per CTA instead of once per thread saves most of the
         // unpacking work. Rows [first, first + rows) of the B|C pair.
+        // With several threads per chain (with_dlu), the stage's dl (after
+        // softplus) and dl * x are computed once per channel into the slot's
+        // dlu buffer by the same cooperative pass. A CTA-wide mbarrier closes
+        // the pass (bounded wait), so the warps need no CTA barrier.
+        constexpr bool kCoop = kBf16 || NSPLIT > 1;
         auto stage_rows = [&](const unsigned char *p, int s, uint32_t r, int first, int rows, const float **Bs,
-                              const float **Cs) -> bool {
+                              const float **Cs, bool with_dlu) -> bool {
             if constexpr (kBf16) {
                 float *cb = conv_buf + s * cfloats;
                 const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p + 2 * xbytes);
                 const int lo = first * TT * (int)Nrow, hi = (first + rows) * TT * (int)Nrow;
                 for (int e = lo + threadIdx.x; e < hi; e += THREADS)
                     cb[e] = __bfloat162float(src[e]);
+            }
+            if constexpr (NSPLIT > 1) {
+                if (with_dlu) {
+                    float2 *db = dlu + s * TT * DPB;
+                    const T *xt = reinterpret_cast<const T *>(p);
+                    const T *dt = reinterpret_cast<const T *>(p + xbytes);
+                    static_assert((TT * DPB) % THREADS == 0, "whole rounds of the cooperative pass");
+#pragma unroll
+                    for (int e0 = 0; e0 < TT * DPB; e0 += THREADS) {
+                        const int e = e0 + threadIdx.x;
+                        const int tt = e / DPB, c = e % DPB;
+                        const int col = (c / W) * (TT * W) + tt * W + c % W;
+                        float dl = smem_val(dt + col);
+                        if (SOFTPLUS)
+                            dl = softplus(dl);
+                        db[e] = make_float2(dl, dl * smem_val(xt + col));
+                    }
+                }
+            }
+            if constexpr (kCoop) {
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&conv[s]);
                 if (!__all_sync(0xffffffffu, mbar_wait(&conv[s], (r / STAGES) & 1u)))
                     return false;
+            }
+            if constexpr (kBf16) {
+                float *cb = conv_buf + s * cfloats;
                 *Bs = cb + n0;
                 *Cs = cb + TT * Nrow + n0;
             } else {
@@ -439,7 +472,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 const T *zs = reinterpret_cast<const T *>(p + 2 * xbytes + 2 * nbytes) + xcol;
                 const float *Bs;
                 const float *Cs;
-                if (!stage_rows(p, s, r, 0, 2, &Bs, &Cs)) {
+                if (!stage_rows(p, s, r, 0, 2, &Bs, &Cs, true)) {
                     ok = false;
                     break;
                 }
@@ -449,6 +482,16 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 // Phase 1, breadth first: TT independent softplus evaluations
                 // advance together, so their dependent FMAs interleave.
                 float dlv[TT], uv[TT];
+                if constexpr (NSPLIT > 1) {
+                    // Computed once per channel by the cooperative pass.
+                    const float2 *db = dlu + s * TT * DPB + grp;
+#pragma unroll
+                    for (int tt = 0; tt < TT; ++tt) {
+                        const float2 v = db[tt * DPB];
+                        dlv[tt] = v.x;
+                        uv[tt] = v.y;
+                    }
+                } else {
 #pragma unroll
                 for (int tt = 0; tt < TT; ++tt)
                     dlv[tt] = smem_val(ds + tt * W);
@@ -480,6 +523,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                                                 make_float2(smem_val(xs + 2 * j * W), smem_val(xs + (2 * j + 1) * W)));
                     uv[2 * j] = u.x;
                     uv[2 * j + 1] = u.y;
+                }
                 }
                 if constexpr (TRACK) {
                     // Stage sum of dl by pairwise halving (rows past the chunk
@@ -790,7 +834,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
             const T *zs = reinterpret_cast<const T *>(p + 2 * xbytes + 2 * nbytes) + xcol;
             const float *Bs = nullptr;
             const float *Cs = nullptr;
-            ok = ok && stage_rows(p, s, r, 1, 1, &Bs, &Cs);
+            ok = ok && stage_rows(p, s, r, 1, 1, &Bs, &Cs, false);
             const int64_t rem = nsteps - (int64_t)i * TT;
             const int tc = rem < TT ? (int)rem : TT;
             if (alive && ok) {
@@ -879,7 +923,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     const uint32_t r2 = ring + i2;
                     if (!__all_sync(0xffffffffu, mbar_wait(&full[r2 % STAGES], (r2 / STAGES) & 1u)))
                         ok = false;
-                    if constexpr (kBf16) {
+                    if constexpr (kCoop) {
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive(&conv[r2 % STAGES]);
@@ -908,11 +952,12 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
     }
 }
 
-inline size_t fused_smem_bytes(size_t es, int TT, int DPB, int64_t Nrow, int stages, bool gate)
+inline size_t fused_smem_bytes(size_t es, int TT, int DPB, int64_t Nrow, int stages, bool gate, int nsplit)
 {
     const size_t stage = ((gate ? 3 : 2) * (size_t)TT * DPB + 2 * (size_t)TT * (size_t)Nrow) * es;
     const size_t conv = es == 2 ? 2 * (size_t)TT * (size_t)Nrow * 4 : 0;
-    return (size_t)stages * (stage + conv) + (size_t)stages * (8 + 8 + 8 + 4) + 16;
+    const size_t dlu = nsplit > 1 ? 2 * (size_t)TT * DPB * 4 : 0;
+    return (size_t)stages * (stage + conv + dlu) + (size_t)stages * (8 + 8 + 8 + 4) + 16;
 }
 
 } // namespace selscan

@@ -198,6 +198,9 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     long want = env_long("SELSCAN_NSPLIT", 0);
     if ((want == 2 || want == 4) && want > nsplit && N >= 4 * want)
         nsplit = (int)want;
+    // (Two threads per chain for one-pass plans with 3 to 6 warps of chains
+    // per SM measured slower on B300: Bsz=8 L=2048 D=2048 bf16 took 260 us
+    // against 237 with one thread per chain.)
     int64_t per = (N + nsplit - 1) / nsplit;
     int ns = per <= 4 ? 4 : (per <= 8 ? 8 : 16);
     p->ns = ns;
@@ -254,9 +257,9 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     if (chunk < min_for_grid) chunk = min_for_grid;
     p->chunk = chunk;
     p->K = L > 0 ? (int)((L + chunk - 1) / chunk) : 1;
-    // The chunked TMA kernel runs CTAs of kFusedChunkedThreads; everything
-    // else CTAs of kScanThreads.
-    p->threads = (p->tma && p->K > 1) ? kFusedChunkedThreads : kScanThreads;
+    // The fused kernel's CTA size (fused_threads); the plain-load kernels run
+    // CTAs of kScanThreads.
+    p->threads = p->tma ? fused_threads(p->K > 1, nsplit) : kScanThreads;
     p->dtiles = (int)tiles(p->threads);
     // Readouts of every chunk load h0 when they start, and the last chunk's
     // readouts write hT when they end: in place, that would race.
@@ -1028,6 +1031,7 @@ extern "C" int selscan_check_device_error(void *stream)
         if (e != cudaSuccess) return cuda_fail(e, "clearing the stream's fault word");
         const char *what = fault == kFaultTmaTimeout    ? "an input tile never arrived"
                            : fault == kFaultFlagTimeout ? "a chunk carry never appeared"
+                           : fault == 3                 ? "a tensor-core product never completed"
                                                         : "unknown";
         return fail(SELSCAN_ERR_TIMEOUT, "a kernel gave up waiting (fault code %u: %s)", fault, what);
     }

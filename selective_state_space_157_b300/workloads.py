@@ -12,6 +12,9 @@ Workloads (the five shapes the selective-scan benchmark is quoted on):
   3 mamba370m  bf16  Bsz=8   L=2048    D=2048 N=16  softplus on; A fp32
   4 long       fp32  Bsz=1   L=131072  D=1536 N=16  softplus on; returns hT
   5 decode     fp32  Bsz=256 D=2560    N=16   1024 decode steps, state in place
+ (6-9: the gated, zero-order-hold, conv1d and backward forms of the 130M
+ layer; 10: the Mamba-2 SSD layer of the pages' section 5.2, Bsz=1 L=1024,
+ 64 heads of headdim 64, N=128, bf16 I/O.)
 
 Value distributions: x, B, C ~ N(0, 1); the delta pre-activation
 u ~ N(-3, 1) (N(-4, 1) for the long workload); A[d, n] = -(n + 1) (the
@@ -52,6 +55,7 @@ class Workload:
     zoh: bool = False     # zero-order-hold discretisation instead of dl * B
     conv_K: int = 0       # > 0: the causal conv1d + SiLU before the scan, with K taps
     backward: bool = False  # the backward pass (dy from bwd_grads, no dhT)
+    ssd_heads: int = 0      # > 0: the Mamba-2 SSD with this many heads of headdim D / ssd_heads (ssd_inputs)
 
     @property
     def elems(self) -> int:
@@ -69,6 +73,7 @@ WORKLOADS = {
     7: Workload(7, "mamba130m-zoh", 2, 2048, 1536, 16, F32, -3.0, "arange", 107, zoh=True),
     8: Workload(8, "mamba130m-conv1d", 2, 2048, 1536, 16, F32, -3.0, "arange", 108, conv_K=4),
     9: Workload(9, "mamba130m-bwd", 2, 2048, 1536, 16, F32, -3.0, "arange", 109, backward=True),
+    10: Workload(10, "mamba2-ssd", 1, 1024, 4096, 128, BF16, -3.0, "loguniform", 110, ssd_heads=64),
 }
 
 
@@ -225,6 +230,18 @@ def bwd_grads(Bsz: int, L: int, D: int, N: int, *, seed: int, with_dhT: bool = T
     dy = normal(rng(seed, _TID["dy"]), (Bsz, L, D))
     dhT = normal(rng(seed, _TID["dhT"]), (Bsz, D, N)) if with_dhT else None
     return dy, dhT
+
+
+def ssd_workload_inputs(wid: int):
+    """Inputs of an SSD workload: x, dt, A, B, C (fp32; x, B, C rounded to
+    bf16 values for bf16 I/O) and the shape (Bsz, L, H, P, N)."""
+    w = WORKLOADS[wid]
+    H = w.ssd_heads
+    P = w.D // H
+    x, dt, A, B, C, _ = ssd_inputs(w.Bsz, w.L, H, P, w.N, seed=w.seed, u_mean=w.u_mean)
+    if w.dtype == BF16:
+        x, B, C = (bf16_bits_to_f32(to_bf16_bits(a)) for a in (x, B, C))
+    return (x, dt, A, B, C), (w.Bsz, w.L, H, P, w.N)
 
 
 def ssd_inputs(Bsz: int, L: int, H: int, P: int, N: int, *, seed: int, u_mean: float = -3.0,

@@ -240,3 +240,25 @@ def test_bwd_argument_errors(lib, kw, code):
 
 def test_bwd_empty_channel_count_is_ok_without_cuda(lib):
     assert bwd(lib, D=0, A=None, dA=None) == ss.OK
+
+
+def ssd(lib, **kw):
+    a = dict(x=16, dt=8, A=8, B=16, C=16, y=16, h0=None, hT=None, Bsz=1, L=4, H=2, P=64, N=128, dtype=0,
+             softplus=1)
+    a.update(kw)
+    return lib.selscan_ssd_fwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["y"], a["h0"], a["hT"], a["Bsz"],
+                               a["L"], a["H"], a["P"], a["N"], a["dtype"], a["softplus"], None)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(dtype=7), ss.ERR_INVALID_ARG), (dict(L=-1), ss.ERR_INVALID_ARG), (dict(P=0), ss.ERR_INVALID_ARG),
+    (dict(N=32), ss.ERR_UNSUPPORTED), (dict(P=48), ss.ERR_UNSUPPORTED), (dict(x=None), ss.ERR_INVALID_ARG),
+    (dict(A=None), ss.ERR_INVALID_ARG), (dict(y=12), ss.ERR_INVALID_ARG), (dict(x=24), ss.ERR_INVALID_ARG), (dict(Bsz=70000), ss.ERR_UNSUPPORTED),
+])
+def test_ssd_argument_errors(lib, kw, code):
+    """Argument checks of selscan_ssd_fwd run before any CUDA call."""
+    assert ssd(lib, **kw) == code
+
+
+def test_ssd_empty_problem_is_ok_without_cuda(lib):
+    assert ssd(lib, Bsz=0) == ss.OK and ssd(lib, H=0) == ss.OK
