@@ -6,22 +6,28 @@
 namespace selscan {
 namespace {
 
+template <typename T, int RUN>
+void launch_conv1d_vec(const ConvArgs &a, int64_t K, cudaStream_t st)
+{
+    const dim3 grid((unsigned)((a.D / 4 + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
+                    (unsigned)((a.L + RUN - 1) / RUN));
+    switch (K) {
+    case 1: conv1d_vec_kernel<T, 1, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 2: conv1d_vec_kernel<T, 2, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 3: conv1d_vec_kernel<T, 3, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 4: conv1d_vec_kernel<T, 4, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 5: conv1d_vec_kernel<T, 5, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 6: conv1d_vec_kernel<T, 6, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 7: conv1d_vec_kernel<T, 7, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    default: conv1d_vec_kernel<T, 8, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    }
+}
+
 template <typename T>
 int launch_conv1d_t(const ConvArgs &a, int64_t K, bool vec, cudaStream_t st)
 {
     if (vec) {
-        const dim3 grid((unsigned)((a.D / 4 + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
-                        (unsigned)((a.L + kConvVecT - 1) / kConvVecT));
-        switch (K) {
-        case 1: conv1d_vec_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 2: conv1d_vec_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 3: conv1d_vec_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 4: conv1d_vec_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 5: conv1d_vec_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 6: conv1d_vec_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a); break;
-        case 7: conv1d_vec_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a); break;
-        default: conv1d_vec_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a); break;
-        }
+        launch_conv1d_vec<T, kConvVecRun>(a, K, st);
     } else {
         const dim3 grid((unsigned)((a.D + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
                         (unsigned)((a.L + kConvT - 1) / kConvT));

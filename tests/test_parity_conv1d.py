@@ -31,12 +31,13 @@ def test_conv1d_matches_oracle(orc, K, dtype, with_state):
     assert np.array_equal(to_np(st).astype(np.float32), st_ref)
 
 
-@pytest.mark.parametrize("L", [1, 3, 31, 32, 33, 63, 64, 65, 129])
+@pytest.mark.parametrize("L", [1, 3, 15, 16, 17, 31, 32, 33, 63, 64, 65, 129])
 @pytest.mark.parametrize("D", [70, 72])
 @pytest.mark.parametrize("vec", ["1", "0"])
 def test_conv1d_run_boundaries(orc, monkeypatch, L, D, vec):
-    """Runs of 32 (four channels per thread, D % 4 == 0) and 64 (one channel
-    per thread) timesteps, ragged tails, and both kernels on the same D."""
+    """Runs of 32 timesteps loaded in batches of 16 (four channels per
+    thread, D % 4 == 0) and runs of 64 (one channel per thread), ragged tails,
+    and both kernels on the same D."""
     monkeypatch.setenv("SELSCAN_CONV_VEC", vec)
     x, w, bias, state = W.conv_inputs(2, L, D, 4, seed=L + D, with_state=True)
     out, st = ss.conv1d(to_dev(x), to_dev(w), to_dev(bias), state_in=to_dev(state), return_state=True)
