@@ -814,7 +814,7 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     pk["source"] = peak_source(src, alu, sms, max_mhz)
     work = bwd_work_counts(w.Bsz, w.L, w.D, w.N)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
-                    kernel="scan_bwd_kernel (1 launch + 3 memsets)")
+                    kernel="bwd_local + bwd_carry + bwd_main kernels (3 launches + 3 memsets)")
     cpu = None
     if not args.no_cpu_baseline:
         import oracle

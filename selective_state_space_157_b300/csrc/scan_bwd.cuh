@@ -12,25 +12,35 @@
 //   d dl_t = sum_n (g_t h_{t-1} a_t A + g_t B_t x_t),  times sigmoid(u)
 //            when dl = softplus(u)
 //   dh0   = a_0 g_0.
+// a_t h_{t-1} is taken as h_t - dl_t x_t B_t, so the adjoint needs the
+// recomputed states but not the decays of the step before.
 //
-// Layout of the work. One chain (b, d) is P lanes (P = the power of two
-// >= N, at most 32), one state index n per lane, so the sums over n are
-// shuffles within the lane group and the state of a whole chunk fits in
-// registers. A block is kBwdThreads lanes = cpb chains of one batch row b.
-//   1. A forward pass over L writes the state at the start of every chunk of
-//      kBwdT steps to a workspace (b, chunk, d, n).
-//   2. The chunks are then taken last to first: the chunk's states and decays
-//      are recomputed from its checkpoint into registers, and the adjoint runs
-//      backwards through them.
-// Per-timestep inputs of a chunk are loaded by the whole block with
-// coalesced loads (one row of cpb channels per step) into registers one
-// chunk ahead, then staged in shared memory. Each lane keeps its dx and
-// d delta terms for the chunk's steps; one reduce-scatter over the lane group
-// per chunk leaves every lane with whole steps to store. dB and dC are summed
-// over the chains of a warp with shuffles, over the warps in shared memory,
-// and added to global memory with one atomic per block, timestep and state;
-// dA is summed over t in registers and added with one atomic per chain.
-// Chunks that lie wholly inside L run without per-step bounds checks.
+// Layout of the work. A thread owns kBwdS = 4 states of one chain (b, d),
+// P threads a chain (P = the power of two >= N / 4, at most 8); a block is
+// kBwdThreads threads = CPB = kBwdThreads / P chains of one batch row. Sums
+// over n are a thread's own four states, then shuffles over its P lanes;
+// sums over d (dB, dC) are a reduce-scatter over the chains of a warp, then
+// over the warps in shared memory, then one atomic per block, step and state.
+//
+// The sequence is cut into K segments of whole chunks (kBwdT steps), so that
+// K * (channel tiles) * Bsz blocks fill the GPU. Segments are independent
+// until their carries are composed, the associative pairs of
+// booiljung.github.io "3.1 ...", section 3.1.5.2, in both directions:
+//   1. bwd_local_kernel: per segment, the forward recurrence from a zero
+//      state, writing the local state and the running sum of dl at every
+//      chunk start (the checkpoints), the end state and the segment's sum of
+//      dl; then the adjoint recurrence from zero at the segment's end back
+//      to its start (what the segment alone sends into the state before it).
+//   2. bwd_carry_kernel: per (b, d, n), the true state entering each segment
+//      (h_in(k+1) = exp(A S_k) h_in(k) + hl(k), from h0) and the adjoint
+//      entering each segment from the right (g_out(k-1) = exp(A S_k) g_out(k)
+//      + gl(k), from dLoss/dhT).
+//   3. bwd_main_kernel: per segment, chunks last to first: the chunk's start
+//      state is its local checkpoint plus exp(A S) h_in, its states are
+//      recomputed into registers, and the adjoint runs back through them from
+//      g_out, producing every gradient.
+// Steps past L are staged as zeros with dl = 0, so they leave h and g as
+// they are and contribute nothing; only their stores are skipped.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -40,366 +50,583 @@
 
 namespace selscan {
 
-// 128-lane blocks with 32-step chunks: fewer, longer chunks amortise the
-// per-chunk barriers, staging latency and atomics, and three blocks fit on
-// an SM at N = 16 (measured on B300 for the 130M-like layer: 0.384 ms per
-// call, against 0.418 ms for 16-step chunks and 0.476 ms for 16-step chunks
-// in 256-lane blocks).
 constexpr int kBwdThreads = 128;
 constexpr int kBwdWarps = kBwdThreads / 32;
-constexpr int kBwdT = 32;      // timesteps per chunk (registers per lane: about 2 * kBwdT)
+constexpr int kBwdT = 16;      // timesteps per chunk: states of a chunk live in registers
+constexpr int kBwdS = 4;       // states per thread
 
 struct BwdArgs {
     const float *x, *delta, *A, *B, *C, *h0, *gy, *ghT;
     float *dx, *ddelta, *dA, *dB, *dC, *dh0;
-    float *ckpt;               // (Bsz, nch, D, P) chunk-start states
+    float *ckpt;               // (Bsz, nch, D, NP) local state at each chunk start
+    float *spre;               // (Bsz, nch, D) sum of dl from the segment start to the chunk start
+    float *hl, *gl;            // (Bsz, K, D, NP) segment end state from zero; adjoint out of the segment from zero
+    float *sdl;                // (Bsz, K, D) the segment's sum of dl
+    float *hin, *gout;         // (Bsz, K, D, NP) the composed carries
     int64_t Bsz, L, D, N;
     int64_t nch;               // chunks of kBwdT steps
-    int P;                     // lanes per chain: power of two >= N, <= 32
-    int cpb;                   // chains per block = kBwdThreads / P
+    int64_t cps;               // chunks per segment
+    int K;                     // segments
     int softplus;
 };
-
-// Shared memory of one block, in floats.
-__host__ __device__ constexpr int64_t bwd_smem_floats(int P, int cpb)
-{
-    return 4 * int64_t(kBwdT) * cpb + 2 * int64_t(kBwdT) * P + 2 * int64_t(kBwdT) * kBwdWarps * P;
-}
 
 // sigmoid(u) = d softplus(u) / du. ex2 of a large argument gives +inf and
 // the quotient 0, the limit.
 __device__ __forceinline__ float bwd_sigmoid(float u)
 {
-    return 1.0f / (1.0f + ex2(-u * kLog2e));
+    return __fdividef(1.0f, 1.0f + ex2(-u * kLog2e));
 }
 
-// The raw per-timestep inputs of one chunk that this thread stages: it loads
-// them into registers one chunk ahead, so the loads are in flight while the
-// block works on the current chunk. Element j = threadIdx.x + r * kBwdThreads
-// of the chunk's (step, channel) rows and (step, state) rows.
-template <int P> struct BwdChunkRegs {
-    static constexpr int CPB = kBwdThreads / P;
+// Shared memory of the main kernel, in bytes: two buffers of a chunk's raw
+// inputs as they arrive (delta, x, gy per step and chain; B and C rows; each
+// thread's checkpoint and its chain's sum of dl), the cooked chunk (dl, x,
+// gy, sigmoid) per step and chain, dx and d delta per step and chain, and
+// the per-warp sums of the dB and dC terms.
+__host__ __device__ constexpr int bwd_main_smem(int P)
+{
+    return (2 * 3 * kBwdT * (kBwdThreads / P) + 2 * 2 * kBwdT * 4 * P + 2 * 4 * kBwdThreads + 2 * (kBwdThreads / P) +
+            kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * (kBwdThreads / P) + kBwdT * kBwdWarps * 2 * 4 * P) * 4;
+}
+__host__ __device__ constexpr int bwd_local_smem(int P)
+{
+    return (kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * 4 * P) * 4;
+}
+
+// The raw inputs of one chunk that this thread stages: loaded into registers
+// one chunk ahead, so the loads are in flight while the block works on the
+// current chunk. Element j = threadIdx.x + q * kBwdThreads of the chunk's
+// (step, chain) rows and (step, state) rows.
+template <int P> struct BwdRegs {
+    static constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
     static constexpr int RX = (kBwdT * CPB + kBwdThreads - 1) / kBwdThreads;
-    static constexpr int RB = (kBwdT * P + kBwdThreads - 1) / kBwdThreads;
-    float x[RX], u[RX], gy[RX], B[RB], C[RB];
+    static constexpr int RB = (kBwdT * NP + kBwdThreads - 1) / kBwdThreads;
+    float u[RX], x[RX], gy[RX], B[RB], C[RB];
 };
 
-// Loads chunk t0 .. t0 + kBwdT of batch row b for channels d0 .. d0 + CPB
-// (zeros beyond L, D and N). ADJ: also gy and C (the adjoint pass).
-template <int P, bool ADJ>
-__device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0, int64_t t0, BwdChunkRegs<P> &r)
+template <int P, bool WX, bool WGY, bool WB, bool WC>
+__device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0, int64_t t0, BwdRegs<P> &r)
 {
-    using R = BwdChunkRegs<P>;
+    using R = BwdRegs<P>;
 #pragma unroll
     for (int q = 0; q < R::RX; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
         const int i = j / R::CPB, c = j % R::CPB;
         const bool ok = j < kBwdT * R::CPB && t0 + i < a.L && d0 + c < a.D;
         const int64_t idx = (b * a.L + t0 + i) * a.D + d0 + c;
-        r.x[q] = ok ? __ldg(a.x + idx) : 0.0f;
         r.u[q] = ok ? __ldg(a.delta + idx) : 0.0f;
-        if (ADJ)
-            r.gy[q] = ok ? __ldg(a.gy + idx) : 0.0f;
+        if (WX) r.x[q] = ok ? __ldg(a.x + idx) : 0.0f;
+        if (WGY) r.gy[q] = ok ? __ldg(a.gy + idx) : 0.0f;
     }
 #pragma unroll
     for (int q = 0; q < R::RB; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
-        const int i = j / P, m = j % P;
-        const bool ok = j < kBwdT * P && t0 + i < a.L && m < a.N;
+        const int i = j / R::NP, m = j % R::NP;
+        const bool ok = j < kBwdT * R::NP && t0 + i < a.L && m < a.N;
         const int64_t idx = (b * a.L + t0 + i) * a.N + m;
-        r.B[q] = ok ? __ldg(a.B + idx) : 0.0f;
-        if (ADJ)
-            r.C[q] = ok ? __ldg(a.C + idx) : 0.0f;
+        if (WB) r.B[q] = ok ? __ldg(a.B + idx) : 0.0f;
+        if (WC) r.C[q] = ok ? __ldg(a.C + idx) : 0.0f;
     }
 }
 
-// Writes loaded inputs to the block's staging rows, with dl = softplus(u)
-// and its derivative when asked.
-template <int P, bool ADJ>
-__device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdChunkRegs<P> &r, float *s_x, float *s_dl,
-                                        float *s_sg, float *s_gy, float *s_B, float *s_C)
+// Writes the loaded chunk to shared memory: (dl, x, gy, sigmoid(u)) per step
+// and chain (dl = 0 past L), B and C rows.
+template <int P, bool WX, bool WGY, bool WB, bool WC>
+__device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P> &r, int64_t d0, int64_t t0, float4 *s_in,
+                                        float *s_B, float *s_C)
 {
-    using R = BwdChunkRegs<P>;
+    using R = BwdRegs<P>;
 #pragma unroll
     for (int q = 0; q < R::RX; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
         if (j < kBwdT * R::CPB) {
-            s_x[j] = r.x[q];
-            s_dl[j] = a.softplus ? softplus(r.u[q]) : r.u[q];
-            if (ADJ) {
-                s_sg[j] = a.softplus ? bwd_sigmoid(r.u[q]) : 1.0f;
-                s_gy[j] = r.gy[q];
-            }
+            const int i = j / R::CPB, c = j % R::CPB;
+            const bool ok = t0 + i < a.L && d0 + c < a.D;
+            const float dl = !ok ? 0.0f : (a.softplus ? softplus(r.u[q]) : r.u[q]);
+            const float sg = (ok && a.softplus && WX && WGY) ? bwd_sigmoid(r.u[q]) : 1.0f;
+            s_in[j] = make_float4(dl, WX ? r.x[q] : 0.0f, WGY ? r.gy[q] : 0.0f, sg);
         }
     }
 #pragma unroll
     for (int q = 0; q < R::RB; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
-        if (j < kBwdT * P) {
-            s_B[j] = r.B[q];
-            if (ADJ)
-                s_C[j] = r.C[q];
+        if (j < kBwdT * R::NP) {
+            if (WB) s_B[j] = r.B[q];
+            if (WC) s_C[j] = r.C[q];
         }
     }
 }
 
-// Reduce-scatter of v[0 .. T) over the P lanes of a lane group (recursive
-// halving). Lane n of the group ends with, for P <= T, the sums of entries
-// n*T/P .. (n+1)*T/P - 1 in v[0 .. T/P); for P > T, the sum of entry
-// n / (P/T) in v[0].
-template <int O, int M, int T> struct GroupReduceScatter {
-    __device__ __forceinline__ static void run(float (&v)[T], int n)
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// Asynchronous copies global -> shared (cp.async): 4 or 16 bytes, zeros
+// instead when !ok (no byte is read then).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool ok)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(ok ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool ok)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+}
+// A shared-memory load the compiler must issue where it stands: the adjoint
+// reads its step's inputs afresh, so that the recomputation's decays are not
+// kept alive in registers across the chunk.
+__device__ __forceinline__ float4 lds4_fresh(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+    return v;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ float2 ex2v(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+
+// Reduce-scatter of v[0 .. 8) over the chains of a warp (lanes that differ in
+// bits O, O/2, .., P of the lane index; recursive halving while more than
+// one value is left, plain sums after). A lane ends with the sums of
+// max(1, 8 P / 32) consecutive entries, starting at the entry its lane bits
+// select (bwd_rs_first).
+template <int O, int P, int M> struct ChainReduceScatter {
+    __device__ __forceinline__ static void run(float (&v)[8], int lane)
     {
-        if constexpr (O >= 1) {
+        if constexpr (O >= P) {
             if constexpr (M > 1) {
-                const bool up = (n & O) != 0;
+                const bool up = (lane & O) != 0;
 #pragma unroll
                 for (int j = 0; j < M / 2; ++j) {
                     const float keep = up ? v[j + M / 2] : v[j];
                     const float send = up ? v[j] : v[j + M / 2];
                     v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
                 }
-                GroupReduceScatter<O / 2, M / 2, T>::run(v, n);
+                ChainReduceScatter<O / 2, P, M / 2>::run(v, lane);
             } else {
                 v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-                GroupReduceScatter<O / 2, 1, T>::run(v, n);
+                ChainReduceScatter<O / 2, P, 1>::run(v, lane);
             }
         }
     }
 };
 
-// The state recurrence over one staged chunk (forward pass).
-template <int P, bool TAIL>
-__device__ __forceinline__ float bwd_fwd_chunk(float h, float A2, int64_t t0, int64_t L, int n, int c,
-                                               const float *s_x, const float *s_dl, const float *s_B)
+template <int P> __device__ __forceinline__ int bwd_rs_first(int lane)
 {
-    constexpr int CPB = kBwdThreads / P;
-#pragma unroll
-    for (int i = 0; i < kBwdT; ++i) {
-        if (!TAIL || t0 + i < L) {
-            const float dl = s_dl[i * CPB + c];
-            h = fmaf(ex2(dl * A2), h, dl * s_B[i * P + n] * s_x[i * CPB + c]);
-        }
-    }
-    return h;
+    int f = (lane & 16) ? 4 : 0;
+    if (P <= 8 && (lane & 8)) f += 2;
+    if (P <= 4 && (lane & 4)) f += 1;
+    return f;
+}
+// Lanes that hold a copy of another lane's sums after the plain levels.
+template <int P> __device__ __forceinline__ bool bwd_rs_writer(int lane)
+{
+    return (lane & (3 & ~(P - 1))) == 0;
 }
 
-// One staged chunk of the adjoint pass: recompute its states and decays from
-// hs, run the adjoint g back through them, write dx and d delta, leave the
-// chain-group sums of the dB and dC terms in s_pB / s_pC, and return the
-// chunk's dA term.
-template <int P, bool TAIL>
-__device__ __forceinline__ float bwd_adj_chunk(const BwdArgs &a, float &g, float hs, float An, float A2,
-                                               int64_t b, int64_t d, bool chain, int64_t t0, int n, int c,
-                                               int lane, int warp, const float *s_x, const float *s_dl,
-                                               const float *s_sg, const float *s_gy, const float *s_B,
-                                               const float *s_C, float *s_pB, float *s_pC)
-{
-    constexpr int CPB = kBwdThreads / P;
-    const int64_t L = a.L;
-    float hc[kBwdT], ac[kBwdT];
-    float hh = hs;
-#pragma unroll
-    for (int i = 0; i < kBwdT; ++i) {
-        hc[i] = 0.0f;
-        ac[i] = 1.0f;
-        if (!TAIL || t0 + i < L) {
-            const float dl = s_dl[i * CPB + c];
-            const float av = ex2(dl * A2);
-            hh = fmaf(av, hh, dl * s_B[i * P + n] * s_x[i * CPB + c]);
-            hc[i] = hh;
-            ac[i] = av;
-        }
-    }
-
-    float gx[kBwdT], gdl[kBwdT];
-    float dAk = 0.0f;
-#pragma unroll
-    for (int i = kBwdT - 1; i >= 0; --i) {
-        gx[i] = 0.0f;
-        gdl[i] = 0.0f;
-        if (!TAIL || t0 + i < L) {                 // uniform over the block
-            const float dl = s_dl[i * CPB + c], xv = s_x[i * CPB + c], gyv = s_gy[i * CPB + c];
-            const float Bn = s_B[i * P + n], Cn = s_C[i * P + n];
-            g = fmaf(gyv, Cn, g);                          // y_t reads h_t
-            float pC = gyv * hc[i];
-            const float hp = i > 0 ? hc[i - 1] : hs;       // h_{t-1}
-            const float dan = g * hp * ac[i];
-            gdl[i] = fmaf(dan, An, g * Bn * xv);
-            dAk = fmaf(dan, dl, dAk);
-            float pB = g * dl * xv;
-            gx[i] = g * dl * Bn;
-            g *= ac[i];                                    // into h_{t-1}
-#pragma unroll
-            for (int off = P; off < 32; off <<= 1) {
-                pB += __shfl_xor_sync(0xffffffffu, pB, off);
-                pC += __shfl_xor_sync(0xffffffffu, pC, off);
-            }
-            if (lane < P) {
-                s_pB[(i * kBwdWarps + warp) * P + lane] = pB;
-                s_pC[(i * kBwdWarps + warp) * P + lane] = pC;
-            }
-        }
-    }
-
-    // dx and d delta: sums over the P states of the chain, one step per lane
-    GroupReduceScatter<P / 2, kBwdT, kBwdT>::run(gx, n);
-    GroupReduceScatter<P / 2, kBwdT, kBwdT>::run(gdl, n);
-    if constexpr (P <= kBwdT) {
-        constexpr int S = kBwdT / P;
-#pragma unroll
-        for (int q = 0; q < S; ++q) {
-            const int i = n * S + q;
-            if (chain && (!TAIL || t0 + i < L)) {
-                const int64_t idx = (b * L + t0 + i) * a.D + d;
-                a.dx[idx] = gx[q];
-                a.ddelta[idx] = gdl[q] * s_sg[i * CPB + c];
-            }
-        }
-    } else {
-        constexpr int R = P / kBwdT;
-        const int i = n / R;
-        if (chain && n % R == 0 && (!TAIL || t0 + i < L)) {
-            const int64_t idx = (b * L + t0 + i) * a.D + d;
-            a.dx[idx] = gx[0];
-            a.ddelta[idx] = gdl[0] * s_sg[i * CPB + c];
-        }
-    }
-    return dAk;
-}
-
-// grid (ceil(D / CPB), Bsz), kBwdThreads threads,
-// bwd_smem_floats(P, CPB) * 4 bytes of dynamic shared memory.
-// dA, dB and dC must be zero on entry (they are accumulated atomically).
+// ---------------------------------------------------------------- kernel 1
+// grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_local_smem(P) bytes.
 template <int P>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(BwdArgs a)
+__global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs a)
 {
-    constexpr int CPB = kBwdThreads / P;
-    extern __shared__ float bwd_smem[];
-    float *s_x = bwd_smem;
-    float *s_dl = s_x + kBwdT * CPB;
-    float *s_sg = s_dl + kBwdT * CPB;
-    float *s_gy = s_sg + kBwdT * CPB;
-    float *s_B = s_gy + kBwdT * CPB;
-    float *s_C = s_B + kBwdT * P;
-    float *s_pB = s_C + kBwdT * P;              // [kBwdT][kBwdWarps][P]
-    float *s_pC = s_pB + kBwdT * kBwdWarps * P;
+    constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
+    extern __shared__ float4 bwd_smem4[];
+    float4 *s_in = bwd_smem4;
+    float *s_B = reinterpret_cast<float *>(s_in + kBwdT * CPB);
+    float *s_C = s_B + kBwdT * NP;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = tid % P, c = tid / P;
-    const int64_t b = blockIdx.y;
-    const int64_t d0 = int64_t(blockIdx.x) * CPB, d = d0 + c;
-    const bool chain = d < a.D;                 // this lane's chain exists
-    const bool act = chain && n < a.N;          // ... and its state index too
+    const int tid = threadIdx.x, j = tid % P, c = tid / P;
+    const int64_t b = blockIdx.y, k = blockIdx.z;
+    const int64_t d0 = (int64_t)blockIdx.x * CPB, d = d0 + c;
+    const bool chain = d < a.D;
     const int64_t L = a.L, D = a.D, N = a.N, nch = a.nch;
-
-    const float An = act ? __ldg(a.A + d * N + n) : 0.0f;
-    const float A2 = An * kLog2e;
-    BwdChunkRegs<P> r;
-
-    // 1. forward pass: the state at the start of every chunk
-    float h = (act && a.h0) ? __ldg(a.h0 + (b * D + d) * N + n) : 0.0f;
-    bwd_load<P, false>(a, b, d0, 0, r);
-    for (int64_t k = 0; k < nch; ++k) {
-        const int64_t t0 = k * kBwdT;
-        bwd_put<P, false>(a, r, s_x, s_dl, s_sg, s_gy, s_B, s_C);
-        if (chain)
-            a.ckpt[((b * nch + k) * D + d) * P + n] = h;
-        if (k + 1 < nch)
-            bwd_load<P, false>(a, b, d0, t0 + kBwdT, r);
-        __syncthreads();
-        if (t0 + kBwdT <= L)
-            h = bwd_fwd_chunk<P, false>(h, A2, t0, L, n, c, s_x, s_dl, s_B);
-        else
-            h = bwd_fwd_chunk<P, true>(h, A2, t0, L, n, c, s_x, s_dl, s_B);
-        __syncthreads();
-    }
-
-    // 2. the chunks last to first: recompute, then run the adjoint back
-    float g = (act && a.ghT) ? __ldg(a.ghT + (b * D + d) * N + n) : 0.0f;
-    float dAacc = 0.0f;
-    bwd_load<P, true>(a, b, d0, (nch - 1) * kBwdT, r);
-    float hs_next = chain ? a.ckpt[((b * nch + nch - 1) * D + d) * P + n] : 0.0f;
-    for (int64_t k = nch - 1; k >= 0; --k) {
-        const int64_t t0 = k * kBwdT;
-        bwd_put<P, true>(a, r, s_x, s_dl, s_sg, s_gy, s_B, s_C);
-        const float hs = hs_next;
-        if (k > 0) {
-            bwd_load<P, true>(a, b, d0, t0 - kBwdT, r);
-            hs_next = chain ? a.ckpt[((b * nch + k - 1) * D + d) * P + n] : 0.0f;
-        }
-        __syncthreads();
-        if (t0 + kBwdT <= L)
-            dAacc += bwd_adj_chunk<P, false>(a, g, hs, An, A2, b, d, chain, t0, n, c, lane, warp, s_x, s_dl, s_sg,
-                                             s_gy, s_B, s_C, s_pB, s_pC);
-        else
-            dAacc += bwd_adj_chunk<P, true>(a, g, hs, An, A2, b, d, chain, t0, n, c, lane, warp, s_x, s_dl, s_sg,
-                                            s_gy, s_B, s_C, s_pB, s_pC);
-        __syncthreads();
-        for (int j = tid; j < kBwdT * N; j += kBwdThreads) {
-            const int i = j / int(N), m = j - i * int(N);
-            const int64_t t = t0 + i;
-            if (t < L) {
-                float sB = 0.0f, sC = 0.0f;
+    float2 A2[2];
 #pragma unroll
-                for (int w = 0; w < kBwdWarps; ++w) {
-                    sB += s_pB[(i * kBwdWarps + w) * P + m];
-                    sC += s_pC[(i * kBwdWarps + w) * P + m];
-                }
-                atomicAdd(a.dB + (b * L + t) * N + m, sB);
-                atomicAdd(a.dC + (b * L + t) * N + m, sC);
-            }
+    for (int e = 0; e < 2; ++e) {
+        const int n0 = kBwdS * j + 2 * e;
+        A2[e].x = (chain && n0 < N) ? __ldg(a.A + d * N + n0) * kLog2e : 0.0f;
+        A2[e].y = (chain && n0 + 1 < N) ? __ldg(a.A + d * N + n0 + 1) * kLog2e : 0.0f;
+    }
+    const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
+    const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
+
+    // Forward from a zero state: checkpoints, end state, sum of dl (chunk
+    // sums added with compensation).
+    float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float S = 0.0f, Sc = 0.0f;
+    BwdRegs<P> r;
+    bwd_load<P, true, false, true, false>(a, b, d0, ci0 * kBwdT, r);
+    for (int64_t ci = ci0; ci < ci1; ++ci) {
+        __syncthreads();
+        bwd_put<P, true, false, true, false>(a, r, d0, ci * kBwdT, s_in, s_B, s_C);
+        if (ci + 1 < ci1)
+            bwd_load<P, true, false, true, false>(a, b, d0, (ci + 1) * kBwdT, r);
+        if (chain) {
+            const int64_t o = (b * nch + ci) * D + d;
+            *reinterpret_cast<float4 *>(a.ckpt + o * NP + kBwdS * j) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+            if (j == 0)
+                a.spre[o] = S;
+        }
+        __syncthreads();
+        float sc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kBwdT; ++i) {
+            const float4 in = s_in[i * CPB + c];
+            const float4 B4 = *reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j);
+            const float dl = in.x, u = dl * in.y;
+            const float2 dl2 = f2(dl), u2 = f2(u);
+            h[0] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
+            h[1] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
+            sc += dl;
+        }
+        const float yk = sc - Sc, tk = S + yk;   // S += sc, compensated
+        Sc = (tk - S) - yk;
+        S = tk;
+    }
+    if (chain) {
+        *reinterpret_cast<float4 *>(a.hl + pair) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+        if (j == 0)
+            a.sdl[(b * a.K + k) * D + d] = S;
+    }
+    if (k == 0)
+        return;   // nothing lies before the first segment
+
+    // Adjoint from zero at the segment's end back to its start.
+    float2 g[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    bwd_load<P, false, true, false, true>(a, b, d0, (ci1 - 1) * kBwdT, r);
+    for (int64_t ci = ci1 - 1; ci >= ci0; --ci) {
+        __syncthreads();
+        bwd_put<P, false, true, false, true>(a, r, d0, ci * kBwdT, s_in, s_B, s_C);
+        if (ci > ci0)
+            bwd_load<P, false, true, false, true>(a, b, d0, (ci - 1) * kBwdT, r);
+        __syncthreads();
+#pragma unroll
+        for (int i = kBwdT - 1; i >= 0; --i) {
+            const float4 in = s_in[i * CPB + c];
+            const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
+            const float2 dl2 = f2(in.x), gy2 = f2(in.z);
+            g[0] = __fmul2_rn(ex2v(__fmul2_rn(dl2, A2[0])), __ffma2_rn(gy2, make_float2(C4.x, C4.y), g[0]));
+            g[1] = __fmul2_rn(ex2v(__fmul2_rn(dl2, A2[1])), __ffma2_rn(gy2, make_float2(C4.z, C4.w), g[1]));
         }
     }
-    if (act) {
-        atomicAdd(a.dA + d * N + n, dAacc);
-        if (a.dh0)
-            a.dh0[(b * D + d) * N + n] = g;
+    if (chain)
+        *reinterpret_cast<float4 *>(a.gl + pair) = make_float4(g[0].x, g[0].y, g[1].x, g[1].y);
+}
+
+// ---------------------------------------------------------------- kernel 2
+// One thread per (b, d, n < NP); grid-stride.
+__global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
+{
+    const int64_t total = a.Bsz * a.D * NP;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int n = (int)(e % NP);
+        const int64_t bd = e / NP, d = bd % a.D, b = bd / a.D;
+        const bool st = n < a.N;
+        const float A2 = st ? __ldg(a.A + d * a.N + n) * kLog2e : 0.0f;
+        float h = (st && a.h0) ? __ldg(a.h0 + bd * a.N + n) : 0.0f;
+        for (int k = 0; k < a.K; ++k) {
+            const int64_t s = (b * a.K + k) * a.D + d, idx = s * NP + n;
+            a.hin[idx] = h;
+            h = fmaf(ex2(A2 * a.sdl[s]), h, a.hl[idx]);
+        }
+        float g = (st && a.ghT) ? __ldg(a.ghT + bd * a.N + n) : 0.0f;
+        for (int k = a.K - 1; k >= 0; --k) {
+            const int64_t s = (b * a.K + k) * a.D + d, idx = s * NP + n;
+            a.gout[idx] = g;
+            if (k > 0)
+                g = fmaf(ex2(A2 * a.sdl[s]), g, a.gl[idx]);
+        }
     }
 }
 
-// ---- host side: the launch shape and the launch --------------------------
+// ---------------------------------------------------------------- kernel 3
+// grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_main_smem(P) bytes.
+// dA, dB and dC must be zero on entry (they are accumulated atomically).
+// Chunk inputs arrive by cp.async into one of two raw buffers while the
+// block works on the other, so no register holds a chunk in flight.
+template <int P>
+__global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs a)
+{
+    constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
+    constexpr int TC = kBwdT * CPB, TN = kBwdT * NP;
+    constexpr int RS = (8 * P / 32) > 1 ? 8 * P / 32 : 1;   // reduce-scatter values left per lane
+    extern __shared__ float4 bwd_smem4[];
+    float4 *s_ck = bwd_smem4;                       // [2][kBwdThreads] checkpoints
+    float4 *s_in = s_ck + 2 * kBwdThreads;          // [T][CPB] (dl, x, gy, sigmoid)
+    float *s_raw = reinterpret_cast<float *>(s_in + TC);   // [2][3][T][CPB] delta, x, gy
+    float *s_rB = s_raw + 2 * 3 * TC;               // [2][T][NP]
+    float *s_rC = s_rB + 2 * TN;
+    float *s_sp = s_rC + 2 * TN;                    // [2][CPB]
+    float *s_dx = s_sp + 2 * CPB;                   // [T][CPB]
+    float *s_dd = s_dx + TC;
+    float *s_part = s_dd + TC;                      // [T][warps][2][NP]
 
-// The checkpoint workspace of a call is Bsz * nch * D * P floats.
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, j = tid % P, c = tid / P;
+    const int64_t b = blockIdx.y, k = blockIdx.z;
+    const int64_t d0 = (int64_t)blockIdx.x * CPB, d = d0 + c;
+    const bool chain = d < a.D;
+    const int64_t L = a.L, D = a.D, N = a.N, nch = a.nch;
+    float2 A2[2], An[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int n0 = kBwdS * j + 2 * e;
+        An[e].x = (chain && n0 < N) ? __ldg(a.A + d * N + n0) : 0.0f;
+        An[e].y = (chain && n0 + 1 < N) ? __ldg(a.A + d * N + n0 + 1) : 0.0f;
+        A2[e] = __fmul2_rn(An[e], f2(kLog2e));
+    }
+    const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
+    const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
+    float2 hin[2], g[2], dA[2];
+    {
+        const float4 hv = chain ? *reinterpret_cast<const float4 *>(a.hin + pair) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 gv = chain ? *reinterpret_cast<const float4 *>(a.gout + pair) : make_float4(0.f, 0.f, 0.f, 0.f);
+        hin[0] = make_float2(hv.x, hv.y);
+        hin[1] = make_float2(hv.z, hv.w);
+        g[0] = make_float2(gv.x, gv.y);
+        g[1] = make_float2(gv.z, gv.w);
+        dA[0] = dA[1] = make_float2(0.f, 0.f);
+    }
+
+    // Issues the copies of chunk ci into raw buffer s.
+    auto stage = [&](int64_t ci, int sb) {
+        const int64_t t0 = ci * kBwdT;
+        float *ru = s_raw + (sb * 3) * TC, *rx = ru + TC, *rg = rx + TC;
+        for (int e = tid; e < TC; e += kBwdThreads) {
+            const int i = e / CPB, cc = e % CPB;
+            const bool ok = t0 + i < L && d0 + cc < D;
+            const int64_t idx = ok ? (b * L + t0 + i) * D + d0 + cc : 0;
+            cp_async4(ru + e, a.delta + idx, ok);
+            cp_async4(rx + e, a.x + idx, ok);
+            cp_async4(rg + e, a.gy + idx, ok);
+        }
+        for (int e = tid; e < TN; e += kBwdThreads) {
+            const int i = e / NP, m = e % NP;
+            const bool ok = t0 + i < L && m < N;
+            const int64_t idx = ok ? (b * L + t0 + i) * N + m : 0;
+            cp_async4(s_rB + sb * TN + e, a.B + idx, ok);
+            cp_async4(s_rC + sb * TN + e, a.C + idx, ok);
+        }
+        const int64_t o = (b * nch + ci) * D + d;
+        cp_async16(s_ck + sb * kBwdThreads + tid, a.ckpt + (chain ? o * NP + kBwdS * j : 0), chain);
+        if (j == 0)
+            cp_async4(s_sp + sb * CPB + c, a.spre + (chain ? o : 0), chain);
+        cp_async_commit();
+    };
+
+    stage(ci1 - 1, (int)((ci1 - 1) & 1));
+    for (int64_t ci = ci1 - 1; ci >= ci0; --ci) {
+        const int64_t t0 = ci * kBwdT;
+        const int cur = (int)(ci & 1);
+        cp_async_wait_all();
+        __syncthreads();   // the chunk has landed; the one before is done with s_in
+        if (ci > ci0)
+            stage(ci - 1, cur ^ 1);
+        {
+            const float *ru = s_raw + (cur * 3) * TC, *rx = ru + TC, *rg = rx + TC;
+            for (int e = tid; e < TC; e += kBwdThreads) {
+                const int i = e / CPB, cc = e % CPB;
+                const bool ok = t0 + i < L && d0 + cc < D;
+                const float u = ru[e];
+                const float dl = !ok ? 0.0f : (a.softplus ? softplus(u) : u);
+                const float sg = (ok && a.softplus) ? bwd_sigmoid(u) : 1.0f;
+                s_in[e] = make_float4(dl, rx[e], rg[e], sg);
+            }
+        }
+        __syncthreads();
+        const float *s_B = s_rB + cur * TN, *s_C = s_rC + cur * TN;
+
+        // The chunk's states: from the true state at its start.
+        float2 hs[kBwdT][2];
+        {
+            const float4 ck = s_ck[cur * kBwdThreads + tid];
+            const float2 sp2 = f2(s_sp[cur * CPB + c]);
+            float2 h0v = __ffma2_rn(ex2v(__fmul2_rn(sp2, A2[0])), hin[0], make_float2(ck.x, ck.y));
+            float2 h1v = __ffma2_rn(ex2v(__fmul2_rn(sp2, A2[1])), hin[1], make_float2(ck.z, ck.w));
+#pragma unroll
+            for (int i = 0; i < kBwdT; ++i) {
+                const float4 in = s_in[i * CPB + c];
+                const float4 B4 = *reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j);
+                const float2 dl2 = f2(in.x), u2 = f2(in.x * in.y);
+                h0v = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h0v, __fmul2_rn(u2, make_float2(B4.x, B4.y)));
+                h1v = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h1v, __fmul2_rn(u2, make_float2(B4.z, B4.w)));
+                hs[i][0] = h0v;
+                hs[i][1] = h1v;
+            }
+        }
+
+        // The adjoint back through the chunk.
+#pragma unroll
+        for (int i = kBwdT - 1; i >= 0; --i) {
+            const float4 in = lds4_fresh(s_in + i * CPB + c);
+            const float4 B4 = lds4_fresh(reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j));
+            const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
+            const float dl = in.x, xv = in.y, gyv = in.z, sg = in.w, u = dl * xv;
+            const float2 dl2 = f2(dl), u2 = f2(u), gy2 = f2(gyv), nu2 = f2(-u);
+            const float2 Bp[2] = {make_float2(B4.x, B4.y), make_float2(B4.z, B4.w)};
+            const float2 Cp[2] = {make_float2(C4.x, C4.y), make_float2(C4.z, C4.w)};
+            float2 pB[2], pC[2], sdl2 = make_float2(0.f, 0.f), sgb2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                g[e] = __ffma2_rn(gy2, Cp[e], g[e]);                    // dLoss/dh_t
+                pC[e] = __fmul2_rn(gy2, hs[i][e]);
+                const float2 dan = __fmul2_rn(g[e], __ffma2_rn(nu2, Bp[e], hs[i][e]));   // g a_t h_{t-1}
+                sdl2 = __ffma2_rn(dan, An[e], sdl2);
+                sgb2 = __ffma2_rn(g[e], Bp[e], sgb2);
+                dA[e] = __ffma2_rn(dan, dl2, dA[e]);
+                pB[e] = __fmul2_rn(g[e], u2);
+                g[e] = __fmul2_rn(g[e], ex2v(__fmul2_rn(dl2, A2[e])));  // into h_{t-1}
+            }
+            // dx and d delta: the chain's sums over n
+            float sdl = sdl2.x + sdl2.y, sgb = sgb2.x + sgb2.y;
+#pragma unroll
+            for (int o = 1; o < P; o <<= 1) {
+                sdl += __shfl_xor_sync(0xffffffffu, sdl, o);
+                sgb += __shfl_xor_sync(0xffffffffu, sgb, o);
+            }
+            if (j == 0) {
+                s_dx[i * CPB + c] = sgb * dl;
+                s_dd[i * CPB + c] = fmaf(xv, sgb, sdl) * sg;
+            }
+            // dB and dC: sums over the warp's chains
+            float v[8] = {pB[0].x, pB[0].y, pB[1].x, pB[1].y, pC[0].x, pC[0].y, pC[1].x, pC[1].y};
+            ChainReduceScatter<16, P, 8>::run(v, lane);
+            if (bwd_rs_writer<P>(lane)) {
+                const int f = bwd_rs_first<P>(lane);
+#pragma unroll
+                for (int q = 0; q < RS; ++q) {
+                    const int vi = f + q, kind = vi >> 2, n = kBwdS * j + (vi & 3);
+                    s_part[((i * kBwdWarps + warp) * 2 + kind) * NP + n] = v[q];
+                }
+            }
+        }
+        __syncthreads();
+
+        // The chunk's outputs: dx and d delta rows, the block's dB and dC.
+        for (int e = tid; e < TC; e += kBwdThreads) {
+            const int i = e / CPB, cc = e % CPB;
+            const int64_t t = t0 + i, dd = d0 + cc;
+            if (t < L && dd < D) {
+                const int64_t idx = (b * L + t) * D + dd;
+                a.dx[idx] = s_dx[e];
+                a.ddelta[idx] = s_dd[e];
+            }
+        }
+        for (int e = tid; e < kBwdT * 2 * NP; e += kBwdThreads) {
+            const int i = e / (2 * NP), rem = e % (2 * NP), kind = rem / NP, n = rem % NP;
+            const int64_t t = t0 + i;
+            if (t < L && n < N) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kBwdWarps; ++w)
+                    sum += s_part[(i * kBwdWarps + w) * 2 * NP + rem];
+                atomicAdd((kind ? a.dC : a.dB) + (b * L + t) * N + n, sum);
+            }
+        }
+    }
+    if (chain) {
+        const float dv[4] = {dA[0].x, dA[0].y, dA[1].x, dA[1].y}, gv[4] = {g[0].x, g[0].y, g[1].x, g[1].y};
+#pragma unroll
+        for (int e = 0; e < kBwdS; ++e) {
+            const int64_t n = kBwdS * j + e;
+            if (n < N) {
+                atomicAdd(a.dA + d * N + n, dv[e]);
+                if (k == 0 && a.dh0)
+                    a.dh0[(b * D + d) * N + n] = gv[e];
+            }
+        }
+    }
+}
+
+// ---- host side: the launch shape and the launches -------------------------
+
 struct BwdShape {
-    int P;           // lanes per chain
+    int P;           // threads per chain
+    int NP;          // padded states per chain (kBwdS * P)
     int cpb;         // chains per block
     int64_t nch;     // chunks of kBwdT steps
+    int64_t cps;     // chunks per segment
+    int K;           // segments
     int64_t gx;      // blocks along D
-    size_t smem;     // dynamic shared memory per block, bytes
 };
 
-inline BwdShape bwd_shape(int64_t L, int64_t D, int64_t N)
+// Segments: as many as fill the resident blocks of the main kernel in one
+// wave, each at least 4 chunks long.
+inline BwdShape bwd_shape(int64_t Bsz, int64_t L, int64_t D, int64_t N, int resident_blocks)
 {
     BwdShape s;
     s.P = 1;
-    while (s.P < N) s.P <<= 1;
+    while (s.P * kBwdS < N) s.P <<= 1;
+    s.NP = kBwdS * s.P;
     s.cpb = kBwdThreads / s.P;
     s.nch = (L + kBwdT - 1) / kBwdT;
     s.gx = (D + s.cpb - 1) / s.cpb;
-    s.smem = (size_t)bwd_smem_floats(s.P, s.cpb) * 4;
+    int64_t K = 1;
+    const int64_t cols = s.gx * Bsz;
+    if (cols > 0 && cols < resident_blocks) K = resident_blocks / cols;
+    const int64_t maxK = (s.nch + 3) / 4;
+    if (K > maxK) K = maxK;
+    if (K > 65535) K = 65535;
+    if (K < 1) K = 1;
+    s.cps = (s.nch + K - 1) / K;
+    if (s.cps < 1) s.cps = 1;
+    s.K = (int)((s.nch + s.cps - 1) / s.cps);
+    if (s.K < 1) s.K = 1;
     return s;
 }
 
-// a.P, a.cpb and a.nch are filled in from s; grid (s.gx, Bsz).
+// The three launches; bwd_prepare(P) must have run on this device.
+template <int P>
+inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_t st)
+{
+    const dim3 grid((unsigned)s.gx, (unsigned)a.Bsz, (unsigned)s.K);
+    bwd_local_kernel<P><<<grid, kBwdThreads, bwd_local_smem(P), st>>>(a);
+    const int64_t carry = a.Bsz * a.D * s.NP;
+    const unsigned cb = (unsigned)((carry + 255) / 256 < 65536 ? (carry + 255) / 256 : 65536);
+    bwd_carry_kernel<<<cb, 256, 0, st>>>(a, s.NP);
+    bwd_main_kernel<P><<<grid, kBwdThreads, bwd_main_smem(P), st>>>(a);
+    return cudaGetLastError();
+}
+
 inline cudaError_t launch_scan_bwd(BwdArgs a, const BwdShape &s, cudaStream_t st)
 {
-    a.P = s.P;
-    a.cpb = s.cpb;
     a.nch = s.nch;
-    void (*kern)(BwdArgs);
+    a.cps = s.cps;
+    a.K = s.K;
     switch (s.P) {
-    case 1: kern = scan_bwd_kernel<1>; break;
-    case 2: kern = scan_bwd_kernel<2>; break;
-    case 4: kern = scan_bwd_kernel<4>; break;
-    case 8: kern = scan_bwd_kernel<8>; break;
-    case 16: kern = scan_bwd_kernel<16>; break;
-    default: kern = scan_bwd_kernel<32>; break;
+    case 1: return launch_bwd_p<1>(a, s, st);
+    case 2: return launch_bwd_p<2>(a, s, st);
+    case 4: return launch_bwd_p<4>(a, s, st);
+    default: return launch_bwd_p<8>(a, s, st);
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s.smem);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)s.gx, (unsigned)a.Bsz), kBwdThreads, s.smem, st>>>(a);
-    return cudaGetLastError();
+}
+
+// Sets the kernels' shared-memory limits for threads-per-chain P and returns
+// how many blocks of the main kernel are resident per SM (0 on error).
+template <int P>
+inline int bwd_prepare_p()
+{
+    if (cudaFuncSetAttribute(bwd_main_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_main_smem(P)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(bwd_local_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_local_smem(P)) !=
+            cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<P>, kBwdThreads, bwd_main_smem(P)) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+inline int bwd_prepare(int P)
+{
+    switch (P) {
+    case 1: return bwd_prepare_p<1>();
+    case 2: return bwd_prepare_p<2>();
+    case 4: return bwd_prepare_p<4>();
+    default: return bwd_prepare_p<8>();
+    }
 }
 
 } // namespace selscan

@@ -1,5 +1,5 @@
-// selscan_bwd.cu -- the backward pass: scan_bwd_kernel (scan_bwd.cuh), its
-// argument checks, checkpoint workspace and launch.
+// selscan_bwd.cu -- the backward pass: the kernels of scan_bwd.cuh, their
+// argument checks, workspace and launches.
 #include <cstring>
 
 #include "host_common.h"
@@ -66,30 +66,49 @@ extern "C" int selscan_bwd(const float *x, const float *delta, const float *A, c
         (e = cudaMemsetAsync(dC, 0, (size_t)nln * 4, st)) != cudaSuccess)
         return cuda_fail(e, "dB, dC zero fill");
 
-    const BwdShape shape = bwd_shape(L, D, N);
-    int64_t ckpt_floats;
-    if (!mul_ok(Bsz * shape.nch, D, shape.P, &ckpt_floats))
-        return fail(SELSCAN_ERR_INVALID_ARG, "checkpoint workspace size overflows");
-    if (shape.gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
-
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc != SELSCAN_OK) return rc;
+    int P = 1;
+    while (P * kBwdS < N) P <<= 1;
+    const int per_sm = bwd_prepare(P);
+    if (per_sm <= 0) {
+        cudaGetLastError();
+        return fail(SELSCAN_ERR_CUDA, "backward kernels: shared-memory limit or occupancy query failed");
+    }
+    const BwdShape shape = bwd_shape(Bsz, L, D, N, sms * per_sm);
+    if (shape.gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
+
+    // Workspace: checkpoints (Bsz, nch, D, NP) and their sums of dl
+    // (Bsz, nch, D); per segment hl, gl, h_in, g_out (Bsz, K, D, NP) and the
+    // sum of dl (Bsz, K, D). Each array starts on a 256-byte boundary.
+    int64_t ck, sp, seg, sdl;
+    if (!mul_ok(Bsz * shape.nch, D, shape.NP, &ck) || !mul_ok(Bsz, shape.nch, D, &sp) ||
+        !mul_ok(Bsz * shape.K, D, shape.NP, &seg) || !mul_ok(Bsz, shape.K, D, &sdl))
+        return fail(SELSCAN_ERR_INVALID_ARG, "backward workspace size overflows");
+    auto up = [](int64_t floats) { return ((size_t)floats * 4 + 255) & ~(size_t)255; };
+    const size_t total = up(ck) + up(sp) + 4 * up(seg) + up(sdl);
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
     void *ws = nullptr;
-    e = cudaMallocFromPoolAsync(&ws, (size_t)ckpt_floats * 4, pool, st);
+    e = cudaMallocFromPoolAsync(&ws, total, pool, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SELSCAN_ERR_NO_MEMORY, "checkpoint workspace of %lld bytes: %s", (long long)ckpt_floats * 4,
-                    cudaGetErrorString(e));
+        return fail(SELSCAN_ERR_NO_MEMORY, "backward workspace of %zu bytes: %s", total, cudaGetErrorString(e));
     }
     BwdArgs a;
     memset(&a, 0, sizeof a);
     a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.h0 = h0; a.gy = dy; a.ghT = dhT;
     a.dx = dx; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dh0 = dh0;
-    a.ckpt = static_cast<float *>(ws);
+    char *w = static_cast<char *>(ws);
+    a.ckpt = reinterpret_cast<float *>(w); w += up(ck);
+    a.spre = reinterpret_cast<float *>(w); w += up(sp);
+    a.hl = reinterpret_cast<float *>(w); w += up(seg);
+    a.gl = reinterpret_cast<float *>(w); w += up(seg);
+    a.hin = reinterpret_cast<float *>(w); w += up(seg);
+    a.gout = reinterpret_cast<float *>(w); w += up(seg);
+    a.sdl = reinterpret_cast<float *>(w);
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.softplus = delta_softplus ? 1 : 0;
     e = launch_scan_bwd(a, shape, st);

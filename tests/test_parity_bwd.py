@@ -1,10 +1,12 @@
 """selscan_bwd: the backward pass of the scan against the fp64 oracle's
 reverse sweep, on the same fp32 inputs and upstream gradients. Covers one
-and many 32-step chunks with ragged tails, channel counts that leave the
-last block partly empty, every lane-group width (N = 1, 2, 3 to 4, 5 to 8,
-16, 32), with and without softplus, h0 and dhT, the empty sequence, the
-130M-like layer at full size, and autograd through the differentiable
-wrapper."""
+and many 16-step chunks with ragged tails, one segment and many (the
+sequence is cut into segments whose carries are composed in both
+directions), channel counts that leave the last block partly empty, every
+width of a chain (1, 2, 4 and 8 threads of four states: N = 1 to 4, 5 to 8,
+9 to 16, 17 to 32), with and without softplus, h0 and dhT, the empty
+sequence, the 130M-like layer at full size, and autograd through the
+differentiable wrapper."""
 import numpy as np
 import pytest
 import torch
@@ -47,9 +49,16 @@ def test_shapes(orc, shape, softplus):
 @pytest.mark.parametrize("shape", [(2, 50, 300, 1), (1, 45, 130, 2), (1, 70, 9, 32), (1, 41, 33, 5),
                                    (3, 1, 40, 16)])
 def test_lane_group_widths_and_one_step(orc, shape):
-    """P = 1 (256 chains a block), 2, 32 (one warp a chain, two lanes a
-    step in the reduce-scatter), 8 with padding lanes, and L = 1."""
+    """One thread a chain (N = 1, 2: 128 chains a block), eight (N = 32: four
+    chains a warp, two sums a lane left by the reduce-scatter), two with
+    padded states (N = 5), and L = 1."""
     run(orc, *shape, seed=sum(shape))
+
+
+def test_one_segment_when_channels_fill_the_gpu(orc):
+    """Enough chains for every resident block: the whole sequence is one
+    segment (the carries pass h0 and dhT through unchanged)."""
+    run(orc, 4, 40, 4800, 16, seed=17)
 
 
 def test_without_initial_state_or_final_gradient(orc):
