@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
 }
 
 // ---------------------------------------------------------------- kernel 2
-// One thread per (b, d, n < NP); grid-stride.
+// One thread per (b, d, n < NP); grid-stride. The segments' values are
+// loaded kCarryBatch at a time ahead of the dependent arithmetic.
+constexpr int kCarryBatch = 8;
+
 __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
 {
     const int64_t total = a.Bsz * a.D * NP;
@@ -325,18 +328,40 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
         const int64_t bd = e / NP, d = bd % a.D, b = bd / a.D;
         const bool st = n < a.N;
         const float A2 = st ? __ldg(a.A + d * a.N + n) * kLog2e : 0.0f;
+        const int64_t s_of0 = b * a.K * a.D + d;    // segment k: s_of0 + k * D
         float h = (st && a.h0) ? __ldg(a.h0 + bd * a.N + n) : 0.0f;
-        for (int k = 0; k < a.K; ++k) {
-            const int64_t s = (b * a.K + k) * a.D + d, idx = s * NP + n;
-            a.hin[idx] = h;
-            h = fmaf(ex2(A2 * a.sdl[s]), h, a.hl[idx]);
+        for (int k0 = 0; k0 < a.K; k0 += kCarryBatch) {
+            float dec[kCarryBatch], loc[kCarryBatch];
+#pragma unroll
+            for (int q = 0; q < kCarryBatch; ++q) {
+                const int64_t s = s_of0 + (int64_t)(k0 + q) * a.D;
+                dec[q] = k0 + q < a.K ? a.sdl[s] : 0.0f;
+                loc[q] = k0 + q < a.K ? a.hl[s * NP + n] : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < kCarryBatch; ++q) {
+                if (k0 + q < a.K) {
+                    a.hin[(s_of0 + (int64_t)(k0 + q) * a.D) * NP + n] = h;
+                    h = fmaf(ex2(A2 * dec[q]), h, loc[q]);
+                }
+            }
         }
         float g = (st && a.ghT) ? __ldg(a.ghT + bd * a.N + n) : 0.0f;
-        for (int k = a.K - 1; k >= 0; --k) {
-            const int64_t s = (b * a.K + k) * a.D + d, idx = s * NP + n;
-            a.gout[idx] = g;
-            if (k > 0)
-                g = fmaf(ex2(A2 * a.sdl[s]), g, a.gl[idx]);
+        for (int k0 = a.K - 1; k0 >= 0; k0 -= kCarryBatch) {
+            float dec[kCarryBatch], loc[kCarryBatch];
+#pragma unroll
+            for (int q = 0; q < kCarryBatch; ++q) {
+                const int64_t s = s_of0 + (int64_t)(k0 - q) * a.D;
+                dec[q] = k0 - q >= 1 ? a.sdl[s] : 0.0f;
+                loc[q] = k0 - q >= 1 ? a.gl[s * NP + n] : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < kCarryBatch; ++q) {
+                if (k0 - q >= 0) {
+                    a.gout[(s_of0 + (int64_t)(k0 - q) * a.D) * NP + n] = g;
+                    g = fmaf(ex2(A2 * dec[q]), g, loc[q]);
+                }
+            }
         }
     }
 }
