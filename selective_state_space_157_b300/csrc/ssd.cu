@@ -16,10 +16,13 @@
 //   S = (B o w)^T X,   w_r = exp(s_last - s_r) dl_r,
 // with H_out = exp(s_last) H_in + S. Three kernels:
 //   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q);
-//   2. ssd_carry_kernel: H_in of every chunk in order, elementwise, and hT;
-//   3. ssd_out_kernel: G = C B^T (M = Q, N = Q, K = N), the masked, decayed
-//      G times X (M = Q, N = P, K = Q) and C e^s times H_in (K = N), both
-//      accumulated into one TMEM tile, then y.
+//   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
+//      written as fp16 in the output kernel's operand layout, and hT;
+//   3. ssd_out_kernel: G = C B^T (M = Q, N = Q, K = N) and C H_in (K = N)
+//      into two TMEM tiles, then the masked, decayed G times X (M = Q, N = P,
+//      K = Q) into a third; y = G X + diag(e^s) C H_in.
+// Each CTA brings every tile it needs into shared memory in one round trip
+// (cp.async, zeros past the sequence), then converts and transposes there.
 // Operands are fp16 in shared memory (bf16 and fp32 inputs are converted
 // on the way in; fp16 keeps three more mantissa bits than bf16, and every
 // operand here stays far inside its range), accumulators fp32 in TMEM.
@@ -49,7 +52,8 @@ struct SsdArgs {
     void *y;             // (Bsz, L, H, P), dtype
     const float *h0;     // (Bsz, H, N, P) or null
     float *hT;           // (Bsz, H, N, P) or null
-    float *S;            // (Bsz, H, nch, N, P): chunk states from zero, then the state entering each chunk
+    float *S;            // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n]
+    __half *Hin;         // (Bsz, H, nch, P x N): the state entering each chunk, fp16 operand order
     float *dec;          // (Bsz, H, nch): exp(s_last) of each chunk
     unsigned *fault;
     int64_t Bsz, L, H;
@@ -57,27 +61,32 @@ struct SsdArgs {
     int softplus;
 };
 
-__device__ __forceinline__ float ld_in(const float *p) { return __ldg(p); }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
-__device__ __forceinline__ void st_out(float *p, float v) { *p = v; }
-__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
-
-// Eight consecutive inputs as fp32 (one 16-byte load for bf16, two for fp32).
-__device__ __forceinline__ void ld8(const float *p, float (&v)[8])
+// 16-byte asynchronous copy global -> shared; zeros instead when !ok.
+__device__ __forceinline__ void ssd_cp16(void *dst, const void *src, bool ok)
 {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
 }
-__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&v)[8])
+__device__ __forceinline__ void ssd_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void ssd_cp_wait() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Copies rows [0, Q) of a global tile (rows >= rows zero) of W elements per
+// row, row stride ld elements, into dst[Q][W] (row-major, contiguous).
+template <typename T, int Q, int W>
+__device__ __forceinline__ void copy_tile(const T *g, int64_t ld, int rows, T *dst)
 {
-    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(u[i] << 16);
-        v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    constexpr int PR = W * (int)sizeof(T) / 16;   // 16-byte pieces per row
+    for (int e = threadIdx.x; e < Q * PR; e += kSsdThreads) {
+        const int r = e / PR, pc = e % PR;
+        const bool ok = r < rows;
+        ssd_cp16(reinterpret_cast<char *>(dst) + (size_t)e * 16,
+                 ok ? reinterpret_cast<const char *>(g + (int64_t)r * ld) + pc * 16 : reinterpret_cast<const char *>(g),
+                 ok);
     }
 }
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // Eight fp32 values as eight fp16 in one 16-byte word.
 __device__ __forceinline__ uint4 pack8(const float (&v)[8])
@@ -92,64 +101,37 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8])
     return r;
 }
 
-// Rows [0, Q) of a row-major global tile (row stride ld elements, K columns,
-// rows >= rows zero) as a K-major fp16 operand in core-matrix order, scaled
-// row by row by scale[] when given. Each thread moves eight columns at a time.
-template <typename T, int Q, int K>
-__device__ __forceinline__ void stage_rows(const T *g, int64_t ld, int rows, const float *scale, __half *dst)
+// A row-major [R][K] tile in shared memory as a K-major fp16 operand with R
+// rows, in core-matrix order. Each thread moves eight columns at a time.
+template <typename T, int R, int K>
+__device__ __forceinline__ void rows_to_operand(const T *src, __half *dst)
 {
 #pragma unroll 4
-    for (int e = threadIdx.x; e < Q * (K / 8); e += kSsdThreads) {
+    for (int e = threadIdx.x; e < R * (K / 8); e += kSsdThreads) {
         const int r = e / (K / 8), k = (e % (K / 8)) * 8;
         float v[8];
-        if (r < rows) {
-            ld8(g + r * ld + k, v);
-            if (scale) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] *= scale[r];
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = 0.0f;
-        }
+        for (int i = 0; i < 8; ++i)
+            v[i] = to_f32(src[r * K + k + i]);
         *reinterpret_cast<uint4 *>(dst + core_index(r, k, K)) = pack8(v);
     }
 }
 
-// The transpose of rows [0, Q) of a row-major global tile with R columns
-// (row stride ld; rows >= rows zero), optionally scaled per source row by
-// scale[]: a K-major operand with R rows and K = Q, in core-matrix order.
-// The tile goes through a padded fp16 staging buffer (row stride R + 8, so
-// the column reads below hit distinct banks), then each thread gathers eight
-// source rows of one column into one 16-byte core row.
+// The transpose of a row-major [Q][R] tile in shared memory, scaled per
+// source row by scale[] when given: a K-major operand with R rows and K = Q,
+// in core-matrix order. Each thread gathers eight source rows of one column
+// (consecutive lanes take consecutive columns: no bank conflicts) into one
+// 16-byte core row.
 template <typename T, int Q, int R>
-__device__ __forceinline__ void stage_transposed(const T *g, int64_t ld, int rows, const float *scale, __half *stg,
-                                                 __half *dst)
+__device__ __forceinline__ void transpose_to_operand(const T *src, const float *scale, __half *dst)
 {
-    constexpr int S = R + 8;
-#pragma unroll 4
-    for (int e = threadIdx.x; e < Q * (R / 8); e += kSsdThreads) {
-        const int k = e / (R / 8), r = (e % (R / 8)) * 8;
-        float v[8];
-        if (k < rows) {
-            ld8(g + k * ld + r, v);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = 0.0f;
-        }
-        *reinterpret_cast<uint4 *>(stg + k * S + r) = pack8(v);
-    }
-    __syncthreads();
 #pragma unroll 4
     for (int e = threadIdx.x; e < R * (Q / 8); e += kSsdThreads) {
         const int r = e % R, k = (e / R) * 8;
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            v[i] = __half2float(stg[(k + i) * S + r]) * (scale ? scale[k + i] : 1.0f);
+            v[i] = to_f32(src[(k + i) * R + r]) * (scale ? scale[k + i] : 1.0f);
         *reinterpret_cast<uint4 *>(dst + core_index(r, k, Q)) = pack8(v);
     }
 }
@@ -197,7 +179,7 @@ __device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t parity)
 }
 
 // 1. Each chunk's contribution to the state, S = (B o w)^T X (N x P),
-// stored transposed, [p][n], for the carry scan and the output kernel.
+// stored transposed, [p][n], for the carry scan.
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 {
@@ -205,8 +187,9 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     extern __shared__ __align__(1024) unsigned char sm[];
     __half *A3 = reinterpret_cast<__half *>(sm);                  // (B o w)^T: N rows, K = Q
     __half *BX = A3 + N * Q;                                       // X^T: P rows, K = Q
-    __half *stg = BX + P * Q;                                      // staging, Q x (max(N, P) + 8)
-    float *dl = reinterpret_cast<float *>(stg + Q * ((N > P ? N : P) + 8));
+    T *rB = reinterpret_cast<T *>(BX + P * Q);                     // B tile [Q][N]
+    T *rX = rB + Q * N;                                            // X tile [Q][P]
+    float *dl = reinterpret_cast<float *>(rX + Q * P);
     float *s = dl + Q;
     float *w = s + Q;
     __shared__ uint32_t tbase;
@@ -216,26 +199,28 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     const int64_t b = blockIdx.z, h = blockIdx.y, c = blockIdx.x;
     const int64_t t0 = c * Q;
     const int rows = (int)min((int64_t)Q, a.L - t0);
-    const T *xg = static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P;
-    const T *Bg = static_cast<const T *>(a.B) + (b * a.L + t0) * N;
-
+    // TMEM first: the allocation permit is given up at once, so the SM can
+    // start the next CTA while this one loads.
+    if (warp == 0)
+        tmem_alloc(&tbase, P);
+    copy_tile<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, rB);
+    copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
+    ssd_cp_commit();
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
     if (warp == 0)
         ssd_decays(a, b, h, t0, rows, dl, s);
+    ssd_cp_wait();
     __syncthreads();
     const float slast = s[Q - 1];
     if (tid < Q)
         w[tid] = ex2((slast - s[tid]) * kLog2e) * dl[tid];
     __syncthreads();
-    stage_transposed<T, Q, N>(Bg, N, rows, w, stg, A3);
-    __syncthreads();
-    stage_transposed<T, Q, P>(xg, a.H * P, rows, nullptr, stg, BX);
+    transpose_to_operand<T, Q, N>(rB, w, A3);
+    transpose_to_operand<T, Q, P>(rX, nullptr, BX);
     fence_proxy_async_smem();   // the tensor core reads shared memory through the async proxy
-    if (warp == 0)
-        tmem_alloc(&tbase, P);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -275,58 +260,83 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
         tmem_dealloc(tm, P);
 }
 
-// 2. The state entering each chunk, in chunk order (in place of S, still
-// [p][n]), and hT ([n][p]). A thread's chunk states are all loaded before
-// the serial fold, up to kCarryBatch at a time.
-constexpr int kCarryBatch = 16;
+// 2. The state entering each chunk, in chunk order: fp32 carries, stored as
+// fp16 in the output kernel's operand order (P rows, K = N, core-matrix
+// order), and hT ([n][p], fp32). A thread owns eight consecutive n of one p
+// (one 16-byte core row); the chunk states are loaded kCarryBatch chunks
+// ahead of the serial fold.
+constexpr int kCarryBatch = 8;
 
-__global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a, int N, int P)
+template <int N, int P>
+__global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
 {
-    const int64_t NP = (int64_t)N * P;
+    constexpr int NP = N * P;
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    if (i >= a.Bsz * a.H * NP)
+    if (i >= a.Bsz * a.H * (NP / 8))
         return;
-    const int64_t bh = i / NP, pn = i - bh * NP;
-    const int64_t p = pn / N, n = pn - p * N;
-    float carry = a.h0 ? __ldg(a.h0 + bh * NP + n * P + p) : 0.0f;
-    float *Sp = a.S + bh * a.nch * NP + pn;
+    const int64_t bh = i / (NP / 8);
+    const int pn = (int)(i - bh * (NP / 8)) * 8;
+    const int p = pn / N, n0 = pn % N;
+    float carry[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        carry[q] = a.h0 ? __ldg(a.h0 + bh * NP + (int64_t)(n0 + q) * P + p) : 0.0f;
+    const float *Sp = a.S + bh * a.nch * NP + pn;
+    __half *Hp = a.Hin + bh * a.nch * NP + core_index(p, n0, N);
     const float *dp = a.dec + bh * a.nch;
     for (int c0 = 0; c0 < a.nch; c0 += kCarryBatch) {
-        float sv[kCarryBatch], dv[kCarryBatch];
+        float4 sv[kCarryBatch][2];
+        float dv[kCarryBatch];
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             const int cc = c0 + j < a.nch ? c0 + j : a.nch - 1;
-            sv[j] = __ldcg(Sp + (int64_t)cc * NP);
+            const float4 *src = reinterpret_cast<const float4 *>(Sp + (int64_t)cc * NP);
+            sv[j][0] = __ldcg(src);
+            sv[j][1] = __ldcg(src + 1);
             dv[j] = __ldg(dp + cc);
         }
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             if (c0 + j < a.nch) {
-                Sp[(int64_t)(c0 + j) * NP] = carry;
-                carry = fmaf(dv[j], carry, sv[j]);
+                *reinterpret_cast<uint4 *>(Hp + (int64_t)(c0 + j) * NP) = pack8(carry);
+                const float sj[8] = {sv[j][0].x, sv[j][0].y, sv[j][0].z, sv[j][0].w,
+                                     sv[j][1].x, sv[j][1].y, sv[j][1].z, sv[j][1].w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    carry[q] = fmaf(dv[j], carry[q], sj[q]);
             }
         }
     }
-    if (a.hT)
-        a.hT[bh * NP + n * P + p] = carry;
+    if (a.hT) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            a.hT[bh * NP + (int64_t)(n0 + q) * P + p] = carry[q];
+    }
 }
 
 // 3. Each chunk's outputs: the masked dual form inside the chunk plus the
 // decayed incoming state.
+template <int P>
+__host__ __device__ constexpr int ssd_out_cols()   // TMEM columns: G (64), G X (P) and C H_in (P)
+{
+    return 64 + 2 * P <= 128 ? 128 : (64 + 2 * P <= 256 ? 256 : 512);
+}
+
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
 {
     constexpr int Q = kSsdQ;
-    constexpr int COLS = 64 + P <= 128 ? 128 : 256;   // G (64 columns) and Y (P)
+    constexpr int COLS = ssd_out_cols<P>();
     extern __shared__ __align__(1024) unsigned char sm[];
     __half *A1 = reinterpret_cast<__half *>(sm);                       // C: Q rows, K = N
-    __half *A4 = A1 + Q * N;                                            // C e^s: Q rows, K = N
-    __half *B1 = A4 + Q * N;                                            // B: Q rows, K = N
+    __half *B1 = A1 + Q * N;                                            // B: Q rows, K = N
     __half *B4 = B1 + Q * N;                                            // H_in^T: P rows, K = N
     __half *BX = B4 + P * N;                                            // X^T: P rows, K = Q
-    __half *A2 = BX + P * Q;                                            // masked G: Q rows, K = Q
-    __half *stg = A2 + Q * Q;                                           // staging, Q x (P + 8)
-    float *dl = reinterpret_cast<float *>(stg + Q * (P + 8));
+    T *rC = reinterpret_cast<T *>(BX + P * Q);                          // C tile [Q][N]
+    __half *A2 = reinterpret_cast<__half *>(rC);                        // masked G (over rC once converted)
+    T *rB = rC + Q * N;                                                 // B tile [Q][N]
+    T *rX = rB + Q * N;                                                 // X tile [Q][P]
+    float *dl = reinterpret_cast<float *>(rX + Q * P);
     float *s = dl + Q;
     float *es = s + Q;
     __shared__ uint32_t tbase;
@@ -337,38 +347,42 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     const int64_t t0 = c * Q;
     const int rows = (int)min((int64_t)Q, a.L - t0);
     const bool carry = c > 0 || a.h0 != nullptr;
-    const T *xg = static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P;
-    const T *Bg = static_cast<const T *>(a.B) + (b * a.L + t0) * N;
-    const T *Cg = static_cast<const T *>(a.C) + (b * a.L + t0) * N;
-
+    if (warp == 0)   // first, as in the state kernel
+        tmem_alloc(&tbase, COLS);
+    copy_tile<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, rC);
+    copy_tile<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, rB);
+    copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
+    if (carry)   // already in operand order: a plain copy
+        copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
+    ssd_cp_commit();
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
     if (warp == 0)
         ssd_decays(a, b, h, t0, rows, dl, s);
+    ssd_cp_wait();
     __syncthreads();
     if (tid < Q)
         es[tid] = ex2(s[tid] * kLog2e);
-    __syncthreads();
-    stage_rows<T, Q, N>(Cg, N, rows, nullptr, A1);
-    stage_rows<T, Q, N>(Cg, N, rows, es, A4);
-    stage_rows<T, Q, N>(Bg, N, rows, nullptr, B1);
-    if (carry)   // the incoming state, [p][n] fp32: P rows of K = N
-        stage_rows<float, P, N>(a.S + ((b * a.H + h) * a.nch + c) * N * P, N, P, nullptr, B4);
-    stage_transposed<T, Q, P>(xg, a.H * P, rows, nullptr, stg, BX);
+    rows_to_operand<T, Q, N>(rC, A1);
+    rows_to_operand<T, Q, N>(rB, B1);
+    transpose_to_operand<T, Q, P>(rX, nullptr, BX);
     fence_proxy_async_smem();
-    if (warp == 0)
-        tmem_alloc(&tbase, COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tG = tbase, tY = tbase + 64;
+    const uint32_t tG = tbase, tY = tbase + 64, tH = tbase + 64 + P;
     if (tid == 0) {
-        constexpr uint32_t id = umma_idesc_f16(Q, Q);
+        constexpr uint32_t idG = umma_idesc_f16(Q, Q), idY = umma_idesc_f16(Q, P);
 #pragma unroll
         for (int kk = 0; kk < N / 16; ++kk)
-            umma_f16(tG, umma_tile_desc(A1, N, kk), umma_tile_desc(B1, N, kk), id, kk > 0);
+            umma_f16(tG, umma_tile_desc(A1, N, kk), umma_tile_desc(B1, N, kk), idG, kk > 0);
+        if (carry) {
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk)
+                umma_f16(tH, umma_tile_desc(A1, N, kk), umma_tile_desc(B4, N, kk), idY, kk > 0);
+        }
         umma_commit(&mbar);
     }
     bool ok = mma_wait(&mbar, 0);
@@ -404,25 +418,40 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
 #pragma unroll
         for (int kk = 0; kk < Q / 16; ++kk)
             umma_f16(tY, umma_tile_desc(A2, Q, kk), umma_tile_desc(BX, Q, kk), id, kk > 0);
-        if (carry) {
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk)
-                umma_f16(tY, umma_tile_desc(A4, N, kk), umma_tile_desc(B4, N, kk), id, true);
-        }
         umma_commit(&mbar);
     }
     ok = mma_wait(&mbar, 1) && ok;
     tc_fence_after();
     T *yg = static_cast<T *>(a.y) + ((b * a.L + t0 + t) * a.H + h) * P;
     const bool mine = ok && lane < 16 && t < rows;
+    const float et = es[t < Q ? t : 0];
 #pragma unroll
     for (int p0 = 0; p0 < P; p0 += 16) {
-        float v[16];
+        float v[16], hv[16];
         tmem_ld16(tY + lanes + (uint32_t)p0, v);
+        if (carry)
+            tmem_ld16(tH + lanes + (uint32_t)p0, hv);
         if (mine) {
+            if (carry) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                st_out(yg + p0 + i, v[i]);
+                for (int i = 0; i < 16; ++i)
+                    v[i] = fmaf(et, hv[i], v[i]);
+            }
+            if constexpr (sizeof(T) == 2) {
+                uint4 u[2];
+                uint32_t *w = reinterpret_cast<uint32_t *>(u);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const __nv_bfloat162 q = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                    w[i] = *reinterpret_cast<const uint32_t *>(&q);
+                }
+                reinterpret_cast<uint4 *>(yg + p0)[0] = u[0];
+                reinterpret_cast<uint4 *>(yg + p0)[1] = u[1];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4)
+                    *reinterpret_cast<float4 *>(yg + p0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            }
         }
     }
     if (tid == 0 && !ok)
@@ -433,17 +462,29 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
         tmem_dealloc(tbase, COLS);
 }
 
-template <int N, int P>
+template <typename T, int N, int P>
 constexpr size_t ssd_state_smem()
 {
-    return ((size_t)(N + P) * kSsdQ + (size_t)kSsdQ * ((N > P ? N : P) + 8)) * 2 + 3 * kSsdQ * 4;
+    return (size_t)(N + P) * kSsdQ * 2 + (size_t)kSsdQ * (N + P) * sizeof(T) + 3 * kSsdQ * 4;
 }
 
-template <int N, int P>
+template <typename T, int N, int P>
 constexpr size_t ssd_out_smem()
 {
-    return ((size_t)3 * kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ + (size_t)kSsdQ * kSsdQ +
-            (size_t)kSsdQ * (P + 8)) * 2 + 3 * kSsdQ * 4;
+    return ((size_t)2 * kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ) * 2 +
+           (size_t)kSsdQ * (2 * N + P) * sizeof(T) + 3 * kSsdQ * 4;
+}
+
+// Shared memory that keeps at most max_ctas CTAs of a kernel on one SM, so
+// that their TMEM allocations never exceed the SM's 512 columns: max_ctas + 1
+// CTAs (each with the 1 KB the runtime reserves) must not fit in the SM's
+// 228 KB. Never above the 227 KB a CTA may have.
+inline size_t ssd_pad(size_t smem, int max_ctas)
+{
+    constexpr size_t kSm = (size_t)228 * 1024, kReserved = 1024, kMax = (size_t)227 * 1024;
+    size_t pad = kSm / (size_t)(max_ctas + 1) - kReserved + 1;
+    if (pad > kMax) pad = kMax;
+    return smem > pad ? smem : pad;
 }
 
 template <typename T, int N, int P>
@@ -451,20 +492,15 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
 {
     auto k1 = ssd_state_kernel<T, N, P>;
     auto k3 = ssd_out_kernel<T, N, P>;
-    // At most 512 / P state-kernel CTAs per SM (P TMEM columns each), so that
-    // their allocations never exceed the SM's 512 columns: shared memory is
-    // padded to keep more from fitting.
-    constexpr size_t kPad = (size_t)228 * 1024 / (512 / P) - 1024 + 1;
-    const size_t s1 = ssd_state_smem<N, P>() > kPad ? ssd_state_smem<N, P>() : kPad;
-    const size_t s3 = ssd_out_smem<N, P>();
+    const size_t s1 = ssd_pad(ssd_state_smem<T, N, P>(), 512 / P);
+    const size_t s3 = ssd_pad(ssd_out_smem<T, N, P>(), 512 / ssd_out_cols<P>());
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3);
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
     k1<<<grid, kSsdThreads, s1, st>>>(a);
-    const int64_t NP = (int64_t)N * P;
-    const int64_t total = a.Bsz * a.H * NP;
-    ssd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a, N, P);
+    const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
+    ssd_carry_kernel<N, P><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
     k3<<<grid, kSsdThreads, s3, st>>>(a);
     e = cudaGetLastError();
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "SSD kernel launch");
@@ -542,18 +578,22 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
-    const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 4, dbytes = (size_t)(Bsz * H * nch) * 4;
+    // Workspace: S (fp32), the incoming states (fp16), the chunk decays.
+    const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 4, hbytes = sbytes / 2,
+                 dbytes = (size_t)(Bsz * H * nch) * 4;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + dbytes, pool, st);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + hbytes + dbytes, pool, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", sbytes + dbytes, cudaGetErrorString(e));
+        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", sbytes + hbytes + dbytes,
+                    cudaGetErrorString(e));
     }
     SsdArgs a;
     memset(&a, 0, sizeof a);
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.y = y; a.h0 = h0; a.hT = hT;
     a.S = static_cast<float *>(ws);
-    a.dec = a.S + sbytes / 4;
+    a.Hin = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes);
+    a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
     a.Bsz = Bsz; a.L = L; a.H = H;
     a.nch = (int)nch;
     a.softplus = dt_softplus ? 1 : 0;
