@@ -397,12 +397,22 @@ class _FwdBench:
     """Device inputs of a forward workload, rotated over enough copies that
     more than 2x L2 is touched between reuses, and its step function."""
 
-    def __init__(self, wid, dev):
+    def __init__(self, wid, dev, seq_len=None):
+        import dataclasses
         import torch
         import selective_state_space_157_b300 as ss
         from selective_state_space_157_b300 import workloads as W
         self.w = w = W.WORKLOADS[wid]
-        self.inp = inp = W.workload_inputs(wid)
+        if seq_len:
+            # A shorter sequence of the same workload (same kernels, same
+            # distributions): the small case a full profiler capture runs on.
+            if w.gated:
+                raise SystemExit("--seq-len is not offered for the gated workload")
+            self.w = w = dataclasses.replace(w, L=seq_len)
+            self.inp = inp = W.fwd_inputs(w.Bsz, w.L, w.D, w.N, seed=w.seed, dtype=w.dtype, u_mean=w.u_mean,
+                                          a_init=w.a_init, delta_softplus=True)
+        else:
+            self.inp = inp = W.workload_inputs(wid)
         self.bf16 = bf16 = w.dtype == W.BF16
         self.es = es = 2 if bf16 else 4
         self.gate = W.workload_gate_inputs(wid) if w.gated else None
@@ -502,7 +512,8 @@ def run_gpu(args, world, rank, local):
     if w.backward:
         return run_bwd(args, world, rank, local, dev, w, alu)
 
-    fb = _FwdBench(args.workload, dev)
+    fb = _FwdBench(args.workload, dev, args.seq_len)
+    w = fb.w
     Bsz, L, D, N, bf16 = fb.Bsz, fb.L, fb.D, fb.N, fb.bf16
     sec, clocks = timed_steps(fb.step, args.steps, args.warmup, world, dev, local)
     per_step = sec / args.steps
@@ -519,7 +530,7 @@ def run_gpu(args, world, rank, local):
     e2e = fwd_e2e(args, world, dev, w, inp, gate, bf16, elems)
 
     per_config = None
-    if args.workload == DEFAULT_WORKLOAD and not args.no_per_config:
+    if args.workload == DEFAULT_WORKLOAD and not args.no_per_config and not args.seq_len:
         per_config = {}
         for wid in PER_CONFIG:
             per_config[str(wid)] = measure_config(wid, args, world, local, dev, alu)
@@ -535,7 +546,7 @@ def run_gpu(args, world, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pk = peaks(sms, max_mhz, hbm_gbs, alu)
     pk["source"] = peak_source(src, alu, sms, max_mhz)
-    roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
+    roof = roofline(work, pk, per_step, traffic=None if args.seq_len else profiled_traffic(args.workload),
                     kernel=f"selscan_fwd call ({plan['launches']} launches, {plan['chunks']} chunks)")
 
     cpu = None
@@ -568,30 +579,19 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
     hT_host = torch.empty(inp.x.shape[0], inp.x.shape[2], inp.A.shape[1], pin_memory=True) \
         if w.return_state else None
     e2e_steps = max(1, min(args.steps, 20 if elems < 50_000_000 else 5))
-    if w.zoh:
-        host = [t.pin_memory() for t in host]
-
-        def e2e_call():
-            d = [t.to(dev, non_blocking=True) for t in host]
-            yd = ss.selscan_fwd(*d, True, zoh=True)
-            y_host.copy_(yd, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-    elif w.gated:
-        # The gated form takes device tensors: copy the step's inputs in,
-        # run it, copy y out, synchronise.
+    kw = {}
+    if w.gated:
+        # The block's skip and gate: Dskip and z from host memory as well.
         host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
-        host = [t.pin_memory() for t in host]
+    host = [t.pin_memory() for t in host]
+    if w.gated:
+        kw = {"z": host[5], "D_skip": host[6]}
+    if w.zoh:
+        kw["zoh"] = True
 
-        def e2e_call():
-            d = [t.to(dev, non_blocking=True) for t in host]
-            yd = ss.selscan_fwd(*d[:5], True, D_skip=d[6], z=d[5])
-            y_host.copy_(yd, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-    else:
-        host = [t.pin_memory() for t in host]
-
-        def e2e_call():
-            ss.selscan_fwd(*host, True, y=y_host, hT=hT_host)  # H2D, kernels, D2H, synchronise
+    def e2e_call():
+        # selscan_fwd_host(_ex): H2D, kernels, D2H, synchronise
+        ss.selscan_fwd(*host[:5], True, y=y_host, hT=hT_host, **kw)
     e2e_call()                                       # warm the copy path
     barrier(world, dev)
     t0 = time.perf_counter()
@@ -1238,6 +1238,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per_config measurements")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run a forward workload at this sequence length instead (profiling a small case)")
     ap.add_argument("--ref-chains", type=int, default=192, help="chains per reference step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":

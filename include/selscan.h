@@ -101,15 +101,17 @@ typedef enum {
  * Aliasing: y may equal x or delta exactly (in-place output); h0 may equal
  * hT exactly (resume in place). Any other overlap between y or hT and
  * another argument is SELSCAN_ERR_INVALID_ARG. When the sequence is cut
- * into chunks, in-place output makes the readout of each chunk wait until
- * that chunk's reduction has read its inputs, and in-place resume writes
- * the final state to the workspace first and copies it to hT after the
- * scan.
+ * into chunks, output in place over delta takes the plain-load kernels
+ * (whose chunk reductions finish before any output is written; the fused
+ * kernel's correction pass reads delta after the first pass wrote y), and
+ * in-place resume writes the final state to the workspace first and copies
+ * it to hT after the scan.
  *
- * Memory: long sequences use a small library-owned workspace for the chunk
- * carries ((ceil(L / chunk) - 1) * Bsz * D * (N + 1) fp32 plus one flag per
- * chunk and channel tile, plus Bsz * D * N fp32 for in-place resume), taken
- * from a
+ * Memory: chunked plans use a library-owned workspace: the chunk carries
+ * (ceil(L / chunk) * Bsz * D * (N + 1) fp32), a ticket and two flags per
+ * channel group, with bf16 output on the fused path the bf16 rounding
+ * residual of the first pass (Bsz * L * D bf16), and Bsz * D * N fp32 for
+ * in-place resume. selscan_fwd_plan reports its size. It is taken from a
  * private stream-ordered pool on `stream` and returned to it before the
  * call's work completes; selscan_release_workspace() gives the pool's
  * memory back to the device. SELSCAN_ERR_NO_MEMORY if it cannot be had.
@@ -219,8 +221,9 @@ int selscan_step_ex(float *state, const float *x, const float *delta, const floa
  * and it splits the work the same way. The scratch array holds
  * SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB); every GPU that loads the library
  * holds it until the process exits. A call whose plan needs more scratch
- * (the workspace_bytes that selscan_fwd_plan reports; about
- * 4 * (chunks - 1) * Bsz * D * (N + 1) bytes) returns SELSCAN_ERR_UNSUPPORTED
+ * (the workspace_bytes that selscan_fwd_plan reports: see selscan_fwd's
+ * "Memory"; chunked bf16 plans include Bsz * L * D * 2 bytes for the
+ * rounding residual) returns SELSCAN_ERR_UNSUPPORTED
  * before anything is launched; run such a problem through selscan_fwd, or in
  * pieces along L, handing hT of one piece to h0 of the next.
  *
@@ -282,6 +285,19 @@ int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, int dtype,
 int selscan_fwd_host(const void *x, const void *delta, const float *A, const void *B,
                      const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
                      int dtype, int delta_softplus, const float *h0, float *hT, void *stream);
+
+/*
+ * selscan_fwd_host_ex -- selscan_fwd_ex (the block's skip and gate, the
+ * flags word) with every tensor in HOST memory, pipelined like
+ * selscan_fwd_host. Dskip (D fp32) and z (Bsz, L, D, like x) are host
+ * pointers or NULL, as in selscan_fwd_ex; z travels with the other
+ * per-step inputs of each piece. Arguments, aliasing rules, blocking and
+ * errors as for selscan_fwd_ex and selscan_fwd_host.
+ */
+int selscan_fwd_host_ex(const void *x, const void *delta, const float *A, const void *B,
+                        const void *C, const float *Dskip, const void *z, void *y, int64_t Bsz,
+                        int64_t L, int64_t D, int64_t N, int dtype, int flags, const float *h0,
+                        float *hT, void *stream);
 
 /*
  * selscan_conv1d -- the causal depthwise convolution and SiLU in front of
@@ -400,9 +416,9 @@ const char *selscan_last_error(void);
 int selscan_check_device_error(void *stream);
 
 /* Test hook for the timeout path: makes a wait run out without any fault.
- * With withhold_carries = 1, the reduction items of later chunked forward
- * calls in this process raise no completion flags, so every readout of a
- * later chunk waits for a flag that nothing sets; wait_limit_ms (1..2000)
+ * With withhold_carries = 1, later chunked forward calls in this process
+ * never announce their composed chunk carries, so every correction pass of
+ * a later chunk waits for a flag that nothing sets; wait_limit_ms (1..2000)
  * shortens that wait (0 = the default 2 s). Such calls end early with
  * invalid outputs, and selscan_check_device_error on their stream returns
  * SELSCAN_ERR_TIMEOUT (fault code 2). selscan_test_fault_injection(0, 0)

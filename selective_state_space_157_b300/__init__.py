@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_conv1d_step.argtypes = [P, P, P, P, P, I64, I64, I64, INT, P]
         L.selscan_fwd_host.restype = INT
         L.selscan_fwd_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
+        L.selscan_fwd_host_ex.restype = INT
+        L.selscan_fwd_host_ex.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, INT, P, P, P]
         L.selscan_fwd_plan.restype = INT
         L.selscan_fwd_plan.argtypes = [I64, I64, I64, I64, INT, P, P, P, P]
         L.selscan_ssd_fwd.restype = INT
@@ -163,7 +165,7 @@ def _need(t, name, shape, dtype, device):
 
 def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
                 return_final_state: bool = False, y=None, hT=None, stream=None,
-                D_skip=None, z=None, zoh: bool = False):
+                D_skip=None, z=None, zoh: bool = False, check: bool = False):
     """Forward selective scan (see ``include/selscan.h``).
 
     x, delta: (Bsz, L, D) float32 or bfloat16; A: (D, N) float32;
@@ -172,15 +174,15 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
     ``return_final_state``. ``y`` / ``hT`` may be passed preallocated.
     ``D_skip`` (D,) float32 and ``z`` (like x) add the block's skip and gate
     (selscan_fwd_gated): y = (scan + D_skip * x) * silu(z). ``zoh`` selects
-    the zero-order-hold discretisation (selscan_fwd_ex). Device tensors only
-    for those.
+    the zero-order-hold discretisation (selscan_fwd_ex). Host (CPU) tensors
+    take the host-buffer entry points (selscan_fwd_host, selscan_fwd_host_ex).
+    ``check`` waits for the call and raises if a wait inside the
+    kernel ran out (``check_device_error``): the outputs are invalid then.
     """
     import torch
     gated = D_skip is not None or z is not None
     if x.device.type == "cpu":
-        if gated or zoh:
-            raise ValueError("D_skip / z / zoh are supported for device tensors only")
-        return _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT)
+        return _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT, D_skip, z, zoh)
     dev = x.device
     Bsz, L, D = x.shape
     N = A.shape[1] if A.dim() == 2 else -1
@@ -215,11 +217,13 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
                                    Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
                                    _stream_ptr(stream))
     _check(rc)
+    if check:
+        check_device_error(stream)
     return (y, hT) if (return_final_state or hT is not None) else y
 
 
 def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dhT=None,
-                want_dh0: bool = True, stream=None):
+                want_dh0: bool = True, stream=None, check: bool = False):
     """Backward pass of the forward scan (fp32, no skip or gate; see
     ``include/selscan.h``): gradients of a loss with respect to x, delta, A,
     B, C and h0, given dy (Bsz, L, D) = dLoss/dy and dhT (Bsz, D, N) =
@@ -251,6 +255,8 @@ def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dh
                                _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
                                _ptr(g.get("dh0")), Bsz, L, D, N, int(bool(delta_softplus)), _stream_ptr(stream))
     _check(rc)
+    if check:
+        check_device_error(stream)
     return g
 
 
@@ -266,10 +272,12 @@ def _selective_scan_fn():
 
         class SelectiveScan(torch.autograd.Function):
             @staticmethod
-            def forward(ctx, x, delta, A, B, C, h0, delta_softplus):
-                y, hT = selscan_fwd(x, delta, A, B, C, delta_softplus, h0=h0, return_final_state=True)
+            def forward(ctx, x, delta, A, B, C, h0, delta_softplus, check):
+                y, hT = selscan_fwd(x, delta, A, B, C, delta_softplus, h0=h0, return_final_state=True,
+                                    check=check)
                 ctx.save_for_backward(x, delta, A, B, C, h0)
                 ctx.delta_softplus = delta_softplus
+                ctx.check = check
                 return y, hT
 
             @staticmethod
@@ -277,22 +285,25 @@ def _selective_scan_fn():
                 x, delta, A, B, C, h0 = ctx.saved_tensors
                 want_dh0 = h0 is not None and ctx.needs_input_grad[5]
                 g = selscan_bwd(x, delta, A, B, C, dy.contiguous(), ctx.delta_softplus, h0=h0,
-                                dhT=None if dhT is None else dhT.contiguous(), want_dh0=want_dh0)
-                return g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dh0"), None
+                                dhT=None if dhT is None else dhT.contiguous(), want_dh0=want_dh0,
+                                check=ctx.check)
+                return g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dh0"), None, None
 
         _autograd_fn = SelectiveScan
     return _autograd_fn
 
 
-def selective_scan(x, delta, A, B, C, delta_softplus: bool = False, h0=None):
+def selective_scan(x, delta, A, B, C, delta_softplus: bool = False, h0=None, check: bool = False):
     """The forward scan as a differentiable torch operation: returns (y, hT),
     and ``backward`` runs ``selscan_bwd`` (the states are recomputed, not
-    stored). Device float32 tensors; h0 (Bsz, D, N) or None."""
-    return _selective_scan_fn().apply(x, delta, A, B, C, h0, bool(delta_softplus))
+    stored). Device float32 tensors; h0 (Bsz, D, N) or None. ``check`` makes
+    the forward and the backward wait for their kernels and raise if a wait
+    inside one ran out."""
+    return _selective_scan_fn().apply(x, delta, A, B, C, h0, bool(delta_softplus), bool(check))
 
 
 def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=None, hT=None,
-                        stream=None):
+                        stream=None, check: bool = False):
     """selscan_fwd without any allocation, for callers that cannot allocate
     device memory (another allocator owns it, or allocation latency is not
     allowed); see ``include/selscan.h``. Device tensors only, with the outputs
@@ -315,6 +326,8 @@ def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=N
                                        Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
                                        _stream_ptr(stream))
     _check(rc)
+    if check:
+        check_device_error(stream)
     return y
 
 
@@ -418,7 +431,7 @@ def conv1d_step(conv_state, x, w, bias=None, silu: bool = True, out=None, stream
 
 
 def ssd_fwd(x, dt, A, B, C, dt_softplus: bool = True, h0=None, return_final_state: bool = False, y=None,
-            hT=None, stream=None):
+            hT=None, stream=None, check: bool = False):
     """Mamba-2 SSD forward (selscan_ssd_fwd): x (Bsz, L, H, P) float32 or
     bfloat16, dt (Bsz, L, H) float32, A (H,) float32, B, C (Bsz, L, N) like
     x, h0 (Bsz, H, N, P) float32 or None. Returns y (like x), or (y, hT)
@@ -448,6 +461,8 @@ def ssd_fwd(x, dt, A, B, C, dt_softplus: bool = True, h0=None, return_final_stat
         rc = lib().selscan_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(y), _ptr(h0), _ptr(hT),
                                    Bsz, L, H, P, N, code, int(bool(dt_softplus)), _stream_ptr(stream))
     _check(rc)
+    if check:
+        check_device_error(stream)
     return (y, hT) if (return_final_state or hT is not None) else y
 
 
@@ -457,9 +472,11 @@ def _to_dev(t, dev):
     return None if t is None else t.to(dev, non_blocking=True)
 
 
-def _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT):
-    """Host tensors: one selscan_fwd_host call (the library pipelines the
-    copies in, the scan and the copies out on the current device). Returns
+def _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT, D_skip=None, z=None,
+              zoh=False):
+    """Host tensors: one selscan_fwd_host (or, with the skip, gate or
+    zero-order hold, selscan_fwd_host_ex) call: the library pipelines the
+    copies in, the scan and the copies out on the current device. Returns
     once the outputs are in host memory. Page-locked tensors let the copies
     overlap the scan."""
     import torch
@@ -482,9 +499,18 @@ def _fwd_host(x, delta, A, B, C, delta_softplus, h0, return_final_state, y, hT):
         hT = torch.empty((Bsz, D, N), dtype=torch.float32, pin_memory=True)
     if hT is not None:
         _need(hT, "hT", (Bsz, D, N), torch.float32, cpu)
-    rc = lib().selscan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
-                                Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
-                                _stream_ptr(None))
+    if D_skip is not None:
+        _need(D_skip, "D_skip", (D,), torch.float32, cpu)
+    if z is not None:
+        _need(z, "z", (Bsz, L, D), x.dtype, cpu)
+    if D_skip is not None or z is not None or zoh:
+        flags = (FLAG_SOFTPLUS if delta_softplus else 0) | (FLAG_ZOH if zoh else 0)
+        rc = lib().selscan_fwd_host_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D_skip), _ptr(z),
+                                       _ptr(y), Bsz, L, D, N, code, flags, _ptr(h0), _ptr(hT), _stream_ptr(None))
+    else:
+        rc = lib().selscan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y),
+                                    Bsz, L, D, N, code, int(bool(delta_softplus)), _ptr(h0), _ptr(hT),
+                                    _stream_ptr(None))
     _check(rc)
     return (y, hT) if want_state else y
 

@@ -134,8 +134,8 @@ namespace {
 // Off unless selscan_test_fault_injection turns it on; nothing in the
 // environment can enable it.
 std::mutex g_test_mu;
-int g_test_withhold = 0;      // aggregates raise no done flags
-long g_test_wait_ms = 0;      // readouts' wait limit (0: the default)
+int g_test_withhold = 0;      // chunk carries are never announced
+long g_test_wait_ms = 0;      // limit of the waits for them (0: the default)
 
 // ---- forward planning ---------------------------------------------------
 
@@ -261,8 +261,8 @@ void plan_fwd(int64_t Bsz, int64_t L, int64_t D, int64_t N, size_t es, const voi
     // CTAs of kScanThreads.
     p->threads = p->tma ? fused_threads(p->K > 1, nsplit) : kScanThreads;
     p->dtiles = (int)tiles(p->threads);
-    // Readouts of every chunk load h0 when they start, and the last chunk's
-    // readouts write hT when they end: in place, that would race.
+    // Every chunk's first pass (fused kernel) or readout (plain kernels) may
+    // load h0 while the final state is written: in place, that would race.
     p->stage_hT = hT != nullptr && hT == h0 && p->K > 1;
 }
 
@@ -295,7 +295,8 @@ size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t L, int64_t 
     return fwd_workspace_layout(plan, Bsz, L, D, N, dtype).total;
 }
 
-// TMA path: one persistent kernel (aggregates, carries and readout together).
+// TMA path: one persistent kernel (local scans, carry composition and
+// corrections together).
 // Returns SELSCAN_ERR_UNSUPPORTED when TMA cannot be set up (the caller then
 // takes the plain path); nothing has been enqueued in that case.
 int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, float *ws, unsigned *fault,
@@ -674,9 +675,21 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
                                 const void *C, void *y, int64_t Bsz, int64_t L, int64_t D, int64_t N,
                                 int dtype, int delta_softplus, const float *h0, float *hT, void *stream)
 {
+    return selscan_fwd_host_ex(x, delta, A, B, C, nullptr, nullptr, y, Bsz, L, D, N, dtype,
+                               delta_softplus ? SELSCAN_FLAG_SOFTPLUS : 0, h0, hT, stream);
+}
+
+extern "C" int selscan_fwd_host_ex(const void *x, const void *delta, const float *A, const void *B,
+                                   const void *C, const float *Dskip, const void *z, void *y, int64_t Bsz,
+                                   int64_t L, int64_t D, int64_t N, int dtype, int flags, const float *h0,
+                                   float *hT, void *stream)
+{
     g_err[0] = '\0';
+    if (flags & ~(SELSCAN_FLAG_SOFTPLUS | SELSCAN_FLAG_ZOH))
+        return fail(SELSCAN_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)flags);
+    const int delta_softplus = (flags & SELSCAN_FLAG_SOFTPLUS) != 0;
     bool empty = false;
-    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty);
+    int rc = check_fwd_args(x, delta, A, B, C, y, Bsz, L, D, N, dtype, h0, hT, &empty, Dskip, z);
     if (rc != SELSCAN_OK || empty) return rc;
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     const size_t state_bytes = (size_t)(Bsz * D * N) * 4;
@@ -703,7 +716,7 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     // 2700 or 4096 steps against 43 ms in pieces of 676 (fewer, larger
     // copies and launches per call).
     // SELSCAN_HOST_PIECE overrides it, for tests.
-    const size_t step_in = (size_t)Bsz * (size_t)(2 * D + 2 * N) * es;
+    const size_t step_in = (size_t)Bsz * (size_t)((z ? 3 : 2) * D + 2 * N) * es;
     int64_t lp = (int64_t)((32u << 20) / (step_in ? step_in : 1));
     if (lp < 64) lp = 64;
     if (lp >= L && L >= 128) lp = (L + 1) / 2;
@@ -713,14 +726,15 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     const int64_t pieces = (L + lp - 1) / lp;
     const bool chain = pieces > 1 || h0 || hT;
 
-    // Device staging: per slot x, delta, y (Bsz, lp, D) and B, C (Bsz, lp, N);
-    // then A and two states (piece p reads one and writes the other, so no
-    // scan updates its state in place). Every part starts on a 256-byte
-    // boundary.
+    // Device staging: per slot x, delta, y (and z) (Bsz, lp, D) and B, C
+    // (Bsz, lp, N); then A, Dskip, and two states (piece p reads one and
+    // writes the other, so no scan updates its state in place). Every part
+    // starts on a 256-byte boundary.
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
     const size_t bx = up((size_t)(Bsz * lp * D) * es), bn = up((size_t)(Bsz * lp * N) * es);
-    const size_t slot_bytes = 3 * bx + 2 * bn;
-    const size_t total = 2 * slot_bytes + up((size_t)(D * N) * 4) + (chain ? 2 * up(state_bytes) : 0);
+    const size_t slot_bytes = (z ? 4 : 3) * bx + 2 * bn;
+    const size_t a_bytes = up((size_t)(D * N) * 4), dsk_bytes = Dskip ? up((size_t)D * 4) : 0;
+    const size_t total = 2 * slot_bytes + a_bytes + dsk_bytes + (chain ? 2 * up(state_bytes) : 0);
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
@@ -746,13 +760,16 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
     cudaStreamWaitEvent(hp->in2, ev_alloc, 0);
     cudaStreamWaitEvent(hp->out, ev_alloc, 0);
     float *A_d = reinterpret_cast<float *>(ws + 2 * slot_bytes);
+    float *Dskip_d = Dskip ? reinterpret_cast<float *>(ws + 2 * slot_bytes + a_bytes) : nullptr;
     float *state_d[2] = {nullptr, nullptr};
     if (chain) {
-        state_d[0] = reinterpret_cast<float *>(ws + 2 * slot_bytes + up((size_t)(D * N) * 4));
+        state_d[0] = reinterpret_cast<float *>(ws + 2 * slot_bytes + a_bytes + dsk_bytes);
         state_d[1] = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(state_d[0]) + up(state_bytes));
     }
 
     e = cudaMemcpyAsync(A_d, A, (size_t)(D * N) * 4, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess && Dskip)
+        e = cudaMemcpyAsync(Dskip_d, Dskip, (size_t)D * 4, cudaMemcpyHostToDevice, hp->in);
     if (e == cudaSuccess && h0)
         e = cudaMemcpyAsync(state_d[0], h0, state_bytes, cudaMemcpyHostToDevice, hp->in);
 
@@ -762,6 +779,7 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
         const int slot = (int)(p & 1);
         unsigned char *base = ws + slot * slot_bytes;
         void *x_d = base, *dl_d = base + bx, *y_d = base + 2 * bx, *B_d = base + 3 * bx, *C_d = base + 3 * bx + bn;
+        void *z_d = z ? base + 3 * bx + 2 * bn : nullptr;
         const int64_t l0 = p * lp;
         const int64_t n = L - l0 < lp ? L - l0 : lp;
         const size_t wx = (size_t)(n * D) * es, wn = (size_t)(n * N) * es;
@@ -779,6 +797,8 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
             e = copy_rows(B_d, wn, static_cast<const unsigned char *>(B) + on, npitch, wn, rows, cudaMemcpyHostToDevice, hp->in);
         if (e == cudaSuccess)
             e = copy_rows(C_d, wn, static_cast<const unsigned char *>(C) + on, npitch, wn, rows, cudaMemcpyHostToDevice, in2);
+        if (e == cudaSuccess && z)
+            e = copy_rows(z_d, wx, static_cast<const unsigned char *>(z) + ox, xpitch, wx, rows, cudaMemcpyHostToDevice, in2);
         if (e != cudaSuccess) break;
         cudaEventRecord(ev_in[slot], hp->in);
         if (two_in) cudaEventRecord(ev_in2[slot], in2);
@@ -797,7 +817,9 @@ extern "C" int selscan_fwd_host(const void *x, const void *delta, const float *A
         a.h0 = h_in;
         a.hT = h_out;
         a.Bsz = Bsz; a.L = n; a.D = D; a.N = N;
+        a.Dskip = Dskip_d; a.z = z_d;
         a.softplus = delta_softplus ? 1 : 0;
+        a.zoh = (flags & SELSCAN_FLAG_ZOH) ? 1 : 0;
         rc = launch_fwd(a, plan, dtype, dev, sms, hp->comp);
         if (rc != SELSCAN_OK) break;
         cudaEventRecord(ev_comp[slot], hp->comp);

@@ -392,21 +392,23 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     // columns (one core row) per 16-byte store.
     const int t = 16 * warp + lane;
     const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+    // The whole row first (one wait for the four loads).
+    uint32_t graw[Q / 16][16];
 #pragma unroll
-    for (int s0 = 0; s0 < Q; s0 += 16) {
-        float g[16];
-        tmem_ld16(tG + lanes + (uint32_t)s0, g);
-        if (lane < 16) {
+    for (int q = 0; q < Q / 16; ++q)
+        tmem_ld16_async(tG + lanes + (uint32_t)(16 * q), graw[q]);
+    tmem_wait_ld();
+    if (lane < 16) {
+        const float st = s[t];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float m[8];
+        for (int s0 = 0; s0 < Q; s0 += 8) {
+            float m[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = s0 + 8 * half + i;
-                    m[i] = r <= t ? g[8 * half + i] * ex2((s[t] - s[r]) * kLog2e) * dl[r] : 0.0f;
-                }
-                *reinterpret_cast<uint4 *>(A2 + core_index(t, s0 + 8 * half, Q)) = pack8(m);
+            for (int i = 0; i < 8; ++i) {
+                const int r = s0 + i;
+                m[i] = r <= t ? __uint_as_float(graw[r / 16][r % 16]) * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
             }
+            *reinterpret_cast<uint4 *>(A2 + core_index(t, s0, Q)) = pack8(m);
         }
     }
     fence_proxy_async_smem();
@@ -427,10 +429,17 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     const float et = es[t < Q ? t : 0];
 #pragma unroll
     for (int p0 = 0; p0 < P; p0 += 16) {
-        float v[16], hv[16];
-        tmem_ld16(tY + lanes + (uint32_t)p0, v);
+        uint32_t vr[16], hr[16];
+        tmem_ld16_async(tY + lanes + (uint32_t)p0, vr);
         if (carry)
-            tmem_ld16(tH + lanes + (uint32_t)p0, hv);
+            tmem_ld16_async(tH + lanes + (uint32_t)p0, hr);
+        tmem_wait_ld();
+        float v[16], hv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = __uint_as_float(vr[i]);
+            hv[i] = __uint_as_float(hr[i]);
+        }
         if (mine) {
             if (carry) {
 #pragma unroll

@@ -22,7 +22,8 @@ def fake_fwd(orc):
 
 
 def fake_bwd(orc):
-    def f(x, delta, A, B, C, dy, delta_softplus=False, h0=None, dhT=None, want_dh0=True, stream=None):
+    def f(x, delta, A, B, C, dy, delta_softplus=False, h0=None, dhT=None, want_dh0=True, stream=None,
+          check=False):
         n = lambda t: None if t is None else t.detach().numpy().astype(np.float64)
         g = orc.selscan_bwd(x.detach().numpy(), delta.detach().numpy(), A.detach().numpy(),
                             B.detach().numpy(), C.detach().numpy(), n(dy), delta_softplus, h0=n(h0), ghT=n(dhT))
@@ -85,3 +86,27 @@ def test_smoke_backward_block_runs_on_stand_ins(orc, monkeypatch):
     monkeypatch.setattr(ss, "selscan_bwd", fake_bwd(orc))
     err = lambda got, ref: float(np.max(np.abs(got - ref) / (1.0 + np.abs(ref))))
     ge._smoke_backward(torch.device("cpu"), err)
+
+
+def test_selective_scan_check_reaches_both_passes(orc, monkeypatch):
+    """selective_scan(check=True) asks the forward and the backward call to
+    wait for their kernels and report a timed-out wait."""
+    seen = []
+    fwd, bwd = fake_fwd(orc), fake_bwd(orc)
+
+    def f(*a, check=False, **kw):
+        seen.append(("fwd", check))
+        return fwd(*a, **kw)
+
+    def b(*a, check=False, **kw):
+        seen.append(("bwd", check))
+        return bwd(*a, **kw)
+
+    monkeypatch.setattr(ss, "selscan_fwd", f)
+    monkeypatch.setattr(ss, "selscan_bwd", b)
+    inp = W.fwd_inputs(1, 5, 2, 4, seed=23, a_init="loguniform")
+    x, dl, A, B, C = (torch.tensor(inp.f32(k) if k != "A" else inp.A, requires_grad=True)
+                      for k in ("x", "delta", "A", "B", "C"))
+    y, hT = ss.selective_scan(x, dl, A, B, C, True, check=True)
+    y.sum().backward()
+    assert seen == [("fwd", True), ("bwd", True)]

@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: every wait inside the
-kernels is bounded. Here the chunked forward path's reduction items withhold
-their completion flags (a flag that nothing sets; selscan_test_fault_injection),
-so the readouts of later chunks run their wait to a short limit; the kernel
+kernels is bounded. Here the chunked forward path never announces its
+composed chunk carries (a flag that nothing sets; selscan_test_fault_injection),
+so the correction passes of later chunks run their wait to a short limit; the kernel
 must end, the host must read SELSCAN_ERR_TIMEOUT with fault code 2 on the
 stream the kernel ran on (and on no other), and the context must stay usable
 for a correct call right after."""
@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 def test_withheld_carries_end_in_timeout_status(orc, monkeypatch):
     inp = W.fwd_inputs(2, 512, 256, 16, seed=21, with_h0=True)
     x, dl, A, B, C, h0 = fwd_dev(inp)
-    monkeypatch.setenv("SELSCAN_CHUNK", "64")            # 8 chunks: readouts of chunks 1..7 wait
+    monkeypatch.setenv("SELSCAN_CHUNK", "64")            # 8 chunks: corrections of chunks 1..7 wait
     assert ss.fwd_plan(2, 512, 256, 16)["chunks"] == 8
     other = torch.cuda.Stream()
     ss.check_device_error(other)

@@ -85,3 +85,22 @@ def test_host_calls_behind_busy_device_are_deterministic():
     y1 = ss.selscan_fwd(x, dl, A, B, C, True)
     y2 = ss.selscan_fwd(x, dl, A, B, C, True)
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("form", ["gated", "zoh", "gated_zoh"])
+def test_gated_and_zoh_from_host(orc, monkeypatch, form):
+    """selscan_fwd_host_ex: the block's skip and gate and the zero-order hold
+    from host buffers, over several pieces, against the oracle."""
+    monkeypatch.setenv("SELSCAN_HOST_PIECE", "64")
+    inp = W.fwd_inputs(2, 300, 96, 16, seed=61, with_h0=True)
+    x, dl, A, B, C, h0 = host(inp, True)
+    gated, zoh = form != "zoh", form != "gated"
+    Dskip, z = W.gate_inputs(2, 300, 96, seed=61)
+    kw = {"D_skip": torch.from_numpy(Dskip).pin_memory(), "z": torch.from_numpy(z).pin_memory()} if gated else {}
+    y, hT = ss.selscan_fwd(x, dl, A, B, C, True, h0, return_final_state=True, zoh=zoh, **kw)
+    assert y.device.type == "cpu"
+    yr, hr = orc.selscan_fwd(inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), True,
+                             inp.h0.astype(np.float64), Dskip=Dskip if gated else None, z=z if gated else None,
+                             zoh=zoh)
+    assert scaled_err(as_np(y), yr) <= TOL[W.F32]
+    assert scaled_err(as_np(hT), hr) <= TOL[W.F32]

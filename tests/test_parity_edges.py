@@ -214,7 +214,7 @@ def test_in_place_gated_output_over_z(orc, monkeypatch):
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("path", ["tma-chunked", "plain-chunked"])
 def test_resume_in_place_on_chunked_paths(orc, monkeypatch, dtype, path):
-    """hT written over h0 while every chunk's readout reads h0."""
+    """hT written over h0 while every chunk's first pass may still read h0."""
     for k, v in PATHS[path].items():
         monkeypatch.setenv(k, v)
     inp = _fused_chunked_inputs(dtype, seed=41)
