@@ -18,9 +18,11 @@
 //   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q);
 //   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
 //      written as fp16 in the output kernel's operand layout, and hT;
-//   3. ssd_out_kernel: G = C B^T (M = Q, N = Q, K = N) and C H_in (K = N)
-//      into two TMEM tiles, then the masked, decayed G times X (M = Q, N = P,
-//      K = Q) into a third; y = G X + diag(e^s) C H_in.
+//      The same launch has one more CTA per batch row and chunk that forms
+//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32.
+//   3. ssd_out_kernel: C H_in (K = N) into one TMEM tile, the masked and
+//      decayed G (from shared memory) times X (M = Q, N = P, K = Q) into a
+//      second; y = G X + diag(e^s) C H_in.
 // Each CTA brings every tile it needs into shared memory in one round trip
 // (cp.async, zeros past the sequence), then converts and transposes there.
 // Operands are fp16 in shared memory (bf16 and fp32 inputs are converted
@@ -54,6 +56,7 @@ struct SsdArgs {
     float *hT;           // (Bsz, H, N, P) or null
     float *S;            // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n]
     __half *Hin;         // (Bsz, H, nch, P x N): the state entering each chunk, fp16 operand order
+    float *G;            // (Bsz, nch, Q, Q): C B^T of each chunk, [t][r]
     float *dec;          // (Bsz, H, nch): exp(s_last) of each chunk
     unsigned *fault;
     int64_t Bsz, L, H;
@@ -113,6 +116,49 @@ __device__ __forceinline__ void rows_to_operand(const T *src, __half *dst)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             v[i] = to_f32(src[r * K + k + i]);
+        *reinterpret_cast<uint4 *>(dst + core_index(r, k, K)) = pack8(v);
+    }
+}
+
+// Rows [0, Q) of a row-major global tile (row stride ld elements, K columns,
+// rows >= rows zero) as a K-major fp16 operand in core-matrix order. Every
+// load of the tile is issued before the first store, so a thread waits on
+// memory once.
+template <typename T, int Q, int K>
+__device__ __forceinline__ void global_rows_to_operand(const T *g, int64_t ld, int rows, __half *dst)
+{
+    constexpr int PER = Q * (K / 8) / kSsdThreads;   // eight-column pieces per thread
+    static_assert(PER * kSsdThreads == Q * (K / 8), "the tile must split evenly over the threads");
+    constexpr int W = (int)sizeof(T) * 8 / 16;       // 16-byte words per piece
+    uint4 raw[PER][W];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int e = threadIdx.x + q * kSsdThreads, r = e / (K / 8), k = (e % (K / 8)) * 8;
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+            raw[q][w] = r < rows ? __ldg(reinterpret_cast<const uint4 *>(g + (int64_t)r * ld + k) + w)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int e = threadIdx.x + q * kSsdThreads, r = e / (K / 8), k = (e % (K / 8)) * 8;
+        float v[8];
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t u[4] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(u[i] << 16);
+                v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                v[4 * w] = __uint_as_float(raw[q][w].x);
+                v[4 * w + 1] = __uint_as_float(raw[q][w].y);
+                v[4 * w + 2] = __uint_as_float(raw[q][w].z);
+                v[4 * w + 3] = __uint_as_float(raw[q][w].w);
+            }
+        }
         *reinterpret_cast<uint4 *>(dst + core_index(r, k, K)) = pack8(v);
     }
 }
@@ -178,12 +224,21 @@ __device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t parity)
     return __syncthreads_and(mbar_wait(bar, parity));
 }
 
+// TMEM columns of the state kernel: the state's P, or the 64 of C B^T.
+template <int P>
+__host__ __device__ constexpr int ssd_state_cols()
+{
+    return P < 64 ? 64 : P;
+}
+
 // 1. Each chunk's contribution to the state, S = (B o w)^T X (N x P),
-// stored transposed, [p][n], for the carry scan.
+// stored transposed, [p][n], for the carry scan. CTAs with blockIdx.y == H
+// instead form C B^T of their chunk (fp32, [t][r]) for the output kernel.
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 {
     constexpr int Q = kSsdQ;
+    constexpr int COLS = ssd_state_cols<P>();
     extern __shared__ __align__(1024) unsigned char sm[];
     __half *A3 = reinterpret_cast<__half *>(sm);                  // (B o w)^T: N rows, K = Q
     __half *BX = A3 + N * Q;                                       // X^T: P rows, K = Q
@@ -202,7 +257,57 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     // TMEM first: the allocation permit is given up at once, so the SM can
     // start the next CTA while this one loads.
     if (warp == 0)
-        tmem_alloc(&tbase, P);
+        tmem_alloc(&tbase, COLS);
+
+    if (h == a.H) {
+        // C B^T of the chunk: C and B rows as K-major operands (over the
+        // space the state's operands use in the other CTAs).
+        __half *A1 = A3, *B1 = reinterpret_cast<__half *>(rB);
+        global_rows_to_operand<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, A1);
+        global_rows_to_operand<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, B1);
+        if (tid == 0) {
+            mbar_init(&mbar, 1);
+            fence_mbar_init();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tm = tbase;
+        if (tid == 0) {
+            constexpr uint32_t id = umma_idesc_f16(Q, Q);
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk)
+                umma_f16(tm, umma_tile_desc(A1, N, kk), umma_tile_desc(B1, N, kk), id, kk > 0);
+            umma_commit(&mbar);
+        }
+        const bool ok = mma_wait(&mbar, 0);
+        tc_fence_after();
+        // Row t of C B^T sits in lane 32w + (t - 16w) of warp w (M = 64).
+        uint32_t graw[Q / 16][16];
+#pragma unroll
+        for (int q = 0; q < Q / 16; ++q)
+            tmem_ld16_async(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)(16 * q), graw[q]);
+        tmem_wait_ld();
+        if (ok && lane < 16) {
+            const int t = 16 * warp + lane;
+            float4 *dst = reinterpret_cast<float4 *>(a.G + ((b * a.nch + c) * Q + t) * Q);
+#pragma unroll
+            for (int q = 0; q < Q / 4; ++q)
+                dst[q] = make_float4(__uint_as_float(graw[q / 4][(q % 4) * 4]),
+                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 1]),
+                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 2]),
+                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 3]));
+        }
+        if (tid == 0 && !ok)
+            record_fault(a.fault, kFaultMmaTimeout);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0)
+            tmem_dealloc(tm, COLS);
+        return;
+    }
+
     copy_tile<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, rB);
     copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
     ssd_cp_commit();
@@ -257,7 +362,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
-        tmem_dealloc(tm, P);
+        tmem_dealloc(tm, COLS);
 }
 
 // 2. The state entering each chunk, in chunk order: fp32 carries, stored as
@@ -317,9 +422,9 @@ __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
 // 3. Each chunk's outputs: the masked dual form inside the chunk plus the
 // decayed incoming state.
 template <int P>
-__host__ __device__ constexpr int ssd_out_cols()   // TMEM columns: G (64), G X (P) and C H_in (P)
+__host__ __device__ constexpr int ssd_out_cols()   // TMEM columns: G X (P) and C H_in (P)
 {
-    return 64 + 2 * P <= 128 ? 128 : (64 + 2 * P <= 256 ? 256 : 512);
+    return 2 * P <= 32 ? 32 : (2 * P <= 64 ? 64 : (2 * P <= 128 ? 128 : 256));
 }
 
 template <typename T, int N, int P>
@@ -329,13 +434,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     constexpr int COLS = ssd_out_cols<P>();
     extern __shared__ __align__(1024) unsigned char sm[];
     __half *A1 = reinterpret_cast<__half *>(sm);                       // C: Q rows, K = N
-    __half *B1 = A1 + Q * N;                                            // B: Q rows, K = N
-    __half *B4 = B1 + Q * N;                                            // H_in^T: P rows, K = N
+    __half *B4 = A1 + Q * N;                                            // H_in^T: P rows, K = N
     __half *BX = B4 + P * N;                                            // X^T: P rows, K = Q
-    T *rC = reinterpret_cast<T *>(BX + P * Q);                          // C tile [Q][N]
-    __half *A2 = reinterpret_cast<__half *>(rC);                        // masked G (over rC once converted)
-    T *rB = rC + Q * N;                                                 // B tile [Q][N]
-    T *rX = rB + Q * N;                                                 // X tile [Q][P]
+    __half *A2 = BX + P * Q;                                            // masked G: Q rows, K = Q
+    float *rG = reinterpret_cast<float *>(A2 + Q * Q);                  // C B^T [Q][Q]
+    T *rX = reinterpret_cast<T *>(rG + Q * Q);                          // X tile [Q][P]
     float *dl = reinterpret_cast<float *>(rX + Q * P);
     float *s = dl + Q;
     float *es = s + Q;
@@ -349,12 +452,12 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     const bool carry = c > 0 || a.h0 != nullptr;
     if (warp == 0)   // first, as in the state kernel
         tmem_alloc(&tbase, COLS);
-    copy_tile<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, rC);
-    copy_tile<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, rB);
+    copy_tile<float, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, rG);
     copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
     if (carry)   // already in operand order: a plain copy
         copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
     ssd_cp_commit();
+    global_rows_to_operand<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, A1);
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
@@ -365,51 +468,31 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     __syncthreads();
     if (tid < Q)
         es[tid] = ex2(s[tid] * kLog2e);
-    rows_to_operand<T, Q, N>(rC, A1);
-    rows_to_operand<T, Q, N>(rB, B1);
     transpose_to_operand<T, Q, P>(rX, nullptr, BX);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tG = tbase, tY = tbase + 64, tH = tbase + 64 + P;
-    if (tid == 0) {
-        constexpr uint32_t idG = umma_idesc_f16(Q, Q), idY = umma_idesc_f16(Q, P);
+    const uint32_t tY = tbase, tH = tbase + P;
+    if (tid == 0 && carry) {
+        constexpr uint32_t id = umma_idesc_f16(Q, P);
 #pragma unroll
         for (int kk = 0; kk < N / 16; ++kk)
-            umma_f16(tG, umma_tile_desc(A1, N, kk), umma_tile_desc(B1, N, kk), idG, kk > 0);
-        if (carry) {
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk)
-                umma_f16(tH, umma_tile_desc(A1, N, kk), umma_tile_desc(B4, N, kk), idY, kk > 0);
-        }
-        umma_commit(&mbar);
+            umma_f16(tH, umma_tile_desc(A1, N, kk), umma_tile_desc(B4, N, kk), id, kk > 0);
     }
-    bool ok = mma_wait(&mbar, 0);
-    tc_fence_after();
-    // Row t of G sits in lane 32w + (t - 16w) of warp w (M = 64). Mask,
-    // decay and scale it into the masked product's A operand, eight
-    // columns (one core row) per 16-byte store.
-    const int t = 16 * warp + lane;
-    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
-    // The whole row first (one wait for the four loads).
-    uint32_t graw[Q / 16][16];
-#pragma unroll
-    for (int q = 0; q < Q / 16; ++q)
-        tmem_ld16_async(tG + lanes + (uint32_t)(16 * q), graw[q]);
-    tmem_wait_ld();
-    if (lane < 16) {
+    // Mask, decay and scale C B^T into the masked product's A operand while
+    // C H_in runs: every thread takes eight columns (one core row) at a time.
+#pragma unroll 2
+    for (int e = tid; e < Q * (Q / 8); e += kSsdThreads) {
+        const int t = e / (Q / 8), r0 = (e % (Q / 8)) * 8;
         const float st = s[t];
+        float m[8];
 #pragma unroll
-        for (int s0 = 0; s0 < Q; s0 += 8) {
-            float m[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = s0 + i;
-                m[i] = r <= t ? __uint_as_float(graw[r / 16][r % 16]) * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
-            }
-            *reinterpret_cast<uint4 *>(A2 + core_index(t, s0, Q)) = pack8(m);
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + i;
+            m[i] = r <= t ? rG[t * Q + r] * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
         }
+        *reinterpret_cast<uint4 *>(A2 + core_index(t, r0, Q)) = pack8(m);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -420,10 +503,13 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
 #pragma unroll
         for (int kk = 0; kk < Q / 16; ++kk)
             umma_f16(tY, umma_tile_desc(A2, Q, kk), umma_tile_desc(BX, Q, kk), id, kk > 0);
-        umma_commit(&mbar);
+        umma_commit(&mbar);   // both products
     }
-    ok = mma_wait(&mbar, 1) && ok;
+    const bool ok = mma_wait(&mbar, 0);
     tc_fence_after();
+    // Row t of each product sits in lane 32w + (t - 16w) of warp w (M = 64).
+    const int t = 16 * warp + lane;
+    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
     T *yg = static_cast<T *>(a.y) + ((b * a.L + t0 + t) * a.H + h) * P;
     const bool mine = ok && lane < 16 && t < rows;
     const float et = es[t < Q ? t : 0];
@@ -448,11 +534,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
             }
             if constexpr (sizeof(T) == 2) {
                 uint4 u[2];
-                uint32_t *w = reinterpret_cast<uint32_t *>(u);
+                uint32_t *wd = reinterpret_cast<uint32_t *>(u);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const __nv_bfloat162 q = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                    w[i] = *reinterpret_cast<const uint32_t *>(&q);
+                    wd[i] = *reinterpret_cast<const uint32_t *>(&q);
                 }
                 reinterpret_cast<uint4 *>(yg + p0)[0] = u[0];
                 reinterpret_cast<uint4 *>(yg + p0)[1] = u[1];
@@ -480,8 +566,8 @@ constexpr size_t ssd_state_smem()
 template <typename T, int N, int P>
 constexpr size_t ssd_out_smem()
 {
-    return ((size_t)2 * kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ) * 2 +
-           (size_t)kSsdQ * (2 * N + P) * sizeof(T) + 3 * kSsdQ * 4;
+    return ((size_t)kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ + (size_t)kSsdQ * kSsdQ) * 2 +
+           (size_t)kSsdQ * kSsdQ * 4 + (size_t)kSsdQ * P * sizeof(T) + 3 * kSsdQ * 4;
 }
 
 // Shared memory that keeps at most max_ctas CTAs of a kernel on one SM, so
@@ -501,13 +587,13 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
 {
     auto k1 = ssd_state_kernel<T, N, P>;
     auto k3 = ssd_out_kernel<T, N, P>;
-    const size_t s1 = ssd_pad(ssd_state_smem<T, N, P>(), 512 / P);
+    const size_t s1 = ssd_pad(ssd_state_smem<T, N, P>(), 512 / ssd_state_cols<P>());
     const size_t s3 = ssd_pad(ssd_out_smem<T, N, P>(), 512 / ssd_out_cols<P>());
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3);
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
-    k1<<<grid, kSsdThreads, s1, st>>>(a);
+    k1<<<dim3(grid.x, grid.y + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
     const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
     ssd_carry_kernel<N, P><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
     k3<<<grid, kSsdThreads, s3, st>>>(a);
@@ -554,8 +640,8 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
         return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
     if (Bsz == 0 || H == 0)
         return SELSCAN_OK;
-    if (Bsz > 65535 || H > 65535)
-        return fail(SELSCAN_ERR_UNSUPPORTED, "SSD: Bsz and H must be at most 65535");
+    if (Bsz > 65535 || H > 65534)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "SSD: Bsz must be at most 65535 and H at most 65534");
     if (!A || (L > 0 && (!x || !dt || !B || !C || !y)))
         return fail(SELSCAN_ERR_INVALID_ARG, "A, and x, dt, B, C, y when L > 0, must be non-NULL");
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;   // element size of x, B, C, y
@@ -587,14 +673,15 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
-    // Workspace: S (fp32), the incoming states (fp16), the chunk decays.
+    // Workspace: S (fp32), the incoming states (fp16), C B^T of every chunk
+    // (fp32), the chunk decays.
     const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 4, hbytes = sbytes / 2,
-                 dbytes = (size_t)(Bsz * H * nch) * 4;
+                 gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 4, dbytes = (size_t)(Bsz * H * nch) * 4;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + hbytes + dbytes, pool, st);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + hbytes + gbytes + dbytes, pool, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", sbytes + hbytes + dbytes,
+        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", sbytes + hbytes + gbytes + dbytes,
                     cudaGetErrorString(e));
     }
     SsdArgs a;
@@ -602,7 +689,8 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.y = y; a.h0 = h0; a.hT = hT;
     a.S = static_cast<float *>(ws);
     a.Hin = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes);
-    a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
+    a.G = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
+    a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes);
     a.Bsz = Bsz; a.L = L; a.H = H;
     a.nch = (int)nch;
     a.softplus = dt_softplus ? 1 : 0;
