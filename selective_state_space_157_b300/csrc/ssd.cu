@@ -182,26 +182,41 @@ __device__ __forceinline__ void transpose_to_operand(const T *src, const float *
     }
 }
 
+// The raw step pre-activations of one chunk, dt[t] for t = lane and
+// lane + 32 (0 past the sequence); warp 0 loads them ahead of other work.
+struct SsdDt {
+    float v[2];
+    float Ah;
+};
+
+__device__ __forceinline__ SsdDt ssd_dt_load(const SsdArgs &a, int64_t b, int64_t h, int64_t t0, int rows)
+{
+    const int lane = threadIdx.x;
+    SsdDt r;
+    r.Ah = __ldg(a.A + h);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int t = lane + 32 * i;
+        r.v[i] = t < rows ? __ldg(a.dt + (b * a.L + t0 + t) * a.H + h) : 0.0f;
+    }
+    return r;
+}
+
 // Step sizes and cumulative log-decays of one chunk: dl[t] (after softplus)
 // and s[t] = sum_{r <= t} dl[r] A[h], t < Q. Rows past the sequence get
 // dl = 0, so they neither decay nor add. Warp 0 only.
-__device__ __forceinline__ void ssd_decays(const SsdArgs &a, int64_t b, int64_t h, int64_t t0, int rows, float *dl,
-                                           float *s)
+__device__ __forceinline__ void ssd_decays_from(const SsdArgs &a, const SsdDt &raw, int rows, float *dl, float *s)
 {
     const int lane = threadIdx.x;
-    const float Ah = __ldg(a.A + h);
     float v[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int t = lane + 32 * i;
-        float d = 0.0f;
-        if (t < rows) {
-            d = __ldg(a.dt + (b * a.L + t0 + t) * a.H + h);
-            if (a.softplus)
-                d = softplus(d);
-        }
+        float d = raw.v[i];
+        if (t < rows && a.softplus)
+            d = softplus(d);
         dl[t] = d;
-        v[i] = d * Ah;
+        v[i] = d * raw.Ah;
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -215,6 +230,13 @@ __device__ __forceinline__ void ssd_decays(const SsdArgs &a, int64_t b, int64_t 
     const float first_half = __shfl_sync(0xffffffffu, v[0], 31);
     s[lane] = v[0];
     s[lane + 32] = v[1] + first_half;
+}
+
+// The same, loaded and computed in one go. Warp 0 only.
+__device__ __forceinline__ void ssd_decays(const SsdArgs &a, int64_t b, int64_t h, int64_t t0, int rows, float *dl,
+                                           float *s)
+{
+    ssd_decays_from(a, ssd_dt_load(a, b, h, t0, rows), rows, dl, s);
 }
 
 // Waits (bounded) for the phase with the given parity of an MMA completion
@@ -457,13 +479,16 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     if (carry)   // already in operand order: a plain copy
         copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
     ssd_cp_commit();
+    SsdDt dtv{};
+    if (warp == 0)   // in flight with the tiles
+        dtv = ssd_dt_load(a, b, h, t0, rows);
     global_rows_to_operand<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, A1);
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
     if (warp == 0)
-        ssd_decays(a, b, h, t0, rows, dl, s);
+        ssd_decays_from(a, dtv, rows, dl, s);
     ssd_cp_wait();
     __syncthreads();
     if (tid < Q)
