@@ -565,6 +565,29 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def pcie_rates(dev, nbytes=256 << 20, reps=4):
+    """One-way copy rates between pinned host memory and this GPU (GB/s),
+    timed with CUDA events on a side stream: the bound the end-to-end leg's
+    copies can approach."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(dev)
+    rates = []
+    for dst, src in ((d, h), (h, d)):
+        with torch.cuda.stream(st):
+            dst.copy_(src, non_blocking=True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            e1.record(st)
+        st.synchronize()
+        rates.append(reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, d
+    return rates[0], rates[1]
+
+
 def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
     """End to end through the public API: the step's inputs copied in from
     pinned host memory, the scan, y copied out, inside the timed region."""
@@ -600,8 +623,17 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
     t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = y_host.numel() * y_host.element_size() + (hT_host.numel() * 4 if hT_host is not None else 0)
+    h2d_gbs, d2h_gbs = pcie_rates(dev)
+    # The link copies both ways at once, so the copies alone take at least
+    # the longer of the two directions.
+    bound = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9))
+    per_step = t_e2e / e2e_steps
     return {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": per_step * 1e3,
+            "pcie": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "copy_bound_ms": bound * 1e3,
+                     "frac_of_copy_bound": bound / per_step,
+                     "note": "one-way rates of 256 MB pinned copies measured in this run"}}
 
 
 def measure_config(wid, args, world, local, dev, alu):

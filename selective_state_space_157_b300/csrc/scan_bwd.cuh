@@ -87,31 +87,40 @@ __host__ __device__ constexpr int bwd_main_smem(int P)
     return (2 * 3 * kBwdT * (kBwdThreads / P) + 2 * 2 * kBwdT * 4 * P + 2 * 4 * kBwdThreads + 2 * (kBwdThreads / P) +
             kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * (kBwdThreads / P) + kBwdT * kBwdWarps * 2 * 4 * P) * 4;
 }
+// Steps a stage of the local kernel stages: whole chunks, as many as keep the
+// values a thread loads ahead (at most 16 per array) in registers without
+// spills.
+__host__ __device__ constexpr int bwd_local_tt(int P)
+{
+    return P >= 8 ? 64 : (P >= 2 ? 32 : 16);
+}
 __host__ __device__ constexpr int bwd_local_smem(int P)
 {
-    return (kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * 4 * P) * 4;
+    return (bwd_local_tt(P) * (kBwdThreads / P) * 4 + 2 * bwd_local_tt(P) * 4 * P) * 4;
 }
 
 // The raw inputs of one chunk that this thread stages: loaded into registers
 // one chunk ahead, so the loads are in flight while the block works on the
 // current chunk. Element j = threadIdx.x + q * kBwdThreads of the chunk's
 // (step, chain) rows and (step, state) rows.
-template <int P> struct BwdRegs {
+template <int P, int TT> struct BwdRegs {
     static constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
-    static constexpr int RX = (kBwdT * CPB + kBwdThreads - 1) / kBwdThreads;
-    static constexpr int RB = (kBwdT * NP + kBwdThreads - 1) / kBwdThreads;
+    static constexpr int RX = (TT * CPB + kBwdThreads - 1) / kBwdThreads;
+    static constexpr int RB = (TT * NP + kBwdThreads - 1) / kBwdThreads;
     float u[RX], x[RX], gy[RX], B[RB], C[RB];
 };
 
-template <int P, bool WX, bool WGY, bool WB, bool WC>
-__device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0, int64_t t0, BwdRegs<P> &r)
+// Loads steps t0 .. t0 + TT (zeros from step lim on, and past D and N).
+template <int P, int TT, bool WX, bool WGY, bool WB, bool WC>
+__device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0, int64_t t0, int64_t lim,
+                                         BwdRegs<P, TT> &r)
 {
-    using R = BwdRegs<P>;
+    using R = BwdRegs<P, TT>;
 #pragma unroll
     for (int q = 0; q < R::RX; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
         const int i = j / R::CPB, c = j % R::CPB;
-        const bool ok = j < kBwdT * R::CPB && t0 + i < a.L && d0 + c < a.D;
+        const bool ok = j < TT * R::CPB && t0 + i < lim && d0 + c < a.D;
         const int64_t idx = (b * a.L + t0 + i) * a.D + d0 + c;
         r.u[q] = ok ? __ldg(a.delta + idx) : 0.0f;
         if (WX) r.x[q] = ok ? __ldg(a.x + idx) : 0.0f;
@@ -121,26 +130,26 @@ __device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0
     for (int q = 0; q < R::RB; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
         const int i = j / R::NP, m = j % R::NP;
-        const bool ok = j < kBwdT * R::NP && t0 + i < a.L && m < a.N;
+        const bool ok = j < TT * R::NP && t0 + i < lim && m < a.N;
         const int64_t idx = (b * a.L + t0 + i) * a.N + m;
         if (WB) r.B[q] = ok ? __ldg(a.B + idx) : 0.0f;
         if (WC) r.C[q] = ok ? __ldg(a.C + idx) : 0.0f;
     }
 }
 
-// Writes the loaded chunk to shared memory: (dl, x, gy, sigmoid(u)) per step
-// and chain (dl = 0 past L), B and C rows.
-template <int P, bool WX, bool WGY, bool WB, bool WC>
-__device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P> &r, int64_t d0, int64_t t0, float4 *s_in,
-                                        float *s_B, float *s_C)
+// Writes the loaded steps to shared memory: (dl, x, gy, sigmoid(u)) per step
+// and chain (dl = 0 from step lim on), B and C rows.
+template <int P, int TT, bool WX, bool WGY, bool WB, bool WC>
+__device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P, TT> &r, int64_t d0, int64_t t0,
+                                        int64_t lim, float4 *s_in, float *s_B, float *s_C)
 {
-    using R = BwdRegs<P>;
+    using R = BwdRegs<P, TT>;
 #pragma unroll
     for (int q = 0; q < R::RX; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
-        if (j < kBwdT * R::CPB) {
+        if (j < TT * R::CPB) {
             const int i = j / R::CPB, c = j % R::CPB;
-            const bool ok = t0 + i < a.L && d0 + c < a.D;
+            const bool ok = t0 + i < lim && d0 + c < a.D;
             const float dl = !ok ? 0.0f : (a.softplus ? softplus(r.u[q]) : r.u[q]);
             const float sg = (ok && a.softplus && WX && WGY) ? bwd_sigmoid(r.u[q]) : 1.0f;
             s_in[j] = make_float4(dl, WX ? r.x[q] : 0.0f, WGY ? r.gy[q] : 0.0f, sg);
@@ -149,7 +158,7 @@ __device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P> &r, i
 #pragma unroll
     for (int q = 0; q < R::RB; ++q) {
         const int j = threadIdx.x + q * kBwdThreads;
-        if (j < kBwdT * R::NP) {
+        if (j < TT * R::NP) {
             if (WB) s_B[j] = r.B[q];
             if (WC) s_C[j] = r.C[q];
         }
@@ -228,14 +237,18 @@ template <int P> __device__ __forceinline__ bool bwd_rs_writer(int lane)
 
 // ---------------------------------------------------------------- kernel 1
 // grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_local_smem(P) bytes.
+// Stages of TL = bwd_local_tt(P) steps (whole chunks; zeros past the
+// segment's end, which belong to the next segment), loaded into registers one
+// stage ahead.
 template <int P>
 __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs a)
 {
     constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
+    constexpr int TL = bwd_local_tt(P), CH = TL / kBwdT;
     extern __shared__ float4 bwd_smem4[];
     float4 *s_in = bwd_smem4;
-    float *s_B = reinterpret_cast<float *>(s_in + kBwdT * CPB);
-    float *s_C = s_B + kBwdT * NP;
+    float *s_B = reinterpret_cast<float *>(s_in + TL * CPB);
+    float *s_C = s_B + TL * NP;
 
     const int tid = threadIdx.x, j = tid % P, c = tid / P;
     const int64_t b = blockIdx.y, k = blockIdx.z;
@@ -250,40 +263,48 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
         A2[e].y = (chain && n0 + 1 < N) ? __ldg(a.A + d * N + n0 + 1) * kLog2e : 0.0f;
     }
     const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
+    const int64_t s0 = ci0 * kBwdT, s1 = min(ci1 * kBwdT, L);   // the segment's steps
+    const int nst = (int)((s1 - s0 + TL - 1) / TL);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
 
     // Forward from a zero state: checkpoints, end state, sum of dl (chunk
     // sums added with compensation).
     float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float S = 0.0f, Sc = 0.0f;
-    BwdRegs<P> r;
-    bwd_load<P, true, false, true, false>(a, b, d0, ci0 * kBwdT, r);
-    for (int64_t ci = ci0; ci < ci1; ++ci) {
+    BwdRegs<P, TL> r;
+    bwd_load<P, TL, true, false, true, false>(a, b, d0, s0, s1, r);
+    for (int st = 0; st < nst; ++st) {
+        const int64_t t0 = s0 + (int64_t)st * TL;
         __syncthreads();
-        bwd_put<P, true, false, true, false>(a, r, d0, ci * kBwdT, s_in, s_B, s_C);
-        if (ci + 1 < ci1)
-            bwd_load<P, true, false, true, false>(a, b, d0, (ci + 1) * kBwdT, r);
-        if (chain) {
-            const int64_t o = (b * nch + ci) * D + d;
-            *reinterpret_cast<float4 *>(a.ckpt + o * NP + kBwdS * j) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-            if (j == 0)
-                a.spre[o] = S;
-        }
+        bwd_put<P, TL, true, false, true, false>(a, r, d0, t0, s1, s_in, s_B, s_C);
+        if (st + 1 < nst)
+            bwd_load<P, TL, true, false, true, false>(a, b, d0, t0 + TL, s1, r);
         __syncthreads();
-        float sc = 0.0f;
+#pragma unroll 1
+        for (int q = 0; q < CH; ++q) {
+            const int64_t ci = ci0 + (int64_t)st * CH + q;
+            if (chain && ci < ci1) {
+                const int64_t o = (b * nch + ci) * D + d;
+                *reinterpret_cast<float4 *>(a.ckpt + o * NP + kBwdS * j) =
+                    make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                if (j == 0)
+                    a.spre[o] = S;
+            }
+            float sc = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kBwdT; ++i) {
-            const float4 in = s_in[i * CPB + c];
-            const float4 B4 = *reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j);
-            const float dl = in.x, u = dl * in.y;
-            const float2 dl2 = f2(dl), u2 = f2(u);
-            h[0] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
-            h[1] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
-            sc += dl;
+            for (int i = q * kBwdT; i < (q + 1) * kBwdT; ++i) {
+                const float4 in = s_in[i * CPB + c];
+                const float4 B4 = *reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j);
+                const float dl = in.x, u = dl * in.y;
+                const float2 dl2 = f2(dl), u2 = f2(u);
+                h[0] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
+                h[1] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
+                sc += dl;
+            }
+            const float yk = sc - Sc, tk = S + yk;   // S += sc, compensated
+            Sc = (tk - S) - yk;
+            S = tk;
         }
-        const float yk = sc - Sc, tk = S + yk;   // S += sc, compensated
-        Sc = (tk - S) - yk;
-        S = tk;
     }
     if (chain) {
         *reinterpret_cast<float4 *>(a.hl + pair) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
@@ -295,15 +316,16 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
 
     // Adjoint from zero at the segment's end back to its start.
     float2 g[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    bwd_load<P, false, true, false, true>(a, b, d0, (ci1 - 1) * kBwdT, r);
-    for (int64_t ci = ci1 - 1; ci >= ci0; --ci) {
+    bwd_load<P, TL, false, true, false, true>(a, b, d0, s0 + (int64_t)(nst - 1) * TL, s1, r);
+    for (int st = nst - 1; st >= 0; --st) {
+        const int64_t t0 = s0 + (int64_t)st * TL;
         __syncthreads();
-        bwd_put<P, false, true, false, true>(a, r, d0, ci * kBwdT, s_in, s_B, s_C);
-        if (ci > ci0)
-            bwd_load<P, false, true, false, true>(a, b, d0, (ci - 1) * kBwdT, r);
+        bwd_put<P, TL, false, true, false, true>(a, r, d0, t0, s1, s_in, s_B, s_C);
+        if (st > 0)
+            bwd_load<P, TL, false, true, false, true>(a, b, d0, t0 - TL, s1, r);
         __syncthreads();
-#pragma unroll
-        for (int i = kBwdT - 1; i >= 0; --i) {
+#pragma unroll 4
+        for (int i = TL - 1; i >= 0; --i) {
             const float4 in = s_in[i * CPB + c];
             const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
             const float2 dl2 = f2(in.x), gy2 = f2(in.z);
