@@ -15,7 +15,8 @@
 // and the chunk's own contribution to the state is
 //   S = (B o w)^T X,   w_r = exp(s_last - s_r) dl_r,
 // with H_out = exp(s_last) H_in + S. Three kernels:
-//   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q);
+//   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q),
+//      stored fp16 (the precision it has as an operand anyway);
 //   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
 //      written as fp16 in the output kernel's operand layout, and hT;
 //      The same launch has one more CTA per batch row and chunk that forms
@@ -54,7 +55,7 @@ struct SsdArgs {
     void *y;             // (Bsz, L, H, P), dtype
     const float *h0;     // (Bsz, H, N, P) or null
     float *hT;           // (Bsz, H, N, P) or null
-    float *S;            // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n]
+    __half *S;           // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n], fp16
     __half *Hin;         // (Bsz, H, nch, P x N): the state entering each chunk, fp16 operand order
     float *G;            // (Bsz, nch, Q, Q): C B^T of each chunk, [t][r]
     float *dec;          // (Bsz, H, nch): exp(s_last) of each chunk
@@ -254,7 +255,7 @@ __host__ __device__ constexpr int ssd_state_cols()
 }
 
 // 1. Each chunk's contribution to the state, S = (B o w)^T X (N x P),
-// stored transposed, [p][n], for the carry scan. CTAs with blockIdx.y == H
+// stored transposed, [p][n], fp16, for the carry scan. CTAs with blockIdx.y == H
 // instead form C B^T of their chunk (fp32, [t][r]) for the output kernel.
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     // a warp's lanes hold consecutive n, so the [p][n] stores coalesce.
     const int n = N == 128 ? 32 * warp + lane : 16 * warp + lane;
     const bool mine = ok && (N == 128 || lane < 16);
-    float *dst = a.S + ((b * a.H + h) * a.nch + c) * N * P + n;
+    __half *dst = a.S + ((b * a.H + h) * a.nch + c) * N * P + n;
 #pragma unroll
     for (int p0 = 0; p0 < P; p0 += 16) {
         float v[16];
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
         if (mine) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                dst[(p0 + i) * N] = v[i];
+                dst[(p0 + i) * N] = __float2half_rn(v[i]);
         }
     }
     if (tid == 0) {
@@ -408,29 +409,29 @@ __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
 #pragma unroll
     for (int q = 0; q < 8; ++q)
         carry[q] = a.h0 ? __ldg(a.h0 + bh * NP + (int64_t)(n0 + q) * P + p) : 0.0f;
-    const float *Sp = a.S + bh * a.nch * NP + pn;
+    const __half *Sp = a.S + bh * a.nch * NP + pn;
     __half *Hp = a.Hin + bh * a.nch * NP + core_index(p, n0, N);
     const float *dp = a.dec + bh * a.nch;
     for (int c0 = 0; c0 < a.nch; c0 += kCarryBatch) {
-        float4 sv[kCarryBatch][2];
+        uint4 sv[kCarryBatch];
         float dv[kCarryBatch];
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             const int cc = c0 + j < a.nch ? c0 + j : a.nch - 1;
-            const float4 *src = reinterpret_cast<const float4 *>(Sp + (int64_t)cc * NP);
-            sv[j][0] = __ldcg(src);
-            sv[j][1] = __ldcg(src + 1);
+            sv[j] = __ldcg(reinterpret_cast<const uint4 *>(Sp + (int64_t)cc * NP));
             dv[j] = __ldg(dp + cc);
         }
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             if (c0 + j < a.nch) {
                 *reinterpret_cast<uint4 *>(Hp + (int64_t)(c0 + j) * NP) = pack8(carry);
-                const float sj[8] = {sv[j][0].x, sv[j][0].y, sv[j][0].z, sv[j][0].w,
-                                     sv[j][1].x, sv[j][1].y, sv[j][1].z, sv[j][1].w};
+                const __half2 *hs = reinterpret_cast<const __half2 *>(&sv[j]);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    carry[q] = fmaf(dv[j], carry[q], sj[q]);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __half22float2(hs[q]);
+                    carry[2 * q] = fmaf(dv[j], carry[2 * q], f.x);
+                    carry[2 * q + 1] = fmaf(dv[j], carry[2 * q + 1], f.y);
+                }
             }
         }
     }
@@ -698,9 +699,9 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
-    // Workspace: S (fp32), the incoming states (fp16), C B^T of every chunk
+    // Workspace: S and the incoming states (fp16), C B^T of every chunk
     // (fp32), the chunk decays.
-    const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 4, hbytes = sbytes / 2,
+    const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 2, hbytes = sbytes,
                  gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 4, dbytes = (size_t)(Bsz * H * nch) * 4;
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + hbytes + gbytes + dbytes, pool, st);
@@ -712,7 +713,7 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     SsdArgs a;
     memset(&a, 0, sizeof a);
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.y = y; a.h0 = h0; a.hT = hT;
-    a.S = static_cast<float *>(ws);
+    a.S = static_cast<__half *>(ws);
     a.Hin = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes);
     a.G = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
     a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes);
