@@ -203,9 +203,18 @@ __device__ __forceinline__ SsdDt ssd_dt_load(const SsdArgs &a, int64_t b, int64_
     return r;
 }
 
+// A step's log-decay dl A is taken as at least -kSsdMinLogDecay. The chunk's
+// products use differences s_t - s_r of the cumulative sums; after a step of
+// dl A = -1280 (dl = 80, A = -16) the sums reach magnitudes where fp32 keeps
+// those differences only to about 1e-2. A decay of e^-40 already leaves less
+// than fp32 resolution of anything carried across that step (as the true,
+// smaller decay does), and with the bound |s| stays below 64 * 40 within a
+// chunk, where differences keep about 2e-4.
+constexpr float kSsdMinLogDecay = 40.0f;
+
 // Step sizes and cumulative log-decays of one chunk: dl[t] (after softplus)
-// and s[t] = sum_{r <= t} dl[r] A[h], t < Q. Rows past the sequence get
-// dl = 0, so they neither decay nor add. Warp 0 only.
+// and s[t] = sum_{r <= t} max(dl[r] A[h], -kSsdMinLogDecay), t < Q. Rows past
+// the sequence get dl = 0, so they neither decay nor add. Warp 0 only.
 __device__ __forceinline__ void ssd_decays_from(const SsdArgs &a, const SsdDt &raw, int rows, float *dl, float *s)
 {
     const int lane = threadIdx.x;
@@ -217,7 +226,7 @@ __device__ __forceinline__ void ssd_decays_from(const SsdArgs &a, const SsdDt &r
         if (t < rows && a.softplus)
             d = softplus(d);
         dl[t] = d;
-        v[i] = d * raw.Ah;
+        v[i] = fmaxf(d * raw.Ah, -kSsdMinLogDecay);
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

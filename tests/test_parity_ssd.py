@@ -77,3 +77,60 @@ def test_unsupported_sizes_are_refused():
         ss.ssd_fwd(x, torch.zeros(1, 4, 1, device="cuda"), -torch.ones(1, device="cuda"),
                    torch.zeros(1, 4, 64, device="cuda"), torch.zeros(1, 4, 64, device="cuda"))
     assert e.value.code == ss.ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- limiting cases
+# The limits of booiljung.github.io "3.1 LTI systems and input-dependent
+# parameters", section 0.4.2, for the scalar decay of each head: a step of 0
+# keeps the state (exp(0 A) = 1, no input), a large step resets it to the
+# current input term, and A = 0 turns the state into a running sum. Where the
+# sums cancel, the error is measured against the magnitude of what was
+# summed (the oracle on |x|, |B|, |C|, |h0|), the forward-error bound of a
+# floating-point sum, as for the selective scan's limits.
+
+def _run_edge(orc, dt, A, seed, softplus, cancelling, Bsz=1, L=200, H=3, P=64, N=128):
+    x, _, _, B, C, hh = W.ssd_inputs(Bsz, L, H, P, N, seed=seed, with_h0=True)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    y, hT = ss.ssd_fwd(dev(x), dev(dt), dev(A), dev(B), dev(C), softplus, h0=dev(hh), return_final_state=True,
+                       check=True)
+    yr, hr = orc.ssd_fwd(x, dt, A, B, C, softplus, h0=hh.astype(np.float64))
+    if cancelling:
+        ym, hm = orc.ssd_fwd(np.abs(x), dt, A, np.abs(B), np.abs(C), softplus, h0=np.abs(hh).astype(np.float64))
+        ey = float(np.max(np.abs(to_np(y) - yr) / (1.0 + np.abs(ym))))
+        eh = float(np.max(np.abs(to_np(hT) - hr) / (1.0 + np.abs(hm))))
+    else:
+        ey, eh = scaled_err(to_np(y), yr), scaled_err(to_np(hT), hr)
+    assert ey <= TOL, f"y error {ey:.3e}"
+    assert eh <= TOL, f"hT error {eh:.3e}"
+    return hh, hT
+
+
+def test_zero_step_keeps_the_state(orc):
+    """dt = 0 with softplus off: no decay and no input, so hT equals h0 bit for
+    bit and y is C h0 at every step."""
+    H = 3
+    A = -np.array([1.0, 4.0, 16.0], np.float32)
+    hh, hT = _run_edge(orc, np.zeros((1, 200, H), np.float32), A, seed=101, softplus=False, cancelling=False)
+    assert torch.equal(hT.cpu(), torch.from_numpy(hh)), "dt = 0 must leave the state exactly as it was"
+
+
+def test_softplus_tails(orc):
+    """Step pre-activations far in either tail: softplus gives steps of e^-80
+    (the state is kept) and of 80 (the state resets to the current input).
+    Steps of 80 make terms of thousands in the masked product that cancel to a
+    much smaller y, so the bound is the magnitude one (a numpy emulation of
+    the chunked form with fp16 operands gives the same 9.5e-2 plain error the
+    kernel does, and 4e-12 in fp64)."""
+    g = np.random.default_rng(102)
+    dt = g.choice(np.array([-80.0, -20.0, -5.0, 0.0, 5.0, 20.0, 80.0], np.float32), size=(1, 200, 3))
+    _run_edge(orc, dt.astype(np.float32), -np.array([1.0, 4.0, 16.0], np.float32), seed=102, softplus=True,
+              cancelling=True)
+
+
+def test_zero_decay_heads_and_mixed_steps(orc):
+    """A = 0 on some heads (running sums over 512 steps) and steps mixed from
+    0 to 20 with softplus off."""
+    g = np.random.default_rng(103)
+    dt = g.choice(np.array([0.0, 1e-3, 0.05, 1.0, 20.0], np.float32), size=(1, 512, 3))
+    _run_edge(orc, dt.astype(np.float32), np.array([0.0, -2.0, 0.0], np.float32), seed=103, softplus=False,
+              cancelling=True, L=512)
