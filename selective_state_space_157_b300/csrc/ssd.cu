@@ -20,7 +20,8 @@
 //   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
 //      written as fp16 in the output kernel's operand layout, and hT;
 //      The same launch has one more CTA per batch row and chunk that forms
-//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32.
+//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32,
+//      and stores C converted to the output kernel's fp16 operand order.
 //   3. ssd_out_kernel: C H_in (K = N) into one TMEM tile, the masked and
 //      decayed G (from shared memory) times X (M = Q, N = P, K = Q) into a
 //      second; y = G X + diag(e^s) C H_in.
@@ -58,6 +59,7 @@ struct SsdArgs {
     __half *S;           // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n], fp16
     __half *Hin;         // (Bsz, H, nch, P x N): the state entering each chunk, fp16 operand order
     float *G;            // (Bsz, nch, Q, Q): C B^T of each chunk, [t][r]
+    __half *Cop;         // (Bsz, nch, Q x N): C of each chunk as the output kernel's fp16 A operand
     float *dec;          // (Bsz, H, nch): exp(s_last) of each chunk
     unsigned *fault;
     int64_t Bsz, L, H;
@@ -265,7 +267,8 @@ __host__ __device__ constexpr int ssd_state_cols()
 
 // 1. Each chunk's contribution to the state, S = (B o w)^T X (N x P),
 // stored transposed, [p][n], fp16, for the carry scan. CTAs with blockIdx.y == H
-// instead form C B^T of their chunk (fp32, [t][r]) for the output kernel.
+// instead form C B^T of their chunk (fp32, [t][r]) for the output kernel, and
+// store C in its operand order for it.
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 {
@@ -330,6 +333,14 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
                                      __uint_as_float(graw[q / 4][(q % 4) * 4 + 1]),
                                      __uint_as_float(graw[q / 4][(q % 4) * 4 + 2]),
                                      __uint_as_float(graw[q / 4][(q % 4) * 4 + 3]));
+        }
+        // C as the output kernel's A operand, already in core-matrix order.
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(A1);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.Cop + (b * a.nch + c) * Q * N);
+#pragma unroll 4
+            for (int e = tid; e < Q * N / 8; e += kSsdThreads)
+                dst[e] = src[e];
         }
         if (tid == 0 && !ok)
             record_fault(a.fault, kFaultMmaTimeout);
@@ -465,13 +476,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     constexpr int Q = kSsdQ;
     constexpr int COLS = ssd_out_cols<P>();
     extern __shared__ __align__(1024) unsigned char sm[];
+    constexpr int UNION = Q * P * (int)sizeof(T) > Q * Q * 2 ? Q * P * (int)sizeof(T) : Q * Q * 2;
     __half *A1 = reinterpret_cast<__half *>(sm);                       // C: Q rows, K = N
     __half *B4 = A1 + Q * N;                                            // H_in^T: P rows, K = N
     __half *BX = B4 + P * N;                                            // X^T: P rows, K = Q
-    __half *A2 = BX + P * Q;                                            // masked G: Q rows, K = Q
-    float *rG = reinterpret_cast<float *>(A2 + Q * Q);                  // C B^T [Q][Q]
-    T *rX = reinterpret_cast<T *>(rG + Q * Q);                          // X tile [Q][P]
-    float *dl = reinterpret_cast<float *>(rX + Q * P);
+    float *rG = reinterpret_cast<float *>(BX + P * Q);                  // C B^T [Q][Q]
+    unsigned char *un = reinterpret_cast<unsigned char *>(rG + Q * Q);
+    T *rX = reinterpret_cast<T *>(un);                                  // X tile [Q][P] ...
+    __half *A2 = reinterpret_cast<__half *>(un);                        // ... then the masked G: Q rows, K = Q
+    float *dl = reinterpret_cast<float *>(un + UNION);
     float *s = dl + Q;
     float *es = s + Q;
     __shared__ uint32_t tbase;
@@ -486,13 +499,14 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
         tmem_alloc(&tbase, COLS);
     copy_tile<float, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, rG);
     copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
-    if (carry)   // already in operand order: a plain copy
+    // C and the incoming state are already in operand order: plain copies.
+    copy_tile<__half, Q, N>(a.Cop + (b * a.nch + c) * Q * N, N, Q, A1);
+    if (carry)
         copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
     ssd_cp_commit();
     SsdDt dtv{};
     if (warp == 0)   // in flight with the tiles
         dtv = ssd_dt_load(a, b, h, t0, rows);
-    global_rows_to_operand<T, Q, N>(static_cast<const T *>(a.C) + (b * a.L + t0) * N, N, rows, A1);
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
@@ -598,11 +612,15 @@ constexpr size_t ssd_state_smem()
     return (size_t)(N + P) * kSsdQ * 2 + (size_t)kSsdQ * (N + P) * sizeof(T) + 3 * kSsdQ * 4;
 }
 
+// The X tile and the masked product share their space: X is transposed into
+// its operand before the masking writes.
 template <typename T, int N, int P>
 constexpr size_t ssd_out_smem()
 {
-    return ((size_t)kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ + (size_t)kSsdQ * kSsdQ) * 2 +
-           (size_t)kSsdQ * kSsdQ * 4 + (size_t)kSsdQ * P * sizeof(T) + 3 * kSsdQ * 4;
+    return ((size_t)kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ) * 2 + (size_t)kSsdQ * kSsdQ * 4 +
+           ((size_t)kSsdQ * P * sizeof(T) > (size_t)kSsdQ * kSsdQ * 2 ? (size_t)kSsdQ * P * sizeof(T)
+                                                                       : (size_t)kSsdQ * kSsdQ * 2) +
+           3 * kSsdQ * 4;
 }
 
 // Shared memory that keeps at most max_ctas CTAs of a kernel on one SM, so
@@ -626,6 +644,10 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
     const size_t s3 = ssd_pad(ssd_out_smem<T, N, P>(), 512 / ssd_out_cols<P>());
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3);
+    // All of the SM's unified L1/shared storage as shared memory: these
+    // kernels read their tiles through cp.async and __ldg only.
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k1, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
     k1<<<dim3(grid.x, grid.y + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
@@ -709,15 +731,16 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
     // Workspace: S and the incoming states (fp16), C B^T of every chunk
-    // (fp32), the chunk decays.
+    // (fp32), C of every chunk as an fp16 operand, the chunk decays.
     const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 2, hbytes = sbytes,
-                 gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 4, dbytes = (size_t)(Bsz * H * nch) * 4;
+                 gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 4, cbytes = (size_t)(Bsz * nch) * kSsdQ * N * 2,
+                 dbytes = (size_t)(Bsz * H * nch) * 4;
+    const size_t total = sbytes + hbytes + gbytes + cbytes + dbytes;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, sbytes + hbytes + gbytes + dbytes, pool, st);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, pool, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", sbytes + hbytes + gbytes + dbytes,
-                    cudaGetErrorString(e));
+        return fail(SELSCAN_ERR_NO_MEMORY, "SSD workspace of %zu bytes: %s", total, cudaGetErrorString(e));
     }
     SsdArgs a;
     memset(&a, 0, sizeof a);
@@ -725,7 +748,8 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     a.S = static_cast<__half *>(ws);
     a.Hin = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes);
     a.G = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
-    a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes);
+    a.Cop = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes);
+    a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes + cbytes);
     a.Bsz = Bsz; a.L = L; a.H = H;
     a.nch = (int)nch;
     a.softplus = dt_softplus ? 1 : 0;
