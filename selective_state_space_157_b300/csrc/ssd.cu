@@ -67,6 +67,14 @@ struct SsdArgs {
     int softplus;
 };
 
+// Programmatic dependent launch: a kernel launched with it may start while
+// the kernel before it on the stream is still running; it calls
+// grid_dep_wait() before it reads anything that kernel wrote (the wait
+// returns once that whole grid has completed and its writes are visible).
+// grid_dep_trigger() lets the next such kernel start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 16-byte asynchronous copy global -> shared; zeros instead when !ok.
 __device__ __forceinline__ void ssd_cp16(void *dst, const void *src, bool ok)
 {
@@ -318,6 +326,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
         }
         const bool ok = mma_wait(&mbar, 0);
         tc_fence_after();
+        grid_dep_trigger();
         // Row t of C B^T sits in lane 32w + (t - 16w) of warp w (M = 64).
         uint32_t graw[Q / 16][16];
 #pragma unroll
@@ -382,6 +391,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     }
     const bool ok = mma_wait(&mbar, 0);
     tc_fence_after();
+    grid_dep_trigger();
     // Row n of S sits in TMEM lane n (N = 128) or lane 32w + (n - 16w) (N = 64);
     // a warp's lanes hold consecutive n, so the [p][n] stores coalesce.
     const int n = N == 128 ? 32 * warp + lane : 16 * warp + lane;
@@ -419,6 +429,8 @@ template <int N, int P>
 __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
 {
     constexpr int NP = N * P;
+    grid_dep_wait();      // the chunk states and decays of the state kernel
+    grid_dep_trigger();   // the output kernel may start its own loads
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (i >= a.Bsz * a.H * (NP / 8))
         return;
@@ -497,16 +509,19 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     const bool carry = c > 0 || a.h0 != nullptr;
     if (warp == 0)   // first, as in the state kernel
         tmem_alloc(&tbase, COLS);
-    copy_tile<float, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, rG);
+    // The call's own inputs first; then, once the kernels before have
+    // completed, what they wrote: C B^T, C in operand order and the incoming
+    // state (plain copies, already in operand order).
     copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
-    // C and the incoming state are already in operand order: plain copies.
+    SsdDt dtv{};
+    if (warp == 0)
+        dtv = ssd_dt_load(a, b, h, t0, rows);
+    grid_dep_wait();
+    copy_tile<float, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, rG);
     copy_tile<__half, Q, N>(a.Cop + (b * a.nch + c) * Q * N, N, Q, A1);
     if (carry)
         copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
     ssd_cp_commit();
-    SsdDt dtv{};
-    if (warp == 0)   // in flight with the tiles
-        dtv = ssd_dt_load(a, b, h, t0, rows);
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
@@ -652,9 +667,25 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
     k1<<<dim3(grid.x, grid.y + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
     const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
-    ssd_carry_kernel<N, P><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
-    k3<<<grid, kSsdThreads, s3, st>>>(a);
+    // The carry and output kernels start early (programmatic dependent
+    // launch) and wait in the kernel for what the one before wrote.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3((unsigned)((total + 255) / 256));
+    cfg2.blockDim = dim3(256);
+    cfg2.stream = st;
+    cfg2.attrs = pdl;
+    cfg2.numAttrs = 1;
     e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg2, ssd_carry_kernel<N, P>, a);
+    cudaLaunchConfig_t cfg3 = cfg2;
+    cfg3.gridDim = grid;
+    cfg3.blockDim = dim3(kSsdThreads);
+    cfg3.dynamicSmemBytes = s3;
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg3, k3, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "SSD kernel launch");
 }
 
