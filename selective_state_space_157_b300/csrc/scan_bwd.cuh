@@ -29,8 +29,8 @@
 //   1. bwd_local_kernel: per segment, the forward recurrence from a zero
 //      state, writing the local state and the running sum of dl at every
 //      chunk start (the checkpoints), the end state and the segment's sum of
-//      dl; then the adjoint recurrence from zero at the segment's end back
-//      to its start (what the segment alone sends into the state before it).
+//      dl; in the same pass, what the segment alone sends into the state
+//      before it (the adjoint from zero at its end, summed in closed form).
 //   2. bwd_carry_kernel: per (b, d, n), the true state entering each segment
 //      (h_in(k+1) = exp(A S_k) h_in(k) + hl(k), from h0) and the adjoint
 //      entering each segment from the right (g_out(k-1) = exp(A S_k) g_out(k)
@@ -92,7 +92,7 @@ __host__ __device__ constexpr int bwd_main_smem(int P)
 // spills.
 __host__ __device__ constexpr int bwd_local_tt(int P)
 {
-    return P >= 8 ? 64 : (P >= 2 ? 32 : 16);
+    return P >= 4 ? 32 : 16;
 }
 __host__ __device__ constexpr int bwd_local_smem(int P)
 {
@@ -237,9 +237,14 @@ template <int P> __device__ __forceinline__ bool bwd_rs_writer(int lane)
 
 // ---------------------------------------------------------------- kernel 1
 // grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_local_smem(P) bytes.
-// Stages of TL = bwd_local_tt(P) steps (whole chunks; zeros past the
-// segment's end, which belong to the next segment), loaded into registers one
-// stage ahead.
+// One pass over the segment from its start, in stages of TL =
+// bwd_local_tt(P) steps (whole chunks; zeros past the segment's end, which
+// belong to the next segment), loaded into registers one stage ahead. It
+// runs the forward recurrence from a zero state (checkpoints, end state, sum
+// of dl) and, in the same pass, forms what the segment alone sends into the
+// state before it: the adjoint from zero at the segment's end, which
+// unrolls to gl = sum_t exp(A S_t) gy_t C_t with S_t the sum of dl from the
+// segment's start through step t.
 template <int P>
 __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs a)
 {
@@ -267,18 +272,17 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
     const int nst = (int)((s1 - s0 + TL - 1) / TL);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
 
-    // Forward from a zero state: checkpoints, end state, sum of dl (chunk
-    // sums added with compensation).
     float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float S = 0.0f, Sc = 0.0f;
+    float2 gl[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float S = 0.0f, Sc = 0.0f;   // compensated sum of dl through the last chunk
     BwdRegs<P, TL> r;
-    bwd_load<P, TL, true, false, true, false>(a, b, d0, s0, s1, r);
+    bwd_load<P, TL, true, true, true, true>(a, b, d0, s0, s1, r);
     for (int st = 0; st < nst; ++st) {
         const int64_t t0 = s0 + (int64_t)st * TL;
         __syncthreads();
-        bwd_put<P, TL, true, false, true, false>(a, r, d0, t0, s1, s_in, s_B, s_C);
+        bwd_put<P, TL, true, true, true, true>(a, r, d0, t0, s1, s_in, s_B, s_C);
         if (st + 1 < nst)
-            bwd_load<P, TL, true, false, true, false>(a, b, d0, t0 + TL, s1, r);
+            bwd_load<P, TL, true, true, true, true>(a, b, d0, t0 + TL, s1, r);
         __syncthreads();
 #pragma unroll 1
         for (int q = 0; q < CH; ++q) {
@@ -295,11 +299,15 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
             for (int i = q * kBwdT; i < (q + 1) * kBwdT; ++i) {
                 const float4 in = s_in[i * CPB + c];
                 const float4 B4 = *reinterpret_cast<const float4 *>(s_B + i * NP + kBwdS * j);
+                const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
                 const float dl = in.x, u = dl * in.y;
-                const float2 dl2 = f2(dl), u2 = f2(u);
+                const float2 dl2 = f2(dl), u2 = f2(u), gy2 = f2(in.z);
                 h[0] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
                 h[1] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
                 sc += dl;
+                const float2 St = f2(S + sc);   // sum of dl from the segment's start through this step
+                gl[0] = __ffma2_rn(ex2v(__fmul2_rn(St, A2[0])), __fmul2_rn(gy2, make_float2(C4.x, C4.y)), gl[0]);
+                gl[1] = __ffma2_rn(ex2v(__fmul2_rn(St, A2[1])), __fmul2_rn(gy2, make_float2(C4.z, C4.w)), gl[1]);
             }
             const float yk = sc - Sc, tk = S + yk;   // S += sc, compensated
             Sc = (tk - S) - yk;
@@ -310,31 +318,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
         *reinterpret_cast<float4 *>(a.hl + pair) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
         if (j == 0)
             a.sdl[(b * a.K + k) * D + d] = S;
+        if (k > 0)   // nothing lies before the first segment
+            *reinterpret_cast<float4 *>(a.gl + pair) = make_float4(gl[0].x, gl[0].y, gl[1].x, gl[1].y);
     }
-    if (k == 0)
-        return;   // nothing lies before the first segment
-
-    // Adjoint from zero at the segment's end back to its start.
-    float2 g[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    bwd_load<P, TL, false, true, false, true>(a, b, d0, s0 + (int64_t)(nst - 1) * TL, s1, r);
-    for (int st = nst - 1; st >= 0; --st) {
-        const int64_t t0 = s0 + (int64_t)st * TL;
-        __syncthreads();
-        bwd_put<P, TL, false, true, false, true>(a, r, d0, t0, s1, s_in, s_B, s_C);
-        if (st > 0)
-            bwd_load<P, TL, false, true, false, true>(a, b, d0, t0 - TL, s1, r);
-        __syncthreads();
-#pragma unroll 4
-        for (int i = TL - 1; i >= 0; --i) {
-            const float4 in = s_in[i * CPB + c];
-            const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
-            const float2 dl2 = f2(in.x), gy2 = f2(in.z);
-            g[0] = __fmul2_rn(ex2v(__fmul2_rn(dl2, A2[0])), __ffma2_rn(gy2, make_float2(C4.x, C4.y), g[0]));
-            g[1] = __fmul2_rn(ex2v(__fmul2_rn(dl2, A2[1])), __ffma2_rn(gy2, make_float2(C4.z, C4.w), g[1]));
-        }
-    }
-    if (chain)
-        *reinterpret_cast<float4 *>(a.gl + pair) = make_float4(g[0].x, g[0].y, g[1].x, g[1].y);
 }
 
 // ---------------------------------------------------------------- kernel 2
