@@ -167,6 +167,14 @@ __device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P, TT> &
 
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
+// Programmatic dependent launch: the carry and main kernels may start while
+// the kernel before them is finishing; they call bwd_dep_wait() before they
+// read anything it wrote (the wait returns once that whole grid has
+// completed and its writes are visible). bwd_dep_trigger() lets the next
+// kernel start early.
+__device__ __forceinline__ void bwd_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void bwd_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Asynchronous copies global -> shared (cp.async): 4 or 16 bytes, zeros
 // instead when !ok (no byte is read then).
 __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool ok)
@@ -272,6 +280,19 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
     const int nst = (int)((s1 - s0 + TL - 1) / TL);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
 
+    // The main kernel adds dA, dB and dC up atomically: zero them here, over
+    // the whole grid.
+    {
+        const int64_t nthr = (int64_t)gridDim.x * gridDim.y * gridDim.z * kBwdThreads;
+        const int64_t gt = (((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kBwdThreads + tid;
+        for (int64_t i = gt; i < a.Bsz * L * N; i += nthr) {
+            a.dB[i] = 0.0f;
+            a.dC[i] = 0.0f;
+        }
+        for (int64_t i = gt; i < D * N; i += nthr)
+            a.dA[i] = 0.0f;
+    }
+
     float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 gl[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float S = 0.0f, Sc = 0.0f;   // compensated sum of dl through the last chunk
@@ -314,6 +335,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
             S = tk;
         }
     }
+    bwd_dep_trigger();
     if (chain) {
         *reinterpret_cast<float4 *>(a.hl + pair) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
         if (j == 0)
@@ -330,6 +352,8 @@ constexpr int kCarryBatch = 8;
 
 __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
 {
+    bwd_dep_wait();      // the local kernel's pairs
+    bwd_dep_trigger();
     const int64_t total = a.Bsz * a.D * NP;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
         const int n = (int)(e % NP);
@@ -376,7 +400,7 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
 
 // ---------------------------------------------------------------- kernel 3
 // grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_main_smem(P) bytes.
-// dA, dB and dC must be zero on entry (they are accumulated atomically).
+// dA, dB and dC are accumulated atomically (the local kernel zeroed them).
 // Chunk inputs arrive by cp.async into one of two raw buffers while the
 // block works on the other, so no register holds a chunk in flight.
 template <int P>
@@ -411,6 +435,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
     }
     const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
+    bwd_dep_wait();   // the carries (and, through the carry kernel's own wait, the checkpoints)
     float2 hin[2], g[2], dA[2];
     {
         const float4 hv = chain ? *reinterpret_cast<const float4 *>(a.hin + pair) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -617,9 +642,25 @@ inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_
     bwd_local_kernel<P><<<grid, kBwdThreads, bwd_local_smem(P), st>>>(a);
     const int64_t carry = a.Bsz * a.D * s.NP;
     const unsigned cb = (unsigned)((carry + 255) / 256 < 65536 ? (carry + 255) / 256 : 65536);
-    bwd_carry_kernel<<<cb, 256, 0, st>>>(a, s.NP);
-    bwd_main_kernel<P><<<grid, kBwdThreads, bwd_main_smem(P), st>>>(a);
-    return cudaGetLastError();
+    // The carry and main kernels are programmatic dependents of the kernel
+    // before them (they wait in the kernel); the local kernel launches
+    // normally, after whatever the stream held.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cb);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_carry_kernel, a, s.NP);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = bwd_main_smem(P);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<P>, a);
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 inline cudaError_t launch_scan_bwd(BwdArgs a, const BwdShape &s, cudaStream_t st)

@@ -53,8 +53,11 @@ extern "C" int selscan_bwd(const float *x, const float *delta, const float *A, c
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)(D * N) * 4, st);
-    if (e != cudaSuccess) return cuda_fail(e, "dA zero fill");
+    cudaError_t e = cudaSuccess;
+    if (Bsz == 0 || L == 0) {   // no kernel runs: dA is zero
+        e = cudaMemsetAsync(dA, 0, (size_t)(D * N) * 4, st);
+        if (e != cudaSuccess) return cuda_fail(e, "dA zero fill");
+    }
     if (Bsz == 0) return SELSCAN_OK;
     if (L == 0) {
         if (!dh0) return SELSCAN_OK;
@@ -62,9 +65,7 @@ extern "C" int selscan_bwd(const float *x, const float *delta, const float *A, c
                 : cudaMemsetAsync(dh0, 0, (size_t)ndn * 4, st);
         return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "L == 0 state gradient");
     }
-    if ((e = cudaMemsetAsync(dB, 0, (size_t)nln * 4, st)) != cudaSuccess ||
-        (e = cudaMemsetAsync(dC, 0, (size_t)nln * 4, st)) != cudaSuccess)
-        return cuda_fail(e, "dB, dC zero fill");
+    // With L > 0 the local kernel zeroes dA, dB and dC itself.
 
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
