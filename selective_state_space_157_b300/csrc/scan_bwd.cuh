@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
 
     float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 gl[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    // exp(A S_t), S_t the sum of dl from the segment's start through step t:
+    // the running product of the steps' decays.
+    float2 ep[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
     float S = 0.0f, Sc = 0.0f;   // compensated sum of dl through the last chunk
     BwdRegs<P, TL> r;
     bwd_load<P, TL, true, true, true, true>(a, b, d0, s0, s1, r);
@@ -323,12 +326,14 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
                 const float4 C4 = *reinterpret_cast<const float4 *>(s_C + i * NP + kBwdS * j);
                 const float dl = in.x, u = dl * in.y;
                 const float2 dl2 = f2(dl), u2 = f2(u), gy2 = f2(in.z);
-                h[0] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[0])), h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
-                h[1] = __ffma2_rn(ex2v(__fmul2_rn(dl2, A2[1])), h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
+                const float2 a0 = ex2v(__fmul2_rn(dl2, A2[0])), a1 = ex2v(__fmul2_rn(dl2, A2[1]));
+                h[0] = __ffma2_rn(a0, h[0], __fmul2_rn(u2, make_float2(B4.x, B4.y)));
+                h[1] = __ffma2_rn(a1, h[1], __fmul2_rn(u2, make_float2(B4.z, B4.w)));
                 sc += dl;
-                const float2 St = f2(S + sc);   // sum of dl from the segment's start through this step
-                gl[0] = __ffma2_rn(ex2v(__fmul2_rn(St, A2[0])), __fmul2_rn(gy2, make_float2(C4.x, C4.y)), gl[0]);
-                gl[1] = __ffma2_rn(ex2v(__fmul2_rn(St, A2[1])), __fmul2_rn(gy2, make_float2(C4.z, C4.w)), gl[1]);
+                ep[0] = __fmul2_rn(ep[0], a0);
+                ep[1] = __fmul2_rn(ep[1], a1);
+                gl[0] = __ffma2_rn(ep[0], __fmul2_rn(gy2, make_float2(C4.x, C4.y)), gl[0]);
+                gl[1] = __ffma2_rn(ep[1], __fmul2_rn(gy2, make_float2(C4.z, C4.w)), gl[1]);
             }
             const float yk = sc - Sc, tk = S + yk;   // S += sc, compensated
             Sc = (tk - S) - yk;
