@@ -314,7 +314,7 @@ int selscan_fwd_host_ex(const void *x, const void *delta, const float *A, const 
  *               the next piece of the sequence or for selscan_conv1d_step
  *   silu      : 0 leaves the sum without the SiLU
  *
- * Sizes: Bsz, L, D >= 0 (Bsz <= 65535, L <= 65535 * 32); 1 <= K <= 8
+ * Sizes: Bsz, L, D >= 0 (Bsz <= 65535, L <= 65535 * 64); 1 <= K <= 8
  * (K = 1 carries no state). out must not overlap any input; state_out must
  * not overlap out or any input (state_in included: pass another buffer).
  * L == 0 copies state_in (or zeros) to state_out. Errors as for selscan_fwd.

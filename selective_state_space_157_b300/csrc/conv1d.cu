@@ -6,28 +6,39 @@
 namespace selscan {
 namespace {
 
-template <typename T, int RUN>
-void launch_conv1d_vec(const ConvArgs &a, int64_t K, cudaStream_t st)
+template <typename T>
+int launch_conv1d_ring(const ConvArgs &a, int64_t K, cudaStream_t st)
 {
-    const dim3 grid((unsigned)((a.D / 4 + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
-                    (unsigned)((a.L + RUN - 1) / RUN));
+    int dev = 0, sms = 0;
+    const int rc = device_info(&dev, &sms);
+    if (rc != SELSCAN_OK) return rc;
+    // Segments of equal length, enough for about kConvRingPerSm CTAs on
+    // every SM.
+    const int64_t cols = (a.D / 4 + kConvThreads - 1) / kConvThreads;
+    const int64_t want = (int64_t)sms * kConvRingPerSm;
+    const int64_t nseg0 = (want + cols * a.Bsz - 1) / (cols * a.Bsz);
+    int64_t seg = (a.L + nseg0 - 1) / nseg0;
+    if (seg < (a.L + 65534) / 65535) seg = (a.L + 65534) / 65535;
+    const dim3 grid((unsigned)cols, (unsigned)a.Bsz, (unsigned)((a.L + seg - 1) / seg));
     switch (K) {
-    case 1: conv1d_vec_kernel<T, 1, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 2: conv1d_vec_kernel<T, 2, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 3: conv1d_vec_kernel<T, 3, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 4: conv1d_vec_kernel<T, 4, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 5: conv1d_vec_kernel<T, 5, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 6: conv1d_vec_kernel<T, 6, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    case 7: conv1d_vec_kernel<T, 7, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
-    default: conv1d_vec_kernel<T, 8, RUN><<<grid, kConvThreads, 0, st>>>(a); break;
+    case 1: conv1d_ring_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 2: conv1d_ring_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 3: conv1d_ring_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 4: conv1d_ring_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 5: conv1d_ring_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 6: conv1d_ring_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 7: conv1d_ring_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    default: conv1d_ring_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a, seg); break;
     }
+    return SELSCAN_OK;
 }
 
 template <typename T>
 int launch_conv1d_t(const ConvArgs &a, int64_t K, bool vec, cudaStream_t st)
 {
     if (vec) {
-        launch_conv1d_vec<T, kConvVecRun>(a, K, st);
+        const int rc = launch_conv1d_ring<T>(a, K, st);
+        if (rc != SELSCAN_OK) return rc;
     } else {
         const dim3 grid((unsigned)((a.D + kConvThreads - 1) / kConvThreads), (unsigned)a.Bsz,
                         (unsigned)((a.L + kConvT - 1) / kConvT));

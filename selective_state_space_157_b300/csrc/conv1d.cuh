@@ -105,16 +105,8 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a)
     }
 }
 
-// Four consecutive channels per thread (16-byte fp32 or 8-byte bf16 loads
-// and stores) over a run of kConvVecRun timesteps; taken when D is a
-// multiple of 4 and x and out are aligned for it. Lanes cover 4 * 32
-// channels of a row. The run's inputs are loaded in batches of 16, each
-// batch (with the K - 1 halo inputs for the first) issued before any of its
-// outputs is computed, so a thread waits on memory twice per run. Measured
-// on B300 (Bsz=2 L=2048 D=1536 K=4 fp32): 11.4 us, against 11.7 us for runs
-// of 16 and 12.6 us for runs of 8 (more, shorter threads) or for batches of 8.
-constexpr int kConvVecRun = 32;
-
+// Loads and stores of four consecutive channels (16-byte fp32 or 8-byte
+// bf16), widened to fp32.
 template <typename T> struct Vec4;
 template <> struct Vec4<float> {
     using S = float4;
@@ -150,40 +142,78 @@ __device__ __forceinline__ float4 conv_state4(const ConvArgs &a, int64_t b, int6
                        conv_state_value<K>(a, b, d0 + 2, tau), conv_state_value<K>(a, b, d0 + 3, tau));
 }
 
-// Inputs loaded ahead per batch of a run, and the CTAs per SM the register
-// budget of that batch (x, the filter and the window, 4 floats each, plus
-// addressing) leaves room for.
-__host__ __device__ constexpr int conv_vec_batch(int run) { return run < 16 ? run : 16; }
-__host__ __device__ constexpr int conv_vec_min_blocks(int run, int K)
-{
-    return 65536 / (kConvThreads * (4 * (conv_vec_batch(run) + 2 * K) + 24)) < 1
-               ? 1
-               : 65536 / (kConvThreads * (4 * (conv_vec_batch(run) + 2 * K) + 24));
-}
+// Four consecutive channels per thread, taken when D is a multiple of 4 and x
+// and out are aligned for vector access. The inputs stream through a
+// per-thread ring of kConvRing slots in shared memory filled by cp.async:
+// the thread keeps kConvRing - 1 rows in flight while it computes and stores
+// the oldest, so it never waits a whole round trip between batches. Each
+// thread reads back only the slots it filled itself, so the block needs no
+// barrier. A CTA walks one segment of seg consecutive timesteps of one batch
+// row and 4 * 128 channels; the K - 1 inputs before the segment are plain
+// loads. Measured on B300 (Bsz=2 L=2048 D=1536 K=4 fp32, CUDA graph): 11.4 us
+// with segments for three CTAs per SM (11.8, 12.1 and 14.7 us for four, six
+// and eight), against 11.7 us for the earlier register-batched form (runs of
+// 32 timesteps in two batches of 16) and 9.8 us for a plain device copy of
+// the same bytes.
+constexpr int kConvRing = 16;
+constexpr int kConvRingPerSm = 3;   // CTAs per SM the segments are sized for
 
-template <typename T, int K, int RUN>
-__global__ void __launch_bounds__(kConvThreads, conv_vec_min_blocks(RUN, K)) conv1d_vec_kernel(const ConvArgs a)
+template <typename T> struct RingIo;
+template <> struct RingIo<float> {
+    using Slot = float4;
+    __device__ __forceinline__ static void copy(Slot *dst, const float *src)
+    {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                     "l"(src)
+                     : "memory");
+    }
+    __device__ __forceinline__ static float4 get(const Slot *s) { return *s; }
+};
+template <> struct RingIo<__nv_bfloat16> {
+    using Slot = uint2;
+    __device__ __forceinline__ static void copy(Slot *dst, const __nv_bfloat16 *src)
+    {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                     "l"(src)
+                     : "memory");
+    }
+    __device__ __forceinline__ static float4 get(const Slot *s)
+    {
+        const uint2 u = *s;
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+};
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads) conv1d_ring_kernel(const ConvArgs a, int64_t seg)
 {
-    constexpr int BATCH = conv_vec_batch(RUN);
-    const int64_t d0 = ((int64_t)blockIdx.x * kConvThreads + threadIdx.x) * 4;
+    using Slot = typename RingIo<T>::Slot;
+    __shared__ Slot ring[kConvRing][kConvThreads];
+    const int tid = threadIdx.x;
+    const int64_t d0 = ((int64_t)blockIdx.x * kConvThreads + tid) * 4;
     const int64_t b = blockIdx.y;
-    const int64_t t0 = (int64_t)blockIdx.z * RUN;
+    const int64_t t0 = (int64_t)blockIdx.z * seg;
     if (d0 >= a.D)
         return;
     const int64_t D = a.D, L = a.L;
-    const int64_t n = L - t0 < RUN ? L - t0 : RUN;
-    const T *xp = static_cast<const T *>(a.x) + b * L * D + d0;
-    T *op = static_cast<T *>(a.out) + b * L * D + d0;
+    const int64_t n = L - t0 < seg ? L - t0 : seg;
+    const T *xp = static_cast<const T *>(a.x) + (b * L + t0) * D + d0;
+    T *op = static_cast<T *>(a.out) + (b * L + t0) * D + d0;
 
-    float4 xb[BATCH];
+    // Rows 0 .. kConvRing - 2 of the segment in flight (one commit group per
+    // row, empty past the segment's end).
 #pragma unroll
-    for (int i = 0; i < BATCH; ++i)
-        xb[i] = i < n ? Vec4<T>::load(xp + (t0 + i) * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < kConvRing - 1; ++i) {
+        if (i < n)
+            RingIo<T>::copy(&ring[i][tid], xp + i * D);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     float4 win[K > 1 ? K - 1 : 1];
 #pragma unroll
     for (int j = 0; j < K - 1; ++j) {
         const int64_t tau = t0 - (K - 1) + j;
-        win[j] = tau >= 0 ? Vec4<T>::load(xp + tau * D) : conv_state4<K>(a, b, d0, tau);
+        win[j] = tau >= 0 ? Vec4<T>::load(xp + (j - (K - 1)) * D) : conv_state4<K>(a, b, d0, tau);
     }
     float4 w[K];
 #pragma unroll
@@ -193,44 +223,43 @@ __global__ void __launch_bounds__(kConvThreads, conv_vec_min_blocks(RUN, K)) con
     const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
 
 #pragma unroll 1
-    for (int tb = 0; tb < RUN; tb += BATCH) {
-        if (tb > 0) {
+    for (int64_t i = 0; i < n; ++i) {
+        // Row i has landed once at most kConvRing - 2 younger groups are pending.
+        asm volatile("cp.async.wait_group %0;" ::"n"(kConvRing - 2) : "memory");
+        const float4 xv = RingIo<T>::get(&ring[i % kConvRing][tid]);
+        // The slot row i - 1 used (consumed last iteration) takes row
+        // i + kConvRing - 1.
+        const int64_t nx = i + kConvRing - 1;
+        if (nx < n)
+            RingIo<T>::copy(&ring[nx % kConvRing][tid], xp + nx * D);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        float4 acc = bias;
 #pragma unroll
-            for (int i = 0; i < BATCH; ++i)
-                xb[i] = tb + i < n ? Vec4<T>::load(xp + (t0 + tb + i) * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K - 1; ++k) {
+            acc.x = fmaf(w[k].x, win[k].x, acc.x);
+            acc.y = fmaf(w[k].y, win[k].y, acc.y);
+            acc.z = fmaf(w[k].z, win[k].z, acc.z);
+            acc.w = fmaf(w[k].w, win[k].w, acc.w);
         }
+        acc.x = fmaf(w[K - 1].x, xv.x, acc.x);
+        acc.y = fmaf(w[K - 1].y, xv.y, acc.y);
+        acc.z = fmaf(w[K - 1].z, xv.z, acc.z);
+        acc.w = fmaf(w[K - 1].w, xv.w, acc.w);
 #pragma unroll
-        for (int i = 0; i < BATCH; ++i) {
-            const float4 xv = xb[i];
-            float4 acc = bias;
-#pragma unroll
-            for (int k = 0; k < K - 1; ++k) {
-                acc.x = fmaf(w[k].x, win[k].x, acc.x);
-                acc.y = fmaf(w[k].y, win[k].y, acc.y);
-                acc.z = fmaf(w[k].z, win[k].z, acc.z);
-                acc.w = fmaf(w[k].w, win[k].w, acc.w);
-            }
-            acc.x = fmaf(w[K - 1].x, xv.x, acc.x);
-            acc.y = fmaf(w[K - 1].y, xv.y, acc.y);
-            acc.z = fmaf(w[K - 1].z, xv.z, acc.z);
-            acc.w = fmaf(w[K - 1].w, xv.w, acc.w);
-#pragma unroll
-            for (int k = 0; k + 1 < K - 1; ++k)
-                win[k] = win[k + 1];
-            if (K > 1)
-                win[K > 1 ? K - 2 : 0] = xv;
-            if (tb + i < n)
-                Vec4<T>::store(op + (t0 + tb + i) * D,
-                               make_float4(conv_out(acc.x, a.silu), conv_out(acc.y, a.silu), conv_out(acc.z, a.silu),
-                                           conv_out(acc.w, a.silu)));
-        }
+        for (int k = 0; k + 1 < K - 1; ++k)
+            win[k] = win[k + 1];
+        if (K > 1)
+            win[K > 1 ? K - 2 : 0] = xv;
+        Vec4<T>::store(op + i * D, make_float4(conv_out(acc.x, a.silu), conv_out(acc.y, a.silu),
+                                               conv_out(acc.z, a.silu), conv_out(acc.w, a.silu)));
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 
     if (a.state_out && t0 + n == L) {
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
             const int64_t tau = L - (K - 1) + j;
-            const float4 v = tau >= 0 ? Vec4<T>::load(xp + tau * D) : conv_state4<K>(a, b, d0, tau);
+            const float4 v = tau >= 0 ? Vec4<T>::load(xp + (tau - t0) * D) : conv_state4<K>(a, b, d0, tau);
             a.state_out[(b * D + d0) * (K - 1) + j] = v.x;
             a.state_out[(b * D + d0 + 1) * (K - 1) + j] = v.y;
             a.state_out[(b * D + d0 + 2) * (K - 1) + j] = v.z;

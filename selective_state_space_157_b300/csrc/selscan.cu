@@ -936,8 +936,8 @@ extern "C" int selscan_conv1d(const void *x, const float *w, const float *bias, 
         return fail(SELSCAN_ERR_INVALID_ARG, "sizes overflow");
     if (Bsz == 0 || D == 0)
         return SELSCAN_OK;
-    if (Bsz > 65535 || (L + kConvVecRun - 1) / kConvVecRun > 65535 || (D + kConvThreads - 1) / kConvThreads > 0x7fffffffLL)
-        return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large (Bsz <= 65535, L <= %lld)", 65535LL * kConvVecRun);
+    if (Bsz > 65535 || (L + kConvT - 1) / kConvT > 65535 || (D + kConvThreads - 1) / kConvThreads > 0x7fffffffLL)
+        return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large (Bsz <= 65535, L <= %lld)", 65535LL * kConvT);
     const size_t es = dtype == SELSCAN_F32 ? 4 : 2;
     if (!w || (L > 0 && (!x || !out)))
         return fail(SELSCAN_ERR_INVALID_ARG, "w, and x and out when L > 0, must be non-NULL");

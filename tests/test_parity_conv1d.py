@@ -35,15 +35,29 @@ def test_conv1d_matches_oracle(orc, K, dtype, with_state):
 @pytest.mark.parametrize("D", [70, 72])
 @pytest.mark.parametrize("vec", ["1", "0"])
 def test_conv1d_run_boundaries(orc, monkeypatch, L, D, vec):
-    """Runs of 32 timesteps loaded in batches of 16 (four channels per
-    thread, D % 4 == 0) and runs of 64 (one channel per thread), ragged tails,
-    and both kernels on the same D."""
+    """Short segments of the streaming kernel (four channels per thread,
+    D % 4 == 0) and runs of 64 (one channel per thread), ragged tails, and
+    both kernels on the same D."""
     monkeypatch.setenv("SELSCAN_CONV_VEC", vec)
     x, w, bias, state = W.conv_inputs(2, L, D, 4, seed=L + D, with_state=True)
     out, st = ss.conv1d(to_dev(x), to_dev(w), to_dev(bias), state_in=to_dev(state), return_state=True)
     torch.cuda.synchronize()
     ref, st_ref = orc.conv1d(x, w, bias, state_in=state)
     assert scaled_err(to_np(out), ref) <= TOL[W.F32]
+    assert np.array_equal(to_np(st).astype(np.float32), st_ref)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("K,Bsz,L,D", [(4, 2, 3000, 1032), (8, 1, 17761, 72), (2, 3, 997, 516)])
+def test_conv1d_segments_longer_than_the_ring(orc, dtype, K, Bsz, L, D):
+    """Sizes at which the streaming kernel's segments (sized for three CTAs
+    per SM) run past its 16-slot ring, so slots are refilled in flight, with
+    a ragged last segment and a ragged last group of channels."""
+    x, w, bias, state = W.conv_inputs(Bsz, L, D, K, seed=L + K, dtype=dtype, with_state=True)
+    out, st = ss.conv1d(to_dev(x, dtype), to_dev(w), to_dev(bias), state_in=to_dev(state), return_state=True)
+    torch.cuda.synchronize()
+    ref, st_ref = orc.conv1d(f32(x, dtype), w, bias, state_in=state)
+    assert scaled_err(to_np(out), ref) <= TOL[dtype]
     assert np.array_equal(to_np(st).astype(np.float32), st_ref)
 
 
