@@ -16,15 +16,16 @@
 //   S = (B o w)^T X,   w_r = exp(s_last - s_r) dl_r,
 // with H_out = exp(s_last) H_in + S. Three kernels:
 //   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q),
-//      stored fp16 (the precision it has as an operand anyway);
+//      stored fp16 (the precision it has as an operand anyway). The same
+//      launch has one more CTA per batch row and chunk that forms
+//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32,
+//      and stores C converted to the output kernel's fp16 operand order;
 //   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
 //      written as fp16 in the output kernel's operand layout, and hT;
-//      The same launch has one more CTA per batch row and chunk that forms
-//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32,
-//      and stores C converted to the output kernel's fp16 operand order.
 //   3. ssd_out_kernel: C H_in (K = N) into one TMEM tile, the masked and
 //      decayed G (from shared memory) times X (M = Q, N = P, K = Q) into a
 //      second; y = G X + diag(e^s) C H_in.
+// Kernels 2 and 3 are launched as programmatic dependents of the one before.
 // Each CTA brings every tile it needs into shared memory in one round trip
 // (cp.async, zeros past the sequence), then converts and transposes there.
 // Operands are fp16 in shared memory (bf16 and fp32 inputs are converted
