@@ -565,27 +565,58 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def evict_host_caches(nbytes=512 << 20):
+    """Writes and reads a host buffer larger than the CPU's caches, so that
+    host inputs written shortly before sit in DRAM, as inputs a loader wrote
+    earlier would. On the B300 machines a DMA read of pinned memory whose lines
+    were still dirty in the CPU cache ran at 15-17 GB/s instead of 55."""
+    import numpy as np
+    scratch = np.ones(nbytes // 8)
+    float(scratch.sum())
+    del scratch
+
+
 def pcie_rates(dev, nbytes=256 << 20, reps=4):
-    """One-way copy rates between pinned host memory and this GPU (GB/s),
-    timed with CUDA events on a side stream: the bound the end-to-end leg's
-    copies can approach."""
+    """Copy rates between pinned host memory and this GPU (GB/s), timed with
+    CUDA events: host to device, device to host, and both directions at once
+    on two streams (their sum; the link does not carry both directions at
+    their one-way rates together). The bound the end-to-end leg's copies can
+    approach."""
     import torch
     h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    st = torch.cuda.Stream(dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st, st2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     rates = []
-    for dst, src in ((d, h), (h, d)):
-        with torch.cuda.stream(st):
-            dst.copy_(src, non_blocking=True)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            for _ in range(reps):
+    for pairs in (((d, h),), ((h, d),), ((d, h), (h2, d2))):
+        streams = (st, st2)[:len(pairs)]
+        for (dst, src), s_ in zip(pairs, streams):
+            with torch.cuda.stream(s_):
                 dst.copy_(src, non_blocking=True)
-            e1.record(st)
-        st.synchronize()
-        rates.append(reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
-    del h, d
-    return rates[0], rates[1]
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        if len(pairs) > 1:
+            st2.wait_event(e0)
+        for (dst, src), s_ in zip(pairs, streams):
+            with torch.cuda.stream(s_):
+                for _ in range(reps):
+                    dst.copy_(src, non_blocking=True)
+        if len(pairs) > 1:
+            st.wait_stream(st2)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        rates.append(len(pairs) * reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, h2, d, d2
+    return rates[0], rates[1], rates[2]
+
+
+def copy_bound_s(h2d, d2h, rates):
+    """The least time the copies of one step can take: each direction at its
+    own rate, and both together at the two-way rate."""
+    h2d_gbs, d2h_gbs, both_gbs = rates
+    return max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9), (h2d + d2h) / (both_gbs * 1e9))
 
 
 def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
@@ -616,6 +647,7 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
         # selscan_fwd_host(_ex): H2D, kernels, D2H, synchronise
         ss.selscan_fwd(*host[:5], True, y=y_host, hT=hT_host, **kw)
     e2e_call()                                       # warm the copy path
+    evict_host_caches()
     barrier(world, dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -623,17 +655,16 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
     t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = y_host.numel() * y_host.element_size() + (hT_host.numel() * 4 if hT_host is not None else 0)
-    h2d_gbs, d2h_gbs = pcie_rates(dev)
-    # The link copies both ways at once, so the copies alone take at least
-    # the longer of the two directions.
-    bound = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9))
+    rates = pcie_rates(dev)
+    bound = copy_bound_s(h2d, d2h, rates)
     per_step = t_e2e / e2e_steps
     return {"value": world * elems * e2e_steps / t_e2e, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": per_step * 1e3,
-            "pcie": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "copy_bound_ms": bound * 1e3,
-                     "frac_of_copy_bound": bound / per_step,
-                     "note": "one-way rates of 256 MB pinned copies measured in this run"}}
+            "pcie": {"h2d_gbs": rates[0], "d2h_gbs": rates[1], "both_ways_gbs": rates[2],
+                     "copy_bound_ms": bound * 1e3, "frac_of_copy_bound": bound / per_step,
+                     "note": "rates of 256 MB pinned copies measured in this run (one way each, and both "
+                             "ways at once); host inputs evicted from the CPU caches before the timed calls"}}
 
 
 def measure_config(wid, args, world, local, dev, alu):
@@ -744,6 +775,7 @@ def run_conv(args, world, rank, local, dev, w, alu=None):
     hx = torch.from_numpy(x).pin_memory()
     hy = torch.empty(hx.shape, dtype=hx.dtype, pin_memory=True)
     e2e_steps = max(1, min(args.steps, 20))
+    evict_host_caches()
     barrier(world, dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -831,6 +863,7 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
             "dC": (w.Bsz, w.L, w.N)}
     hout = {k: torch.empty(shape, dtype=torch.float32, pin_memory=True) for k, shape in outs.items()}
     e2e_steps = max(1, min(args.steps, 10))
+    evict_host_caches()
     barrier(world, dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -953,6 +986,7 @@ def run_decode(args, world, rank, local, dev, w, alu=None):
     hx = [torch.from_numpy(a).pin_memory() for a in W.decode_step_inputs(w, 0)]
     hy = torch.empty(w.Bsz, w.D, pin_memory=True)
     e2e_steps = max(1, min(args.steps, 50))
+    evict_host_caches()
     barrier(world, dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -1049,6 +1083,7 @@ def run_ssd(args, world, rank, local, dev, w):
             for a, d in ((x, tdt), (dt, torch.float32), (A, torch.float32), (B, tdt), (C, tdt))]
     hy = torch.empty(tuple(x.shape), dtype=tdt, pin_memory=True)
     e2e_steps = max(1, min(args.steps, 20))
+    evict_host_caches()
     barrier(world, dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
