@@ -18,12 +18,12 @@
 //   1. ssd_state_kernel: S of every chunk (tcgen05: M = N, N = P, K = Q),
 //      stored fp16 (the precision it has as an operand anyway). The same
 //      launch has one more CTA per batch row and chunk that forms
-//      G = C B^T (M = Q, N = Q, K = N), which no head changes, stored fp32,
-//      and stores C converted to the output kernel's fp16 operand order;
+//      G = C B^T (M = Q, N = Q, K = N), which no head changes, and stores it,
+//      and C, as fp16 in the output kernel's operand order;
 //   2. ssd_carry_kernel: H_in of every chunk in order, elementwise in fp32,
 //      written as fp16 in the output kernel's operand layout, and hT;
-//   3. ssd_out_kernel: C H_in (K = N) into one TMEM tile, the masked and
-//      decayed G (from shared memory) times X (M = Q, N = P, K = Q) into a
+//   3. ssd_out_kernel: G masked and decayed in place in shared memory, times
+//      X (M = Q, N = P, K = Q) into one TMEM tile, C H_in (K = N) into a
 //      second; y = G X + diag(e^s) C H_in.
 // Kernels 2 and 3 are launched as programmatic dependents of the one before.
 // Each CTA brings every tile it needs into shared memory in one round trip
@@ -59,7 +59,7 @@ struct SsdArgs {
     float *hT;           // (Bsz, H, N, P) or null
     __half *S;           // (Bsz, H, nch, P, N): each chunk's state from zero, [p][n], fp16
     __half *Hin;         // (Bsz, H, nch, P x N): the state entering each chunk, fp16 operand order
-    float *G;            // (Bsz, nch, Q, Q): C B^T of each chunk, [t][r]
+    __half *G;           // (Bsz, nch, Q x Q): C B^T of each chunk, fp16, in operand order (K = Q)
     __half *Cop;         // (Bsz, nch, Q x N): C of each chunk as the output kernel's fp16 A operand
     float *dec;          // (Bsz, H, nch): exp(s_last) of each chunk
     unsigned *fault;
@@ -335,14 +335,17 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
             tmem_ld16_async(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)(16 * q), graw[q]);
         tmem_wait_ld();
         if (ok && lane < 16) {
+            // Row t as fp16 core rows of the output kernel's A operand (K = Q).
             const int t = 16 * warp + lane;
-            float4 *dst = reinterpret_cast<float4 *>(a.G + ((b * a.nch + c) * Q + t) * Q);
+            __half *dst = a.G + (b * a.nch + c) * Q * Q;
 #pragma unroll
-            for (int q = 0; q < Q / 4; ++q)
-                dst[q] = make_float4(__uint_as_float(graw[q / 4][(q % 4) * 4]),
-                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 1]),
-                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 2]),
-                                     __uint_as_float(graw[q / 4][(q % 4) * 4 + 3]));
+            for (int r0 = 0; r0 < Q; r0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __uint_as_float(graw[(r0 + i) / 16][(r0 + i) % 16]);
+                *reinterpret_cast<uint4 *>(dst + core_index(t, r0, Q)) = pack8(v);
+            }
         }
         // C as the output kernel's A operand, already in core-matrix order.
         {
@@ -483,21 +486,26 @@ __host__ __device__ constexpr int ssd_out_cols()   // TMEM columns: G X (P) and 
     return 2 * P <= 32 ? 32 : (2 * P <= 64 ? 64 : (2 * P <= 128 ? 128 : 256));
 }
 
+// The first shared-memory region holds the X tile until it is transposed,
+// then the incoming state's operand.
+template <typename T, int N, int P>
+__host__ __device__ constexpr int ssd_out_region1()
+{
+    return P * N * 2 > kSsdQ * P * (int)sizeof(T) ? P * N * 2 : kSsdQ * P * (int)sizeof(T);
+}
+
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
 {
     constexpr int Q = kSsdQ;
     constexpr int COLS = ssd_out_cols<P>();
     extern __shared__ __align__(1024) unsigned char sm[];
-    constexpr int UNION = Q * P * (int)sizeof(T) > Q * Q * 2 ? Q * P * (int)sizeof(T) : Q * Q * 2;
-    __half *A1 = reinterpret_cast<__half *>(sm);                       // C: Q rows, K = N
-    __half *B4 = A1 + Q * N;                                            // H_in^T: P rows, K = N
-    __half *BX = B4 + P * N;                                            // X^T: P rows, K = Q
-    float *rG = reinterpret_cast<float *>(BX + P * Q);                  // C B^T [Q][Q]
-    unsigned char *un = reinterpret_cast<unsigned char *>(rG + Q * Q);
-    T *rX = reinterpret_cast<T *>(un);                                  // X tile [Q][P] ...
-    __half *A2 = reinterpret_cast<__half *>(un);                        // ... then the masked G: Q rows, K = Q
-    float *dl = reinterpret_cast<float *>(un + UNION);
+    __half *B4 = reinterpret_cast<__half *>(sm);                        // H_in^T: P rows, K = N ...
+    T *rX = reinterpret_cast<T *>(sm);                                  // ... after the X tile [Q][P]
+    __half *A1 = reinterpret_cast<__half *>(sm + ssd_out_region1<T, N, P>());   // C: Q rows, K = N
+    __half *BX = A1 + Q * N;                                            // X^T: P rows, K = Q
+    __half *GA = BX + P * Q;                                            // C B^T, then masked: Q rows, K = Q
+    float *dl = reinterpret_cast<float *>(GA + Q * Q);
     float *s = dl + Q;
     float *es = s + Q;
     __shared__ uint32_t tbase;
@@ -510,18 +518,17 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     const bool carry = c > 0 || a.h0 != nullptr;
     if (warp == 0)   // first, as in the state kernel
         tmem_alloc(&tbase, COLS);
-    // The call's own inputs first; then, once the kernels before have
-    // completed, what they wrote: C B^T, C in operand order and the incoming
-    // state (plain copies, already in operand order).
+    // The call's own inputs, and what the state kernel wrote (C B^T and C,
+    // already in operand order): this kernel starts only once every CTA of
+    // the carry kernel has passed its own wait for the state kernel, so that
+    // kernel has completed. The incoming state, the carry kernel's result,
+    // comes once the X tile is out of its space.
     copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
     SsdDt dtv{};
     if (warp == 0)
         dtv = ssd_dt_load(a, b, h, t0, rows);
-    grid_dep_wait();
-    copy_tile<float, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, rG);
+    copy_tile<__half, Q, Q>(a.G + (b * a.nch + c) * Q * Q, Q, Q, GA);
     copy_tile<__half, Q, N>(a.Cop + (b * a.nch + c) * Q * N, N, Q, A1);
-    if (carry)
-        copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
     ssd_cp_commit();
     if (tid == 0) {
         mbar_init(&mbar, 1);
@@ -534,40 +541,59 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     if (tid < Q)
         es[tid] = ex2(s[tid] * kLog2e);
     transpose_to_operand<T, Q, P>(rX, nullptr, BX);
+    __syncthreads();   // the X tile is consumed
+    // Every CTA waits for the carry kernel, also when it reads nothing of it,
+    // so that this grid never completes before that one.
+    grid_dep_wait();
+    if (carry) {
+        copy_tile<__half, P, N>(a.Hin + ((b * a.H + h) * a.nch + c) * N * P, N, P, B4);
+        ssd_cp_commit();
+    }
+    // Mask, decay and scale C B^T in place into the masked product's A
+    // operand while the incoming state arrives: every thread takes one core
+    // row (eight columns of one row) at a time.
+#pragma unroll 2
+    for (int e = tid; e < Q * (Q / 8); e += kSsdThreads) {
+        const int t = e / (Q / 8), r0 = (e % (Q / 8)) * 8;
+        uint4 *cell = reinterpret_cast<uint4 *>(GA + core_index(t, r0, Q));
+        const uint4 graw = *cell;
+        const __half2 *g2 = reinterpret_cast<const __half2 *>(&graw);
+        const float st = s[t];
+        float m[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 gf = __half22float2(g2[i]);
+            const int r = r0 + 2 * i;
+            m[2 * i] = r <= t ? gf.x * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
+            m[2 * i + 1] = r + 1 <= t ? gf.y * ex2((st - s[r + 1]) * kLog2e) * dl[r + 1] : 0.0f;
+        }
+        *cell = pack8(m);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tY = tbase, tH = tbase + P;
-    if (tid == 0 && carry) {
-        constexpr uint32_t id = umma_idesc_f16(Q, P);
-#pragma unroll
-        for (int kk = 0; kk < N / 16; ++kk)
-            umma_f16(tH, umma_tile_desc(A1, N, kk), umma_tile_desc(B4, N, kk), id, kk > 0);
-    }
-    // Mask, decay and scale C B^T into the masked product's A operand while
-    // C H_in runs: every thread takes eight columns (one core row) at a time.
-#pragma unroll 2
-    for (int e = tid; e < Q * (Q / 8); e += kSsdThreads) {
-        const int t = e / (Q / 8), r0 = (e % (Q / 8)) * 8;
-        const float st = s[t];
-        float m[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + i;
-            m[i] = r <= t ? rG[t * Q + r] * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
-        }
-        *reinterpret_cast<uint4 *>(A2 + core_index(t, r0, Q)) = pack8(m);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     if (tid == 0) {
         constexpr uint32_t id = umma_idesc_f16(Q, P);
 #pragma unroll
         for (int kk = 0; kk < Q / 16; ++kk)
-            umma_f16(tY, umma_tile_desc(A2, Q, kk), umma_tile_desc(BX, Q, kk), id, kk > 0);
+            umma_f16(tY, umma_tile_desc(GA, Q, kk), umma_tile_desc(BX, Q, kk), id, kk > 0);
+    }
+    if (carry) {
+        ssd_cp_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (tid == 0) {
+        if (carry) {
+            constexpr uint32_t id = umma_idesc_f16(Q, P);
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk)
+                umma_f16(tH, umma_tile_desc(A1, N, kk), umma_tile_desc(B4, N, kk), id, kk > 0);
+        }
         umma_commit(&mbar);   // both products
     }
     const bool ok = mma_wait(&mbar, 0);
@@ -628,14 +654,12 @@ constexpr size_t ssd_state_smem()
     return (size_t)(N + P) * kSsdQ * 2 + (size_t)kSsdQ * (N + P) * sizeof(T) + 3 * kSsdQ * 4;
 }
 
-// The X tile and the masked product share their space: X is transposed into
-// its operand before the masking writes.
+// The X tile and the incoming state's operand share their space; C B^T is
+// masked in place.
 template <typename T, int N, int P>
 constexpr size_t ssd_out_smem()
 {
-    return ((size_t)kSsdQ * N + (size_t)P * N + (size_t)P * kSsdQ) * 2 + (size_t)kSsdQ * kSsdQ * 4 +
-           ((size_t)kSsdQ * P * sizeof(T) > (size_t)kSsdQ * kSsdQ * 2 ? (size_t)kSsdQ * P * sizeof(T)
-                                                                       : (size_t)kSsdQ * kSsdQ * 2) +
+    return (size_t)ssd_out_region1<T, N, P>() + ((size_t)kSsdQ * N + (size_t)P * kSsdQ + (size_t)kSsdQ * kSsdQ) * 2 +
            3 * kSsdQ * 4;
 }
 
@@ -762,10 +786,10 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
-    // Workspace: S and the incoming states (fp16), C B^T of every chunk
-    // (fp32), C of every chunk as an fp16 operand, the chunk decays.
+    // Workspace: S and the incoming states (fp16), C B^T and C of every
+    // chunk as fp16 operands, the chunk decays.
     const size_t sbytes = (size_t)(Bsz * H * nch) * (size_t)(N * P) * 2, hbytes = sbytes,
-                 gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 4, cbytes = (size_t)(Bsz * nch) * kSsdQ * N * 2,
+                 gbytes = (size_t)(Bsz * nch) * kSsdQ * kSsdQ * 2, cbytes = (size_t)(Bsz * nch) * kSsdQ * N * 2,
                  dbytes = (size_t)(Bsz * H * nch) * 4;
     const size_t total = sbytes + hbytes + gbytes + cbytes + dbytes;
     void *ws = nullptr;
@@ -779,7 +803,7 @@ extern "C" int selscan_ssd_fwd(const void *x, const float *dt, const float *A, c
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.y = y; a.h0 = h0; a.hT = hT;
     a.S = static_cast<__half *>(ws);
     a.Hin = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes);
-    a.G = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes);
+    a.G = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes + hbytes);
     a.Cop = reinterpret_cast<__half *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes);
     a.dec = reinterpret_cast<float *>(static_cast<char *>(ws) + sbytes + hbytes + gbytes + cbytes);
     a.Bsz = Bsz; a.L = L; a.H = H;
