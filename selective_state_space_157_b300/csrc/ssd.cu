@@ -203,7 +203,7 @@ struct SsdDt {
 
 __device__ __forceinline__ SsdDt ssd_dt_load(const SsdArgs &a, int64_t b, int64_t h, int64_t t0, int rows)
 {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     SsdDt r;
     r.Ah = __ldg(a.A + h);
 #pragma unroll
@@ -225,10 +225,10 @@ constexpr float kSsdMinLogDecay = 40.0f;
 
 // Step sizes and cumulative log-decays of one chunk: dl[t] (after softplus)
 // and s[t] = sum_{r <= t} max(dl[r] A[h], -kSsdMinLogDecay), t < Q. Rows past
-// the sequence get dl = 0, so they neither decay nor add. Warp 0 only.
+// the sequence get dl = 0, so they neither decay nor add. One warp.
 __device__ __forceinline__ void ssd_decays_from(const SsdArgs &a, const SsdDt &raw, int rows, float *dl, float *s)
 {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     float v[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -253,7 +253,7 @@ __device__ __forceinline__ void ssd_decays_from(const SsdArgs &a, const SsdDt &r
     s[lane + 32] = v[1] + first_half;
 }
 
-// The same, loaded and computed in one go. Warp 0 only.
+// The same, loaded and computed in one go. One warp.
 __device__ __forceinline__ void ssd_decays(const SsdArgs &a, int64_t b, int64_t h, int64_t t0, int rows, float *dl,
                                            float *s)
 {
@@ -267,35 +267,49 @@ __device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t parity)
     return __syncthreads_and(mbar_wait(bar, parity));
 }
 
-// TMEM columns of the state kernel: the state's P, or the 64 of C B^T.
-template <int P>
-__host__ __device__ constexpr int ssd_state_cols()
+// Heads per CTA of the state kernel: they share the chunk's B^T operand.
+template <typename T, int P>
+__host__ __device__ constexpr int ssd_state_heads()
 {
-    return P < 64 ? 64 : P;
+    return sizeof(T) == 2 ? (P <= 64 ? 4 : 2) : (P <= 64 ? 2 : 1);
 }
 
-// 1. Each chunk's contribution to the state, S = (B o w)^T X (N x P),
-// stored transposed, [p][n], fp16, for the carry scan. CTAs with blockIdx.y == H
-// instead form C B^T of their chunk (fp32, [t][r]) for the output kernel, and
-// store C in its operand order for it.
+// TMEM columns of the state kernel: P for each of its heads, or the 64 of
+// C B^T.
+template <typename T, int P>
+__host__ __device__ constexpr int ssd_state_cols()
+{
+    return ssd_state_heads<T, P>() * P < 64 ? 64 : ssd_state_heads<T, P>() * P;
+}
+
+// 1. Each chunk's contribution to the state, S = (B o w)^T X = B^T (w o X)
+// (N x P), stored transposed, [p][n], fp16, for the carry scan. A CTA takes
+// HPC heads of one chunk: the chunk's B^T is converted once and serves as the
+// A operand of every head's product; each head's X rows are scaled by its
+// own w. CTAs with blockIdx.y == the number of head groups instead form
+// C B^T of their chunk for the output kernel, and C, both as fp16 operands.
 template <typename T, int N, int P>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 {
     constexpr int Q = kSsdQ;
-    constexpr int COLS = ssd_state_cols<P>();
+    constexpr int HPC = ssd_state_heads<T, P>();
+    constexpr int COLS = ssd_state_cols<T, P>();
     extern __shared__ __align__(1024) unsigned char sm[];
-    __half *A3 = reinterpret_cast<__half *>(sm);                  // (B o w)^T: N rows, K = Q
-    __half *BX = A3 + N * Q;                                       // X^T: P rows, K = Q
-    T *rB = reinterpret_cast<T *>(BX + P * Q);                     // B tile [Q][N]
-    T *rX = rB + Q * N;                                            // X tile [Q][P]
-    float *dl = reinterpret_cast<float *>(rX + Q * P);
-    float *s = dl + Q;
-    float *w = s + Q;
+    __half *A3 = reinterpret_cast<__half *>(sm);                  // B^T: N rows, K = Q
+    __half *BX = A3 + N * Q;                                       // HPC x (w o X)^T: P rows, K = Q
+    T *rB = reinterpret_cast<T *>(BX + HPC * P * Q);               // B tile [Q][N]
+    T *rX = rB + Q * N;                                            // HPC x X tile [Q][P]
+    float *dl = reinterpret_cast<float *>(rX + HPC * Q * P);       // HPC x [Q]
+    float *s = dl + HPC * Q;
+    float *w = s + HPC * Q;
     __shared__ uint32_t tbase;
     __shared__ __align__(8) uint64_t mbar;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t b = blockIdx.z, h = blockIdx.y, c = blockIdx.x;
+    const int64_t b = blockIdx.z, c = blockIdx.x;
+    const int64_t ngroups = (a.H + HPC - 1) / HPC;
+    const int64_t h0 = (int64_t)blockIdx.y * HPC;    // the group's first head
+    const int nh = (int)min((int64_t)HPC, a.H - h0);
     const int64_t t0 = c * Q;
     const int rows = (int)min((int64_t)Q, a.L - t0);
     // TMEM first: the allocation permit is given up at once, so the SM can
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     if (warp == 0)
         tmem_alloc(&tbase, COLS);
 
-    if (h == a.H) {
+    if ((int64_t)blockIdx.y == ngroups) {
         // C B^T of the chunk: C and B rows as K-major operands (over the
         // space the state's operands use in the other CTAs).
         __half *A1 = A3, *B1 = reinterpret_cast<__half *>(rB);
@@ -365,22 +379,24 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     }
 
     copy_tile<T, Q, N>(static_cast<const T *>(a.B) + (b * a.L + t0) * N, N, rows, rB);
-    copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h) * P, a.H * P, rows, rX);
+    for (int j = 0; j < nh; ++j)
+        copy_tile<T, Q, P>(static_cast<const T *>(a.x) + ((b * a.L + t0) * a.H + h0 + j) * P, a.H * P, rows,
+                           rX + j * Q * P);
     ssd_cp_commit();
     if (tid == 0) {
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
-    if (warp == 0)
-        ssd_decays(a, b, h, t0, rows, dl, s);
+    if (warp < nh)   // warp j: head j's step sizes and decays
+        ssd_decays(a, b, h0 + warp, t0, rows, dl + warp * Q, s + warp * Q);
     ssd_cp_wait();
     __syncthreads();
-    const float slast = s[Q - 1];
-    if (tid < Q)
-        w[tid] = ex2((slast - s[tid]) * kLog2e) * dl[tid];
+    for (int e = tid; e < nh * Q; e += kSsdThreads)   // w = exp(s_last - s_t) dl_t, head e / Q
+        w[e] = ex2((s[(e / Q) * Q + Q - 1] - s[e]) * kLog2e) * dl[e];
     __syncthreads();
-    transpose_to_operand<T, Q, N>(rB, w, A3);
-    transpose_to_operand<T, Q, P>(rX, nullptr, BX);
+    transpose_to_operand<T, Q, N>(rB, nullptr, A3);
+    for (int j = 0; j < nh; ++j)
+        transpose_to_operand<T, Q, P>(rX + j * Q * P, w + j * Q, BX + j * P * Q);
     fence_proxy_async_smem();   // the tensor core reads shared memory through the async proxy
     tc_fence_before();
     __syncthreads();
@@ -388,9 +404,12 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     const uint32_t tm = tbase;
     if (tid == 0) {
         constexpr uint32_t id = umma_idesc_f16(N, P);
+        for (int j = 0; j < nh; ++j) {
 #pragma unroll
-        for (int kk = 0; kk < Q / 16; ++kk)
-            umma_f16(tm, umma_tile_desc(A3, Q, kk), umma_tile_desc(BX, Q, kk), id, kk > 0);
+            for (int kk = 0; kk < Q / 16; ++kk)
+                umma_f16(tm + (uint32_t)(j * P), umma_tile_desc(A3, Q, kk), umma_tile_desc(BX + j * P * Q, Q, kk),
+                         id, kk > 0);
+        }
         umma_commit(&mbar);
     }
     const bool ok = mma_wait(&mbar, 0);
@@ -400,22 +419,23 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     // a warp's lanes hold consecutive n, so the [p][n] stores coalesce.
     const int n = N == 128 ? 32 * warp + lane : 16 * warp + lane;
     const bool mine = ok && (N == 128 || lane < 16);
-    __half *dst = a.S + ((b * a.H + h) * a.nch + c) * N * P + n;
+    for (int j = 0; j < nh; ++j) {
+        __half *dst = a.S + ((b * a.H + h0 + j) * a.nch + c) * N * P + n;
 #pragma unroll
-    for (int p0 = 0; p0 < P; p0 += 16) {
-        float v[16];
-        tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)p0, v);
-        if (mine) {
+        for (int p0 = 0; p0 < P; p0 += 16) {
+            float v[16];
+            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)(j * P + p0), v);
+            if (mine) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                dst[(p0 + i) * N] = __float2half_rn(v[i]);
+                for (int i = 0; i < 16; ++i)
+                    dst[(p0 + i) * N] = __float2half_rn(v[i]);
+            }
         }
     }
-    if (tid == 0) {
-        a.dec[(b * a.H + h) * a.nch + c] = ex2(slast * kLog2e);
-        if (!ok)
-            record_fault(a.fault, kFaultMmaTimeout);
-    }
+    if (tid < nh)
+        a.dec[(b * a.H + h0 + tid) * a.nch + c] = ex2(s[tid * Q + Q - 1] * kLog2e);
+    if (tid == 0 && !ok)
+        record_fault(a.fault, kFaultMmaTimeout);
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
@@ -651,7 +671,9 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
 template <typename T, int N, int P>
 constexpr size_t ssd_state_smem()
 {
-    return (size_t)(N + P) * kSsdQ * 2 + (size_t)kSsdQ * (N + P) * sizeof(T) + 3 * kSsdQ * 4;
+    constexpr size_t hpc = (size_t)ssd_state_heads<T, P>();
+    return ((size_t)N + hpc * P) * kSsdQ * 2 + (size_t)kSsdQ * ((size_t)N + hpc * P) * sizeof(T) +
+           3 * hpc * kSsdQ * 4;
 }
 
 // The X tile and the incoming state's operand share their space; C B^T is
@@ -680,7 +702,7 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
 {
     auto k1 = ssd_state_kernel<T, N, P>;
     auto k3 = ssd_out_kernel<T, N, P>;
-    const size_t s1 = ssd_pad(ssd_state_smem<T, N, P>(), 512 / ssd_state_cols<P>());
+    const size_t s1 = ssd_pad(ssd_state_smem<T, N, P>(), 512 / ssd_state_cols<T, P>());
     const size_t s3 = ssd_pad(ssd_out_smem<T, N, P>(), 512 / ssd_out_cols<P>());
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3);
@@ -690,7 +712,8 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
-    k1<<<dim3(grid.x, grid.y + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
+    const unsigned groups = (unsigned)((a.H + ssd_state_heads<T, P>() - 1) / ssd_state_heads<T, P>());
+    k1<<<dim3(grid.x, groups + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
     const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
     // The carry and output kernels start early (programmatic dependent
     // launch) and wait in the kernel for what the one before wrote.

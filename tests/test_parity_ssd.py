@@ -49,10 +49,14 @@ def test_pages_layer_bf16(orc, h0):
 
 
 @pytest.mark.parametrize("shape", [(2, 100, 3, 64, 128), (1, 1, 2, 64, 64), (2, 200, 2, 32, 64),
-                                   (1, 129, 2, 128, 128), (3, 64, 1, 32, 128), (1, 63, 4, 64, 64)],
+                                   (1, 129, 2, 128, 128), (3, 64, 1, 32, 128), (1, 63, 4, 64, 64),
+                                   (1, 70, 5, 128, 64), (2, 65, 6, 32, 128), (1, 130, 9, 64, 128)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 def test_shapes(orc, shape, dtype):
+    """Every state size and headdim, partial last chunks, and head counts
+    that leave the last group of heads (the state kernel takes several per
+    CTA) partly empty."""
     Bsz, L, H, P, N = shape
     run_case(orc, Bsz, L, H, P, N, dtype, seed=sum(shape) + (dtype == W.BF16), h0=(L % 2 == 1))
 
