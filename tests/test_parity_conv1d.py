@@ -61,6 +61,18 @@ def test_conv1d_segments_longer_than_the_ring(orc, dtype, K, Bsz, L, D):
     assert np.array_equal(to_np(st).astype(np.float32), st_ref)
 
 
+def test_conv1d_workload_full_size(orc):
+    """The benchmark's conv1d workload (Bsz=2 L=2048 D=1536 K=4, fp32, SiLU,
+    carried state), every output and the handed-over state."""
+    w = W.WORKLOADS[8]
+    x, wt, bias, state = W.conv_inputs(w.Bsz, w.L, w.D, w.conv_K, seed=w.seed, with_state=True)
+    out, st = ss.conv1d(to_dev(x), to_dev(wt), to_dev(bias), state_in=to_dev(state), return_state=True)
+    torch.cuda.synchronize()
+    ref, st_ref = orc.conv1d(x, wt, bias, state_in=state)
+    assert scaled_err(to_np(out), ref) <= TOL[W.F32]
+    assert np.array_equal(to_np(st).astype(np.float32), st_ref)
+
+
 def test_conv1d_without_silu_or_bias(orc):
     x, w, _, _ = W.conv_inputs(2, 100, 64, 4, seed=5)
     out = ss.conv1d(to_dev(x), to_dev(w), None, silu=False)

@@ -57,20 +57,25 @@ def test_workload_mamba370m_bf16_all_outputs(orc):
     check(orc, inp)
 
 
-def test_workload_long_sampled_chains(orc):
-    """L = 131072 at full size, in the launch configuration the benchmark uses;
-    every output of 48 chains spread over the channels, and their final states."""
+def test_workload_long_all_outputs(orc):
+    """L = 131072 at full size, in the launch configuration the benchmark uses
+    (37 chunks): every output and the final state against the oracle over the
+    whole workload (201 M outputs; the oracle runs on all host cores, and the
+    error is taken slice by slice to bound host memory)."""
     inp = W.workload_inputs(4)
     x, dl, A, B, C, _ = fwd_dev(inp)
     y, hT = ss.selscan_fwd(x, dl, A, B, C, delta_softplus=True, return_final_state=True)
     torch.cuda.synchronize()
-    D = inp.x.shape[2]
-    chains = np.unique(np.linspace(0, D - 1, 48).astype(np.int64))
-    yr, hr = orc.selscan_fwd_chains(inp.x, inp.delta, inp.A, inp.B, inp.C, chains, True)
-    yg = to_np(y[0][:, torch.from_numpy(chains).cuda()]).T        # (nchains, L)
-    assert scaled_err(yg, yr) <= TOL[W.F32]
-    assert scaled_err(to_np(hT[0][torch.from_numpy(chains).cuda()]), hr) <= TOL[W.F32]
-    assert torch.isfinite(y).all()
+    del x, dl, B, C
+    yr, hr = orc.selscan_fwd(inp.x, inp.delta, inp.A, inp.B, inp.C, True)
+    yg = to_np(y)
+    del y
+    L = yg.shape[1]
+    worst = 0.0
+    for t in range(0, L, 8192):
+        worst = max(worst, scaled_err(yg[:, t:t + 8192], yr[:, t:t + 8192]))
+    assert worst <= TOL[W.F32], worst
+    assert scaled_err(to_np(hT), hr) <= TOL[W.F32]
 
 
 # ---------------------------------------------------------------- shapes
