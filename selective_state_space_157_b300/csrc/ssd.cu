@@ -445,8 +445,10 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 // 2. The state entering each chunk, in chunk order: fp32 carries, stored as
 // fp16 in the output kernel's operand order (P rows, K = N, core-matrix
 // order), and hT ([n][p], fp32). A thread owns eight consecutive n of one p
-// (one 16-byte core row); the chunk states are loaded kCarryBatch chunks
-// ahead of the serial fold.
+// (one 16-byte core row); consecutive threads take consecutive core rows of
+// the operand, so a warp's stores are 512 contiguous bytes (and its loads of
+// the [p][n] chunk states 64-byte runs). The chunk states are loaded
+// kCarryBatch chunks ahead of the serial fold.
 constexpr int kCarryBatch = 8;
 
 template <int N, int P>
@@ -459,14 +461,15 @@ __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
     if (i >= a.Bsz * a.H * (NP / 8))
         return;
     const int64_t bh = i / (NP / 8);
-    const int pn = (int)(i - bh * (NP / 8)) * 8;
-    const int p = pn / N, n0 = pn % N;
+    const int r = (int)(i - bh * (NP / 8));            // core row r of the operand
+    const int p = ((r >> 3) / (N / 8)) * 8 + (r & 7), n0 = ((r >> 3) % (N / 8)) * 8;
+    const int pn = p * N + n0;
     float carry[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
         carry[q] = a.h0 ? __ldg(a.h0 + bh * NP + (int64_t)(n0 + q) * P + p) : 0.0f;
     const __half *Sp = a.S + bh * a.nch * NP + pn;
-    __half *Hp = a.Hin + bh * a.nch * NP + core_index(p, n0, N);
+    __half *Hp = a.Hin + bh * a.nch * NP + (int64_t)r * 8;   // = core_index(p, n0, N)
     const float *dp = a.dec + bh * a.nch;
     for (int c0 = 0; c0 < a.nch; c0 += kCarryBatch) {
         uint4 sv[kCarryBatch];
