@@ -354,9 +354,12 @@ int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const
  * Sizes: Bsz, L, D >= 0 with Bsz <= 65535; 1 <= N <= 32. Every output is
  * overwritten; no output may overlap an input or another output. Pointers
  * 4-byte aligned. L == 0 gives dA = 0 and dh0 = dhT (or zeros).
- * Workspace: the state at the start of every 32-step chunk, Bsz * D * P
- * * ceil(L / 32) floats with P the power of two >= N, from the same
- * stream-ordered pool as selscan_fwd's.
+ * Workspace, from the same stream-ordered pool as selscan_fwd's: the local
+ * state and the running sum of dl at the start of every 16-step chunk,
+ * Bsz * ceil(L / 16) * D * (Np + 1) floats with Np the smallest of 4, 8, 16
+ * and 32 that is >= N; and per segment (L is cut into K segments of whole
+ * chunks, K at most the number of blocks that fill the GPU once) four
+ * Bsz * K * D * Np arrays and one of Bsz * K * D floats.
  * dA, dB and dC are sums formed with atomic additions, so their last bits
  * may differ from run to run; dx, ddelta and dh0 are reproducible.
  * Errors as for selscan_fwd.
@@ -390,8 +393,11 @@ int selscan_bwd(const float *x, const float *delta, const float *A, const float 
  * results agree with an exact evaluation to about 1e-3 relative for either
  * dtype. Pointers: x, B, C, y, h0 and hT 16-byte aligned, dt and A
  * 4-byte aligned. y and hT must not overlap any input or each other.
- * Workspace: Bsz * H * ceil(L / 64) * (N * P + 1) fp32 from the same
- * stream-ordered pool as selscan_fwd's. Errors as for selscan_fwd.
+ * Workspace, from the same stream-ordered pool as selscan_fwd's, with
+ * nch = ceil(L / 64): 4 * Bsz * H * nch * N * P bytes (each chunk's own state
+ * and the state entering it, fp16), 2 * Bsz * nch * 64 * (64 + N) bytes
+ * (C B^T and C of each chunk, fp16) and 4 * Bsz * H * nch bytes (the chunk
+ * decays). Errors as for selscan_fwd.
  */
 int selscan_ssd_fwd(const void *x, const float *dt, const float *A, const void *B,
                     const void *C, void *y, const float *h0, float *hT, int64_t Bsz,

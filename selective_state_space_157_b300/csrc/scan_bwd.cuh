@@ -88,8 +88,9 @@ __host__ __device__ constexpr int bwd_main_smem(int P)
             kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * (kBwdThreads / P) + kBwdT * kBwdWarps * 2 * 4 * P) * 4;
 }
 // Steps a stage of the local kernel stages: whole chunks, as many as keep the
-// values a thread loads ahead (at most 16 per array) in registers without
-// spills.
+// values a thread loads ahead (at most 16 per array) in registers; at
+// P = 4 and 8 that leaves at most a 12-byte spill, at P = 1 and 2 (N <= 8,
+// more chains per block) the kernel spills more but those shapes are small.
 __host__ __device__ constexpr int bwd_local_tt(int P)
 {
     return P >= 4 ? 32 : 16;
