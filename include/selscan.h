@@ -371,6 +371,30 @@ int selscan_bwd(const float *x, const float *delta, const float *A, const float 
                 void *stream);
 
 /*
+ * selscan_bwd_gated -- selscan_bwd for the block's output with its skip and
+ * gate (the MambaBlock listing of youngju.dev "Mamba: Selective State Space
+ * Models", section 3.4: y = (scan + Dskip * x) * silu(z), as selscan_fwd_gated
+ * computes it), dy being dLoss/dy of that output. With s the scan's read-out
+ * and silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z))):
+ *
+ *   the scan's upstream gradient  gs = dy * silu(z)   (dy without a gate)
+ *   dz[b,t,d]  = dy (s + Dskip x) silu'(z)
+ *   dDskip[d]  = sum_{b,t} gs x                dx += gs Dskip
+ *
+ * and every other gradient as selscan_bwd with gs in place of dy.
+ *
+ *   Dskip, dDskip : (D) fp32, both or neither     z, dz : (Bsz, L, D) fp32, both or neither
+ *
+ * Everything else as selscan_bwd (with both NULL it is selscan_bwd). dDskip
+ * is a sum formed with atomic additions, like dA; dz is reproducible.
+ */
+int selscan_bwd_gated(const float *x, const float *delta, const float *A, const float *B,
+                      const float *C, const float *Dskip, const float *z, const float *h0,
+                      const float *dy, const float *dhT, float *dx, float *ddelta, float *dA,
+                      float *dB, float *dC, float *dDskip, float *dz, float *dh0, int64_t Bsz,
+                      int64_t L, int64_t D, int64_t N, int delta_softplus, void *stream);
+
+/*
  * selscan_ssd_fwd -- the Mamba-2 state space duality (SSD) forward
  * (youngju.dev "Mamba: Selective State Space Models", section 4.1: the
  * recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t and its dual form

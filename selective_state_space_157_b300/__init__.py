@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.selscan_test_fault_injection.argtypes = [INT, INT]
         L.selscan_bwd.restype = INT
         L.selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, P]
+        L.selscan_bwd_gated.restype = INT
+        L.selscan_bwd_gated.argtypes = [P] * 18 + [I64, I64, I64, I64, INT, P]
         _lib = L
     return _lib
 
@@ -223,13 +225,15 @@ def selscan_fwd(x, delta, A, B, C, delta_softplus: bool = False, h0=None,
 
 
 def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dhT=None,
-                want_dh0: bool = True, stream=None, check: bool = False):
-    """Backward pass of the forward scan (fp32, no skip or gate; see
-    ``include/selscan.h``): gradients of a loss with respect to x, delta, A,
-    B, C and h0, given dy (Bsz, L, D) = dLoss/dy and dhT (Bsz, D, N) =
-    dLoss/dhT or None. Device float32 tensors only. Returns a dict with
-    dx, ddelta (Bsz, L, D), dA (D, N), dB, dC (Bsz, L, N) and, when
-    ``want_dh0``, dh0 (Bsz, D, N).
+                want_dh0: bool = True, stream=None, check: bool = False, D_skip=None, z=None):
+    """Backward pass of the forward scan (fp32; see ``include/selscan.h``):
+    gradients of a loss with respect to x, delta, A, B, C and h0, given dy
+    (Bsz, L, D) = dLoss/dy and dhT (Bsz, D, N) = dLoss/dhT or None. Device
+    float32 tensors only. Returns a dict with dx, ddelta (Bsz, L, D), dA
+    (D, N), dB, dC (Bsz, L, N) and, when ``want_dh0``, dh0 (Bsz, D, N).
+    With ``D_skip`` (D,) and/or ``z`` (like x), dy is the gradient of the
+    block's output (scan + D_skip x) silu(z) (``selscan_bwd_gated``), and the
+    dict adds dD_skip and/or dz.
     """
     import torch
     dev = x.device
@@ -245,15 +249,30 @@ def selscan_bwd(x, delta, A, B, C, dy, delta_softplus: bool = False, h0=None, dh
         _need(h0, "h0", (Bsz, D, N), f, dev)
     if dhT is not None:
         _need(dhT, "dhT", (Bsz, D, N), f, dev)
+    if D_skip is not None:
+        _need(D_skip, "D_skip", (D,), f, dev)
+    if z is not None:
+        _need(z, "z", (Bsz, L, D), f, dev)
     g = dict(dx=torch.empty((Bsz, L, D), dtype=f, device=dev), ddelta=torch.empty((Bsz, L, D), dtype=f, device=dev),
              dA=torch.empty((D, N), dtype=f, device=dev), dB=torch.empty((Bsz, L, N), dtype=f, device=dev),
              dC=torch.empty((Bsz, L, N), dtype=f, device=dev))
     if want_dh0:
         g["dh0"] = torch.empty((Bsz, D, N), dtype=f, device=dev)
+    if D_skip is not None:
+        g["dD_skip"] = torch.empty((D,), dtype=f, device=dev)
+    if z is not None:
+        g["dz"] = torch.empty((Bsz, L, D), dtype=f, device=dev)
     with torch.cuda.device(dev):
-        rc = lib().selscan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(dy), _ptr(dhT),
-                               _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-                               _ptr(g.get("dh0")), Bsz, L, D, N, int(bool(delta_softplus)), _stream_ptr(stream))
+        if D_skip is None and z is None:
+            rc = lib().selscan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(dy), _ptr(dhT),
+                                   _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                                   _ptr(g.get("dh0")), Bsz, L, D, N, int(bool(delta_softplus)), _stream_ptr(stream))
+        else:
+            rc = lib().selscan_bwd_gated(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D_skip), _ptr(z),
+                                         _ptr(h0), _ptr(dy), _ptr(dhT), _ptr(g["dx"]), _ptr(g["ddelta"]),
+                                         _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD_skip")),
+                                         _ptr(g.get("dz")), _ptr(g.get("dh0")), Bsz, L, D, N,
+                                         int(bool(delta_softplus)), _stream_ptr(stream))
     _check(rc)
     if check:
         check_device_error(stream)
@@ -272,34 +291,37 @@ def _selective_scan_fn():
 
         class SelectiveScan(torch.autograd.Function):
             @staticmethod
-            def forward(ctx, x, delta, A, B, C, h0, delta_softplus, check):
+            def forward(ctx, x, delta, A, B, C, h0, delta_softplus, check, D_skip, z):
                 y, hT = selscan_fwd(x, delta, A, B, C, delta_softplus, h0=h0, return_final_state=True,
-                                    check=check)
-                ctx.save_for_backward(x, delta, A, B, C, h0)
+                                    check=check, D_skip=D_skip, z=z)
+                ctx.save_for_backward(x, delta, A, B, C, h0, D_skip, z)
                 ctx.delta_softplus = delta_softplus
                 ctx.check = check
                 return y, hT
 
             @staticmethod
             def backward(ctx, dy, dhT):
-                x, delta, A, B, C, h0 = ctx.saved_tensors
+                x, delta, A, B, C, h0, D_skip, z = ctx.saved_tensors
                 want_dh0 = h0 is not None and ctx.needs_input_grad[5]
                 g = selscan_bwd(x, delta, A, B, C, dy.contiguous(), ctx.delta_softplus, h0=h0,
                                 dhT=None if dhT is None else dhT.contiguous(), want_dh0=want_dh0,
-                                check=ctx.check)
-                return g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dh0"), None, None
+                                check=ctx.check, D_skip=D_skip, z=z)
+                return (g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dh0"), None, None,
+                        g.get("dD_skip"), g.get("dz"))
 
         _autograd_fn = SelectiveScan
     return _autograd_fn
 
 
-def selective_scan(x, delta, A, B, C, delta_softplus: bool = False, h0=None, check: bool = False):
+def selective_scan(x, delta, A, B, C, delta_softplus: bool = False, h0=None, check: bool = False,
+                   D_skip=None, z=None):
     """The forward scan as a differentiable torch operation: returns (y, hT),
     and ``backward`` runs ``selscan_bwd`` (the states are recomputed, not
-    stored). Device float32 tensors; h0 (Bsz, D, N) or None. ``check`` makes
-    the forward and the backward wait for their kernels and raise if a wait
-    inside one ran out."""
-    return _selective_scan_fn().apply(x, delta, A, B, C, h0, bool(delta_softplus), bool(check))
+    stored). Device float32 tensors; h0 (Bsz, D, N) or None; ``D_skip`` (D,)
+    and ``z`` (like x) make y the block's output (scan + D_skip x) silu(z),
+    differentiable in both. ``check`` makes the forward and the backward wait
+    for their kernels and raise if a wait inside one ran out."""
+    return _selective_scan_fn().apply(x, delta, A, B, C, h0, bool(delta_softplus), bool(check), D_skip, z)
 
 
 def selscan_fwd_noalloc(x, delta, A, B, C, y, delta_softplus: bool = False, h0=None, hT=None,

@@ -15,6 +15,12 @@
 // a_t h_{t-1} is taken as h_t - dl_t x_t B_t, so the adjoint needs the
 // recomputed states but not the decays of the step before.
 //
+// The block's skip and gate (GATE kernels): with y = (s + Dskip x) silu(z),
+// s the scan's read-out, the scan's upstream gradient is gs = gy silu(z)
+// (gy where there is no gate), and
+//   dz_t = gy_t (s_t + Dskip x_t) silu'(z_t),  silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z)))
+//   dx_t += gs_t Dskip,   dDskip = sum_{b,t} gs_t x_t.
+//
 // Layout of the work. A thread owns kBwdS = 4 states of one chain (b, d),
 // P threads a chain (P = the power of two >= N / 4, at most 8); a block is
 // kBwdThreads threads = CPB = kBwdThreads / P chains of one batch row. Sums
@@ -57,7 +63,9 @@ constexpr int kBwdS = 4;       // states per thread
 
 struct BwdArgs {
     const float *x, *delta, *A, *B, *C, *h0, *gy, *ghT;
+    const float *Dskip, *z;    // the block's skip (D) and gate (Bsz, L, D), or null (GATE kernels)
     float *dx, *ddelta, *dA, *dB, *dC, *dh0;
+    float *dDskip, *dz;        // their gradients, written when Dskip / z are given
     float *ckpt;               // (Bsz, nch, D, NP) local state at each chunk start
     float *spre;               // (Bsz, nch, D) sum of dl from the segment start to the chunk start
     float *hl, *gl;            // (Bsz, K, D, NP) segment end state from zero; adjoint out of the segment from zero
@@ -82,10 +90,12 @@ __device__ __forceinline__ float bwd_sigmoid(float u)
 // thread's checkpoint and its chain's sum of dl), the cooked chunk (dl, x,
 // gy, sigmoid) per step and chain, dx and d delta per step and chain, and
 // the per-warp sums of the dB and dC terms.
-__host__ __device__ constexpr int bwd_main_smem(int P)
+// GATE kernels also stage z, and keep gy silu'(z) and dz per step and chain.
+__host__ __device__ constexpr int bwd_main_smem(int P, bool gate = false)
 {
-    return (2 * 3 * kBwdT * (kBwdThreads / P) + 2 * 2 * kBwdT * 4 * P + 2 * 4 * kBwdThreads + 2 * (kBwdThreads / P) +
-            kBwdT * (kBwdThreads / P) * 4 + 2 * kBwdT * (kBwdThreads / P) + kBwdT * kBwdWarps * 2 * 4 * P) * 4;
+    return (2 * (gate ? 4 : 3) * kBwdT * (kBwdThreads / P) + 2 * 2 * kBwdT * 4 * P + 2 * 4 * kBwdThreads +
+            2 * (kBwdThreads / P) + kBwdT * (kBwdThreads / P) * 4 + (gate ? 4 : 2) * kBwdT * (kBwdThreads / P) +
+            kBwdT * kBwdWarps * 2 * 4 * P) * 4;
 }
 // Steps a stage of the local kernel stages: whole chunks, as many as keep the
 // values a thread loads ahead (at most 16 per array) in registers; at
@@ -108,11 +118,12 @@ template <int P, int TT> struct BwdRegs {
     static constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
     static constexpr int RX = (TT * CPB + kBwdThreads - 1) / kBwdThreads;
     static constexpr int RB = (TT * NP + kBwdThreads - 1) / kBwdThreads;
-    float u[RX], x[RX], gy[RX], B[RB], C[RB];
+    float u[RX], x[RX], gy[RX], z[RX], B[RB], C[RB];
 };
 
 // Loads steps t0 .. t0 + TT (zeros from step lim on, and past D and N).
-template <int P, int TT, bool WX, bool WGY, bool WB, bool WC>
+// WZ: also the gate z (when the call has one).
+template <int P, int TT, bool WX, bool WGY, bool WB, bool WC, bool WZ = false>
 __device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0, int64_t t0, int64_t lim,
                                          BwdRegs<P, TT> &r)
 {
@@ -126,6 +137,7 @@ __device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0
         r.u[q] = ok ? __ldg(a.delta + idx) : 0.0f;
         if (WX) r.x[q] = ok ? __ldg(a.x + idx) : 0.0f;
         if (WGY) r.gy[q] = ok ? __ldg(a.gy + idx) : 0.0f;
+        if (WZ) r.z[q] = (ok && a.z) ? __ldg(a.z + idx) : 0.0f;
     }
 #pragma unroll
     for (int q = 0; q < R::RB; ++q) {
@@ -139,8 +151,9 @@ __device__ __forceinline__ void bwd_load(const BwdArgs &a, int64_t b, int64_t d0
 }
 
 // Writes the loaded steps to shared memory: (dl, x, gy, sigmoid(u)) per step
-// and chain (dl = 0 from step lim on), B and C rows.
-template <int P, int TT, bool WX, bool WGY, bool WB, bool WC>
+// and chain (dl = 0 from step lim on), B and C rows. WZ: gy is taken times
+// silu(z), the scan's share of it, when the call has a gate.
+template <int P, int TT, bool WX, bool WGY, bool WB, bool WC, bool WZ = false>
 __device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P, TT> &r, int64_t d0, int64_t t0,
                                         int64_t lim, float4 *s_in, float *s_B, float *s_C)
 {
@@ -153,7 +166,10 @@ __device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P, TT> &
             const bool ok = t0 + i < lim && d0 + c < a.D;
             const float dl = !ok ? 0.0f : (a.softplus ? softplus(r.u[q]) : r.u[q]);
             const float sg = (ok && a.softplus && WX && WGY) ? bwd_sigmoid(r.u[q]) : 1.0f;
-            s_in[j] = make_float4(dl, WX ? r.x[q] : 0.0f, WGY ? r.gy[q] : 0.0f, sg);
+            float gv = WGY ? r.gy[q] : 0.0f;
+            if (WZ && a.z)
+                gv *= silu(r.z[q]);
+            s_in[j] = make_float4(dl, WX ? r.x[q] : 0.0f, gv, sg);
         }
     }
 #pragma unroll
@@ -254,7 +270,7 @@ template <int P> __device__ __forceinline__ bool bwd_rs_writer(int lane)
 // state before it: the adjoint from zero at the segment's end, which
 // unrolls to gl = sum_t exp(A S_t) gy_t C_t with S_t the sum of dl from the
 // segment's start through step t.
-template <int P>
+template <int P, bool GATE>
 __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs a)
 {
     constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
@@ -292,6 +308,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
         }
         for (int64_t i = gt; i < D * N; i += nthr)
             a.dA[i] = 0.0f;
+        if (GATE && a.dDskip)
+            for (int64_t i = gt; i < D; i += nthr)
+                a.dDskip[i] = 0.0f;
     }
 
     float2 h[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -301,13 +320,13 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
     float2 ep[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
     float S = 0.0f, Sc = 0.0f;   // compensated sum of dl through the last chunk
     BwdRegs<P, TL> r;
-    bwd_load<P, TL, true, true, true, true>(a, b, d0, s0, s1, r);
+    bwd_load<P, TL, true, true, true, true, GATE>(a, b, d0, s0, s1, r);
     for (int st = 0; st < nst; ++st) {
         const int64_t t0 = s0 + (int64_t)st * TL;
         __syncthreads();
-        bwd_put<P, TL, true, true, true, true>(a, r, d0, t0, s1, s_in, s_B, s_C);
+        bwd_put<P, TL, true, true, true, true, GATE>(a, r, d0, t0, s1, s_in, s_B, s_C);
         if (st + 1 < nst)
-            bwd_load<P, TL, true, true, true, true>(a, b, d0, t0 + TL, s1, r);
+            bwd_load<P, TL, true, true, true, true, GATE>(a, b, d0, t0 + TL, s1, r);
         __syncthreads();
 #pragma unroll 1
         for (int q = 0; q < CH; ++q) {
@@ -409,7 +428,7 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
 // dA, dB and dC are accumulated atomically (the local kernel zeroed them).
 // Chunk inputs arrive by cp.async into one of two raw buffers while the
 // block works on the other, so no register holds a chunk in flight.
-template <int P>
+template <int P, bool GATE>
 __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs a)
 {
     constexpr int CPB = kBwdThreads / P, NP = kBwdS * P;
@@ -417,14 +436,17 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
     constexpr int RS = (8 * P / 32) > 1 ? 8 * P / 32 : 1;   // reduce-scatter values left per lane
     extern __shared__ float4 bwd_smem4[];
     float4 *s_ck = bwd_smem4;                       // [2][kBwdThreads] checkpoints
-    float4 *s_in = s_ck + 2 * kBwdThreads;          // [T][CPB] (dl, x, gy, sigmoid)
-    float *s_raw = reinterpret_cast<float *>(s_in + TC);   // [2][3][T][CPB] delta, x, gy
-    float *s_rB = s_raw + 2 * 3 * TC;               // [2][T][NP]
+    constexpr int NRAW = GATE ? 4 : 3;
+    float4 *s_in = s_ck + 2 * kBwdThreads;          // [T][CPB] (dl, x, gy, sigmoid); gy times silu(z) if gated
+    float *s_raw = reinterpret_cast<float *>(s_in + TC);   // [2][NRAW][T][CPB] delta, x, gy (, z)
+    float *s_rB = s_raw + 2 * NRAW * TC;            // [2][T][NP]
     float *s_rC = s_rB + 2 * TN;
     float *s_sp = s_rC + 2 * TN;                    // [2][CPB]
     float *s_dx = s_sp + 2 * CPB;                   // [T][CPB]
     float *s_dd = s_dx + TC;
     float *s_part = s_dd + TC;                      // [T][warps][2][NP]
+    float *s_zf = s_part + kBwdT * kBwdWarps * 2 * NP;   // GATE: [T][CPB] gy silu'(z)
+    float *s_dz = s_zf + TC;                        // GATE: [T][CPB] dz
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, j = tid % P, c = tid / P;
     const int64_t b = blockIdx.y, k = blockIdx.z;
@@ -452,11 +474,14 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
         g[1] = make_float2(gv.z, gv.w);
         dA[0] = dA[1] = make_float2(0.f, 0.f);
     }
+    const bool has_z = GATE && a.z != nullptr, has_sk = GATE && a.Dskip != nullptr;
+    const float dsk = (has_sk && chain) ? __ldg(a.Dskip + d) : 0.0f;
+    float ddsk = 0.0f;   // dDskip of this chain, summed over the segment (lane j == 0)
 
     // Issues the copies of chunk ci into raw buffer s.
     auto stage = [&](int64_t ci, int sb) {
         const int64_t t0 = ci * kBwdT;
-        float *ru = s_raw + (sb * 3) * TC, *rx = ru + TC, *rg = rx + TC;
+        float *ru = s_raw + (sb * NRAW) * TC, *rx = ru + TC, *rg = rx + TC;
         for (int e = tid; e < TC; e += kBwdThreads) {
             const int i = e / CPB, cc = e % CPB;
             const bool ok = t0 + i < L && d0 + cc < D;
@@ -464,6 +489,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
             cp_async4(ru + e, a.delta + idx, ok);
             cp_async4(rx + e, a.x + idx, ok);
             cp_async4(rg + e, a.gy + idx, ok);
+            if (GATE)
+                cp_async4(rg + TC + e, a.z + (has_z ? idx : 0), ok && has_z);
         }
         for (int e = tid; e < TN; e += kBwdThreads) {
             const int i = e / NP, m = e % NP;
@@ -488,14 +515,20 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
         if (ci > ci0)
             stage(ci - 1, cur ^ 1);
         {
-            const float *ru = s_raw + (cur * 3) * TC, *rx = ru + TC, *rg = rx + TC;
+            const float *ru = s_raw + (cur * NRAW) * TC, *rx = ru + TC, *rg = rx + TC;
             for (int e = tid; e < TC; e += kBwdThreads) {
                 const int i = e / CPB, cc = e % CPB;
                 const bool ok = t0 + i < L && d0 + cc < D;
                 const float u = ru[e];
                 const float dl = !ok ? 0.0f : (a.softplus ? softplus(u) : u);
                 const float sg = (ok && a.softplus) ? bwd_sigmoid(u) : 1.0f;
-                s_in[e] = make_float4(dl, rx[e], rg[e], sg);
+                float gv = rg[e];
+                if (has_z) {   // the scan's share silu(z) of gy; dz's factor gy silu'(z)
+                    const float zv = rg[TC + e], sz = silu_gate(zv);
+                    s_zf[e] = gv * sz * fmaf(zv, 1.0f - sz, 1.0f);
+                    gv *= zv * sz;
+                }
+                s_in[e] = make_float4(dl, rx[e], gv, sg);
             }
         }
         __syncthreads();
@@ -542,16 +575,28 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
                 pB[e] = __fmul2_rn(g[e], u2);
                 g[e] = __fmul2_rn(g[e], ex2v(__fmul2_rn(dl2, A2[e])));  // into h_{t-1}
             }
-            // dx and d delta: the chain's sums over n
-            float sdl = sdl2.x + sdl2.y, sgb = sgb2.x + sgb2.y;
+            // dx and d delta: the chain's sums over n (and, gated, the
+            // scan's read-out s_t for dz)
+            float sdl = sdl2.x + sdl2.y, sgb = sgb2.x + sgb2.y, ys = 0.0f;
+            if constexpr (GATE) {
+                const float2 y2 = __ffma2_rn(Cp[1], hs[i][1], __fmul2_rn(Cp[0], hs[i][0]));
+                ys = y2.x + y2.y;
+            }
 #pragma unroll
             for (int o = 1; o < P; o <<= 1) {
                 sdl += __shfl_xor_sync(0xffffffffu, sdl, o);
                 sgb += __shfl_xor_sync(0xffffffffu, sgb, o);
+                if constexpr (GATE)
+                    ys += __shfl_xor_sync(0xffffffffu, ys, o);
             }
             if (j == 0) {
-                s_dx[i * CPB + c] = sgb * dl;
+                s_dx[i * CPB + c] = GATE ? fmaf(gyv, dsk, sgb * dl) : sgb * dl;
                 s_dd[i * CPB + c] = fmaf(xv, sgb, sdl) * sg;
+                if constexpr (GATE) {
+                    if (has_z)
+                        s_dz[i * CPB + c] = s_zf[i * CPB + c] * fmaf(dsk, xv, ys);
+                    ddsk = fmaf(gyv, xv, ddsk);
+                }
             }
             // dB and dC: sums over the warp's chains
             float v[8] = {pB[0].x, pB[0].y, pB[1].x, pB[1].y, pC[0].x, pC[0].y, pC[1].x, pC[1].y};
@@ -575,6 +620,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
                 const int64_t idx = (b * L + t) * D + dd;
                 a.dx[idx] = s_dx[e];
                 a.ddelta[idx] = s_dd[e];
+                if (has_z)
+                    a.dz[idx] = s_dz[e];
             }
         }
         for (int e = tid; e < kBwdT * 2 * NP; e += kBwdThreads) {
@@ -590,6 +637,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
         }
     }
     if (chain) {
+        if (has_sk && j == 0)
+            atomicAdd(a.dDskip + d, ddsk);
         const float dv[4] = {dA[0].x, dA[0].y, dA[1].x, dA[1].y}, gv[4] = {g[0].x, g[0].y, g[1].x, g[1].y};
 #pragma unroll
         for (int e = 0; e < kBwdS; ++e) {
@@ -641,11 +690,11 @@ inline BwdShape bwd_shape(int64_t Bsz, int64_t L, int64_t D, int64_t N, int resi
 }
 
 // The three launches; bwd_prepare(P) must have run on this device.
-template <int P>
+template <int P, bool GATE>
 inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_t st)
 {
     const dim3 grid((unsigned)s.gx, (unsigned)a.Bsz, (unsigned)s.K);
-    bwd_local_kernel<P><<<grid, kBwdThreads, bwd_local_smem(P), st>>>(a);
+    bwd_local_kernel<P, GATE><<<grid, kBwdThreads, bwd_local_smem(P), st>>>(a);
     const int64_t carry = a.Bsz * a.D * s.NP;
     const unsigned cb = (unsigned)((carry + 255) / 256 < 65536 ? (carry + 255) / 256 : 65536);
     // The carry and main kernels are programmatic dependents of the kernel
@@ -664,48 +713,50 @@ inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_
     if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_carry_kernel, a, s.NP);
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kBwdThreads);
-    cfg.dynamicSmemBytes = bwd_main_smem(P);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<P>, a);
+    cfg.dynamicSmemBytes = bwd_main_smem(P, GATE);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<P, GATE>, a);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
+// GATE kernels when the call has a skip or a gate.
 inline cudaError_t launch_scan_bwd(BwdArgs a, const BwdShape &s, cudaStream_t st)
 {
     a.nch = s.nch;
     a.cps = s.cps;
     a.K = s.K;
+    const bool gate = a.Dskip != nullptr || a.z != nullptr;
     switch (s.P) {
-    case 1: return launch_bwd_p<1>(a, s, st);
-    case 2: return launch_bwd_p<2>(a, s, st);
-    case 4: return launch_bwd_p<4>(a, s, st);
-    default: return launch_bwd_p<8>(a, s, st);
+    case 1: return gate ? launch_bwd_p<1, true>(a, s, st) : launch_bwd_p<1, false>(a, s, st);
+    case 2: return gate ? launch_bwd_p<2, true>(a, s, st) : launch_bwd_p<2, false>(a, s, st);
+    case 4: return gate ? launch_bwd_p<4, true>(a, s, st) : launch_bwd_p<4, false>(a, s, st);
+    default: return gate ? launch_bwd_p<8, true>(a, s, st) : launch_bwd_p<8, false>(a, s, st);
     }
 }
 
 // Sets the kernels' shared-memory limits for threads-per-chain P and returns
 // how many blocks of the main kernel are resident per SM (0 on error).
-template <int P>
+template <int P, bool GATE>
 inline int bwd_prepare_p()
 {
-    if (cudaFuncSetAttribute(bwd_main_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_main_smem(P)) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(bwd_local_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_local_smem(P)) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(bwd_main_kernel<P, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bwd_main_smem(P, GATE)) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_local_kernel<P, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bwd_local_smem(P)) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<P>, kBwdThreads, bwd_main_smem(P)) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<P, GATE>, kBwdThreads,
+                                                      bwd_main_smem(P, GATE)) != cudaSuccess)
         return 0;
     return n;
 }
 
-inline int bwd_prepare(int P)
+inline int bwd_prepare(int P, bool gate)
 {
     switch (P) {
-    case 1: return bwd_prepare_p<1>();
-    case 2: return bwd_prepare_p<2>();
-    case 4: return bwd_prepare_p<4>();
-    default: return bwd_prepare_p<8>();
+    case 1: return gate ? bwd_prepare_p<1, true>() : bwd_prepare_p<1, false>();
+    case 2: return gate ? bwd_prepare_p<2, true>() : bwd_prepare_p<2, false>();
+    case 4: return gate ? bwd_prepare_p<4, true>() : bwd_prepare_p<4, false>();
+    default: return gate ? bwd_prepare_p<8, true>() : bwd_prepare_p<8, false>();
     }
 }
 

@@ -242,6 +242,35 @@ def test_bwd_empty_channel_count_is_ok_without_cuda(lib):
     assert bwd(lib, D=0, A=None, dA=None) == ss.OK
 
 
+def bwd_gated(lib, **kw):
+    a = dict(x=0x10000, delta=0x20000, A=0x30000, B=0x40000, C=0x50000, Dskip=0xD0000, z=0xE0000, h0=None,
+             dy=0x60000, dhT=None, dx=0x70000, ddelta=0x80000, dA=0x90000, dB=0xA0000, dC=0xB0000,
+             dDskip=0xF0000, dz=0x100000, dh0=None, Bsz=1, L=8, D=4, N=16, sp=1)
+    a.update(kw)
+    return lib.selscan_bwd_gated(*(a[k] for k in ("x", "delta", "A", "B", "C", "Dskip", "z", "h0", "dy", "dhT",
+                                                   "dx", "ddelta", "dA", "dB", "dC", "dDskip", "dz", "dh0",
+                                                   "Bsz", "L", "D", "N", "sp")), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dDskip=None), ss.ERR_INVALID_ARG),                  # Dskip without its gradient
+    (dict(Dskip=None), ss.ERR_INVALID_ARG),                   # dDskip without Dskip
+    (dict(dz=None), ss.ERR_INVALID_ARG),                      # z without its gradient
+    (dict(z=None), ss.ERR_INVALID_ARG),                       # dz without z
+    (dict(z=0xE0002), ss.ERR_INVALID_ARG),                    # misaligned
+    (dict(dz=0x70000 + 4), ss.ERR_INVALID_ARG),               # dz overlaps dx
+    (dict(dDskip=0xD0000), ss.ERR_INVALID_ARG),               # dDskip overlaps Dskip
+    (dict(dz=0xE0000 + 16), ss.ERR_INVALID_ARG),              # dz overlaps z
+])
+def test_bwd_gated_argument_errors(lib, kw, code):
+    assert bwd_gated(lib, **kw) == code
+    assert ss.last_error() != ""
+
+
+def test_bwd_gated_empty_channel_count_is_ok_without_cuda(lib):
+    assert bwd_gated(lib, D=0, A=None, dA=None) == ss.OK
+
+
 def ssd(lib, **kw):
     a = dict(x=16, dt=8, A=8, B=16, C=16, y=16, h0=None, hT=None, Bsz=1, L=4, H=2, P=64, N=128, dtype=0,
              softplus=1)

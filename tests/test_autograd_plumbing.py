@@ -13,21 +13,25 @@ from selective_state_space_157_b300 import workloads as W
 
 
 def fake_fwd(orc):
-    def f(x, delta, A, B, C, delta_softplus=False, h0=None, return_final_state=False, **kw):
+    def f(x, delta, A, B, C, delta_softplus=False, h0=None, return_final_state=False, D_skip=None, z=None, **kw):
+        n = lambda t: None if t is None else t.detach().numpy()
         y, hT = orc.selscan_fwd(x.detach().numpy(), delta.detach().numpy(), A.detach().numpy(),
                                 B.detach().numpy(), C.detach().numpy(), delta_softplus,
-                                h0=None if h0 is None else h0.detach().numpy().astype(np.float64))
+                                h0=None if h0 is None else h0.detach().numpy().astype(np.float64),
+                                Dskip=n(D_skip), z=n(z))
         return torch.from_numpy(y), torch.from_numpy(hT)
     return f
 
 
 def fake_bwd(orc):
     def f(x, delta, A, B, C, dy, delta_softplus=False, h0=None, dhT=None, want_dh0=True, stream=None,
-          check=False):
+          check=False, D_skip=None, z=None):
         n = lambda t: None if t is None else t.detach().numpy().astype(np.float64)
+        f32 = lambda t: None if t is None else t.detach().numpy()
         g = orc.selscan_bwd(x.detach().numpy(), delta.detach().numpy(), A.detach().numpy(),
-                            B.detach().numpy(), C.detach().numpy(), n(dy), delta_softplus, h0=n(h0), ghT=n(dhT))
-        out = {k: torch.from_numpy(v) for k, v in g.items()}
+                            B.detach().numpy(), C.detach().numpy(), n(dy), delta_softplus, h0=n(h0), ghT=n(dhT),
+                            Dskip=f32(D_skip), z=f32(z))
+        out = {("dD_skip" if k == "dDskip" else k): torch.from_numpy(v) for k, v in g.items()}
         if not want_dh0:
             del out["dh0"]
         return out
@@ -110,3 +114,38 @@ def test_selective_scan_check_reaches_both_passes(orc, monkeypatch):
     y, hT = ss.selective_scan(x, dl, A, B, C, True, check=True)
     y.sum().backward()
     assert seen == [("fwd", True), ("bwd", True)]
+
+
+@pytest.mark.parametrize("skip,gate", [(True, True), (True, False), (False, True)])
+def test_selective_scan_gated_gradients(orc, monkeypatch, skip, gate):
+    """The block's skip and gate through the wrapper: D_skip and z reach the
+    forward and the backward, and their gradients come back to them."""
+    monkeypatch.setattr(ss, "selscan_fwd", fake_fwd(orc))
+    monkeypatch.setattr(ss, "selscan_bwd", fake_bwd(orc))
+    Bsz, L, D, N = 2, 7, 3, 4
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=31, a_init="loguniform")
+    zz = W.normal(W.rng(32, 1), (Bsz, L, D))
+    dsk = W.normal(W.rng(32, 2), (D,))
+    wy = torch.from_numpy(W.normal(W.rng(32, 3), (Bsz, L, D))).double()
+
+    def leaves(dtype):
+        ts = [torch.tensor(np.asarray(a, np.float64), dtype=dtype, requires_grad=True)
+              for a in (inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), dsk, zz)]
+        return ts
+
+    x, dl, A, B, C, Dk, z = leaves(torch.float32)
+    y, _ = ss.selective_scan(x, dl, A, B, C, True, D_skip=Dk if skip else None, z=z if gate else None)
+    (y * wy).sum().backward()
+
+    rx, rdl, rA, rB, rC, rDk, rz = leaves(torch.float64)
+    ry, _ = unrolled(rx, rdl, rA, rB, rC, None, True)
+    if skip:
+        ry = ry + rDk * rx
+    if gate:
+        ry = ry * torch.nn.functional.silu(rz)
+    (ry * wy).sum().backward()
+    assert torch.allclose(y.double(), ry, rtol=1e-9, atol=1e-12)
+    pairs = [(x, rx), (dl, rdl), (A, rA), (B, rB), (C, rC)] + ([(Dk, rDk)] if skip else []) + \
+        ([(z, rz)] if gate else [])
+    for got, ref in pairs:
+        assert torch.allclose(got.grad.double(), ref.grad, rtol=1e-6, atol=1e-7)

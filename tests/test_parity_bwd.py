@@ -6,7 +6,8 @@ directions), channel counts that leave the last block partly empty, every
 width of a chain (1, 2, 4 and 8 threads of four states: N = 1 to 4, 5 to 8,
 9 to 16, 17 to 32), with and without softplus, h0 and dhT, the empty
 sequence, the 130M-like layer at full size, and autograd through the
-differentiable wrapper."""
+differentiable wrapper; and the block's skip and gate (selscan_bwd_gated,
+against the oracle's gated reverse sweep: dD_skip and dz as well)."""
 import numpy as np
 import pytest
 import torch
@@ -110,4 +111,56 @@ def test_selective_scan_autograd(orc):
     ref = orc.selscan_bwd(inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), wy, True,
                           h0=inp.h0.astype(np.float64), ghT=wh.astype(np.float64))
     for t, k in zip(leaves, NAMES):
+        assert scaled_err(to_np(t.grad), ref[k]) <= TOL[W.F32], k
+
+
+def run_gated(orc, Bsz, L, D, N, seed, skip=True, gate=True, a_init="loguniform", with_h0=True):
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=seed, a_init=a_init, with_h0=with_h0)
+    dy, dhT = W.bwd_grads(Bsz, L, D, N, seed=seed + 1)
+    Dskip, z = W.gate_inputs(Bsz, L, D, seed=seed + 2)
+    x, u, h0 = inp.f32("x"), inp.f32("delta"), inp.h0
+    got = ss.selscan_bwd(to_dev(x), to_dev(u), to_dev(inp.A), to_dev(inp.f32("B")), to_dev(inp.f32("C")),
+                         to_dev(dy), True, h0=to_dev(h0), dhT=to_dev(dhT),
+                         D_skip=to_dev(Dskip) if skip else None, z=to_dev(z) if gate else None)
+    torch.cuda.synchronize()
+    ss.check_device_error()
+    ref = orc.selscan_bwd(x, u, inp.A, inp.f32("B"), inp.f32("C"), dy, True,
+                          h0=None if h0 is None else h0.astype(np.float64), ghT=dhT.astype(np.float64),
+                          Dskip=Dskip if skip else None, z=z if gate else None)
+    names = list(NAMES) + (["dD_skip"] if skip else []) + (["dz"] if gate else [])
+    errs = {k: scaled_err(to_np(got[k]), ref["dDskip" if k == "dD_skip" else k]) for k in names}
+    assert max(errs.values()) <= TOL[W.F32], errs
+
+
+@pytest.mark.parametrize("terms", ["both", "skip", "gate"])
+@pytest.mark.parametrize("shape", [(2, 300, 96, 16), (1, 41, 33, 5), (1, 70, 9, 32), (2, 50, 300, 1)])
+def test_gated_shapes(orc, shape, terms):
+    """Each term alone and both, over chain widths of 1, 2, 4 and 8 threads,
+    ragged chunks and partly empty blocks."""
+    run_gated(orc, *shape, seed=sum(shape) + len(terms), skip=terms != "gate", gate=terms != "skip")
+
+
+def test_gated_mamba130m_layer_full_size(orc):
+    """The 130M-like layer with its skip and gate (Bsz 2, L 2048, D 1536,
+    N 16), every output compared."""
+    w = W.WORKLOADS[6]
+    run_gated(orc, w.Bsz, w.L, w.D, w.N, seed=w.seed, a_init="arange", with_h0=False)
+
+
+def test_gated_selective_scan_autograd(orc):
+    """loss.backward() through the wrapper with D_skip and z reaches the gated
+    CUDA backward; every gradient equals the oracle's."""
+    Bsz, L, D, N = 2, 100, 48, 16
+    inp = W.fwd_inputs(Bsz, L, D, N, seed=41, a_init="loguniform")
+    wy, _ = W.bwd_grads(Bsz, L, D, N, seed=42)
+    Dskip, z = W.gate_inputs(Bsz, L, D, seed=43)
+    leaves = [to_dev(a).requires_grad_() for a in (inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"),
+                                                   inp.f32("C"), Dskip, z)]
+    x, dl, A, B, C, Dk, zz = leaves
+    y, _ = ss.selective_scan(x, dl, A, B, C, True, D_skip=Dk, z=zz)
+    (y * to_dev(wy)).sum().backward()
+    torch.cuda.synchronize()
+    ref = orc.selscan_bwd(inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), wy, True,
+                          Dskip=Dskip, z=z)
+    for t, k in zip(leaves, ("dx", "ddelta", "dA", "dB", "dC", "dDskip", "dz")):
         assert scaled_err(to_np(t.grad), ref[k]) <= TOL[W.F32], k
