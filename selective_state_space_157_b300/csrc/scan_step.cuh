@@ -47,9 +47,15 @@ __device__ __forceinline__ float step_block(const StepArgs &a, float yv, float x
 }
 
 // V 16-byte groups (4V states) per lane, G lanes per chain (N = 4 V G).
+// Launched as a programmatic dependent of the kernel before it on the stream
+// (the previous decode step, typically): it may be scheduled while that one
+// drains, and waits for it to complete before reading anything; it lets the
+// next step be scheduled as soon as all of its own CTAs have started.
 template <int G, int V, bool ZOH>
 __global__ void __launch_bounds__(kStepThreads) step_vec_kernel(const StepArgs a)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t chains = a.Bsz * a.D;
     const int64_t gt = (int64_t)blockIdx.x * kStepThreads + threadIdx.x;
     const int64_t chain_raw = gt / G;

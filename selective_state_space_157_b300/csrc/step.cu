@@ -3,6 +3,26 @@
 #include "launch.h"
 
 namespace selscan {
+namespace {
+
+// A launch that may start while the kernel before it on the stream drains
+// (the kernel waits for it in its first instruction).
+template <typename K>
+cudaError_t launch_dependent(K kernel, unsigned blocks, cudaStream_t st, const StepArgs &a)
+{
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kStepThreads);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+} // namespace
 
 int launch_step_kernel(const StepArgs &a, int G, int V, bool vec, bool zoh, cudaStream_t st)
 {
@@ -11,10 +31,11 @@ int launch_step_kernel(const StepArgs &a, int G, int V, bool vec, bool zoh, cuda
         const int64_t blocks = (chains * G + kStepThreads - 1) / kStepThreads;
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
         const unsigned nb = (unsigned)blocks;
+        cudaError_t le = cudaSuccess;
 #define SELSCAN_STEP_CASE(g, v) \
         if (G == g && V == v) { \
-            if (zoh) step_vec_kernel<g, v, true><<<nb, kStepThreads, 0, st>>>(a); \
-            else step_vec_kernel<g, v, false><<<nb, kStepThreads, 0, st>>>(a); \
+            le = zoh ? launch_dependent(step_vec_kernel<g, v, true>, nb, st, a) \
+                     : launch_dependent(step_vec_kernel<g, v, false>, nb, st, a); \
         }
         SELSCAN_STEP_CASE(1, 1) else SELSCAN_STEP_CASE(2, 1) else SELSCAN_STEP_CASE(4, 1)
         else SELSCAN_STEP_CASE(8, 1) else SELSCAN_STEP_CASE(16, 1)
@@ -23,6 +44,7 @@ int launch_step_kernel(const StepArgs &a, int G, int V, bool vec, bool zoh, cuda
         else SELSCAN_STEP_CASE(4, 4)
         else return fail(SELSCAN_ERR_UNSUPPORTED, "no decode kernel for G=%d V=%d", G, V);
 #undef SELSCAN_STEP_CASE
+        if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
     } else {
         const int64_t blocks = (chains + kStepThreads - 1) / kStepThreads;
         if (blocks > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
