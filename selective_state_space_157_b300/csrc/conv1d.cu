@@ -19,18 +19,29 @@ int launch_conv1d_ring(const ConvArgs &a, int64_t K, cudaStream_t st)
     const int64_t nseg0 = (want + cols * a.Bsz - 1) / (cols * a.Bsz);
     int64_t seg = (a.L + nseg0 - 1) / nseg0;
     if (seg < (a.L + 65534) / 65535) seg = (a.L + 65534) / 65535;
-    const dim3 grid((unsigned)cols, (unsigned)a.Bsz, (unsigned)((a.L + seg - 1) / seg));
+    // A programmatic dependent of the kernel before it on the stream (the
+    // kernel waits for it first thing).
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cols, (unsigned)a.Bsz, (unsigned)((a.L + seg - 1) / seg));
+    cfg.blockDim = dim3(kConvThreads);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     switch (K) {
-    case 1: conv1d_ring_kernel<T, 1><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 2: conv1d_ring_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 3: conv1d_ring_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 4: conv1d_ring_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 5: conv1d_ring_kernel<T, 5><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 6: conv1d_ring_kernel<T, 6><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    case 7: conv1d_ring_kernel<T, 7><<<grid, kConvThreads, 0, st>>>(a, seg); break;
-    default: conv1d_ring_kernel<T, 8><<<grid, kConvThreads, 0, st>>>(a, seg); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 1>, a, seg); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 2>, a, seg); break;
+    case 3: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 3>, a, seg); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 4>, a, seg); break;
+    case 5: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 5>, a, seg); break;
+    case 6: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 6>, a, seg); break;
+    case 7: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 7>, a, seg); break;
+    default: e = cudaLaunchKernelEx(&cfg, conv1d_ring_kernel<T, 8>, a, seg); break;
     }
-    return SELSCAN_OK;
+    return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
 template <typename T>

@@ -187,11 +187,15 @@ template <> struct RingIo<__nv_bfloat16> {
     }
 };
 
+// Launched as a programmatic dependent of the kernel before it: it may be
+// scheduled while that one drains and waits for it before touching memory.
 template <typename T, int K>
 __global__ void __launch_bounds__(kConvThreads) conv1d_ring_kernel(const ConvArgs a, int64_t seg)
 {
     using Slot = typename RingIo<T>::Slot;
     __shared__ Slot ring[kConvRing][kConvThreads];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int64_t d0 = ((int64_t)blockIdx.x * kConvThreads + tid) * 4;
     const int64_t b = blockIdx.y;

@@ -297,6 +297,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
     const int nst = (int)((s1 - s0 + TL - 1) / TL);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
 
+    // Launched as a programmatic dependent of the kernel before it (the
+    // previous call's main kernel, typically, which may still be adding into
+    // the outputs zeroed below): nothing is touched before it has completed.
+    bwd_dep_wait();
     // The main kernel adds dA, dB and dC up atomically: zero them here, over
     // the whole grid.
     {
@@ -694,22 +698,24 @@ template <int P, bool GATE>
 inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_t st)
 {
     const dim3 grid((unsigned)s.gx, (unsigned)a.Bsz, (unsigned)s.K);
-    bwd_local_kernel<P, GATE><<<grid, kBwdThreads, bwd_local_smem(P), st>>>(a);
     const int64_t carry = a.Bsz * a.D * s.NP;
     const unsigned cb = (unsigned)((carry + 255) / 256 < 65536 ? (carry + 255) / 256 : 65536);
-    // The carry and main kernels are programmatic dependents of the kernel
-    // before them (they wait in the kernel); the local kernel launches
-    // normally, after whatever the stream held.
+    // All three kernels are programmatic dependents of the kernel before them
+    // (each waits in the kernel before it touches what that one uses).
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cb);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = bwd_local_smem(P);
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_local_kernel<P, GATE>, a);
+    cfg.gridDim = dim3(cb);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
     if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_carry_kernel, a, s.NP);
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kBwdThreads);

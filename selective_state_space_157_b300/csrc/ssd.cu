@@ -316,6 +316,10 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
     // start the next CTA while this one loads.
     if (warp == 0)
         tmem_alloc(&tbase, COLS);
+    // Launched as a programmatic dependent of the kernel before it (the
+    // previous call's output kernel, typically, whose workspace this call's
+    // may reuse): nothing is read or written before it has completed.
+    grid_dep_wait();
 
     if ((int64_t)blockIdx.y == ngroups) {
         // C B^T of the chunk: C and B rows as K-major operands (over the
@@ -716,13 +720,23 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
     const unsigned groups = (unsigned)((a.H + ssd_state_heads<T, P>() - 1) / ssd_state_heads<T, P>());
-    k1<<<dim3(grid.x, groups + 1, grid.z), kSsdThreads, s1, st>>>(a);   // + the C B^T CTAs
     const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
-    // The carry and output kernels start early (programmatic dependent
-    // launch) and wait in the kernel for what the one before wrote.
+    // All three kernels start early (programmatic dependent launch) and wait
+    // in the kernel for what the one before wrote.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg1 = {};
+        cfg1.gridDim = dim3(grid.x, groups + 1, grid.z);   // + the C B^T CTAs
+        cfg1.blockDim = dim3(kSsdThreads);
+        cfg1.dynamicSmemBytes = s1;
+        cfg1.stream = st;
+        cfg1.attrs = pdl;
+        cfg1.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg1, k1, a);
+        if (e != cudaSuccess) return cuda_fail(e, "SSD state kernel launch");
+    }
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3((unsigned)((total + 255) / 256));
     cfg2.blockDim = dim3(256);
