@@ -640,6 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
             }
         }
     }
+    bwd_dep_trigger();   // the next call's local kernel may be scheduled
     if (chain) {
         if (has_sk && j == 0)
             atomicAdd(a.dDskip + d, ddsk);

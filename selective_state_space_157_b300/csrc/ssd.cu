@@ -625,6 +625,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     }
     const bool ok = mma_wait(&mbar, 0);
     tc_fence_after();
+    grid_dep_trigger();   // the next call's state kernel may be scheduled
     // Row t of each product sits in lane 32w + (t - 16w) of warp w (M = 64).
     const int t = 16 * warp + lane;
     const uint32_t lanes = (uint32_t)(32 * warp) << 16;
