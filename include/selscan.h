@@ -358,7 +358,7 @@ int selscan_conv1d_step(float *conv_state, const float *x, const float *w, const
  * state and the running sum of dl at the start of every 16-step chunk,
  * Bsz * ceil(L / 16) * D * (Np + 1) floats with Np the smallest of 4, 8, 16
  * and 32 that is >= N; and per segment (L is cut into K segments of whole
- * chunks, K at most the number of blocks that fill the GPU once) four
+ * chunks, K at most the number of blocks that fill the GPU once) two
  * Bsz * K * D * Np arrays and one of Bsz * K * D floats.
  * dA, dB and dC are sums formed with atomic additions, so their last bits
  * may differ from run to run; dx, ddelta and dh0 are reproducible.

@@ -37,14 +37,14 @@
 //      chunk start (the checkpoints), the end state and the segment's sum of
 //      dl; in the same pass, what the segment alone sends into the state
 //      before it (the adjoint from zero at its end, summed in closed form).
-//   2. bwd_carry_kernel: per (b, d, n), the true state entering each segment
-//      (h_in(k+1) = exp(A S_k) h_in(k) + hl(k), from h0) and the adjoint
-//      entering each segment from the right (g_out(k-1) = exp(A S_k) g_out(k)
-//      + gl(k), from dLoss/dhT).
-//   3. bwd_main_kernel: per segment, chunks last to first: the chunk's start
-//      state is its local checkpoint plus exp(A S) h_in, its states are
-//      recomputed into registers, and the adjoint runs back through them from
-//      g_out, producing every gradient.
+//   2. bwd_main_kernel: per segment, first the carries: the true state
+//      entering the segment (h_in(k+1) = exp(A S_k) h_in(k) + hl(k), from
+//      h0) and the adjoint entering it from the right (g_out(k-1) =
+//      exp(A S_k) g_out(k) + gl(k), from dLoss/dhT), each thread composing
+//      the pairs of the segments before and after its own; then chunks last
+//      to first: the chunk's start state is its local checkpoint plus
+//      exp(A S) h_in, its states are recomputed into registers, and the
+//      adjoint runs back through them from g_out, producing every gradient.
 // Steps past L are staged as zeros with dl = 0, so they leave h and g as
 // they are and contribute nothing; only their stores are skipped.
 #pragma once
@@ -70,7 +70,6 @@ struct BwdArgs {
     float *spre;               // (Bsz, nch, D) sum of dl from the segment start to the chunk start
     float *hl, *gl;            // (Bsz, K, D, NP) segment end state from zero; adjoint out of the segment from zero
     float *sdl;                // (Bsz, K, D) the segment's sum of dl
-    float *hin, *gout;         // (Bsz, K, D, NP) the composed carries
     int64_t Bsz, L, D, N;
     int64_t nch;               // chunks of kBwdT steps
     int64_t cps;               // chunks per segment
@@ -184,11 +183,11 @@ __device__ __forceinline__ void bwd_put(const BwdArgs &a, const BwdRegs<P, TT> &
 
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
-// Programmatic dependent launch: the carry and main kernels may start while
-// the kernel before them is finishing; they call bwd_dep_wait() before they
-// read anything it wrote (the wait returns once that whole grid has
-// completed and its writes are visible). bwd_dep_trigger() lets the next
-// kernel start early.
+// Programmatic dependent launch: the kernels may start while the kernel
+// before them is finishing; they call bwd_dep_wait() before they touch
+// anything it uses (the wait returns once that whole grid has completed and
+// its writes are visible). bwd_dep_trigger() lets the next kernel start
+// early.
 __device__ __forceinline__ void bwd_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void bwd_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -374,60 +373,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_local_kernel(const BwdArgs
     }
 }
 
+constexpr int kBwdFold = 8;   // segments whose pairs the main kernel loads at once
+
 // ---------------------------------------------------------------- kernel 2
-// One thread per (b, d, n < NP); grid-stride. The segments' values are
-// loaded kCarryBatch at a time ahead of the dependent arithmetic.
-constexpr int kCarryBatch = 8;
-
-__global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a, int NP)
-{
-    bwd_dep_wait();      // the local kernel's pairs
-    bwd_dep_trigger();
-    const int64_t total = a.Bsz * a.D * NP;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int n = (int)(e % NP);
-        const int64_t bd = e / NP, d = bd % a.D, b = bd / a.D;
-        const bool st = n < a.N;
-        const float A2 = st ? __ldg(a.A + d * a.N + n) * kLog2e : 0.0f;
-        const int64_t s_of0 = b * a.K * a.D + d;    // segment k: s_of0 + k * D
-        float h = (st && a.h0) ? __ldg(a.h0 + bd * a.N + n) : 0.0f;
-        for (int k0 = 0; k0 < a.K; k0 += kCarryBatch) {
-            float dec[kCarryBatch], loc[kCarryBatch];
-#pragma unroll
-            for (int q = 0; q < kCarryBatch; ++q) {
-                const int64_t s = s_of0 + (int64_t)(k0 + q) * a.D;
-                dec[q] = k0 + q < a.K ? a.sdl[s] : 0.0f;
-                loc[q] = k0 + q < a.K ? a.hl[s * NP + n] : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < kCarryBatch; ++q) {
-                if (k0 + q < a.K) {
-                    a.hin[(s_of0 + (int64_t)(k0 + q) * a.D) * NP + n] = h;
-                    h = fmaf(ex2(A2 * dec[q]), h, loc[q]);
-                }
-            }
-        }
-        float g = (st && a.ghT) ? __ldg(a.ghT + bd * a.N + n) : 0.0f;
-        for (int k0 = a.K - 1; k0 >= 0; k0 -= kCarryBatch) {
-            float dec[kCarryBatch], loc[kCarryBatch];
-#pragma unroll
-            for (int q = 0; q < kCarryBatch; ++q) {
-                const int64_t s = s_of0 + (int64_t)(k0 - q) * a.D;
-                dec[q] = k0 - q >= 1 ? a.sdl[s] : 0.0f;
-                loc[q] = k0 - q >= 1 ? a.gl[s * NP + n] : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < kCarryBatch; ++q) {
-                if (k0 - q >= 0) {
-                    a.gout[(s_of0 + (int64_t)(k0 - q) * a.D) * NP + n] = g;
-                    g = fmaf(ex2(A2 * dec[q]), g, loc[q]);
-                }
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------- kernel 3
 // grid (ceil(D / CPB), Bsz, K), kBwdThreads threads, bwd_main_smem(P) bytes.
 // dA, dB and dC are accumulated atomically (the local kernel zeroed them).
 // Chunk inputs arrive by cp.async into one of two raw buffers while the
@@ -467,17 +415,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
     }
     const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
     const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
-    bwd_dep_wait();   // the carries (and, through the carry kernel's own wait, the checkpoints)
+    bwd_dep_wait();   // the local kernel's checkpoints and segment pairs
     float2 hin[2], g[2], dA[2];
-    {
-        const float4 hv = chain ? *reinterpret_cast<const float4 *>(a.hin + pair) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 gv = chain ? *reinterpret_cast<const float4 *>(a.gout + pair) : make_float4(0.f, 0.f, 0.f, 0.f);
-        hin[0] = make_float2(hv.x, hv.y);
-        hin[1] = make_float2(hv.z, hv.w);
-        g[0] = make_float2(gv.x, gv.y);
-        g[1] = make_float2(gv.z, gv.w);
-        dA[0] = dA[1] = make_float2(0.f, 0.f);
-    }
+    dA[0] = dA[1] = make_float2(0.f, 0.f);
     const bool has_z = GATE && a.z != nullptr, has_sk = GATE && a.Dskip != nullptr;
     const float dsk = (has_sk && chain) ? __ldg(a.Dskip + d) : 0.0f;
     float ddsk = 0.0f;   // dDskip of this chain, summed over the segment (lane j == 0)
@@ -511,6 +451,66 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
     };
 
     stage(ci1 - 1, (int)((ci1 - 1) & 1));
+    // While the first chunk arrives: the state entering this segment, h0
+    // carried through segments 0 .. k-1 (h_in(k'+1) = exp(A S_k') h_in(k') +
+    // hl(k')), and the adjoint entering it from the right, dLoss/dhT carried
+    // back through segments K-1 .. k+1 (g(k'-1) = exp(A S_k') g(k') + gl(k')):
+    // the associative pairs of booiljung.github.io "3.1 ...", section 3.1.5.2,
+    // composed in both directions. Up to kBwdFold segments' pairs are loaded
+    // before their dependent arithmetic.
+    {
+        float hv[kBwdS], gv[kBwdS];
+#pragma unroll
+        for (int e = 0; e < kBwdS; ++e) {
+            const int64_t n = kBwdS * j + e;
+            const bool st = chain && n < N;
+            hv[e] = (st && a.h0) ? __ldg(a.h0 + (b * D + d) * N + n) : 0.0f;
+            gv[e] = (st && a.ghT) ? __ldg(a.ghT + (b * D + d) * N + n) : 0.0f;
+        }
+        hin[0] = make_float2(hv[0], hv[1]);
+        hin[1] = make_float2(hv[2], hv[3]);
+        g[0] = make_float2(gv[0], gv[1]);
+        g[1] = make_float2(gv[2], gv[3]);
+        const int64_t seg0 = b * a.K * D + d;   // segment kk of this chain: seg0 + kk * D
+        for (int64_t k0 = 0; k0 < k; k0 += kBwdFold) {
+            float dec[kBwdFold];
+            float4 lv[kBwdFold];
+#pragma unroll
+            for (int q = 0; q < kBwdFold; ++q) {
+                const bool ok = chain && k0 + q < k;
+                const int64_t sg = seg0 + (k0 + q) * D;
+                dec[q] = ok ? a.sdl[sg] : 0.0f;
+                lv[q] = ok ? *reinterpret_cast<const float4 *>(a.hl + sg * NP + kBwdS * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kBwdFold; ++q) {
+                if (k0 + q < k) {
+                    const float2 d2 = f2(dec[q]);
+                    hin[0] = __ffma2_rn(ex2v(__fmul2_rn(d2, A2[0])), hin[0], make_float2(lv[q].x, lv[q].y));
+                    hin[1] = __ffma2_rn(ex2v(__fmul2_rn(d2, A2[1])), hin[1], make_float2(lv[q].z, lv[q].w));
+                }
+            }
+        }
+        for (int64_t k0 = a.K - 1; k0 > k; k0 -= kBwdFold) {
+            float dec[kBwdFold];
+            float4 lv[kBwdFold];
+#pragma unroll
+            for (int q = 0; q < kBwdFold; ++q) {
+                const bool ok = chain && k0 - q > k;
+                const int64_t sg = seg0 + (k0 - q) * D;
+                dec[q] = ok ? a.sdl[sg] : 0.0f;
+                lv[q] = ok ? *reinterpret_cast<const float4 *>(a.gl + sg * NP + kBwdS * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kBwdFold; ++q) {
+                if (k0 - q > k) {
+                    const float2 d2 = f2(dec[q]);
+                    g[0] = __ffma2_rn(ex2v(__fmul2_rn(d2, A2[0])), g[0], make_float2(lv[q].x, lv[q].y));
+                    g[1] = __ffma2_rn(ex2v(__fmul2_rn(d2, A2[1])), g[1], make_float2(lv[q].z, lv[q].w));
+                }
+            }
+        }
+    }
     for (int64_t ci = ci1 - 1; ci >= ci0; --ci) {
         const int64_t t0 = ci * kBwdT;
         const int cur = (int)(ci & 1);
@@ -699,9 +699,7 @@ template <int P, bool GATE>
 inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_t st)
 {
     const dim3 grid((unsigned)s.gx, (unsigned)a.Bsz, (unsigned)s.K);
-    const int64_t carry = a.Bsz * a.D * s.NP;
-    const unsigned cb = (unsigned)((carry + 255) / 256 < 65536 ? (carry + 255) / 256 : 65536);
-    // All three kernels are programmatic dependents of the kernel before them
+    // Both kernels are programmatic dependents of the kernel before them
     // (each waits in the kernel before it touches what that one uses).
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -714,12 +712,6 @@ inline cudaError_t launch_bwd_p(const BwdArgs &a, const BwdShape &s, cudaStream_
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_local_kernel<P, GATE>, a);
-    cfg.gridDim = dim3(cb);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_carry_kernel, a, s.NP);
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kBwdThreads);
     cfg.dynamicSmemBytes = bwd_main_smem(P, GATE);
     if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<P, GATE>, a);
     return e == cudaSuccess ? cudaGetLastError() : e;

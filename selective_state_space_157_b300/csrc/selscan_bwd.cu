@@ -96,14 +96,14 @@ extern "C" int selscan_bwd_gated(const float *x, const float *delta, const float
     if (shape.gx > 0x7fffffffLL) return fail(SELSCAN_ERR_UNSUPPORTED, "grid too large");
 
     // Workspace: checkpoints (Bsz, nch, D, NP) and their sums of dl
-    // (Bsz, nch, D); per segment hl, gl, h_in, g_out (Bsz, K, D, NP) and the
-    // sum of dl (Bsz, K, D). Each array starts on a 256-byte boundary.
+    // (Bsz, nch, D); per segment hl, gl (Bsz, K, D, NP) and the sum of dl
+    // (Bsz, K, D). Each array starts on a 256-byte boundary.
     int64_t ck, sp, seg, sdl;
     if (!mul_ok(Bsz * shape.nch, D, shape.NP, &ck) || !mul_ok(Bsz, shape.nch, D, &sp) ||
         !mul_ok(Bsz * shape.K, D, shape.NP, &seg) || !mul_ok(Bsz, shape.K, D, &sdl))
         return fail(SELSCAN_ERR_INVALID_ARG, "backward workspace size overflows");
     auto up = [](int64_t floats) { return ((size_t)floats * 4 + 255) & ~(size_t)255; };
-    const size_t total = up(ck) + up(sp) + 4 * up(seg) + up(sdl);
+    const size_t total = up(ck) + up(sp) + 2 * up(seg) + up(sdl);
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(dev, &pool);
     if (rc != SELSCAN_OK) return rc;
@@ -123,8 +123,6 @@ extern "C" int selscan_bwd_gated(const float *x, const float *delta, const float
     a.spre = reinterpret_cast<float *>(w); w += up(sp);
     a.hl = reinterpret_cast<float *>(w); w += up(seg);
     a.gl = reinterpret_cast<float *>(w); w += up(seg);
-    a.hin = reinterpret_cast<float *>(w); w += up(seg);
-    a.gout = reinterpret_cast<float *>(w); w += up(seg);
     a.sdl = reinterpret_cast<float *>(w);
     a.Bsz = Bsz; a.L = L; a.D = D; a.N = N;
     a.softplus = delta_softplus ? 1 : 0;
