@@ -813,7 +813,7 @@ def run_conv(args, world, rank, local, dev, w, alu=None):
               "launch": f"CUDA graph replay of {per_graph} captured selscan_conv1d calls"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
-                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+                       launches=2 * args.steps, clocks=clk.summary(), dtype="f32")
 
 
 def run_bwd(args, world, rank, local, dev, w, alu=None):
@@ -888,7 +888,7 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     pk["source"] = peak_source(src, alu, sms, max_mhz)
     work = bwd_work_counts(w.Bsz, w.L, w.D, w.N)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
-                    kernel="bwd_local + bwd_carry + bwd_main kernels (3 launches + 3 memsets)")
+                    kernel="bwd_local + bwd_main kernels (2 launches)")
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
@@ -903,7 +903,7 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
               "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
-                       launches=args.steps, clocks=clk.summary(), dtype="f32")
+                       launches=2 * args.steps, clocks=clk.summary(), dtype="f32")
 
 
 def decode_time(w, steps, warmup, world, dev, local, eager=True):
