@@ -61,6 +61,16 @@ def test_shapes(orc, shape, dtype):
     run_case(orc, Bsz, L, H, P, N, dtype, seed=sum(shape) + (dtype == W.BF16), h0=(L % 2 == 1))
 
 
+@pytest.mark.parametrize("shape", [(1, 600, 3, 64, 128), (2, 2100, 2, 32, 64), (1, 8192, 2, 32, 64),
+                                   (1, 8250, 1, 32, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_long_sequences(orc, shape):
+    """Sequences of 10, 33, 128 and 129 chunks: the carry kernel folds each
+    row's chunk states in batches of eight, so these take two to seventeen
+    batches with ragged last ones; with h0, so the carries start from it."""
+    run_case(orc, *shape, W.BF16, seed=sum(shape), h0=True)
+
+
 def test_softplus_off(orc):
     run_case(orc, 1, 300, 2, 64, 128, W.F32, seed=95, h0=True, softplus=False)
 
