@@ -88,7 +88,7 @@ def work_counts(Bsz, L, D, N, elem_bytes, softplus=True, h0=False, hT=False, gat
     return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": mufu, "fp32": fp32}
 
 
-def bwd_work_counts(Bsz, L, D, N):
+def bwd_work_counts(Bsz, L, D, N, gated=False):
     """Algorithmic work of one backward call (fp32, softplus on, no h0/dhT).
 
     bytes: x, delta, dy read and dx, ddelta written (5 * B*L*D fp32), B, C read
@@ -100,11 +100,20 @@ def bwd_work_counts(Bsz, L, D, N):
     forward), 13 for the adjoint step (g += gy*C, gy*h, g*h*a, (.)*A + g*B*x,
     dA += (.)*dl, g*dl*x, g*dl*B, g *= a), and one addition for each of the
     four sums (dx and ddelta over n, dB and dC over d).
+    gated (the block's skip and gate): z read and dz written, Dskip read and
+    dDskip written; per (t, d) sigmoid(z) (exp and reciprocal) and 12 fp32
+    operations (silu, silu', dz, the skip's share of dx and dDskip); per
+    (t, d, n) 2 more for the scan's read-out s_t that dz needs.
     """
     E = Bsz * L * D
     S = Bsz * L * N
     nbytes = 5 * E * 4 + 4 * S * 4 + 2 * D * N * 4
-    return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": E * N + 4 * E, "fp32": 21 * E * N}
+    mufu, fp32 = E * N + 4 * E, 21 * E * N
+    if gated:
+        nbytes += 2 * E * 4 + 2 * D * 4
+        mufu += 2 * E
+        fp32 += 2 * E * N + 12 * E
+    return {"elems": E, "updates": E * N, "bytes": nbytes, "mufu": mufu, "fp32": fp32}
 
 
 def step_work_counts(Bsz, D, N):
@@ -828,6 +837,10 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     dy, _ = W.bwd_grads(w.Bsz, w.L, w.D, w.N, seed=w.seed, with_dhT=False)
     host = {k: inp.f32(k) for k in ("x", "delta", "B", "C")}
     host["dy"] = dy
+    Dsk = None
+    if w.gated:   # the block's skip and gate: z with the inputs, Dskip once
+        Dskip, host["z"] = W.gate_inputs(w.Bsz, w.L, w.D, seed=w.seed)
+        Dsk = torch.from_numpy(Dskip).to(dev)
     foot = sum(a.nbytes for a in host.values())
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(1, -(-(2 * l2) // foot))
@@ -836,7 +849,8 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
 
     def step(i):
         s = sets[i % copies]
-        return ss.selscan_bwd(s["x"], s["delta"], A, s["B"], s["C"], s["dy"], True, want_dh0=False)
+        return ss.selscan_bwd(s["x"], s["delta"], A, s["B"], s["C"], s["dy"], True, want_dh0=False,
+                              D_skip=Dsk, z=s.get("z"))
 
     for i in range(args.warmup):
         step(i)
@@ -861,6 +875,8 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     hin = {k: torch.from_numpy(a).pin_memory() for k, a in host.items()}
     outs = {"dx": (w.Bsz, w.L, w.D), "ddelta": (w.Bsz, w.L, w.D), "dA": (w.D, w.N), "dB": (w.Bsz, w.L, w.N),
             "dC": (w.Bsz, w.L, w.N)}
+    if w.gated:
+        outs.update({"dz": (w.Bsz, w.L, w.D), "dD_skip": (w.D,)})
     hout = {k: torch.empty(shape, dtype=torch.float32, pin_memory=True) for k, shape in outs.items()}
     e2e_steps = max(1, min(args.steps, 10))
     evict_host_caches()
@@ -868,7 +884,8 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         d = {k: t.to(dev, non_blocking=True) for k, t in hin.items()}
-        g = ss.selscan_bwd(d["x"], d["delta"], A, d["B"], d["C"], d["dy"], True, want_dh0=False)
+        g = ss.selscan_bwd(d["x"], d["delta"], A, d["B"], d["C"], d["dy"], True, want_dh0=False,
+                           D_skip=Dsk, z=d.get("z"))
         for k in outs:
             hout[k].copy_(g[k], non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -886,19 +903,21 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pk = peaks(sms, max_mhz, hbm_gbs, alu)
     pk["source"] = peak_source(src, alu, sms, max_mhz)
-    work = bwd_work_counts(w.Bsz, w.L, w.D, w.N)
+    work = bwd_work_counts(w.Bsz, w.L, w.D, w.N, gated=w.gated)
     roof = roofline(work, pk, per_step, traffic=profiled_traffic(args.workload),
                     kernel="bwd_local + bwd_main kernels (2 launches)")
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
         t0 = time.perf_counter()
-        oracle.default().selscan_bwd(host["x"], host["delta"], inp.A, host["B"], host["C"], dy, True)
+        oracle.default().selscan_bwd(host["x"], host["delta"], inp.A, host["B"], host["C"], dy, True,
+                                     **({"Dskip": Dskip, "z": host["z"]} if w.gated else {}))
         secs = time.perf_counter() - t0
         cpu = {"value": elems / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"the whole workload ({elems} elements, {secs:.2f} s, fp64 reverse sweep, one thread)"}
     config = {"workload": f"{w.name}: Bsz={w.Bsz} L={w.L} D={w.D} N={w.N} f32, softplus on, backward "
-                          "(dx, ddelta, dA, dB, dC from dy)",
+                          + ("of the block's gated output (dx, ddelta, dA, dB, dC, dz, dDskip from dy)" if w.gated
+                             else "(dx, ddelta, dA, dB, dC from dy)"),
               "global_batch": w.Bsz * world, "seq_len": w.L, "parallelism": f"replicas x{world}",
               "l2": f"{copies} rotating input sets ({copies * foot / 1e6:.0f} MB) > 2x L2"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
@@ -1252,12 +1271,16 @@ def run_reference_bwd(args, world, w):
     inp = W.workload_inputs(args.workload)
     dy, _ = W.bwd_grads(w.Bsz, w.L, w.D, w.N, seed=w.seed, with_dhT=False)
     a = (inp.f32("x"), inp.f32("delta"), inp.A, inp.f32("B"), inp.f32("C"), dy, True)
+    kw = {}
+    if w.gated:
+        Dskip, z = W.gate_inputs(w.Bsz, w.L, w.D, seed=w.seed)
+        kw = {"Dskip": Dskip, "z": z}
     o = oracle.default()
     for _ in range(args.warmup):
-        o.selscan_bwd(*a)
+        o.selscan_bwd(*a, **kw)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        o.selscan_bwd(*a)
+        o.selscan_bwd(*a, **kw)
     tot = time.perf_counter() - t0
     elems = w.Bsz * w.L * w.D
     value = elems * args.steps / tot
@@ -1310,7 +1333,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=list(range(1, 11)))
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=list(range(1, 12)))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per_config measurements")

@@ -74,6 +74,8 @@ WORKLOADS = {
     8: Workload(8, "mamba130m-conv1d", 2, 2048, 1536, 16, F32, -3.0, "arange", 108, conv_K=4),
     9: Workload(9, "mamba130m-bwd", 2, 2048, 1536, 16, F32, -3.0, "arange", 109, backward=True),
     10: Workload(10, "mamba2-ssd", 1, 1024, 4096, 128, BF16, -3.0, "loguniform", 110, ssd_heads=64),
+    11: Workload(11, "mamba130m-bwd-gated", 2, 2048, 1536, 16, F32, -3.0, "arange", 111, gated=True,
+                 backward=True),
 }
 
 
