@@ -535,6 +535,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
     float *dl = reinterpret_cast<float *>(GA + Q * Q);
     float *s = dl + Q;
     float *es = s + Q;
+    float *wr = es + Q;   // exp(-s_r) dl_r
     __shared__ uint32_t tbase;
     __shared__ __align__(8) uint64_t mbar;
 
@@ -565,10 +566,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
         ssd_decays_from(a, dtv, rows, dl, s);
     ssd_cp_wait();
     __syncthreads();
-    if (tid < Q)
+    if (tid < Q) {
         es[tid] = ex2(s[tid] * kLog2e);
+        wr[tid] = ex2(-s[tid] * kLog2e) * dl[tid];
+    }
     transpose_to_operand<T, Q, P>(rX, nullptr, BX);
-    __syncthreads();   // the X tile is consumed
+    // The X tile is consumed. exp(s_t - s_r) = exp(s_t) exp(-s_r) when no
+    // |s| exceeds 80 (both factors then stay inside fp32's normal range);
+    // otherwise each term takes its own exponential.
+    const bool wide = __syncthreads_or(tid < Q && !(fabsf(s[tid]) <= 80.0f));
     // Every CTA waits for the carry kernel, also when it reads nothing of it,
     // so that this grid never completes before that one.
     grid_dep_wait();
@@ -585,14 +591,24 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_kernel(const SsdArgs a)
         uint4 *cell = reinterpret_cast<uint4 *>(GA + core_index(t, r0, Q));
         const uint4 graw = *cell;
         const __half2 *g2 = reinterpret_cast<const __half2 *>(&graw);
-        const float st = s[t];
+        const float st = s[t], et = es[t];
         float m[8];
+        if (!wide) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 gf = __half22float2(g2[i]);
-            const int r = r0 + 2 * i;
-            m[2 * i] = r <= t ? gf.x * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
-            m[2 * i + 1] = r + 1 <= t ? gf.y * ex2((st - s[r + 1]) * kLog2e) * dl[r + 1] : 0.0f;
+            for (int i = 0; i < 4; ++i) {
+                const float2 gf = __half22float2(g2[i]);
+                const int r = r0 + 2 * i;
+                m[2 * i] = r <= t ? gf.x * et * wr[r] : 0.0f;
+                m[2 * i + 1] = r + 1 <= t ? gf.y * et * wr[r + 1] : 0.0f;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 gf = __half22float2(g2[i]);
+                const int r = r0 + 2 * i;
+                m[2 * i] = r <= t ? gf.x * ex2((st - s[r]) * kLog2e) * dl[r] : 0.0f;
+                m[2 * i + 1] = r + 1 <= t ? gf.y * ex2((st - s[r + 1]) * kLog2e) * dl[r + 1] : 0.0f;
+            }
         }
         *cell = pack8(m);
     }
@@ -690,7 +706,7 @@ template <typename T, int N, int P>
 constexpr size_t ssd_out_smem()
 {
     return (size_t)ssd_out_region1<T, N, P>() + ((size_t)kSsdQ * N + (size_t)P * kSsdQ + (size_t)kSsdQ * kSsdQ) * 2 +
-           3 * kSsdQ * 4;
+           4 * kSsdQ * 4;
 }
 
 // Shared memory that keeps at most max_ctas CTAs of a kernel on one SM, so
