@@ -414,7 +414,6 @@ __global__ void __launch_bounds__(kBwdThreads, 4) bwd_main_kernel(const BwdArgs 
         A2[e] = __fmul2_rn(An[e], f2(kLog2e));
     }
     const int64_t ci0 = k * a.cps, ci1 = min(ci0 + a.cps, nch);
-    const int64_t pair = ((b * a.K + k) * D + d) * NP + kBwdS * j;
     bwd_dep_wait();   // the local kernel's checkpoints and segment pairs
     float2 hin[2], g[2], dA[2];
     dA[0] = dA[1] = make_float2(0.f, 0.f);

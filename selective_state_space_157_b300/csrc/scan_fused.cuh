@@ -469,7 +469,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                 const unsigned char *p = buf(r);
                 const T *xs = reinterpret_cast<const T *>(p) + xcol;
                 const T *ds = reinterpret_cast<const T *>(p + xbytes) + xcol;
-                const T *zs = reinterpret_cast<const T *>(p + 2 * xbytes + 2 * nbytes) + xcol;
+                [[maybe_unused]] const T *zs = reinterpret_cast<const T *>(p + 2 * xbytes + 2 * nbytes) + xcol;
                 const float *Bs;
                 const float *Cs;
                 if (!stage_rows(p, s, r, 0, 2, &Bs, &Cs, true)) {
@@ -557,7 +557,7 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
                     SmemStateLoad<float, NS, VEC>::run(Bs + tt * Nrow, valid, Bv);
                     const float2 dl2 = make_float2(dlv[tt], dlv[tt]);
                     const float2 u2 = make_float2(uv[tt], uv[tt]);
-                    const float xt = ZOH ? smem_val(xs + tt * W) : 0.0f;
+                    [[maybe_unused]] const float xt = ZOH ? smem_val(xs + tt * W) : 0.0f;
                     float Cv[NS];
                     SmemStateLoad<float, NS, VEC>::run(Cs + tt * Nrow, valid, Cv);
                     float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
