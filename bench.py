@@ -574,6 +574,23 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def host_like(t):
+    """A copy of host tensor ``t`` in page-locked memory from the library's
+    host allocator (``selscan_host_alloc``), whose buffers the DMA engines
+    read at the link's rate."""
+    import selective_state_space_157_b300 as ss
+    h = ss.host_empty(tuple(t.shape), t.dtype)
+    h.copy_(t)
+    return h
+
+
+def host_zeros(shape, dtype=None):
+    import selective_state_space_157_b300 as ss
+    h = ss.host_empty(shape, dtype)
+    h.zero_()
+    return h
+
+
 def evict_host_caches(nbytes=512 << 20):
     """Writes and reads a host buffer larger than the CPU's caches, so that
     host inputs written shortly before sit in DRAM, as inputs a loader wrote
@@ -586,14 +603,16 @@ def evict_host_caches(nbytes=512 << 20):
 
 
 def pcie_rates(dev, nbytes=256 << 20, reps=4):
-    """Copy rates between pinned host memory and this GPU (GB/s), timed with
-    CUDA events: host to device, device to host, and both directions at once
-    on two streams (their sum; the link does not carry both directions at
-    their one-way rates together). The bound the end-to-end leg's copies can
-    approach."""
+    """Copy rates between page-locked host memory (the library's host
+    allocator, written and then evicted from the CPU caches, as the end-to-end
+    legs' buffers are) and this GPU (GB/s), timed with CUDA events: host to
+    device, device to host, and both directions at once on two streams (their
+    sum; the link does not carry both directions at their one-way rates
+    together). The bound the end-to-end leg's copies can approach."""
     import torch
-    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h = host_zeros((nbytes,), torch.uint8)
+    h2 = host_zeros((nbytes,), torch.uint8)
+    evict_host_caches()
     d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     st, st2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -638,15 +657,15 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
             torch.from_numpy(inp.A),
             torch.from_numpy(inp.B.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.B),
             torch.from_numpy(inp.C.view("int16")).view(torch.bfloat16) if bf16 else torch.from_numpy(inp.C)]
-    y_host = torch.empty(tuple(inp.x.shape), dtype=torch.bfloat16 if bf16 else torch.float32, pin_memory=True)
-    hT_host = torch.empty(inp.x.shape[0], inp.x.shape[2], inp.A.shape[1], pin_memory=True) \
+    y_host = host_zeros(tuple(inp.x.shape), torch.bfloat16 if bf16 else torch.float32)
+    hT_host = host_zeros((inp.x.shape[0], inp.x.shape[2], inp.A.shape[1])) \
         if w.return_state else None
     e2e_steps = max(1, min(args.steps, 20 if elems < 50_000_000 else 5))
     kw = {}
     if w.gated:
         # The block's skip and gate: Dskip and z from host memory as well.
         host += [torch.from_numpy(gate[1]), torch.from_numpy(gate[0])]
-    host = [t.pin_memory() for t in host]
+    host = [host_like(t) for t in host]
     if w.gated:
         kw = {"z": host[5], "D_skip": host[6]}
     if w.zoh:
@@ -672,8 +691,9 @@ def fwd_e2e(args, world, dev, w, inp, gate, bf16, elems):
             "ms_per_step": per_step * 1e3,
             "pcie": {"h2d_gbs": rates[0], "d2h_gbs": rates[1], "both_ways_gbs": rates[2],
                      "copy_bound_ms": bound * 1e3, "frac_of_copy_bound": bound / per_step,
-                     "note": "rates of 256 MB pinned copies measured in this run (one way each, and both "
-                             "ways at once); host inputs evicted from the CPU caches before the timed calls"}}
+                     "note": "rates of 256 MB page-locked copies measured in this run (one way each, and both "
+                             "ways at once); host buffers from selscan_host_alloc, inputs evicted from the CPU "
+                             "caches before the timed calls"}}
 
 
 def measure_config(wid, args, world, local, dev, alu):
@@ -781,8 +801,8 @@ def run_conv(args, world, rank, local, dev, w, alu=None):
     elems = w.Bsz * w.L * w.D
     value = world * elems * args.steps / sec
 
-    hx = torch.from_numpy(x).pin_memory()
-    hy = torch.empty(hx.shape, dtype=hx.dtype, pin_memory=True)
+    hx = host_like(torch.from_numpy(x))
+    hy = host_zeros(tuple(hx.shape), hx.dtype)
     e2e_steps = max(1, min(args.steps, 20))
     evict_host_caches()
     barrier(world, dev)
@@ -872,12 +892,12 @@ def run_bwd(args, world, rank, local, dev, w, alu=None):
     elems = w.Bsz * w.L * w.D
     value = world * elems * args.steps / sec
 
-    hin = {k: torch.from_numpy(a).pin_memory() for k, a in host.items()}
+    hin = {k: host_like(torch.from_numpy(a)) for k, a in host.items()}
     outs = {"dx": (w.Bsz, w.L, w.D), "ddelta": (w.Bsz, w.L, w.D), "dA": (w.D, w.N), "dB": (w.Bsz, w.L, w.N),
             "dC": (w.Bsz, w.L, w.N)}
     if w.gated:
         outs.update({"dz": (w.Bsz, w.L, w.D), "dD_skip": (w.D,)})
-    hout = {k: torch.empty(shape, dtype=torch.float32, pin_memory=True) for k, shape in outs.items()}
+    hout = {k: host_zeros(shape) for k, shape in outs.items()}
     e2e_steps = max(1, min(args.steps, 10))
     evict_host_caches()
     barrier(world, dev)
@@ -1002,8 +1022,8 @@ def run_decode(args, world, rank, local, dev, w, alu=None):
     value = world * elems / per_step
 
     # end to end: host inputs of the step in, y out, state kept on the device
-    hx = [torch.from_numpy(a).pin_memory() for a in W.decode_step_inputs(w, 0)]
-    hy = torch.empty(w.Bsz, w.D, pin_memory=True)
+    hx = [host_like(torch.from_numpy(a)) for a in W.decode_step_inputs(w, 0)]
+    hy = host_zeros((w.Bsz, w.D))
     e2e_steps = max(1, min(args.steps, 50))
     evict_host_caches()
     barrier(world, dev)
@@ -1098,9 +1118,9 @@ def run_ssd(args, world, rank, local, dev, w):
     elems = Bsz * L * H * P
     value = world * elems * args.steps / sec
 
-    host = [torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(d).pin_memory()
+    host = [host_like(torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(d))
             for a, d in ((x, tdt), (dt, torch.float32), (A, torch.float32), (B, tdt), (C, tdt))]
-    hy = torch.empty(tuple(x.shape), dtype=tdt, pin_memory=True)
+    hy = host_zeros(tuple(x.shape), tdt)
     e2e_steps = max(1, min(args.steps, 20))
     evict_host_caches()
     barrier(world, dev)

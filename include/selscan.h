@@ -51,6 +51,7 @@
 #ifndef SELSCAN_H
 #define SELSCAN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -455,6 +456,18 @@ int selscan_check_device_error(void *stream);
  * restores normal operation. Off by default; nothing in the environment can
  * turn it on. SELSCAN_ERR_INVALID_ARG for arguments out of range. */
 int selscan_test_fault_injection(int withhold_carries, int wait_limit_ms);
+
+/* Page-locked host memory for the host-buffer entry points: `bytes` rounded
+ * up to 2 MB, 2 MB aligned, from an anonymous mapping (transparent huge
+ * pages requested) registered with the CUDA driver for every device. On
+ * the B300 hosts measured, copies from such buffers ran at 52-55 GB/s,
+ * while buffers from cudaHostAlloc ran anywhere from 11 to 55 GB/s (and any
+ * pinned buffer whose lines were still dirty in the CPU cache at 15-17
+ * GB/s). Returns NULL on failure (selscan_last_error says why). Free with
+ * selscan_host_free, which returns SELSCAN_ERR_INVALID_ARG for a pointer
+ * this call did not return; NULL is ignored. Thread-safe. */
+void *selscan_host_alloc(size_t bytes);
+int selscan_host_free(void *ptr);
 
 /* Returns the memory held by the chunk-carry workspace pools of every
  * device this process used to the device. Safe to call at any time; work

@@ -22,7 +22,7 @@ import os
 
 __all__ = ["selscan_fwd", "selscan_bwd", "selective_scan", "selscan_fwd_noalloc", "selscan_step", "conv1d", "conv1d_step",
            "ssd_fwd", "fwd_plan", "last_error", "check_device_error",
-           "release_workspace", "version", "library_path", "SelscanError",
+           "release_workspace", "version", "library_path", "SelscanError", "host_empty",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_NO_MEMORY", "ERR_TIMEOUT",
            "MAX_N", "FLAG_SOFTPLUS", "FLAG_ZOH"]
 
@@ -95,6 +95,10 @@ def lib() -> ctypes.CDLL:
         L.selscan_test_fault_injection.argtypes = [INT, INT]
         L.selscan_bwd.restype = INT
         L.selscan_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, INT, P]
+        L.selscan_host_alloc.restype = P
+        L.selscan_host_alloc.argtypes = [ctypes.c_size_t]
+        L.selscan_host_free.restype = INT
+        L.selscan_host_free.argtypes = [P]
         L.selscan_bwd_gated.restype = INT
         L.selscan_bwd_gated.argtypes = [P] * 18 + [I64, I64, I64, I64, INT, P]
         _lib = L
@@ -119,6 +123,27 @@ def fwd_plan(Bsz: int, L: int, D: int, N: int, bf16: bool = False) -> dict:
     _check(lib().selscan_fwd_plan(Bsz, L, D, N, BF16 if bf16 else F32, ctypes.byref(k),
                                   ctypes.byref(t), ctypes.byref(n), ctypes.byref(w)))
     return {"chunks": k.value, "chunk_len": t.value, "launches": n.value, "workspace_bytes": w.value}
+
+
+def host_empty(shape, dtype=None):
+    """An uninitialised host tensor in page-locked memory from
+    ``selscan_host_alloc`` (see ``include/selscan.h``): the DMA engines read
+    and write it at the link's full rate. The memory is given back with
+    ``selscan_host_free`` when the tensor is no longer referenced."""
+    import math
+    import weakref
+    import torch
+    dtype = torch.float32 if dtype is None else dtype
+    shape = tuple(int(v) for v in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    nbytes = max(1, math.prod(shape) * torch.empty((), dtype=dtype).element_size())
+    ptr = lib().selscan_host_alloc(nbytes)
+    if not ptr:
+        raise SelscanError(ERR_NO_MEMORY, last_error())
+    buf = (ctypes.c_uint8 * nbytes).from_address(ptr)
+    weakref.finalize(buf, lib().selscan_host_free, ptr)
+    n = math.prod(shape)
+    return torch.frombuffer(buf, dtype=torch.uint8)[:n * torch.empty((), dtype=dtype).element_size()] \
+        .view(dtype).view(shape)
 
 
 def release_workspace() -> None:

@@ -271,6 +271,15 @@ def test_bwd_gated_empty_channel_count_is_ok_without_cuda(lib):
     assert bwd_gated(lib, D=0, A=None, dA=None) == ss.OK
 
 
+def test_host_alloc_checks_its_arguments(lib):
+    """The host allocator refuses an empty request and frees only its own
+    blocks (no CUDA call is reached on these paths)."""
+    assert lib.selscan_host_alloc(0) is None
+    assert ss.last_error() != ""
+    assert lib.selscan_host_free(ctypes.c_void_p(0x123000)) == ss.ERR_INVALID_ARG
+    assert lib.selscan_host_free(None) == ss.OK
+
+
 def ssd(lib, **kw):
     a = dict(x=16, dt=8, A=8, B=16, C=16, y=16, h0=None, hT=None, Bsz=1, L=4, H=2, P=64, N=128, dtype=0,
              softplus=1)

@@ -104,3 +104,25 @@ def test_gated_and_zoh_from_host(orc, monkeypatch, form):
                              zoh=zoh)
     assert scaled_err(as_np(y), yr) <= TOL[W.F32]
     assert scaled_err(as_np(hT), hr) <= TOL[W.F32]
+
+
+def test_host_empty_round_trip_and_forward(orc):
+    """Tensors from the library's page-locked host allocator: asynchronous
+    copies both ways keep every byte, and the host-buffer forward reads and
+    writes them like any pinned buffer."""
+    t = ss.host_empty((257, 33))
+    src = torch.randn(257, 33)
+    t.copy_(src)
+    d = t.to("cuda", non_blocking=True)
+    back = ss.host_empty((257, 33))
+    back.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    inp = W.fwd_inputs(2, 300, 64, 16, seed=71)
+    host = [ss.host_empty(a.shape) for a in (inp.x, inp.delta, inp.A, inp.B, inp.C)]
+    for h, a in zip(host, (inp.x, inp.delta, inp.A, inp.B, inp.C)):
+        h.copy_(torch.from_numpy(a))
+    y = ss.host_empty(inp.x.shape)
+    ss.selscan_fwd(*host, True, y=y)
+    yr, _ = orc.selscan_fwd(inp.x, inp.delta, inp.A, inp.B, inp.C, True)
+    assert scaled_err(y.numpy(), yr) <= TOL[W.F32]
