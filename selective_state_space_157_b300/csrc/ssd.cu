@@ -448,49 +448,55 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_state_kernel(const SsdArgs a)
 
 // 2. The state entering each chunk, in chunk order: fp32 carries, stored as
 // fp16 in the output kernel's operand order (P rows, K = N, core-matrix
-// order), and hT ([n][p], fp32). A thread owns eight consecutive n of one p
-// (one 16-byte core row); consecutive threads take consecutive core rows of
-// the operand, so a warp's stores are 512 contiguous bytes (and its loads of
-// the [p][n] chunk states 64-byte runs). The chunk states are loaded
+// order), and hT ([n][p], fp32). A thread owns four consecutive n of one p
+// (half a 16-byte core row); consecutive threads take consecutive half rows
+// of the operand, so a warp's stores are 256 contiguous bytes (and its loads
+// of the [p][n] chunk states 32-byte runs). The chunk states are loaded
 // kCarryBatch chunks ahead of the serial fold.
 constexpr int kCarryBatch = 8;
+constexpr int kCarryE = 4;   // n per thread
 
 template <int N, int P>
 __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
 {
-    constexpr int NP = N * P;
+    constexpr int NP = N * P, E = kCarryE;
     grid_dep_wait();      // the chunk states and decays of the state kernel
     grid_dep_trigger();   // the output kernel may start its own loads
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    if (i >= a.Bsz * a.H * (NP / 8))
+    if (i >= a.Bsz * a.H * (NP / E))
         return;
-    const int64_t bh = i / (NP / 8);
-    const int r = (int)(i - bh * (NP / 8));            // core row r of the operand
-    const int p = ((r >> 3) / (N / 8)) * 8 + (r & 7), n0 = ((r >> 3) % (N / 8)) * 8;
+    const int64_t bh = i / (NP / E);
+    const int hr = (int)(i - bh * (NP / E));           // half row hr of the operand
+    const int r = hr >> 1, q0 = (hr & 1) * E;          // core row r, its n offset
+    const int p = ((r >> 3) / (N / 8)) * 8 + (r & 7), n0 = ((r >> 3) % (N / 8)) * 8 + q0;
     const int pn = p * N + n0;
-    float carry[8];
+    float carry[E];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < E; ++q)
         carry[q] = a.h0 ? __ldg(a.h0 + bh * NP + (int64_t)(n0 + q) * P + p) : 0.0f;
     const __half *Sp = a.S + bh * a.nch * NP + pn;
-    __half *Hp = a.Hin + bh * a.nch * NP + (int64_t)r * 8;   // = core_index(p, n0, N)
+    __half *Hp = a.Hin + bh * a.nch * NP + (int64_t)r * 8 + q0;   // = core_index(p, n0, N)
     const float *dp = a.dec + bh * a.nch;
     for (int c0 = 0; c0 < a.nch; c0 += kCarryBatch) {
-        uint4 sv[kCarryBatch];
+        uint2 sv[kCarryBatch];
         float dv[kCarryBatch];
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             const int cc = c0 + j < a.nch ? c0 + j : a.nch - 1;
-            sv[j] = __ldcg(reinterpret_cast<const uint4 *>(Sp + (int64_t)cc * NP));
+            sv[j] = __ldcg(reinterpret_cast<const uint2 *>(Sp + (int64_t)cc * NP));
             dv[j] = __ldg(dp + cc);
         }
 #pragma unroll
         for (int j = 0; j < kCarryBatch; ++j) {
             if (c0 + j < a.nch) {
-                *reinterpret_cast<uint4 *>(Hp + (int64_t)(c0 + j) * NP) = pack8(carry);
+                uint2 o;
+                __half2 *oh = reinterpret_cast<__half2 *>(&o);
+                oh[0] = __floats2half2_rn(carry[0], carry[1]);
+                oh[1] = __floats2half2_rn(carry[2], carry[3]);
+                *reinterpret_cast<uint2 *>(Hp + (int64_t)(c0 + j) * NP) = o;
                 const __half2 *hs = reinterpret_cast<const __half2 *>(&sv[j]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     const float2 f = __half22float2(hs[q]);
                     carry[2 * q] = fmaf(dv[j], carry[2 * q], f.x);
                     carry[2 * q + 1] = fmaf(dv[j], carry[2 * q + 1], f.y);
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(256) ssd_carry_kernel(const SsdArgs a)
     }
     if (a.hT) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < E; ++q)
             a.hT[bh * NP + (int64_t)(n0 + q) * P + p] = carry[q];
     }
 }
@@ -737,7 +743,7 @@ int launch_ssd_t(const SsdArgs &a, cudaStream_t st)
     if (e != cudaSuccess) return cuda_fail(e, "SSD kernel attributes");
     const dim3 grid((unsigned)a.nch, (unsigned)a.H, (unsigned)a.Bsz);
     const unsigned groups = (unsigned)((a.H + ssd_state_heads<T, P>() - 1) / ssd_state_heads<T, P>());
-    const int64_t total = a.Bsz * a.H * (int64_t)(N * P / 8);
+    const int64_t total = a.Bsz * a.H * (int64_t)(N * P / kCarryE);
     // All three kernels start early (programmatic dependent launch) and wait
     // in the kernel for what the one before wrote.
     cudaLaunchAttribute pdl[1];
