@@ -121,3 +121,18 @@ def test_conv1d_rejects_in_place_and_bad_K():
     with pytest.raises(ss.SelscanError) as e:
         ss.conv1d(x, torch.randn(16, 9, device="cuda"))
     assert e.value.code == ss.ERR_UNSUPPORTED
+
+
+def test_back_to_back_calls_see_each_others_outputs(orc):
+    """The streaming kernel starts early and waits for the kernel before it:
+    a second convolution over the first one's output, launched right after
+    it, reads the finished output."""
+    Bsz, L, D, K = 2, 3000, 1032, 4
+    x, w, bias, _ = W.conv_inputs(Bsz, L, D, K, seed=81)
+    o1 = ss.conv1d(to_dev(x), to_dev(w), to_dev(bias))
+    o2 = ss.conv1d(o1, to_dev(w), to_dev(bias))
+    torch.cuda.synchronize()
+    r1, _ = orc.conv1d(x, w, bias)
+    r2, _ = orc.conv1d(to_np(o1).astype(np.float32), w, bias)
+    assert scaled_err(to_np(o1), r1) <= TOL[W.F32]
+    assert scaled_err(to_np(o2), r2) <= TOL[W.F32]

@@ -148,3 +148,17 @@ def test_zero_decay_heads_and_mixed_steps(orc):
     dt = g.choice(np.array([0.0, 1e-3, 0.05, 1.0, 20.0], np.float32), size=(1, 512, 3))
     _run_edge(orc, dt.astype(np.float32), np.array([0.0, -2.0, 0.0], np.float32), seed=103, softplus=False,
               cancelling=True, L=512)
+
+
+def test_back_to_back_calls_see_each_others_outputs(orc):
+    """Two calls on one stream, the second reading the first's y as its x
+    (its kernels start early and wait for the kernel before them)."""
+    Bsz, L, H, P, N = 1, 200, 3, 64, 128
+    x, dt, A, B, C, _ = W.ssd_inputs(Bsz, L, H, P, N, seed=61)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    y1 = ss.ssd_fwd(dev(x), dev(dt), dev(A), dev(B), dev(C), True)
+    y2 = ss.ssd_fwd(y1, dev(dt), dev(A), dev(B), dev(C), True)
+    torch.cuda.synchronize()
+    ss.check_device_error()
+    r2, _ = orc.ssd_fwd(to_np(y1).astype(np.float32), dt, A, B, C, True)
+    assert scaled_err(to_np(y2), r2) <= TOL
