@@ -233,6 +233,12 @@ scan_fused_kernel(const __grid_constant__ FusedArgs fa)
 {
     static_assert(NS % 4 == 0, "states are processed in pairs of pairs");
     static_assert(TT % 2 == 0, "timesteps are processed in pairs");
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: the CTAs may be resident early, and touch nothing before that
+    // kernel has completed; the next kernel may be scheduled once every CTA
+    // of this one has started.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int DPB = THREADS / NSPLIT;
     // x, delta and z tiles arrive as NB boxes of W channels each (a TMA box
     // spans at most 256 elements), stored [NB][TT][W].

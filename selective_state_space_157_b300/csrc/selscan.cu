@@ -370,7 +370,17 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         fa.nslices = (int)((dpb * a.N + fl.threads - 1) / fl.threads);
     }
     void *args[] = {&fa};
-    cudaError_t e = cudaLaunchKernel(fl.kernel, dim3((unsigned)grid), dim3(fl.threads), args, fl.smem, st);
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(fl.threads);
+    cfg.dynamicSmemBytes = fl.smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fl.kernel, args);
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
