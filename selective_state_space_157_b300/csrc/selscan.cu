@@ -295,6 +295,32 @@ size_t fwd_workspace_bytes(const FwdPlan &plan, int64_t Bsz, int64_t L, int64_t 
     return fwd_workspace_layout(plan, Bsz, L, D, N, dtype).total;
 }
 
+// Clears a chunked call's control words, as a programmatic dependent of the
+// kernel before it (the previous call, which may still use words at the
+// same addresses), so that the fused kernel after it can be one too.
+__global__ void __launch_bounds__(256) clear_ctrl_kernel(unsigned *w, int n)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256)
+        w[i] = 0u;
+}
+
+cudaError_t launch_dependent(const void *kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void **args)
+{
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
 // TMA path: one persistent kernel (local scans, carry composition and
 // corrections together).
 // Returns SELSCAN_ERR_UNSUPPORTED when TMA cannot be set up (the caller then
@@ -357,7 +383,11 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         fa.ctrl = reinterpret_cast<unsigned *>(reinterpret_cast<unsigned char *>(ws) + w.pairs);
         if (w.res)
             fa.yres = reinterpret_cast<unsigned char *>(ws) + w.pairs + ((w.flags + 255) & ~(size_t)255);
-        cudaError_t e = cudaMemsetAsync(fa.ctrl, 0, w.flags, st);
+        unsigned *ctrl = fa.ctrl;
+        int nwords = (int)(w.flags / sizeof(unsigned));
+        void *cargs[] = {&ctrl, &nwords};
+        const unsigned cblocks = (unsigned)((nwords + 255) / 256 < 148 ? (nwords + 255) / 256 : 148);
+        cudaError_t e = launch_dependent((const void *)clear_ctrl_kernel, dim3(cblocks), dim3(256), 0, st, cargs);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the chunk flags");
         const int64_t resident = (int64_t)sms * fl.ctas_per_sm;
         if (grid > resident) grid = resident;
@@ -370,17 +400,7 @@ int launch_fused(const ScanArgs &a, const FwdPlan &plan, int dtype, int sms, flo
         fa.nslices = (int)((dpb * a.N + fl.threads - 1) / fl.threads);
     }
     void *args[] = {&fa};
-    cudaLaunchAttribute pdl[1];
-    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(fl.threads);
-    cfg.dynamicSmemBytes = fl.smem;
-    cfg.stream = st;
-    cfg.attrs = pdl;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fl.kernel, args);
+    cudaError_t e = launch_dependent(fl.kernel, dim3((unsigned)grid), dim3(fl.threads), fl.smem, st, args);
     return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e, "kernel launch");
 }
 
