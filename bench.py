@@ -842,7 +842,7 @@ def run_conv(args, world, rank, local, dev, w, alu=None):
               "launch": f"CUDA graph replay of {per_graph} captured selscan_conv1d calls"}
     return result_line(value=value, n_gpus=world, steps=args.steps, warmup=args.warmup,
                        ms_per_step=per_step * 1e3, config=config, roof=roof, cpu=cpu, e2e=e2e,
-                       launches=2 * args.steps, clocks=clk.summary(), dtype="f32")
+                       launches=args.steps, clocks=clk.summary(), dtype="f32")
 
 
 def run_bwd(args, world, rank, local, dev, w, alu=None):

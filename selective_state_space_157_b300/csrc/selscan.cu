@@ -1053,7 +1053,9 @@ extern "C" int selscan_fwd_plan(int64_t Bsz, int64_t L, int64_t D, int64_t N, in
     if (chunk_len) *chunk_len = empty ? 0 : plan.chunk;
     // The TMA path runs as one kernel (plus a flag reset when chunked); the
     // plain path as aggregate + carry + readout kernels.
-    if (launches) *launches = empty ? 0 : (plan.tma ? 1 : (plan.K > 1 ? 3 : 1));
+    // TMA path: the fused kernel, after the kernel that clears the control
+    // words of a chunked plan; plain path: aggregate, carry and readout.
+    if (launches) *launches = empty ? 0 : (plan.K > 1 ? (plan.tma ? 2 : 3) : 1);
     if (workspace_bytes) *workspace_bytes = empty ? 0 : (int64_t)fwd_workspace_bytes(plan, Bsz, L, D, N, dtype);
     return SELSCAN_OK;
 }
