@@ -115,6 +115,30 @@ def test_forced_chunk_lengths(orc, env, chunk):
     check(orc, inp)
 
 
+@pytest.mark.parametrize("dtype,D", [(W.F32, 44), (W.BF16, 40)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_one_pass_output_any_alignment(orc, env, dtype, D, offset):
+    """The one-pass fused kernel writes y wherever it starts: 16-byte aligned,
+    or one element past a boundary (the inputs stay aligned, so the TMA path
+    runs). The last warp of each channel tile is partly past D, and L ends in
+    a partial stage."""
+    L = 333
+    env(SELSCAN_CHUNK=L)
+    inp = W.fwd_inputs(3, L, D, 16, seed=70 + offset, dtype=dtype, with_h0=True)
+    p = ss.fwd_plan(3, L, D, 16, bf16=dtype == W.BF16)
+    assert p["chunks"] == 1 and p["launches"] == 1   # aligned rows: the fused kernel, one pass
+    x, dl, A, B, C, h0 = fwd_dev(inp)
+    buf = torch.full((x.numel() + offset,), float("nan"), device="cuda", dtype=x.dtype)
+    y = buf[offset:].view(x.shape)
+    assert (y.data_ptr() % 16 == 0) == (offset == 0)
+    ss.selscan_fwd(x, dl, A, B, C, delta_softplus=True, h0=h0, y=y)
+    torch.cuda.synchronize()
+    yr, _ = oracle_fwd(orc, inp)
+    assert scaled_err(to_np(y), yr) <= TOL[dtype]
+    if offset:
+        assert torch.isnan(buf[0])   # nothing written before y
+
+
 @pytest.mark.parametrize("nsplit", [2, 4])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 def test_threads_per_chain(orc, env, nsplit, dtype):
